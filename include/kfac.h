@@ -1,0 +1,207 @@
+/*
+ * kfac.h -- C ABI of the GB300 (sm_103a) K-FAC curvature-step library
+ * (libkfac_gb300.so).
+ *
+ * The library implements the per-layer Kronecker-factored curvature step of
+ * Osawa et al., "Large-Scale Distributed Second-Order Optimization Using
+ * Kronecker-Factored Approximate Curvature for Deep Convolutional Neural
+ * Networks" (section 3.2, Eq. 4-7, and the diagonal BatchNorm Fisher of
+ * section 1):
+ *   kfac_factor_update   builds A = E[a a^T] / G = E[g g^T] and folds it into a
+ *                        running average                      (Eq. 5)
+ *   kfac_damp_invert     damps both factors of a layer (pi-split Tikhonov) and
+ *                        inverts them                           (Eq. 6)
+ *   kfac_precondition    G^-1 grad A^-1                         (Eq. 7)
+ *   kfac_bn_diag_fisher  diagonal Fisher of BatchNorm parameters and the
+ *                        damped diagonal preconditioned gradient
+ *
+ * Conventions shared by every entry point:
+ *   - Every buffer pointer inside a descriptor is a DEVICE pointer on the
+ *     current CUDA device, owned by the caller; descriptor arrays themselves
+ *     are HOST memory and may be freed when the call returns.
+ *   - The library allocates no device memory.  Calls that need scratch take a
+ *     caller-owned device `workspace` of at least the size the matching
+ *     *_workspace_size query returns (256-byte aligned); its contents need no
+ *     initialisation and are clobbered.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous: results are ready once the stream has
+ *     reached that point.  The library keeps no global state; concurrent calls
+ *     on different streams with disjoint buffers and workspaces are allowed.
+ *   - KFAC_ERR_INVALID / KFAC_ERR_UNSUPPORTED / KFAC_ERR_WORKSPACE are
+ *     returned BEFORE anything is enqueued (outputs untouched).
+ *     KFAC_ERR_CUDA reports a launch failure (cudaGetLastError after a
+ *     launch); the stream may then hold part of the work.
+ *   - Matrices are row-major with an explicit leading dimension (elements).
+ *     bf16 values are passed as uint16_t bit patterns.
+ */
+#ifndef KFAC_GB300_H
+#define KFAC_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KFAC_OK = 0,
+    KFAC_ERR_INVALID = 1,      /* null pointer, non-positive size, ld < width, ... */
+    KFAC_ERR_UNSUPPORTED = 2,  /* valid but not implemented (dtype, shape limit)  */
+    KFAC_ERR_NOT_PD = 3,       /* reserved for host-side reporting of info[]      */
+    KFAC_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed             */
+    KFAC_ERR_WORKSPACE = 5     /* workspace missing, misaligned or too small      */
+} kfac_status;
+
+typedef enum { KFAC_BF16 = 0, KFAC_F32 = 1 } kfac_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *kfac_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int kfac_version(void);
+
+/* ======================================================================
+ * kfac_factor_update -- Kronecker factor statistic + running average.
+ *
+ * Osawa et al. section 3.2, Eq. 5: A_{l-1} is built from the layer's input
+ * activations, G_l from the gradients of the layer's output.  For each
+ * descriptor the call forms the patch matrix P [M x d] of the source tensor
+ * and updates the UPPER triangle (i <= j) of the fp32 factor F in place:
+ *
+ *     F[i][j] <- beta * F[i][j] + alpha * sum_m P[m][i] * P[m][j]
+ *
+ * The running average F <- xi F + (1 - xi) P^T P / M is alpha = (1 - xi)/M,
+ * beta = xi; accumulating one statistic over several chunks of rows uses
+ * beta = xi on the first chunk and beta = 1 afterwards with alpha = (1-xi)/M_total.
+ * Entries strictly below the diagonal are neither read nor written.
+ *
+ * Patch matrix (im2col; row m = (img*Ho + ho)*Wo + wo):
+ *   P[m][(r*kw + s)*c + ch] = x[img][ho*stride_h - pad_h + r][wo*stride_w - pad_w + s][ch]
+ *   (zero outside the image), Ho = (h + 2*pad_h - kh)/stride_h + 1 (same for Wo),
+ *   and when append_one != 0 a last column of ones (an FC bias), so
+ *   d = kh*kw*c + (append_one ? 1 : 0).
+ * A fully connected layer or an output-gradient source [M x C] is
+ * h = w = kh = kw = stride = 1, pad = 0, n = M rows.
+ *
+ * Fields:
+ *   dtype   KFAC_BF16 (tensor-core path) or KFAC_F32 (fp32 CUDA-core path)
+ *   x       device, dense NHWC [n][h][w][c] of dtype (channel stride 1)
+ *   F, ldf  device fp32 [d][ldf], ldf >= d; upper triangle updated
+ * Errors: INVALID for null x/F, n,h,w,c,kh,kw,stride < 1, pad < 0, Ho/Wo < 1,
+ *   ldf < d; UNSUPPORTED for d > 65536 or more than 2^31 rows.
+ * Workspace: kfac_factor_update_workspace_size(descs, count) bytes.
+ * ==================================================================== */
+typedef struct {
+    int32_t dtype;
+    const void *x;
+    int32_t n, h, w, c;
+    int32_t kh, kw, stride_h, stride_w, pad_h, pad_w;
+    int32_t append_one;
+    float *F;
+    int64_t ldf;
+    float alpha, beta;
+} kfac_factor_desc;
+
+size_t kfac_factor_update_workspace_size(const kfac_factor_desc *descs, int count);
+kfac_status kfac_factor_update(const kfac_factor_desc *descs, int count,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/* ======================================================================
+ * kfac_damp_invert -- damped inverses of both factors of each layer.
+ *
+ * Osawa et al. section 3.2, Eq. 6: (G (x) A)^-1 = G^-1 (x) A^-1.  Damping
+ * (the paper states none; Tikhonov split by pi as in the K-FAC paper it
+ * cites):
+ *     pi = sqrt((tr A / dA) / (tr G / dG)),
+ *     damp_A = pi * sqrt(gamma),  damp_G = sqrt(gamma) / pi      (pi_split != 0)
+ *     damp_A = damp_G = sqrt(gamma)                              (pi_split == 0)
+ * and writes the FULL symmetric fp32 inverses
+ *     A_inv = (A + damp_A I)^-1,  G_inv = (G + damp_G I)^-1
+ * computed in fp32 by a blocked Cholesky-based inversion.  Only the upper
+ * triangles of A and G are read.  Optional bf16 copies of the inverses are
+ * written when the *_bf16 pointers are non-NULL (their ld must be a multiple
+ * of 8 elements and their base 16-byte aligned, for the tensor-core
+ * preconditioner).
+ *
+ * Device outputs besides the inverses:
+ *   info   int32 [2*count] (may be NULL): info[2l] for A of layer l,
+ *          info[2l+1] for its G; 0 = success, k+1 = the k-th pivot was not
+ *          positive or not finite (matrix not positive definite); the
+ *          corresponding inverse is then undefined.  The call itself still
+ *          returns KFAC_OK: read info after synchronising the stream.
+ *   damp   float [2*count] (may be NULL): the damp_A, damp_G applied.
+ * Errors: INVALID for null A/G/A_inv/G_inv, dA/dG < 1, ld < d, gamma < 0;
+ *   UNSUPPORTED for d > 16384 or a bf16 ld not a multiple of 8.
+ * Workspace: kfac_damp_invert_workspace_size(descs, count) bytes.
+ * ==================================================================== */
+typedef struct {
+    const float *A; int32_t dA; int64_t lda;
+    const float *G; int32_t dG; int64_t ldg;
+    float *A_inv; int64_t ld_ainv;
+    float *G_inv; int64_t ld_ginv;
+    uint16_t *A_inv_bf16; int64_t ld_ainv_bf16;   /* optional */
+    uint16_t *G_inv_bf16; int64_t ld_ginv_bf16;   /* optional */
+} kfac_invert_desc;
+
+size_t kfac_damp_invert_workspace_size(const kfac_invert_desc *descs, int count);
+kfac_status kfac_damp_invert(const kfac_invert_desc *descs, int count, float gamma,
+                             int pi_split, int32_t *info, float *damp,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/* ======================================================================
+ * kfac_precondition -- preconditioned gradient of each layer.
+ *
+ * Osawa et al. section 3.2, Eq. 7 in row-major form: for grad [dG x dA],
+ *     out = G_inv * grad * A_inv            (out fp32 [dG][ld_out])
+ * i.e. (G (x) A)^-1 vec(grad) with symmetric inverses.  A_inv and G_inv are
+ * read as FULL matrices (kfac_damp_invert writes both triangles).
+ * dtype KFAC_BF16: G_inv, A_inv, grad are bf16 (tensor cores, fp32
+ *   accumulation; the intermediate grad*A_inv is rounded to bf16); each ld
+ *   must be a multiple of 8 and each base 16-byte aligned.
+ * dtype KFAC_F32: all operands fp32 (CUDA cores).
+ * Errors: INVALID for null pointers, d < 1, ld < width; UNSUPPORTED for a
+ *   bf16 ld/alignment violation or d > 65536.
+ * Workspace: kfac_precondition_workspace_size(descs, count, dtype) bytes.
+ * ==================================================================== */
+typedef struct {
+    int32_t dG, dA;
+    const void *G_inv; int64_t ld_ginv;
+    const void *A_inv; int64_t ld_ainv;
+    const void *grad;  int64_t ld_grad;
+    float *out;        int64_t ld_out;
+} kfac_precond_desc;
+
+size_t kfac_precondition_workspace_size(const kfac_precond_desc *descs, int count, int dtype);
+kfac_status kfac_precondition(const kfac_precond_desc *descs, int count, int dtype,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/* ======================================================================
+ * kfac_bn_diag_fisher -- diagonal Fisher of BatchNorm parameters.
+ *
+ * Osawa et al. section 1 (contributions): the Fisher of BatchNormalization
+ * layers is approximated as diagonal.  For each descriptor, from per-sample
+ * gradients x [n_samples][C] (fp32, row-major, dense):
+ *     F_c       <- xi * F_c + (1 - xi) * (1/n) sum_i x_ic^2   (xi = 0: plain)
+ *     grad_mean_c = (1/n) sum_i x_ic
+ *     precond_c   = grad_mean_c / (F_c + gamma)
+ * F is read only when xi != 0.  grad_mean may be NULL.  The reduction order
+ * is fixed, so results are bitwise reproducible run to run.
+ * Errors: INVALID for null x/F/precond, C < 1, n_samples < 1, gamma < 0.
+ * No workspace.
+ * ==================================================================== */
+typedef struct {
+    const float *x;
+    int32_t C;
+    float *F;
+    float *grad_mean;
+    float *precond;
+} kfac_bn_desc;
+
+kfac_status kfac_bn_diag_fisher(const kfac_bn_desc *descs, int count, int n_samples,
+                                float gamma, float xi, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KFAC_GB300_H */

@@ -1,0 +1,358 @@
+// api.cu -- the C ABI of libkfac_gb300 (declared in include/kfac.h):
+// argument validation, workspace planning and dispatch to the kernels.
+//
+// Osawa et al., "Large-Scale Distributed Second-Order Optimization Using
+// Kronecker-Factored Approximate Curvature for Deep Convolutional Neural
+// Networks", section 3.2 (Eq. 5-7) and section 1 (diagonal BatchNorm Fisher).
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+
+namespace kfac {
+
+int device_sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+EncodeTiledFn encode_tiled_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    });
+    return fn;
+}
+
+namespace {
+
+struct FactorGeom {
+    int ho, wo;
+    long long M;
+    int dcore, d;
+    bool direct;  // bf16 source usable as the patch matrix itself
+};
+
+bool geom_of(const kfac_factor_desc &d, FactorGeom &g) {
+    g.ho = (d.h + 2 * d.pad_h - d.kh) / d.stride_h + 1;
+    g.wo = (d.w + 2 * d.pad_w - d.kw) / d.stride_w + 1;
+    if (d.h + 2 * d.pad_h < d.kh || d.w + 2 * d.pad_w < d.kw || g.ho < 1 || g.wo < 1) return false;
+    g.M = (long long)d.n * g.ho * g.wo;
+    g.dcore = d.kh * d.kw * d.c;
+    g.d = g.dcore + (d.append_one ? 1 : 0);
+    g.direct = d.dtype == KFAC_BF16 && d.kh == 1 && d.kw == 1 && d.stride_h == 1 &&
+               d.stride_w == 1 && d.pad_h == 0 && d.pad_w == 0 && d.c % 8 == 0 &&
+               ((uintptr_t)d.x % 16) == 0;
+    return true;
+}
+
+kfac_status validate_factor(const kfac_factor_desc *descs, int count, std::vector<FactorGeom> &geo) {
+    if (count < 0 || (count > 0 && !descs)) return KFAC_ERR_INVALID;
+    geo.resize(count);
+    for (int i = 0; i < count; ++i) {
+        const kfac_factor_desc &d = descs[i];
+        if (!d.x || !d.F) return KFAC_ERR_INVALID;
+        if (d.dtype != KFAC_BF16 && d.dtype != KFAC_F32) return KFAC_ERR_INVALID;
+        if (d.n < 1 || d.h < 1 || d.w < 1 || d.c < 1 || d.kh < 1 || d.kw < 1 || d.stride_h < 1 ||
+            d.stride_w < 1 || d.pad_h < 0 || d.pad_w < 0)
+            return KFAC_ERR_INVALID;
+        if (!std::isfinite(d.alpha) || !std::isfinite(d.beta)) return KFAC_ERR_INVALID;
+        if (!geom_of(d, geo[i])) return KFAC_ERR_INVALID;
+        if (d.ldf < geo[i].d) return KFAC_ERR_INVALID;
+        if (geo[i].d > 65536 || geo[i].M >= (1LL << 31)) return KFAC_ERR_UNSUPPORTED;
+    }
+    return KFAC_OK;
+}
+
+// Everything the factor update enqueues, laid out in one arena.
+struct FactorPlan {
+    std::vector<Im2colJob> im16, im32;
+    std::vector<TcJob> tc;
+    std::vector<SgJob> sg;
+    std::vector<ColsumJob> cs;
+    int *err = nullptr;
+    char *tc_ws = nullptr;
+    size_t tc_bytes = 0;
+};
+
+kfac_status plan_factor(const kfac_factor_desc *descs, int count, const std::vector<FactorGeom> &geo,
+                        Arena &ws, FactorPlan &p) {
+    p.err = ws.take<int>(64);
+    for (int i = 0; i < count; ++i) {
+        const kfac_factor_desc &d = descs[i];
+        const FactorGeom &g = geo[i];
+        if (d.dtype == KFAC_F32) {
+            // fp32 path: explicit patches (with the ones column) + CUDA-core SYRK
+            const long long ldp = g.d;
+            float *P = ws.take<float>((size_t)g.M * ldp);
+            p.im32.push_back(Im2colJob{d.x, d.n, d.h, d.w, d.c, d.kh, d.kw, d.stride_h, d.stride_w,
+                                       d.pad_h, d.pad_w, g.ho, g.wo, d.append_one, P, ldp});
+            p.sg.push_back(SgJob{P, ldp, 1, P, ldp, 0, d.F, d.ldf, nullptr, 0, g.d, g.d, (int)g.M,
+                                 d.alpha, d.beta, 1});
+            continue;
+        }
+        const uint16_t *src;
+        long long lds;
+        if (g.direct) {
+            src = (const uint16_t *)d.x;
+            lds = d.c;
+        } else {
+            lds = (g.dcore + 7) / 8 * 8;
+            uint16_t *P = ws.take<uint16_t>((size_t)g.M * lds);
+            p.im16.push_back(Im2colJob{d.x, d.n, d.h, d.w, d.c, d.kh, d.kw, d.stride_h, d.stride_w,
+                                       d.pad_h, d.pad_w, g.ho, g.wo, 0, P, lds});
+            src = P;
+        }
+        TcJob j{};
+        j.a = src; j.lda = lds; j.a_rows = (int)g.M; j.a_cols = g.dcore; j.a_mn = 1;
+        j.b = src; j.ldb = lds; j.b_rows = (int)g.M; j.b_cols = g.dcore; j.b_mn = 1;
+        j.M = g.dcore; j.N = g.dcore; j.K = (int)g.M;
+        j.syrk = 1;
+        j.epi = TC_EPI_ACCUM;
+        j.alpha = d.alpha; j.beta = d.beta;
+        j.C = d.F; j.ldc = d.ldf;
+        p.tc.push_back(j);
+        if (d.append_one) {
+            // bias row/column: needs the source rows [M][c]; an FC layer has
+            // h = w = kh = kw = 1 so the source is x itself
+            if (!(d.kh == 1 && d.kw == 1 && d.h == 1 && d.w == 1)) return KFAC_ERR_UNSUPPORTED;
+            p.cs.push_back(ColsumJob{(const uint16_t *)d.x, g.M, d.c, d.F, d.ldf, d.alpha, d.beta});
+        }
+    }
+    p.tc_bytes = tc_workspace_bytes(p.tc.data(), (int)p.tc.size());
+    p.tc_ws = ws.take<char>(p.tc_bytes);
+    return KFAC_OK;
+}
+
+}  // namespace
+}  // namespace kfac
+
+using namespace kfac;
+
+extern "C" const char *kfac_status_string(int status) {
+    switch (status) {
+        case KFAC_OK: return "KFAC_OK";
+        case KFAC_ERR_INVALID: return "KFAC_ERR_INVALID: invalid argument";
+        case KFAC_ERR_UNSUPPORTED: return "KFAC_ERR_UNSUPPORTED: valid but not supported";
+        case KFAC_ERR_NOT_PD: return "KFAC_ERR_NOT_PD: matrix not positive definite";
+        case KFAC_ERR_CUDA: return "KFAC_ERR_CUDA: CUDA launch or runtime error";
+        case KFAC_ERR_WORKSPACE: return "KFAC_ERR_WORKSPACE: workspace missing or too small";
+        default: return "unknown kfac_status";
+    }
+}
+
+extern "C" int kfac_version(void) { return 100; }
+
+// ------------------------------------------------------------ factor update
+
+extern "C" size_t kfac_factor_update_workspace_size(const kfac_factor_desc *descs, int count) {
+    std::vector<FactorGeom> geo;
+    if (validate_factor(descs, count, geo) != KFAC_OK) return 0;
+    Arena a;
+    FactorPlan p;
+    if (plan_factor(descs, count, geo, a, p) != KFAC_OK) return 0;
+    return a.used;
+}
+
+extern "C" kfac_status kfac_factor_update(const kfac_factor_desc *descs, int count, void *workspace,
+                                          size_t workspace_bytes, void *stream) {
+    std::vector<FactorGeom> geo;
+    kfac_status s = validate_factor(descs, count, geo);
+    if (s != KFAC_OK) return s;
+    if (count == 0) return KFAC_OK;
+    if (!workspace || ((uintptr_t)workspace % 256) != 0) return KFAC_ERR_WORKSPACE;
+    Arena ws(workspace, workspace_bytes);
+    FactorPlan p;
+    if ((s = plan_factor(descs, count, geo, ws, p)) != KFAC_OK) return s;
+    if (!ws.fits()) return KFAC_ERR_WORKSPACE;
+    Arena tail(p.tc_ws, p.tc_bytes);
+    cudaStream_t st = (cudaStream_t)stream;
+    KFAC_CUDA_TRY(cudaMemsetAsync(p.err, 0, sizeof(int), st));
+    if (!p.im16.empty() && (s = im2col_run(p.im16.data(), (int)p.im16.size(), KFAC_BF16, st)) != KFAC_OK)
+        return s;
+    if (!p.im32.empty() && (s = im2col_run(p.im32.data(), (int)p.im32.size(), KFAC_F32, st)) != KFAC_OK)
+        return s;
+    if (!p.tc.empty() && (s = tc_run(p.tc.data(), (int)p.tc.size(), tail, p.err, st)) != KFAC_OK) return s;
+    if (!p.sg.empty() && (s = sg_run(p.sg.data(), (int)p.sg.size(), st)) != KFAC_OK) return s;
+    if (!p.cs.empty() && (s = colsum_run(p.cs.data(), (int)p.cs.size(), st)) != KFAC_OK) return s;
+    return KFAC_OK;
+}
+
+// ------------------------------------------------------------ damp + invert
+
+namespace {
+
+kfac_status validate_invert(const kfac_invert_desc *descs, int count, float gamma) {
+    if (count < 0 || (count > 0 && !descs) || !(gamma >= 0.f) || !std::isfinite(gamma))
+        return KFAC_ERR_INVALID;
+    for (int i = 0; i < count; ++i) {
+        const kfac_invert_desc &d = descs[i];
+        if (!d.A || !d.G || !d.A_inv || !d.G_inv) return KFAC_ERR_INVALID;
+        if (d.dA < 1 || d.dG < 1 || d.lda < d.dA || d.ldg < d.dG || d.ld_ainv < d.dA ||
+            d.ld_ginv < d.dG)
+            return KFAC_ERR_INVALID;
+        if ((d.A_inv_bf16 && d.ld_ainv_bf16 < d.dA) || (d.G_inv_bf16 && d.ld_ginv_bf16 < d.dG))
+            return KFAC_ERR_INVALID;
+        if (d.dA > 16384 || d.dG > 16384) return KFAC_ERR_UNSUPPORTED;
+        if ((d.A_inv_bf16 && (d.ld_ainv_bf16 % 8 || (uintptr_t)d.A_inv_bf16 % 16)) ||
+            (d.G_inv_bf16 && (d.ld_ginv_bf16 % 8 || (uintptr_t)d.G_inv_bf16 % 16)))
+            return KFAC_ERR_UNSUPPORTED;
+    }
+    return KFAC_OK;
+}
+
+std::vector<InvMatrix> inv_mats(const kfac_invert_desc *descs, int count) {
+    std::vector<InvMatrix> m(2 * count);
+    for (int i = 0; i < count; ++i) {
+        const kfac_invert_desc &d = descs[i];
+        m[2 * i] = InvMatrix{d.A, d.lda, d.dA, d.A_inv, d.ld_ainv, d.A_inv_bf16, d.ld_ainv_bf16};
+        m[2 * i + 1] = InvMatrix{d.G, d.ldg, d.dG, d.G_inv, d.ld_ginv, d.G_inv_bf16, d.ld_ginv_bf16};
+    }
+    return m;
+}
+
+}  // namespace
+
+extern "C" size_t kfac_damp_invert_workspace_size(const kfac_invert_desc *descs, int count) {
+    if (validate_invert(descs, count, 0.f) != KFAC_OK) return 0;
+    std::vector<InvMatrix> m = inv_mats(descs, count);
+    Arena a;
+    a.take<float>(2 * (size_t)count);   // damping values
+    a.take<int>(2 * (size_t)count);     // info
+    a.take<char>(inv_workspace_bytes(m.data(), (int)m.size()));
+    return a.used;
+}
+
+extern "C" kfac_status kfac_damp_invert(const kfac_invert_desc *descs, int count, float gamma,
+                                        int pi_split, int32_t *info, float *damp, void *workspace,
+                                        size_t workspace_bytes, void *stream) {
+    kfac_status s = validate_invert(descs, count, gamma);
+    if (s != KFAC_OK) return s;
+    if (count == 0) return KFAC_OK;
+    if (!workspace || ((uintptr_t)workspace % 256) != 0) return KFAC_ERR_WORKSPACE;
+    if (workspace_bytes < kfac_damp_invert_workspace_size(descs, count)) return KFAC_ERR_WORKSPACE;
+    std::vector<InvMatrix> m = inv_mats(descs, count);
+    Arena ws(workspace, workspace_bytes);
+    float *dmp = ws.take<float>(2 * (size_t)count);
+    int *inf = ws.take<int>(2 * (size_t)count);
+    if (damp) dmp = damp;
+    if (info) inf = info;
+    cudaStream_t st = (cudaStream_t)stream;
+    KFAC_CUDA_TRY(cudaMemsetAsync(inf, 0, 2 * (size_t)count * sizeof(int), st));
+    if ((s = damping_run(m.data(), count, gamma, pi_split, dmp, st)) != KFAC_OK) return s;
+    return inv_run(m.data(), (int)m.size(), dmp, inf, ws, st);
+}
+
+// ------------------------------------------------------------ precondition
+
+namespace {
+
+kfac_status validate_precond(const kfac_precond_desc *descs, int count, int dtype) {
+    if (count < 0 || (count > 0 && !descs)) return KFAC_ERR_INVALID;
+    if (dtype != KFAC_BF16 && dtype != KFAC_F32) return KFAC_ERR_INVALID;
+    for (int i = 0; i < count; ++i) {
+        const kfac_precond_desc &d = descs[i];
+        if (!d.G_inv || !d.A_inv || !d.grad || !d.out) return KFAC_ERR_INVALID;
+        if (d.dG < 1 || d.dA < 1 || d.ld_ginv < d.dG || d.ld_ainv < d.dA || d.ld_grad < d.dA ||
+            d.ld_out < d.dA)
+            return KFAC_ERR_INVALID;
+        if (d.dG > 65536 || d.dA > 65536) return KFAC_ERR_UNSUPPORTED;
+        if (dtype == KFAC_BF16 &&
+            (d.ld_ginv % 8 || d.ld_ainv % 8 || d.ld_grad % 8 || (uintptr_t)d.G_inv % 16 ||
+             (uintptr_t)d.A_inv % 16 || (uintptr_t)d.grad % 16))
+            return KFAC_ERR_UNSUPPORTED;
+    }
+    return KFAC_OK;
+}
+
+struct PrecondPlan {
+    std::vector<TcJob> g1, g2;
+    std::vector<SgJob> s1, s2;
+    int *err = nullptr;
+    char *tc_ws = nullptr;
+    size_t tc_bytes = 0;
+};
+
+void plan_precond(const kfac_precond_desc *descs, int count, int dtype, Arena &ws, PrecondPlan &p) {
+    p.err = ws.take<int>(64);
+    for (int i = 0; i < count; ++i) {
+        const kfac_precond_desc &d = descs[i];
+        if (dtype == KFAC_BF16) {
+            const long long ldt = (d.dA + 7) / 8 * 8;
+            uint16_t *T = ws.take<uint16_t>((size_t)d.dG * ldt);
+            TcJob a{};  // T = grad * A_inv   (A_inv symmetric: read rows as B^T)
+            a.a = (const uint16_t *)d.grad; a.lda = d.ld_grad; a.a_rows = d.dG; a.a_cols = d.dA; a.a_mn = 0;
+            a.b = (const uint16_t *)d.A_inv; a.ldb = d.ld_ainv; a.b_rows = d.dA; a.b_cols = d.dA; a.b_mn = 0;
+            a.M = d.dG; a.N = d.dA; a.K = d.dA;
+            a.epi = TC_EPI_STORE; a.alpha = 1.f; a.beta = 0.f;
+            a.Cb = T; a.ldcb = ldt;
+            p.g1.push_back(a);
+            TcJob b{};  // out = G_inv * T
+            b.a = (const uint16_t *)d.G_inv; b.lda = d.ld_ginv; b.a_rows = d.dG; b.a_cols = d.dG; b.a_mn = 0;
+            b.b = T; b.ldb = ldt; b.b_rows = d.dG; b.b_cols = d.dA; b.b_mn = 1;
+            b.M = d.dG; b.N = d.dA; b.K = d.dG;
+            b.epi = TC_EPI_STORE; b.alpha = 1.f; b.beta = 0.f;
+            b.C = d.out; b.ldc = d.ld_out;
+            p.g2.push_back(b);
+        } else {
+            float *T = ws.take<float>((size_t)d.dG * d.dA);
+            p.s1.push_back(SgJob{(const float *)d.grad, d.ld_grad, 0, (const float *)d.A_inv, d.ld_ainv, 0,
+                                 T, d.dA, nullptr, 0, d.dG, d.dA, d.dA, 1.f, 0.f, 0});
+            p.s2.push_back(SgJob{(const float *)d.G_inv, d.ld_ginv, 0, T, d.dA, 0, d.out, d.ld_out,
+                                 nullptr, 0, d.dG, d.dA, d.dG, 1.f, 0.f, 0});
+        }
+    }
+    size_t t1 = tc_workspace_bytes(p.g1.data(), (int)p.g1.size());
+    size_t t2 = tc_workspace_bytes(p.g2.data(), (int)p.g2.size());
+    p.tc_bytes = std::max(t1, t2);
+    p.tc_ws = ws.take<char>(p.tc_bytes);
+}
+
+}  // namespace
+
+extern "C" size_t kfac_precondition_workspace_size(const kfac_precond_desc *descs, int count, int dtype) {
+    if (validate_precond(descs, count, dtype) != KFAC_OK) return 0;
+    Arena a;
+    PrecondPlan p;
+    plan_precond(descs, count, dtype, a, p);
+    return a.used;
+}
+
+extern "C" kfac_status kfac_precondition(const kfac_precond_desc *descs, int count, int dtype,
+                                         void *workspace, size_t workspace_bytes, void *stream) {
+    kfac_status s = validate_precond(descs, count, dtype);
+    if (s != KFAC_OK) return s;
+    if (count == 0) return KFAC_OK;
+    if (!workspace || ((uintptr_t)workspace % 256) != 0) return KFAC_ERR_WORKSPACE;
+    Arena ws(workspace, workspace_bytes);
+    PrecondPlan p;
+    plan_precond(descs, count, dtype, ws, p);
+    if (!ws.fits()) return KFAC_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (dtype == KFAC_BF16) {
+        KFAC_CUDA_TRY(cudaMemsetAsync(p.err, 0, sizeof(int), st));
+        Arena t_a(p.tc_ws, p.tc_bytes);
+        if ((s = tc_run(p.g1.data(), (int)p.g1.size(), t_a, p.err, st)) != KFAC_OK) return s;
+        Arena t_b(p.tc_ws, p.tc_bytes);
+        return tc_run(p.g2.data(), (int)p.g2.size(), t_b, p.err, st);
+    }
+    if ((s = sg_run(p.s1.data(), (int)p.s1.size(), st)) != KFAC_OK) return s;
+    return sg_run(p.s2.data(), (int)p.s2.size(), st);
+}

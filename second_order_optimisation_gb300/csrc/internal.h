@@ -1,0 +1,115 @@
+// internal.h -- host-side interfaces between the translation units of
+// libkfac_gb300 (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace kfac {
+
+// ----------------------------------------------------- tensor-core GEMM
+// One problem of the tcgen05 engine: C[M x N] = alpha * op(A) op(B) (+ beta C)
+// with bf16 operands and fp32 accumulation.
+//   a_mn = 1: A stored [K][M] (M contiguous);  a_mn = 0: A stored [M][K].
+//   b_mn = 1: B stored [K][N] (N contiguous);  b_mn = 0: B stored [N][K].
+//   syrk = 1: B is the same matrix as A (the Gram matrix A^T A of a [K][M]
+//             source), only tiles touching the upper triangle are computed
+//             and only entries i <= j are written.
+enum TcEpilogue : int {
+    TC_EPI_ACCUM = 0,  // fp32 C[i][j] = beta*C[i][j] + alpha*acc (C read only if beta != 0)
+    TC_EPI_STORE = 1   // C (fp32, optional) and/or Cb (bf16, optional) = alpha*acc
+};
+
+struct TcJob {
+    const uint16_t *a;
+    long long lda;
+    int a_rows, a_cols, a_mn;
+    const uint16_t *b;
+    long long ldb;
+    int b_rows, b_cols, b_mn;
+    int M, N, K;
+    int syrk;
+    int epi;
+    float alpha, beta;
+    float *C;
+    long long ldc;
+    uint16_t *Cb;
+    long long ldcb;
+};
+
+// Workspace needed by tc_run for these jobs (split-K partials, counters).
+size_t tc_workspace_bytes(const TcJob *jobs, int njobs);
+// Enqueue the jobs (one or more persistent launches).  `err` is a device
+// int that collects timeout codes.  Returns KFAC_OK or an error.
+kfac_status tc_run(const TcJob *jobs, int njobs, Arena &ws, int *err, cudaStream_t st);
+
+// ----------------------------------------------------- CUDA-core GEMM (fp32)
+// C[M x N] = alpha * op(A) op(B) + beta * C, fp32.
+//   ta = 0: A stored [M][K];  ta = 1: A stored [K][M]
+//   tb = 0: B stored [K][N];  tb = 1: B stored [N][K]
+//   upper = 1: only entries i <= j are written (and only tiles touching them run)
+//   Ct (optional): also writes the transposed result Ct[j][i]
+struct SgJob {
+    const float *A;
+    long long lda;
+    int ta;
+    const float *B;
+    long long ldb;
+    int tb;
+    float *C;
+    long long ldc;
+    float *Ct;
+    long long ldct;
+    int M, N, K;
+    float alpha, beta;
+    int upper;
+};
+kfac_status sg_run(const SgJob *jobs, int njobs, cudaStream_t st);
+
+// ----------------------------------------------------- patches / reductions
+// bf16 or fp32 im2col into P[M][ldp] (columns d..ldp-1 untouched).
+struct Im2colJob {
+    const void *x;
+    int n, h, w, c, kh, kw, sh, sw, ph, pw;
+    int ho, wo;
+    int append_one;
+    void *P;
+    long long ldp;
+};
+kfac_status im2col_run(const Im2colJob *jobs, int njobs, int dtype, cudaStream_t st);
+
+// Bias row/column of an FC factor with append_one: for a bf16 source x[M][c]
+// (no patch matrix formed), updates F[i][c] (i < c) with alpha * colsum_i
+// and F[c][c] with alpha * M, both scaled by beta first.
+struct ColsumJob {
+    const uint16_t *x;
+    long long M;
+    int c;
+    float *F;
+    long long ldf;
+    float alpha, beta;
+};
+kfac_status colsum_run(const ColsumJob *jobs, int njobs, cudaStream_t st);
+
+// ----------------------------------------------------- inversion
+struct InvMatrix {
+    const float *F;   // factor, upper triangle read
+    long long ldf;
+    int d;
+    float *out;       // full symmetric inverse
+    long long ldo;
+    uint16_t *out_bf16;
+    long long ldo_bf16;
+};
+size_t inv_workspace_bytes(const InvMatrix *mats, int nmats);
+// damp[k] (device) is added to the diagonal of matrix k; info[k] receives 0
+// or the 1-based index of the first bad pivot.
+kfac_status inv_run(const InvMatrix *mats, int nmats, const float *damp_dev, int *info_dev,
+                    Arena &ws, cudaStream_t st);
+// Traces -> pi-split damping for each layer (pairs A, G) into damp_dev[2l], [2l+1].
+kfac_status damping_run(const InvMatrix *mats, int nlayers, float gamma, int pi_split,
+                        float *damp_dev, cudaStream_t st);
+
+}  // namespace kfac

@@ -1,0 +1,316 @@
+"""Thin ctypes binding of libkfac_gb300.so (C ABI in include/kfac.h).
+
+Argument marshalling only: every step of the K-FAC curvature path runs in the
+library's CUDA kernels.  PyTorch supplies device memory (tensors, the
+workspace) and the stream.  There is no CPU or PyTorch fallback: if the
+library is missing, loading it raises.
+
+The functions keep the C names:
+  kfac_factor_update   (Osawa et al. section 3.2, Eq. 5 + running average)
+  kfac_damp_invert     (Eq. 6, pi-split Tikhonov damping)
+  kfac_precondition    (Eq. 7)
+  kfac_bn_diag_fisher  (diagonal BatchNorm Fisher, section 1)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkfac_gb300.so")
+
+KFAC_OK, KFAC_ERR_INVALID, KFAC_ERR_UNSUPPORTED, KFAC_ERR_NOT_PD, KFAC_ERR_CUDA, KFAC_ERR_WORKSPACE = range(6)
+KFAC_BF16, KFAC_F32 = 0, 1
+
+EXPORTS = ("kfac_status_string", "kfac_version", "kfac_factor_update_workspace_size",
+           "kfac_factor_update", "kfac_damp_invert_workspace_size", "kfac_damp_invert",
+           "kfac_precondition_workspace_size", "kfac_precondition", "kfac_bn_diag_fisher")
+
+
+class KfacError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)}")
+        self.status = status
+
+
+class FactorDesc(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("x", ctypes.c_void_p),
+                ("n", ctypes.c_int32), ("h", ctypes.c_int32), ("w", ctypes.c_int32), ("c", ctypes.c_int32),
+                ("kh", ctypes.c_int32), ("kw", ctypes.c_int32),
+                ("stride_h", ctypes.c_int32), ("stride_w", ctypes.c_int32),
+                ("pad_h", ctypes.c_int32), ("pad_w", ctypes.c_int32),
+                ("append_one", ctypes.c_int32),
+                ("F", ctypes.c_void_p), ("ldf", ctypes.c_int64),
+                ("alpha", ctypes.c_float), ("beta", ctypes.c_float)]
+
+
+class InvertDesc(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("dA", ctypes.c_int32), ("lda", ctypes.c_int64),
+                ("G", ctypes.c_void_p), ("dG", ctypes.c_int32), ("ldg", ctypes.c_int64),
+                ("A_inv", ctypes.c_void_p), ("ld_ainv", ctypes.c_int64),
+                ("G_inv", ctypes.c_void_p), ("ld_ginv", ctypes.c_int64),
+                ("A_inv_bf16", ctypes.c_void_p), ("ld_ainv_bf16", ctypes.c_int64),
+                ("G_inv_bf16", ctypes.c_void_p), ("ld_ginv_bf16", ctypes.c_int64)]
+
+
+class PrecondDesc(ctypes.Structure):
+    _fields_ = [("dG", ctypes.c_int32), ("dA", ctypes.c_int32),
+                ("G_inv", ctypes.c_void_p), ("ld_ginv", ctypes.c_int64),
+                ("A_inv", ctypes.c_void_p), ("ld_ainv", ctypes.c_int64),
+                ("grad", ctypes.c_void_p), ("ld_grad", ctypes.c_int64),
+                ("out", ctypes.c_void_p), ("ld_out", ctypes.c_int64)]
+
+
+class BnDesc(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("C", ctypes.c_int32), ("F", ctypes.c_void_p),
+                ("grad_mean", ctypes.c_void_p), ("precond", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libkfac_gb300.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.kfac_status_string.argtypes = [i32]
+        lib.kfac_status_string.restype = ctypes.c_char_p
+        lib.kfac_version.restype = i32
+        lib.kfac_factor_update_workspace_size.argtypes = [vp, i32]
+        lib.kfac_factor_update_workspace_size.restype = sz
+        lib.kfac_factor_update.argtypes = [vp, i32, vp, sz, vp]
+        lib.kfac_damp_invert_workspace_size.argtypes = [vp, i32]
+        lib.kfac_damp_invert_workspace_size.restype = sz
+        lib.kfac_damp_invert.argtypes = [vp, i32, f32, i32, vp, vp, vp, sz, vp]
+        lib.kfac_precondition_workspace_size.argtypes = [vp, i32, i32]
+        lib.kfac_precondition_workspace_size.restype = sz
+        lib.kfac_precondition.argtypes = [vp, i32, i32, vp, sz, vp]
+        lib.kfac_bn_diag_fisher.argtypes = [vp, i32, i32, f32, f32, vp]
+        for f in ("kfac_factor_update", "kfac_damp_invert", "kfac_precondition", "kfac_bn_diag_fisher"):
+            getattr(lib, f).restype = i32
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().kfac_status_string(int(status)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int, what: str):
+    if status != KFAC_OK:
+        raise KfacError(status, what)
+
+
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.Tensor:
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise KfacError(KFAC_ERR_WORKSPACE, "workspace too small")
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def _ld(t: torch.Tensor) -> int:
+    assert t.dim() == 2 and t.stride(1) == 1, "matrices must be row-major with unit column stride"
+    return t.stride(0)
+
+
+# ------------------------------------------------------------ factor update
+
+@dataclass
+class FactorSource:
+    """One factor update: F[:d, :d] (upper) <- beta F + alpha P^T P, P the patch
+    matrix of x.  x: NHWC [n, h, w, c] (conv) or [rows, c] (FC / output grads)."""
+    x: torch.Tensor
+    F: torch.Tensor
+    kh: int = 1
+    kw: int = 1
+    stride: tuple = (1, 1)
+    pad: tuple = (0, 0)
+    append_one: bool = False
+    alpha: float = 1.0
+    beta: float = 0.0
+
+
+def _factor_descs(sources: Sequence[FactorSource]):
+    arr = (FactorDesc * max(len(sources), 1))()
+    for i, s in enumerate(sources):
+        x = s.x
+        assert x.is_contiguous(), "x must be dense"
+        if x.dim() == 2:
+            n, h, w, c = x.shape[0], 1, 1, x.shape[1]
+        else:
+            n, h, w, c = x.shape
+        if x.dtype == torch.bfloat16:
+            dt = KFAC_BF16
+        elif x.dtype == torch.float32:
+            dt = KFAC_F32
+        else:
+            raise TypeError(f"unsupported source dtype {x.dtype}")
+        assert s.F.dtype == torch.float32
+        arr[i] = FactorDesc(dt, x.data_ptr(), n, h, w, c, s.kh, s.kw, s.stride[0], s.stride[1],
+                            s.pad[0], s.pad[1], int(bool(s.append_one)), s.F.data_ptr(), _ld(s.F),
+                            float(s.alpha), float(s.beta))
+    return arr
+
+
+def kfac_factor_update_workspace_size(sources: Sequence[FactorSource]) -> int:
+    arr = _factor_descs(sources)
+    return int(load().kfac_factor_update_workspace_size(arr, len(sources)))
+
+
+def kfac_factor_update(sources: Sequence[FactorSource], workspace: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    """Enqueue the factor updates; returns the workspace used (its first int32
+    is the library's device error word: 0 = no internal timeout)."""
+    lib = load()
+    arr = _factor_descs(sources)
+    need = int(lib.kfac_factor_update_workspace_size(arr, len(sources)))
+    if need == 0 and len(sources):
+        _check(lib.kfac_factor_update(arr, len(sources), None, 0, _stream(stream)), "kfac_factor_update")
+    ws = _workspace(need, sources[0].x.device if sources else "cuda", workspace)
+    _check(lib.kfac_factor_update(arr, len(sources), ws.data_ptr(), ws.numel() * ws.element_size(),
+                                  _stream(stream)), "kfac_factor_update")
+    return ws
+
+
+# ------------------------------------------------------------ damp + invert
+
+@dataclass
+class InvertPair:
+    """Both factors of one layer and where their damped inverses go."""
+    A: torch.Tensor
+    G: torch.Tensor
+    A_inv: torch.Tensor
+    G_inv: torch.Tensor
+    A_inv_bf16: Optional[torch.Tensor] = None
+    G_inv_bf16: Optional[torch.Tensor] = None
+    dA: Optional[int] = None
+    dG: Optional[int] = None
+
+
+def _invert_descs(pairs: Sequence[InvertPair]):
+    arr = (InvertDesc * max(len(pairs), 1))()
+    for i, p in enumerate(pairs):
+        dA = p.dA or p.A.shape[0]
+        dG = p.dG or p.G.shape[0]
+        arr[i] = InvertDesc(p.A.data_ptr(), dA, _ld(p.A), p.G.data_ptr(), dG, _ld(p.G),
+                            p.A_inv.data_ptr(), _ld(p.A_inv), p.G_inv.data_ptr(), _ld(p.G_inv),
+                            _ptr(p.A_inv_bf16), _ld(p.A_inv_bf16) if p.A_inv_bf16 is not None else 0,
+                            _ptr(p.G_inv_bf16), _ld(p.G_inv_bf16) if p.G_inv_bf16 is not None else 0)
+    return arr
+
+
+def kfac_damp_invert_workspace_size(pairs: Sequence[InvertPair]) -> int:
+    return int(load().kfac_damp_invert_workspace_size(_invert_descs(pairs), len(pairs)))
+
+
+def kfac_damp_invert(pairs: Sequence[InvertPair], gamma: float, pi_split: bool = True,
+                     info: Optional[torch.Tensor] = None, damp: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Enqueue the damped inversions; returns the workspace used."""
+    lib = load()
+    arr = _invert_descs(pairs)
+    need = int(lib.kfac_damp_invert_workspace_size(arr, len(pairs)))
+    ws = _workspace(need, pairs[0].A.device if pairs else "cuda", workspace)
+    if info is not None:
+        assert info.dtype == torch.int32 and info.numel() >= 2 * len(pairs)
+    if damp is not None:
+        assert damp.dtype == torch.float32 and damp.numel() >= 2 * len(pairs)
+    _check(lib.kfac_damp_invert(arr, len(pairs), float(gamma), int(bool(pi_split)), _ptr(info), _ptr(damp),
+                                ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+           "kfac_damp_invert")
+    return ws
+
+
+# ------------------------------------------------------------ precondition
+
+@dataclass
+class PrecondItem:
+    """out = G_inv @ grad @ A_inv for one layer (grad [dG, dA])."""
+    G_inv: torch.Tensor
+    A_inv: torch.Tensor
+    grad: torch.Tensor
+    out: torch.Tensor
+    dG: Optional[int] = None
+    dA: Optional[int] = None
+
+
+def _precond_descs(items: Sequence[PrecondItem]):
+    arr = (PrecondDesc * max(len(items), 1))()
+    for i, it in enumerate(items):
+        dG = it.dG or it.grad.shape[0]
+        dA = it.dA or it.grad.shape[1]
+        arr[i] = PrecondDesc(dG, dA, it.G_inv.data_ptr(), _ld(it.G_inv), it.A_inv.data_ptr(), _ld(it.A_inv),
+                             it.grad.data_ptr(), _ld(it.grad), it.out.data_ptr(), _ld(it.out))
+    return arr
+
+
+def _precond_dtype(items: Sequence[PrecondItem]) -> int:
+    dts = {it.grad.dtype for it in items} | {it.A_inv.dtype for it in items} | {it.G_inv.dtype for it in items}
+    if dts == {torch.bfloat16}:
+        return KFAC_BF16
+    if dts == {torch.float32}:
+        return KFAC_F32
+    raise TypeError(f"operands must be all bf16 or all fp32, got {dts}")
+
+
+def kfac_precondition_workspace_size(items: Sequence[PrecondItem]) -> int:
+    return int(load().kfac_precondition_workspace_size(_precond_descs(items), len(items),
+                                                       _precond_dtype(items)))
+
+
+def kfac_precondition(items: Sequence[PrecondItem], workspace: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+    lib = load()
+    arr = _precond_descs(items)
+    dt = _precond_dtype(items)
+    need = int(lib.kfac_precondition_workspace_size(arr, len(items), dt))
+    ws = _workspace(need, items[0].grad.device if items else "cuda", workspace)
+    _check(lib.kfac_precondition(arr, len(items), dt, ws.data_ptr(), ws.numel() * ws.element_size(),
+                                 _stream(stream)), "kfac_precondition")
+    return ws
+
+
+# ------------------------------------------------------------ BN diagonal Fisher
+
+@dataclass
+class BnItem:
+    x: torch.Tensor            # [n_samples, C] fp32
+    F: torch.Tensor            # [C] fp32
+    precond: torch.Tensor      # [C] fp32
+    grad_mean: Optional[torch.Tensor] = None
+
+
+def kfac_bn_diag_fisher(items: Sequence[BnItem], gamma: float, xi: float = 0.0, stream=None) -> None:
+    lib = load()
+    arr = (BnDesc * max(len(items), 1))()
+    ns = items[0].x.shape[0] if items else 1
+    for i, it in enumerate(items):
+        assert it.x.dtype == torch.float32 and it.x.is_contiguous() and it.x.shape[0] == ns
+        arr[i] = BnDesc(it.x.data_ptr(), it.x.shape[1], it.F.data_ptr(), _ptr(it.grad_mean),
+                        it.precond.data_ptr())
+    _check(lib.kfac_bn_diag_fisher(arr, len(items), ns, float(gamma), float(xi), _stream(stream)),
+           "kfac_bn_diag_fisher")

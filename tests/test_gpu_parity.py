@@ -1,0 +1,280 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
+the same seeded inputs, at sizes the oracle finishes in seconds that still
+span several 128-wide tiles and a ragged tail.
+
+Tolerances (relative Frobenius error unless stated):
+  factors / preconditioned gradients from bf16 inputs   <= 2e-2
+  factors / preconditioned gradients from fp32 inputs   <= 1e-4
+  damped inverses: max |(F + damp I) inv - I|           <= 1e-3
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from second_order_optimisation_gb300 import kfac, workloads
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def rel(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    nb = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (nb if nb > 0 else 1.0))
+
+
+def bf16(a):
+    return workloads.to_bf16(a)
+
+
+def f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+# -------------------------------------------------------------- BN diag Fisher
+
+@pytest.mark.parametrize("C,ns", [(64, 1024), (96, 33), (7, 5), (2048, 1024), (130, 17)])
+def test_bn_diag_fisher(C, ns):
+    x = workloads.normal_f32((ns, C), 1e-2, "bn", C, ns)
+    xd = torch.from_numpy(x).to(DEV)
+    F = torch.full((C,), 0.5, device=DEV)
+    g = torch.empty(C, device=DEV)
+    p = torch.empty(C, device=DEV)
+    kfac.kfac_bn_diag_fisher([kfac.BnItem(xd, F, p, g)], 1e-3, xi=0.0)
+    torch.cuda.synchronize()
+    Fo, go, po = oracle.bn_diag_fisher(x, 1e-3)
+    assert rel(f64(F), Fo) <= 1e-4
+    assert rel(f64(g), go) <= 1e-4
+    assert rel(f64(p), po) <= 1e-4
+
+
+def test_bn_diag_fisher_ema_and_many_layers():
+    chans = [64, 256, 33, 2048, 512]
+    items, ref = [], []
+    for i, C in enumerate(chans):
+        x = workloads.normal_f32((64, C), 1e-2, "bnmany", i)
+        F0 = np.full(C, 0.25, dtype=np.float32)
+        it = kfac.BnItem(torch.from_numpy(x).to(DEV), torch.from_numpy(F0).to(DEV),
+                         torch.empty(C, device=DEV), torch.empty(C, device=DEV))
+        items.append(it)
+        ref.append(oracle.bn_diag_fisher(x, 1e-3, xi=0.9, F=F0))
+    kfac.kfac_bn_diag_fisher(items, 1e-3, xi=0.9)
+    torch.cuda.synchronize()
+    for it, (Fo, go, po) in zip(items, ref):
+        assert rel(f64(it.F), Fo) <= 1e-4
+        assert rel(f64(it.precond), po) <= 1e-4
+
+
+# -------------------------------------------------------------- factor update
+
+FACTOR_CASES = [
+    # name, (n, h, w, c), k, stride, pad, append_one
+    ("fc_ragged", (300, 1, 1, 200), 1, 1, 0, False),
+    ("fc_bias", (77, 1, 1, 136), 1, 1, 0, True),
+    ("fc_small_d", (1000, 1, 1, 8), 1, 1, 0, False),
+    ("conv3x3", (3, 9, 9, 64), 3, 1, 1, False),
+    ("conv7x7s2_c3", (2, 15, 15, 3), 7, 2, 3, False),
+    ("conv1x1s2", (2, 10, 10, 72), 1, 2, 0, False),
+    ("conv1x1_tall", (16, 14, 14, 64), 1, 1, 0, False),
+    ("conv3x3_wide", (2, 7, 7, 136), 3, 1, 1, False),
+]
+
+
+@pytest.mark.parametrize("case", FACTOR_CASES, ids=[c[0] for c in FACTOR_CASES])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_factor_statistic(case, dtype):
+    """Raw statistic (beta = 0, alpha = 1/M) and the EMA form from I, upper
+    triangle only; entries below the diagonal must stay untouched."""
+    name, shape, k, s, p, bias = case
+    x = workloads.relu_normal_f32(shape, "factor", name)
+    if dtype == "bf16":
+        xt = bf16(x)
+        xo = xt.float().numpy()
+    else:
+        xt = torch.from_numpy(x)
+        xo = x
+    xd = xt.to(DEV)
+    if shape[1] == 1 and shape[2] == 1:
+        xd = xd.reshape(shape[0], shape[3])
+        xo2 = xo.reshape(shape[0], shape[3])
+    else:
+        xo2 = xo
+    P = oracle.im2col(xo2, k, k, (s, s), (p, p), append_one=bias)
+    M, d = P.shape
+    S = oracle.gram(P)
+    ldf = d + 5
+    sentinel = -12345.0
+    for xi in (0.0, 0.95):
+        F = torch.full((d, ldf), sentinel, device=DEV)
+        up_mask = torch.triu(torch.ones(d, d, dtype=torch.bool, device=DEV))
+        init = torch.eye(d, device=DEV) if xi else torch.zeros(d, d, device=DEV)
+        F[:, :d] = torch.where(up_mask, init, torch.full_like(init, sentinel))
+        src = kfac.FactorSource(xd, F, k, k, (s, s), (p, p), bias, alpha=(1 - xi) / M, beta=xi)
+        ws = kfac.kfac_factor_update([src])
+        torch.cuda.synchronize()
+        assert int(ws[:4].view(torch.int32).item()) == 0
+        Fh = F.cpu().numpy().astype(np.float64)
+        up = np.triu(Fh[:, :d])
+        ref = np.triu(xi * np.eye(d) + (1 - xi) * S / M)
+        tol = 2e-2 if dtype == "bf16" else 1e-4
+        assert rel(up, ref) <= tol, (xi, rel(up, ref))
+        low = np.tril(np.ones((d, d), bool), -1)
+        assert np.all(Fh[:, :d][low] == sentinel)   # strictly-lower entries never written
+        assert np.all(Fh[:, d:] == sentinel)        # nothing written past d
+
+
+def test_factor_many_layers_one_call():
+    """A heterogeneous batch (several layers, A and G) in one call."""
+    layers = [workloads.Layer("a", 64, 40, 3, 1, 1, 6, 6), workloads.Layer("b", 24, 136, 1, 2, 0, 8, 4),
+              workloads.Layer("c", 136, 256, 1, 1, 0, 5, 5)]
+    srcs, refs = [], []
+    for L in layers:
+        x, g, _ = workloads.layer_inputs(L, 3, "many", grad_w=False)
+        M = L.rows(3)
+        A = torch.zeros(L.d_a, L.d_a, device=DEV)
+        G = torch.zeros(L.d_g, L.d_g, device=DEV)
+        srcs.append(kfac.FactorSource(x.to(DEV), A, L.k, L.k, (L.stride,) * 2, (L.pad,) * 2,
+                                      alpha=1.0 / M))
+        srcs.append(kfac.FactorSource(g.to(DEV), G, alpha=1.0 / M))
+        P = oracle.im2col(x.float().numpy(), L.k, L.k, (L.stride,) * 2, (L.pad,) * 2)
+        refs.append(oracle.gram(P) / M)
+        refs.append(oracle.gram(g.float().numpy()) / M)
+    kfac.kfac_factor_update(srcs)
+    torch.cuda.synchronize()
+    for s_, r in zip(srcs, refs):
+        assert rel(np.triu(f64(s_.F)), np.triu(r)) <= 2e-2
+
+
+def test_factor_chunked_accumulation():
+    """Statistic accumulated over 4 chunks (beta = xi, then 1) equals the
+    single statistic of all rows (gradient accumulation, section 2)."""
+    x = bf16(workloads.relu_normal_f32((4 * 50, 96), "chunks"))
+    M, xi = 200, 0.95
+    Fa = torch.eye(96, device=DEV)
+    for c in range(4):
+        kfac.kfac_factor_update([kfac.FactorSource(x[c * 50:(c + 1) * 50].contiguous().to(DEV), Fa,
+                                                   alpha=(1 - xi) / M, beta=xi if c == 0 else 1.0)])
+    torch.cuda.synchronize()
+    ref = oracle.factor_ema(np.eye(96), x.float().numpy(), xi)
+    assert rel(np.triu(f64(Fa)), np.triu(ref)) <= 2e-2
+
+
+# -------------------------------------------------------------- damped inverse
+
+def _spd_factor(d, tag, M=None, xi=0.0):
+    M = M or max(2 * d, 16)
+    P = workloads.relu_normal_f32((M, d), "inv", tag)
+    return oracle.factor_ema(np.eye(d), P, xi) if xi else oracle.gram(P) / M
+
+
+@pytest.mark.parametrize("dA,dG", [(1, 1), (5, 3), (64, 128), (129, 127), (200, 64), (300, 257),
+                                   (700, 130)])
+def test_damp_invert(dA, dG):
+    A = _spd_factor(dA, f"A{dA}").astype(np.float32)
+    G = (_spd_factor(dG, f"G{dG}") * 1e-4).astype(np.float32)
+    gamma = 1e-3
+    Ad = torch.from_numpy(np.triu(A)).to(DEV)       # only the upper triangle is read
+    Gd = torch.from_numpy(np.triu(G)).to(DEV)
+    Ai = torch.empty(dA, dA, device=DEV)
+    Gi = torch.empty(dG, dG + 3, device=DEV)
+    lda16 = (dA + 7) // 8 * 8
+    Ab = torch.empty(dA, lda16, dtype=torch.bfloat16, device=DEV)
+    info = torch.full((2,), -7, dtype=torch.int32, device=DEV)
+    damp = torch.empty(2, device=DEV)
+    kfac.kfac_damp_invert([kfac.InvertPair(Ad, Gd, Ai, Gi[:, :dG], Ab[:, :dA], None)], gamma,
+                          info=info, damp=damp)
+    torch.cuda.synchronize()
+    assert info.cpu().tolist() == [0, 0]
+    da, dg = oracle.pi_damping(A.astype(np.float64), G.astype(np.float64), gamma)
+    np.testing.assert_allclose(damp.cpu().numpy(), [da, dg], rtol=1e-4)
+    for F, inv, dmp in ((A, f64(Ai), da), (G, f64(Gi[:, :dG]), dg)):
+        d = F.shape[0]
+        R = (F.astype(np.float64) + dmp * np.eye(d)) @ inv - np.eye(d)
+        assert np.abs(R).max() <= 1e-3, np.abs(R).max()
+        assert np.array_equal(inv, inv.T)
+        ref = oracle.damped_inverse(F.astype(np.float64), dmp)
+        assert rel(inv, ref) <= 1e-3
+    np.testing.assert_allclose(f64(Ab[:, :dA]), f64(Ai), rtol=1e-2, atol=1e-2 * np.abs(f64(Ai)).max())
+
+
+def test_damp_invert_not_pd_reports_info():
+    """-I with gamma = 0 and no pi split: the first pivot fails; info says so
+    and nothing hangs."""
+    for d in (5, 200):
+        A = torch.triu(-torch.eye(d, device=DEV))
+        G = torch.eye(3, device=DEV)
+        info = torch.zeros(2, dtype=torch.int32, device=DEV)
+        kfac.kfac_damp_invert([kfac.InvertPair(A, G, torch.empty_like(A), torch.empty_like(G))], 0.0,
+                              pi_split=False, info=info)
+        torch.cuda.synchronize()
+        assert info.cpu().tolist() == [1, 0]
+
+
+# -------------------------------------------------------------- precondition
+
+@pytest.mark.parametrize("dG,dA", [(32, 65), (128, 200), (256, 576), (130, 1001)])
+def test_precondition_bf16(dG, dA):
+    rng_tag = ("pc", dG, dA)
+    Gi = workloads.normal_f32((dG, dG), 1.0, *rng_tag, "G")
+    Gi = (Gi + Gi.T) / 2
+    Ai = workloads.normal_f32((dA, dA), 1.0, *rng_tag, "A")
+    Ai = (Ai + Ai.T) / 2
+    grad = workloads.normal_f32((dG, dA), 1e-3, *rng_tag, "g")
+    Gb, Ab, gb = bf16(Gi), bf16(Ai), bf16(grad)
+    ld = (dA + 7) // 8 * 8
+    Abd = torch.zeros(dA, ld, dtype=torch.bfloat16, device=DEV)
+    Abd[:, :dA] = Ab.to(DEV)
+    gd = torch.zeros(dG, ld, dtype=torch.bfloat16, device=DEV)
+    gd[:, :dA] = gb.to(DEV)
+    ldg = (dG + 7) // 8 * 8
+    Gd = torch.zeros(dG, ldg, dtype=torch.bfloat16, device=DEV)
+    Gd[:, :dG] = Gb.to(DEV)
+    out = torch.empty(dG, dA, device=DEV)
+    kfac.kfac_precondition([kfac.PrecondItem(Gd[:, :dG], Abd[:, :dA], gd[:, :dA], out)])
+    torch.cuda.synchronize()
+    ref = oracle.precondition(Gb.float().numpy(), gb.float().numpy(), Ab.float().numpy())
+    assert rel(f64(out), ref) <= 2e-2
+
+
+def test_precondition_f32():
+    dG, dA = 70, 133
+    Gi = workloads.normal_f32((dG, dG), 1.0, "pcf", "G")
+    Ai = workloads.normal_f32((dA, dA), 1.0, "pcf", "A")
+    grad = workloads.normal_f32((dG, dA), 1e-3, "pcf", "g")
+    out = torch.empty(dG, dA, device=DEV)
+    kfac.kfac_precondition([kfac.PrecondItem(torch.from_numpy(Gi).to(DEV), torch.from_numpy(Ai).to(DEV),
+                                             torch.from_numpy(grad).to(DEV), out)])
+    torch.cuda.synchronize()
+    assert rel(f64(out), oracle.precondition(Gi, grad, Ai)) <= 1e-4
+
+
+# -------------------------------------------------------------- whole layer step
+
+def test_fc64x32_fp32_step():
+    """The single-FC-layer case: a[32,64] + bias column, g[32,32], fp32,
+    factors from I, xi = 0.95, gamma = 1e-3 split by pi."""
+    a, g = workloads.fc_small_fp32()
+    P = oracle.im2col(a.astype(np.float64), append_one=True)
+    grad = oracle.weight_grad(P, g.astype(np.float64), 32)
+    ref = oracle.kfac_layer_step(np.eye(65), np.eye(32), P, g.astype(np.float64), grad, xi=0.95,
+                                 gamma=1e-3)
+    A = torch.eye(65, device=DEV)
+    G = torch.eye(32, device=DEV)
+    kfac.kfac_factor_update([kfac.FactorSource(torch.from_numpy(a).to(DEV), A, append_one=True,
+                                               alpha=0.05 / 32, beta=0.95),
+                             kfac.FactorSource(torch.from_numpy(g).to(DEV), G, alpha=0.05 / 32, beta=0.95)])
+    Ai, Gi = torch.empty_like(A), torch.empty_like(G)
+    info = torch.zeros(2, dtype=torch.int32, device=DEV)
+    kfac.kfac_damp_invert([kfac.InvertPair(A, G, Ai, Gi)], 1e-3, info=info)
+    out = torch.empty(32, 65, device=DEV)
+    kfac.kfac_precondition([kfac.PrecondItem(Gi, Ai, torch.from_numpy(grad.astype(np.float32)).to(DEV), out)])
+    torch.cuda.synchronize()
+    assert info.cpu().tolist() == [0, 0]
+    assert rel(np.triu(f64(A)), np.triu(ref["A"])) <= 1e-4
+    assert rel(np.triu(f64(G)), np.triu(ref["G"])) <= 1e-4
+    for F, inv, dmp in ((ref["A"], f64(Ai), ref["damp_A"]), (ref["G"], f64(Gi), ref["damp_G"])):
+        R = (F + dmp * np.eye(F.shape[0])) @ inv - np.eye(F.shape[0])
+        assert np.abs(R).max() <= 1e-3
+    assert rel(f64(out), ref["precond"]) <= 1e-4
