@@ -61,6 +61,10 @@ const char *kfac_status_string(int status);
 /* Library version as major*10000 + minor*100 + patch. */
 int kfac_version(void);
 
+/* Number of kernel launches this library has enqueued in this process so far
+ * (a diagnostic counter; every entry point adds the launches it makes). */
+long long kfac_launch_count(void);
+
 /* ======================================================================
  * kfac_factor_update -- Kronecker factor statistic + running average.
  *

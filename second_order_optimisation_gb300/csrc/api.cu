@@ -5,6 +5,7 @@
 // Kronecker-Factored Approximate Curvature for Deep Convolutional Neural
 // Networks", section 3.2 (Eq. 5-7) and section 1 (diagonal BatchNorm Fisher).
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -13,6 +14,9 @@
 #include "internal.h"
 
 namespace kfac {
+
+static std::atomic<long long> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int device_sm_count() {
     static int cache[64] = {0};
@@ -159,6 +163,8 @@ extern "C" const char *kfac_status_string(int status) {
 }
 
 extern "C" int kfac_version(void) { return 100; }
+
+extern "C" long long kfac_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 // ------------------------------------------------------------ factor update
 

@@ -136,7 +136,7 @@ extern "C" kfac_status kfac_bn_diag_fisher(const kfac_bn_desc *descs, int count,
         P->gamma = gamma;
         P->xi = xi;
         bn_fisher_kernel<<<chunks, 256, 0, st>>>(*P);
-        if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
+        KFAC_LAUNCH_CHECK();
     }
     return KFAC_OK;
 }

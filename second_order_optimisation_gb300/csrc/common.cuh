@@ -25,8 +25,13 @@ namespace kfac {
         if (e_ != cudaSuccess) return KFAC_ERR_CUDA;             \
     } while (0)
 
+// Counts every kernel launch the library enqueues (diagnostic only; read
+// through kfac_launch_count()).
+void count_launch();
+
 #define KFAC_LAUNCH_CHECK()                                      \
     do {                                                         \
+        ::kfac::count_launch();                                  \
         if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA; \
     } while (0)
 

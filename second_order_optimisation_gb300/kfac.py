@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_HERE, "libkfac_gb300.so")
 KFAC_OK, KFAC_ERR_INVALID, KFAC_ERR_UNSUPPORTED, KFAC_ERR_NOT_PD, KFAC_ERR_CUDA, KFAC_ERR_WORKSPACE = range(6)
 KFAC_BF16, KFAC_F32 = 0, 1
 
-EXPORTS = ("kfac_status_string", "kfac_version", "kfac_factor_update_workspace_size",
+EXPORTS = ("kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_factor_update_workspace_size",
            "kfac_factor_update", "kfac_damp_invert_workspace_size", "kfac_damp_invert",
            "kfac_precondition_workspace_size", "kfac_precondition", "kfac_bn_diag_fisher")
 
@@ -89,6 +89,7 @@ def load() -> ctypes.CDLL:
         lib.kfac_status_string.argtypes = [i32]
         lib.kfac_status_string.restype = ctypes.c_char_p
         lib.kfac_version.restype = i32
+        lib.kfac_launch_count.restype = ctypes.c_longlong
         lib.kfac_factor_update_workspace_size.argtypes = [vp, i32]
         lib.kfac_factor_update_workspace_size.restype = sz
         lib.kfac_factor_update.argtypes = [vp, i32, vp, sz, vp]
@@ -103,6 +104,11 @@ def load() -> ctypes.CDLL:
             getattr(lib, f).restype = i32
         _lib = lib
     return _lib
+
+
+def launch_count() -> int:
+    """Kernel launches the library has enqueued in this process."""
+    return int(load().kfac_launch_count())
 
 
 def status_string(status: int) -> str:

@@ -1,0 +1,124 @@
+"""One K-FAC curvature step over a layer set, through the C ABI.
+
+`KfacStep` owns the per-layer state (running factors A, G; damped inverses in
+fp32 and bf16; preconditioned gradients) and the three workspaces, all
+allocated once on the device.  `run()` enqueues the hot path of Osawa et al.
+(section 3.2, Eq. 5-7) for every layer on the current stream:
+
+    kfac_factor_update  (A from the layer inputs, G from the output grads,
+                         running average with xi, all layers in one call)
+    kfac_damp_invert    (pi-split Tikhonov damping, all layers in one call)
+    kfac_precondition   (G^-1 grad A^-1, all layers in one call)
+
+Inputs are the per-layer bf16 tensors x (NHWC), g ([M, C_out]) and grad
+([C_out, d_A]); with `rows_total` the statistic of several chunks of a larger
+mini-batch can be accumulated before the inversion (gradient accumulation,
+section 2).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import kfac
+from .workloads import Layer
+
+
+def _ld8(d: int) -> int:
+    return (d + 7) // 8 * 8
+
+
+@dataclass
+class LayerState:
+    layer: Layer
+    A: torch.Tensor
+    G: torch.Tensor
+    A_inv: torch.Tensor
+    G_inv: torch.Tensor
+    A_inv16: torch.Tensor      # [dA, ld8(dA)] bf16 (view of the first dA columns used)
+    G_inv16: torch.Tensor
+    out: torch.Tensor          # preconditioned gradient [dG, dA] fp32
+
+
+class KfacStep:
+    def __init__(self, layers: Sequence[Layer], batch: int, xi: float = 0.95, gamma: float = 1e-3,
+                 device="cuda"):
+        self.layers = list(layers)
+        self.batch = batch
+        self.xi = xi
+        self.gamma = gamma
+        self.device = torch.device(device)
+        self.state: List[LayerState] = []
+        for L in self.layers:
+            dA, dG = L.d_a, L.d_g
+            self.state.append(LayerState(
+                L,
+                torch.eye(dA, device=self.device), torch.eye(dG, device=self.device),
+                torch.empty(dA, dA, device=self.device), torch.empty(dG, dG, device=self.device),
+                torch.empty(dA, _ld8(dA), dtype=torch.bfloat16, device=self.device),
+                torch.empty(dG, _ld8(dG), dtype=torch.bfloat16, device=self.device),
+                torch.empty(dG, dA, device=self.device)))
+        self.info = torch.zeros(2 * len(self.layers), dtype=torch.int32, device=self.device)
+        self.damp = torch.zeros(2 * len(self.layers), device=self.device)
+        self._ws = {}
+
+    # ---------------------------------------------------------------- pieces
+    def reset_factors(self):
+        for s in self.state:
+            s.A.copy_(torch.eye(s.A.shape[0], device=self.device))
+            s.G.copy_(torch.eye(s.G.shape[0], device=self.device))
+
+    def factor_sources(self, xs, gs, rows_total: Optional[Sequence[int]] = None, first: bool = True):
+        srcs = []
+        for i, (s, x, g) in enumerate(zip(self.state, xs, gs)):
+            L = s.layer
+            M = rows_total[i] if rows_total is not None else L.rows(self.batch)
+            alpha = (1.0 - self.xi) / M
+            beta = self.xi if first else 1.0
+            if L.name == "fc" or (L.hin == 1 and L.k == 1):
+                xa = x.reshape(x.shape[0], -1)
+            else:
+                xa = x
+            srcs.append(kfac.FactorSource(xa, s.A, L.k, L.k, (L.stride, L.stride), (L.pad, L.pad),
+                                          L.bias, alpha, beta))
+            srcs.append(kfac.FactorSource(g, s.G, alpha=alpha, beta=beta))
+        return srcs
+
+    def invert_pairs(self):
+        return [kfac.InvertPair(s.A, s.G, s.A_inv, s.G_inv, s.A_inv16[:, :s.A.shape[0]],
+                                s.G_inv16[:, :s.G.shape[0]]) for s in self.state]
+
+    def precond_items(self, grads):
+        return [kfac.PrecondItem(s.G_inv16[:, :s.G.shape[0]], s.A_inv16[:, :s.A.shape[0]], gr, s.out)
+                for s, gr in zip(self.state, grads)]
+
+    def _workspace(self, key, nbytes):
+        w = self._ws.get(key)
+        if w is None or w.numel() < nbytes:
+            w = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+            self._ws[key] = w
+        return w
+
+    # ---------------------------------------------------------------- phases
+    def factor_update(self, xs, gs, rows_total=None, first=True, stream=None):
+        srcs = self.factor_sources(xs, gs, rows_total, first)
+        ws = self._workspace("factor", kfac.kfac_factor_update_workspace_size(srcs))
+        kfac.kfac_factor_update(srcs, ws, stream)
+
+    def damp_invert(self, stream=None):
+        pairs = self.invert_pairs()
+        ws = self._workspace("invert", kfac.kfac_damp_invert_workspace_size(pairs))
+        kfac.kfac_damp_invert(pairs, self.gamma, True, self.info, self.damp, ws, stream)
+
+    def precondition(self, grads, stream=None):
+        items = self.precond_items(grads)
+        ws = self._workspace("precond", kfac.kfac_precondition_workspace_size(items))
+        kfac.kfac_precondition(items, ws, stream)
+
+    def run(self, xs, gs, grads, stream=None):
+        """One full step: factors + inverse + preconditioning for all layers."""
+        self.factor_update(xs, gs, stream=stream)
+        self.damp_invert(stream)
+        self.precondition(grads, stream)
