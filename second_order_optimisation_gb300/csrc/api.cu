@@ -94,11 +94,19 @@ struct FactorPlan {
     int *err = nullptr;
     char *tc_ws = nullptr;
     size_t tc_bytes = 0;
+    std::vector<CUtensorMap> maps;
+    CUtensorMap *dev_maps = nullptr;
 };
 
+// Lays out the workspace (error word, tensor maps, patch matrices, engine
+// scratch) and the jobs; tensor maps are encoded only when `encode` is set
+// (the size query runs without real pointers).
 kfac_status plan_factor(const kfac_factor_desc *descs, int count, const std::vector<FactorGeom> &geo,
-                        Arena &ws, FactorPlan &p) {
+                        Arena &ws, FactorPlan &p, bool encode) {
     p.err = ws.take<int>(64);
+    int nbf16 = 0;
+    for (int i = 0; i < count; ++i) nbf16 += descs[i].dtype == KFAC_BF16;
+    p.dev_maps = ws.take<CUtensorMap>(std::max(nbf16, 1));
     for (int i = 0; i < count; ++i) {
         const kfac_factor_desc &d = descs[i];
         const FactorGeom &g = geo[i];
@@ -125,8 +133,11 @@ kfac_status plan_factor(const kfac_factor_desc *descs, int count, const std::vec
             src = P;
         }
         TcJob j{};
-        j.a = src; j.lda = lds; j.a_rows = (int)g.M; j.a_cols = g.dcore; j.a_mn = 1;
-        j.b = src; j.ldb = lds; j.b_rows = (int)g.M; j.b_cols = g.dcore; j.b_mn = 1;
+        j.map_a = j.map_b = (int)p.maps.size();
+        p.maps.emplace_back();
+        if (encode && !tc_make_map(&p.maps.back(), TC_KIND_BF16, src, lds, (int)g.M, g.dcore, 1))
+            return KFAC_ERR_CUDA;
+        j.a_mn = j.b_mn = 1;
         j.M = g.dcore; j.N = g.dcore; j.K = (int)g.M;
         j.syrk = 1;
         j.epi = TC_EPI_ACCUM;
@@ -140,7 +151,7 @@ kfac_status plan_factor(const kfac_factor_desc *descs, int count, const std::vec
             p.cs.push_back(ColsumJob{(const uint16_t *)d.x, g.M, d.c, d.F, d.ldf, d.alpha, d.beta});
         }
     }
-    p.tc_bytes = tc_workspace_bytes(p.tc.data(), (int)p.tc.size());
+    p.tc_bytes = tc_workspace_bytes(p.tc.data(), (int)p.tc.size(), TC_KIND_BF16);
     p.tc_ws = ws.take<char>(p.tc_bytes);
     return KFAC_OK;
 }
@@ -173,7 +184,7 @@ extern "C" size_t kfac_factor_update_workspace_size(const kfac_factor_desc *desc
     if (validate_factor(descs, count, geo) != KFAC_OK) return 0;
     Arena a;
     FactorPlan p;
-    if (plan_factor(descs, count, geo, a, p) != KFAC_OK) return 0;
+    if (plan_factor(descs, count, geo, a, p, false) != KFAC_OK) return 0;
     return a.used;
 }
 
@@ -186,7 +197,11 @@ extern "C" kfac_status kfac_factor_update(const kfac_factor_desc *descs, int cou
     if (!workspace || ((uintptr_t)workspace % 256) != 0) return KFAC_ERR_WORKSPACE;
     Arena ws(workspace, workspace_bytes);
     FactorPlan p;
-    if ((s = plan_factor(descs, count, geo, ws, p)) != KFAC_OK) return s;
+    if ((s = plan_factor(descs, count, geo, ws, p, false)) != KFAC_OK) return s;
+    if (!ws.fits()) return KFAC_ERR_WORKSPACE;
+    ws = Arena(workspace, workspace_bytes);
+    p = FactorPlan();
+    if ((s = plan_factor(descs, count, geo, ws, p, true)) != KFAC_OK) return s;
     if (!ws.fits()) return KFAC_ERR_WORKSPACE;
     Arena tail(p.tc_ws, p.tc_bytes);
     cudaStream_t st = (cudaStream_t)stream;
@@ -195,7 +210,11 @@ extern "C" kfac_status kfac_factor_update(const kfac_factor_desc *descs, int cou
         return s;
     if (!p.im32.empty() && (s = im2col_run(p.im32.data(), (int)p.im32.size(), KFAC_F32, st)) != KFAC_OK)
         return s;
-    if (!p.tc.empty() && (s = tc_run(p.tc.data(), (int)p.tc.size(), tail, p.err, st)) != KFAC_OK) return s;
+    if (!p.tc.empty()) {
+        if ((s = tc_upload_maps(p.maps.data(), (int)p.maps.size(), p.dev_maps, st)) != KFAC_OK) return s;
+        if ((s = tc_run(p.tc.data(), (int)p.tc.size(), TC_KIND_BF16, p.dev_maps, tail, p.err, st)) != KFAC_OK)
+            return s;
+    }
     if (!p.sg.empty() && (s = sg_run(p.sg.data(), (int)p.sg.size(), st)) != KFAC_OK) return s;
     if (!p.cs.empty() && (s = colsum_run(p.cs.data(), (int)p.cs.size(), st)) != KFAC_OK) return s;
     return KFAC_OK;
@@ -294,28 +313,39 @@ struct PrecondPlan {
     int *err = nullptr;
     char *tc_ws = nullptr;
     size_t tc_bytes = 0;
+    std::vector<CUtensorMap> maps;
+    CUtensorMap *dev_maps = nullptr;
 };
 
-void plan_precond(const kfac_precond_desc *descs, int count, int dtype, Arena &ws, PrecondPlan &p) {
+kfac_status plan_precond(const kfac_precond_desc *descs, int count, int dtype, Arena &ws, PrecondPlan &p,
+                         bool encode) {
     p.err = ws.take<int>(64);
+    if (dtype == KFAC_BF16) p.dev_maps = ws.take<CUtensorMap>(4 * (size_t)count);
+    auto map = [&](const void *ptr, long long ld, int rows, int cols, int mn) {
+        p.maps.emplace_back();
+        if (encode && !tc_make_map(&p.maps.back(), TC_KIND_BF16, ptr, ld, rows, cols, mn)) return -1;
+        return (int)p.maps.size() - 1;
+    };
     for (int i = 0; i < count; ++i) {
         const kfac_precond_desc &d = descs[i];
         if (dtype == KFAC_BF16) {
             const long long ldt = (d.dA + 7) / 8 * 8;
             uint16_t *T = ws.take<uint16_t>((size_t)d.dG * ldt);
-            TcJob a{};  // T = grad * A_inv   (A_inv symmetric: read rows as B^T)
-            a.a = (const uint16_t *)d.grad; a.lda = d.ld_grad; a.a_rows = d.dG; a.a_cols = d.dA; a.a_mn = 0;
-            a.b = (const uint16_t *)d.A_inv; a.ldb = d.ld_ainv; a.b_rows = d.dA; a.b_cols = d.dA; a.b_mn = 0;
+            TcJob a{};  // T = grad * A_inv   (A_inv symmetric: its rows are the columns of B)
+            a.map_a = map(d.grad, d.ld_grad, d.dG, d.dA, 0);
+            a.map_b = map(d.A_inv, d.ld_ainv, d.dA, d.dA, 0);
             a.M = d.dG; a.N = d.dA; a.K = d.dA;
             a.epi = TC_EPI_STORE; a.alpha = 1.f; a.beta = 0.f;
             a.Cb = T; a.ldcb = ldt;
-            p.g1.push_back(a);
-            TcJob b{};  // out = G_inv * T
-            b.a = (const uint16_t *)d.G_inv; b.lda = d.ld_ginv; b.a_rows = d.dG; b.a_cols = d.dG; b.a_mn = 0;
-            b.b = T; b.ldb = ldt; b.b_rows = d.dG; b.b_cols = d.dA; b.b_mn = 1;
+            TcJob b{};  // out = G_inv * T   (T read MN-major)
+            b.map_a = map(d.G_inv, d.ld_ginv, d.dG, d.dG, 0);
+            b.map_b = map(T, ldt, d.dG, d.dA, 1);
+            b.b_mn = 1;
             b.M = d.dG; b.N = d.dA; b.K = d.dG;
             b.epi = TC_EPI_STORE; b.alpha = 1.f; b.beta = 0.f;
             b.C = d.out; b.ldc = d.ld_out;
+            if (a.map_a < 0 || a.map_b < 0 || b.map_a < 0 || b.map_b < 0) return KFAC_ERR_CUDA;
+            p.g1.push_back(a);
             p.g2.push_back(b);
         } else {
             float *T = ws.take<float>((size_t)d.dG * d.dA);
@@ -325,10 +355,11 @@ void plan_precond(const kfac_precond_desc *descs, int count, int dtype, Arena &w
                                  nullptr, 0, d.dG, d.dA, d.dG, 1.f, 0.f, 0});
         }
     }
-    size_t t1 = tc_workspace_bytes(p.g1.data(), (int)p.g1.size());
-    size_t t2 = tc_workspace_bytes(p.g2.data(), (int)p.g2.size());
+    size_t t1 = tc_workspace_bytes(p.g1.data(), (int)p.g1.size(), TC_KIND_BF16);
+    size_t t2 = tc_workspace_bytes(p.g2.data(), (int)p.g2.size(), TC_KIND_BF16);
     p.tc_bytes = std::max(t1, t2);
     p.tc_ws = ws.take<char>(p.tc_bytes);
+    return KFAC_OK;
 }
 
 }  // namespace
@@ -337,7 +368,7 @@ extern "C" size_t kfac_precondition_workspace_size(const kfac_precond_desc *desc
     if (validate_precond(descs, count, dtype) != KFAC_OK) return 0;
     Arena a;
     PrecondPlan p;
-    plan_precond(descs, count, dtype, a, p);
+    if (plan_precond(descs, count, dtype, a, p, false) != KFAC_OK) return 0;
     return a.used;
 }
 
@@ -349,15 +380,20 @@ extern "C" kfac_status kfac_precondition(const kfac_precond_desc *descs, int cou
     if (!workspace || ((uintptr_t)workspace % 256) != 0) return KFAC_ERR_WORKSPACE;
     Arena ws(workspace, workspace_bytes);
     PrecondPlan p;
-    plan_precond(descs, count, dtype, ws, p);
+    if ((s = plan_precond(descs, count, dtype, ws, p, false)) != KFAC_OK) return s;
     if (!ws.fits()) return KFAC_ERR_WORKSPACE;
+    ws = Arena(workspace, workspace_bytes);
+    p = PrecondPlan();
+    if ((s = plan_precond(descs, count, dtype, ws, p, true)) != KFAC_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
     if (dtype == KFAC_BF16) {
         KFAC_CUDA_TRY(cudaMemsetAsync(p.err, 0, sizeof(int), st));
+        if ((s = tc_upload_maps(p.maps.data(), (int)p.maps.size(), p.dev_maps, st)) != KFAC_OK) return s;
         Arena t_a(p.tc_ws, p.tc_bytes);
-        if ((s = tc_run(p.g1.data(), (int)p.g1.size(), t_a, p.err, st)) != KFAC_OK) return s;
+        if ((s = tc_run(p.g1.data(), (int)p.g1.size(), TC_KIND_BF16, p.dev_maps, t_a, p.err, st)) != KFAC_OK)
+            return s;
         Arena t_b(p.tc_ws, p.tc_bytes);
-        return tc_run(p.g2.data(), (int)p.g2.size(), t_b, p.err, st);
+        return tc_run(p.g2.data(), (int)p.g2.size(), TC_KIND_BF16, p.dev_maps, t_b, p.err, st);
     }
     if ((s = sg_run(p.s1.data(), (int)p.s1.size(), st)) != KFAC_OK) return s;
     return sg_run(p.s2.data(), (int)p.s2.size(), st);

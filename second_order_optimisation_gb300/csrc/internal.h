@@ -10,40 +10,54 @@
 namespace kfac {
 
 // ----------------------------------------------------- tensor-core GEMM
-// One problem of the tcgen05 engine: C[M x N] = alpha * op(A) op(B) (+ beta C)
-// with bf16 operands and fp32 accumulation.
-//   a_mn = 1: A stored [K][M] (M contiguous);  a_mn = 0: A stored [M][K].
-//   b_mn = 1: B stored [K][N] (N contiguous);  b_mn = 0: B stored [N][K].
-//   syrk = 1: B is the same matrix as A (the Gram matrix A^T A of a [K][M]
-//             source), only tiles touching the upper triangle are computed
-//             and only entries i <= j are written.
+// One problem of the tcgen05 engine: C[M x N] = alpha * op(A) op(B) (+ beta C),
+// fp32 accumulation.  Operands are read through tensor maps (see tc_make_map)
+// that the caller uploads into device memory with tc_upload_maps; a problem
+// names its maps by index and its operand sub-blocks by (row0, col0).
+//   TC_KIND_BF16:   a_mn = 1: A stored [K][M] (M contiguous); 0: A stored [M][K].
+//                   b_mn = 1: B stored [K][N] (N contiguous); 0: B stored [N][K].
+//                   syrk = 1: B is A (Gram matrix of a [K][M] source), only
+//                   tiles touching the upper triangle run and only i <= j is written.
+//   TC_KIND_TF32X3: K-major only (A [M][K], B [N][K]); maps come in (hi, lo)
+//                   pairs at consecutive indices; 3 MMAs per K slice.
+enum TcKind : int { TC_KIND_BF16 = 0, TC_KIND_TF32X3 = 1 };
 enum TcEpilogue : int {
     TC_EPI_ACCUM = 0,  // fp32 C[i][j] = beta*C[i][j] + alpha*acc (C read only if beta != 0)
-    TC_EPI_STORE = 1   // C (fp32, optional) and/or Cb (bf16, optional) = alpha*acc
+    TC_EPI_STORE = 1,  // C (fp32, optional) and/or Cb (bf16, optional) = alpha*acc
+    TC_EPI_SPLIT = 2   // v = alpha*acc + beta*(C + C_lo); C = tf32(v), C_lo = v - C;
+                       // optional transposed copy into Ct / Ct_lo
 };
 
 struct TcJob {
-    const uint16_t *a;
-    long long lda;
-    int a_rows, a_cols, a_mn;
-    const uint16_t *b;
-    long long ldb;
-    int b_rows, b_cols, b_mn;
+    int map_a, map_b;
+    int a_mn, b_mn;
+    int a_row0, a_col0, b_row0, b_col0;
     int M, N, K;
     int syrk;
+    int no_split;
     int epi;
     float alpha, beta;
     float *C;
+    float *C_lo;
     long long ldc;
+    float *Ct;
+    float *Ct_lo;
+    long long ldct;
     uint16_t *Cb;
     long long ldcb;
 };
 
+// Tensor map of a row-major [rows][cols] matrix (ld elements) for the engine:
+// 128-byte swizzle, box 128 bytes wide and 128 rows (64 rows if mn_major).
+bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int mn_major);
+// Copies host-built maps into device memory (128-byte aligned) on the stream.
+kfac_status tc_upload_maps(const CUtensorMap *maps, int n, CUtensorMap *dev, cudaStream_t st);
 // Workspace needed by tc_run for these jobs (split-K partials, counters).
-size_t tc_workspace_bytes(const TcJob *jobs, int njobs);
-// Enqueue the jobs (one or more persistent launches).  `err` is a device
-// int that collects timeout codes.  Returns KFAC_OK or an error.
-kfac_status tc_run(const TcJob *jobs, int njobs, Arena &ws, int *err, cudaStream_t st);
+size_t tc_workspace_bytes(const TcJob *jobs, int njobs, int kind);
+// Enqueue the jobs (one or more persistent launches).  `err` is a device int
+// that collects timeout codes.
+kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *dev_maps, Arena &ws,
+                   int *err, cudaStream_t st);
 
 // ----------------------------------------------------- CUDA-core GEMM (fp32)
 // C[M x N] = alpha * op(A) op(B) + beta * C, fp32.

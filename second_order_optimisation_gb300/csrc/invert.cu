@@ -8,24 +8,32 @@
 //     pi = sqrt((tr A/dA) / (tr G/dG)),  damp_A = pi sqrt(gamma),  damp_G = sqrt(gamma)/pi.
 //
 // Algorithm (every matrix of the call advances in lock-step, one batched
-// launch per step):
+// launch per step kind):
 //   1. traces -> damping values (one CTA per layer, fixed reduction order);
-//   2. X = sym(F) + damp I into the output buffer (F's upper triangle read);
-//   3. blocked Cholesky-based inversion by recursive 2x2 blocking
+//   2. X = sym(F) + damp I, padded with an identity block to a multiple of
+//      128 (the inverse of diag(X, I) is diag(X^-1, I)), stored as a (hi, lo)
+//      pair with hi exactly representable in tf32 and hi + lo = X;
+//   3. blocked Cholesky-based inversion by recursive 2x2 blocking on 128-row
+//      block boundaries; the Schur complement X22 - X21 X11^-1 X12 is the
+//      trailing update of a block Cholesky step:
 //        X11 <- X11^-1                               (recursion / leaf)
-//        T   <- X11 X12                              (GEMM)
-//        X22 <- X22 - X12^T T     (Schur complement = trailing Cholesky update)
+//        T   <- X11 X12,   U <- T^T                  (tensor cores)
+//        X22 <- X22 - X21 T                          (tensor cores)
 //        X22 <- X22^-1                               (recursion / leaf)
-//        X12 <- -T X22,  X21 <- X12^T                (GEMM)
-//        X11 <- X11 - X12 T^T                        (GEMM)
-//      leaves (n <= 128) run in one CTA in shared memory: Cholesky
-//      X = U^T U, triangular inverse V = U^-1, then V V^T;
-//   4. mirror the upper triangle to the lower one (exact symmetry) and write
-//      the optional bf16 copies.
-// A pivot that is not positive and finite records its 1-based global index in
+//        X12 <- -T X22,    X21 <- X12^T              (tensor cores)
+//        X11 <- X11 - X12 T^T                        (tensor cores)
+//      The GEMMs run on tcgen05 with three tf32 products per slice
+//      (hi*hi + hi*lo + lo*hi) and fp32 accumulation.  Leaves are 128 x 128
+//      blocks inverted by one CTA with the matrix in registers: Cholesky
+//      X = U^T U, triangular inverse V = U^-1, then V V^T, each step one
+//      barrier with the pivot row broadcast through shared memory;
+//   4. out = hi + lo of the upper triangle mirrored to the lower one (exact
+//      symmetry), plus the optional bf16 copy.
+// A pivot that is not positive and finite records its 1-based index in
 // info[matrix]; nothing traps or waits.
 #include <algorithm>
 #include <memory>
+#include <mutex>
 #include <vector>
 
 #include "internal.h"
@@ -37,6 +45,12 @@ namespace {
 constexpr int LEAF = 128;
 constexpr int LEAF_THREADS = 512;
 constexpr int MAT_MAX = 224;
+
+inline int padded(int d) { return (int)ceil_div(d, LEAF) * LEAF; }
+
+__device__ __forceinline__ float tf32_hi(float v) {
+    return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+}
 
 // ---------------------------------------------------------------- damping
 
@@ -85,68 +99,101 @@ __global__ void __launch_bounds__(256) damping_kernel(const __grid_constant__ Da
     }
 }
 
-// --------------------------------------------------- symmetrise / mirror
+// ------------------------------------------------------ prepare / finish
 
-struct SymMat {
-    const float *src;
-    long long lds;
-    float *dst;
-    long long ldd;
-    uint16_t *dst16;
+struct TileMat {
+    const float *F;   // prep: factor (upper read); finish: unused
+    long long ldf;
+    float *Xh, *Xl;   // working pair [dp][dp]
+    int d, dp;
+    float *out;       // finish: full symmetric fp32 output
+    long long ldo;
+    uint16_t *out16;  // finish: optional bf16 copy
     long long ld16;
-    int n;
-    int tiles;      // tiles per side (32x32)
-    int damp_idx;   // -1: none
+    int damp_idx;
+    int tiles;        // per side
 };
 
-struct SymParams {
-    SymMat m[MAT_MAX];
+struct TileParams {
+    TileMat m[MAT_MAX];
     int begin[MAT_MAX + 1];
     int n;
-    int in_place;   // 1: src == dst, mirror upper -> lower
     const float *damp;
 };
 
-__global__ void __launch_bounds__(256) sym_kernel(const __grid_constant__ SymParams P) {
+// X = split(sym(F) + damp I) on [d, d], identity on the padding.
+__global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ TileParams P) {
     __shared__ float t[32][33];
     int lo = 0, hi = P.n - 1;
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
         if (P.begin[mid] <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
     }
-    const SymMat &q = P.m[lo];
+    const TileMat &q = P.m[lo];
     const int tt = blockIdx.x - P.begin[lo];
     const int ti = tt / q.tiles, tj = tt - ti * q.tiles;
     const int si = min(ti, tj), sj = max(ti, tj);
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-    // load source tile (si, sj) of the upper triangle
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     for (int r = ty; r < 32; r += 8) {
         const int i = si * 32 + r, j = sj * 32 + tx;
-        t[r][tx] = (i < q.n && j < q.n) ? q.src[(long long)i * q.lds + j] : 0.f;
+        t[r][tx] = (i < q.d && j < q.d) ? q.F[(long long)i * q.ldf + j] : 0.f;
     }
     __syncthreads();
-    if (P.in_place && ti < tj && !q.dst16) return;
-    const float dv = (q.damp_idx >= 0) ? P.damp[q.damp_idx] : 0.f;
+    const float dv = P.damp[q.damp_idx];
     for (int r = ty; r < 32; r += 8) {
         const int i = ti * 32 + r, j = tj * 32 + tx;
-        if (i >= q.n || j >= q.n) continue;
+        float v;
+        if (i >= q.d || j >= q.d) {
+            v = (i == j) ? 1.f : 0.f;
+        } else {
+            if (ti < tj) v = t[r][tx];
+            else if (ti > tj) v = t[tx][r];
+            else v = (r <= tx) ? t[r][tx] : t[tx][r];
+            if (i == j) v += dv;
+        }
+        const float h = tf32_hi(v);
+        q.Xh[(long long)i * q.dp + j] = h;
+        q.Xl[(long long)i * q.dp + j] = v - h;
+    }
+}
+
+// out = hi + lo of the upper triangle, mirrored; optional bf16 copy.
+__global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ TileParams P) {
+    __shared__ float t[32][33];
+    int lo = 0, hi = P.n - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (P.begin[mid] <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
+    }
+    const TileMat &q = P.m[lo];
+    const int tt = blockIdx.x - P.begin[lo];
+    const int ti = tt / q.tiles, tj = tt - ti * q.tiles;
+    const int si = min(ti, tj), sj = max(ti, tj);
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int r = ty; r < 32; r += 8) {
+        const int i = si * 32 + r, j = sj * 32 + tx;
+        const long long o = (long long)i * q.dp + j;
+        t[r][tx] = (i < q.d && j < q.d) ? q.Xh[o] + q.Xl[o] : 0.f;
+    }
+    __syncthreads();
+    for (int r = ty; r < 32; r += 8) {
+        const int i = ti * 32 + r, j = tj * 32 + tx;
+        if (i >= q.d || j >= q.d) continue;
         float v;
         if (ti < tj) v = t[r][tx];
         else if (ti > tj) v = t[tx][r];
         else v = (r <= tx) ? t[r][tx] : t[tx][r];
-        if (i == j) v += dv;
-        if (!(P.in_place && ti < tj)) q.dst[(long long)i * q.ldd + j] = v;
-        if (q.dst16) q.dst16[(long long)i * q.ld16 + j] = f32_to_bf16_bits(v);
+        q.out[(long long)i * q.ldo + j] = v;
+        if (q.out16) q.out16[(long long)i * q.ld16 + j] = f32_to_bf16_bits(v);
     }
 }
 
 // ------------------------------------------------------------------ leaf
 
 struct LeafJob {
-    float *X;       // block start (row o, column o)
+    float *Xh, *Xl;  // block start (row o, column o) of the working pair
     long long ld;
-    int n;
-    int o;          // global offset, for info
+    int o;           // global offset, for info
     int *info;
 };
 
@@ -155,152 +202,374 @@ struct LeafParams {
     int n;
 };
 
-__global__ void __launch_bounds__(LEAF_THREADS) leaf_kernel(const __grid_constant__ LeafParams P) {
-    extern __shared__ float sm[];
-    const LeafJob &J = P.j[blockIdx.x];
-    const int n = J.n, ls = n + 1;
-    float *S = sm;              // n x (n+1)
-    float *u = S + n * ls;      // n
-    float *vd = u + n;          // n
+// In-place inverse of one SPD 128 x 128 block, one CTA of 512 threads, the
+// block in shared memory, blocked by 32-wide panels:
+//   A. Cholesky X = U^T U: per panel p, warp 0 factors the 32 x 32 diagonal
+//      block in registers (one column per lane, pivots and row broadcasts by
+//      warp shuffles), then the panel row is solved (U_pp^T U_pq = X_pq, one
+//      column per thread) and the trailing matrix gets the rank-32 update
+//      X_qr -= U_pq^T U_pr (all threads, register tiles);
+//   B. V = U^-1: four warps invert the four diagonal blocks with shuffles,
+//      then V_pq = -V_pp (sum_{p<r<=q} U_pr V_rq) one block diagonal at a time;
+//   C. X^-1 = V V^T, written back as a (hi, lo) pair.
+__global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_constant__ LeafParams P) {
+    constexpr int N = LEAF, LS = LEAF + 1, PW = 32;
+    extern __shared__ float smem_leaf[];
+    float *S = smem_leaf;            // N x LS: the block, U in its upper triangle
+    float *V = S + N * LS;           // N x LS: V = U^-1 (upper)
+    float *T = V + N * LS;           // 3 x PW x (PW+1): block temporaries
     __shared__ int bad;
-    const int tid = threadIdx.x, nt = blockDim.x;
+    __shared__ float rdiag[N];
+    const LeafJob &J = P.j[blockIdx.x];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned FULL = 0xffffffffu;
     if (tid == 0) bad = -1;
-    for (int e = tid; e < n * n; e += nt) {
-        const int i = e / n, j = e - i * n;
-        S[i * ls + j] = J.X[(long long)i * J.ld + j];
+    for (int e = tid; e < N * N; e += LEAF_THREADS) {
+        const int i = e >> 7, j = e & 127;
+        const long long o = (long long)i * J.ld + j;
+        S[i * LS + j] = J.Xh[o] + J.Xl[o];
     }
     __syncthreads();
-    // Cholesky, upper: S[k][j>=k] <- U[k][j]
-    for (int k = 0; k < n; ++k) {
-        const float d = S[k * ls + k];
-        const bool okp = d > 0.f && isfinite(d);
-        if (tid == 0 && !okp && bad < 0) bad = k;
-        const float piv = okp ? sqrtf(d) : 1.f;
-        const float rp = 1.0f / piv;
-        for (int j = k + tid; j < n; j += nt) u[j] = (j == k) ? piv : S[k * ls + j] * rp;
-        __syncthreads();
-        const int c = n - k - 1;
-        for (int e = tid; e < c * c; e += nt) {
-            const int i = k + 1 + e / c, j = k + 1 + e % c;
-            if (j >= i) S[i * ls + j] -= u[i] * u[j];
+
+    // ---------------------------------------------------------- A. Cholesky
+    for (int p = 0; p < N / PW; ++p) {
+        const int o = p * PW;
+        if (warp == 0) {
+            float d[PW];  // column `lane` of the diagonal block, rows 0..31 (upper part)
+#pragma unroll
+            for (int i = 0; i < PW; ++i) d[i] = (i <= lane) ? S[(o + i) * LS + o + lane] : 0.f;
+#pragma unroll
+            for (int k = 0; k < PW; ++k) {
+                const float piv = __shfl_sync(FULL, d[k], k);
+                const bool ok = piv > 0.f && isfinite(piv);
+                if (!ok && lane == 0 && bad < 0) bad = o + k;
+                const float rs = ok ? rsqrtf(piv) : 1.f;
+                // selects, not branches: per-lane predicates inside this
+                // unrolled loop would serialise the warp at every step
+                const float u = (lane >= k) ? d[k] * rs : 0.f;
+                d[k] = (lane >= k) ? u : d[k];
+#pragma unroll
+                for (int i = 0; i < PW; ++i) {  // fixed trip count keeps d[] in registers
+                    if (i > k) {
+                        const float uki = __shfl_sync(FULL, u, i);
+                        const float t = fmaf(-uki, u, d[i]);
+                        d[i] = (lane >= i) ? t : d[i];
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < PW; ++i) {
+                const float keep = S[(o + i) * LS + o + lane];
+                S[(o + i) * LS + o + lane] = (i <= lane) ? d[i] : keep;
+            }
+            rdiag[o + lane] = 1.0f / S[(o + lane) * LS + o + lane];  // 1 / U[i][i] for the panel solve
         }
-        for (int j = k + tid; j < n; j += nt) S[k * ls + j] = u[j];
+        __syncthreads();
+        const int c0 = o + PW, m = N - c0;  // trailing columns [c0, N)
+        if (m == 0) break;
+        // panel row: U_pp^T X = A_p,trail, one column per thread (forward
+        // substitution, column-oriented)
+        if (tid < m) {
+            const int j = c0 + tid;
+            float x[PW];
+#pragma unroll
+            for (int i = 0; i < PW; ++i) x[i] = S[(o + i) * LS + j];
+#pragma unroll
+            for (int i = 0; i < PW; ++i) {
+                x[i] *= rdiag[o + i];
+#pragma unroll
+                for (int l = i + 1; l < PW; ++l) x[l] = fmaf(-S[(o + i) * LS + o + l], x[i], x[l]);
+            }
+#pragma unroll
+            for (int i = 0; i < PW; ++i) S[(o + i) * LS + j] = x[i];
+        }
+        __syncthreads();
+        // rank-32 trailing update: rows c0 + ty + 16 r, columns c0 + tx + 32 c
+        {
+            const int ty = tid >> 5, tx = tid & 31;
+            const int nr = m / 16, nc = m / 32;  // 6x3, 4x2, 2x1 per thread
+            float acc[6][3];
+#pragma unroll
+            for (int r = 0; r < 6; ++r)
+#pragma unroll
+                for (int c = 0; c < 3; ++c) acc[r][c] = 0.f;
+            for (int l = 0; l < PW; ++l) {
+                const float *row = S + (o + l) * LS + c0;
+                float ai[6], bj[3];
+#pragma unroll
+                for (int r = 0; r < 6; ++r) ai[r] = (r < nr) ? row[ty + 16 * r] : 0.f;
+#pragma unroll
+                for (int c = 0; c < 3; ++c) bj[c] = (c < nc) ? row[tx + 32 * c] : 0.f;
+#pragma unroll
+                for (int r = 0; r < 6; ++r)
+#pragma unroll
+                    for (int c = 0; c < 3; ++c) acc[r][c] = fmaf(ai[r], bj[c], acc[r][c]);
+            }
+#pragma unroll
+            for (int r = 0; r < 6; ++r)
+#pragma unroll
+                for (int c = 0; c < 3; ++c)
+                    if (r < nr && c < nc) S[(c0 + ty + 16 * r) * LS + c0 + tx + 32 * c] -= acc[r][c];
+        }
         __syncthreads();
     }
-    // triangular inverse V = U^-1; V[i][j] (i<j) kept at S[j][i], diag in vd
-    for (int e = tid; e < n * n; e += nt) {
-        const int i = e / n, j = e - i * n;
-        if (j < i) S[i * ls + j] = 0.f;
+
+    // ---------------------------------------------------------- B. V = U^-1
+    if (warp < N / PW) {  // diagonal blocks, one warp each
+        const int o = warp * PW;
+        float u[PW], r[PW];
+#pragma unroll
+        for (int i = 0; i < PW; ++i) {
+            u[i] = (i <= lane) ? S[(o + i) * LS + o + lane] : 0.f;
+            r[i] = (i == lane) ? 1.f : 0.f;
+        }
+#pragma unroll
+        for (int k = PW - 1; k >= 0; --k) {
+            const float ukk = __shfl_sync(FULL, u[k], k);
+            const float v = r[k] / ukk;
+            r[k] = v;
+#pragma unroll
+            for (int i = 0; i < k; ++i) {
+                const float uik = __shfl_sync(FULL, u[i], k);
+                r[i] = fmaf(-uik, v, r[i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < PW; ++i) V[(o + i) * LS + o + lane] = (i <= lane) ? r[i] : 0.f;
     }
-    for (int i = tid; i < n; i += nt) vd[i] = 1.0f / S[i * ls + i];
     __syncthreads();
-    for (int k = n - 1; k >= 0; --k) {
-        const float r = vd[k];
-        for (int j = k + 1 + tid; j < n; j += nt) S[j * ls + k] *= r;
-        __syncthreads();
-        // R[i][j] -= U[i][k] V[k][j] for i < k <= j
-        const int w = n - k;
-        for (int e = tid; e < k * w; e += nt) {
-            const int j = k + e / k, i = e - (e / k) * k;
-            const float vkj = (j == k) ? r : S[j * ls + k];
-            S[j * ls + i] -= S[i * ls + k] * vkj;
+    // off-diagonal blocks V_pq, q = p + dd: T_pq = sum_{p<r<=q} U_pr V_rq, then
+    // V_pq = -V_pp T_pq.  Warp w takes rows w, w+16, ... of the nb*32 block
+    // rows on this diagonal, lane = column; independent accumulators per row.
+    for (int dd = 1; dd < N / PW; ++dd) {
+        const int nb = N / PW - dd, rows = nb * PW, per = rows / 16;  // 6, 4, 2 rows per warp
+        float t[6];
+#pragma unroll
+        for (int k = 0; k < 6; ++k) t[k] = 0.f;
+#pragma unroll
+        for (int k = 0; k < 6; ++k) {
+            if (k < per) {
+                const int gr = warp + 16 * k, b = gr / PW, i = gr % PW, p = b, q = b + dd;
+                float sum = 0.f;
+                for (int rr = p + 1; rr <= q; ++rr)
+#pragma unroll 8
+                    for (int l = 0; l < PW; ++l)
+                        sum = fmaf(S[(p * PW + i) * LS + rr * PW + l], V[(rr * PW + l) * LS + q * PW + lane], sum);
+                t[k] = sum;
+            }
         }
+#pragma unroll
+        for (int k = 0; k < 6; ++k)
+            if (k < per) {
+                const int gr = warp + 16 * k, b = gr / PW, i = gr % PW;
+                T[(b * PW + i) * (PW + 1) + lane] = t[k];
+            }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 6; ++k) {
+            if (k < per) {
+                const int gr = warp + 16 * k, b = gr / PW, i = gr % PW, p = b;
+                float sum = 0.f;
+#pragma unroll 8
+                for (int l = 0; l < PW; ++l)
+                    sum = fmaf(V[(p * PW + i) * LS + p * PW + l], T[(b * PW + l) * (PW + 1) + lane], sum);
+                t[k] = -sum;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 6; ++k)
+            if (k < per) {
+                const int gr = warp + 16 * k, b = gr / PW, i = gr % PW, p = b, q = b + dd;
+                V[(p * PW + i) * LS + q * PW + lane] = t[k];
+            }
         __syncthreads();
     }
-    // X = V V^T, X[i][j] = sum_{l >= max(i,j)} V[i][l] V[j][l]
-    for (int e = tid; e < n * n; e += nt) {
-        const int i = e / n, j = e - i * n;
-        if (j < i) continue;
-        float acc = 0.f;
-        for (int l = j; l < n; ++l) {
-            const float vil = (l == i) ? vd[i] : S[l * ls + i];
-            const float vjl = (l == j) ? vd[j] : S[l * ls + j];
-            acc = fmaf(vil, vjl, acc);
+    // lower blocks of V are zero
+    for (int e = tid; e < N * N; e += LEAF_THREADS) {
+        const int i = e >> 7, j = e & 127;
+        if ((i >> 5) > (j >> 5)) V[i * LS + j] = 0.f;
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------- C. V V^T
+    {
+        const int ty = tid >> 5, tx = tid & 31;
+        float x[8][4];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) x[r][c] = 0.f;
+        for (int l = 0; l < N; ++l) {
+            float vi[8], vj[4];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) vi[r] = V[(ty + 16 * r) * LS + l];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) vj[c] = V[(tx + 32 * c) * LS + l];
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                if (ty + 16 * r <= l) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) x[r][c] = fmaf(vi[r], vj[c], x[r][c]);
+                }
         }
-        J.X[(long long)i * J.ld + j] = acc;
-        J.X[(long long)j * J.ld + i] = acc;
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = ty + 16 * r, j = tx + 32 * c;
+                const long long o = (long long)i * J.ld + j;
+                const float h = tf32_hi(x[r][c]);
+                J.Xh[o] = h;
+                J.Xl[o] = x[r][c] - h;
+            }
     }
     if (tid == 0 && bad >= 0 && J.info) atomicCAS(J.info, 0, J.o + bad + 1);
 }
-
-size_t leaf_smem(int n) { return (size_t)(n * (n + 1) + 2 * n) * sizeof(float); }
 
 // ------------------------------------------------------------- scheduler
 
 struct Op {
     int leaf;
     LeafJob lj;
-    SgJob g;
+    TcJob g;
 };
 
-int split_of(int n) {
-    int h = (n / 2 + 31) / 32 * 32;
-    return std::min(h, n - 1);
-}
+// Working buffers of one matrix with d > LEAF.
+struct MatWork {
+    int d, dp;
+    float *Xh, *Xl, *Th, *Tl, *Uh, *Ul;
+    int mx, mt, mu;  // map indices (hi; lo at +1)
+};
 
-void gen_ops(std::vector<Op> &ops, float *X, long long ld, float *T, long long ldt, int o, int n,
-             int *info) {
-    if (n <= LEAF) {
+void gen_ops(std::vector<Op> &ops, const MatWork &w, int o, int n, int *info) {
+    const long long ld = w.dp;
+    if (n == LEAF) {
         Op op{};
         op.leaf = 1;
-        op.lj = LeafJob{X + (long long)o * ld + o, ld, n, o, info};
+        op.lj = LeafJob{w.Xh + o * ld + o, w.Xl + o * ld + o, ld, o, info};
         ops.push_back(op);
         return;
     }
-    const int h = split_of(n), m = n - h;
-    gen_ops(ops, X, ld, T, ldt, o, h, info);
-    float *X11 = X + (long long)o * ld + o;
-    float *X12 = X11 + h;
-    float *X21 = X11 + (long long)h * ld;
-    float *X22 = X21 + h;
-    float *Tn = T + (long long)o * ldt;
-    auto gemm = [&](const float *A, long long lda, int ta, const float *B, long long ldb, int tb,
-                    float *C, long long ldc, float *Ct, long long ldct, int M, int N, int K,
-                    float alpha, float beta) {
+    const int nb = n / LEAF, h = LEAF * (nb / 2), m = n - h;
+    gen_ops(ops, w, o, h, info);
+    auto gemm = [&](int ma, int ar, int ac, int mb, int br, int bc, int M, int N, int K, float alpha,
+                    float beta, float *Ch, float *Cl, float *Cth, float *Ctl) {
         Op op{};
         op.leaf = 0;
-        op.g = SgJob{A, lda, ta, B, ldb, tb, C, ldc, Ct, ldct, M, N, K, alpha, beta, 0};
+        TcJob &j = op.g;
+        j.map_a = ma; j.a_row0 = ar; j.a_col0 = ac;
+        j.map_b = mb; j.b_row0 = br; j.b_col0 = bc;
+        j.M = M; j.N = N; j.K = K;
+        j.epi = TC_EPI_SPLIT;
+        j.alpha = alpha; j.beta = beta;
+        j.C = Ch; j.C_lo = Cl; j.ldc = ld;
+        j.Ct = Cth; j.Ct_lo = Ctl; j.ldct = ld;
         ops.push_back(op);
     };
-    gemm(X11, ld, 0, X12, ld, 0, Tn, ldt, nullptr, 0, h, m, h, 1.f, 0.f);      // T = X11 X12
-    gemm(X12, ld, 1, Tn, ldt, 0, X22, ld, nullptr, 0, m, m, h, -1.f, 1.f);     // X22 -= X12^T T
-    gen_ops(ops, X, ld, T, ldt, o + h, m, info);                               // X22 <- X22^-1
-    gemm(Tn, ldt, 0, X22, ld, 0, X12, ld, X21, ld, h, m, m, -1.f, 0.f);        // X12 = -T X22
-    gemm(X12, ld, 0, Tn, ldt, 1, X11, ld, nullptr, 0, h, h, m, -1.f, 1.f);     // X11 -= X12 T^T
+    const long long x11 = o * ld + o, x12 = o * ld + o + h, x21 = (o + h) * ld + o, x22 = (o + h) * ld + o + h;
+    const long long tt = o * ld;  // T block: rows [o, o+h), columns [0, m)
+    // T = X11 X12 (B rows = X21 rows), U = T^T
+    gemm(w.mx, o, o, w.mx, o + h, o, h, m, h, 1.f, 0.f, w.Th + tt, w.Tl + tt, w.Uh, w.Ul);
+    // X22 -= X21 T  (B rows = U rows)
+    gemm(w.mx, o + h, o, w.mu, 0, 0, m, m, h, -1.f, 1.f, w.Xh + x22, w.Xl + x22, nullptr, nullptr);
+    gen_ops(ops, w, o + h, m, info);
+    // X12 = -T X22 (X22 symmetric: B rows = X22 rows), X21 = X12^T
+    gemm(w.mt, o, 0, w.mx, o + h, o + h, h, m, m, -1.f, 0.f, w.Xh + x12, w.Xl + x12, w.Xh + x21, w.Xl + x21);
+    // X11 -= X12 T^T (B rows = T rows)
+    gemm(w.mx, o, o + h, w.mt, o, 0, h, h, m, -1.f, 1.f, w.Xh + x11, w.Xl + x11, nullptr, nullptr);
 }
 
-kfac_status leaf_launch(const std::vector<LeafJob> &jobs, cudaStream_t st) {
-    static bool attr_done = false;
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(leaf_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)leaf_smem(LEAF)) != cudaSuccess)
-            return KFAC_ERR_CUDA;
-        attr_done = true;
+// Workspace layout shared by the size query and the run.
+struct InvPlan {
+    int *err = nullptr;
+    CUtensorMap *dev_maps = nullptr;
+    std::vector<CUtensorMap> maps;
+    std::vector<MatWork> work;
+    std::vector<std::vector<Op>> chains;
+    size_t longest = 0;
+    char *tc_ws = nullptr;
+    size_t tc_bytes = 0;
+};
+
+kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws, InvPlan &p, bool encode) {
+    p.err = ws.take<int>(64);
+    int nbig = 0;
+    for (int k = 0; k < nmats; ++k) nbig += mats[k].d > LEAF;
+    p.dev_maps = ws.take<CUtensorMap>(6 * (size_t)std::max(nbig, 1));
+    p.work.resize(nmats);
+    p.chains.assign(nmats, {});
+    for (int k = 0; k < nmats; ++k) {
+        MatWork &w = p.work[k];
+        w.d = mats[k].d;
+        w.dp = padded(w.d);
+        const size_t sq = (size_t)w.dp * w.dp;
+        w.Xh = ws.take<float>(sq);
+        w.Xl = ws.take<float>(sq);
+        w.Th = w.Tl = w.Uh = w.Ul = nullptr;
+        w.mx = w.mt = w.mu = -1;
+        if (w.d > LEAF) {
+            w.Th = ws.take<float>(sq);
+            w.Tl = ws.take<float>(sq);
+            w.Uh = ws.take<float>(sq);
+            w.Ul = ws.take<float>(sq);
+            float *bufs[6] = {w.Xh, w.Xl, w.Th, w.Tl, w.Uh, w.Ul};
+            const int base = (int)p.maps.size();
+            for (int q = 0; q < 6; ++q) {
+                p.maps.emplace_back();
+                if (encode && !tc_make_map(&p.maps.back(), TC_KIND_TF32X3, bufs[q], w.dp, w.dp, w.dp, 0))
+                    return KFAC_ERR_CUDA;
+            }
+            w.mx = base;
+            w.mt = base + 2;
+            w.mu = base + 4;
+        }
+        gen_ops(p.chains[k], w, 0, w.dp, info_dev ? info_dev + k : nullptr);
+        p.longest = std::max(p.longest, p.chains[k].size());
     }
+    // engine scratch: the largest round
+    size_t tcb = 0;
+    std::vector<TcJob> round;
+    for (size_t r = 0; r < p.longest; ++r) {
+        round.clear();
+        for (int k = 0; k < nmats; ++k)
+            if (r < p.chains[k].size() && !p.chains[k][r].leaf) round.push_back(p.chains[k][r].g);
+        tcb = std::max(tcb, tc_workspace_bytes(round.data(), (int)round.size(), TC_KIND_TF32X3));
+    }
+    p.tc_bytes = tcb;
+    p.tc_ws = ws.take<char>(tcb);
+    return KFAC_OK;
+}
+
+constexpr size_t LEAF_SMEM = (2 * (size_t)LEAF * (LEAF + 1) + 3 * 32 * 33) * sizeof(float);
+
+kfac_status leaf_launch(const std::vector<LeafJob> &jobs, cudaStream_t st) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(leaf_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LEAF_SMEM);
+    });
+    if (attr != cudaSuccess) return KFAC_ERR_CUDA;
     std::unique_ptr<LeafParams> P(new LeafParams);
     size_t pos = 0;
     while (pos < jobs.size()) {
-        int n = 0, nmax = 0;
-        while (pos < jobs.size() && n < MAT_MAX) {
-            P->j[n] = jobs[pos++];
-            nmax = std::max(nmax, P->j[n].n);
-            ++n;
-        }
+        int n = 0;
+        while (pos < jobs.size() && n < MAT_MAX) P->j[n++] = jobs[pos++];
         P->n = n;
-        leaf_kernel<<<n, LEAF_THREADS, leaf_smem(nmax), st>>>(*P);
+        leaf_kernel<<<n, LEAF_THREADS, LEAF_SMEM, st>>>(*P);
         KFAC_LAUNCH_CHECK();
     }
     return KFAC_OK;
 }
 
-kfac_status sym_launch(std::vector<SymMat> &mats, int in_place, const float *damp, cudaStream_t st) {
-    std::unique_ptr<SymParams> P(new SymParams);
+template <bool PREP>
+kfac_status tile_launch(std::vector<TileMat> &mats, const float *damp, cudaStream_t st) {
+    std::unique_ptr<TileParams> P(new TileParams);
     size_t pos = 0;
     while (pos < mats.size()) {
         int n = 0, tiles = 0;
         while (pos < mats.size() && n < MAT_MAX) {
-            SymMat m = mats[pos++];
-            m.tiles = (int)ceil_div(m.n, 32);
+            TileMat m = mats[pos++];
+            m.tiles = (int)ceil_div(PREP ? m.dp : m.d, 32);
             P->m[n] = m;
             P->begin[n] = tiles;
             tiles += m.tiles * m.tiles;
@@ -308,9 +577,9 @@ kfac_status sym_launch(std::vector<SymMat> &mats, int in_place, const float *dam
         }
         P->begin[n] = tiles;
         P->n = n;
-        P->in_place = in_place;
         P->damp = damp;
-        sym_kernel<<<tiles, 256, 0, st>>>(*P);
+        if (PREP) prep_kernel<<<tiles, 256, 0, st>>>(*P);
+        else finish_kernel<<<tiles, 256, 0, st>>>(*P);
         KFAC_LAUNCH_CHECK();
     }
     return KFAC_OK;
@@ -320,8 +589,8 @@ kfac_status sym_launch(std::vector<SymMat> &mats, int in_place, const float *dam
 
 size_t inv_workspace_bytes(const InvMatrix *mats, int nmats) {
     Arena a;
-    for (int k = 0; k < nmats; ++k)
-        if (mats[k].d > LEAF) a.take<float>((size_t)mats[k].d * mats[k].d);
+    InvPlan p;
+    if (plan_inv(mats, nmats, nullptr, a, p, false) != KFAC_OK) return 0;
     return a.used;
 }
 
@@ -352,44 +621,43 @@ kfac_status damping_run(const InvMatrix *mats, int nlayers, float gamma, int pi_
 
 kfac_status inv_run(const InvMatrix *mats, int nmats, const float *damp_dev, int *info_dev,
                     Arena &ws, cudaStream_t st) {
-    // 1. X = sym(F) + damp I
-    std::vector<SymMat> sm(nmats);
-    for (int k = 0; k < nmats; ++k)
-        sm[k] = SymMat{mats[k].F, mats[k].ldf, mats[k].out, mats[k].ldo, nullptr, 0, mats[k].d, 0, k};
-    kfac_status s = sym_launch(sm, 0, damp_dev, st);
+    InvPlan p;
+    kfac_status s = plan_inv(mats, nmats, info_dev, ws, p, true);
     if (s != KFAC_OK) return s;
-
-    // 2. per-matrix op chains
-    std::vector<std::vector<Op>> chains(nmats);
-    size_t longest = 0;
-    for (int k = 0; k < nmats; ++k) {
-        float *T = mats[k].d > LEAF ? ws.take<float>((size_t)mats[k].d * mats[k].d) : nullptr;
-        gen_ops(chains[k], mats[k].out, mats[k].ldo, T, mats[k].d, 0, mats[k].d,
-                info_dev ? info_dev + k : nullptr);
-        longest = std::max(longest, chains[k].size());
-    }
     if (!ws.fits()) return KFAC_ERR_WORKSPACE;
+    KFAC_CUDA_TRY(cudaMemsetAsync(p.err, 0, sizeof(int), st));
+    if (!p.maps.empty() && (s = tc_upload_maps(p.maps.data(), (int)p.maps.size(), p.dev_maps, st)) != KFAC_OK)
+        return s;
 
-    // 3. lock-step rounds: all leaves of a round in one launch, all GEMMs in one
+    // 1. X = split(sym(F) + damp I), identity padding
+    std::vector<TileMat> tm(nmats);
+    for (int k = 0; k < nmats; ++k)
+        tm[k] = TileMat{mats[k].F, mats[k].ldf, p.work[k].Xh, p.work[k].Xl, mats[k].d, p.work[k].dp,
+                        mats[k].out, mats[k].ldo, mats[k].out_bf16, mats[k].ldo_bf16, k, 0};
+    if ((s = tile_launch<true>(tm, damp_dev, st)) != KFAC_OK) return s;
+
+    // 2. lock-step rounds: the leaves of a round in one launch, its GEMMs in one
     std::vector<LeafJob> leaves;
-    std::vector<SgJob> gemms;
-    for (size_t r = 0; r < longest; ++r) {
+    std::vector<TcJob> gemms;
+    for (size_t r = 0; r < p.longest; ++r) {
         leaves.clear();
         gemms.clear();
         for (int k = 0; k < nmats; ++k) {
-            if (r >= chains[k].size()) continue;
-            const Op &op = chains[k][r];
+            if (r >= p.chains[k].size()) continue;
+            const Op &op = p.chains[k][r];
             if (op.leaf) leaves.push_back(op.lj); else gemms.push_back(op.g);
         }
         if (!leaves.empty() && (s = leaf_launch(leaves, st)) != KFAC_OK) return s;
-        if (!gemms.empty() && (s = sg_run(gemms.data(), (int)gemms.size(), st)) != KFAC_OK) return s;
+        if (!gemms.empty()) {
+            Arena tail(p.tc_ws, p.tc_bytes);
+            if ((s = tc_run(gemms.data(), (int)gemms.size(), TC_KIND_TF32X3, p.dev_maps, tail, p.err, st)) !=
+                KFAC_OK)
+                return s;
+        }
     }
 
-    // 4. exact symmetry + bf16 copies
-    for (int k = 0; k < nmats; ++k)
-        sm[k] = SymMat{mats[k].out, mats[k].ldo, mats[k].out, mats[k].ldo, mats[k].out_bf16,
-                       mats[k].ldo_bf16, mats[k].d, 0, -1};
-    return sym_launch(sm, 1, damp_dev, st);
+    // 3. out = hi + lo, mirrored; bf16 copies
+    return tile_launch<false>(tm, damp_dev, st);
 }
 
 }  // namespace kfac

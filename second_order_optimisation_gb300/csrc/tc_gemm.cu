@@ -1,23 +1,28 @@
 // tc_gemm.cu -- persistent tcgen05 (5th-generation tensor core) GEMM / SYRK
-// engine for sm_103a, bf16 operands, fp32 accumulation in TMEM.
+// engine for sm_103a with fp32 accumulation in TMEM.  Two operand kinds:
 //
-// Used for the Kronecker-factor statistic A = P^T P / G = Gam^T Gam
-// (Osawa et al., "Large-Scale Distributed Second-Order Optimization Using
-// Kronecker-Factored Approximate Curvature ...", section 3.2, Eq. 5), whose
-// operands are the same [rows x d] matrix read MN-major, and for the two
-// chained GEMMs of the preconditioned gradient G^-1 grad A^-1 (Eq. 7).
+//   KIND_BF16   bf16 operands, one kind::f16 MMA per K=16 slice.  Used for the
+//               Kronecker-factor statistic A = P^T P, G = Gam^T Gam (Osawa et
+//               al., "Large-Scale Distributed Second-Order Optimization Using
+//               Kronecker-Factored Approximate Curvature ...", section 3.2,
+//               Eq. 5; both operands the same [rows x d] matrix read MN-major)
+//               and for the two GEMMs of G^-1 grad A^-1 (Eq. 7).
+//   KIND_TF32X3 fp32 operands carried as (hi, lo) pairs with hi exactly
+//               representable in tf32; three kind::tf32 MMAs per K=8 slice
+//               (hi*hi + hi*lo + lo*hi) give close to fp32 accuracy.  Used for
+//               the Schur-complement updates of the damped inversion (Eq. 6).
 //
 // One launch runs a list of heterogeneous problems.  Each CTA (one per SM)
 // walks a static, strided list of work items (problem, 128x128 output tile,
 // K split).  Warp roles:
-//   warp 0      TMA producer: 128-byte-swizzled tiles into a 6-stage ring
-//   warp 1      TMEM owner + MMA issuer (one thread): tcgen05.mma 128x128x16
+//   warp 0      TMA producer: 128-byte-swizzled tiles into a shared ring
+//   warp 1      TMEM owner + MMA issuer (one thread)
 //   warps 2..5  epilogue: tcgen05.ld TMEM -> registers -> global, with a
 //               double-buffered accumulator so it overlaps the next tile
-// Split-K partial tiles are reduced by the last-arriving CTA of the tile in
-// split order (deterministic; no spin-waits).  The epilogue either
-// accumulates into an fp32 matrix (F <- beta F + alpha acc, optionally upper
-// triangle only) or stores fp32 and/or bf16.
+// Tensor maps live in the caller's workspace (written by a copy kernel at the
+// start of the call); problems refer to them by index and address operand
+// sub-blocks by coordinate offsets.  Split-K partial tiles are reduced by the
+// last-arriving CTA of the tile in split order (deterministic; no spin-waits).
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -29,28 +34,40 @@
 
 namespace kfac {
 
-constexpr int BM = 128, BN = 128, BK = 64, STAGES = 6;
-constexpr int TILE_A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int TILE_B_BYTES = BN * BK * 2;  // 16 KB
-constexpr int STAGE_BYTES = TILE_A_BYTES + TILE_B_BYTES;
-constexpr int MAX_MAPS = 112, MAX_PROBS = 112;
+namespace {
+
+constexpr int BM = 128, BN = 128;
+constexpr int TILE_BYTES = 128 * 128;  // one 128-row x 128-byte operand tile
 constexpr int NUM_THREADS = 192;
-constexpr int TMEM_COLS = 2 * BN;  // two accumulators
-constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int MAX_PROBS = 192;
+constexpr int MAPS_PER_COPY = 240;
+constexpr int STAGE_LD = 33;                              // epilogue staging row pitch (floats)
+constexpr size_t EPI_STAGE_BYTES = 4 * 32 * STAGE_LD * sizeof(float);
+constexpr size_t SMEM_BYTES = 192 * 1024 + 1024 /*align*/ + 256 /*barriers*/ + EPI_STAGE_BYTES;
+
+template <int KIND> struct Traits;
+template <> struct Traits<TC_KIND_BF16> {
+    static constexpr int BK = 64, STAGES = 6, TILES = 2, ESZ = 2;
+};
+template <> struct Traits<TC_KIND_TF32X3> {
+    static constexpr int BK = 32, STAGES = 3, TILES = 4, ESZ = 4;
+};
 
 struct TcProb {
-    int map_a, map_b;
-    int a_mn, b_mn;
-    int M, N;
-    int k_tiles;
-    int tiles_n;
-    int syrk;
-    int ksplit;
-    int work_begin;
-    int epi;
+    int map_a, map_b;        // map indices; tf32x3: hi at map, lo at map + 1
+    int a_mn, b_mn;          // MN-major operand (bf16 only)
+    int a_row0, a_col0;      // operand sub-block origin inside its map (rows, columns)
+    int b_row0, b_col0;
+    int M, N, k_tiles;
+    int tiles_n, syrk, ksplit, work_begin, epi;
     float alpha, beta;
     float *C;
+    float *C_lo;
     long long ldc;
+    float *Ct;
+    float *Ct_lo;
+    long long ldct;
     uint16_t *Cb;
     long long ldcb;
     float *partial;  // [tiles][ksplit][BM*BN] when ksplit > 1
@@ -58,13 +75,32 @@ struct TcProb {
 };
 
 struct TcParams {
-    CUtensorMap maps[MAX_MAPS];
+    const CUtensorMap *maps;  // device (workspace)
     TcProb prob[MAX_PROBS];
     int nprob;
     int total_work;
     int *error;
 };
 static_assert(sizeof(TcParams) <= 32000, "kernel parameter block too large");
+
+struct MapCopyParams {
+    CUtensorMap m[MAPS_PER_COPY];
+    CUtensorMap *dst;
+    int n;
+};
+
+__global__ void map_copy_kernel(const __grid_constant__ MapCopyParams P) {
+    // 8 threads per 128-byte map, 16 bytes each
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    const int m = t >> 3, part = t & 7;
+    if (m < P.n) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(&P.m[m]) + part;
+        uint4 *dst = reinterpret_cast<uint4 *>(P.dst + m) + part;
+        *dst = *src;
+    }
+    // make the generic-proxy writes visible to later tensor-map (async proxy) reads
+    asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
 
 struct Work {
     int p, tile, tm, tn, split, kt0, kt1;
@@ -96,70 +132,134 @@ __device__ __forceinline__ Work decode_work(const TcParams &P, int w) {
     return k;
 }
 
-// Operand tile of 128 (M or N) x 64 (K) bf16 into shared memory.
-//   MN-major source [K][MN]: two 64x64 boxes (MN 0-63 | 64-127), 8 KB apart.
-//   K-major source  [MN][K]: one 64(K) x 128(MN) box.
-__device__ __forceinline__ void load_operand(uint8_t *dst, const CUtensorMap *map, int mn, int mn0,
-                                             int k0, uint64_t *bar) {
-    if (mn) {
-        tma_load_2d(dst, map, mn0, k0, bar);
-        tma_load_2d(dst + 8192, map, mn0 + 64, k0, bar);
+__device__ __forceinline__ void acquire_map(const CUtensorMap *m) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"((uint64_t)m) : "memory");
+}
+
+// One 128 (M or N) x BK (K) operand tile into shared memory.
+//   K-major source  [MN][K]: one BK x 128 box (128-byte rows).
+//   MN-major source [K][MN] (bf16): two 64 x 64 boxes (MN 0-63 | 64-127), 8 KB apart.
+__device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, int mn_major, int row0,
+                                          int col0, int mn0, int k0, uint64_t *bar) {
+    if (mn_major) {
+        tma_load_2d(dst, map, col0 + mn0, row0 + k0, bar);
+        tma_load_2d(dst + 8192, map, col0 + mn0 + 64, row0 + k0, bar);
     } else {
-        tma_load_2d(dst, map, k0, mn0, bar);
+        tma_load_2d(dst, map, col0 + k0, row0 + mn0, bar);
     }
 }
 
-// Descriptor of the kk-th K=16 slice of a staged operand tile.
-__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn, int kk) {
-    // MN-major: 8-row K groups are 1024 B apart (SBO), the two 64-wide MN
-    //           blocks 8192 B apart (LBO); a K=16 slice is two K groups.
-    // K-major : rows 128 B, 8-row groups 1024 B apart (SBO); a K=16 slice is
-    //           32 B inside the swizzled row.
-    return mn ? smem_desc_sw128(base + kk * 2048, 8192, 1024)
-              : smem_desc_sw128(base + kk * 32, 16, 1024);
+// Descriptor of the kk-th 32-byte K slice of a staged operand tile.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, int kk) {
+    // MN-major (bf16): 8-row K groups 1024 B apart (SBO), the two 64-wide MN
+    //   blocks 8192 B apart (LBO); a K=16 slice spans two K groups.
+    // K-major: 128-byte rows, 8-row groups 1024 B apart (SBO); a slice is 32 B
+    //   inside the swizzled row (16 bf16 or 8 tf32).
+    return mn_major ? smem_desc_sw128(base + kk * 2048, 8192, 1024)
+                    : smem_desc_sw128(base + kk * 32, 16, 1024);
 }
 
-__device__ __forceinline__ void epi_store(const TcProb &q, int i, int j0, const float *v, int n) {
-    if (i >= q.M) return;
-    if (q.epi == TC_EPI_ACCUM) {
-        float *row = q.C + (long long)i * q.ldc;
-        const bool upper = q.syrk;
-        const float a = q.alpha, b = q.beta;
-        for (int t = 0; t < n; ++t) {
-            int j = j0 + t;
-            if (j < q.N && (!upper || j >= i)) {
-                float o = a * v[t];
-                if (b != 0.f) o = fmaf(b, row[j], o);
-                row[j] = o;
+__device__ __forceinline__ float tf32_hi(float v) {
+    return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+}
+
+// Epilogue of one 32 x 32 chunk by one warp.  On entry lane l holds row
+// i0 + l, columns j0 .. j0+31 (the TMEM layout).  The transposed copy (if any)
+// is written straight from that layout (coalesced: consecutive lanes are
+// consecutive addresses of Ct); the row-major output goes through a per-warp
+// shared-memory transpose so that each store instruction covers 32
+// consecutive columns of one row.  Old values (beta != 0) are loaded for all
+// 32 rows before any store.
+__device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, const float *v, float *stage,
+                                            int lane) {
+    const float a = q.alpha, b = q.beta;
+    if (q.epi == TC_EPI_SPLIT && q.Ct) {  // host guarantees beta == 0 here
+        const int i = i0 + lane;
+        if (i < q.M) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const int j = j0 + c;
+                if (j < q.N) {
+                    const float o = a * v[c], h = tf32_hi(o);
+                    q.Ct[(long long)j * q.ldct + i] = h;
+                    q.Ct_lo[(long long)j * q.ldct + i] = o - h;
+                }
             }
         }
-    } else {
-        for (int t = 0; t < n; ++t) {
-            int j = j0 + t;
-            if (j < q.N) {
-                float o = q.alpha * v[t];
+    }
+#pragma unroll
+    for (int c = 0; c < 32; ++c) stage[lane * STAGE_LD + c] = v[c];
+    __syncwarp();
+    const int j = j0 + lane;
+    const bool jok = j < q.N;
+    float acc[32], old[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) acc[r] = stage[r * STAGE_LD + lane];
+    __syncwarp();
+    if (q.epi == TC_EPI_ACCUM) {
+        const bool upper = q.syrk;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            const int i = i0 + r;
+            old[r] = (b != 0.f && jok && i < q.M && (!upper || j >= i)) ? q.C[(long long)i * q.ldc + j] : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            const int i = i0 + r;
+            if (jok && i < q.M && (!upper || j >= i)) q.C[(long long)i * q.ldc + j] = fmaf(b, old[r], a * acc[r]);
+        }
+    } else if (q.epi == TC_EPI_STORE) {
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            const int i = i0 + r;
+            if (jok && i < q.M) {
+                const float o = a * acc[r];
                 if (q.C) q.C[(long long)i * q.ldc + j] = o;
                 if (q.Cb) q.Cb[(long long)i * q.ldcb + j] = f32_to_bf16_bits(o);
             }
         }
+    } else {  // TC_EPI_SPLIT
+        float oldl[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            const int i = i0 + r;
+            const bool ok = b != 0.f && jok && i < q.M;
+            old[r] = ok ? q.C[(long long)i * q.ldc + j] : 0.f;
+            oldl[r] = ok ? q.C_lo[(long long)i * q.ldc + j] : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            const int i = i0 + r;
+            if (jok && i < q.M) {
+                const float o = fmaf(b, old[r] + oldl[r], a * acc[r]);
+                const float h = tf32_hi(o);
+                q.C[(long long)i * q.ldc + j] = h;
+                q.C_lo[(long long)i * q.ldc + j] = o - h;
+            }
+        }
     }
 }
 
+template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams P) {
+    using Tr = Traits<KIND>;
+    constexpr int STAGE_BYTES = Tr::TILES * TILE_BYTES;
+    constexpr int KSLICES = Tr::BK * Tr::ESZ / 32;  // 32-byte MMA K slices per stage (4)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t *full = (uint64_t *)(smem + STAGES * STAGE_BYTES);
-    uint64_t *empty = full + STAGES;
-    uint64_t *accf = empty + STAGES;
+    uint64_t *full = (uint64_t *)(smem + Tr::STAGES * STAGE_BYTES);
+    uint64_t *empty = full + Tr::STAGES;
+    uint64_t *accf = empty + Tr::STAGES;
     uint64_t *acce = accf + 2;
     uint32_t *tmem_slot = (uint32_t *)(acce + 2);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
     volatile int *last_flag = abort_flag + 1;
+    float *epi_stage = (float *)(smem + Tr::STAGES * STAGE_BYTES + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < Tr::STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -184,10 +284,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             for (int w = blockIdx.x; w < P.total_work && !*abort_flag; w += gridDim.x) {
                 Work k = decode_work(P, w);
                 const TcProb &q = P.prob[k.p];
-                const CUtensorMap *ma = &P.maps[q.map_a];
-                const CUtensorMap *mb = &P.maps[q.map_b];
-                const bool diag = q.syrk && k.tm == k.tn;
-                const uint32_t bytes = diag ? TILE_A_BYTES : STAGE_BYTES;
+                const CUtensorMap *ma = P.maps + q.map_a;
+                const CUtensorMap *mb = P.maps + q.map_b;
+                acquire_map(ma);
+                acquire_map(mb);
+                if (KIND == TC_KIND_TF32X3) {
+                    acquire_map(ma + 1);
+                    acquire_map(mb + 1);
+                }
+                const bool diag = KIND == TC_KIND_BF16 && q.syrk && k.tm == k.tn;
+                const uint32_t bytes = diag ? TILE_BYTES : STAGE_BYTES;
                 for (int kt = k.kt0; kt < k.kt1; ++kt) {
                     if (!mbar_wait(&empty[stage], phase ^ 1)) {
                         atomicOr(P.error, ERR_TIMEOUT_EMPTY);
@@ -196,9 +302,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     }
                     mbar_arrive_expect_tx(&full[stage], bytes);
                     uint8_t *sa = smem + stage * STAGE_BYTES;
-                    load_operand(sa, ma, q.a_mn, k.tm * BM, kt * BK, &full[stage]);
-                    if (!diag) load_operand(sa + TILE_A_BYTES, mb, q.b_mn, k.tn * BN, kt * BK, &full[stage]);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    const int k0 = kt * Tr::BK;
+                    if (KIND == TC_KIND_BF16) {
+                        load_tile(sa, ma, q.a_mn, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
+                        if (!diag)
+                            load_tile(sa + TILE_BYTES, mb, q.b_mn, q.b_row0, q.b_col0, k.tn * BN, k0,
+                                      &full[stage]);
+                    } else {
+                        load_tile(sa, ma, 0, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
+                        load_tile(sa + TILE_BYTES, ma + 1, 0, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
+                        load_tile(sa + 2 * TILE_BYTES, mb, 0, q.b_row0, q.b_col0, k.tn * BN, k0, &full[stage]);
+                        load_tile(sa + 3 * TILE_BYTES, mb + 1, 0, q.b_row0, q.b_col0, k.tn * BN, k0,
+                                  &full[stage]);
+                    }
+                    if (++stage == Tr::STAGES) { stage = 0; phase ^= 1; }
                 }
             }
         }
@@ -210,7 +327,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             for (int w = blockIdx.x; w < P.total_work && !*abort_flag; w += gridDim.x, ++it) {
                 Work k = decode_work(P, w);
                 const TcProb &q = P.prob[k.p];
-                const bool diag = q.syrk && k.tm == k.tn;
+                const bool diag = KIND == TC_KIND_BF16 && q.syrk && k.tm == k.tn;
                 const int b = it & 1;
                 const uint32_t use = (uint32_t)(it >> 1);
                 if (!mbar_wait(&acce[b], (use & 1) ^ 1)) {
@@ -220,7 +337,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + b * BN;
-                const uint32_t idesc = idesc_bf16_f32(BM, BN, q.a_mn, q.b_mn);
+                const uint32_t idesc = KIND == TC_KIND_BF16 ? idesc_bf16_f32(BM, BN, q.a_mn, q.b_mn)
+                                                            : idesc_tf32_f32(BM, BN);
                 bool ok = true;
                 for (int kt = k.kt0; kt < k.kt1; ++kt) {
                     if (!mbar_wait(&full[stage], phase)) {
@@ -230,16 +348,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(smem + stage * STAGE_BYTES);
-                    const uint32_t b_base = diag ? a_base : a_base + TILE_A_BYTES;
+                    const uint32_t s0 = smem_u32(smem + stage * STAGE_BYTES);
+                    if (KIND == TC_KIND_BF16) {
+                        const uint32_t b_base = diag ? s0 : s0 + TILE_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        tc_mma_f16(d_tmem, operand_desc(a_base, q.a_mn, kk),
-                                   operand_desc(b_base, q.b_mn, kk), idesc,
-                                   (kt > k.kt0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < KSLICES; ++kk)
+                            tc_mma_f16(d_tmem, operand_desc(s0, q.a_mn, kk), operand_desc(b_base, q.b_mn, kk),
+                                       idesc, (kt > k.kt0 || kk > 0) ? 1u : 0u);
+                    } else {
+                        const uint32_t ah = s0, al = s0 + TILE_BYTES, bh = s0 + 2 * TILE_BYTES,
+                                       bl = s0 + 3 * TILE_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < KSLICES; ++kk) {
+                            const uint64_t dah = operand_desc(ah, 0, kk), dbh = operand_desc(bh, 0, kk);
+                            tc_mma_tf32(d_tmem, dah, dbh, idesc, (kt > k.kt0 || kk > 0) ? 1u : 0u);
+                            tc_mma_tf32(d_tmem, dah, operand_desc(bl, 0, kk), idesc, 1u);
+                            tc_mma_tf32(d_tmem, operand_desc(al, 0, kk), dbh, idesc, 1u);
+                        }
                     }
                     tc_commit(&empty[stage]);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    if (++stage == Tr::STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
                 tc_commit(&accf[b]);
@@ -250,6 +378,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const int etid = threadIdx.x - 64;  // 0..127
+        float *stage = epi_stage + (warp - 2) * 32 * STAGE_LD;
         int it = 0;
         for (int w = blockIdx.x; w < P.total_work && !*abort_flag; w += gridDim.x, ++it) {
             Work k = decode_work(P, w);
@@ -263,13 +392,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             }
             tc_fence_after();
             const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + b * BN;
-            const int i = k.tm * BM + row;
+            const int i0 = k.tm * BM + quarter * 32;
             if (q.ksplit == 1) {
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
                     tmem_ld_32x32b_x32(t_row + c * 32, v);
-                    epi_store(q, i, k.tn * BN + c * 32, v, 32);
+                    chunk_store(q, i0, k.tn * BN + c * 32, v, stage, lane);
                 }
                 tc_fence_before();
                 mbar_arrive(&acce[b]);
@@ -298,14 +427,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     __threadfence();
                     const float4 *base = (const float4 *)(q.partial + (long long)k.tile * q.ksplit * (BM * BN));
 #pragma unroll 1
-                    for (int c4 = 0; c4 < BN / 4; ++c4) {
-                        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int c = 0; c < BN / 32; ++c) {
+                        float v[32];
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) v[t] = 0.f;
                         for (int sp = 0; sp < q.ksplit; ++sp) {
-                            float4 t = __ldcg(base + (long long)sp * (BM * BN / 4) + c4 * BM + row);
-                            s.x += t.x; s.y += t.y; s.z += t.z; s.w += t.w;
+                            const float4 *src = base + (long long)sp * (BM * BN / 4) + (c * 8) * BM + row;
+#pragma unroll
+                            for (int f = 0; f < 8; ++f) {
+                                const float4 t = __ldcg(src + f * BM);
+                                v[4 * f] += t.x; v[4 * f + 1] += t.y; v[4 * f + 2] += t.z; v[4 * f + 3] += t.w;
+                            }
                         }
-                        float v[4] = {s.x, s.y, s.z, s.w};
-                        epi_store(q, i, k.tn * BN + c4 * 4, v, 4);
+                        chunk_store(q, i0, k.tn * BN + c * 32, v, stage, lane);
                     }
                     if (etid == 0) q.counters[k.tile] = 0;
                 }
@@ -322,8 +456,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 
 // ------------------------------------------------------------------ host
 
-namespace {
-
 struct Plan {
     std::vector<int> order;    // job indices in launch order
     std::vector<int> ksplit;   // per job
@@ -331,12 +463,14 @@ struct Plan {
     std::vector<int> k_tiles;  // per job
 };
 
+int bk_of(int kind) { return kind == TC_KIND_BF16 ? Traits<TC_KIND_BF16>::BK : Traits<TC_KIND_TF32X3>::BK; }
+
 int tiles_of(const TcJob &j) {
     int tm = (int)ceil_div(j.M, BM), tn = (int)ceil_div(j.N, BN);
     return j.syrk ? tn * (tn + 1) / 2 : tm * tn;
 }
 
-Plan make_plan(const TcJob *jobs, int n) {
+Plan make_plan(const TcJob *jobs, int n, int kind) {
     Plan p;
     p.ksplit.resize(n);
     p.tiles.resize(n);
@@ -344,15 +478,16 @@ Plan make_plan(const TcJob *jobs, int n) {
     double total = 0.0;
     for (int i = 0; i < n; ++i) {
         p.tiles[i] = tiles_of(jobs[i]);
-        p.k_tiles[i] = (int)ceil_div(jobs[i].K, BK);
+        p.k_tiles[i] = (int)ceil_div(jobs[i].K, bk_of(kind));
         total += (double)p.tiles[i] * p.k_tiles[i];
     }
     const int sms = device_sm_count();
-    // aim for ~4 work items per SM, at least 8 K tiles (512 rows) per item
-    double target = std::max(8.0, total / (sms * 4.0));
+    // aim for ~4 work items per SM, at least 8 K tiles per item
+    const double target = std::max(8.0, total / (sms * 4.0));
     for (int i = 0; i < n; ++i) {
         int ks = (int)std::ceil(p.k_tiles[i] / target);
         ks = std::max(1, std::min(ks, std::min(p.k_tiles[i], 256)));
+        if (jobs[i].no_split) ks = 1;
         p.ksplit[i] = ks;
     }
     p.order.resize(n);
@@ -365,93 +500,109 @@ Plan make_plan(const TcJob *jobs, int n) {
     return p;
 }
 
-void take_buffers(const Plan &p, const TcJob *jobs, int n, Arena &ws, std::vector<float *> &part,
-                  std::vector<int *> &cnt, int **cnt_base, size_t *cnt_count) {
-    part.assign(n, nullptr);
-    cnt.assign(n, nullptr);
+struct Buffers {
+    std::vector<float *> part;
+    std::vector<int *> cnt;
+    int *cnt_base = nullptr;
     size_t ncnt = 0;
+};
+
+void take_buffers(const Plan &p, int n, Arena &ws, Buffers &b) {
+    b.part.assign(n, nullptr);
+    b.cnt.assign(n, nullptr);
+    b.ncnt = 0;
     for (int i = 0; i < n; ++i)
-        if (p.ksplit[i] > 1) ncnt += p.tiles[i];
-    int *cb = ws.take<int>(std::max<size_t>(ncnt, 1));
+        if (p.ksplit[i] > 1) b.ncnt += p.tiles[i];
+    b.cnt_base = ws.take<int>(std::max<size_t>(b.ncnt, 1));
     size_t off = 0;
     for (int i = 0; i < n; ++i) {
         if (p.ksplit[i] > 1) {
-            part[i] = ws.take<float>((size_t)p.tiles[i] * p.ksplit[i] * BM * BN);
-            cnt[i] = cb ? cb + off : nullptr;
+            b.part[i] = ws.take<float>((size_t)p.tiles[i] * p.ksplit[i] * BM * BN);
+            b.cnt[i] = b.cnt_base ? b.cnt_base + off : nullptr;
             off += p.tiles[i];
         }
     }
-    *cnt_base = cb;
-    *cnt_count = ncnt;
-    (void)jobs;
 }
 
-bool make_map(CUtensorMap *m, const uint16_t *ptr, long long ld, int rows, int cols, int mn) {
-    EncodeTiledFn enc = encode_tiled_fn();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    cuuint32_t box[2] = {64u, mn ? 64u : 128u};
-    cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)ptr, dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+template <int KIND>
+cudaError_t set_smem_attr() {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(tc_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)SMEM_BYTES);
+    });
+    return err;
 }
 
 }  // namespace
 
-size_t tc_workspace_bytes(const TcJob *jobs, int njobs) {
+bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int mn_major) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return false;
+    const int esz = kind == TC_KIND_BF16 ? 2 : 4;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * esz};
+    const cuuint32_t inner = 128u / esz;  // 128-byte rows
+    cuuint32_t box[2] = {inner, mn_major ? 64u : 128u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(m, kind == TC_KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                     2, (void *)ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+kfac_status tc_upload_maps(const CUtensorMap *maps, int n, CUtensorMap *dev, cudaStream_t st) {
+    std::unique_ptr<MapCopyParams> P(new MapCopyParams);
+    for (int base = 0; base < n; base += MAPS_PER_COPY) {
+        const int cnt = std::min(MAPS_PER_COPY, n - base);
+        std::memcpy(P->m, maps + base, sizeof(CUtensorMap) * cnt);
+        P->dst = dev + base;
+        P->n = cnt;
+        map_copy_kernel<<<(int)ceil_div(cnt * 8, 256), 256, 0, st>>>(*P);
+        KFAC_LAUNCH_CHECK();
+    }
+    return KFAC_OK;
+}
+
+size_t tc_workspace_bytes(const TcJob *jobs, int njobs, int kind) {
     if (njobs <= 0) return 0;
-    Plan p = make_plan(jobs, njobs);
+    Plan p = make_plan(jobs, njobs, kind);
     Arena a;
-    std::vector<float *> part;
-    std::vector<int *> cnt;
-    int *cb;
-    size_t nc;
-    take_buffers(p, jobs, njobs, a, part, cnt, &cb, &nc);
+    Buffers b;
+    take_buffers(p, njobs, a, b);
     return a.used;
 }
 
-kfac_status tc_run(const TcJob *jobs, int njobs, Arena &ws, int *err, cudaStream_t st) {
+kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *dev_maps, Arena &ws,
+                   int *err, cudaStream_t st) {
     if (njobs <= 0) return KFAC_OK;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)SMEM_BYTES);
-    });
-    if (attr_err != cudaSuccess) return KFAC_ERR_CUDA;
-
-    Plan p = make_plan(jobs, njobs);
-    std::vector<float *> part;
-    std::vector<int *> cnt;
-    int *cnt_base;
-    size_t ncnt;
-    take_buffers(p, jobs, njobs, ws, part, cnt, &cnt_base, &ncnt);
+    if ((kind == TC_KIND_BF16 ? set_smem_attr<TC_KIND_BF16>() : set_smem_attr<TC_KIND_TF32X3>()) != cudaSuccess)
+        return KFAC_ERR_CUDA;
+    Plan p = make_plan(jobs, njobs, kind);
+    Buffers bufs;
+    take_buffers(p, njobs, ws, bufs);
     if (!ws.fits()) return KFAC_ERR_WORKSPACE;
-    if (ncnt) KFAC_CUDA_TRY(cudaMemsetAsync(cnt_base, 0, ncnt * sizeof(int), st));
+    if (bufs.ncnt) KFAC_CUDA_TRY(cudaMemsetAsync(bufs.cnt_base, 0, bufs.ncnt * sizeof(int), st));
 
     const int sms = device_sm_count();
     std::unique_ptr<TcParams> P(new TcParams);
     size_t pos = 0;
     while (pos < p.order.size()) {
-        std::memset(P.get(), 0, sizeof(TcParams));
-        int nmaps = 0, nprob = 0, work = 0;
-        while (pos < p.order.size() && nprob < MAX_PROBS && nmaps + 2 <= MAX_MAPS) {
+        int nprob = 0, work = 0;
+        while (pos < p.order.size() && nprob < MAX_PROBS) {
             const int ji = p.order[pos];
             const TcJob &j = jobs[ji];
             TcProb &q = P->prob[nprob];
-            q.map_a = nmaps;
-            if (!make_map(&P->maps[nmaps++], j.a, j.lda, j.a_rows, j.a_cols, j.a_mn)) return KFAC_ERR_CUDA;
-            if (j.syrk) {
-                q.map_b = q.map_a;
-            } else {
-                q.map_b = nmaps;
-                if (!make_map(&P->maps[nmaps++], j.b, j.ldb, j.b_rows, j.b_cols, j.b_mn)) return KFAC_ERR_CUDA;
-            }
+            std::memset(&q, 0, sizeof(q));
+            q.map_a = j.map_a;
+            q.map_b = j.syrk ? j.map_a : j.map_b;
             q.a_mn = j.a_mn;
             q.b_mn = j.syrk ? j.a_mn : j.b_mn;
+            q.a_row0 = j.a_row0; q.a_col0 = j.a_col0;
+            q.b_row0 = j.syrk ? j.a_row0 : j.b_row0;
+            q.b_col0 = j.syrk ? j.a_col0 : j.b_col0;
             q.M = j.M;
             q.N = j.N;
             q.k_tiles = p.k_tiles[ji];
@@ -462,21 +613,24 @@ kfac_status tc_run(const TcJob *jobs, int njobs, Arena &ws, int *err, cudaStream
             q.epi = j.epi;
             q.alpha = j.alpha;
             q.beta = j.beta;
-            q.C = j.C;
-            q.ldc = j.ldc;
-            q.Cb = j.Cb;
-            q.ldcb = j.ldcb;
-            q.partial = part[ji];
-            q.counters = cnt[ji];
+            q.C = j.C; q.C_lo = j.C_lo; q.ldc = j.ldc;
+            q.Ct = j.Ct; q.Ct_lo = j.Ct_lo; q.ldct = j.ldct;
+            q.Cb = j.Cb; q.ldcb = j.ldcb;
+            q.partial = bufs.part[ji];
+            q.counters = bufs.cnt[ji];
             work += p.tiles[ji] * p.ksplit[ji];
             ++nprob;
             ++pos;
         }
+        P->maps = dev_maps;
         P->nprob = nprob;
         P->total_work = work;
         P->error = err;
-        int grid = std::min(work, sms);
-        tc_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(*P);
+        const int grid = std::min(work, sms);
+        if (kind == TC_KIND_BF16)
+            tc_gemm_kernel<TC_KIND_BF16><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(*P);
+        else
+            tc_gemm_kernel<TC_KIND_TF32X3><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(*P);
         KFAC_LAUNCH_CHECK();
     }
     return KFAC_OK;

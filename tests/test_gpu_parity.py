@@ -147,6 +147,38 @@ def test_factor_many_layers_one_call():
         assert rel(np.triu(f64(s_.F)), np.triu(r)) <= 2e-2
 
 
+def test_factor_repeated_batched_calls_and_workspace_bounds():
+    """The same heterogeneous batch (im2col and direct sources) three times in
+    a row with beta = 0 gives the same, correct statistics each time, and
+    nothing is written past the workspace size the library asks for."""
+    layers = [workloads.Layer("c7", 3, 16, 7, 2, 3, 18, 9), workloads.Layer("c3", 64, 72, 3, 1, 1, 6, 6),
+              workloads.Layer("c1", 136, 64, 1, 1, 0, 5, 5)]
+    srcs, refs = [], []
+    for L in layers:
+        x, g, _ = workloads.layer_inputs(L, 4, "repeat", grad_w=False)
+        M = L.rows(4)
+        srcs.append(kfac.FactorSource(x.to(DEV), torch.zeros(L.d_a, L.d_a, device=DEV), L.k, L.k,
+                                      (L.stride,) * 2, (L.pad,) * 2, alpha=1.0 / M))
+        srcs.append(kfac.FactorSource(g.to(DEV), torch.zeros(L.d_g, L.d_g, device=DEV), alpha=1.0 / M))
+        P = oracle.im2col(x.float().numpy(), L.k, L.k, (L.stride,) * 2, (L.pad,) * 2)
+        refs += [oracle.gram(P) / M, oracle.gram(g.float().numpy()) / M]
+    need = kfac.kfac_factor_update_workspace_size(srcs)
+    ws = torch.full((need + 4096,), 0xAB, dtype=torch.uint8, device=DEV)
+    first = None
+    for call in range(3):
+        kfac.kfac_factor_update(srcs, ws[:need])
+        torch.cuda.synchronize()
+        got = [np.triu(f64(s_.F)) for s_ in srcs]
+        for gt, r in zip(got, refs):
+            assert np.all(np.isfinite(gt)) and rel(gt, np.triu(r)) <= 2e-2
+        if first is None:
+            first = got
+        else:
+            for a_, b_ in zip(got, first):
+                assert np.array_equal(a_, b_)        # deterministic across calls
+    assert int((ws[need:] != 0xAB).sum().item()) == 0
+
+
 def test_factor_chunked_accumulation():
     """Statistic accumulated over 4 chunks (beta = xi, then 1) equals the
     single statistic of all rows (gradient accumulation, section 2)."""
@@ -170,7 +202,7 @@ def _spd_factor(d, tag, M=None, xi=0.0):
 
 
 @pytest.mark.parametrize("dA,dG", [(1, 1), (5, 3), (64, 128), (129, 127), (200, 64), (300, 257),
-                                   (700, 130)])
+                                   (700, 130), (2049, 1000)])
 def test_damp_invert(dA, dG):
     A = _spd_factor(dA, f"A{dA}").astype(np.float32)
     G = (_spd_factor(dG, f"G{dG}") * 1e-4).astype(np.float32)
