@@ -28,7 +28,8 @@ KFAC_BF16, KFAC_F32 = 0, 1
 
 EXPORTS = ("kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_factor_update_workspace_size",
            "kfac_factor_update", "kfac_damp_invert_workspace_size", "kfac_damp_invert",
-           "kfac_precondition_workspace_size", "kfac_precondition", "kfac_bn_diag_fisher")
+           "kfac_precondition_workspace_size", "kfac_precondition", "kfac_bn_diag_fisher",
+           "kfac_noalloc_scratch_bytes", "kfac_precondition_noalloc")
 
 
 class KfacError(RuntimeError):
@@ -100,7 +101,10 @@ def load() -> ctypes.CDLL:
         lib.kfac_precondition_workspace_size.restype = sz
         lib.kfac_precondition.argtypes = [vp, i32, i32, vp, sz, vp]
         lib.kfac_bn_diag_fisher.argtypes = [vp, i32, i32, f32, f32, vp]
-        for f in ("kfac_factor_update", "kfac_damp_invert", "kfac_precondition", "kfac_bn_diag_fisher"):
+        lib.kfac_noalloc_scratch_bytes.restype = sz
+        lib.kfac_precondition_noalloc.argtypes = [vp, i32, i32, vp]
+        for f in ("kfac_factor_update", "kfac_damp_invert", "kfac_precondition", "kfac_bn_diag_fisher",
+                  "kfac_precondition_noalloc"):
             getattr(lib, f).restype = i32
         _lib = lib
     return _lib
@@ -298,6 +302,15 @@ def kfac_precondition(items: Sequence[PrecondItem], workspace: Optional[torch.Te
     _check(lib.kfac_precondition(arr, len(items), dt, ws.data_ptr(), ws.numel() * ws.element_size(),
                                  _stream(stream)), "kfac_precondition")
     return ws
+
+
+def kfac_precondition_noalloc(items: Sequence[PrecondItem], stream=None) -> None:
+    """kfac_precondition with the library's fixed device scratch instead of a
+    workspace: for callers that cannot allocate device memory (see kfac.h)."""
+    lib = load()
+    arr = _precond_descs(items)
+    _check(lib.kfac_precondition_noalloc(arr, len(items), _precond_dtype(items), _stream(stream)),
+           "kfac_precondition_noalloc")
 
 
 # ------------------------------------------------------------ BN diagonal Fisher
