@@ -57,6 +57,62 @@ def flops(layers, batch):
     return dict(syrk=syrk, inv=inv, precond=pc, total=syrk + inv + pc)
 
 
+def schur_gemm_flops(d, leaf=128):
+    """Useful fp32 flops of the tensor-core Schur-complement GEMMs that invert
+    one d x d factor (padded to a multiple of 128, split on 128-row block
+    boundaries; the two symmetric updates count half)."""
+    def rec(n):
+        if n <= leaf:
+            return 0
+        nb = n // leaf
+        h = leaf * (nb // 2)
+        m = n - h
+        return rec(h) + rec(m) + 2 * h * m * h + m * m * h + 2 * h * m * m + h * h * m
+    dp = -(-d // leaf) * leaf
+    return rec(dp)
+
+
+def leaf_count(d, leaf=128):
+    return -(-d // leaf)
+
+
+def kernel_rooflines(kern, layers, batch, fl, pk, steps):
+    """Per-kernel achieved rate vs its roofline from the per-phase event
+    totals.  Algorithmic work per step:
+      tc_gemm_bf16 (factors)  SYRK M*d(d+1) per factor            (tensor, bf16 peak)
+      tc_gemm_bf16 (precond)  2 dG^2 dA + 2 dG dA^2 per layer      (tensor, bf16 peak)
+      tc_gemm_tf32x3          Schur GEMM flops (schur_gemm_flops)  (tensor, tf32 peak / 3 products)
+      inv_leaf                128^3 per 128-block leaf             (fp32 ALU)
+      im2col                  bytes of the patch matrices written + inputs read (HBM)"""
+    tf32x3_peak = pk["bf16"] * (1.1 / 2.25) / 3.0
+    schur = sum(schur_gemm_flops(L.d_a) + schur_gemm_flops(L.d_g) for L in layers)
+    leaves = sum(leaf_count(L.d_a) + leaf_count(L.d_g) for L in layers)
+    im2col_bytes = 0
+    for L in layers:
+        if L.k > 1 or L.stride > 1:
+            im2col_bytes += L.rows(batch) * L.k * L.k * L.cin * 2 + batch * L.hin * L.hin * L.cin * 2
+    work = {("factors", "tc_gemm_bf16"): (fl["syrk"], "tensor", pk["bf16"], "TFLOP/s"),
+            ("precond", "tc_gemm_bf16"): (fl["precond"], "tensor", pk["bf16"], "TFLOP/s"),
+            ("inverse", "tc_gemm_tf32x3"): (schur, "tensor", tf32x3_peak, "TFLOP/s"),
+            ("inverse", "inv_leaf"): (leaves * 128 ** 3, "alu", FP32_ALU_PEAK_TFLOPS, "TFLOP/s"),
+            ("factors", "im2col"): (im2col_bytes, "hbm", pk["hbm"], "GB/s")}
+    out = {}
+    for ph, ks in kern.items():
+        for name, (t, n) in ks.items():
+            key = f"{name}@{ph}"
+            ms_step = t / steps
+            rec = {"ms_per_step": ms_step, "launches_per_step": n / steps,
+                   "avg_launch_us": 1e3 * t / max(n, 1)}
+            if (ph, name) in work:
+                w, bound, peak, unit = work[(ph, name)]
+                scale = 1e12 if unit == "TFLOP/s" else 1e9
+                ach = w / (ms_step * 1e-3) / scale
+                rec.update({"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
+                            "traffic": None})
+            out[key] = rec
+    return out
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -222,6 +278,7 @@ def run_reference(args, world, rank):
 
 
 def run_ours(args, world, rank, local):
+    import numpy as np
     import torch
 
     import __graft_entry__
@@ -237,7 +294,9 @@ def run_ours(args, world, rank, local):
     pk = peaks()
 
     # seeded synthetic inputs, pinned on the host and resident on the device
-    hx, hg, hgr, dx, dg, dgr = [], [], [], [], [], []
+    # all inputs of a step packed in ONE pinned host buffer and ONE device
+    # buffer (256-byte aligned slots), so the end-to-end copy is a single H2D
+    host_t, slots, off = [], [], 0
     for L in layers:
         x, g, grad = W.layer_inputs(L, batch, "bench")
         if L.hin == 1:
@@ -245,11 +304,25 @@ def run_ours(args, world, rank, local):
         ld = (L.d_a + 7) // 8 * 8
         gp = torch.zeros(L.d_g, ld, dtype=torch.bfloat16)
         gp[:, :L.d_a] = grad
-        for h, d, t in ((hx, dx, x), (hg, dg, g), (hgr, dgr, gp)):
-            h.append(t.contiguous().pin_memory())
-            d.append(h[-1].to(dev, non_blocking=True))
+        for t in (x, g, gp):
+            t = t.contiguous()
+            host_t.append(t)
+            slots.append((off, t.shape))
+            off += (t.numel() * 2 + 255) // 256 * 256
+    in_bytes = off
+    hbuf = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+    hv, dv = [], []
+    for t, (o, shp) in zip(host_t, slots):
+        n = t.numel() * 2
+        h = hbuf[o:o + n].view(torch.bfloat16).view(shp)
+        h.copy_(t)
+        hv.append(h)
+        dv.append(dbuf[o:o + n].view(torch.bfloat16).view(shp))
+    del host_t
+    dbuf.copy_(hbuf, non_blocking=True)
+    dx, dg, dgr = dv[0::3], dv[1::3], dv[2::3]
     dgr_v = [t[:, :L.d_a] for t, L in zip(dgr, layers)]
-    in_bytes = sum(t.numel() * t.element_size() for t in hx + hg + hgr)
     step = KfacStep(layers, batch, device=dev)
     torch.cuda.synchronize()
 
@@ -272,17 +345,32 @@ def run_ours(args, world, rank, local):
     launches_per_step = kfac.launch_count() - n0
     assert int(step.info.abs().sum().item()) == 0, "an inversion reported a non-positive pivot"
 
-    # per-phase device times (eager), on the launching stream
+    # per-phase device times (eager), on the launching stream, and every
+    # library kernel timed with CUDA events by the library's timing hooks
     stream = torch.cuda.current_stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    kern = {"factors": {}, "inverse": {}, "precond": {}}
+
+    def add(ph):
+        for name, (t, n) in kfac.timing_read().items():
+            a = kern[ph].setdefault(name, [0.0, 0])
+            a[0] += t
+            a[1] += n
+
+    kfac.timing_enable(True)
+    kfac.timing_read()
     for k in range(args.steps):
         ev[k][0].record(stream)
         step.factor_update(dx, dg)
         ev[k][1].record(stream)
+        add("factors")
         step.damp_invert()
         ev[k][2].record(stream)
+        add("inverse")
         step.precondition(dgr_v)
         ev[k][3].record(stream)
+        add("precond")
+    kfac.timing_enable(False)
     torch.cuda.synchronize()
     ph = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ev)
           for i, n in enumerate(("factors", "inverse", "precond"))}
@@ -318,42 +406,74 @@ def run_ours(args, world, rank, local):
     clk = clocks.stop()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
 
-    # end to end through the C ABI with host buffers
-    hout = [torch.empty(s.out.shape, dtype=torch.float32).pin_memory() for s in step.state]
-    out_bytes = sum(t.numel() * 4 for t in hout)
+    # end to end through the C ABI with host buffers: every step copies its
+    # inputs (one pinned H2D of the packed buffer) and reads back every
+    # preconditioned gradient (one D2H); copies run on a second stream, double
+    # buffered, so step k's copies overlap the compute of its neighbours
+    out_sizes = [s.out.numel() for s in step.state]
+    out_dev = [torch.empty(sum(out_sizes), device=dev) for _ in range(2)]
+    out_host = torch.empty(sum(out_sizes)).pin_memory()
+    out_views = []
+    for od in out_dev:
+        vs, o = [], 0
+        for s_, n in zip(step.state, out_sizes):
+            vs.append(od[o:o + n].view(s_.out.shape))
+            o += n
+        out_views.append(vs)
+    dbufs = [dbuf, torch.empty_like(dbuf)]
+    in_views = []
+    for db in dbufs:
+        vv = [db[o:o + int(np.prod(shp)) * 2].view(torch.bfloat16).view(shp) for (o, shp) in slots]
+        in_views.append((vv[0::3], vv[1::3], [t[:, :L.d_a] for t, L in zip(vv[2::3], layers)]))
+    out_bytes = out_dev[0].numel() * 4
+    copy = torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     f0.record(stream)
-    for _ in range(args.steps):
-        for h, d in zip(hx + hg + hgr, dx + dg + dgr):
-            d.copy_(h, non_blocking=True)
-        step.run(dx, dg, dgr_v)
-        for h, s in zip(hout, step.state):
-            h.copy_(s.out, non_blocking=True)
+    copy.wait_stream(stream)
+    with torch.cuda.stream(copy):
+        dbufs[0].copy_(hbuf, non_blocking=True)
+        ev_in[0].record(copy)
+    for k in range(args.steps):
+        b = k % 2
+        if k + 1 < args.steps:
+            with torch.cuda.stream(copy):
+                if k >= 1:
+                    copy.wait_event(ev_done[1 - b])     # step k-1 no longer reads that buffer
+                dbufs[1 - b].copy_(hbuf, non_blocking=True)
+                ev_in[1 - b].record(copy)
+        stream.wait_event(ev_in[b])
+        if k >= 2:
+            stream.wait_event(ev_out[b])                 # D2H of step k-2 has drained out_dev[b]
+        for s_, v in zip(step.state, out_views[b]):
+            s_.out = v
+        xs_, gs_, grs_ = in_views[b]
+        step.run(xs_, gs_, grs_)
+        ev_done[b].record(stream)
+        with torch.cuda.stream(copy):
+            copy.wait_event(ev_done[b])
+            out_host.copy_(out_dev[b], non_blocking=True)
+            ev_out[b].record(copy)
+    stream.wait_stream(copy)
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(f0.elapsed_time(f1) / args.steps, world, dev)
 
-    # roofline of the dominant phase (one kernel type each on the tensor-core path)
+    # BatchNorm diagonal Fisher of the 53 BN layers, per-sample scale and
+    # shift gradients [1024, C] fp32 (the large-mini-batch accumulation case)
+    bn_line = bn_bench(args, dev, stream, pk) if args.workload == "resnet50" else None
+
+    # per-kernel rooflines from the live event timings; the dominant kernel
+    # (largest share of the step's device time) goes in "roofline"
+    kernels = kernel_rooflines(kern, layers, batch, fl, pk, args.steps)
+    dom_name = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
+    roof = dict(kernels[dom_name])
+    roof["kernel"] = dom_name
     phase_share = {k: v / sum(ph.values()) for k, v in ph.items()}
-    dom = max(ph, key=ph.get)
-    if dom == "inverse":
-        ach = fl["inv"] / (ph["inverse"] * 1e-3) / 1e12
-        roof = {"bound": "alu", "kernel": "inversion (sgemm_kernel + leaf_kernel)", "achieved": ach,
-                "peak": FP32_ALU_PEAK_TFLOPS, "unit": "TFLOP/s", "frac": ach / FP32_ALU_PEAK_TFLOPS,
-                "traffic": None, "peak_src": "derived: 152 SMs x 128 fp32 lanes x 2 x 2.07 GHz"}
-    else:
-        key = "syrk" if dom == "factors" else "precond"
-        ach = fl[key] / (ph[dom] * 1e-3) / 1e12
-        roof = {"bound": "tensor", "kernel": "tc_gemm_kernel (" + dom + ")", "achieved": ach,
-                "peak": pk["bf16"], "unit": "TFLOP/s", "frac": ach / pk["bf16"], "traffic": None,
-                "peak_src": f"{pk['src']} bf16 burst"}
-    phases = {}
-    for n, key, bound, peak in (("factors", "syrk", "tensor", pk["bf16"]),
-                                ("inverse", "inv", "alu", FP32_ALU_PEAK_TFLOPS),
-                                ("precond", "precond", "tensor", pk["bf16"])):
-        a = fl[key] / (ph[n] * 1e-3) / 1e12
-        phases[n] = {"ms": ph[n], "share": phase_share[n], "tflops": a, "bound": bound, "frac": a / peak}
+    phases = {n: {"ms": ph[n], "share": phase_share[n]} for n in ph}
 
     line = {"metric": METRIC, "value": ms, "unit": "ms", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
@@ -362,16 +482,53 @@ def run_ours(args, world, rank, local):
                        "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB per step), no flush",
                        "graph": True, "xi": 0.95, "gamma": 1e-3},
             "tflops": fl["total"] / (ms * 1e-3) / 1e12, "gflop_per_step": fl["total"] / 1e9,
-            "eager_ms": eager_ms, "phases": phases, "roofline": roof,
-            "clocks": clk, "gpu_launches": launches_per_step * args.steps,
+            "eager_ms": eager_ms, "phases": phases, "roofline": roof, "kernels": kernels,
+            "clocks": clk, "gpu_launches": launches_per_step * args.steps, "bn_fisher": bn_line,
             "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": in_bytes,
-                    "d2h_bytes_per_step": out_bytes},
+                    "d2h_bytes_per_step": out_bytes,
+                    "how": "C ABI calls with host buffers; per step one pinned H2D of the packed inputs and "
+                           "one D2H of all preconditioned gradients, double-buffered on a copy stream"},
             "wall_s_timed": t_wall}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(layers, batch)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def bn_bench(args, dev, stream, pk, nsamples=1024):
+    import torch
+
+    from second_order_optimisation_gb300 import kfac
+    from second_order_optimisation_gb300 import workloads as W
+    chans = W.resnet50_bn_channels()
+    items = []
+    for xg, xb in W.bn_grads(chans, nsamples, "bench_bn"):
+        for x in (xg, xb):
+            C = x.shape[1]
+            items.append(kfac.BnItem(torch.from_numpy(x).to(dev), torch.empty(C, device=dev),
+                                     torch.empty(C, device=dev), torch.empty(C, device=dev)))
+    read = sum(it.x.numel() * 4 for it in items)
+    written = sum(3 * it.F.numel() * 4 for it in items)
+    kfac.kfac_bn_diag_fisher(items, 1e-3)           # warm (and host set-up) outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()                   # one launch per replay, no host overhead inside
+    with torch.cuda.graph(graph):
+        kfac.kfac_bn_diag_fisher(items, 1e-3)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    gbs = (read + written) / (ms * 1e-3) / 1e9
+    return {"layers": len(chans), "tensors": len(items), "n_samples": nsamples, "ms": ms,
+            "bytes": read + written, "achieved_gbs": gbs, "peak_gbs": pk["hbm"], "frac": gbs / pk["hbm"],
+            "bound": "hbm", "l2": "inputs larger than L2 (%.0f MB), no flush" % (read / 1e6)}
 
 
 def main():

@@ -65,6 +65,18 @@ int kfac_version(void);
  * (a diagnostic counter; every entry point adds the launches it makes). */
 long long kfac_launch_count(void);
 
+/* Optional per-kernel timing (diagnostic, off by default).  While enabled,
+ * every kernel launch the library makes is bracketed by CUDA events recorded
+ * on its launch stream (up to 65536 launches).  kfac_timing_read waits for
+ * those events, writes for each kernel kind k < n the total device time in
+ * milliseconds (ms[k]) and the number of launches (launches[k]), and clears
+ * the record; it returns KFAC_OK or KFAC_ERR_CUDA.  kfac_timing_enable
+ * returns the previous setting.  Kind names: kfac_timing_kind_name(k) ("" past
+ * the last kind).  Do not enable it while a stream is being captured. */
+int kfac_timing_enable(int on);
+int kfac_timing_read(double *ms, long long *launches, int n);
+const char *kfac_timing_kind_name(int k);
+
 /* ======================================================================
  * kfac_factor_update -- Kronecker factor statistic + running average.
  *

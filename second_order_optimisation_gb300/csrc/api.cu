@@ -18,6 +18,43 @@ namespace kfac {
 static std::atomic<long long> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+// Optional per-kernel timing: a pool of event pairs, one pair per launch
+// while enabled (diagnostic; off by default).
+namespace {
+constexpr int TIMING_MAX = 65536;
+struct TimingRec {
+    int kind;
+    cudaEvent_t start, stop;
+};
+std::mutex g_tmu;
+bool g_timing = false;
+std::vector<TimingRec> g_recs;      // in use
+std::vector<TimingRec> g_free;      // recycled event pairs
+}  // namespace
+
+int timing_begin(int kind, cudaStream_t st) {
+    if (!g_timing) return -1;
+    std::lock_guard<std::mutex> lock(g_tmu);
+    if (!g_timing || (int)g_recs.size() >= TIMING_MAX) return -1;
+    TimingRec r{kind, nullptr, nullptr};
+    if (!g_free.empty()) {
+        r.start = g_free.back().start;
+        r.stop = g_free.back().stop;
+        g_free.pop_back();
+    } else if (cudaEventCreate(&r.start) != cudaSuccess || cudaEventCreate(&r.stop) != cudaSuccess) {
+        return -1;
+    }
+    cudaEventRecord(r.start, st);
+    g_recs.push_back(r);
+    return (int)g_recs.size() - 1;
+}
+
+void timing_end(int slot, cudaStream_t st) {
+    if (slot < 0) return;
+    std::lock_guard<std::mutex> lock(g_tmu);
+    if (slot < (int)g_recs.size()) cudaEventRecord(g_recs[slot].stop, st);
+}
+
 int device_sm_count() {
     static int cache[64] = {0};
     int dev = 0;
@@ -81,6 +118,8 @@ kfac_status validate_factor(const kfac_factor_desc *descs, int count, std::vecto
         if (!geom_of(d, geo[i])) return KFAC_ERR_INVALID;
         if (d.ldf < geo[i].d) return KFAC_ERR_INVALID;
         if (geo[i].d > 65536 || geo[i].M >= (1LL << 31)) return KFAC_ERR_UNSUPPORTED;
+        // a materialised patch matrix is indexed with 32-bit element counts
+        if (!geo[i].direct && geo[i].M * (long long)(geo[i].d + 8) >= (1LL << 31)) return KFAC_ERR_UNSUPPORTED;
     }
     return KFAC_OK;
 }
@@ -176,6 +215,41 @@ extern "C" const char *kfac_status_string(int status) {
 extern "C" int kfac_version(void) { return 100; }
 
 extern "C" long long kfac_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+extern "C" int kfac_timing_enable(int on) {
+    std::lock_guard<std::mutex> lock(g_tmu);
+    const int was = g_timing ? 1 : 0;
+    g_timing = on != 0;
+    return was;
+}
+
+extern "C" const char *kfac_timing_kind_name(int k) {
+    static const char *names[KK_COUNT] = {"tc_gemm_bf16", "tc_gemm_tf32x3", "inv_leaf", "inv_prep",
+                                          "inv_finish", "damping", "im2col", "colsum", "sgemm_f32",
+                                          "bn_fisher", "map_copy"};
+    return (k >= 0 && k < KK_COUNT) ? names[k] : "";
+}
+
+extern "C" int kfac_timing_read(double *ms, long long *launches, int n) {
+    std::lock_guard<std::mutex> lock(g_tmu);
+    for (int k = 0; k < n; ++k) {
+        if (ms) ms[k] = 0.0;
+        if (launches) launches[k] = 0;
+    }
+    int status = KFAC_OK;
+    for (TimingRec &r : g_recs) {
+        float t = 0.f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+            status = KFAC_ERR_CUDA;
+        if (r.kind < n) {
+            if (ms) ms[r.kind] += t;
+            if (launches) launches[r.kind] += 1;
+        }
+        g_free.push_back(r);
+    }
+    g_recs.clear();
+    return status;
+}
 
 // ------------------------------------------------------------ factor update
 

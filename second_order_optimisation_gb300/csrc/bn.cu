@@ -135,8 +135,7 @@ extern "C" kfac_status kfac_bn_diag_fisher(const kfac_bn_desc *descs, int count,
         P->ns = n_samples;
         P->gamma = gamma;
         P->xi = xi;
-        bn_fisher_kernel<<<chunks, 256, 0, st>>>(*P);
-        KFAC_LAUNCH_CHECK();
+        KFAC_LAUNCH(KK_BN, st, (bn_fisher_kernel<<<chunks, 256, 0, st>>>(*P)));
     }
     return KFAC_OK;
 }

@@ -29,8 +29,21 @@ namespace kfac {
 // through kfac_launch_count()).
 void count_launch();
 
-#define KFAC_LAUNCH_CHECK()                                      \
+// Kernel kinds for the optional per-kernel timing (kfac_timing_*).
+enum KernelKind : int {
+    KK_TC_BF16 = 0, KK_TC_TF32X3, KK_LEAF, KK_PREP, KK_FINISH, KK_DAMPING, KK_IM2COL, KK_COLSUM,
+    KK_SGEMM, KK_BN, KK_MAPCOPY, KK_COUNT
+};
+// Returns a slot (>= 0) after recording a start event on `st` when timing is
+// enabled, -1 otherwise; timing_end records the matching end event.
+int timing_begin(int kind, cudaStream_t st);
+void timing_end(int slot, cudaStream_t st);
+
+#define KFAC_LAUNCH(kind, st, launch)                            \
     do {                                                         \
+        const int slot_ = ::kfac::timing_begin((kind), (st));    \
+        launch;                                                  \
+        ::kfac::timing_end(slot_, (st));                         \
         ::kfac::count_launch();                                  \
         if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA; \
     } while (0)

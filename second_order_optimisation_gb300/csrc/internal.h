@@ -34,6 +34,8 @@ struct TcJob {
     int a_row0, a_col0, b_row0, b_col0;
     int M, N, K;
     int syrk;
+    int sym;       // TF32X3 + SPLIT, M == N: the result is symmetric; only tiles on or
+                   // above the diagonal run and off-diagonal ones also write their transpose
     int no_split;
     int epi;
     float alpha, beta;

@@ -18,10 +18,10 @@
 //      trailing update of a block Cholesky step:
 //        X11 <- X11^-1                               (recursion / leaf)
 //        T   <- X11 X12,   U <- T^T                  (tensor cores)
-//        X22 <- X22 - X21 T                          (tensor cores)
+//        X22 <- X22 - X21 T       (symmetric: upper tiles + mirror)
 //        X22 <- X22^-1                               (recursion / leaf)
 //        X12 <- -T X22,    X21 <- X12^T              (tensor cores)
-//        X11 <- X11 - X12 T^T                        (tensor cores)
+//        X11 <- X11 - X12 T^T     (symmetric: upper tiles + mirror)
 //      The GEMMs run on tcgen05 with three tf32 products per slice
 //      (hi*hi + hi*lo + lo*hi) and fp32 accumulation.  Leaves are 128 x 128
 //      blocks inverted by one CTA with the matrix in registers: Cholesky
@@ -214,10 +214,12 @@ struct LeafParams {
 //   C. X^-1 = V V^T, written back as a (hi, lo) pair.
 __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_constant__ LeafParams P) {
     constexpr int N = LEAF, LS = LEAF + 1, PW = 32;
-    extern __shared__ float smem_leaf[];
-    float *S = smem_leaf;            // N x LS: the block, U in its upper triangle
-    float *V = S + N * LS;           // N x LS: V = U^-1 (upper)
-    float *T = V + N * LS;           // 3 x PW x (PW+1): block temporaries
+    constexpr int WP = LEAF + 4;     // pitch of V^T for 16-byte row loads
+    extern __shared__ __align__(16) float smem_leaf[];
+    float *V = smem_leaf;            // N x LS: V = U^-1 (upper)
+    float *S = V + N * LS;           // N x LS: the block, U in its upper triangle
+    float *T = S + N * LS;           // 3 x PW x (PW+1): block temporaries
+    float *W = S;                    // N x WP: V^T, overlays S and T once they are free
     __shared__ int bad;
     __shared__ float rdiag[N];
     const LeafJob &J = P.j[blockIdx.x];
@@ -392,31 +394,38 @@ __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_cons
     __syncthreads();
 
     // ---------------------------------------------------------- C. V V^T
+    // W = V^T (W[l][i] = V[i][l], zero for l < i); X[i][j] = sum_l W[l][i] W[l][j].
+    // Warp w owns rows 8w..8w+7 (one broadcast float4 pair per l, and no
+    // work for l < 8w), lane owns columns lane + 32 c.
+    for (int e = tid; e < N * N; e += LEAF_THREADS) {
+        const int l = e >> 7, i = e & 127;
+        W[l * WP + i] = V[i * LS + l];
+    }
+    __syncthreads();
     {
-        const int ty = tid >> 5, tx = tid & 31;
         float x[8][4];
 #pragma unroll
         for (int r = 0; r < 8; ++r)
 #pragma unroll
             for (int c = 0; c < 4; ++c) x[r][c] = 0.f;
-        for (int l = 0; l < N; ++l) {
-            float vi[8], vj[4];
+        const int r0 = 8 * warp;
+        for (int l = r0; l < N; ++l) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(W + l * WP + r0);
+            const float4 a1 = *reinterpret_cast<const float4 *>(W + l * WP + r0 + 4);
+            const float vi[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            float vj[4];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) vi[r] = V[(ty + 16 * r) * LS + l];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) vj[c] = V[(tx + 32 * c) * LS + l];
+            for (int c = 0; c < 4; ++c) vj[c] = W[l * WP + lane + 32 * c];
 #pragma unroll
             for (int r = 0; r < 8; ++r)
-                if (ty + 16 * r <= l) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) x[r][c] = fmaf(vi[r], vj[c], x[r][c]);
-                }
+                for (int c = 0; c < 4; ++c) x[r][c] = fmaf(vi[r], vj[c], x[r][c]);
         }
 #pragma unroll
         for (int r = 0; r < 8; ++r)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int i = ty + 16 * r, j = tx + 32 * c;
+                const int i = r0 + r, j = lane + 32 * c;
                 const long long o = (long long)i * J.ld + j;
                 const float h = tf32_hi(x[r][c]);
                 J.Xh[o] = h;
@@ -453,7 +462,7 @@ void gen_ops(std::vector<Op> &ops, const MatWork &w, int o, int n, int *info) {
     const int nb = n / LEAF, h = LEAF * (nb / 2), m = n - h;
     gen_ops(ops, w, o, h, info);
     auto gemm = [&](int ma, int ar, int ac, int mb, int br, int bc, int M, int N, int K, float alpha,
-                    float beta, float *Ch, float *Cl, float *Cth, float *Ctl) {
+                    float beta, float *Ch, float *Cl, float *Cth, float *Ctl, int sym) {
         Op op{};
         op.leaf = 0;
         TcJob &j = op.g;
@@ -464,19 +473,20 @@ void gen_ops(std::vector<Op> &ops, const MatWork &w, int o, int n, int *info) {
         j.alpha = alpha; j.beta = beta;
         j.C = Ch; j.C_lo = Cl; j.ldc = ld;
         j.Ct = Cth; j.Ct_lo = Ctl; j.ldct = ld;
+        j.sym = sym;
         ops.push_back(op);
     };
     const long long x11 = o * ld + o, x12 = o * ld + o + h, x21 = (o + h) * ld + o, x22 = (o + h) * ld + o + h;
     const long long tt = o * ld;  // T block: rows [o, o+h), columns [0, m)
     // T = X11 X12 (B rows = X21 rows), U = T^T
-    gemm(w.mx, o, o, w.mx, o + h, o, h, m, h, 1.f, 0.f, w.Th + tt, w.Tl + tt, w.Uh, w.Ul);
+    gemm(w.mx, o, o, w.mx, o + h, o, h, m, h, 1.f, 0.f, w.Th + tt, w.Tl + tt, w.Uh, w.Ul, 0);
     // X22 -= X21 T  (B rows = U rows)
-    gemm(w.mx, o + h, o, w.mu, 0, 0, m, m, h, -1.f, 1.f, w.Xh + x22, w.Xl + x22, nullptr, nullptr);
+    gemm(w.mx, o + h, o, w.mu, 0, 0, m, m, h, -1.f, 1.f, w.Xh + x22, w.Xl + x22, nullptr, nullptr, 1);
     gen_ops(ops, w, o + h, m, info);
     // X12 = -T X22 (X22 symmetric: B rows = X22 rows), X21 = X12^T
-    gemm(w.mt, o, 0, w.mx, o + h, o + h, h, m, m, -1.f, 0.f, w.Xh + x12, w.Xl + x12, w.Xh + x21, w.Xl + x21);
+    gemm(w.mt, o, 0, w.mx, o + h, o + h, h, m, m, -1.f, 0.f, w.Xh + x12, w.Xl + x12, w.Xh + x21, w.Xl + x21, 0);
     // X11 -= X12 T^T (B rows = T rows)
-    gemm(w.mx, o, o + h, w.mt, o, 0, h, h, m, -1.f, 1.f, w.Xh + x11, w.Xl + x11, nullptr, nullptr);
+    gemm(w.mx, o, o + h, w.mt, o, 0, h, h, m, -1.f, 1.f, w.Xh + x11, w.Xl + x11, nullptr, nullptr, 1);
 }
 
 // Workspace layout shared by the size query and the run.
@@ -555,8 +565,7 @@ kfac_status leaf_launch(const std::vector<LeafJob> &jobs, cudaStream_t st) {
         int n = 0;
         while (pos < jobs.size() && n < MAT_MAX) P->j[n++] = jobs[pos++];
         P->n = n;
-        leaf_kernel<<<n, LEAF_THREADS, LEAF_SMEM, st>>>(*P);
-        KFAC_LAUNCH_CHECK();
+        KFAC_LAUNCH(KK_LEAF, st, (leaf_kernel<<<n, LEAF_THREADS, LEAF_SMEM, st>>>(*P)));
     }
     return KFAC_OK;
 }
@@ -578,9 +587,8 @@ kfac_status tile_launch(std::vector<TileMat> &mats, const float *damp, cudaStrea
         P->begin[n] = tiles;
         P->n = n;
         P->damp = damp;
-        if (PREP) prep_kernel<<<tiles, 256, 0, st>>>(*P);
-        else finish_kernel<<<tiles, 256, 0, st>>>(*P);
-        KFAC_LAUNCH_CHECK();
+        if (PREP) KFAC_LAUNCH(KK_PREP, st, (prep_kernel<<<tiles, 256, 0, st>>>(*P)));
+        else KFAC_LAUNCH(KK_FINISH, st, (finish_kernel<<<tiles, 256, 0, st>>>(*P)));
     }
     return KFAC_OK;
 }
@@ -613,8 +621,7 @@ kfac_status damping_run(const InvMatrix *mats, int nlayers, float gamma, int pi_
         P->pi_split = pi_split;
         P->damp = damp_dev;
         P->base = base;
-        damping_kernel<<<n, 256, 0, st>>>(*P);
-        KFAC_LAUNCH_CHECK();
+        KFAC_LAUNCH(KK_DAMPING, st, (damping_kernel<<<n, 256, 0, st>>>(*P)));
     }
     return KFAC_OK;
 }

@@ -40,18 +40,19 @@ __global__ void im2col_kernel(const __grid_constant__ ImParams P) {
             if (P.begin[mid] <= u) lo = mid; else hi = mid - 1;
         }
         const Im2colJob &q = P.j[lo];
-        const long long local = u - P.begin[lo];
+        // 32-bit index math (a job has fewer than 2^31 units and rows)
+        const unsigned local = (unsigned)(u - P.begin[lo]);
         const int dcore = q.kh * q.kw * q.c;
         const int d = dcore + q.append_one;
         const bool v8 = P.vec8[lo] != 0;
-        const int per_row = v8 ? dcore / 8 : d;
-        const long long m = local / per_row;
+        const unsigned per_row = v8 ? dcore / 8 : d;
+        const unsigned m = local / per_row;
         const int cu = (int)(local - m * per_row);
-        const int wo = (int)(m % q.wo);
-        const long long t = m / q.wo;
-        const int ho = (int)(t % q.ho);
-        const int img = (int)(t / q.ho);
-        T *prow = (T *)q.P + m * q.ldp;
+        const unsigned t = m / (unsigned)q.wo;
+        const int wo = (int)(m - t * (unsigned)q.wo);
+        const unsigned img = t / (unsigned)q.ho;
+        const int ho = (int)(t - img * (unsigned)q.ho);
+        T *prow = (T *)q.P + (long long)m * q.ldp;
         const T *x = (const T *)q.x;
         if (v8) {
             const int col = cu * 8;
@@ -171,10 +172,9 @@ kfac_status im2col_run(const Im2colJob *jobs, int njobs, int dtype, cudaStream_t
         const int threads = 256;
         const long long blocks = std::min<long long>(ceil_div(units, threads), 152LL * 16);
         if (dtype == KFAC_BF16)
-            im2col_kernel<__nv_bfloat16><<<(int)blocks, threads, 0, st>>>(*P);
+            KFAC_LAUNCH(KK_IM2COL, st, (im2col_kernel<__nv_bfloat16><<<(int)blocks, threads, 0, st>>>(*P)));
         else
-            im2col_kernel<float><<<(int)blocks, threads, 0, st>>>(*P);
-        KFAC_LAUNCH_CHECK();
+            KFAC_LAUNCH(KK_IM2COL, st, (im2col_kernel<float><<<(int)blocks, threads, 0, st>>>(*P)));
     }
     return KFAC_OK;
 }
@@ -194,8 +194,7 @@ kfac_status colsum_run(const ColsumJob *jobs, int njobs, cudaStream_t st) {
         }
         P->begin[n] = chunks;
         P->n = n;
-        colsum_kernel<<<chunks, 256, 0, st>>>(*P);
-        KFAC_LAUNCH_CHECK();
+        KFAC_LAUNCH(KK_COLSUM, st, (colsum_kernel<<<chunks, 256, 0, st>>>(*P)));
     }
     return KFAC_OK;
 }

@@ -1,8 +1,8 @@
-// sgemm.cu -- batched fp32 CUDA-core GEMM for the fp32 parts of the K-FAC
-// step: the Schur-complement updates of the damped inversion (Osawa et al.,
-// "Large-Scale Distributed Second-Order Optimization Using
-// Kronecker-Factored Approximate Curvature ...", section 3.2, Eq. 6) and the
-// fp32-input factor statistic / preconditioning (Eq. 5, Eq. 7).
+// sgemm.cu -- batched fp32 CUDA-core GEMM for the fp32-input path of the
+// K-FAC step (Osawa et al., "Large-Scale Distributed Second-Order
+// Optimization Using Kronecker-Factored Approximate Curvature ...",
+// section 3.2): the factor statistic P^T P of fp32 sources (Eq. 5) and the
+// preconditioned gradient G^-1 grad A^-1 of fp32 operands (Eq. 7).
 //
 // C[M x N] = alpha * op(A) op(B) + beta * C, one 128x128 tile per CTA, 256
 // threads with 8x8 register tiles, K in steps of 16 staged through shared
@@ -160,8 +160,7 @@ kfac_status sg_run(const SgJob *jobs, int njobs, cudaStream_t st) {
         }
         if (n == 0) break;
         P->n = n;
-        sgemm_kernel<<<tiles, STHREADS, 0, st>>>(*P);
-        KFAC_LAUNCH_CHECK();
+        KFAC_LAUNCH(KK_SGEMM, st, (sgemm_kernel<<<tiles, STHREADS, 0, st>>>(*P)));
     }
     return KFAC_OK;
 }

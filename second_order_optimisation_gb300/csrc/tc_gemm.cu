@@ -60,7 +60,7 @@ struct TcProb {
     int a_row0, a_col0;      // operand sub-block origin inside its map (rows, columns)
     int b_row0, b_col0;
     int M, N, k_tiles;
-    int tiles_n, syrk, ksplit, work_begin, epi;
+    int tiles_n, syrk, sym, ksplit, work_begin, epi;
     float alpha, beta;
     float *C;
     float *C_lo;
@@ -118,7 +118,7 @@ __device__ __forceinline__ Work decode_work(const TcParams &P, int w) {
     int local = w - q.work_begin;
     k.tile = local / q.ksplit;
     k.split = local - k.tile * q.ksplit;
-    if (q.syrk) {
+    if (q.syrk || q.sym) {
         int T = q.tiles_n, t = k.tile, tm = 0;
         while (t >= T - tm) { t -= T - tm; ++tm; }
         k.tm = tm;
@@ -171,7 +171,7 @@ __device__ __forceinline__ float tf32_hi(float v) {
 // consecutive columns of one row.  Old values (beta != 0) are loaded for all
 // 32 rows before any store.
 __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, const float *v, float *stage,
-                                            int lane) {
+                                            int lane, bool mirror) {
     const float a = q.alpha, b = q.beta;
     if (q.epi == TC_EPI_SPLIT && q.Ct) {  // host guarantees beta == 0 here
         const int i = i0 + lane;
@@ -230,11 +230,32 @@ __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, con
 #pragma unroll
         for (int r = 0; r < 32; ++r) {
             const int i = i0 + r;
+            const float o = fmaf(b, old[r] + oldl[r], a * acc[r]);
+            const float h = tf32_hi(o);
+            old[r] = h;       // keep the final pair for the mirror below
+            oldl[r] = o - h;
             if (jok && i < q.M) {
-                const float o = fmaf(b, old[r] + oldl[r], a * acc[r]);
-                const float h = tf32_hi(o);
                 q.C[(long long)i * q.ldc + j] = h;
                 q.C_lo[(long long)i * q.ldc + j] = o - h;
+            }
+        }
+        if (mirror) {
+            // symmetric output: this upper tile also fills its transposed
+            // position; go back through the stage so that lane = row and every
+            // store covers 32 consecutive columns of C[j][i0 .. i0+31]
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                float *dst = part ? q.C_lo : q.C;
+#pragma unroll
+                for (int r = 0; r < 32; ++r) stage[r * STAGE_LD + lane] = part ? oldl[r] : old[r];
+                __syncwarp();
+                const int i = i0 + lane;
+#pragma unroll 4
+                for (int c = 0; c < 32; ++c) {
+                    const int jj = j0 + c;
+                    if (i < q.M && jj < q.N) dst[(long long)jj * q.ldc + i] = stage[lane * STAGE_LD + c];
+                }
+                __syncwarp();
             }
         }
     }
@@ -281,16 +302,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
+            int last_p = -1;
             for (int w = blockIdx.x; w < P.total_work && !*abort_flag; w += gridDim.x) {
                 Work k = decode_work(P, w);
                 const TcProb &q = P.prob[k.p];
                 const CUtensorMap *ma = P.maps + q.map_a;
                 const CUtensorMap *mb = P.maps + q.map_b;
-                acquire_map(ma);
-                acquire_map(mb);
-                if (KIND == TC_KIND_TF32X3) {
-                    acquire_map(ma + 1);
-                    acquire_map(mb + 1);
+                if (k.p != last_p) {  // consecutive items of one problem share its maps
+                    acquire_map(ma);
+                    acquire_map(mb);
+                    if (KIND == TC_KIND_TF32X3) {
+                        acquire_map(ma + 1);
+                        acquire_map(mb + 1);
+                    }
+                    last_p = k.p;
                 }
                 const bool diag = KIND == TC_KIND_BF16 && q.syrk && k.tm == k.tn;
                 const uint32_t bytes = diag ? TILE_BYTES : STAGE_BYTES;
@@ -398,7 +423,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
                     tmem_ld_32x32b_x32(t_row + c * 32, v);
-                    chunk_store(q, i0, k.tn * BN + c * 32, v, stage, lane);
+                    chunk_store(q, i0, k.tn * BN + c * 32, v, stage, lane, q.sym && k.tm != k.tn);
                 }
                 tc_fence_before();
                 mbar_arrive(&acce[b]);
@@ -439,7 +464,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                                 v[4 * f] += t.x; v[4 * f + 1] += t.y; v[4 * f + 2] += t.z; v[4 * f + 3] += t.w;
                             }
                         }
-                        chunk_store(q, i0, k.tn * BN + c * 32, v, stage, lane);
+                        chunk_store(q, i0, k.tn * BN + c * 32, v, stage, lane, q.sym && k.tm != k.tn);
                     }
                     if (etid == 0) q.counters[k.tile] = 0;
                 }
@@ -467,7 +492,7 @@ int bk_of(int kind) { return kind == TC_KIND_BF16 ? Traits<TC_KIND_BF16>::BK : T
 
 int tiles_of(const TcJob &j) {
     int tm = (int)ceil_div(j.M, BM), tn = (int)ceil_div(j.N, BN);
-    return j.syrk ? tn * (tn + 1) / 2 : tm * tn;
+    return (j.syrk || j.sym) ? tn * (tn + 1) / 2 : tm * tn;
 }
 
 Plan make_plan(const TcJob *jobs, int n, int kind) {
@@ -482,8 +507,12 @@ Plan make_plan(const TcJob *jobs, int n, int kind) {
         total += (double)p.tiles[i] * p.k_tiles[i];
     }
     const int sms = device_sm_count();
-    // aim for ~4 work items per SM, at least 8 K tiles per item
-    const double target = std::max(8.0, total / (sms * 4.0));
+    // Split K only where one problem's tiles would otherwise be the critical
+    // path: the longest work item should not exceed about twice the average
+    // share of one SM.  A split costs a partial-tile round trip through L2, so
+    // items keep at least 8 (bf16) / 64 (tf32x3) K tiles.
+    const double min_kt = kind == TC_KIND_BF16 ? 8.0 : 64.0;
+    const double target = std::max(min_kt, total / (sms * 2.0));
     for (int i = 0; i < n; ++i) {
         int ks = (int)std::ceil(p.k_tiles[i] / target);
         ks = std::max(1, std::min(ks, std::min(p.k_tiles[i], 256)));
@@ -560,8 +589,7 @@ kfac_status tc_upload_maps(const CUtensorMap *maps, int n, CUtensorMap *dev, cud
         std::memcpy(P->m, maps + base, sizeof(CUtensorMap) * cnt);
         P->dst = dev + base;
         P->n = cnt;
-        map_copy_kernel<<<(int)ceil_div(cnt * 8, 256), 256, 0, st>>>(*P);
-        KFAC_LAUNCH_CHECK();
+        KFAC_LAUNCH(KK_MAPCOPY, st, (map_copy_kernel<<<(int)ceil_div(cnt * 8, 256), 256, 0, st>>>(*P)));
     }
     return KFAC_OK;
 }
@@ -580,6 +608,11 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
     if (njobs <= 0) return KFAC_OK;
     if ((kind == TC_KIND_BF16 ? set_smem_attr<TC_KIND_BF16>() : set_smem_attr<TC_KIND_TF32X3>()) != cudaSuccess)
         return KFAC_ERR_CUDA;
+    for (int i = 0; i < njobs; ++i) {
+        const TcJob &j = jobs[i];
+        if (j.Ct && j.beta != 0.f) return KFAC_ERR_INVALID;                       // transposed copy needs beta == 0
+        if (j.sym && (kind != TC_KIND_TF32X3 || j.M != j.N || j.epi != TC_EPI_SPLIT)) return KFAC_ERR_INVALID;
+    }
     Plan p = make_plan(jobs, njobs, kind);
     Buffers bufs;
     take_buffers(p, njobs, ws, bufs);
@@ -608,6 +641,7 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
             q.k_tiles = p.k_tiles[ji];
             q.tiles_n = (int)ceil_div(j.N, BN);
             q.syrk = j.syrk;
+            q.sym = j.sym;
             q.ksplit = p.ksplit[ji];
             q.work_begin = work;
             q.epi = j.epi;
@@ -628,10 +662,9 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
         P->error = err;
         const int grid = std::min(work, sms);
         if (kind == TC_KIND_BF16)
-            tc_gemm_kernel<TC_KIND_BF16><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(*P);
+            KFAC_LAUNCH(KK_TC_BF16, st, (tc_gemm_kernel<TC_KIND_BF16><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(*P)));
         else
-            tc_gemm_kernel<TC_KIND_TF32X3><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(*P);
-        KFAC_LAUNCH_CHECK();
+            KFAC_LAUNCH(KK_TC_TF32X3, st, (tc_gemm_kernel<TC_KIND_TF32X3><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(*P)));
     }
     return KFAC_OK;
 }

@@ -26,7 +26,8 @@ LIB_PATH = os.path.join(_HERE, "libkfac_gb300.so")
 KFAC_OK, KFAC_ERR_INVALID, KFAC_ERR_UNSUPPORTED, KFAC_ERR_NOT_PD, KFAC_ERR_CUDA, KFAC_ERR_WORKSPACE = range(6)
 KFAC_BF16, KFAC_F32 = 0, 1
 
-EXPORTS = ("kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_factor_update_workspace_size",
+EXPORTS = ("kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_timing_enable",
+           "kfac_timing_read", "kfac_timing_kind_name", "kfac_factor_update_workspace_size",
            "kfac_factor_update", "kfac_damp_invert_workspace_size", "kfac_damp_invert",
            "kfac_precondition_workspace_size", "kfac_precondition", "kfac_bn_diag_fisher",
            "kfac_noalloc_scratch_bytes", "kfac_precondition_noalloc")
@@ -91,6 +92,12 @@ def load() -> ctypes.CDLL:
         lib.kfac_status_string.restype = ctypes.c_char_p
         lib.kfac_version.restype = i32
         lib.kfac_launch_count.restype = ctypes.c_longlong
+        lib.kfac_timing_enable.argtypes = [i32]
+        lib.kfac_timing_enable.restype = i32
+        lib.kfac_timing_read.argtypes = [vp, vp, i32]
+        lib.kfac_timing_read.restype = i32
+        lib.kfac_timing_kind_name.argtypes = [i32]
+        lib.kfac_timing_kind_name.restype = ctypes.c_char_p
         lib.kfac_factor_update_workspace_size.argtypes = [vp, i32]
         lib.kfac_factor_update_workspace_size.restype = sz
         lib.kfac_factor_update.argtypes = [vp, i32, vp, sz, vp]
@@ -113,6 +120,26 @@ def load() -> ctypes.CDLL:
 def launch_count() -> int:
     """Kernel launches the library has enqueued in this process."""
     return int(load().kfac_launch_count())
+
+
+def timing_enable(on: bool = True) -> bool:
+    """Turn the library's per-kernel event timing on or off (diagnostic)."""
+    return bool(load().kfac_timing_enable(int(bool(on))))
+
+
+def timing_read() -> dict:
+    """{kernel kind: (total ms, launches)} since the last read (synchronises)."""
+    lib = load()
+    n = 32
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_longlong * n)()
+    _check(lib.kfac_timing_read(ms, cnt, n), "kfac_timing_read")
+    out = {}
+    for k in range(n):
+        name = lib.kfac_timing_kind_name(k).decode()
+        if name and cnt[k]:
+            out[name] = (ms[k], int(cnt[k]))
+    return out
 
 
 def status_string(status: int) -> str:
