@@ -7,8 +7,8 @@
 // method it builds on):
 //     pi = sqrt((tr A/dA) / (tr G/dG)),  damp_A = pi sqrt(gamma),  damp_G = sqrt(gamma)/pi.
 //
-// Algorithm (every matrix of the call advances in lock-step, one batched
-// launch per step kind):
+// Algorithm (every matrix of the call advances in batched rounds, one launch
+// per round, see schedule_rounds):
 //   1. traces -> damping values (one CTA per layer, fixed reduction order);
 //   2. X = sym(F) + damp I, padded with an identity block to a multiple of
 //      128 (the inverse of diag(X, I) is diag(X^-1, I)), stored as a (hi, lo)
@@ -489,6 +489,58 @@ void gen_ops(std::vector<Op> &ops, const MatWork &w, int o, int n, int *info) {
     gemm(w.mx, o, o + h, w.mt, o, 0, h, h, m, -1.f, 1.f, w.Xh + x11, w.Xl + x11, nullptr, nullptr, 1);
 }
 
+// Round schedule: the longest chain sets the sequence of rounds (one launch
+// each, leaf or GEMM); every other chain is embedded as late as possible into
+// rounds of the same op kind, in order.  The long chain's late rounds are
+// small, latency-bound launches with most SMs idle, and the shorter chains'
+// work fills them; one launch per round.  Falls back to left-aligned
+// lock-step (a leaf and a GEMM launch per round) if a chain does not embed.
+std::vector<std::vector<std::pair<int, int>>> schedule_rounds(const std::vector<std::vector<Op>> &chains,
+                                                              std::vector<int> &round_kind) {
+    int crit = -1;
+    for (int k = 0; k < (int)chains.size(); ++k)
+        if (crit < 0 || chains[k].size() > chains[crit].size()) crit = k;
+    std::vector<std::vector<std::pair<int, int>>> rounds;
+    round_kind.clear();
+    if (crit < 0) return rounds;
+    const int R = (int)chains[crit].size();
+    rounds.assign(R, {});
+    for (int r = 0; r < R; ++r) round_kind.push_back(chains[crit][r].leaf);
+    bool ok = true;
+    std::vector<std::vector<int>> slot(chains.size());
+    for (int k = 0; k < (int)chains.size() && ok; ++k) {
+        const int n = (int)chains[k].size();
+        slot[k].assign(n, -1);
+        int r = R - 1;
+        for (int i = n - 1; i >= 0; --i) {
+            while (r >= 0 && round_kind[r] != chains[k][i].leaf) --r;
+            if (r < 0) { ok = false; break; }
+            slot[k][i] = r--;
+        }
+    }
+    if (ok) {
+        for (int k = 0; k < (int)chains.size(); ++k)
+            for (int i = 0; i < (int)chains[k].size(); ++i) rounds[slot[k][i]].push_back({k, i});
+        return rounds;
+    }
+    // fallback: left-aligned lock-step, leaves then GEMMs in each step
+    size_t longest = 0;
+    for (const auto &c : chains) longest = std::max(longest, c.size());
+    rounds.clear();
+    round_kind.clear();
+    for (size_t r = 0; r < longest; ++r)
+        for (int kind = 1; kind >= 0; --kind) {
+            std::vector<std::pair<int, int>> v;
+            for (int k = 0; k < (int)chains.size(); ++k)
+                if (r < chains[k].size() && chains[k][r].leaf == kind) v.push_back({k, (int)r});
+            if (!v.empty()) {
+                rounds.push_back(v);
+                round_kind.push_back(kind);
+            }
+        }
+    return rounds;
+}
+
 // Workspace layout shared by the size query and the run.
 struct InvPlan {
     int *err = nullptr;
@@ -496,6 +548,8 @@ struct InvPlan {
     std::vector<CUtensorMap> maps;
     std::vector<MatWork> work;
     std::vector<std::vector<Op>> chains;
+    std::vector<std::vector<std::pair<int, int>>> rounds;
+    std::vector<int> round_kind;
     size_t longest = 0;
     char *tc_ws = nullptr;
     size_t tc_bytes = 0;
@@ -536,13 +590,14 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
         gen_ops(p.chains[k], w, 0, w.dp, info_dev ? info_dev + k : nullptr);
         p.longest = std::max(p.longest, p.chains[k].size());
     }
-    // engine scratch: the largest round
+    // engine scratch: the largest GEMM round
+    p.rounds = schedule_rounds(p.chains, p.round_kind);
     size_t tcb = 0;
     std::vector<TcJob> round;
-    for (size_t r = 0; r < p.longest; ++r) {
+    for (size_t r = 0; r < p.rounds.size(); ++r) {
         round.clear();
-        for (int k = 0; k < nmats; ++k)
-            if (r < p.chains[k].size() && !p.chains[k][r].leaf) round.push_back(p.chains[k][r].g);
+        for (const auto &ki : p.rounds[r])
+            if (!p.chains[ki.first][ki.second].leaf) round.push_back(p.chains[ki.first][ki.second].g);
         tcb = std::max(tcb, tc_workspace_bytes(round.data(), (int)round.size(), TC_KIND_TF32X3));
     }
     p.tc_bytes = tcb;
@@ -643,15 +698,14 @@ kfac_status inv_run(const InvMatrix *mats, int nmats, const float *damp_dev, int
                         mats[k].out, mats[k].ldo, mats[k].out_bf16, mats[k].ldo_bf16, k, 0};
     if ((s = tile_launch<true>(tm, damp_dev, st)) != KFAC_OK) return s;
 
-    // 2. lock-step rounds: the leaves of a round in one launch, its GEMMs in one
+    // 2. rounds (see schedule_rounds): each round is one leaf or one GEMM launch
     std::vector<LeafJob> leaves;
     std::vector<TcJob> gemms;
-    for (size_t r = 0; r < p.longest; ++r) {
+    for (size_t r = 0; r < p.rounds.size(); ++r) {
         leaves.clear();
         gemms.clear();
-        for (int k = 0; k < nmats; ++k) {
-            if (r >= p.chains[k].size()) continue;
-            const Op &op = p.chains[k][r];
+        for (const auto &ki : p.rounds[r]) {
+            const Op &op = p.chains[ki.first][ki.second];
             if (op.leaf) leaves.push_back(op.lj); else gemms.push_back(op.g);
         }
         if (!leaves.empty() && (s = leaf_launch(leaves, st)) != KFAC_OK) return s;
