@@ -24,9 +24,8 @@
 //        X11 <- X11 - X12 T^T     (symmetric: upper tiles + mirror)
 //      The GEMMs run on tcgen05 with three tf32 products per slice
 //      (hi*hi + hi*lo + lo*hi) and fp32 accumulation.  Leaves are 128 x 128
-//      blocks inverted by one CTA with the matrix in registers: Cholesky
-//      X = U^T U, triangular inverse V = U^-1, then V V^T, each step one
-//      barrier with the pivot row broadcast through shared memory;
+//      blocks inverted by one CTA in shared memory, by the same block
+//      elimination taken down to 32 x 32 pivot blocks (leaf_kernel);
 //   4. out = hi + lo of the upper triangle mirrored to the lower one (exact
 //      symmetry), plus the optional bf16 copy.
 // A pivot that is not positive and finite records its 1-based index in
@@ -202,26 +201,25 @@ struct LeafParams {
     int n;
 };
 
-// In-place inverse of one SPD 128 x 128 block, one CTA of 512 threads, the
-// block in shared memory, blocked by 32-wide panels:
-//   A. Cholesky X = U^T U: per panel p, warp 0 factors the 32 x 32 diagonal
-//      block in registers (one column per lane, pivots and row broadcasts by
-//      warp shuffles), then the panel row is solved (U_pp^T U_pq = X_pq, one
-//      column per thread) and the trailing matrix gets the rank-32 update
-//      X_qr -= U_pq^T U_pr (all threads, register tiles);
-//   B. V = U^-1: four warps invert the four diagonal blocks with shuffles,
-//      then V_pq = -V_pp (sum_{p<r<=q} U_pr V_rq) one block diagonal at a time;
-//   C. X^-1 = V V^T, written back as a (hi, lo) pair.
+// In-place inverse of one SPD 128 x 128 block (one CTA of 512 threads, the
+// block in shared memory) by blocked Gauss-Jordan elimination with 32-wide
+// pivot blocks -- the same block elimination as the Schur-complement
+// recursion around it, taken down to 32 x 32 pivots; no pivoting is needed
+// because every pivot block of an SPD matrix is SPD.  For p = 0..3:
+//   P^-1  one warp inverts the 32 x 32 pivot block in registers (one column
+//         per lane, Gauss-Jordan steps with the pivot column broadcast by
+//         warp shuffles);
+//   Q     the row panel [P^-1 X_p,j (j outside p) | P^-1] (all threads);
+//   X     X_i,j -= X_i,p Q_p,j for rows i outside p, with X_i,p taken as 0
+//         inside the pivot columns (this also forms -X_i,p P^-1), and the
+//         pivot row panel becomes Q.
 __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_constant__ LeafParams P) {
-    constexpr int N = LEAF, LS = LEAF + 1, PW = 32;
-    constexpr int WP = LEAF + 4;     // pitch of V^T for 16-byte row loads
+    constexpr int N = LEAF, LS = LEAF + 1, PW = 32, QS = LEAF + 4, CS = PW + 1;
     extern __shared__ __align__(16) float smem_leaf[];
-    float *V = smem_leaf;            // N x LS: V = U^-1 (upper)
-    float *S = V + N * LS;           // N x LS: the block, U in its upper triangle
-    float *T = S + N * LS;           // 3 x PW x (PW+1): block temporaries
-    float *W = S;                    // N x WP: V^T, overlays S and T once they are free
+    float *S = smem_leaf;            // N x LS: the block
+    float *Q = S + N * LS;           // PW x QS: row panel of the current step
+    float *Cb = Q + PW * QS;         // (N - PW) x CS: pivot columns of the other rows
     __shared__ int bad;
-    __shared__ float rdiag[N];
     const LeafJob &J = P.j[blockIdx.x];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned FULL = 0xffffffffu;
@@ -233,204 +231,101 @@ __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_cons
     }
     __syncthreads();
 
-    // ---------------------------------------------------------- A. Cholesky
     for (int p = 0; p < N / PW; ++p) {
         const int o = p * PW;
+        // ---- pivot block inverse (warp 0), written into Q's pivot columns
         if (warp == 0) {
-            float d[PW];  // column `lane` of the diagonal block, rows 0..31 (upper part)
+            float c[PW];  // column `lane` of the pivot block
 #pragma unroll
-            for (int i = 0; i < PW; ++i) d[i] = (i <= lane) ? S[(o + i) * LS + o + lane] : 0.f;
+            for (int i = 0; i < PW; ++i) c[i] = S[(o + i) * LS + o + lane];
 #pragma unroll
             for (int k = 0; k < PW; ++k) {
-                const float piv = __shfl_sync(FULL, d[k], k);
+                const float piv = __shfl_sync(FULL, c[k], k);
                 const bool ok = piv > 0.f && isfinite(piv);
                 if (!ok && lane == 0 && bad < 0) bad = o + k;
-                const float rs = ok ? rsqrtf(piv) : 1.f;
-                // selects, not branches: per-lane predicates inside this
-                // unrolled loop would serialise the warp at every step
-                const float u = (lane >= k) ? d[k] * rs : 0.f;
-                d[k] = (lane >= k) ? u : d[k];
+                const float ip = ok ? 1.0f / piv : 0.f;
+                const float rk = c[k] * ip;  // new row k, column `lane`
 #pragma unroll
-                for (int i = 0; i < PW; ++i) {  // fixed trip count keeps d[] in registers
-                    if (i > k) {
-                        const float uki = __shfl_sync(FULL, u, i);
-                        const float t = fmaf(-uki, u, d[i]);
-                        d[i] = (lane >= i) ? t : d[i];
-                    }
+                for (int i = 0; i < PW; ++i) {
+                    const float cik = __shfl_sync(FULL, c[i], k);  // old X[i][k]
+                    float v = (lane == k) ? -cik * ip : fmaf(-cik, rk, c[i]);
+                    if (i == k) v = (lane == k) ? ip : rk;
+                    c[i] = v;
                 }
             }
 #pragma unroll
-            for (int i = 0; i < PW; ++i) {
-                const float keep = S[(o + i) * LS + o + lane];
-                S[(o + i) * LS + o + lane] = (i <= lane) ? d[i] : keep;
-            }
-            rdiag[o + lane] = 1.0f / S[(o + lane) * LS + o + lane];  // 1 / U[i][i] for the panel solve
+            for (int i = 0; i < PW; ++i) Q[i * QS + o + lane] = c[i];
         }
         __syncthreads();
-        const int c0 = o + PW, m = N - c0;  // trailing columns [c0, N)
-        if (m == 0) break;
-        // panel row: U_pp^T X = A_p,trail, one column per thread (forward
-        // substitution, column-oriented)
-        if (tid < m) {
-            const int j = c0 + tid;
-            float x[PW];
+        // ---- row panel: Q[l][j] = sum_m Pinv[l][m] X[o+m][j] for j outside the pivot block
+        if (tid < 4 * (N - PW)) {
+            const int rg = tid / (N - PW), jj = tid % (N - PW);  // rg uniform within a warp
+            const int j = jj < o ? jj : jj + PW;
+            float acc[8];
 #pragma unroll
-            for (int i = 0; i < PW; ++i) x[i] = S[(o + i) * LS + j];
+            for (int r = 0; r < 8; ++r) acc[r] = 0.f;
+#pragma unroll 4
+            for (int m = 0; m < PW; ++m) {
+                const float x = S[(o + m) * LS + j];
 #pragma unroll
-            for (int i = 0; i < PW; ++i) {
-                x[i] *= rdiag[o + i];
-#pragma unroll
-                for (int l = i + 1; l < PW; ++l) x[l] = fmaf(-S[(o + i) * LS + o + l], x[i], x[l]);
+                for (int r = 0; r < 8; ++r) acc[r] = fmaf(Q[(8 * rg + r) * QS + o + m], x, acc[r]);
             }
 #pragma unroll
-            for (int i = 0; i < PW; ++i) S[(o + i) * LS + j] = x[i];
+            for (int r = 0; r < 8; ++r) Q[(8 * rg + r) * QS + j] = acc[r];
+        }
+        // pivot columns of the other rows, before they are overwritten
+        for (int e = tid; e < (N - PW) * PW; e += LEAF_THREADS) {
+            const int ii = e / PW, m = e % PW, i = ii < o ? ii : ii + PW;
+            Cb[ii * CS + m] = S[i * LS + o + m];
         }
         __syncthreads();
-        // rank-32 trailing update: rows c0 + ty + 16 r, columns c0 + tx + 32 c
+        // ---- elimination: rows outside the pivot block, all 128 columns
         {
-            const int ty = tid >> 5, tx = tid & 31;
-            const int nr = m / 16, nc = m / 32;  // 6x3, 4x2, 2x1 per thread
-            float acc[6][3];
+            const int ty = tid >> 5, tx = lane;
+            float acc[6][4];
 #pragma unroll
             for (int r = 0; r < 6; ++r)
 #pragma unroll
-                for (int c = 0; c < 3; ++c) acc[r][c] = 0.f;
-            for (int l = 0; l < PW; ++l) {
-                const float *row = S + (o + l) * LS + c0;
-                float ai[6], bj[3];
+                for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+#pragma unroll 4
+            for (int m = 0; m < PW; ++m) {
+                float a[6], q[4];
 #pragma unroll
-                for (int r = 0; r < 6; ++r) ai[r] = (r < nr) ? row[ty + 16 * r] : 0.f;
+                for (int r = 0; r < 6; ++r) a[r] = Cb[(ty + 16 * r) * CS + m];
 #pragma unroll
-                for (int c = 0; c < 3; ++c) bj[c] = (c < nc) ? row[tx + 32 * c] : 0.f;
+                for (int c = 0; c < 4; ++c) q[c] = Q[m * QS + tx + 32 * c];
 #pragma unroll
                 for (int r = 0; r < 6; ++r)
 #pragma unroll
-                    for (int c = 0; c < 3; ++c) acc[r][c] = fmaf(ai[r], bj[c], acc[r][c]);
+                    for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], q[c], acc[r][c]);
             }
 #pragma unroll
-            for (int r = 0; r < 6; ++r)
+            for (int r = 0; r < 6; ++r) {
+                const int ii = ty + 16 * r, i = ii < o ? ii : ii + PW;
 #pragma unroll
-                for (int c = 0; c < 3; ++c)
-                    if (r < nr && c < nc) S[(c0 + ty + 16 * r) * LS + c0 + tx + 32 * c] -= acc[r][c];
+                for (int c = 0; c < 4; ++c) {
+                    const int j = tx + 32 * c;
+                    const bool inpiv = (j >= o) && (j < o + PW);
+                    const float base = inpiv ? 0.f : S[i * LS + j];
+                    S[i * LS + j] = base - acc[r][c];
+                }
+            }
+            // the pivot row panel becomes Q
+            for (int e = tid; e < PW * N; e += LEAF_THREADS) {
+                const int m = e >> 7, j = e & 127;
+                S[(o + m) * LS + j] = Q[m * QS + j];
+            }
         }
         __syncthreads();
     }
 
-    // ---------------------------------------------------------- B. V = U^-1
-    if (warp < N / PW) {  // diagonal blocks, one warp each
-        const int o = warp * PW;
-        float u[PW], r[PW];
-#pragma unroll
-        for (int i = 0; i < PW; ++i) {
-            u[i] = (i <= lane) ? S[(o + i) * LS + o + lane] : 0.f;
-            r[i] = (i == lane) ? 1.f : 0.f;
-        }
-#pragma unroll
-        for (int k = PW - 1; k >= 0; --k) {
-            const float ukk = __shfl_sync(FULL, u[k], k);
-            const float v = r[k] / ukk;
-            r[k] = v;
-#pragma unroll
-            for (int i = 0; i < k; ++i) {
-                const float uik = __shfl_sync(FULL, u[i], k);
-                r[i] = fmaf(-uik, v, r[i]);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < PW; ++i) V[(o + i) * LS + o + lane] = (i <= lane) ? r[i] : 0.f;
-    }
-    __syncthreads();
-    // off-diagonal blocks V_pq, q = p + dd: T_pq = sum_{p<r<=q} U_pr V_rq, then
-    // V_pq = -V_pp T_pq.  Warp w takes rows w, w+16, ... of the nb*32 block
-    // rows on this diagonal, lane = column; independent accumulators per row.
-    for (int dd = 1; dd < N / PW; ++dd) {
-        const int nb = N / PW - dd, rows = nb * PW, per = rows / 16;  // 6, 4, 2 rows per warp
-        float t[6];
-#pragma unroll
-        for (int k = 0; k < 6; ++k) t[k] = 0.f;
-#pragma unroll
-        for (int k = 0; k < 6; ++k) {
-            if (k < per) {
-                const int gr = warp + 16 * k, b = gr / PW, i = gr % PW, p = b, q = b + dd;
-                float sum = 0.f;
-                for (int rr = p + 1; rr <= q; ++rr)
-#pragma unroll 8
-                    for (int l = 0; l < PW; ++l)
-                        sum = fmaf(S[(p * PW + i) * LS + rr * PW + l], V[(rr * PW + l) * LS + q * PW + lane], sum);
-                t[k] = sum;
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 6; ++k)
-            if (k < per) {
-                const int gr = warp + 16 * k, b = gr / PW, i = gr % PW;
-                T[(b * PW + i) * (PW + 1) + lane] = t[k];
-            }
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < 6; ++k) {
-            if (k < per) {
-                const int gr = warp + 16 * k, b = gr / PW, i = gr % PW, p = b;
-                float sum = 0.f;
-#pragma unroll 8
-                for (int l = 0; l < PW; ++l)
-                    sum = fmaf(V[(p * PW + i) * LS + p * PW + l], T[(b * PW + l) * (PW + 1) + lane], sum);
-                t[k] = -sum;
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 6; ++k)
-            if (k < per) {
-                const int gr = warp + 16 * k, b = gr / PW, i = gr % PW, p = b, q = b + dd;
-                V[(p * PW + i) * LS + q * PW + lane] = t[k];
-            }
-        __syncthreads();
-    }
-    // lower blocks of V are zero
     for (int e = tid; e < N * N; e += LEAF_THREADS) {
         const int i = e >> 7, j = e & 127;
-        if ((i >> 5) > (j >> 5)) V[i * LS + j] = 0.f;
-    }
-    __syncthreads();
-
-    // ---------------------------------------------------------- C. V V^T
-    // W = V^T (W[l][i] = V[i][l], zero for l < i); X[i][j] = sum_l W[l][i] W[l][j].
-    // Warp w owns rows 8w..8w+7 (one broadcast float4 pair per l, and no
-    // work for l < 8w), lane owns columns lane + 32 c.
-    for (int e = tid; e < N * N; e += LEAF_THREADS) {
-        const int l = e >> 7, i = e & 127;
-        W[l * WP + i] = V[i * LS + l];
-    }
-    __syncthreads();
-    {
-        float x[8][4];
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) x[r][c] = 0.f;
-        const int r0 = 8 * warp;
-        for (int l = r0; l < N; ++l) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(W + l * WP + r0);
-            const float4 a1 = *reinterpret_cast<const float4 *>(W + l * WP + r0 + 4);
-            const float vi[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            float vj[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) vj[c] = W[l * WP + lane + 32 * c];
-#pragma unroll
-            for (int r = 0; r < 8; ++r)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) x[r][c] = fmaf(vi[r], vj[c], x[r][c]);
-        }
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int i = r0 + r, j = lane + 32 * c;
-                const long long o = (long long)i * J.ld + j;
-                const float h = tf32_hi(x[r][c]);
-                J.Xh[o] = h;
-                J.Xl[o] = x[r][c] - h;
-            }
+        const long long o = (long long)i * J.ld + j;
+        const float v = S[i * LS + j];
+        const float h = tf32_hi(v);
+        J.Xh[o] = h;
+        J.Xl[o] = v - h;
     }
     if (tid == 0 && bad >= 0 && J.info) atomicCAS(J.info, 0, J.o + bad + 1);
 }
@@ -605,7 +500,8 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
     return KFAC_OK;
 }
 
-constexpr size_t LEAF_SMEM = (2 * (size_t)LEAF * (LEAF + 1) + 3 * 32 * 33) * sizeof(float);
+constexpr size_t LEAF_SMEM =
+    ((size_t)LEAF * (LEAF + 1) + 32 * (LEAF + 4) + (LEAF - 32) * 33) * sizeof(float);
 
 kfac_status leaf_launch(const std::vector<LeafJob> &jobs, cudaStream_t st) {
     static std::once_flag once;
