@@ -50,7 +50,8 @@ struct TcJob {
 };
 
 // Tensor map of a row-major [rows][cols] matrix (ld elements) for the engine:
-// 128-byte swizzle, box 128 bytes wide and 128 rows (64 rows if mn_major).
+// 128-byte swizzle, box 128 bytes wide and 128 rows (64 rows if mn_major, 32
+// rows for tf32).
 bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int mn_major);
 // Copies host-built maps into device memory (128-byte aligned) on the stream.
 kfac_status tc_upload_maps(const CUtensorMap *maps, int n, CUtensorMap *dev, cudaStream_t st);

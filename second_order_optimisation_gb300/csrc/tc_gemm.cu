@@ -42,7 +42,7 @@ constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_PROBS = 192;
 constexpr int MAPS_PER_COPY = 240;
-constexpr int STAGE_LD = 33;                              // epilogue staging row pitch (floats)
+constexpr int STAGE_LD = 36;                              // epilogue staging row pitch (floats)
 constexpr size_t EPI_STAGE_BYTES = 4 * 32 * STAGE_LD * sizeof(float);
 constexpr size_t SMEM_BYTES = 192 * 1024 + 1024 /*align*/ + 256 /*barriers*/ + EPI_STAGE_BYTES;
 
@@ -56,11 +56,15 @@ template <> struct Traits<TC_KIND_TF32X3> {
 
 struct TcProb {
     int map_a, map_b;        // map indices; tf32x3: hi at map, lo at map + 1
-    int a_mn, b_mn;          // MN-major operand (bf16 only)
     int a_row0, a_col0;      // operand sub-block origin inside its map (rows, columns)
     int b_row0, b_col0;
     int M, N, k_tiles;
-    int tiles_n, syrk, sym, ksplit, work_begin, epi;
+    int bn;                  // output tile width: 128, or 64 / 32 to spread small problems over SMs
+    int tiles_n, ksplit, work_begin;
+    uint8_t a_mn, b_mn;      // MN-major operand (bf16 only)
+    uint8_t syrk, sym, epi;
+    uint8_t vec;             // C (and C_lo) rows take 16-byte accesses (ldc % 4 == 0, aligned)
+    uint8_t vecb;            // Cb rows take 8-byte accesses
     float alpha, beta;
     float *C;
     float *C_lo;
@@ -119,10 +123,13 @@ __device__ __forceinline__ Work decode_work(const TcParams &P, int w) {
     k.tile = local / q.ksplit;
     k.split = local - k.tile * q.ksplit;
     if (q.syrk || q.sym) {
-        int T = q.tiles_n, t = k.tile, tm = 0;
-        while (t >= T - tm) { t -= T - tm; ++tm; }
+        // upper tiles only: row block tm (128 rows) runs column blocks from the
+        // one holding its diagonal (r = 128 / bn blocks per diagonal block)
+        const int r = BM / q.bn, T = q.tiles_n;
+        int t = k.tile, tm = 0;
+        while (t >= T - tm * r) { t -= T - tm * r; ++tm; }
         k.tm = tm;
-        k.tn = tm + t;
+        k.tn = tm * r + t;
     } else {
         k.tm = k.tile / q.tiles_n;
         k.tn = k.tile - k.tm * q.tiles_n;
@@ -134,6 +141,13 @@ __device__ __forceinline__ Work decode_work(const TcParams &P, int w) {
 
 __device__ __forceinline__ void acquire_map(const CUtensorMap *m) {
     asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"((uint64_t)m) : "memory");
+}
+
+// tf32 operand rows [mn0, mn0 + rows) x K [k0, k0 + 32) as 32-row boxes
+// (128-byte rows; 32 rows keep the 8-row swizzle atoms of one tall box).
+__device__ __forceinline__ void load_rows_tf32(uint8_t *dst, const CUtensorMap *map, int row0, int col0, int mn0,
+                                               int rows, int k0, uint64_t *bar) {
+    for (int r = 0; r < rows; r += 32) tma_load_2d(dst + r * 128, map, col0 + k0, row0 + mn0 + r, bar);
 }
 
 // One 128 (M or N) x BK (K) operand tile into shared memory.
@@ -163,15 +177,61 @@ __device__ __forceinline__ float tf32_hi(float v) {
     return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
 }
 
-// Epilogue of one 32 x 32 chunk by one warp.  On entry lane l holds row
-// i0 + l, columns j0 .. j0+31 (the TMEM layout).  The transposed copy (if any)
-// is written straight from that layout (coalesced: consecutive lanes are
-// consecutive addresses of Ct); the row-major output goes through a per-warp
-// shared-memory transpose so that each store instruction covers 32
-// consecutive columns of one row.  Old values (beta != 0) are loaded for all
-// 32 rows before any store.
+// Epilogue data layout.  A warp owns 32 accumulator rows (its TMEM lane
+// quarter) and handles them in 32 x 32 chunks.  tcgen05.ld gives lane l row
+// i0 + l; the chunk is restaged through shared memory so that lane l then
+// holds row i0 + 4k + l/8, columns j0 + 4(l%8) .. +3 for k = 0..7: every
+// global access is 16 bytes and a warp instruction covers four 128-byte rows.
+// Old values of C (beta != 0) use the same layout, so they can be fetched
+// before the accumulator is ready.
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ float4 tf32_hi4(float4 v) {
+    return make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
+}
+__device__ __forceinline__ float4 sub4(float4 a, float4 b) {
+    return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w);
+}
+__device__ __forceinline__ float comp(float4 v, int t) { return t == 0 ? v.x : t == 1 ? v.y : t == 2 ? v.z : v.w; }
+
+// Old values of the chunk at (i0, j0) (zeros where beta == 0 or out of range).
+__device__ __forceinline__ void load_old(const TcProb &q, int i0, int j0, int lane, float4 (&oh)[8],
+                                         float4 (&ol)[8]) {
+    const int j = j0 + 4 * (lane & 7);
+    const bool need = q.beta != 0.f && q.epi != TC_EPI_STORE;
+    const bool lo = q.epi == TC_EPI_SPLIT;
+    const bool full = q.vec && j + 3 < q.N;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int i = i0 + 4 * k + (lane >> 3);
+        float4 h = make_float4(0.f, 0.f, 0.f, 0.f), l = h;
+        if (need && i < q.M) {
+            const long long off = (long long)i * q.ldc + j;
+            if (full) {
+                h = ld4(q.C + off);
+                if (lo) l = ld4(q.C_lo + off);
+            } else {
+                float hv[4] = {0.f, 0.f, 0.f, 0.f}, lv[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int t = 0; t < 4; ++t)
+                    if (j + t < q.N) {
+                        hv[t] = q.C[off + t];
+                        if (lo) lv[t] = q.C_lo[off + t];
+                    }
+                h = make_float4(hv[0], hv[1], hv[2], hv[3]);
+                l = make_float4(lv[0], lv[1], lv[2], lv[3]);
+            }
+        }
+        oh[k] = h;
+        ol[k] = l;
+    }
+}
+
+// Epilogue of one 32 x 32 chunk by one warp: v is the TMEM layout (lane =
+// row), oh / ol the old values from load_old.  The transposed copy Ct (if any)
+// is written straight from v (consecutive lanes are consecutive addresses of
+// Ct); the mirror of a symmetric off-diagonal tile goes back through the stage.
 __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, const float *v, float *stage,
-                                            int lane, bool mirror) {
+                                            int lane, bool mirror, float4 (&oh)[8], float4 (&ol)[8]) {
     const float a = q.alpha, b = q.beta;
     if (q.epi == TC_EPI_SPLIT && q.Ct) {  // host guarantees beta == 0 here
         const int i = i0 + lane;
@@ -188,69 +248,98 @@ __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, con
         }
     }
 #pragma unroll
-    for (int c = 0; c < 32; ++c) stage[lane * STAGE_LD + c] = v[c];
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4 *>(&stage[lane * STAGE_LD + 4 * c]) =
+            make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
     __syncwarp();
-    const int j = j0 + lane;
-    const bool jok = j < q.N;
-    float acc[32], old[32];
+    float4 acc[8];
+    const int sl = (lane >> 3) * STAGE_LD + 4 * (lane & 7);
 #pragma unroll
-    for (int r = 0; r < 32; ++r) acc[r] = stage[r * STAGE_LD + lane];
+    for (int k = 0; k < 8; ++k) acc[k] = *reinterpret_cast<const float4 *>(&stage[4 * k * STAGE_LD + sl]);
     __syncwarp();
+    const int j = j0 + 4 * (lane & 7);
+    const bool full = q.vec && j + 3 < q.N;
     if (q.epi == TC_EPI_ACCUM) {
         const bool upper = q.syrk;
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const int i = i0 + r;
-            old[r] = (b != 0.f && jok && i < q.M && (!upper || j >= i)) ? q.C[(long long)i * q.ldc + j] : 0.f;
-        }
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const int i = i0 + r;
-            if (jok && i < q.M && (!upper || j >= i)) q.C[(long long)i * q.ldc + j] = fmaf(b, old[r], a * acc[r]);
+        for (int k = 0; k < 8; ++k) {
+            const int i = i0 + 4 * k + (lane >> 3);
+            if (i >= q.M) continue;
+            const float4 o = make_float4(fmaf(b, oh[k].x, a * acc[k].x), fmaf(b, oh[k].y, a * acc[k].y),
+                                         fmaf(b, oh[k].z, a * acc[k].z), fmaf(b, oh[k].w, a * acc[k].w));
+            float *dst = q.C + (long long)i * q.ldc + j;
+            if (full && (!upper || j >= i)) {
+                st4(dst, o);
+            } else {
+                for (int t = 0; t < 4; ++t)
+                    if (j + t < q.N && (!upper || j + t >= i)) dst[t] = comp(o, t);
+            }
         }
     } else if (q.epi == TC_EPI_STORE) {
+        const bool fullb = q.vecb && j + 3 < q.N;
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const int i = i0 + r;
-            if (jok && i < q.M) {
-                const float o = a * acc[r];
-                if (q.C) q.C[(long long)i * q.ldc + j] = o;
-                if (q.Cb) q.Cb[(long long)i * q.ldcb + j] = f32_to_bf16_bits(o);
+        for (int k = 0; k < 8; ++k) {
+            const int i = i0 + 4 * k + (lane >> 3);
+            if (i >= q.M) continue;
+            const float4 o = make_float4(a * acc[k].x, a * acc[k].y, a * acc[k].z, a * acc[k].w);
+            if (q.C) {
+                float *dst = q.C + (long long)i * q.ldc + j;
+                if (full) {
+                    st4(dst, o);
+                } else {
+                    for (int t = 0; t < 4; ++t)
+                        if (j + t < q.N) dst[t] = comp(o, t);
+                }
+            }
+            if (q.Cb) {
+                uint16_t *dst = q.Cb + (long long)i * q.ldcb + j;
+                if (fullb) {
+                    const uint32_t lo2 = f32_to_bf16_bits(o.x) | ((uint32_t)f32_to_bf16_bits(o.y) << 16);
+                    const uint32_t hi2 = f32_to_bf16_bits(o.z) | ((uint32_t)f32_to_bf16_bits(o.w) << 16);
+                    *reinterpret_cast<uint2 *>(dst) = make_uint2(lo2, hi2);
+                } else {
+                    for (int t = 0; t < 4; ++t)
+                        if (j + t < q.N) dst[t] = f32_to_bf16_bits(comp(o, t));
+                }
             }
         }
     } else {  // TC_EPI_SPLIT
-        float oldl[32];
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const int i = i0 + r;
-            const bool ok = b != 0.f && jok && i < q.M;
-            old[r] = ok ? q.C[(long long)i * q.ldc + j] : 0.f;
-            oldl[r] = ok ? q.C_lo[(long long)i * q.ldc + j] : 0.f;
-        }
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const int i = i0 + r;
-            const float o = fmaf(b, old[r] + oldl[r], a * acc[r]);
-            const float h = tf32_hi(o);
-            old[r] = h;       // keep the final pair for the mirror below
-            oldl[r] = o - h;
-            if (jok && i < q.M) {
-                q.C[(long long)i * q.ldc + j] = h;
-                q.C_lo[(long long)i * q.ldc + j] = o - h;
+        for (int k = 0; k < 8; ++k) {
+            const int i = i0 + 4 * k + (lane >> 3);
+            const float4 o = make_float4(fmaf(b, oh[k].x + ol[k].x, a * acc[k].x),
+                                         fmaf(b, oh[k].y + ol[k].y, a * acc[k].y),
+                                         fmaf(b, oh[k].z + ol[k].z, a * acc[k].z),
+                                         fmaf(b, oh[k].w + ol[k].w, a * acc[k].w));
+            const float4 h = tf32_hi4(o), l = sub4(o, h);
+            oh[k] = h;  // the final pair, kept for the mirror below
+            ol[k] = l;
+            if (i >= q.M) continue;
+            const long long off = (long long)i * q.ldc + j;
+            if (full) {
+                st4(q.C + off, h);
+                st4(q.C_lo + off, l);
+            } else {
+                for (int t = 0; t < 4; ++t)
+                    if (j + t < q.N) {
+                        q.C[off + t] = comp(h, t);
+                        q.C_lo[off + t] = comp(l, t);
+                    }
             }
         }
         if (mirror) {
             // symmetric output: this upper tile also fills its transposed
-            // position; go back through the stage so that lane = row and every
-            // store covers 32 consecutive columns of C[j][i0 .. i0+31]
+            // position; lane = row i0 + lane again, so that every store covers
+            // 32 consecutive columns of C[j][i0 .. i0+31]
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
                 float *dst = part ? q.C_lo : q.C;
 #pragma unroll
-                for (int r = 0; r < 32; ++r) stage[r * STAGE_LD + lane] = part ? oldl[r] : old[r];
+                for (int k = 0; k < 8; ++k)
+                    *reinterpret_cast<float4 *>(&stage[4 * k * STAGE_LD + sl]) = part ? ol[k] : oh[k];
                 __syncwarp();
                 const int i = i0 + lane;
-#pragma unroll 4
+#pragma unroll 8
                 for (int c = 0; c < 32; ++c) {
                     const int jj = j0 + c;
                     if (i < q.M && jj < q.N) dst[(long long)jj * q.ldc + i] = stage[lane * STAGE_LD + c];
@@ -318,7 +407,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     last_p = k.p;
                 }
                 const bool diag = KIND == TC_KIND_BF16 && q.syrk && k.tm == k.tn;
-                const uint32_t bytes = diag ? TILE_BYTES : STAGE_BYTES;
+                const uint32_t bytes = KIND == TC_KIND_TF32X3 ? (uint32_t)(2 * (BM + q.bn) * 128)
+                                       : diag                 ? (uint32_t)TILE_BYTES
+                                                              : (uint32_t)STAGE_BYTES;
                 for (int kt = k.kt0; kt < k.kt1; ++kt) {
                     if (!mbar_wait(&empty[stage], phase ^ 1)) {
                         atomicOr(P.error, ERR_TIMEOUT_EMPTY);
@@ -334,11 +425,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                             load_tile(sa + TILE_BYTES, mb, q.b_mn, q.b_row0, q.b_col0, k.tn * BN, k0,
                                       &full[stage]);
                     } else {
-                        load_tile(sa, ma, 0, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
-                        load_tile(sa + TILE_BYTES, ma + 1, 0, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
-                        load_tile(sa + 2 * TILE_BYTES, mb, 0, q.b_row0, q.b_col0, k.tn * BN, k0, &full[stage]);
-                        load_tile(sa + 3 * TILE_BYTES, mb + 1, 0, q.b_row0, q.b_col0, k.tn * BN, k0,
-                                  &full[stage]);
+                        load_rows_tf32(sa, ma, q.a_row0, q.a_col0, k.tm * BM, BM, k0, &full[stage]);
+                        load_rows_tf32(sa + TILE_BYTES, ma + 1, q.a_row0, q.a_col0, k.tm * BM, BM, k0, &full[stage]);
+                        load_rows_tf32(sa + 2 * TILE_BYTES, mb, q.b_row0, q.b_col0, k.tn * q.bn, q.bn, k0,
+                                       &full[stage]);
+                        load_rows_tf32(sa + 3 * TILE_BYTES, mb + 1, q.b_row0, q.b_col0, k.tn * q.bn, q.bn, k0,
+                                       &full[stage]);
                     }
                     if (++stage == Tr::STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -363,7 +455,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + b * BN;
                 const uint32_t idesc = KIND == TC_KIND_BF16 ? idesc_bf16_f32(BM, BN, q.a_mn, q.b_mn)
-                                                            : idesc_tf32_f32(BM, BN);
+                                                            : idesc_tf32_f32(BM, q.bn);
                 bool ok = true;
                 for (int kt = k.kt0; kt < k.kt1; ++kt) {
                     if (!mbar_wait(&full[stage], phase)) {
@@ -410,6 +502,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             const TcProb &q = P.prob[k.p];
             const int b = it & 1;
             const uint32_t use = (uint32_t)(it >> 1);
+            const int i0 = k.tm * BM + quarter * 32;
+            const int nch = q.bn / 32;
+            const bool mirror = q.sym && k.tn >= (k.tm + 1) * (BM / q.bn);
+            float4 oh[8], ol[8];
+            // the first chunk's old values load while the MMAs run
+            if (q.ksplit == 1) load_old(q, i0, k.tn * q.bn, lane, oh, ol);
             if (!mbar_wait(&accf[b], use & 1)) {
                 atomicOr(P.error, ERR_TIMEOUT_ACC);
                 *abort_flag = 1;
@@ -417,20 +515,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             }
             tc_fence_after();
             const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + b * BN;
-            const int i0 = k.tm * BM + quarter * 32;
             if (q.ksplit == 1) {
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = 0; c < nch; ++c) {
+                    if (c > 0) load_old(q, i0, k.tn * q.bn + c * 32, lane, oh, ol);
                     float v[32];
                     tmem_ld_32x32b_x32(t_row + c * 32, v);
-                    chunk_store(q, i0, k.tn * BN + c * 32, v, stage, lane, q.sym && k.tm != k.tn);
+                    chunk_store(q, i0, k.tn * q.bn + c * 32, v, stage, lane, mirror, oh, ol);
                 }
                 tc_fence_before();
                 mbar_arrive(&acce[b]);
             } else {
                 float4 *part = (float4 *)(q.partial + ((long long)k.tile * q.ksplit + k.split) * (BM * BN));
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = 0; c < nch; ++c) {
                     float v[32];
                     tmem_ld_32x32b_x32(t_row + c * 32, v);
 #pragma unroll
@@ -452,7 +550,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     __threadfence();
                     const float4 *base = (const float4 *)(q.partial + (long long)k.tile * q.ksplit * (BM * BN));
 #pragma unroll 1
-                    for (int c = 0; c < BN / 32; ++c) {
+                    for (int c = 0; c < nch; ++c) {
+                        load_old(q, i0, k.tn * q.bn + c * 32, lane, oh, ol);
                         float v[32];
 #pragma unroll
                         for (int t = 0; t < 32; ++t) v[t] = 0.f;
@@ -464,7 +563,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                                 v[4 * f] += t.x; v[4 * f + 1] += t.y; v[4 * f + 2] += t.z; v[4 * f + 3] += t.w;
                             }
                         }
-                        chunk_store(q, i0, k.tn * BN + c * 32, v, stage, lane, q.sym && k.tm != k.tn);
+                        chunk_store(q, i0, k.tn * q.bn + c * 32, v, stage, lane, mirror, oh, ol);
                     }
                     if (etid == 0) q.counters[k.tile] = 0;
                 }
@@ -482,6 +581,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 // ------------------------------------------------------------------ host
 
 struct Plan {
+    int bn = BN;               // output tile width of every job in the call
     std::vector<int> order;    // job indices in launch order
     std::vector<int> ksplit;   // per job
     std::vector<int> tiles;    // per job
@@ -490,9 +590,13 @@ struct Plan {
 
 int bk_of(int kind) { return kind == TC_KIND_BF16 ? Traits<TC_KIND_BF16>::BK : Traits<TC_KIND_TF32X3>::BK; }
 
-int tiles_of(const TcJob &j) {
-    int tm = (int)ceil_div(j.M, BM), tn = (int)ceil_div(j.N, BN);
-    return (j.syrk || j.sym) ? tn * (tn + 1) / 2 : tm * tn;
+int tiles_of(const TcJob &j, int bn) {
+    const int tm = (int)ceil_div(j.M, BM), tn = (int)ceil_div(j.N, bn);
+    if (!(j.syrk || j.sym)) return tm * tn;
+    const int r = BM / bn;  // upper tiles: row block t runs column blocks t*r .. tn-1
+    int n = 0;
+    for (int t = 0; t < tm; ++t) n += std::max(0, tn - t * r);
+    return n;
 }
 
 Plan make_plan(const TcJob *jobs, int n, int kind) {
@@ -500,13 +604,24 @@ Plan make_plan(const TcJob *jobs, int n, int kind) {
     p.ksplit.resize(n);
     p.tiles.resize(n);
     p.k_tiles.resize(n);
+    const int sms = device_sm_count();
+    // A launch with few 128-wide tiles leaves most SMs idle and funnels each
+    // tile's loads and stores through one SM: narrow the tiles (tf32x3 only)
+    // until the launch covers at least half of the SMs.
+    if (kind == TC_KIND_TF32X3) {
+        for (;;) {
+            long long t = 0;
+            for (int i = 0; i < n; ++i) t += tiles_of(jobs[i], p.bn);
+            if (p.bn == 32 || 2 * t >= sms) break;
+            p.bn /= 2;
+        }
+    }
     double total = 0.0;
     for (int i = 0; i < n; ++i) {
-        p.tiles[i] = tiles_of(jobs[i]);
+        p.tiles[i] = tiles_of(jobs[i], p.bn);
         p.k_tiles[i] = (int)ceil_div(jobs[i].K, bk_of(kind));
         total += (double)p.tiles[i] * p.k_tiles[i];
     }
-    const int sms = device_sm_count();
     // Split K only where one problem's tiles would otherwise be the critical
     // path: the longest work item should not exceed about twice the average
     // share of one SM.  A split costs a partial-tile round trip through L2, so
@@ -573,7 +688,8 @@ bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int ro
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ld * esz};
     const cuuint32_t inner = 128u / esz;  // 128-byte rows
-    cuuint32_t box[2] = {inner, mn_major ? 64u : 128u};
+    // tf32 operands are fetched in 32-row boxes (tiles 32, 64 or 128 wide)
+    cuuint32_t box[2] = {inner, mn_major ? 64u : kind == TC_KIND_TF32X3 ? 32u : 128u};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = enc(m, kind == TC_KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                      2, (void *)ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -639,7 +755,8 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
             q.M = j.M;
             q.N = j.N;
             q.k_tiles = p.k_tiles[ji];
-            q.tiles_n = (int)ceil_div(j.N, BN);
+            q.bn = p.bn;
+            q.tiles_n = (int)ceil_div(j.N, p.bn);
             q.syrk = j.syrk;
             q.sym = j.sym;
             q.ksplit = p.ksplit[ji];
@@ -650,6 +767,8 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
             q.C = j.C; q.C_lo = j.C_lo; q.ldc = j.ldc;
             q.Ct = j.Ct; q.Ct_lo = j.Ct_lo; q.ldct = j.ldct;
             q.Cb = j.Cb; q.ldcb = j.ldcb;
+            q.vec = (j.ldc % 4 == 0) && ((uintptr_t)j.C % 16 == 0) && ((uintptr_t)j.C_lo % 16 == 0);
+            q.vecb = (j.ldcb % 4 == 0) && ((uintptr_t)j.Cb % 8 == 0);
             q.partial = bufs.part[ji];
             q.counters = bufs.cnt[ji];
             work += p.tiles[ji] * p.ksplit[ji];
