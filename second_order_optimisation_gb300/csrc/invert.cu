@@ -24,8 +24,8 @@
 //        X11 <- X11 - X12 T^T     (symmetric: upper tiles + mirror)
 //      The GEMMs run on tcgen05 with three tf32 products per slice
 //      (hi*hi + hi*lo + lo*hi) and fp32 accumulation.  Leaves are 128 x 128
-//      blocks inverted by one CTA in shared memory, by the same block
-//      elimination taken down to 32 x 32 pivot blocks (leaf_kernel);
+//      blocks inverted by one CTA, a Gauss-Jordan sweep with the block in
+//      registers (leaf_kernel);
 //   4. out = hi + lo of the upper triangle mirrored to the lower one (exact
 //      symmetry), plus the optional bf16 copy.
 // A pivot that is not positive and finite records its 1-based index in
@@ -42,7 +42,7 @@ namespace kfac {
 namespace {
 
 constexpr int LEAF = 128;
-constexpr int LEAF_THREADS = 512;
+constexpr int LEAF_THREADS = 256;
 constexpr int MAT_MAX = 224;
 
 inline int padded(int d) { return (int)ceil_div(d, LEAF) * LEAF; }
@@ -201,131 +201,115 @@ struct LeafParams {
     int n;
 };
 
-// In-place inverse of one SPD 128 x 128 block (one CTA of 512 threads, the
-// block in shared memory) by blocked Gauss-Jordan elimination with 32-wide
-// pivot blocks -- the same block elimination as the Schur-complement
-// recursion around it, taken down to 32 x 32 pivots; no pivoting is needed
-// because every pivot block of an SPD matrix is SPD.  For p = 0..3:
-//   P^-1  one warp inverts the 32 x 32 pivot block in registers (one column
-//         per lane, Gauss-Jordan steps with the pivot column broadcast by
-//         warp shuffles);
-//   Q     the row panel [P^-1 X_p,j (j outside p) | P^-1] (all threads);
-//   X     X_i,j -= X_i,p Q_p,j for rows i outside p, with X_i,p taken as 0
-//         inside the pivot columns (this also forms -X_i,p P^-1), and the
-//         pivot row panel becomes Q.
+// In-place inverse of one SPD 128 x 128 block by one CTA of 256 threads: a
+// Gauss-Jordan sweep with the block held in registers (warp w owns rows
+// 16w .. 16w+15, lane l columns 4l .. 4l+3).  Pivot k (in order) maps
+//   a_ij <- a_ij - a_ik a_kj / a_kk   (i, j != k)
+//   a_kj <- a_kj / a_kk,  a_ik <- -a_ik / a_kk,  a_kk <- 1 / a_kk
+// and after the last pivot the block holds its inverse.  No pivoting is
+// needed: every leading principal block of an SPD matrix is SPD.  The sweep
+// keeps the block sign-symmetric -- a_ik = -a_ki when exactly one of i, k has
+// been pivoted, a_ik = a_ki otherwise -- so every update of pivot k is formed
+// from row k alone.  The row's owner publishes it in shared memory (rowbuf:
+// a_kj; colbuf: s_j a_kj / a_kk with s_j = -1 for pivoted j, i.e. the pivot
+// column scaled), which costs one barrier per pivot.  A pivot that is not
+// positive and finite is recorded in info and eliminated as 1 / a_kk = 0.
 __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_constant__ LeafParams P) {
-    constexpr int N = LEAF, LS = LEAF + 1, PW = 32, QS = LEAF + 4, CS = PW + 1;
-    extern __shared__ __align__(16) float smem_leaf[];
-    float *S = smem_leaf;            // N x LS: the block
-    float *Q = S + N * LS;           // PW x QS: row panel of the current step
-    float *Cb = Q + PW * QS;         // (N - PW) x CS: pivot columns of the other rows
+    constexpr int N = LEAF, RW = N / (LEAF_THREADS / 32);  // 16 rows per warp
+    __shared__ __align__(16) float rowbuf[2][N];
+    __shared__ __align__(16) float colbuf[2][N];
+    __shared__ float dbuf[2];
     __shared__ int bad;
     const LeafJob &J = P.j[blockIdx.x];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned FULL = 0xffffffffu;
-    if (tid == 0) bad = -1;
-    for (int e = tid; e < N * N; e += LEAF_THREADS) {
-        const int i = e >> 7, j = e & 127;
-        const long long o = (long long)i * J.ld + j;
-        S[i * LS + j] = J.Xh[o] + J.Xl[o];
+
+    float a[RW][4];
+    {   // 16-byte pieces, every load issued before the first use (the host
+        // guarantees 16-byte aligned rows)
+        float4 h[RW], l[RW];
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            const long long o = (long long)(RW * warp + r) * J.ld + 4 * lane;
+            h[r] = *reinterpret_cast<const float4 *>(J.Xh + o);
+            l[r] = *reinterpret_cast<const float4 *>(J.Xl + o);
+        }
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            a[r][0] = h[r].x + l[r].x;
+            a[r][1] = h[r].y + l[r].y;
+            a[r][2] = h[r].z + l[r].z;
+            a[r][3] = h[r].w + l[r].w;
+        }
     }
+    if (tid == 0) bad = -1;
     __syncthreads();
 
-    for (int p = 0; p < N / PW; ++p) {
-        const int o = p * PW;
-        // ---- pivot block inverse (warp 0), written into Q's pivot columns
-        if (warp == 0) {
-            float c[PW];  // column `lane` of the pivot block
+    // Row kn (its pivot is element kn % 4 of lane kn / 4) published for the
+    // next pivot; called by the owner warp of the row.
+    auto publish = [&](int kn, const float (&row)[4], int e) {
+        const float pv = __shfl_sync(FULL, row[e], kn >> 2);
+        const bool ok = pv > 0.f && isfinite(pv);
+        const float d = ok ? __frcp_rn(pv) : 0.f;
+        if (!ok && lane == 0 && bad < 0) bad = kn;
+        const int buf = kn & 1;
+        *reinterpret_cast<float4 *>(&rowbuf[buf][4 * lane]) = make_float4(row[0], row[1], row[2], row[3]);
+        float cv[4];
 #pragma unroll
-            for (int i = 0; i < PW; ++i) c[i] = S[(o + i) * LS + o + lane];
+        for (int t = 0; t < 4; ++t) cv[t] = (4 * lane + t < kn ? -row[t] : row[t]) * d;
+        *reinterpret_cast<float4 *>(&colbuf[buf][4 * lane]) = make_float4(cv[0], cv[1], cv[2], cv[3]);
+        if (lane == 0) dbuf[buf] = d;
+    };
+
+    if (warp == 0) publish(0, a[0], 0);
+    __syncthreads();
+#pragma unroll 1
+    for (int kb = 0; kb < N / RW; ++kb) {
 #pragma unroll
-            for (int k = 0; k < PW; ++k) {
-                const float piv = __shfl_sync(FULL, c[k], k);
-                const bool ok = piv > 0.f && isfinite(piv);
-                if (!ok && lane == 0 && bad < 0) bad = o + k;
-                const float ip = ok ? 1.0f / piv : 0.f;
-                const float rk = c[k] * ip;  // new row k, column `lane`
+        for (int kk = 0; kk < RW; ++kk) {
+            const int k = RW * kb + kk, buf = kk & 1;
+            const float4 rc4 = *reinterpret_cast<const float4 *>(&rowbuf[buf][4 * lane]);
+            const float rc[4] = {rc4.x, rc4.y, rc4.z, rc4.w};
+            float cb[RW];
 #pragma unroll
-                for (int i = 0; i < PW; ++i) {
-                    const float cik = __shfl_sync(FULL, c[i], k);  // old X[i][k]
-                    float v = (lane == k) ? -cik * ip : fmaf(-cik, rk, c[i]);
-                    if (i == k) v = (lane == k) ? ip : rk;
-                    c[i] = v;
-                }
+            for (int q = 0; q < RW / 4; ++q) {
+                const float4 t = *reinterpret_cast<const float4 *>(&colbuf[buf][RW * warp + 4 * q]);
+                cb[4 * q] = t.x; cb[4 * q + 1] = t.y; cb[4 * q + 2] = t.z; cb[4 * q + 3] = t.w;
+            }
+            // the owner of row k + 1 finishes that row first and publishes it,
+            // so that the next pivot's latency overlaps the bulk update
+            const int rn = (kk + 1) % RW;
+            const bool next_owner = k + 1 < N && warp == (k + 1) / RW;
+            if (next_owner) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) a[rn][c] = fmaf(-cb[rn], rc[c], a[rn][c]);
+                if (lane == (k >> 2)) a[rn][kk & 3] = -cb[rn];
+                publish(k + 1, a[rn], (kk + 1) & 3);
             }
 #pragma unroll
-            for (int i = 0; i < PW; ++i) Q[i * QS + o + lane] = c[i];
+            for (int r = 0; r < RW; ++r) {
+                if (r == rn && next_owner) continue;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) a[r][c] = fmaf(-cb[r], rc[c], a[r][c]);
+                if (lane == (k >> 2)) a[r][kk & 3] = -cb[r];  // column k
+            }
+            if (warp == kb) {  // row k and the pivot
+                const float d = dbuf[buf];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) a[kk][c] = rc[c] * d;
+                if (lane == (k >> 2)) a[kk][kk & 3] = d;
+            }
+            __syncthreads();
         }
-        __syncthreads();
-        // ---- row panel: Q[l][j] = sum_m Pinv[l][m] X[o+m][j] for j outside the pivot block
-        if (tid < 4 * (N - PW)) {
-            const int rg = tid / (N - PW), jj = tid % (N - PW);  // rg uniform within a warp
-            const int j = jj < o ? jj : jj + PW;
-            float acc[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) acc[r] = 0.f;
-#pragma unroll 4
-            for (int m = 0; m < PW; ++m) {
-                const float x = S[(o + m) * LS + j];
-#pragma unroll
-                for (int r = 0; r < 8; ++r) acc[r] = fmaf(Q[(8 * rg + r) * QS + o + m], x, acc[r]);
-            }
-#pragma unroll
-            for (int r = 0; r < 8; ++r) Q[(8 * rg + r) * QS + j] = acc[r];
-        }
-        // pivot columns of the other rows, before they are overwritten
-        for (int e = tid; e < (N - PW) * PW; e += LEAF_THREADS) {
-            const int ii = e / PW, m = e % PW, i = ii < o ? ii : ii + PW;
-            Cb[ii * CS + m] = S[i * LS + o + m];
-        }
-        __syncthreads();
-        // ---- elimination: rows outside the pivot block, all 128 columns
-        {
-            const int ty = tid >> 5, tx = lane;
-            float acc[6][4];
-#pragma unroll
-            for (int r = 0; r < 6; ++r)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
-#pragma unroll 4
-            for (int m = 0; m < PW; ++m) {
-                float a[6], q[4];
-#pragma unroll
-                for (int r = 0; r < 6; ++r) a[r] = Cb[(ty + 16 * r) * CS + m];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) q[c] = Q[m * QS + tx + 32 * c];
-#pragma unroll
-                for (int r = 0; r < 6; ++r)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], q[c], acc[r][c]);
-            }
-#pragma unroll
-            for (int r = 0; r < 6; ++r) {
-                const int ii = ty + 16 * r, i = ii < o ? ii : ii + PW;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int j = tx + 32 * c;
-                    const bool inpiv = (j >= o) && (j < o + PW);
-                    const float base = inpiv ? 0.f : S[i * LS + j];
-                    S[i * LS + j] = base - acc[r][c];
-                }
-            }
-            // the pivot row panel becomes Q
-            for (int e = tid; e < PW * N; e += LEAF_THREADS) {
-                const int m = e >> 7, j = e & 127;
-                S[(o + m) * LS + j] = Q[m * QS + j];
-            }
-        }
-        __syncthreads();
     }
 
-    for (int e = tid; e < N * N; e += LEAF_THREADS) {
-        const int i = e >> 7, j = e & 127;
-        const long long o = (long long)i * J.ld + j;
-        const float v = S[i * LS + j];
-        const float h = tf32_hi(v);
-        J.Xh[o] = h;
-        J.Xl[o] = v - h;
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+        const long long o = (long long)(RW * warp + r) * J.ld + 4 * lane;
+        const float4 h = make_float4(tf32_hi(a[r][0]), tf32_hi(a[r][1]), tf32_hi(a[r][2]), tf32_hi(a[r][3]));
+        *reinterpret_cast<float4 *>(J.Xh + o) = h;
+        *reinterpret_cast<float4 *>(J.Xl + o) =
+            make_float4(a[r][0] - h.x, a[r][1] - h.y, a[r][2] - h.z, a[r][3] - h.w);
     }
     if (tid == 0 && bad >= 0 && J.info) atomicCAS(J.info, 0, J.o + bad + 1);
 }
@@ -500,23 +484,16 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
     return KFAC_OK;
 }
 
-constexpr size_t LEAF_SMEM =
-    ((size_t)LEAF * (LEAF + 1) + 32 * (LEAF + 4) + (LEAF - 32) * 33) * sizeof(float);
-
 kfac_status leaf_launch(const std::vector<LeafJob> &jobs, cudaStream_t st) {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(leaf_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LEAF_SMEM);
-    });
-    if (attr != cudaSuccess) return KFAC_ERR_CUDA;
+    for (const LeafJob &j : jobs)  // the kernel moves rows in 16-byte pieces
+        if (j.ld % 4 != 0 || (uintptr_t)j.Xh % 16 != 0 || (uintptr_t)j.Xl % 16 != 0) return KFAC_ERR_WORKSPACE;
     std::unique_ptr<LeafParams> P(new LeafParams);
     size_t pos = 0;
     while (pos < jobs.size()) {
         int n = 0;
         while (pos < jobs.size() && n < MAT_MAX) P->j[n++] = jobs[pos++];
         P->n = n;
-        KFAC_LAUNCH(KK_LEAF, st, (leaf_kernel<<<n, LEAF_THREADS, LEAF_SMEM, st>>>(*P)));
+        KFAC_LAUNCH(KK_LEAF, st, (leaf_kernel<<<n, LEAF_THREADS, 0, st>>>(*P)));
     }
     return KFAC_OK;
 }
