@@ -31,6 +31,8 @@ struct BnParams {
 };
 
 __global__ void __launch_bounds__(256) bn_fisher_kernel(const __grid_constant__ BnParams P) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float4 red_s[16][17];
     __shared__ float4 red_q[16][17];
     int lo = 0, hi = P.n - 1;
@@ -135,7 +137,7 @@ extern "C" kfac_status kfac_bn_diag_fisher(const kfac_bn_desc *descs, int count,
         P->ns = n_samples;
         P->gamma = gamma;
         P->xi = xi;
-        KFAC_LAUNCH(KK_BN, st, (bn_fisher_kernel<<<chunks, 256, 0, st>>>(*P)));
+        KFAC_LAUNCH(KK_BN, st, bn_fisher_kernel, chunks, 256, 0, *P);
     }
     return KFAC_OK;
 }

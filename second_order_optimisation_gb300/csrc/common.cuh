@@ -11,6 +11,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <utility>
 #include <stdint.h>
 
 #include "../../include/kfac.h"
@@ -39,13 +40,40 @@ enum KernelKind : int {
 int timing_begin(int kind, cudaStream_t st);
 void timing_end(int slot, cudaStream_t st);
 
-#define KFAC_LAUNCH(kind, st, launch)                            \
-    do {                                                         \
-        const int slot_ = ::kfac::timing_begin((kind), (st));    \
-        launch;                                                  \
-        ::kfac::timing_end(slot_, (st));                         \
-        ::kfac::count_launch();                                  \
-        if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA; \
+// Every kernel is launched with programmatic stream serialization
+// (programmatic dependent launch): the next kernel of the stream may be
+// scheduled, and run its prologue, while this one drains.  Each kernel
+// therefore calls pdl_wait() -- which returns once the preceding grid has
+// completed and its memory is visible -- before it touches global memory,
+// and pdl_trigger() after that to let its own successor be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// KFAC_LAUNCH(kind, stream, kernel, grid, block, dynamic smem, args...)
+#define KFAC_LAUNCH(kind, st, kernel, grid, block, smem, ...)                                  \
+    do {                                                                                       \
+        const int slot_ = ::kfac::timing_begin((kind), (st));                                  \
+        const cudaError_t e_ = ::kfac::launch_kernel((kernel), dim3(grid), dim3(block), (smem), \
+                                                     (st), __VA_ARGS__);                        \
+        ::kfac::timing_end(slot_, (st));                                                       \
+        ::kfac::count_launch();                                                                \
+        if (e_ != cudaSuccess || cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;      \
     } while (0)
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }

@@ -66,6 +66,8 @@ struct DampParams {
 };
 
 __global__ void __launch_bounds__(256) damping_kernel(const __grid_constant__ DampParams P) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float ra[256], rg[256];
     const int l = blockIdx.x;
     float ta = 0.f, tg = 0.f;
@@ -122,6 +124,8 @@ struct TileParams {
 
 // X = split(sym(F) + damp I) on [d, d], identity on the padding.
 __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ TileParams P) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float t[32][33];
     int lo = 0, hi = P.n - 1;
     while (lo < hi) {
@@ -158,6 +162,8 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ TileP
 
 // out = hi + lo of the upper triangle, mirrored; optional bf16 copy.
 __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ TileParams P) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float t[32][33];
     int lo = 0, hi = P.n - 1;
     while (lo < hi) {
@@ -215,6 +221,8 @@ struct LeafParams {
 // column scaled), which costs one barrier per pivot.  A pivot that is not
 // positive and finite is recorded in info and eliminated as 1 / a_kk = 0.
 __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_constant__ LeafParams P) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int N = LEAF, RW = N / (LEAF_THREADS / 32);  // 16 rows per warp
     __shared__ __align__(16) float rowbuf[2][N];
     __shared__ __align__(16) float colbuf[2][N];
@@ -493,7 +501,7 @@ kfac_status leaf_launch(const std::vector<LeafJob> &jobs, cudaStream_t st) {
         int n = 0;
         while (pos < jobs.size() && n < MAT_MAX) P->j[n++] = jobs[pos++];
         P->n = n;
-        KFAC_LAUNCH(KK_LEAF, st, (leaf_kernel<<<n, LEAF_THREADS, 0, st>>>(*P)));
+        KFAC_LAUNCH(KK_LEAF, st, leaf_kernel, n, LEAF_THREADS, 0, *P);
     }
     return KFAC_OK;
 }
@@ -515,8 +523,8 @@ kfac_status tile_launch(std::vector<TileMat> &mats, const float *damp, cudaStrea
         P->begin[n] = tiles;
         P->n = n;
         P->damp = damp;
-        if (PREP) KFAC_LAUNCH(KK_PREP, st, (prep_kernel<<<tiles, 256, 0, st>>>(*P)));
-        else KFAC_LAUNCH(KK_FINISH, st, (finish_kernel<<<tiles, 256, 0, st>>>(*P)));
+        if (PREP) KFAC_LAUNCH(KK_PREP, st, prep_kernel, tiles, 256, 0, *P);
+        else KFAC_LAUNCH(KK_FINISH, st, finish_kernel, tiles, 256, 0, *P);
     }
     return KFAC_OK;
 }
@@ -549,7 +557,7 @@ kfac_status damping_run(const InvMatrix *mats, int nlayers, float gamma, int pi_
         P->pi_split = pi_split;
         P->damp = damp_dev;
         P->base = base;
-        KFAC_LAUNCH(KK_DAMPING, st, (damping_kernel<<<n, 256, 0, st>>>(*P)));
+        KFAC_LAUNCH(KK_DAMPING, st, damping_kernel, n, 256, 0, *P);
     }
     return KFAC_OK;
 }

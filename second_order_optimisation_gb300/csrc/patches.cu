@@ -31,6 +31,8 @@ struct ImParams {
 // bf16) when c % 8 == 0, otherwise one element.
 template <typename T>
 __global__ void im2col_kernel(const __grid_constant__ ImParams P) {
+    pdl_wait();
+    pdl_trigger();
     const long long total = P.begin[P.n];
     for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < total;
          u += (long long)gridDim.x * blockDim.x) {
@@ -92,6 +94,8 @@ struct CsParams {
 };
 
 __global__ void __launch_bounds__(256) colsum_kernel(const __grid_constant__ CsParams P) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float red[32][65];
     int lo = 0, hi = P.n - 1;
     while (lo < hi) {
@@ -172,9 +176,9 @@ kfac_status im2col_run(const Im2colJob *jobs, int njobs, int dtype, cudaStream_t
         const int threads = 256;
         const long long blocks = std::min<long long>(ceil_div(units, threads), 152LL * 16);
         if (dtype == KFAC_BF16)
-            KFAC_LAUNCH(KK_IM2COL, st, (im2col_kernel<__nv_bfloat16><<<(int)blocks, threads, 0, st>>>(*P)));
+            KFAC_LAUNCH(KK_IM2COL, st, im2col_kernel<__nv_bfloat16>, (int)blocks, threads, 0, *P);
         else
-            KFAC_LAUNCH(KK_IM2COL, st, (im2col_kernel<float><<<(int)blocks, threads, 0, st>>>(*P)));
+            KFAC_LAUNCH(KK_IM2COL, st, im2col_kernel<float>, (int)blocks, threads, 0, *P);
     }
     return KFAC_OK;
 }
@@ -194,7 +198,7 @@ kfac_status colsum_run(const ColsumJob *jobs, int njobs, cudaStream_t st) {
         }
         P->begin[n] = chunks;
         P->n = n;
-        KFAC_LAUNCH(KK_COLSUM, st, (colsum_kernel<<<chunks, 256, 0, st>>>(*P)));
+        KFAC_LAUNCH(KK_COLSUM, st, colsum_kernel, chunks, 256, 0, *P);
     }
     return KFAC_OK;
 }

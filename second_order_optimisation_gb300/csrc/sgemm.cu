@@ -36,6 +36,8 @@ struct SgParams {
 };
 
 __global__ void __launch_bounds__(STHREADS) sgemm_kernel(const __grid_constant__ SgParams P) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ __align__(16) float As[SK][SB];
     __shared__ __align__(16) float Bs[SK][SB];
 
@@ -160,7 +162,7 @@ kfac_status sg_run(const SgJob *jobs, int njobs, cudaStream_t st) {
         }
         if (n == 0) break;
         P->n = n;
-        KFAC_LAUNCH(KK_SGEMM, st, (sgemm_kernel<<<tiles, STHREADS, 0, st>>>(*P)));
+        KFAC_LAUNCH(KK_SGEMM, st, sgemm_kernel, tiles, STHREADS, 0, *P);
     }
     return KFAC_OK;
 }

@@ -94,6 +94,8 @@ struct MapCopyParams {
 };
 
 __global__ void map_copy_kernel(const __grid_constant__ MapCopyParams P) {
+    pdl_wait();
+    pdl_trigger();
     // 8 threads per 128-byte map, 16 bytes each
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     const int m = t >> 3, part = t & 7;
@@ -386,6 +388,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the prologue above may overlap the preceding kernel; operands, maps and
+    // outputs are touched only after it has completed
+    pdl_wait();
+    pdl_trigger();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -705,7 +711,7 @@ kfac_status tc_upload_maps(const CUtensorMap *maps, int n, CUtensorMap *dev, cud
         std::memcpy(P->m, maps + base, sizeof(CUtensorMap) * cnt);
         P->dst = dev + base;
         P->n = cnt;
-        KFAC_LAUNCH(KK_MAPCOPY, st, (map_copy_kernel<<<(int)ceil_div(cnt * 8, 256), 256, 0, st>>>(*P)));
+        KFAC_LAUNCH(KK_MAPCOPY, st, map_copy_kernel, (int)ceil_div(cnt * 8, 256), 256, 0, *P);
     }
     return KFAC_OK;
 }
@@ -781,9 +787,9 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
         P->error = err;
         const int grid = std::min(work, sms);
         if (kind == TC_KIND_BF16)
-            KFAC_LAUNCH(KK_TC_BF16, st, (tc_gemm_kernel<TC_KIND_BF16><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(*P)));
+            KFAC_LAUNCH(KK_TC_BF16, st, tc_gemm_kernel<TC_KIND_BF16>, grid, NUM_THREADS, SMEM_BYTES, *P);
         else
-            KFAC_LAUNCH(KK_TC_TF32X3, st, (tc_gemm_kernel<TC_KIND_TF32X3><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(*P)));
+            KFAC_LAUNCH(KK_TC_TF32X3, st, tc_gemm_kernel<TC_KIND_TF32X3>, grid, NUM_THREADS, SMEM_BYTES, *P);
     }
     return KFAC_OK;
 }
