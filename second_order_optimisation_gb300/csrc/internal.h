@@ -50,9 +50,11 @@ struct TcJob {
 };
 
 // Tensor map of a row-major [rows][cols] matrix (ld elements) for the engine:
-// 128-byte swizzle, box 128 bytes wide and 128 rows (64 rows if mn_major, 32
-// rows for tf32).
-bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int mn_major);
+// 128-byte swizzle, box 128 bytes wide and box_rows rows (default: 128, or 64
+// if mn_major).  A tf32x3 operand is a run of four maps: hi and lo with
+// 128-row boxes, then hi and lo with 32-row boxes (B of narrow tiles).
+bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int mn_major,
+                 int box_rows = 0);
 // Copies host-built maps into device memory (128-byte aligned) on the stream.
 kfac_status tc_upload_maps(const CUtensorMap *maps, int n, CUtensorMap *dev, cudaStream_t st);
 // Workspace needed by tc_run for these jobs (split-K partials, counters).

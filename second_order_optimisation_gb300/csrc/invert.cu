@@ -44,6 +44,9 @@ namespace {
 constexpr int LEAF = 128;
 constexpr int LEAF_THREADS = 256;
 constexpr int MAT_MAX = 224;
+// tensor maps of one matrix: X, T, U pairs, each as hi / lo with 128-row and
+// with 32-row boxes
+constexpr int MAPS_PER_MATRIX = 12;
 
 inline int padded(int d) { return (int)ceil_div(d, LEAF) * LEAF; }
 
@@ -446,7 +449,7 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
     p.err = ws.take<int>(64);
     int nbig = 0;
     for (int k = 0; k < nmats; ++k) nbig += mats[k].d > LEAF;
-    p.dev_maps = ws.take<CUtensorMap>(6 * (size_t)std::max(nbig, 1));
+    p.dev_maps = ws.take<CUtensorMap>(MAPS_PER_MATRIX * (size_t)std::max(nbig, 1));
     p.work.resize(nmats);
     p.chains.assign(nmats, {});
     for (int k = 0; k < nmats; ++k) {
@@ -465,18 +468,21 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
             w.Ul = ws.take<float>(sq);
             float *bufs[6] = {w.Xh, w.Xl, w.Th, w.Tl, w.Uh, w.Ul};
             const int base = (int)p.maps.size();
-            for (int q = 0; q < 6; ++q) {
-                p.maps.emplace_back();
-                if (encode && !tc_make_map(&p.maps.back(), TC_KIND_TF32X3, bufs[q], w.dp, w.dp, w.dp, 0))
-                    return KFAC_ERR_CUDA;
-            }
+            for (int q = 0; q < 6; q += 2)  // per pair: hi, lo (128-row boxes), hi, lo (32-row boxes)
+                for (int v = 0; v < 4; ++v) {
+                    p.maps.emplace_back();
+                    if (encode && !tc_make_map(&p.maps.back(), TC_KIND_TF32X3, bufs[q + (v & 1)], w.dp, w.dp,
+                                               w.dp, 0, v < 2 ? 128 : 32))
+                        return KFAC_ERR_CUDA;
+                }
             w.mx = base;
-            w.mt = base + 2;
-            w.mu = base + 4;
+            w.mt = base + 4;
+            w.mu = base + 8;
         }
         gen_ops(p.chains[k], w, 0, w.dp, info_dev ? info_dev + k : nullptr);
         p.longest = std::max(p.longest, p.chains[k].size());
     }
+    if (p.maps.size() != (size_t)MAPS_PER_MATRIX * nbig) return KFAC_ERR_WORKSPACE;  // device map area
     // engine scratch: the largest GEMM round
     p.rounds = schedule_rounds(p.chains, p.round_kind);
     size_t tcb = 0;

@@ -55,7 +55,8 @@ template <> struct Traits<TC_KIND_TF32X3> {
 };
 
 struct TcProb {
-    int map_a, map_b;        // map indices; tf32x3: hi at map, lo at map + 1
+    int map_a, map_b;        // map indices; tf32x3: hi at map, lo at map + 1 (B of a narrow
+                             // tile: the 32-row-box pair at map + 2, map + 3)
     int a_row0, a_col0;      // operand sub-block origin inside its map (rows, columns)
     int b_row0, b_col0;
     int M, N, k_tiles;
@@ -431,12 +432,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                             load_tile(sa + TILE_BYTES, mb, q.b_mn, q.b_row0, q.b_col0, k.tn * BN, k0,
                                       &full[stage]);
                     } else {
-                        load_rows_tf32(sa, ma, q.a_row0, q.a_col0, k.tm * BM, BM, k0, &full[stage]);
-                        load_rows_tf32(sa + TILE_BYTES, ma + 1, q.a_row0, q.a_col0, k.tm * BM, BM, k0, &full[stage]);
-                        load_rows_tf32(sa + 2 * TILE_BYTES, mb, q.b_row0, q.b_col0, k.tn * q.bn, q.bn, k0,
-                                       &full[stage]);
-                        load_rows_tf32(sa + 3 * TILE_BYTES, mb + 1, q.b_row0, q.b_col0, k.tn * q.bn, q.bn, k0,
-                                       &full[stage]);
+                        load_tile(sa, ma, 0, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
+                        load_tile(sa + TILE_BYTES, ma + 1, 0, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
+                        if (q.bn == BN) {
+                            load_tile(sa + 2 * TILE_BYTES, mb, 0, q.b_row0, q.b_col0, k.tn * BN, k0, &full[stage]);
+                            load_tile(sa + 3 * TILE_BYTES, mb + 1, 0, q.b_row0, q.b_col0, k.tn * BN, k0,
+                                      &full[stage]);
+                        } else {  // narrow tile: B from the 32-row-box maps
+                            load_rows_tf32(sa + 2 * TILE_BYTES, mb, q.b_row0, q.b_col0, k.tn * q.bn, q.bn, k0,
+                                           &full[stage]);
+                            load_rows_tf32(sa + 3 * TILE_BYTES, mb + 1, q.b_row0, q.b_col0, k.tn * q.bn, q.bn,
+                                           k0, &full[stage]);
+                        }
                     }
                     if (++stage == Tr::STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -687,15 +694,15 @@ cudaError_t set_smem_attr() {
 
 }  // namespace
 
-bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int mn_major) {
+bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int mn_major,
+                 int box_rows) {
     EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) return false;
     const int esz = kind == TC_KIND_BF16 ? 2 : 4;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ld * esz};
     const cuuint32_t inner = 128u / esz;  // 128-byte rows
-    // tf32 operands are fetched in 32-row boxes (tiles 32, 64 or 128 wide)
-    cuuint32_t box[2] = {inner, mn_major ? 64u : kind == TC_KIND_TF32X3 ? 32u : 128u};
+    cuuint32_t box[2] = {inner, box_rows > 0 ? (cuuint32_t)box_rows : mn_major ? 64u : 128u};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = enc(m, kind == TC_KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                      2, (void *)ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -762,6 +769,7 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
             q.N = j.N;
             q.k_tiles = p.k_tiles[ji];
             q.bn = p.bn;
+            if (kind == TC_KIND_TF32X3 && p.bn < BN) q.map_b += 2;
             q.tiles_n = (int)ceil_div(j.N, p.bn);
             q.syrk = j.syrk;
             q.sym = j.sym;
