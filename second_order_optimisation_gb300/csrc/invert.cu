@@ -115,7 +115,8 @@ struct TileMat {
     uint16_t *out16;  // finish: optional bf16 copy
     long long ld16;
     int damp_idx;
-    int tiles;        // per side
+    int tiles;        // 64-wide tiles per side
+    int vec_f, vec_o, vec_b;  // F / out rows take 16-byte, out16 rows 8-byte accesses
 };
 
 struct TileParams {
@@ -125,74 +126,148 @@ struct TileParams {
     const float *damp;
 };
 
-// X = split(sym(F) + damp I) on [d, d], identity on the padding.
+constexpr int TT = 64;  // prep / finish tile
+
+// The upper tile pair (si <= sj) of this CTA: matrix index and tile coordinates.
+__device__ __forceinline__ const TileMat &tile_of(const TileParams &P, int &si, int &sj) {
+    int lo = 0, hi = P.n - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (P.begin[mid] <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
+    }
+    const TileMat &q = P.m[lo];
+    int t = blockIdx.x - P.begin[lo], i = 0;
+    while (t >= q.tiles - i) { t -= q.tiles - i; ++i; }
+    si = i;
+    sj = i + t;
+    return q;
+}
+
+// Value (r, c) of output tile (ti, tj) from the staged upper tile t of the pair
+// (si, sj) = (min, max): the tile itself, its transpose, or (diagonal tile) its
+// upper triangle mirrored.
+__device__ __forceinline__ float tile_val(const float (*t)[TT + 1], int si, int sj, bool transposed, int r, int c) {
+    if (si != sj) return transposed ? t[c][r] : t[r][c];
+    return r <= c ? t[r][c] : t[c][r];
+}
+
+// X = split(sym(F) + damp I) on [d, d], identity on the padding.  One CTA per
+// upper 64 x 64 tile pair: the upper tile of F is read once (16-byte pieces
+// where the rows allow) and written to both its own and its mirrored position.
 __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ TileParams P) {
     pdl_wait();
     pdl_trigger();
-    __shared__ float t[32][33];
-    int lo = 0, hi = P.n - 1;
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (P.begin[mid] <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
-    }
-    const TileMat &q = P.m[lo];
-    const int tt = blockIdx.x - P.begin[lo];
-    const int ti = tt / q.tiles, tj = tt - ti * q.tiles;
-    const int si = min(ti, tj), sj = max(ti, tj);
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    for (int r = ty; r < 32; r += 8) {
-        const int i = si * 32 + r, j = sj * 32 + tx;
-        t[r][tx] = (i < q.d && j < q.d) ? q.F[(long long)i * q.ldf + j] : 0.f;
+    __shared__ float t[TT][TT + 1];
+    int si, sj;
+    const TileMat &q = tile_of(P, si, sj);
+    const int tid = threadIdx.x, rr = tid >> 4, c4 = (tid & 15) * 4;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const int r = rr + 16 * p, i = si * TT + r, j = sj * TT + c4;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (i < q.d) {
+            const float *src = q.F + (long long)i * q.ldf + j;
+            if (q.vec_f && j + 3 < q.d) {
+                const float4 x = *reinterpret_cast<const float4 *>(src);
+                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (j + u < q.d) v[u] = src[u];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) t[r][c4 + u] = v[u];
     }
     __syncthreads();
     const float dv = P.damp[q.damp_idx];
-    for (int r = ty; r < 32; r += 8) {
-        const int i = ti * 32 + r, j = tj * 32 + tx;
-        float v;
-        if (i >= q.d || j >= q.d) {
-            v = (i == j) ? 1.f : 0.f;
-        } else {
-            if (ti < tj) v = t[r][tx];
-            else if (ti > tj) v = t[tx][r];
-            else v = (r <= tx) ? t[r][tx] : t[tx][r];
-            if (i == j) v += dv;
+#pragma unroll
+    for (int side = 0; side < 2; ++side) {
+        if (side == 1 && si == sj) break;
+        const int ti = side ? sj : si, tj = side ? si : sj;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int r = rr + 16 * p, i = ti * TT + r;
+            float h[4], l[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = c4 + u, j = tj * TT + c;
+                float v;
+                if (i >= q.d || j >= q.d) {
+                    v = (i == j) ? 1.f : 0.f;
+                } else {
+                    v = tile_val(t, si, sj, side == 1, r, c);
+                    if (i == j) v += dv;
+                }
+                h[u] = tf32_hi(v);
+                l[u] = v - h[u];
+            }
+            const long long o = (long long)i * q.dp + tj * TT + c4;
+            *reinterpret_cast<float4 *>(q.Xh + o) = make_float4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<float4 *>(q.Xl + o) = make_float4(l[0], l[1], l[2], l[3]);
         }
-        const float h = tf32_hi(v);
-        q.Xh[(long long)i * q.dp + j] = h;
-        q.Xl[(long long)i * q.dp + j] = v - h;
     }
 }
 
-// out = hi + lo of the upper triangle, mirrored; optional bf16 copy.
+// out = hi + lo of the upper triangle, mirrored; optional bf16 copy.  One CTA
+// per upper 64 x 64 tile pair of [d, d].
 __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ TileParams P) {
     pdl_wait();
     pdl_trigger();
-    __shared__ float t[32][33];
-    int lo = 0, hi = P.n - 1;
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (P.begin[mid] <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
-    }
-    const TileMat &q = P.m[lo];
-    const int tt = blockIdx.x - P.begin[lo];
-    const int ti = tt / q.tiles, tj = tt - ti * q.tiles;
-    const int si = min(ti, tj), sj = max(ti, tj);
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    for (int r = ty; r < 32; r += 8) {
-        const int i = si * 32 + r, j = sj * 32 + tx;
-        const long long o = (long long)i * q.dp + j;
-        t[r][tx] = (i < q.d && j < q.d) ? q.Xh[o] + q.Xl[o] : 0.f;
+    __shared__ float t[TT][TT + 1];
+    int si, sj;
+    const TileMat &q = tile_of(P, si, sj);
+    const int tid = threadIdx.x, rr = tid >> 4, c4 = (tid & 15) * 4;
+    {
+        float4 h[4], l[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {  // inside [dp, dp]: always in bounds
+            const long long o = (long long)(si * TT + rr + 16 * p) * q.dp + sj * TT + c4;
+            h[p] = *reinterpret_cast<const float4 *>(q.Xh + o);
+            l[p] = *reinterpret_cast<const float4 *>(q.Xl + o);
+        }
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int r = rr + 16 * p;
+            t[r][c4] = h[p].x + l[p].x;
+            t[r][c4 + 1] = h[p].y + l[p].y;
+            t[r][c4 + 2] = h[p].z + l[p].z;
+            t[r][c4 + 3] = h[p].w + l[p].w;
+        }
     }
     __syncthreads();
-    for (int r = ty; r < 32; r += 8) {
-        const int i = ti * 32 + r, j = tj * 32 + tx;
-        if (i >= q.d || j >= q.d) continue;
-        float v;
-        if (ti < tj) v = t[r][tx];
-        else if (ti > tj) v = t[tx][r];
-        else v = (r <= tx) ? t[r][tx] : t[tx][r];
-        q.out[(long long)i * q.ldo + j] = v;
-        if (q.out16) q.out16[(long long)i * q.ld16 + j] = f32_to_bf16_bits(v);
+#pragma unroll
+    for (int side = 0; side < 2; ++side) {
+        if (side == 1 && si == sj) break;
+        const int ti = side ? sj : si, tj = side ? si : sj;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int r = rr + 16 * p, i = ti * TT + r, j = tj * TT + c4;
+            if (i >= q.d) continue;
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = tile_val(t, si, sj, side == 1, r, c4 + u);
+            float *dst = q.out + (long long)i * q.ldo + j;
+            if (q.vec_o && j + 3 < q.d) {
+                *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (j + u < q.d) dst[u] = v[u];
+            }
+            if (q.out16) {
+                uint16_t *d16 = q.out16 + (long long)i * q.ld16 + j;
+                if (q.vec_b && j + 3 < q.d) {
+                    const uint32_t lo2 = f32_to_bf16_bits(v[0]) | ((uint32_t)f32_to_bf16_bits(v[1]) << 16);
+                    const uint32_t hi2 = f32_to_bf16_bits(v[2]) | ((uint32_t)f32_to_bf16_bits(v[3]) << 16);
+                    *reinterpret_cast<uint2 *>(d16) = make_uint2(lo2, hi2);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (j + u < q.d) d16[u] = f32_to_bf16_bits(v[u]);
+                }
+            }
+        }
     }
 }
 
@@ -212,24 +287,31 @@ struct LeafParams {
 
 // In-place inverse of one SPD 128 x 128 block by one CTA of 256 threads: a
 // Gauss-Jordan sweep with the block held in registers (warp w owns rows
-// 16w .. 16w+15, lane l columns 4l .. 4l+3).  Pivot k (in order) maps
+// 16w .. 16w+15, lane l columns 4l .. 4l+3), taken four pivots at a time.  A
+// single pivot k maps
 //   a_ij <- a_ij - a_ik a_kj / a_kk   (i, j != k)
 //   a_kj <- a_kj / a_kk,  a_ik <- -a_ik / a_kk,  a_kk <- 1 / a_kk
 // and after the last pivot the block holds its inverse.  No pivoting is
-// needed: every leading principal block of an SPD matrix is SPD.  The sweep
-// keeps the block sign-symmetric -- a_ik = -a_ki when exactly one of i, k has
-// been pivoted, a_ik = a_ki otherwise -- so every update of pivot k is formed
-// from row k alone.  The row's owner publishes it in shared memory (rowbuf:
-// a_kj; colbuf: s_j a_kj / a_kk with s_j = -1 for pivoted j, i.e. the pivot
-// column scaled), which costs one barrier per pivot.  A pivot that is not
-// positive and finite is recorded in info and eliminated as 1 / a_kk = 0.
+// needed: every leading principal block of an SPD matrix is SPD.  Four
+// consecutive pivots K = {k .. k+3} together are the block step: with R the
+// rows K, P = R[:, K] and W = P^-1 R,
+//   a_ij -= a_iK W_Kj,  a_Kj <- W_Kj,  a_iK <- -a_iK P^-1,  a_KK <- P^-1.
+// The sweep keeps the block sign-symmetric -- a_ik = -a_ki when exactly one
+// of i, k has been pivoted, a_ik = a_ki otherwise -- so the pivot columns are
+// s_i R[:, i] (s_i = -1 for pivoted i) and the new ones -s_i W[:, i]: every
+// update is formed from rows K alone.  P lies in one thread's registers (lane
+// k/4 of the owner warp), which inverts it by four scalar pivots; the owner
+// warp then publishes W, s R and -s W in shared memory, one barrier per block
+// step.  A pivot that is not positive and finite is recorded in info and
+// eliminated as 1 / a_kk = 0.
 __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_constant__ LeafParams P) {
     pdl_wait();
     pdl_trigger();
     constexpr int N = LEAF, RW = N / (LEAF_THREADS / 32);  // 16 rows per warp
-    __shared__ __align__(16) float rowbuf[2][N];
-    __shared__ __align__(16) float colbuf[2][N];
-    __shared__ float dbuf[2];
+    __shared__ __align__(16) float wbuf[2][4][N];   // W = P^-1 R
+    __shared__ __align__(16) float cbuf[2][4][N];   // s_i R[p][i]: the pivot columns
+    __shared__ __align__(16) float fbuf[2][4][N];   // -s_i W[p][i]: the new pivot columns
+    __shared__ __align__(16) float pbuf[2][16];     // P^-1
     __shared__ int bad;
     const LeafJob &J = P.j[blockIdx.x];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -256,59 +338,133 @@ __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_cons
     if (tid == 0) bad = -1;
     __syncthreads();
 
-    // Row kn (its pivot is element kn % 4 of lane kn / 4) published for the
-    // next pivot; called by the owner warp of the row.
-    auto publish = [&](int kn, const float (&row)[4], int e) {
-        const float pv = __shfl_sync(FULL, row[e], kn >> 2);
-        const bool ok = pv > 0.f && isfinite(pv);
-        const float d = ok ? __frcp_rn(pv) : 0.f;
-        if (!ok && lane == 0 && bad < 0) bad = kn;
-        const int buf = kn & 1;
-        *reinterpret_cast<float4 *>(&rowbuf[buf][4 * lane]) = make_float4(row[0], row[1], row[2], row[3]);
-        float cv[4];
+    // Block step kn (rows kl .. kl+3 of the calling owner warp) published for
+    // the next barrier interval.  Every lane inverts its own 4 x 4 diagonal
+    // piece (only lane kn/4 holds P; the others' results are discarded), so
+    // the warp stays converged.
+    auto publish = [&](int kn, int kl) {
+        float b[4][4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) cv[t] = (4 * lane + t < kn ? -row[t] : row[t]) * d;
-        *reinterpret_cast<float4 *>(&colbuf[buf][4 * lane]) = make_float4(cv[0], cv[1], cv[2], cv[3]);
-        if (lane == 0) dbuf[buf] = d;
+        for (int p = 0; p < 4; ++p)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) b[p][q] = a[kl + p][q];
+        const bool owner = lane == (kn >> 2);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const float x = b[v][v];
+            const bool ok = x > 0.f && isfinite(x);
+            if (owner && !ok && bad < 0) bad = kn + v;
+            const float d = ok ? __frcp_rn(x) : 0.f;
+            float t[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) t[i] = b[i][v] * d;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (i != v && j != v) b[i][j] = fmaf(-t[i], b[v][j], b[i][j]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j != v) b[v][j] *= d;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (i != v) b[i][v] = -t[i];
+            b[v][v] = d;
+        }
+        float pi[4][4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) pi[p][q] = __shfl_sync(FULL, b[p][q], kn >> 2);
+        const int buf = (kn >> 2) & 1;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            float w[4], c[4], f[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                w[t] = pi[p][0] * a[kl][t];
+#pragma unroll
+                for (int q = 1; q < 4; ++q) w[t] = fmaf(pi[p][q], a[kl + q][t], w[t]);
+                const float sg = 4 * lane + t < kn ? -1.f : 1.f;
+                c[t] = sg * a[kl + p][t];
+                f[t] = -sg * w[t];
+            }
+            *reinterpret_cast<float4 *>(&wbuf[buf][p][4 * lane]) = make_float4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<float4 *>(&cbuf[buf][p][4 * lane]) = make_float4(c[0], c[1], c[2], c[3]);
+            *reinterpret_cast<float4 *>(&fbuf[buf][p][4 * lane]) = make_float4(f[0], f[1], f[2], f[3]);
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+                *reinterpret_cast<float4 *>(&pbuf[buf][4 * p]) = make_float4(pi[p][0], pi[p][1], pi[p][2], pi[p][3]);
+        }
     };
 
-    if (warp == 0) publish(0, a[0], 0);
+    // rows r .. r+3 of this thread updated by the block step held in buf
+    auto update4 = [&](int r0, int buf, const float (&w)[4][4], bool colfix) {
+        float cb[4][4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const float4 t = *reinterpret_cast<const float4 *>(&cbuf[buf][p][RW * warp + r0]);
+            cb[p][0] = t.x; cb[p][1] = t.y; cb[p][2] = t.z; cb[p][3] = t.w;
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float v = a[r0 + r][c];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) v = fmaf(-cb[p][r], w[p][c], v);
+                a[r0 + r][c] = v;
+            }
+        if (colfix) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 t = *reinterpret_cast<const float4 *>(&fbuf[buf][q][RW * warp + r0]);
+                a[r0][q] = t.x; a[r0 + 1][q] = t.y; a[r0 + 2][q] = t.z; a[r0 + 3][q] = t.w;
+            }
+        }
+    };
+
+    if (warp == 0) publish(0, 0);
     __syncthreads();
 #pragma unroll 1
     for (int kb = 0; kb < N / RW; ++kb) {
 #pragma unroll
-        for (int kk = 0; kk < RW; ++kk) {
-            const int k = RW * kb + kk, buf = kk & 1;
-            const float4 rc4 = *reinterpret_cast<const float4 *>(&rowbuf[buf][4 * lane]);
-            const float rc[4] = {rc4.x, rc4.y, rc4.z, rc4.w};
-            float cb[RW];
+        for (int mm = 0; mm < RW / 4; ++mm) {
+            const int k = RW * kb + 4 * mm, kk = 4 * mm, buf = mm & 1;
+            float w[4][4];
 #pragma unroll
-            for (int q = 0; q < RW / 4; ++q) {
-                const float4 t = *reinterpret_cast<const float4 *>(&colbuf[buf][RW * warp + 4 * q]);
-                cb[4 * q] = t.x; cb[4 * q + 1] = t.y; cb[4 * q + 2] = t.z; cb[4 * q + 3] = t.w;
+            for (int p = 0; p < 4; ++p) {
+                const float4 t = *reinterpret_cast<const float4 *>(&wbuf[buf][p][4 * lane]);
+                w[p][0] = t.x; w[p][1] = t.y; w[p][2] = t.z; w[p][3] = t.w;
             }
-            // the owner of row k + 1 finishes that row first and publishes it,
-            // so that the next pivot's latency overlaps the bulk update
-            const int rn = (kk + 1) % RW;
-            const bool next_owner = k + 1 < N && warp == (k + 1) / RW;
+            const bool colfix = lane == (k >> 2);  // this lane holds the pivot columns
+            // the owner of the next block step finishes those rows first and
+            // publishes them, so that its latency overlaps the bulk update
+            const int kn = k + 4, rn = (kk + 4) % RW;
+            const bool next_owner = kn < N && warp == kn / RW;
             if (next_owner) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) a[rn][c] = fmaf(-cb[rn], rc[c], a[rn][c]);
-                if (lane == (k >> 2)) a[rn][kk & 3] = -cb[rn];
-                publish(k + 1, a[rn], (kk + 1) & 3);
+                update4(rn, buf, w, colfix);
+                publish(kn, rn);
             }
 #pragma unroll
-            for (int r = 0; r < RW; ++r) {
-                if (r == rn && next_owner) continue;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) a[r][c] = fmaf(-cb[r], rc[c], a[r][c]);
-                if (lane == (k >> 2)) a[r][kk & 3] = -cb[r];  // column k
+            for (int r0 = 0; r0 < RW; r0 += 4) {
+                if (r0 == rn && next_owner) continue;
+                update4(r0, buf, w, colfix);
             }
-            if (warp == kb) {  // row k and the pivot
-                const float d = dbuf[buf];
+            if (warp == kb) {  // the pivot rows and the pivot block
 #pragma unroll
-                for (int c = 0; c < 4; ++c) a[kk][c] = rc[c] * d;
-                if (lane == (k >> 2)) a[kk][kk & 3] = d;
+                for (int p = 0; p < 4; ++p)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) a[kk + p][c] = w[p][c];
+                if (colfix) {
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        const float4 t = *reinterpret_cast<const float4 *>(&pbuf[buf][4 * p]);
+                        a[kk + p][0] = t.x; a[kk + p][1] = t.y; a[kk + p][2] = t.z; a[kk + p][3] = t.w;
+                    }
+                }
             }
             __syncthreads();
         }
@@ -520,10 +676,13 @@ kfac_status tile_launch(std::vector<TileMat> &mats, const float *damp, cudaStrea
         int n = 0, tiles = 0;
         while (pos < mats.size() && n < MAT_MAX) {
             TileMat m = mats[pos++];
-            m.tiles = (int)ceil_div(PREP ? m.dp : m.d, 32);
+            m.tiles = (int)ceil_div(PREP ? m.dp : m.d, TT);
+            m.vec_f = m.F && m.ldf % 4 == 0 && (uintptr_t)m.F % 16 == 0;
+            m.vec_o = m.out && m.ldo % 4 == 0 && (uintptr_t)m.out % 16 == 0;
+            m.vec_b = m.out16 && m.ld16 % 4 == 0 && (uintptr_t)m.out16 % 8 == 0;
             P->m[n] = m;
             P->begin[n] = tiles;
-            tiles += m.tiles * m.tiles;
+            tiles += m.tiles * (m.tiles + 1) / 2;  // upper tile pairs
             ++n;
         }
         P->begin[n] = tiles;
@@ -582,7 +741,7 @@ kfac_status inv_run(const InvMatrix *mats, int nmats, const float *damp_dev, int
     std::vector<TileMat> tm(nmats);
     for (int k = 0; k < nmats; ++k)
         tm[k] = TileMat{mats[k].F, mats[k].ldf, p.work[k].Xh, p.work[k].Xl, mats[k].d, p.work[k].dp,
-                        mats[k].out, mats[k].ldo, mats[k].out_bf16, mats[k].ldo_bf16, k, 0};
+                        mats[k].out, mats[k].ldo, mats[k].out_bf16, mats[k].ldo_bf16, k, 0, 0, 0, 0};
     if ((s = tile_launch<true>(tm, damp_dev, st)) != KFAC_OK) return s;
 
     // 2. rounds (see schedule_rounds): each round is one leaf or one GEMM launch
