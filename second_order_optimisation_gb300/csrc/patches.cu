@@ -19,67 +19,73 @@ namespace kfac {
 namespace {
 
 constexpr int IM_MAX = 64;
+constexpr int IM_ROWS = 32;      // patch rows per CTA (4 per warp)
+constexpr int IM_TABLE = 2048;   // column units per row held in the CTA's table
 
 struct ImParams {
     Im2colJob j[IM_MAX];
-    long long begin[IM_MAX + 1];  // prefix of work units (units of 8 columns or 1 element)
-    int vec8[IM_MAX];
+    int begin[IM_MAX + 1];  // prefix of CTAs (IM_ROWS patch rows each)
+    int vec[IM_MAX];        // 1: a column unit is 16 bytes of channels, 0: one element
     int n;
 };
 
-// One work unit writes 8 consecutive patch columns of one row (16 bytes of
-// bf16) when c % 8 == 0, otherwise one element.
+// One CTA writes IM_ROWS consecutive patch rows of one job.  The columns of a
+// row are cut into units (16 bytes of one tap's channels when c allows it,
+// else single elements); a shared table gives each unit its tap (r, s) and
+// first channel, so that a warp decomposes the output pixel of a row once
+// and each lane then copies units with two compares and one address.
 template <typename T>
-__global__ void im2col_kernel(const __grid_constant__ ImParams P) {
+__global__ void __launch_bounds__(256) im2col_kernel(const __grid_constant__ ImParams P) {
     pdl_wait();
     pdl_trigger();
-    const long long total = P.begin[P.n];
-    for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < total;
-         u += (long long)gridDim.x * blockDim.x) {
-        int lo = 0, hi = P.n - 1;
-        while (lo < hi) {
-            int mid = (lo + hi + 1) >> 1;
-            if (P.begin[mid] <= u) lo = mid; else hi = mid - 1;
-        }
-        const Im2colJob &q = P.j[lo];
-        // 32-bit index math (a job has fewer than 2^31 units and rows)
-        const unsigned local = (unsigned)(u - P.begin[lo]);
-        const int dcore = q.kh * q.kw * q.c;
-        const int d = dcore + q.append_one;
-        const bool v8 = P.vec8[lo] != 0;
-        const unsigned per_row = v8 ? dcore / 8 : d;
-        const unsigned m = local / per_row;
-        const int cu = (int)(local - m * per_row);
-        const unsigned t = m / (unsigned)q.wo;
-        const int wo = (int)(m - t * (unsigned)q.wo);
-        const unsigned img = t / (unsigned)q.ho;
-        const int ho = (int)(t - img * (unsigned)q.ho);
-        T *prow = (T *)q.P + (long long)m * q.ldp;
-        const T *x = (const T *)q.x;
-        if (v8) {
-            const int col = cu * 8;
-            const int rs = col / q.c, ch = col - rs * q.c;
-            const int r = rs / q.kw, s = rs - r * q.kw;
-            const int hi_ = ho * q.sh - q.ph + r, wi = wo * q.sw - q.pw + s;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (hi_ >= 0 && hi_ < q.h && wi >= 0 && wi < q.w)
-                v = *(const uint4 *)(x + (((long long)img * q.h + hi_) * q.w + wi) * q.c + ch);
-            *(uint4 *)(prow + col) = v;
-            if (q.append_one && cu == per_row - 1) prow[dcore] = (T)1.0f;
-        } else {
-            const int col = cu;
-            T v = (T)0.0f;
-            if (col == dcore) {
-                v = (T)1.0f;
+    __shared__ int table[IM_TABLE];  // r | s << 8 | ch << 16 (rows longer than the table: computed per unit)
+    int lo = 0, hi = P.n - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (P.begin[mid] <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
+    }
+    const Im2colJob &q = P.j[lo];
+    const bool vec = P.vec[lo] != 0;
+    constexpr int VW = 16 / sizeof(T);  // elements per 16-byte unit
+    const int dcore = q.kh * q.kw * q.c;
+    const int units = vec ? dcore / VW : dcore;
+    const int step = vec ? VW : 1;
+    const bool tabled = units <= IM_TABLE;
+    auto entry = [&](int e) {
+        const int col = e * step, rs = col / q.c, ch = col - rs * q.c;
+        const int r = rs / q.kw, sx = rs - r * q.kw;
+        return r | (sx << 8) | (ch << 16);
+    };
+    if (tabled)
+        for (int e = threadIdx.x; e < units; e += blockDim.x) table[e] = entry(e);
+    __syncthreads();
+    const long long M = (long long)q.n * q.ho * q.wo;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const T *x = (const T *)q.x;
+#pragma unroll 1
+    for (int rr = warp; rr < IM_ROWS; rr += 8) {
+        const long long m = (long long)(blockIdx.x - P.begin[lo]) * IM_ROWS + rr;
+        if (m >= M) break;
+        const long long t = m / q.wo;
+        const int wo = (int)(m - t * q.wo);
+        const int img = (int)(t / q.ho), ho = (int)(t - (long long)img * q.ho);
+        const int hb = ho * q.sh - q.ph, wb = wo * q.sw - q.pw;
+        const T *xi = x + (long long)img * q.h * q.w * q.c;
+        T *prow = (T *)q.P + m * q.ldp;
+        for (int e = lane; e < units; e += 32) {
+            const int tv = tabled ? table[e] : entry(e);
+            const int hh = hb + (tv & 255), ww = wb + ((tv >> 8) & 255), ch = tv >> 16;
+            const bool in = hh >= 0 && hh < q.h && ww >= 0 && ww < q.w;
+            const T *src = xi + ((long long)hh * q.w + ww) * q.c + ch;
+            if (vec) {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (in) v = *reinterpret_cast<const uint4 *>(src);
+                *reinterpret_cast<uint4 *>(prow + e * VW) = v;
             } else {
-                const int rs = col / q.c, ch = col - rs * q.c;
-                const int r = rs / q.kw, s = rs - r * q.kw;
-                const int hi_ = ho * q.sh - q.ph + r, wi = wo * q.sw - q.pw + s;
-                if (hi_ >= 0 && hi_ < q.h && wi >= 0 && wi < q.w)
-                    v = x[(((long long)img * q.h + hi_) * q.w + wi) * q.c + ch];
+                prow[e] = in ? *src : (T)0.0f;
             }
-            prow[col] = v;
         }
+        if (q.append_one && lane == 0) prow[dcore] = (T)1.0f;
     }
 }
 
@@ -154,31 +160,35 @@ __global__ void __launch_bounds__(256) colsum_kernel(const __grid_constant__ CsP
 
 kfac_status im2col_run(const Im2colJob *jobs, int njobs, int dtype, cudaStream_t st) {
     std::unique_ptr<ImParams> P(new ImParams);
+    const size_t esz = dtype == KFAC_BF16 ? 2 : 4;
+    const int vw = (int)(16 / esz);
     int pos = 0;
     while (pos < njobs) {
         int n = 0;
-        long long units = 0;
+        long long ctas = 0;
         while (pos < njobs && n < IM_MAX) {
-            const Im2colJob &j = jobs[pos++];
-            P->j[n] = j;
-            const int dcore = j.kh * j.kw * j.c;
+            const Im2colJob &j = jobs[pos];
             const long long M = (long long)j.n * j.ho * j.wo;
-            const bool v8 = dtype == KFAC_BF16 && j.c % 8 == 0 && j.ldp % 8 == 0 &&
-                            ((uintptr_t)j.x % 16 == 0) && ((uintptr_t)j.P % 16 == 0);
-            P->vec8[n] = v8 ? 1 : 0;
-            P->begin[n] = units;
-            units += M * (v8 ? dcore / 8 : dcore + j.append_one);
+            const bool vec = j.c % vw == 0 && j.ldp % vw == 0 && ((uintptr_t)j.x % 16 == 0) &&
+                             ((uintptr_t)j.P % 16 == 0);
+            if (j.kh > 255 || j.kw > 255 || j.c >= (1 << 15)) return KFAC_ERR_UNSUPPORTED;
+            const long long c = ceil_div(M, IM_ROWS);
+            if (ctas + c > (1LL << 30)) break;
+            P->j[n] = j;
+            P->vec[n] = vec ? 1 : 0;
+            P->begin[n] = (int)ctas;
+            ctas += c;
             ++n;
+            ++pos;
         }
-        P->begin[n] = units;
+        if (n == 0) return KFAC_ERR_UNSUPPORTED;  // one job alone needs more than 2^30 CTAs
+        P->begin[n] = (int)ctas;
         P->n = n;
-        if (units == 0) continue;
-        const int threads = 256;
-        const long long blocks = std::min<long long>(ceil_div(units, threads), 152LL * 16);
+        if (ctas == 0) continue;
         if (dtype == KFAC_BF16)
-            KFAC_LAUNCH(KK_IM2COL, st, im2col_kernel<__nv_bfloat16>, (int)blocks, threads, 0, *P);
+            KFAC_LAUNCH(KK_IM2COL, st, im2col_kernel<__nv_bfloat16>, (int)ctas, 256, 0, *P);
         else
-            KFAC_LAUNCH(KK_IM2COL, st, im2col_kernel<float>, (int)blocks, threads, 0, *P);
+            KFAC_LAUNCH(KK_IM2COL, st, im2col_kernel<float>, (int)ctas, 256, 0, *P);
     }
     return KFAC_OK;
 }
