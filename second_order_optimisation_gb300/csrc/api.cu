@@ -55,6 +55,13 @@ void timing_end(int slot, cudaStream_t st) {
     if (slot < (int)g_recs.size()) cudaEventRecord(g_recs[slot].stop, st);
 }
 
+namespace {
+thread_local bool t_pdl = true;
+}  // namespace
+bool pdl_enabled() { return t_pdl; }
+PdlScope::PdlScope(bool on) : prev(t_pdl) { t_pdl = on; }
+PdlScope::~PdlScope() { t_pdl = prev; }
+
 int device_sm_count() {
     static int cache[64] = {0};
     int dev = 0;

@@ -49,6 +49,16 @@ void timing_end(int slot, cudaStream_t st);
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Programmatic serialization is on unless a PdlScope on this host thread turns
+// it off (used for work on a concurrent low-priority stream, whose early
+// launched CTAs would otherwise hold SMs while they wait).
+bool pdl_enabled();
+struct PdlScope {
+    bool prev;
+    explicit PdlScope(bool on);
+    ~PdlScope();
+};
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                           Args &&...args) {
@@ -61,7 +71,7 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

@@ -58,11 +58,13 @@ bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int ro
 // Copies host-built maps into device memory (128-byte aligned) on the stream.
 kfac_status tc_upload_maps(const CUtensorMap *maps, int n, CUtensorMap *dev, cudaStream_t st);
 // Workspace needed by tc_run for these jobs (split-K partials, counters).
-size_t tc_workspace_bytes(const TcJob *jobs, int njobs, int kind);
+size_t tc_workspace_bytes(const TcJob *jobs, int njobs, int kind, int max_ctas = 0);
 // Enqueue the jobs (one or more persistent launches).  `err` is a device int
 // that collects timeout codes.
+// `max_ctas` (0: the SM count) caps the persistent grid, e.g. to leave SMs to
+// a concurrent stream.
 kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *dev_maps, Arena &ws,
-                   int *err, cudaStream_t st);
+                   int *err, cudaStream_t st, int max_ctas = 0);
 
 // ----------------------------------------------------- CUDA-core GEMM (fp32)
 // C[M x N] = alpha * op(A) op(B) + beta * C, fp32.

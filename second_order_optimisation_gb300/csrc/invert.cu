@@ -42,7 +42,8 @@ namespace kfac {
 namespace {
 
 constexpr int LEAF = 128;
-constexpr int LEAF_THREADS = 256;
+constexpr int LEAF_ROW_WARPS = 8;                    // leaf: warps owning the block
+constexpr int LEAF_THREADS = 32 * (LEAF_ROW_WARPS + 1);  // plus the publisher warp
 constexpr int MAT_MAX = 224;
 // tensor maps of one matrix: X, T, U pairs, each as hi / lo with 128-row and
 // with 32-row boxes
@@ -285,10 +286,28 @@ struct LeafParams {
     int n;
 };
 
-// In-place inverse of one SPD 128 x 128 block by one CTA of 256 threads: a
-// Gauss-Jordan sweep with the block held in registers (warp w owns rows
-// 16w .. 16w+15, lane l columns 4l .. 4l+3), taken four pivots at a time.  A
-// single pivot k maps
+// 1 / x for a positive finite pivot: the hardware approximate reciprocal
+// refined by one Newton-Raphson step, r <- r + r (1 - x r) (a short
+// dependent chain for the publisher's serial 4 x 4 inverse).
+__device__ __forceinline__ float recip_nr(float x) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    const float e = fmaf(-x, r, 1.0f);
+    return fmaf(r, e, r);
+}
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;  // two fp32 fused multiply-adds in one instruction
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+        " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+// In-place inverse of one SPD 128 x 128 block by one CTA: a Gauss-Jordan
+// sweep with the block held in registers, four pivots at a time.  A single
+// pivot k maps
 //   a_ij <- a_ij - a_ik a_kj / a_kk   (i, j != k)
 //   a_kj <- a_kj / a_kk,  a_ik <- -a_ik / a_kk,  a_kk <- 1 / a_kk
 // and after the last pivot the block holds its inverse.  No pivoting is
@@ -299,27 +318,33 @@ struct LeafParams {
 // The sweep keeps the block sign-symmetric -- a_ik = -a_ki when exactly one
 // of i, k has been pivoted, a_ik = a_ki otherwise -- so the pivot columns are
 // s_i R[:, i] (s_i = -1 for pivoted i) and the new ones -s_i W[:, i]: every
-// update is formed from rows K alone.  P lies in one thread's registers (lane
-// k/4 of the owner warp), which inverts it by four scalar pivots; the owner
-// warp then publishes W, s R and -s W in shared memory, one barrier per block
-// step.  A pivot that is not positive and finite is recorded in info and
-// eliminated as 1 / a_kk = 0.
+// update is formed from rows K alone.
+// Roles: warps 0..7 own the block (warp w rows 16w .. 16w+15, lane l columns
+// 4l .. 4l+3) and apply one block step per barrier interval; warp 8 is the
+// publisher.  During step s it takes the rows of block s+1 (copied to shared
+// memory by their owner one step earlier), applies step s to them, inverts
+// their 4 x 4 diagonal block, and publishes W, s R, -s W and P^-1 of block
+// s+1 -- so that this serial chain overlaps the owners' bulk update.  A pivot
+// that is not positive and finite is recorded in info and eliminated as
+// 1 / a_kk = 0.
 __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_constant__ LeafParams P) {
     pdl_wait();
     pdl_trigger();
-    constexpr int N = LEAF, RW = N / (LEAF_THREADS / 32);  // 16 rows per warp
+    constexpr int N = LEAF, RW = N / LEAF_ROW_WARPS;  // 16 rows per row warp
+    constexpr int NB = N / 4;                         // block steps
     __shared__ __align__(16) float wbuf[2][4][N];   // W = P^-1 R
     __shared__ __align__(16) float cbuf[2][4][N];   // s_i R[p][i]: the pivot columns
     __shared__ __align__(16) float fbuf[2][4][N];   // -s_i W[p][i]: the new pivot columns
     __shared__ __align__(16) float pbuf[2][16];     // P^-1
+    __shared__ __align__(16) float rbuf[2][4][N];   // raw rows of the block after next, for the publisher
     __shared__ int bad;
     const LeafJob &J = P.j[blockIdx.x];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool publisher = warp == LEAF_ROW_WARPS;
     const unsigned FULL = 0xffffffffu;
 
     float a[RW][4];
-    {   // 16-byte pieces, every load issued before the first use (the host
-        // guarantees 16-byte aligned rows)
+    if (!publisher) {  // 16-byte pieces, every load issued before the first use
         float4 h[RW], l[RW];
 #pragma unroll
         for (int r = 0; r < RW; ++r) {
@@ -334,27 +359,31 @@ __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_cons
             a[r][2] = h[r].z + l[r].z;
             a[r][3] = h[r].w + l[r].w;
         }
+        if (warp == 0) {  // rows of blocks 0 and 1 for the publisher
+#pragma unroll
+            for (int p = 0; p < 8; ++p)
+                *reinterpret_cast<float4 *>(&rbuf[p >> 2][p & 3][4 * lane]) =
+                    make_float4(a[p][0], a[p][1], a[p][2], a[p][3]);
+        }
     }
     if (tid == 0) bad = -1;
     __syncthreads();
 
-    // Block step kn (rows kl .. kl+3 of the calling owner warp) published for
-    // the next barrier interval.  Every lane inverts its own 4 x 4 diagonal
-    // piece (only lane kn/4 holds P; the others' results are discarded), so
-    // the warp stays converged.
-    auto publish = [&](int kn, int kl) {
+    // ---- publisher helpers (warp 8; lane l holds columns 4l .. 4l+3 of the rows)
+    // the 4 x 4 diagonal block of the rows (only lane kn/4 holds P; the other
+    // lanes' results are discarded), inverted by four scalar pivots
+    auto publish = [&](const float (&R)[4][4], int kn) {
         float b[4][4];
 #pragma unroll
         for (int p = 0; p < 4; ++p)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) b[p][q] = a[kl + p][q];
-        const bool owner = lane == (kn >> 2);
+            for (int q = 0; q < 4; ++q) b[p][q] = R[p][q];
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
             const float x = b[v][v];
             const bool ok = x > 0.f && isfinite(x);
-            if (owner && !ok && bad < 0) bad = kn + v;
-            const float d = ok ? __frcp_rn(x) : 0.f;
+            if (lane == (kn >> 2) && !ok && bad < 0) bad = kn + v;
+            const float d = ok ? recip_nr(x) : 0.f;
             float t[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) t[i] = b[i][v] * d;
@@ -382,11 +411,11 @@ __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_cons
             float w[4], c[4], f[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-                w[t] = pi[p][0] * a[kl][t];
+                w[t] = pi[p][0] * R[0][t];
 #pragma unroll
-                for (int q = 1; q < 4; ++q) w[t] = fmaf(pi[p][q], a[kl + q][t], w[t]);
+                for (int q = 1; q < 4; ++q) w[t] = fmaf(pi[p][q], R[q][t], w[t]);
                 const float sg = 4 * lane + t < kn ? -1.f : 1.f;
-                c[t] = sg * a[kl + p][t];
+                c[t] = sg * R[p][t];
                 f[t] = -sg * w[t];
             }
             *reinterpret_cast<float4 *>(&wbuf[buf][p][4 * lane]) = make_float4(w[0], w[1], w[2], w[3]);
@@ -399,40 +428,52 @@ __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_cons
                 *reinterpret_cast<float4 *>(&pbuf[buf][4 * p]) = make_float4(pi[p][0], pi[p][1], pi[p][2], pi[p][3]);
         }
     };
+    auto load_rows = [&](float (&R)[4][4], int blk) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const float4 t = *reinterpret_cast<const float4 *>(&rbuf[blk & 1][p][4 * lane]);
+            R[p][0] = t.x; R[p][1] = t.y; R[p][2] = t.z; R[p][3] = t.w;
+        }
+    };
 
-    // rows r .. r+3 of this thread updated by the block step held in buf
-    auto update4 = [&](int r0, int buf, const float (&w)[4][4], bool colfix) {
+    // rows r0 .. r0+3 (of a row warp: local rows; of the publisher: R with
+    // global first row i0) updated by the block step held in buf
+    auto step_rows = [&](float (&X)[4][4], int i0, int buf, const float (&w)[4][4], bool colfix) {
         float cb[4][4];
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-            const float4 t = *reinterpret_cast<const float4 *>(&cbuf[buf][p][RW * warp + r0]);
+            const float4 t = *reinterpret_cast<const float4 *>(&cbuf[buf][p][i0]);
             cb[p][0] = t.x; cb[p][1] = t.y; cb[p][2] = t.z; cb[p][3] = t.w;
         }
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+        for (int p = 0; p < 4; ++p)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float v = a[r0 + r][c];
-#pragma unroll
-                for (int p = 0; p < 4; ++p) v = fmaf(-cb[p][r], w[p][c], v);
-                a[r0 + r][c] = v;
+            for (int r = 0; r < 4; ++r) {
+                const float2 m = make_float2(-cb[p][r], -cb[p][r]);
+                const float2 lo = ffma2(m, make_float2(w[p][0], w[p][1]), make_float2(X[r][0], X[r][1]));
+                const float2 hi = ffma2(m, make_float2(w[p][2], w[p][3]), make_float2(X[r][2], X[r][3]));
+                X[r][0] = lo.x; X[r][1] = lo.y; X[r][2] = hi.x; X[r][3] = hi.y;
             }
         if (colfix) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float4 t = *reinterpret_cast<const float4 *>(&fbuf[buf][q][RW * warp + r0]);
-                a[r0][q] = t.x; a[r0 + 1][q] = t.y; a[r0 + 2][q] = t.z; a[r0 + 3][q] = t.w;
+                const float4 t = *reinterpret_cast<const float4 *>(&fbuf[buf][q][i0]);
+                X[0][q] = t.x; X[1][q] = t.y; X[2][q] = t.z; X[3][q] = t.w;
             }
         }
     };
 
-    if (warp == 0) publish(0, 0);
+    if (publisher) {
+        float R[4][4];
+        load_rows(R, 0);
+        publish(R, 0);
+    }
     __syncthreads();
 #pragma unroll 1
     for (int kb = 0; kb < N / RW; ++kb) {
 #pragma unroll
         for (int mm = 0; mm < RW / 4; ++mm) {
-            const int k = RW * kb + 4 * mm, kk = 4 * mm, buf = mm & 1;
+            const int s = (RW / 4) * kb + mm, k = 4 * s, buf = mm & 1;
             float w[4][4];
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
@@ -440,43 +481,56 @@ __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_cons
                 w[p][0] = t.x; w[p][1] = t.y; w[p][2] = t.z; w[p][3] = t.w;
             }
             const bool colfix = lane == (k >> 2);  // this lane holds the pivot columns
-            // the owner of the next block step finishes those rows first and
-            // publishes them, so that its latency overlaps the bulk update
-            const int kn = k + 4, rn = (kk + 4) % RW;
-            const bool next_owner = kn < N && warp == kn / RW;
-            if (next_owner) {
-                update4(rn, buf, w, colfix);
-                publish(kn, rn);
-            }
+            if (publisher) {
+                if (s + 1 < NB) {  // block s+1: its rows as of step s-1, then step s
+                    float R[4][4];
+                    load_rows(R, s + 1);
+                    step_rows(R, k + 4, buf, w, colfix);
+                    publish(R, k + 4);
+                }
+            } else {
 #pragma unroll
-            for (int r0 = 0; r0 < RW; r0 += 4) {
-                if (r0 == rn && next_owner) continue;
-                update4(r0, buf, w, colfix);
-            }
-            if (warp == kb) {  // the pivot rows and the pivot block
+                for (int r0 = 0; r0 < RW; r0 += 4) {
+                    float (&X)[4][4] = *reinterpret_cast<float (*)[4][4]>(&a[r0][0]);
+                    step_rows(X, RW * warp + r0, buf, w, colfix);
+                }
+                if (warp == kb) {  // the pivot rows and the pivot block
+                    const int kk = 4 * mm;
 #pragma unroll
-                for (int p = 0; p < 4; ++p)
+                    for (int p = 0; p < 4; ++p)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) a[kk + p][c] = w[p][c];
-                if (colfix) {
+                        for (int c = 0; c < 4; ++c) a[kk + p][c] = w[p][c];
+                    if (colfix) {
 #pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        const float4 t = *reinterpret_cast<const float4 *>(&pbuf[buf][4 * p]);
-                        a[kk + p][0] = t.x; a[kk + p][1] = t.y; a[kk + p][2] = t.z; a[kk + p][3] = t.w;
+                        for (int p = 0; p < 4; ++p) {
+                            const float4 t = *reinterpret_cast<const float4 *>(&pbuf[buf][4 * p]);
+                            a[kk + p][0] = t.x; a[kk + p][1] = t.y; a[kk + p][2] = t.z; a[kk + p][3] = t.w;
+                        }
                     }
+                }
+                // rows of block s+2 (after this step) for the publisher
+                const int n2 = s + 2;
+                if (n2 < NB && warp == (4 * n2) / RW) {
+                    const int kl = (4 * n2) % RW;
+#pragma unroll
+                    for (int p = 0; p < 4; ++p)
+                        *reinterpret_cast<float4 *>(&rbuf[n2 & 1][p][4 * lane]) =
+                            make_float4(a[kl + p][0], a[kl + p][1], a[kl + p][2], a[kl + p][3]);
                 }
             }
             __syncthreads();
         }
     }
 
+    if (!publisher) {
 #pragma unroll
-    for (int r = 0; r < RW; ++r) {
-        const long long o = (long long)(RW * warp + r) * J.ld + 4 * lane;
-        const float4 h = make_float4(tf32_hi(a[r][0]), tf32_hi(a[r][1]), tf32_hi(a[r][2]), tf32_hi(a[r][3]));
-        *reinterpret_cast<float4 *>(J.Xh + o) = h;
-        *reinterpret_cast<float4 *>(J.Xl + o) =
-            make_float4(a[r][0] - h.x, a[r][1] - h.y, a[r][2] - h.z, a[r][3] - h.w);
+        for (int r = 0; r < RW; ++r) {
+            const long long o = (long long)(RW * warp + r) * J.ld + 4 * lane;
+            const float4 h = make_float4(tf32_hi(a[r][0]), tf32_hi(a[r][1]), tf32_hi(a[r][2]), tf32_hi(a[r][3]));
+            *reinterpret_cast<float4 *>(J.Xh + o) = h;
+            *reinterpret_cast<float4 *>(J.Xl + o) =
+                make_float4(a[r][0] - h.x, a[r][1] - h.y, a[r][2] - h.z, a[r][3] - h.w);
+        }
     }
     if (tid == 0 && bad >= 0 && J.info) atomicCAS(J.info, 0, J.o + bad + 1);
 }
@@ -535,16 +589,18 @@ void gen_ops(std::vector<Op> &ops, const MatWork &w, int o, int n, int *info) {
     gemm(w.mx, o, o + h, w.mt, o, 0, h, h, m, -1.f, 1.f, w.Xh + x11, w.Xl + x11, nullptr, nullptr, 1);
 }
 
-// Round schedule: the longest chain sets the sequence of rounds (one launch
-// each, leaf or GEMM); every other chain is embedded as late as possible into
-// rounds of the same op kind, in order.  The long chain's late rounds are
-// small, latency-bound launches with most SMs idle, and the shorter chains'
-// work fills them; one launch per round.  Falls back to left-aligned
-// lock-step (a leaf and a GEMM launch per round) if a chain does not embed.
+// Round schedule of a group of chains: the group's longest chain sets the
+// sequence of rounds (one launch each, leaf or GEMM); every other chain of the
+// group is embedded as late as possible into rounds of the same op kind, in
+// order.  The long chain's late rounds are small, latency-bound launches with
+// most SMs idle, and the shorter chains' work fills them.  Falls back to
+// left-aligned lock-step (a leaf and a GEMM launch per round) if a chain does
+// not embed.  Rounds list (chain, op) pairs.
 std::vector<std::vector<std::pair<int, int>>> schedule_rounds(const std::vector<std::vector<Op>> &chains,
+                                                              const std::vector<int> &members,
                                                               std::vector<int> &round_kind) {
     int crit = -1;
-    for (int k = 0; k < (int)chains.size(); ++k)
+    for (int k : members)
         if (crit < 0 || chains[k].size() > chains[crit].size()) crit = k;
     std::vector<std::vector<std::pair<int, int>>> rounds;
     round_kind.clear();
@@ -554,7 +610,7 @@ std::vector<std::vector<std::pair<int, int>>> schedule_rounds(const std::vector<
     for (int r = 0; r < R; ++r) round_kind.push_back(chains[crit][r].leaf);
     bool ok = true;
     std::vector<std::vector<int>> slot(chains.size());
-    for (int k = 0; k < (int)chains.size() && ok; ++k) {
+    for (int k : members) {
         const int n = (int)chains[k].size();
         slot[k].assign(n, -1);
         int r = R - 1;
@@ -563,21 +619,22 @@ std::vector<std::vector<std::pair<int, int>>> schedule_rounds(const std::vector<
             if (r < 0) { ok = false; break; }
             slot[k][i] = r--;
         }
+        if (!ok) break;
     }
     if (ok) {
-        for (int k = 0; k < (int)chains.size(); ++k)
+        for (int k : members)
             for (int i = 0; i < (int)chains[k].size(); ++i) rounds[slot[k][i]].push_back({k, i});
         return rounds;
     }
     // fallback: left-aligned lock-step, leaves then GEMMs in each step
     size_t longest = 0;
-    for (const auto &c : chains) longest = std::max(longest, c.size());
+    for (int k : members) longest = std::max(longest, chains[k].size());
     rounds.clear();
     round_kind.clear();
     for (size_t r = 0; r < longest; ++r)
         for (int kind = 1; kind >= 0; --kind) {
             std::vector<std::pair<int, int>> v;
-            for (int k = 0; k < (int)chains.size(); ++k)
+            for (int k : members)
                 if (r < chains[k].size() && chains[k][r].leaf == kind) v.push_back({k, (int)r});
             if (!v.empty()) {
                 rounds.push_back(v);
@@ -588,17 +645,29 @@ std::vector<std::vector<std::pair<int, int>>> schedule_rounds(const std::vector<
 }
 
 // Workspace layout shared by the size query and the run.
+// The chains run as two concurrent groups: the longest ones (the critical
+// path of the call) on a high-priority stream, all others on a low-priority
+// stream whose GEMM launches leave SMs free for the first group.  Each group
+// has its own rounds and engine scratch.
+constexpr int RESERVED_SMS = 32;  // SMs the second group's GEMM launches leave free
+
+struct InvGroup {
+    std::vector<int> members;  // chain indices
+    std::vector<std::vector<std::pair<int, int>>> rounds;
+    std::vector<int> round_kind;
+    int max_ctas = 0;          // GEMM grid cap (0: all SMs)
+    char *tc_ws = nullptr;
+    size_t tc_bytes = 0;
+};
+
 struct InvPlan {
     int *err = nullptr;
     CUtensorMap *dev_maps = nullptr;
     std::vector<CUtensorMap> maps;
     std::vector<MatWork> work;
     std::vector<std::vector<Op>> chains;
-    std::vector<std::vector<std::pair<int, int>>> rounds;
-    std::vector<int> round_kind;
+    std::vector<InvGroup> groups;  // groups[0]: the critical chains
     size_t longest = 0;
-    char *tc_ws = nullptr;
-    size_t tc_bytes = 0;
 };
 
 kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws, InvPlan &p, bool encode) {
@@ -639,18 +708,32 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
         p.longest = std::max(p.longest, p.chains[k].size());
     }
     if (p.maps.size() != (size_t)MAPS_PER_MATRIX * nbig) return KFAC_ERR_WORKSPACE;  // device map area
-    // engine scratch: the largest GEMM round
-    p.rounds = schedule_rounds(p.chains, p.round_kind);
-    size_t tcb = 0;
-    std::vector<TcJob> round;
-    for (size_t r = 0; r < p.rounds.size(); ++r) {
-        round.clear();
-        for (const auto &ki : p.rounds[r])
-            if (!p.chains[ki.first][ki.second].leaf) round.push_back(p.chains[ki.first][ki.second].g);
-        tcb = std::max(tcb, tc_workspace_bytes(round.data(), (int)round.size(), TC_KIND_TF32X3));
+    // groups: chains at least 3/4 as long as the longest form the critical
+    // group; a second group exists only if it is worth a stream of its own
+    p.groups.assign(1, InvGroup{});
+    InvGroup rest;
+    for (int k = 0; k < nmats; ++k) {
+        if (4 * p.chains[k].size() >= 3 * p.longest) p.groups[0].members.push_back(k);
+        else rest.members.push_back(k);
     }
-    p.tc_bytes = tcb;
-    p.tc_ws = ws.take<char>(tcb);
+    if (!rest.members.empty()) {
+        rest.max_ctas = std::max(1, device_sm_count() - RESERVED_SMS);
+        p.groups.push_back(rest);
+    }
+    // engine scratch of each group: its largest GEMM round
+    std::vector<TcJob> round;
+    for (InvGroup &g : p.groups) {
+        g.rounds = schedule_rounds(p.chains, g.members, g.round_kind);
+        size_t tcb = 0;
+        for (size_t r = 0; r < g.rounds.size(); ++r) {
+            round.clear();
+            for (const auto &ki : g.rounds[r])
+                if (!p.chains[ki.first][ki.second].leaf) round.push_back(p.chains[ki.first][ki.second].g);
+            tcb = std::max(tcb, tc_workspace_bytes(round.data(), (int)round.size(), TC_KIND_TF32X3, g.max_ctas));
+        }
+        g.tc_bytes = tcb;
+        g.tc_ws = ws.take<char>(tcb);
+    }
     return KFAC_OK;
 }
 
@@ -727,6 +810,61 @@ kfac_status damping_run(const InvMatrix *mats, int nlayers, float gamma, int pi_
     return KFAC_OK;
 }
 
+namespace {
+
+// Enqueue one group's rounds on a stream.
+kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st) {
+    std::vector<LeafJob> leaves;
+    std::vector<TcJob> gemms;
+    kfac_status s = KFAC_OK;
+    for (size_t r = 0; r < g.rounds.size(); ++r) {
+        leaves.clear();
+        gemms.clear();
+        for (const auto &ki : g.rounds[r]) {
+            const Op &op = p.chains[ki.first][ki.second];
+            if (op.leaf) leaves.push_back(op.lj); else gemms.push_back(op.g);
+        }
+        if (!leaves.empty() && (s = leaf_launch(leaves, st)) != KFAC_OK) return s;
+        if (!gemms.empty()) {
+            Arena tail(g.tc_ws, g.tc_bytes);
+            if ((s = tc_run(gemms.data(), (int)gemms.size(), TC_KIND_TF32X3, p.dev_maps, tail, p.err, st,
+                            g.max_ctas)) != KFAC_OK)
+                return s;
+        }
+    }
+    return KFAC_OK;
+}
+
+// Library-owned streams and events of one device for the two groups (created
+// on first use; the mutex also keeps concurrent callers from interleaving
+// their fork / join records on the shared events).
+struct GroupStreams {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t hi = nullptr, lo = nullptr;
+    cudaEvent_t fork = nullptr, done_hi = nullptr, done_lo = nullptr;
+};
+
+GroupStreams &group_streams(int dev) {
+    static GroupStreams gs[64];
+    return gs[dev & 63];
+}
+
+kfac_status ensure_streams(GroupStreams &g) {
+    if (g.ready) return KFAC_OK;
+    int least = 0, greatest = 0;
+    KFAC_CUDA_TRY(cudaDeviceGetStreamPriorityRange(&least, &greatest));
+    KFAC_CUDA_TRY(cudaStreamCreateWithPriority(&g.hi, cudaStreamNonBlocking, greatest));
+    KFAC_CUDA_TRY(cudaStreamCreateWithPriority(&g.lo, cudaStreamNonBlocking, least));
+    KFAC_CUDA_TRY(cudaEventCreateWithFlags(&g.fork, cudaEventDisableTiming));
+    KFAC_CUDA_TRY(cudaEventCreateWithFlags(&g.done_hi, cudaEventDisableTiming));
+    KFAC_CUDA_TRY(cudaEventCreateWithFlags(&g.done_lo, cudaEventDisableTiming));
+    g.ready = true;
+    return KFAC_OK;
+}
+
+}  // namespace
+
 kfac_status inv_run(const InvMatrix *mats, int nmats, const float *damp_dev, int *info_dev,
                     Arena &ws, cudaStream_t st) {
     InvPlan p;
@@ -744,23 +882,34 @@ kfac_status inv_run(const InvMatrix *mats, int nmats, const float *damp_dev, int
                         mats[k].out, mats[k].ldo, mats[k].out_bf16, mats[k].ldo_bf16, k, 0, 0, 0, 0};
     if ((s = tile_launch<true>(tm, damp_dev, st)) != KFAC_OK) return s;
 
-    // 2. rounds (see schedule_rounds): each round is one leaf or one GEMM launch
-    std::vector<LeafJob> leaves;
-    std::vector<TcJob> gemms;
-    for (size_t r = 0; r < p.rounds.size(); ++r) {
-        leaves.clear();
-        gemms.clear();
-        for (const auto &ki : p.rounds[r]) {
-            const Op &op = p.chains[ki.first][ki.second];
-            if (op.leaf) leaves.push_back(op.lj); else gemms.push_back(op.g);
+    // 2. rounds (see schedule_rounds): each round is one leaf or one GEMM
+    //    launch; with two groups, the critical one runs on a high-priority
+    //    stream and the other on a low-priority one, forked from and joined
+    //    back into the caller's stream
+    if (p.groups.size() == 1) {
+        if ((s = run_group(p, p.groups[0], st)) != KFAC_OK) return s;
+    } else {
+        int dev = 0;
+        KFAC_CUDA_TRY(cudaGetDevice(&dev));
+        GroupStreams &g = group_streams(dev);
+        std::lock_guard<std::mutex> lock(g.mu);
+        if ((s = ensure_streams(g)) != KFAC_OK) return s;
+        KFAC_CUDA_TRY(cudaEventRecord(g.fork, st));
+        KFAC_CUDA_TRY(cudaStreamWaitEvent(g.hi, g.fork, 0));
+        KFAC_CUDA_TRY(cudaStreamWaitEvent(g.lo, g.fork, 0));
+        const kfac_status s0 = run_group(p, p.groups[0], g.hi);
+        kfac_status s1;
+        {
+            const PdlScope no_pdl(false);
+            s1 = run_group(p, p.groups[1], g.lo);
         }
-        if (!leaves.empty() && (s = leaf_launch(leaves, st)) != KFAC_OK) return s;
-        if (!gemms.empty()) {
-            Arena tail(p.tc_ws, p.tc_bytes);
-            if ((s = tc_run(gemms.data(), (int)gemms.size(), TC_KIND_TF32X3, p.dev_maps, tail, p.err, st)) !=
-                KFAC_OK)
-                return s;
-        }
+        // join in every case, so that a capture or later work stays ordered
+        KFAC_CUDA_TRY(cudaEventRecord(g.done_hi, g.hi));
+        KFAC_CUDA_TRY(cudaEventRecord(g.done_lo, g.lo));
+        KFAC_CUDA_TRY(cudaStreamWaitEvent(st, g.done_hi, 0));
+        KFAC_CUDA_TRY(cudaStreamWaitEvent(st, g.done_lo, 0));
+        if (s0 != KFAC_OK) return s0;
+        if (s1 != KFAC_OK) return s1;
     }
 
     // 3. out = hi + lo, mirrored; bf16 copies

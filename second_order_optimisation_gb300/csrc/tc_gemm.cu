@@ -612,12 +612,11 @@ int tiles_of(const TcJob &j, int bn) {
     return n;
 }
 
-Plan make_plan(const TcJob *jobs, int n, int kind) {
+Plan make_plan(const TcJob *jobs, int n, int kind, int sms) {
     Plan p;
     p.ksplit.resize(n);
     p.tiles.resize(n);
     p.k_tiles.resize(n);
-    const int sms = device_sm_count();
     // A launch with few 128-wide tiles leaves most SMs idle and funnels each
     // tile's loads and stores through one SM: narrow the tiles (tf32x3 only)
     // until the launch covers at least half of the SMs.
@@ -723,9 +722,14 @@ kfac_status tc_upload_maps(const CUtensorMap *maps, int n, CUtensorMap *dev, cud
     return KFAC_OK;
 }
 
-size_t tc_workspace_bytes(const TcJob *jobs, int njobs, int kind) {
+int cta_cap(int max_ctas) {
+    const int sms = device_sm_count();
+    return max_ctas > 0 ? std::min(max_ctas, sms) : sms;
+}
+
+size_t tc_workspace_bytes(const TcJob *jobs, int njobs, int kind, int max_ctas) {
     if (njobs <= 0) return 0;
-    Plan p = make_plan(jobs, njobs, kind);
+    Plan p = make_plan(jobs, njobs, kind, cta_cap(max_ctas));
     Arena a;
     Buffers b;
     take_buffers(p, njobs, a, b);
@@ -733,7 +737,7 @@ size_t tc_workspace_bytes(const TcJob *jobs, int njobs, int kind) {
 }
 
 kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *dev_maps, Arena &ws,
-                   int *err, cudaStream_t st) {
+                   int *err, cudaStream_t st, int max_ctas) {
     if (njobs <= 0) return KFAC_OK;
     if ((kind == TC_KIND_BF16 ? set_smem_attr<TC_KIND_BF16>() : set_smem_attr<TC_KIND_TF32X3>()) != cudaSuccess)
         return KFAC_ERR_CUDA;
@@ -742,13 +746,13 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
         if (j.Ct && j.beta != 0.f) return KFAC_ERR_INVALID;                       // transposed copy needs beta == 0
         if (j.sym && (kind != TC_KIND_TF32X3 || j.M != j.N || j.epi != TC_EPI_SPLIT)) return KFAC_ERR_INVALID;
     }
-    Plan p = make_plan(jobs, njobs, kind);
+    const int sms = cta_cap(max_ctas);
+    Plan p = make_plan(jobs, njobs, kind, sms);
     Buffers bufs;
     take_buffers(p, njobs, ws, bufs);
     if (!ws.fits()) return KFAC_ERR_WORKSPACE;
     if (bufs.ncnt) KFAC_CUDA_TRY(cudaMemsetAsync(bufs.cnt_base, 0, bufs.ncnt * sizeof(int), st));
 
-    const int sms = device_sm_count();
     std::unique_ptr<TcParams> P(new TcParams);
     size_t pos = 0;
     while (pos < p.order.size()) {
