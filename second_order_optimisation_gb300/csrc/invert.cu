@@ -42,8 +42,7 @@ namespace kfac {
 namespace {
 
 constexpr int LEAF = 128;
-constexpr int LEAF_ROW_WARPS = 8;                    // leaf: warps owning the block
-constexpr int LEAF_THREADS = 32 * (LEAF_ROW_WARPS + 1);  // plus the publisher warp
+constexpr int LEAF_THREADS = 256;  // leaf: publisher warp + 7 warps owning the block
 constexpr int MAT_MAX = 224;
 // tensor maps of one matrix: X, T, U pairs, each as hi / lo with 128-row and
 // with 32-row boxes
@@ -312,59 +311,68 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 //   a_kj <- a_kj / a_kk,  a_ik <- -a_ik / a_kk,  a_kk <- 1 / a_kk
 // and after the last pivot the block holds its inverse.  No pivoting is
 // needed: every leading principal block of an SPD matrix is SPD.  Four
-// consecutive pivots K = {k .. k+3} together are the block step: with R the
-// rows K, P = R[:, K] and W = P^-1 R,
+// consecutive pivots K = {k .. k+3} (row group s = k / 4) together are the
+// block step: with R the rows K, P = R[:, K] and W = P^-1 R,
 //   a_ij -= a_iK W_Kj,  a_Kj <- W_Kj,  a_iK <- -a_iK P^-1,  a_KK <- P^-1.
 // The sweep keeps the block sign-symmetric -- a_ik = -a_ki when exactly one
 // of i, k has been pivoted, a_ik = a_ki otherwise -- so the pivot columns are
 // s_i R[:, i] (s_i = -1 for pivoted i) and the new ones -s_i W[:, i]: every
 // update is formed from rows K alone.
-// Roles: warps 0..7 own the block (warp w rows 16w .. 16w+15, lane l columns
-// 4l .. 4l+3) and apply one block step per barrier interval; warp 8 is the
-// publisher.  During step s it takes the rows of block s+1 (copied to shared
-// memory by their owner one step earlier), applies step s to them, inverts
-// their 4 x 4 diagonal block, and publishes W, s R, -s W and P^-1 of block
-// s+1 -- so that this serial chain overlaps the owners' bulk update.  A pivot
-// that is not positive and finite is recorded in info and eliminated as
-// 1 / a_kk = 0.
+// Roles (8 warps): warp 0 is the publisher; warps 1..7 own the 32 row groups
+// (lane l holds columns 4l .. 4l+3 of its warp's rows).  During step s the
+// publisher takes the rows of group s+1 (copied to shared memory by their
+// owner one step earlier), applies step s to them, inverts their 4 x 4
+// diagonal block and publishes W, s R, -s W and P^-1 of group s+1, while the
+// owners apply step s to their rows.  Warp 4 shares the publisher's SM
+// sub-partition and owns only 2 groups, the others 5 each, so that the
+// publisher's serial chain gets most of its sub-partition's issue slots.  A
+// pivot that is not positive and finite is recorded in info and eliminated
+// as 1 / a_kk = 0.
+__device__ __forceinline__ int leaf_group_start(int hw) {  // first row group of row warp hw (1..7)
+    return hw <= 3 ? 5 * (hw - 1) : hw == 4 ? 15 : 17 + 5 * (hw - 5);
+}
+__device__ __forceinline__ int leaf_group_count(int hw) { return hw == 4 ? 2 : 5; }
+
 __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_constant__ LeafParams P) {
     pdl_wait();
     pdl_trigger();
-    constexpr int N = LEAF, RW = N / LEAF_ROW_WARPS;  // 16 rows per row warp
-    constexpr int NB = N / 4;                         // block steps
+    constexpr int N = LEAF, NB = N / 4, MAXG = 5;
     __shared__ __align__(16) float wbuf[2][4][N];   // W = P^-1 R
     __shared__ __align__(16) float cbuf[2][4][N];   // s_i R[p][i]: the pivot columns
     __shared__ __align__(16) float fbuf[2][4][N];   // -s_i W[p][i]: the new pivot columns
     __shared__ __align__(16) float pbuf[2][16];     // P^-1
-    __shared__ __align__(16) float rbuf[2][4][N];   // raw rows of the block after next, for the publisher
+    __shared__ __align__(16) float rbuf[2][4][N];   // raw rows of the group after next, for the publisher
     __shared__ int bad;
     const LeafJob &J = P.j[blockIdx.x];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool publisher = warp == LEAF_ROW_WARPS;
+    const bool publisher = warp == 0;
+    const int g0 = publisher ? 0 : leaf_group_start(warp), gn = publisher ? 0 : leaf_group_count(warp);
     const unsigned FULL = 0xffffffffu;
 
-    float a[RW][4];
-    if (!publisher) {  // 16-byte pieces, every load issued before the first use
-        float4 h[RW], l[RW];
+    float a[4 * MAXG][4];
 #pragma unroll
-        for (int r = 0; r < RW; ++r) {
-            const long long o = (long long)(RW * warp + r) * J.ld + 4 * lane;
-            h[r] = *reinterpret_cast<const float4 *>(J.Xh + o);
-            l[r] = *reinterpret_cast<const float4 *>(J.Xl + o);
+    for (int lg = 0; lg < MAXG; ++lg) {  // 16-byte pieces, all loads issued before the first use
+        if (lg >= gn) break;
+        float4 h[4], l[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const long long o = (long long)(4 * (g0 + lg) + p) * J.ld + 4 * lane;
+            h[p] = *reinterpret_cast<const float4 *>(J.Xh + o);
+            l[p] = *reinterpret_cast<const float4 *>(J.Xl + o);
         }
 #pragma unroll
-        for (int r = 0; r < RW; ++r) {
-            a[r][0] = h[r].x + l[r].x;
-            a[r][1] = h[r].y + l[r].y;
-            a[r][2] = h[r].z + l[r].z;
-            a[r][3] = h[r].w + l[r].w;
+        for (int p = 0; p < 4; ++p) {
+            a[4 * lg + p][0] = h[p].x + l[p].x;
+            a[4 * lg + p][1] = h[p].y + l[p].y;
+            a[4 * lg + p][2] = h[p].z + l[p].z;
+            a[4 * lg + p][3] = h[p].w + l[p].w;
         }
-        if (warp == 0) {  // rows of blocks 0 and 1 for the publisher
+    }
+    if (warp == 1) {  // groups 0 and 1 for the publisher (both owned by warp 1)
 #pragma unroll
-            for (int p = 0; p < 8; ++p)
-                *reinterpret_cast<float4 *>(&rbuf[p >> 2][p & 3][4 * lane]) =
-                    make_float4(a[p][0], a[p][1], a[p][2], a[p][3]);
-        }
+        for (int p = 0; p < 8; ++p)
+            *reinterpret_cast<float4 *>(&rbuf[p >> 2][p & 3][4 * lane]) =
+                make_float4(a[p][0], a[p][1], a[p][2], a[p][3]);
     }
     if (tid == 0) bad = -1;
     __syncthreads();
@@ -470,66 +478,62 @@ __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_cons
     }
     __syncthreads();
 #pragma unroll 1
-    for (int kb = 0; kb < N / RW; ++kb) {
+    for (int s = 0; s < NB; ++s) {
+        const int k = 4 * s, buf = s & 1;
+        float w[4][4];
 #pragma unroll
-        for (int mm = 0; mm < RW / 4; ++mm) {
-            const int s = (RW / 4) * kb + mm, k = 4 * s, buf = mm & 1;
-            float w[4][4];
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                const float4 t = *reinterpret_cast<const float4 *>(&wbuf[buf][p][4 * lane]);
-                w[p][0] = t.x; w[p][1] = t.y; w[p][2] = t.z; w[p][3] = t.w;
+        for (int p = 0; p < 4; ++p) {
+            const float4 t = *reinterpret_cast<const float4 *>(&wbuf[buf][p][4 * lane]);
+            w[p][0] = t.x; w[p][1] = t.y; w[p][2] = t.z; w[p][3] = t.w;
+        }
+        const bool colfix = lane == s;  // this lane holds the pivot columns k .. k+3
+        if (publisher) {
+            if (s + 1 < NB) {  // group s+1: its rows as of step s-1, then step s
+                float R[4][4];
+                load_rows(R, s + 1);
+                step_rows(R, k + 4, buf, w, colfix);
+                publish(R, k + 4);
             }
-            const bool colfix = lane == (k >> 2);  // this lane holds the pivot columns
-            if (publisher) {
-                if (s + 1 < NB) {  // block s+1: its rows as of step s-1, then step s
-                    float R[4][4];
-                    load_rows(R, s + 1);
-                    step_rows(R, k + 4, buf, w, colfix);
-                    publish(R, k + 4);
-                }
-            } else {
+        } else {
 #pragma unroll
-                for (int r0 = 0; r0 < RW; r0 += 4) {
-                    float (&X)[4][4] = *reinterpret_cast<float (*)[4][4]>(&a[r0][0]);
-                    step_rows(X, RW * warp + r0, buf, w, colfix);
-                }
-                if (warp == kb) {  // the pivot rows and the pivot block
-                    const int kk = 4 * mm;
+            for (int lg = 0; lg < MAXG; ++lg) {
+                if (lg >= gn) break;
+                float (&X)[4][4] = *reinterpret_cast<float (*)[4][4]>(&a[4 * lg][0]);
+                step_rows(X, 4 * (g0 + lg), buf, w, colfix);
+                if (g0 + lg == s) {  // the pivot rows and the pivot block
 #pragma unroll
                     for (int p = 0; p < 4; ++p)
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) a[kk + p][c] = w[p][c];
+                        for (int c = 0; c < 4; ++c) X[p][c] = w[p][c];
                     if (colfix) {
 #pragma unroll
                         for (int p = 0; p < 4; ++p) {
                             const float4 t = *reinterpret_cast<const float4 *>(&pbuf[buf][4 * p]);
-                            a[kk + p][0] = t.x; a[kk + p][1] = t.y; a[kk + p][2] = t.z; a[kk + p][3] = t.w;
+                            X[p][0] = t.x; X[p][1] = t.y; X[p][2] = t.z; X[p][3] = t.w;
                         }
                     }
                 }
-                // rows of block s+2 (after this step) for the publisher
-                const int n2 = s + 2;
-                if (n2 < NB && warp == (4 * n2) / RW) {
-                    const int kl = (4 * n2) % RW;
+                if (g0 + lg == s + 2 && s + 2 < NB) {  // rows of group s+2 (after this step) for the publisher
 #pragma unroll
                     for (int p = 0; p < 4; ++p)
-                        *reinterpret_cast<float4 *>(&rbuf[n2 & 1][p][4 * lane]) =
-                            make_float4(a[kl + p][0], a[kl + p][1], a[kl + p][2], a[kl + p][3]);
+                        *reinterpret_cast<float4 *>(&rbuf[(s + 2) & 1][p][4 * lane]) =
+                            make_float4(X[p][0], X[p][1], X[p][2], X[p][3]);
                 }
             }
-            __syncthreads();
         }
+        __syncthreads();
     }
 
-    if (!publisher) {
 #pragma unroll
-        for (int r = 0; r < RW; ++r) {
-            const long long o = (long long)(RW * warp + r) * J.ld + 4 * lane;
-            const float4 h = make_float4(tf32_hi(a[r][0]), tf32_hi(a[r][1]), tf32_hi(a[r][2]), tf32_hi(a[r][3]));
+    for (int lg = 0; lg < MAXG; ++lg) {
+        if (lg >= gn) break;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const float *v = a[4 * lg + p];
+            const long long o = (long long)(4 * (g0 + lg) + p) * J.ld + 4 * lane;
+            const float4 h = make_float4(tf32_hi(v[0]), tf32_hi(v[1]), tf32_hi(v[2]), tf32_hi(v[3]));
             *reinterpret_cast<float4 *>(J.Xh + o) = h;
-            *reinterpret_cast<float4 *>(J.Xl + o) =
-                make_float4(a[r][0] - h.x, a[r][1] - h.y, a[r][2] - h.z, a[r][3] - h.w);
+            *reinterpret_cast<float4 *>(J.Xl + o) = make_float4(v[0] - h.x, v[1] - h.y, v[2] - h.z, v[3] - h.w);
         }
     }
     if (tid == 0 && bad >= 0 && J.info) atomicCAS(J.info, 0, J.o + bad + 1);
