@@ -83,7 +83,10 @@ def kernel_rooflines(kern, layers, batch, fl, pk, steps):
       tc_gemm_bf16 (precond)  2 dG^2 dA + 2 dG dA^2 per layer      (tensor, bf16 peak)
       tc_gemm_tf32x3          Schur GEMM flops (schur_gemm_flops)  (tensor, tf32 peak / 3 products)
       inv_leaf                128^3 per 128-block leaf             (fp32 ALU)
-      im2col                  bytes of the patch matrices written + inputs read (HBM)"""
+      im2col                  bytes of the patch matrices written + inputs read (HBM)
+      inv_prep                upper triangle of F read (4 B) + the (hi, lo) pair written, dp^2 x 8 B
+      inv_finish              upper triangle of the pair read (8 B) + fp32 and bf16 inverses written
+                              (d^2 x 6 B)                          (HBM)"""
     tf32x3_peak = pk["bf16"] * (1.1 / 2.25) / 3.0
     schur = sum(schur_gemm_flops(L.d_a) + schur_gemm_flops(L.d_g) for L in layers)
     leaves = sum(leaf_count(L.d_a) + leaf_count(L.d_g) for L in layers)
@@ -91,7 +94,13 @@ def kernel_rooflines(kern, layers, batch, fl, pk, steps):
     for L in layers:
         if L.k > 1 or L.stride > 1:
             im2col_bytes += L.rows(batch) * L.k * L.k * L.cin * 2 + batch * L.hin * L.hin * L.cin * 2
+    pad = lambda d: (d + 127) // 128 * 128
+    dims = [L.d_a for L in layers] + [L.d_g for L in layers]
+    prep_bytes = sum(d * (d + 1) // 2 * 4 + pad(d) ** 2 * 8 for d in dims)
+    finish_bytes = sum(d * (d + 1) // 2 * 8 + d * d * 6 for d in dims)
     work = {("factors", "tc_gemm_bf16"): (fl["syrk"], "tensor", pk["bf16"], "TFLOP/s"),
+            ("inverse", "inv_prep"): (prep_bytes, "hbm", pk["hbm"], "GB/s"),
+            ("inverse", "inv_finish"): (finish_bytes, "hbm", pk["hbm"], "GB/s"),
             ("precond", "tc_gemm_bf16"): (fl["precond"], "tensor", pk["bf16"], "TFLOP/s"),
             ("inverse", "tc_gemm_tf32x3"): (schur, "tensor", tf32x3_peak, "TFLOP/s"),
             ("inverse", "inv_leaf"): (leaves * 128 ** 3, "alu", FP32_ALU_PEAK_TFLOPS, "TFLOP/s"),

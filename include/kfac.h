@@ -25,8 +25,10 @@
  *     initialisation and are clobbered.
  *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and is asynchronous: results are ready once the stream has
- *     reached that point.  The library keeps no global state; concurrent calls
- *     on different streams with disjoint buffers and workspaces are allowed.
+ *     reached that point.  The library keeps no global state beyond the
+ *     per-device streams and events of kfac_damp_invert (below); concurrent
+ *     calls on different streams with disjoint buffers and workspaces are
+ *     allowed.
  *   - KFAC_ERR_INVALID / KFAC_ERR_UNSUPPORTED / KFAC_ERR_WORKSPACE are
  *     returned BEFORE anything is enqueued (outputs untouched).
  *     KFAC_ERR_CUDA reports a launch failure (cudaGetLastError after a
@@ -134,8 +136,17 @@ kfac_status kfac_factor_update(const kfac_factor_desc *descs, int count,
  *     damp_A = damp_G = sqrt(gamma)                              (pi_split == 0)
  * and writes the FULL symmetric fp32 inverses
  *     A_inv = (A + damp_A I)^-1,  G_inv = (G + damp_G I)^-1
- * computed in fp32 by a blocked Cholesky-based inversion.  Only the upper
- * triangles of A and G are read.  Optional bf16 copies of the inverses are
+ * computed in fp32 by block elimination: Schur complements on tensor cores
+ * (three tf32 products per slice) down to 128 x 128 blocks inverted by a
+ * Gauss-Jordan sweep.  Only the upper triangles of A and G are read.
+ *
+ * Streams: the call is ordered on `stream` as a whole.  When its matrices
+ * form chains of very different length, the middle part forks onto two
+ * library-owned streams of the current device (the longest chains at high
+ * priority, the rest at low priority; created on the first such call,
+ * with three events) and joins back into `stream` before the final kernel,
+ * so stream capture records a graph with two parallel branches.  Make the
+ * first call of a process outside stream capture.  Optional bf16 copies of the inverses are
  * written when the *_bf16 pointers are non-NULL (their ld must be a multiple
  * of 8 elements and their base 16-byte aligned, for the tensor-core
  * preconditioner).

@@ -7,13 +7,14 @@
 // method it builds on):
 //     pi = sqrt((tr A/dA) / (tr G/dG)),  damp_A = pi sqrt(gamma),  damp_G = sqrt(gamma)/pi.
 //
-// Algorithm (every matrix of the call advances in batched rounds, one launch
-// per round, see schedule_rounds):
+// Algorithm (the matrices advance in batched rounds, one launch per round, see
+// schedule_rounds; the longest chains and the rest run as two concurrent
+// groups, see InvGroup):
 //   1. traces -> damping values (one CTA per layer, fixed reduction order);
 //   2. X = sym(F) + damp I, padded with an identity block to a multiple of
 //      128 (the inverse of diag(X, I) is diag(X^-1, I)), stored as a (hi, lo)
 //      pair with hi exactly representable in tf32 and hi + lo = X;
-//   3. blocked Cholesky-based inversion by recursive 2x2 blocking on 128-row
+//   3. inversion by recursive 2x2 blocking on 128-row
 //      block boundaries; the Schur complement X22 - X21 X11^-1 X12 is the
 //      trailing update of a block Cholesky step:
 //        X11 <- X11^-1                               (recursion / leaf)
