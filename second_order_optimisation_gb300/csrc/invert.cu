@@ -32,6 +32,7 @@
 // A pivot that is not positive and finite records its 1-based index in
 // info[matrix]; nothing traps or waits.
 #include <algorithm>
+#include <cfloat>
 #include <memory>
 #include <mutex>
 #include <vector>
@@ -387,11 +388,12 @@ __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_cons
         for (int p = 0; p < 4; ++p)
 #pragma unroll
             for (int q = 0; q < 4; ++q) b[p][q] = R[p][q];
+        int first_bad = -1;  // branch-free inside the serial chain; recorded once below
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
             const float x = b[v][v];
-            const bool ok = x > 0.f && isfinite(x);
-            if (lane == (kn >> 2) && !ok && bad < 0) bad = kn + v;
+            const bool ok = x > 0.f && x <= FLT_MAX;  // positive and finite (NaN fails both)
+            first_bad = (!ok && first_bad < 0) ? kn + v : first_bad;
             const float d = ok ? recip_nr(x) : 0.f;
             float t[4];
 #pragma unroll
@@ -409,6 +411,7 @@ __global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_cons
                 if (i != v) b[i][v] = -t[i];
             b[v][v] = d;
         }
+        if (lane == (kn >> 2) && first_bad >= 0 && bad < 0) bad = first_bad;
         float pi[4][4];
 #pragma unroll
         for (int p = 0; p < 4; ++p)
