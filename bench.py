@@ -83,7 +83,7 @@ def kernel_rooflines(kern, layers, batch, fl, pk, steps):
       tc_gemm_bf16 (precond)  2 dG^2 dA + 2 dG dA^2 per layer      (tensor, bf16 peak)
       tc_gemm_tf32x3          Schur GEMM flops (schur_gemm_flops)  (tensor, tf32 peak / 3 products)
       inv_leaf                128^3 per 128-block leaf             (fp32 ALU)
-      im2col                  bytes of the patch matrices written + inputs read (HBM)
+      im2col                  bytes of the materialised patch matrices written + inputs read (HBM)
       inv_prep                upper triangle of F read (4 B) + the (hi, lo) pair written, dp^2 x 8 B
       inv_finish              upper triangle of the pair read (8 B) + fp32 and bf16 inverses written
                               (d^2 x 6 B)                          (HBM)"""
@@ -92,7 +92,9 @@ def kernel_rooflines(kern, layers, batch, fl, pk, steps):
     leaves = sum(leaf_count(L.d_a) + leaf_count(L.d_g) for L in layers)
     im2col_bytes = 0
     for L in layers:
-        if L.k > 1 or L.stride > 1:
+        # patches are materialised only where the SYRK cannot read the input
+        # through an im2col tensor map (channels not in whole 64-wide taps)
+        if (L.k > 1 or L.stride > 1) and L.cin % 64 != 0:
             im2col_bytes += L.rows(batch) * L.k * L.k * L.cin * 2 + batch * L.hin * L.hin * L.cin * 2
     pad = lambda d: (d + 127) // 128 * 128
     dims = [L.d_a for L in layers] + [L.d_g for L in layers]

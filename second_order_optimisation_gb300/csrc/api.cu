@@ -89,6 +89,20 @@ EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
+EncodeIm2colFn encode_im2col_fn() {
+    static std::once_flag once;
+    static EncodeIm2colFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeIm2colFn)p;
+    });
+    return fn;
+}
+
 namespace {
 
 struct FactorGeom {
@@ -164,6 +178,30 @@ kfac_status plan_factor(const kfac_factor_desc *descs, int count, const std::vec
                                        d.pad_h, d.pad_w, g.ho, g.wo, d.append_one, P, ldp});
             p.sg.push_back(SgJob{P, ldp, 1, P, ldp, 0, d.F, d.ldf, nullptr, 0, g.d, g.d, (int)g.M,
                                  d.alpha, d.beta, 1});
+            continue;
+        }
+        // a convolution whose channels fill 64-wide taps is read straight
+        // from its input through an im2col tensor map (no patch matrix)
+        const bool implicit = !g.direct && !d.append_one && d.c % 64 == 0 && d.kh == d.kw &&
+                              d.stride_h == d.stride_w && d.pad_h == d.pad_w && d.stride_h <= 8 &&
+                              d.pad_h <= 127 && d.pad_h - (d.kh - 1) >= -128 && d.kh <= 255 &&
+                              ((uintptr_t)d.x % 16) == 0;
+        if (implicit) {
+            TcJob j{};
+            j.map_a = j.map_b = (int)p.maps.size();
+            p.maps.emplace_back();
+            if (encode && !tc_make_im2col_map(&p.maps.back(), d.x, d.n, d.h, d.w, d.c, d.kh, d.stride_h, d.pad_h))
+                return KFAC_ERR_CUDA;
+            j.a_mn = j.b_mn = 1;
+            j.M = g.dcore; j.N = g.dcore; j.K = (int)g.M;
+            j.syrk = 1;
+            j.epi = TC_EPI_ACCUM;
+            j.alpha = d.alpha; j.beta = d.beta;
+            j.C = d.F; j.ldc = d.ldf;
+            j.im2col = 1;
+            j.im_c = d.c; j.im_k = d.kh; j.im_stride = d.stride_h; j.im_pad = d.pad_h;
+            j.im_wo = g.wo; j.im_howo = g.ho * g.wo;
+            p.tc.push_back(j);
             continue;
         }
         const uint16_t *src;

@@ -47,14 +47,22 @@ struct TcJob {
     long long ldct;
     uint16_t *Cb;
     long long ldcb;
+    // BF16 SYRK of a convolution read straight from its NHWC input through an
+    // im2col tensor map (map_a): K runs over output pixels, the MN index over
+    // d = (r * k + s) * c + channel.  c is a multiple of 64.
+    int im2col;
+    int im_c, im_k, im_stride, im_pad, im_wo, im_howo;
 };
 
 // Tensor map of a row-major [rows][cols] matrix (ld elements) for the engine:
-// 128-byte swizzle, box 128 bytes wide and box_rows rows (default: 128, or 64
-// if mn_major).  A tf32x3 operand is a run of four maps: hi and lo with
+// 128-byte swizzle, box 128 bytes wide and box_rows rows (default 128).  A tf32x3 operand is a run of four maps: hi and lo with
 // 128-row boxes, then hi and lo with 32-row boxes (B of narrow tiles).
 bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int mn_major,
                  int box_rows = 0);
+// Im2col tensor map of a bf16 NHWC tensor [n][h][w][c] for a square k x k
+// convolution (stride, pad): 64 channels x 128 output pixels per load,
+// 128-byte swizzle.  Requires c % 64 == 0 and a 16-byte aligned base.
+bool tc_make_im2col_map(CUtensorMap *m, const void *x, int n, int h, int w, int c, int k, int stride, int pad);
 // Copies host-built maps into device memory (128-byte aligned) on the stream.
 kfac_status tc_upload_maps(const CUtensorMap *maps, int n, CUtensorMap *dev, cudaStream_t st);
 // Workspace needed by tc_run for these jobs (split-K partials, counters).

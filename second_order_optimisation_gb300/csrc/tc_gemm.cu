@@ -37,10 +37,10 @@ namespace kfac {
 namespace {
 
 constexpr int BM = 128, BN = 128;
-constexpr int TILE_BYTES = 128 * 128;  // one 128-row x 128-byte operand tile
+constexpr int TILE_BYTES = 128 * 128;  // one tf32 operand tile: 128 rows x 128 bytes
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int MAX_PROBS = 192;
+constexpr int MAX_PROBS = 176;
 constexpr int MAPS_PER_COPY = 240;
 constexpr int STAGE_LD = 36;                              // epilogue staging row pitch (floats)
 constexpr size_t EPI_STAGE_BYTES = 4 * 32 * STAGE_LD * sizeof(float);
@@ -48,10 +48,13 @@ constexpr size_t SMEM_BYTES = 192 * 1024 + 1024 /*align*/ + 256 /*barriers*/ + E
 
 template <int KIND> struct Traits;
 template <> struct Traits<TC_KIND_BF16> {
-    static constexpr int BK = 64, STAGES = 6, TILES = 2, ESZ = 2;
+    // 128 K per stage: every operand box is 64 x 128 elements (16 KB); a
+    // streaming SM sustains about twice the bytes with 16 KB TMA boxes as
+    // with 8 KB ones (the per-SM rate of box loads is the limit)
+    static constexpr int BK = 128, STAGES = 3, TILES = 2, ESZ = 2, TILE = 128 * 128 * 2;
 };
 template <> struct Traits<TC_KIND_TF32X3> {
-    static constexpr int BK = 32, STAGES = 3, TILES = 4, ESZ = 4;
+    static constexpr int BK = 32, STAGES = 3, TILES = 4, ESZ = 4, TILE = TILE_BYTES;
 };
 
 struct TcProb {
@@ -66,6 +69,8 @@ struct TcProb {
     uint8_t syrk, sym, epi;
     uint8_t vec;             // C (and C_lo) rows take 16-byte accesses (ldc % 4 == 0, aligned)
     uint8_t vecb;            // Cb rows take 8-byte accesses
+    uint8_t im2col, im_k, im_stride, im_pad;  // operands through an im2col map (see TcJob)
+    int im_c, im_wo, im_ho, im_howo;
     float alpha, beta;
     float *C;
     float *C_lo;
@@ -153,27 +158,102 @@ __device__ __forceinline__ void load_rows_tf32(uint8_t *dst, const CUtensorMap *
     for (int r = 0; r < rows; r += 32) tma_load_2d(dst + r * 128, map, col0 + k0, row0 + mn0 + r, bar);
 }
 
-// One 128 (M or N) x BK (K) operand tile into shared memory.
-//   K-major source  [MN][K]: one BK x 128 box (128-byte rows).
-//   MN-major source [K][MN] (bf16): two 64 x 64 boxes (MN 0-63 | 64-127), 8 KB apart.
-__device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, int mn_major, int row0,
-                                          int col0, int mn0, int k0, uint64_t *bar) {
-    if (mn_major) {
-        tma_load_2d(dst, map, col0 + mn0, row0 + k0, bar);
-        tma_load_2d(dst + 8192, map, col0 + mn0 + 64, row0 + k0, bar);
-    } else {
-        tma_load_2d(dst, map, col0 + k0, row0 + mn0, bar);
+__device__ __forceinline__ void tma_load_im2col_4d(void *dst, const CUtensorMap *map, int c, int w, int h, int n,
+                                                   uint16_t off_w, uint16_t off_h, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8};" ::"r"(smem_u32(dst)),
+        "l"((uint64_t)map), "r"(c), "r"(w), "r"(h), "r"(n), "r"(smem_u32(bar)), "h"(off_w), "h"(off_h)
+        : "memory");
+}
+
+// Producer state for a convolution's patch-matrix operands read through the
+// im2col map.  A 128-wide MN (= d) block is two 64-wide halves, each one
+// filter tap (r, s) and 64 channels; a K tile is 128 consecutive output pixels
+// (rows past the end of the batch fall outside the tensor and read 0).  The
+// taps are decomposed once per work item and the pixel position advances by
+// 128 per K tile without divisions, so the single producer thread keeps up
+// with the MMAs.
+struct Im2colCursor {
+    int c0[4], sx[4], r[4];  // A halves 0, 1; B halves 0, 1
+    int img, ho, wo;         // first output pixel of the next K tile
+};
+
+__device__ __forceinline__ void im2col_taps(const TcProb &q, int mn0, int *c0, int *sx, int *r) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        // a half past the last tap only feeds outputs that are never stored:
+        // load a valid one instead
+        const int d0 = min(mn0 + 64 * half, q.M - 64);
+        const int rs = d0 / q.im_c;
+        c0[half] = d0 - rs * q.im_c;
+        r[half] = rs / q.im_k;
+        sx[half] = rs - r[half] * q.im_k;
     }
 }
 
-// Descriptor of the kk-th 32-byte K slice of a staged operand tile.
+__device__ __forceinline__ void im2col_start(const TcProb &q, const Work &k, Im2colCursor &cur) {
+    im2col_taps(q, k.tm * BM, cur.c0, cur.sx, cur.r);
+    im2col_taps(q, k.tn * BN, cur.c0 + 2, cur.sx + 2, cur.r + 2);
+    const int m0 = k.kt0 * 128;
+    cur.img = m0 / q.im_howo;
+    const int rem = m0 - cur.img * q.im_howo;
+    cur.ho = rem / q.im_wo;
+    cur.wo = rem - cur.ho * q.im_wo;
+}
+
+__device__ __forceinline__ void im2col_load(uint8_t *dst, const CUtensorMap *map, const TcProb &q,
+                                            const Im2colCursor &cur, int which, uint64_t *bar) {
+    const int w = cur.wo * q.im_stride - q.im_pad, h = cur.ho * q.im_stride - q.im_pad;
+#pragma unroll
+    for (int half = 0; half < 2; ++half)
+        tma_load_im2col_4d(dst + 16384 * half, map, cur.c0[2 * which + half], w, h, cur.img,
+                           (uint16_t)cur.sx[2 * which + half], (uint16_t)cur.r[2 * which + half], bar);
+}
+
+__device__ __forceinline__ void im2col_advance(const TcProb &q, Im2colCursor &cur) {
+    cur.wo += 128;
+    while (cur.wo >= q.im_wo) {
+        cur.wo -= q.im_wo;
+        if (++cur.ho == q.im_ho) {
+            cur.ho = 0;
+            ++cur.img;
+        }
+    }
+}
+
+// One 128 (M or N) x BK (K) operand tile into shared memory.
+//   tf32, K-major source [MN][K]: one 32 x 128 box (128-byte rows).
+//   bf16, K-major source [MN][K]: two 64 x 128 boxes (K 0-63 | 64-127), 16 KB apart.
+//   bf16, MN-major source [K][MN]: two 64 x 128 boxes (MN 0-63 | 64-127), 16 KB apart.
+__device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, int mn_major, int row0,
+                                          int col0, int mn0, int k0, uint64_t *bar) {
+    tma_load_2d(dst, map, col0 + k0, row0 + mn0, bar);
+}
+__device__ __forceinline__ void load_tile_bf16(uint8_t *dst, const CUtensorMap *map, int mn_major, int row0,
+                                               int col0, int mn0, int k0, uint64_t *bar) {
+    if (mn_major) {
+        tma_load_2d(dst, map, col0 + mn0, row0 + k0, bar);
+        tma_load_2d(dst + 16384, map, col0 + mn0 + 64, row0 + k0, bar);
+    } else {
+        tma_load_2d(dst, map, col0 + k0, row0 + mn0, bar);
+        tma_load_2d(dst + 16384, map, col0 + k0 + 64, row0 + mn0, bar);
+    }
+}
+
+// Descriptors of the kk-th 32-byte K slice of a staged operand tile.
+// tf32 (K-major): 128-byte rows, 8-row groups 1024 B apart (SBO); a slice is
+//   32 B (8 tf32) inside the swizzled row.
 __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, int kk) {
-    // MN-major (bf16): 8-row K groups 1024 B apart (SBO), the two 64-wide MN
-    //   blocks 8192 B apart (LBO); a K=16 slice spans two K groups.
-    // K-major: 128-byte rows, 8-row groups 1024 B apart (SBO); a slice is 32 B
-    //   inside the swizzled row (16 bf16 or 8 tf32).
-    return mn_major ? smem_desc_sw128(base + kk * 2048, 8192, 1024)
-                    : smem_desc_sw128(base + kk * 32, 16, 1024);
+    return smem_desc_sw128(base + kk * 32, 16, 1024);
+}
+// bf16 (16 elements per slice, 8 slices per 128-K stage):
+//   MN-major: 8-row K groups 1024 B apart (SBO), the two 64-wide MN blocks
+//     16 KB apart (LBO); a slice spans two K groups.
+//   K-major: slices 0-3 in the first 64-K box, 4-7 in the second (16 KB on).
+__device__ __forceinline__ uint64_t operand_desc_bf16(uint32_t base, int mn_major, int kk) {
+    return mn_major ? smem_desc_sw128(base + kk * 2048, 16384, 1024)
+                    : smem_desc_sw128(base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
 }
 
 __device__ __forceinline__ float tf32_hi(float v) {
@@ -356,7 +436,7 @@ __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, con
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams P) {
     using Tr = Traits<KIND>;
-    constexpr int STAGE_BYTES = Tr::TILES * TILE_BYTES;
+    constexpr int STAGE_BYTES = Tr::TILES * Tr::TILE;
     constexpr int KSLICES = Tr::BK * Tr::ESZ / 32;  // 32-byte MMA K slices per stage (4)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -414,8 +494,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     last_p = k.p;
                 }
                 const bool diag = KIND == TC_KIND_BF16 && q.syrk && k.tm == k.tn;
+                Im2colCursor cur;
+                if (KIND == TC_KIND_BF16 && q.im2col) im2col_start(q, k, cur);
                 const uint32_t bytes = KIND == TC_KIND_TF32X3 ? (uint32_t)(2 * (BM + q.bn) * 128)
-                                       : diag                 ? (uint32_t)TILE_BYTES
+                                       : diag                 ? (uint32_t)Tr::TILE
                                                               : (uint32_t)STAGE_BYTES;
                 for (int kt = k.kt0; kt < k.kt1; ++kt) {
                     if (!mbar_wait(&empty[stage], phase ^ 1)) {
@@ -426,11 +508,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     mbar_arrive_expect_tx(&full[stage], bytes);
                     uint8_t *sa = smem + stage * STAGE_BYTES;
                     const int k0 = kt * Tr::BK;
-                    if (KIND == TC_KIND_BF16) {
-                        load_tile(sa, ma, q.a_mn, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
+                    if (KIND == TC_KIND_BF16 && q.im2col) {
+                        im2col_load(sa, ma, q, cur, 0, &full[stage]);
+                        if (!diag) im2col_load(sa + Tr::TILE, mb, q, cur, 1, &full[stage]);
+                        im2col_advance(q, cur);
+                    } else if (KIND == TC_KIND_BF16) {
+                        load_tile_bf16(sa, ma, q.a_mn, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
                         if (!diag)
-                            load_tile(sa + TILE_BYTES, mb, q.b_mn, q.b_row0, q.b_col0, k.tn * BN, k0,
-                                      &full[stage]);
+                            load_tile_bf16(sa + Tr::TILE, mb, q.b_mn, q.b_row0, q.b_col0, k.tn * BN, k0,
+                                           &full[stage]);
                     } else {
                         load_tile(sa, ma, 0, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
                         load_tile(sa + TILE_BYTES, ma + 1, 0, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
@@ -480,10 +566,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     tc_fence_after();
                     const uint32_t s0 = smem_u32(smem + stage * STAGE_BYTES);
                     if (KIND == TC_KIND_BF16) {
-                        const uint32_t b_base = diag ? s0 : s0 + TILE_BYTES;
+                        const uint32_t b_base = diag ? s0 : s0 + Tr::TILE;
 #pragma unroll
                         for (int kk = 0; kk < KSLICES; ++kk)
-                            tc_mma_f16(d_tmem, operand_desc(s0, q.a_mn, kk), operand_desc(b_base, q.b_mn, kk),
+                            tc_mma_f16(d_tmem, operand_desc_bf16(s0, q.a_mn, kk), operand_desc_bf16(b_base, q.b_mn, kk),
                                        idesc, (kt > k.kt0 || kk > 0) ? 1u : 0u);
                     } else {
                         const uint32_t ah = s0, al = s0 + TILE_BYTES, bh = s0 + 2 * TILE_BYTES,
@@ -701,11 +787,27 @@ bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int ro
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ld * esz};
     const cuuint32_t inner = 128u / esz;  // 128-byte rows
-    cuuint32_t box[2] = {inner, box_rows > 0 ? (cuuint32_t)box_rows : mn_major ? 64u : 128u};
+    cuuint32_t box[2] = {inner, box_rows > 0 ? (cuuint32_t)box_rows : 128u};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = enc(m, kind == TC_KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                      2, (void *)ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool tc_make_im2col_map(CUtensorMap *m, const void *x, int n, int h, int w, int c, int k, int stride, int pad) {
+    EncodeIm2colFn enc = encode_im2col_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)c, (cuuint64_t)w, (cuuint64_t)h, (cuuint64_t)n};
+    cuuint64_t strides[3] = {(cuuint64_t)c * 2, (cuuint64_t)w * c * 2, (cuuint64_t)h * w * c * 2};
+    // base pixels run from -pad to the last one whose k x k window still
+    // starts inside the padded input (offsets from the two corners)
+    int lower[2] = {-pad, -pad};
+    int upper[2] = {pad - (k - 1), pad - (k - 1)};
+    cuuint32_t estr[4] = {1u, (cuuint32_t)stride, (cuuint32_t)stride, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void *)x, dims, strides, lower, upper, 64u, 128u, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -787,6 +889,10 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
             q.Cb = j.Cb; q.ldcb = j.ldcb;
             q.vec = (j.ldc % 4 == 0) && ((uintptr_t)j.C % 16 == 0) && ((uintptr_t)j.C_lo % 16 == 0);
             q.vecb = (j.ldcb % 4 == 0) && ((uintptr_t)j.Cb % 8 == 0);
+            q.im2col = j.im2col ? 1 : 0;
+            q.im_k = (uint8_t)j.im_k; q.im_stride = (uint8_t)j.im_stride; q.im_pad = (uint8_t)j.im_pad;
+            q.im_c = j.im_c; q.im_wo = j.im_wo; q.im_howo = j.im_howo;
+            q.im_ho = j.im_wo > 0 ? j.im_howo / j.im_wo : 0;
             q.partial = bufs.part[ji];
             q.counters = bufs.cnt[ji];
             work += p.tiles[ji] * p.ksplit[ji];

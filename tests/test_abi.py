@@ -62,11 +62,18 @@ def test_factor_update_rejects_invalid(lib, bad):
     assert lib.kfac_factor_update_workspace_size(arr, 1) == 0
 
 
-def test_factor_update_workspace_and_count_checks(lib):
+def test_factor_update_implicit_im2col_needs_no_patch_matrix(lib):
+    # c = 64 fills whole 64-channel taps: the SYRK reads the input through an
+    # im2col tensor map and no patch matrix is laid out
     arr = (kfac.FactorDesc * 1)(_fdesc())
+    assert 0 < lib.kfac_factor_update_workspace_size(arr, 1) < 4 * 6 * 6 * 576 * 2
+
+
+def test_factor_update_workspace_and_count_checks(lib):
+    arr = (kfac.FactorDesc * 1)(_fdesc(c=8, ldf=72))
     need = lib.kfac_factor_update_workspace_size(arr, 1)
-    # patch matrix of 4*6*6 rows x 576 bf16 columns must fit in the workspace
-    assert need >= 4 * 6 * 6 * 576 * 2
+    # c = 8: the patch matrix of 4*6*6 rows x 72 bf16 columns must fit in the workspace
+    assert need >= 4 * 6 * 6 * 72 * 2
     assert lib.kfac_factor_update(arr, 1, None, 0, None) == kfac.KFAC_ERR_WORKSPACE
     assert lib.kfac_factor_update(arr, 1, 0x1001, need, None) == kfac.KFAC_ERR_WORKSPACE  # misaligned
     assert lib.kfac_factor_update(arr, 1, 0x100000, need - 1024, None) == kfac.KFAC_ERR_WORKSPACE

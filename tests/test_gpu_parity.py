@@ -79,6 +79,10 @@ FACTOR_CASES = [
     ("conv1x1s2", (2, 10, 10, 72), 1, 2, 0, False),
     ("conv1x1_tall", (16, 14, 14, 64), 1, 1, 0, False),
     ("conv3x3_wide", (2, 7, 7, 136), 3, 1, 1, False),
+    # channels in whole 64-wide taps: bf16 reads the input through an im2col tensor map
+    ("conv3x3s2_c128", (3, 11, 11, 128), 3, 2, 1, False),
+    ("conv1x1s2_c64", (2, 9, 9, 64), 1, 2, 0, False),
+    ("conv3x3_c192_wrap", (5, 5, 5, 192), 3, 1, 1, False),
 ]
 
 
