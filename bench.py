@@ -31,7 +31,6 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "ResNet-50 K-FAC step ms (factors+inverse+precond); TFLOP/s vs GB300 peak"
-FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12   # SMs x fp32 lanes x FMA x max clock
 
 
 # ------------------------------------------------------------------ workloads
@@ -57,12 +56,13 @@ def flops(layers, batch):
     return dict(syrk=syrk, inv=inv, precond=pc, total=syrk + inv + pc)
 
 
-def schur_gemm_flops(d, leaf=128):
+def schur_gemm_flops(d, leaf=128, leaf_max=256):
     """Useful fp32 flops of the tensor-core Schur-complement GEMMs that invert
     one d x d factor (padded to a multiple of 128, split on 128-row block
-    boundaries; the two symmetric updates count half)."""
+    boundaries down to leaves of 128 or 256 rows; the two symmetric updates
+    count half)."""
     def rec(n):
-        if n <= leaf:
+        if n <= leaf or n == leaf_max:
             return 0
         nb = n // leaf
         h = leaf * (nb // 2)
@@ -72,8 +72,24 @@ def schur_gemm_flops(d, leaf=128):
     return rec(dp)
 
 
-def leaf_count(d, leaf=128):
-    return -(-d // leaf)
+def leaf_sizes(d, leaf=128, leaf_max=256):
+    """Block sizes of the leaves that invert one d x d factor."""
+    out = []
+    def rec(n):
+        if n <= leaf or n == leaf_max:
+            out.append(n)
+            return
+        nb = n // leaf
+        h = leaf * (nb // 2)
+        rec(h)
+        rec(n - h)
+    rec(-(-d // leaf) * leaf)
+    return out
+
+
+def leaf_flops(n):
+    """Gauss-Jordan inverse of an n x n block: n^3 multiply-adds (2 n^3 flops)."""
+    return 2 * n ** 3
 
 
 def kernel_rooflines(kern, layers, batch, fl, pk, steps):
@@ -82,14 +98,14 @@ def kernel_rooflines(kern, layers, batch, fl, pk, steps):
       tc_gemm_bf16 (factors)  SYRK M*d(d+1) per factor            (tensor, bf16 peak)
       tc_gemm_bf16 (precond)  2 dG^2 dA + 2 dG dA^2 per layer      (tensor, bf16 peak)
       tc_gemm_tf32x3          Schur GEMM flops (schur_gemm_flops)  (tensor, tf32 peak / 3 products)
-      inv_leaf                128^3 per 128-block leaf             (fp32 ALU)
+      inv_leaf                2 n^3 per n-block leaf (n = 128, 256)  (tensor, tf32 peak / 3 products)
       im2col                  bytes of the materialised patch matrices written + inputs read (HBM)
       inv_prep                upper triangle of F read (4 B) + the (hi, lo) pair written, dp^2 x 8 B
       inv_finish              upper triangle of the pair read (8 B) + fp32 and bf16 inverses written
                               (d^2 x 6 B)                          (HBM)"""
     tf32x3_peak = pk["bf16"] * (1.1 / 2.25) / 3.0
     schur = sum(schur_gemm_flops(L.d_a) + schur_gemm_flops(L.d_g) for L in layers)
-    leaves = sum(leaf_count(L.d_a) + leaf_count(L.d_g) for L in layers)
+    leaves = sum(leaf_flops(n) for L in layers for d in (L.d_a, L.d_g) for n in leaf_sizes(d))
     im2col_bytes = 0
     for L in layers:
         # patches are materialised only where the SYRK cannot read the input
@@ -105,7 +121,7 @@ def kernel_rooflines(kern, layers, batch, fl, pk, steps):
             ("inverse", "inv_finish"): (finish_bytes, "hbm", pk["hbm"], "GB/s"),
             ("precond", "tc_gemm_bf16"): (fl["precond"], "tensor", pk["bf16"], "TFLOP/s"),
             ("inverse", "tc_gemm_tf32x3"): (schur, "tensor", tf32x3_peak, "TFLOP/s"),
-            ("inverse", "inv_leaf"): (leaves * 128 ** 3, "alu", FP32_ALU_PEAK_TFLOPS, "TFLOP/s"),
+            ("inverse", "inv_leaf"): (leaves, "tensor", tf32x3_peak, "TFLOP/s"),
             ("factors", "im2col"): (im2col_bytes, "hbm", pk["hbm"], "GB/s")}
     out = {}
     for ph, ks in kern.items():

@@ -137,8 +137,10 @@ kfac_status kfac_factor_update(const kfac_factor_desc *descs, int count,
  * and writes the FULL symmetric fp32 inverses
  *     A_inv = (A + damp_A I)^-1,  G_inv = (G + damp_G I)^-1
  * computed in fp32 by block elimination: Schur complements on tensor cores
- * (three tf32 products per slice) down to 128 x 128 blocks inverted by a
- * Gauss-Jordan sweep.  Only the upper triangles of A and G are read.
+ * (three tf32 products per slice) down to 128 x 128 or 256 x 256 blocks,
+ * each inverted by a Gauss-Jordan sweep whose 32-wide block steps are
+ * tensor-core products on the block held in tensor memory.  Only the upper
+ * triangles of A and G are read.
  *
  * Streams: the call is ordered on `stream` as a whole.  When its matrices
  * form chains of very different length, the middle part forks onto two

@@ -14,9 +14,9 @@
 //   2. X = sym(F) + damp I, padded with an identity block to a multiple of
 //      128 (the inverse of diag(X, I) is diag(X^-1, I)), stored as a (hi, lo)
 //      pair with hi exactly representable in tf32 and hi + lo = X;
-//   3. inversion by recursive 2x2 blocking on 128-row
-//      block boundaries; the Schur complement X22 - X21 X11^-1 X12 is the
-//      trailing update of a block Cholesky step:
+//   3. inversion by recursive 2x2 blocking on 128-row block boundaries down
+//      to leaves of 128 or 256 rows; the Schur complement X22 - X21 X11^-1 X12
+//      is the trailing update of a block Cholesky step:
 //        X11 <- X11^-1                               (recursion / leaf)
 //        T   <- X11 X12,   U <- T^T                  (tensor cores)
 //        X22 <- X22 - X21 T       (symmetric: upper tiles + mirror)
@@ -24,13 +24,13 @@
 //        X12 <- -T X22,    X21 <- X12^T              (tensor cores)
 //        X11 <- X11 - X12 T^T     (symmetric: upper tiles + mirror)
 //      The GEMMs run on tcgen05 with three tf32 products per slice
-//      (hi*hi + hi*lo + lo*hi) and fp32 accumulation.  Leaves are 128 x 128
-//      blocks inverted by one CTA, a Gauss-Jordan sweep with the block in
-//      registers (leaf_kernel);
+//      (hi*hi + hi*lo + lo*hi) and fp32 accumulation.  A leaf is inverted
+//      by one CTA with the block resident in TMEM: a Gauss-Jordan sweep in
+//      32-wide block steps, each one rank-32 tensor-core product (tleaf_kernel);
 //   4. out = hi + lo of the upper triangle mirrored to the lower one (exact
 //      symmetry), plus the optional bf16 copy.
 // A pivot that is not positive and finite records its 1-based index in
-// info[matrix]; nothing traps or waits.
+// info[matrix]; nothing traps, and every wait on a barrier has a time limit.
 #include <algorithm>
 #include <cfloat>
 #include <memory>
@@ -44,7 +44,7 @@ namespace kfac {
 namespace {
 
 constexpr int LEAF = 128;
-constexpr int LEAF_THREADS = 256;  // leaf: publisher warp + 7 warps owning the block
+constexpr int LEAF_MAX = 256;  // largest leaf block (one CTA, block resident in TMEM)
 constexpr int MAT_MAX = 224;
 // tensor maps of one matrix: X, T, U pairs, each as hi / lo with 128-row and
 // with 32-row boxes
@@ -273,274 +273,308 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Til
     }
 }
 
-// ------------------------------------------------------------------ leaf
+// ------------------------------------------------------------------ leaves
 
 struct LeafJob {
     float *Xh, *Xl;  // block start (row o, column o) of the working pair
     long long ld;
     int o;           // global offset, for info
     int *info;
+    int n;           // block size: LEAF or 2 LEAF
 };
 
 struct LeafParams {
     LeafJob j[MAT_MAX];
     int n;
+    int *error;      // timeout bits (TMEM-resident leaf)
 };
 
-// 1 / x for a positive finite pivot: the hardware approximate reciprocal
-// refined by one Newton-Raphson step, r <- r + r (1 - x r) (a short
-// dependent chain for the publisher's serial 4 x 4 inverse).
-__device__ __forceinline__ float recip_nr(float x) {
-    float r;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
-    const float e = fmaf(-x, r, 1.0f);
-    return fmaf(r, e, r);
-}
-
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    float2 d;  // two fp32 fused multiply-adds in one instruction
-    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
-        " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
-}
-
-// In-place inverse of one SPD 128 x 128 block by one CTA: a Gauss-Jordan
-// sweep with the block held in registers, four pivots at a time.  A single
-// pivot k maps
-//   a_ij <- a_ij - a_ik a_kj / a_kk   (i, j != k)
-//   a_kj <- a_kj / a_kk,  a_ik <- -a_ik / a_kk,  a_kk <- 1 / a_kk
-// and after the last pivot the block holds its inverse.  No pivoting is
-// needed: every leading principal block of an SPD matrix is SPD.  Four
-// consecutive pivots K = {k .. k+3} (row group s = k / 4) together are the
-// block step: with R the rows K, P = R[:, K] and W = P^-1 R,
-//   a_ij -= a_iK W_Kj,  a_Kj <- W_Kj,  a_iK <- -a_iK P^-1,  a_KK <- P^-1.
-// The sweep keeps the block sign-symmetric -- a_ik = -a_ki when exactly one
-// of i, k has been pivoted, a_ik = a_ki otherwise -- so the pivot columns are
-// s_i R[:, i] (s_i = -1 for pivoted i) and the new ones -s_i W[:, i]: every
-// update is formed from rows K alone.
-// Roles (8 warps): warp 0 is the publisher; warps 1..7 own the 32 row groups
-// (lane l holds columns 4l .. 4l+3 of its warp's rows).  During step s the
-// publisher takes the rows of group s+1 (copied to shared memory by their
-// owner one step earlier), applies step s to them, inverts their 4 x 4
-// diagonal block and publishes W, s R, -s W and P^-1 of group s+1, while the
-// owners apply step s to their rows.  Warp 4 shares the publisher's SM
-// sub-partition and owns only 2 groups, the others 5 each, so that the
-// publisher's serial chain gets most of its sub-partition's issue slots.  A
-// pivot that is not positive and finite is recorded in info and eliminated
+// In-place inverse of one SPD N x N block (N = 128 or 256) by one CTA of N
+// threads, a blocked Gauss-Jordan sweep whose block steps run on the tensor
+// cores.  The block lives in TMEM for the whole sweep (row i at lane i % 128,
+// columns (i / 128) N .. +N-1); the CTA holds all of TMEM when N = 256.
+// Block step s pivots on K = {32s .. 32s+31}.  With C = A[:, K] (the pivot
+// column panel), P = A[K, K], W = P^-1 A[K, :] and E_K the rows of the
+// identity on K, the complete Gauss-Jordan update
+//   a_ij -= a_iK W_Kj,  a_Kj <- W_Kj,  a_iK <- -a_iK P^-1,  a_KK <- P^-1
+// is the single rank-32 product  A += (-C~) W~^T  where C~ = C - E_K (rows K
+// of the panel become P - I) and W~ = W with the columns K replaced by
+// I + P^-1; it runs as tf32 products of (hi, lo) splits (hi*hi + hi*lo +
+// lo*hi) with fp32 accumulation in TMEM.  The block stays sign-symmetric
+// (a_ij = -a_ji when exactly one of i, j has been pivoted), so A[K, j] is
+// +-C[j, :] and W never needs the pivot rows themselves: the product on the
+// columns K runs first and gives -C P^-1, and its rows are the columns of W
+// up to sign.  The next step's panel columns are updated (and signalled) ahead
+// of the rest of the product, whose MMAs overlap the next pivot block's
+// inverse (P^-1: a 32 x 32 Gauss-Jordan sweep by the warp holding rows K).
+// A pivot that is not positive and finite is recorded in info and eliminated
 // as 1 / a_kk = 0.
-__device__ __forceinline__ int leaf_group_start(int hw) {  // first row group of row warp hw (1..7)
-    return hw <= 3 ? 5 * (hw - 1) : hw == 4 ? 15 : 17 + 5 * (hw - 5);
-}
-__device__ __forceinline__ int leaf_group_count(int hw) { return hw == 4 ? 2 : 5; }
+template <int N>
+struct TLeafSmem {
+    static constexpr int NH = N / 128;                 // 128-row halves
+    static constexpr uint32_t A_TILE = 128 * 128;      // 128 rows x 32 tf32 (128-byte swizzled rows)
+    static constexpr uint32_t B_TILE = N * 128;        // N rows x 32 tf32
+    static constexpr uint32_t OFF_A = 0;               // [2 buffers][NH][hi, lo]
+    static constexpr uint32_t OFF_B = OFF_A + 2 * NH * 2 * A_TILE;  // [hi, lo]
+    static constexpr uint32_t OFF_K = OFF_B + 2 * B_TILE;           // pivot block B operand [hi, lo]
+    static constexpr uint32_t OFF_BAR = OFF_K + 2 * 4096;
+    static constexpr uint32_t BYTES = OFF_BAR + 64 + 1024;          // + alignment slack
+    static constexpr int STG = 36;                                  // row pitch of the I/O staging (floats)
+};
 
-__global__ void __launch_bounds__(LEAF_THREADS, 1) leaf_kernel(const __grid_constant__ LeafParams P) {
+// Row r (32 tf32 of K) of a 128-byte-swizzled K-major operand tile, split
+// into hi / lo tiles.
+__device__ __forceinline__ void stage_row_split(uint8_t *hi, uint8_t *lo, int r, const float *x) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const float4 v = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+        const float4 h = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
+        const uint32_t off = (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4);
+        *reinterpret_cast<float4 *>(hi + off) = h;
+        *reinterpret_cast<float4 *>(lo + off) = make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
+    }
+}
+
+// D[128 x ncols] += A[128 x 32] B[ncols x 32]^T with (hi, lo) operand tiles.
+__device__ __forceinline__ void tleaf_mma(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo,
+                                          int ncols) {
+    const uint32_t idesc = idesc_tf32_f32(128, ncols);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t ah = smem_desc_sw128(a_hi + kk * 32, 16, 1024), al = smem_desc_sw128(a_lo + kk * 32, 16, 1024);
+        const uint64_t bh = smem_desc_sw128(b_hi + kk * 32, 16, 1024), bl = smem_desc_sw128(b_lo + kk * 32, 16, 1024);
+        tc_mma_tf32(d, ah, bh, idesc, 1u);
+        tc_mma_tf32(d, ah, bl, idesc, 1u);
+        tc_mma_tf32(d, al, bh, idesc, 1u);
+    }
+}
+
+// 1 / x for a pivot in [FLT_MIN, inf): the flush-to-zero approximate
+// reciprocal refined by one Newton-Raphson step, r <- r + r (1 - x r).
+__device__ __forceinline__ float recip_ftz_nr(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return fmaf(r, fmaf(-x, r, 1.0f), r);
+}
+
+// In-place inverse of the 32 x 32 pivot block held by one warp (lane r: row
+// r), Gauss-Jordan without pivoting (every leading block of an SPD matrix is
+// SPD).  The pivot row is broadcast with shuffles.  The row registers rotate
+// by one column per pivot (position j holds column (k + j) mod 32 before
+// pivot k), so that the pivot column is always p[0] and every index is
+// static; after 32 pivots the columns are back in place.  Rows i != k take
+// a_ij - f a_kj with f = a_ik / a_kk; the pivot row takes f = 1 - 1 / a_kk,
+// which turns the same FMA into a_kj / a_kk.  Returns the first pivot that
+// was not in [FLT_MIN, inf) (-1 if none); such a pivot is eliminated as
+// 1 / a_kk = 0.
+__device__ __forceinline__ int pivot_block_inverse(float (&p)[32], int lane) {
+    int bad = -1;
+#pragma unroll 2
+    for (int k = 0; k < 32; ++k) {
+        float pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pk[j] = __shfl_sync(0xffffffffu, p[j], k);
+        const float d = pk[0];
+        const bool ok = d >= 1.17549435e-38f && d < INFINITY;
+        const float inv = ok ? recip_ftz_nr(d) : 0.f;
+        if (!ok && bad < 0) bad = k;
+        const bool own = lane == k;
+        const float f = own ? 1.f - inv : p[0] * inv;
+#pragma unroll
+        for (int j = 0; j < 31; ++j) p[j] = fmaf(-f, pk[j + 1], p[j + 1]);
+        p[31] = own ? inv : -f;  // column k, now at the last position
+    }
+    return bad;
+}
+
+template <int N>
+__global__ void __launch_bounds__(N, 1) tleaf_kernel(const __grid_constant__ LeafParams P) {
+    using S = TLeafSmem<N>;
+    constexpr int NH = S::NH, NS = N / 32;
+    constexpr uint32_t NCOL = N == 128 ? 128 : 512;
+    extern __shared__ uint8_t tl_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)tl_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *bar_k = (uint64_t *)(smem + S::OFF_BAR);
+    uint64_t *bar_next = bar_k + 1;
+    uint64_t *bar_done = bar_k + 2;
+    uint32_t *tmem_slot = (uint32_t *)(bar_k + 3);
+    int *bad_s = (int *)(tmem_slot + 1);
+    volatile int *abort_s = bad_s + 1;  // a wait ran out: every thread leaves the sweep
+
+    const LeafJob &J = P.j[blockIdx.x];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = warp >> 2, q = warp & 3;
+    const int row = 128 * h + 32 * q + lane;   // this thread's row of the block
+    const int row0 = row - lane;               // first row of this warp
+    const uint32_t lane_field = (uint32_t)(32 * q) << 16;
+
+    if (warp == 0) tmem_alloc(tmem_slot, NCOL);
+    if (tid == 0) {
+        mbar_init(bar_k, 1);
+        mbar_init(bar_next, 1);
+        mbar_init(bar_done, 1);
+        *bad_s = -1;
+        *abort_s = 0;
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t t_row = tmem + lane_field + (uint32_t)(h * N);  // column 0 of this thread's row
     pdl_wait();
     pdl_trigger();
-    constexpr int N = LEAF, NB = N / 4, MAXG = 5;
-    __shared__ __align__(16) float wbuf[2][4][N];   // W = P^-1 R
-    __shared__ __align__(16) float cbuf[2][4][N];   // s_i R[p][i]: the pivot columns
-    __shared__ __align__(16) float fbuf[2][4][N];   // -s_i W[p][i]: the new pivot columns
-    __shared__ __align__(16) float pbuf[2][16];     // P^-1
-    __shared__ __align__(16) float rbuf[2][4][N];   // raw rows of the group after next, for the publisher
-    __shared__ int bad;
-    const LeafJob &J = P.j[blockIdx.x];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool publisher = warp == 0;
-    const int g0 = publisher ? 0 : leaf_group_start(warp), gn = publisher ? 0 : leaf_group_count(warp);
-    const unsigned FULL = 0xffffffffu;
 
-    float a[4 * MAXG][4];
-#pragma unroll
-    for (int lg = 0; lg < MAXG; ++lg) {  // 16-byte pieces, all loads issued before the first use
-        if (lg >= gn) break;
-        float4 h[4], l[4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const long long o = (long long)(4 * (g0 + lg) + p) * J.ld + 4 * lane;
-            h[p] = *reinterpret_cast<const float4 *>(J.Xh + o);
-            l[p] = *reinterpret_cast<const float4 *>(J.Xl + o);
-        }
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            a[4 * lg + p][0] = h[p].x + l[p].x;
-            a[4 * lg + p][1] = h[p].y + l[p].y;
-            a[4 * lg + p][2] = h[p].z + l[p].z;
-            a[4 * lg + p][3] = h[p].w + l[p].w;
-        }
-    }
-    if (warp == 1) {  // groups 0 and 1 for the publisher (both owned by warp 1)
-#pragma unroll
-        for (int p = 0; p < 8; ++p)
-            *reinterpret_cast<float4 *>(&rbuf[p >> 2][p & 3][4 * lane]) =
-                make_float4(a[p][0], a[p][1], a[p][2], a[p][3]);
-    }
-    if (tid == 0) bad = -1;
-    __syncthreads();
-
-    // ---- publisher helpers (warp 8; lane l holds columns 4l .. 4l+3 of the rows)
-    // the 4 x 4 diagonal block of the rows (only lane kn/4 holds P; the other
-    // lanes' results are discarded), inverted by four scalar pivots
-    auto publish = [&](const float (&R)[4][4], int kn) {
-        float b[4][4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) b[p][q] = R[p][q];
-        int first_bad = -1;  // branch-free inside the serial chain; recorded once below
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            const float x = b[v][v];
-            const bool ok = x > 0.f && x <= FLT_MAX;  // positive and finite (NaN fails both)
-            first_bad = (!ok && first_bad < 0) ? kn + v : first_bad;
-            const float d = ok ? recip_nr(x) : 0.f;
-            float t[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) t[i] = b[i][v] * d;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (i != v && j != v) b[i][j] = fmaf(-t[i], b[v][j], b[i][j]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (j != v) b[v][j] *= d;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (i != v) b[i][v] = -t[i];
-            b[v][v] = d;
-        }
-        if (lane == (kn >> 2) && first_bad >= 0 && bad < 0) bad = first_bad;
-        float pi[4][4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) pi[p][q] = __shfl_sync(FULL, b[p][q], kn >> 2);
-        const int buf = (kn >> 2) & 1;
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            float w[4], c[4], f[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                w[t] = pi[p][0] * R[0][t];
-#pragma unroll
-                for (int q = 1; q < 4; ++q) w[t] = fmaf(pi[p][q], R[q][t], w[t]);
-                const float sg = 4 * lane + t < kn ? -1.f : 1.f;
-                c[t] = sg * R[p][t];
-                f[t] = -sg * w[t];
-            }
-            *reinterpret_cast<float4 *>(&wbuf[buf][p][4 * lane]) = make_float4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<float4 *>(&cbuf[buf][p][4 * lane]) = make_float4(c[0], c[1], c[2], c[3]);
-            *reinterpret_cast<float4 *>(&fbuf[buf][p][4 * lane]) = make_float4(f[0], f[1], f[2], f[3]);
-        }
-        if (lane == 0) {
-#pragma unroll
-            for (int p = 0; p < 4; ++p)
-                *reinterpret_cast<float4 *>(&pbuf[buf][4 * p]) = make_float4(pi[p][0], pi[p][1], pi[p][2], pi[p][3]);
-        }
-    };
-    auto load_rows = [&](float (&R)[4][4], int blk) {
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const float4 t = *reinterpret_cast<const float4 *>(&rbuf[blk & 1][p][4 * lane]);
-            R[p][0] = t.x; R[p][1] = t.y; R[p][2] = t.z; R[p][3] = t.w;
-        }
-    };
-
-    // rows r0 .. r0+3 (of a row warp: local rows; of the publisher: R with
-    // global first row i0) updated by the block step held in buf
-    auto step_rows = [&](float (&X)[4][4], int i0, int buf, const float (&w)[4][4], bool colfix) {
-        float cb[4][4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const float4 t = *reinterpret_cast<const float4 *>(&cbuf[buf][p][i0]);
-            cb[p][0] = t.x; cb[p][1] = t.y; cb[p][2] = t.z; cb[p][3] = t.w;
-        }
-#pragma unroll
-        for (int p = 0; p < 4; ++p)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const float2 m = make_float2(-cb[p][r], -cb[p][r]);
-                const float2 lo = ffma2(m, make_float2(w[p][0], w[p][1]), make_float2(X[r][0], X[r][1]));
-                const float2 hi = ffma2(m, make_float2(w[p][2], w[p][3]), make_float2(X[r][2], X[r][3]));
-                X[r][0] = lo.x; X[r][1] = lo.y; X[r][2] = hi.x; X[r][3] = hi.y;
-            }
-        if (colfix) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 t = *reinterpret_cast<const float4 *>(&fbuf[buf][q][i0]);
-                X[0][q] = t.x; X[1][q] = t.y; X[2][q] = t.z; X[3][q] = t.w;
-            }
-        }
-    };
-
-    if (publisher) {
-        float R[4][4];
-        load_rows(R, 0);
-        publish(R, 0);
-    }
-    __syncthreads();
+    // ---- load: X = hi + lo into TMEM (coalesced through a per-warp stage)
+    float *stg = (float *)(smem + S::OFF_A) + warp * 32 * S::STG;
 #pragma unroll 1
-    for (int s = 0; s < NB; ++s) {
-        const int k = 4 * s, buf = s & 1;
-        float w[4][4];
+    for (int c = 0; c < N / 32; ++c) {
+        float4 hv[8], lv[8];
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const float4 t = *reinterpret_cast<const float4 *>(&wbuf[buf][p][4 * lane]);
-            w[p][0] = t.x; w[p][1] = t.y; w[p][2] = t.z; w[p][3] = t.w;
+        for (int k = 0; k < 8; ++k) {
+            const long long off = (long long)(row0 + 4 * k + (lane >> 3)) * J.ld + 32 * c + 4 * (lane & 7);
+            hv[k] = *reinterpret_cast<const float4 *>(J.Xh + off);
+            lv[k] = *reinterpret_cast<const float4 *>(J.Xl + off);
         }
-        const bool colfix = lane == s;  // this lane holds the pivot columns k .. k+3
-        if (publisher) {
-            if (s + 1 < NB) {  // group s+1: its rows as of step s-1, then step s
-                float R[4][4];
-                load_rows(R, s + 1);
-                step_rows(R, k + 4, buf, w, colfix);
-                publish(R, k + 4);
-            }
-        } else {
 #pragma unroll
-            for (int lg = 0; lg < MAXG; ++lg) {
-                if (lg >= gn) break;
-                float (&X)[4][4] = *reinterpret_cast<float (*)[4][4]>(&a[4 * lg][0]);
-                step_rows(X, 4 * (g0 + lg), buf, w, colfix);
-                if (g0 + lg == s) {  // the pivot rows and the pivot block
+        for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4 *>(&stg[(4 * k + (lane >> 3)) * S::STG + 4 * (lane & 7)]) =
+                make_float4(hv[k].x + lv[k].x, hv[k].y + lv[k].y, hv[k].z + lv[k].z, hv[k].w + lv[k].w);
+        __syncwarp();
+        float v[32];
 #pragma unroll
-                    for (int p = 0; p < 4; ++p)
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) X[p][c] = w[p][c];
-                    if (colfix) {
-#pragma unroll
-                        for (int p = 0; p < 4; ++p) {
-                            const float4 t = *reinterpret_cast<const float4 *>(&pbuf[buf][4 * p]);
-                            X[p][0] = t.x; X[p][1] = t.y; X[p][2] = t.z; X[p][3] = t.w;
-                        }
-                    }
-                }
-                if (g0 + lg == s + 2 && s + 2 < NB) {  // rows of group s+2 (after this step) for the publisher
-#pragma unroll
-                    for (int p = 0; p < 4; ++p)
-                        *reinterpret_cast<float4 *>(&rbuf[(s + 2) & 1][p][4 * lane]) =
-                            make_float4(X[p][0], X[p][1], X[p][2], X[p][3]);
-                }
-            }
+        for (int j = 0; j < 8; ++j) {
+            const float4 t = *reinterpret_cast<const float4 *>(&stg[lane * S::STG + 4 * j]);
+            v[4 * j] = t.x; v[4 * j + 1] = t.y; v[4 * j + 2] = t.z; v[4 * j + 3] = t.w;
         }
-        __syncthreads();
+        tmem_st_32x32b_x32(t_row + 32 * c, v);
+        __syncwarp();
     }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncthreads();
 
+    uint8_t *const kb_hi = smem + S::OFF_K, *const kb_lo = kb_hi + 4096;
+    uint8_t *const bu_hi = smem + S::OFF_B, *const bu_lo = bu_hi + S::B_TILE;
+#pragma unroll 1
+    for (int s = 0; s < NS; ++s) {
+        const int ks = 32 * s;
+        const int pw = 4 * (ks >> 7) + ((ks & 127) >> 5);  // warp holding rows K
+        uint8_t *const au_hi = smem + S::OFF_A + (uint32_t)(((s & 1) * NH + h) * 2) * S::A_TILE;
+        uint8_t *const au_lo = au_hi + S::A_TILE;
+        // panel C = A[:, K] (updated by the previous step's first MMAs); the
+        // thread issuing the previous step's remaining MMAs joins later
+        if (s > 0 && !mbar_wait(bar_next, (uint32_t)((s - 1) & 1))) *abort_s = 1;
+        __syncwarp();  // warp 0 reconverges after its MMA issue (tcgen05.ld is warp-collective)
+        tc_fence_after();
+        float c[32];
+        tmem_ld_32x32b_x32(t_row + ks, c);
+        const bool in_k = row >= ks && row < ks + 32;
+        {
+            const int dj = in_k ? row - ks : -1;  // this row's column inside K
+            float a[32];  // -(C - E_K)
 #pragma unroll
-    for (int lg = 0; lg < MAXG; ++lg) {
-        if (lg >= gn) break;
+            for (int j = 0; j < 32; ++j) a[j] = __int_as_float(__float_as_int(1.f) & -(int)(dj == j)) - c[j];
+            stage_row_split(au_hi, au_lo, 32 * q + lane, a);
+        }
+        if (warp == pw) {  // P^-1, then the pivot block's B rows I + P^-1
+            const int bad = pivot_block_inverse(c, lane);
+            if (lane == 0 && bad >= 0 && *bad_s < 0) *bad_s = ks + bad;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const float *v = a[4 * lg + p];
-            const long long o = (long long)(4 * (g0 + lg) + p) * J.ld + 4 * lane;
-            const float4 h = make_float4(tf32_hi(v[0]), tf32_hi(v[1]), tf32_hi(v[2]), tf32_hi(v[3]));
-            *reinterpret_cast<float4 *>(J.Xh + o) = h;
-            *reinterpret_cast<float4 *>(J.Xl + o) = make_float4(v[0] - h.x, v[1] - h.y, v[2] - h.z, v[3] - h.w);
+            for (int j = 0; j < 32; ++j) c[j] += j == lane ? 1.f : 0.f;
+            stage_row_split(kb_hi, kb_lo, lane, c);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (*abort_s) break;
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh) {
+                const uint32_t a0 = smem_u32(smem + S::OFF_A + (uint32_t)(((s & 1) * NH + hh) * 2) * S::A_TILE);
+                tleaf_mma(tmem + (uint32_t)(hh * N + ks), a0, a0 + S::A_TILE, smem_u32(kb_hi), smem_u32(kb_lo), 32);
+            }
+            tc_commit(bar_k);
+        }
+        // columns K now hold -C P^-1 (rows outside K) and P^-1 (rows K);
+        // W[:, i] = +v (i pivoted before this step) or -v (i after K)
+        if (!mbar_wait(bar_k, (uint32_t)(s & 1))) *abort_s = 1;
+        __syncwarp();
+        tc_fence_after();
+        {
+            float v[32];
+            tmem_ld_32x32b_x32(t_row + ks, v);
+            if (!in_k) {
+                if (row > ks) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = -v[j];
+                }
+                stage_row_split(bu_hi, bu_lo, row, v);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (*abort_s) break;
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t bh = smem_u32(bu_hi), bl = smem_u32(bu_lo);
+            const bool more = s + 1 < NS;
+            if (more) {  // the next panel first
+#pragma unroll
+                for (int hh = 0; hh < NH; ++hh) {
+                    const uint32_t a0 = smem_u32(smem + S::OFF_A + (uint32_t)(((s & 1) * NH + hh) * 2) * S::A_TILE);
+                    tleaf_mma(tmem + (uint32_t)(hh * N + ks + 32), a0, a0 + S::A_TILE, bh + (ks + 32) * 128,
+                              bl + (ks + 32) * 128, 32);
+                }
+                tc_commit(bar_next);
+            }
+            const int r1 = more ? ks + 64 : N;  // remaining columns: [0, ks) and [r1, N)
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh) {
+                const uint32_t a0 = smem_u32(smem + S::OFF_A + (uint32_t)(((s & 1) * NH + hh) * 2) * S::A_TILE);
+                if (ks > 0) tleaf_mma(tmem + (uint32_t)(hh * N), a0, a0 + S::A_TILE, bh, bl, ks);
+                if (r1 < N)
+                    tleaf_mma(tmem + (uint32_t)(hh * N + r1), a0, a0 + S::A_TILE, bh + r1 * 128, bl + r1 * 128, N - r1);
+            }
+            if (!more) tc_commit(bar_done);
         }
     }
-    if (tid == 0 && bad >= 0 && J.info) atomicCAS(J.info, 0, J.o + bad + 1);
+    bool ok = !*abort_s && mbar_wait(bar_done, 0u);
+    ok = __syncthreads_and(ok);
+    if (!ok && tid == 0 && P.error) atomicOr(P.error, ERR_TIMEOUT_LEAF);
+    tc_fence_after();
+
+    // ---- store: A^-1 as (hi, lo) (coalesced through the per-warp stage)
+    if (ok) {
+#pragma unroll 1
+        for (int c = 0; c < N / 32; ++c) {
+            float v[32];
+            tmem_ld_32x32b_x32(t_row + 32 * c, v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<float4 *>(&stg[lane * S::STG + 4 * j]) =
+                    make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float4 t = *reinterpret_cast<const float4 *>(&stg[(4 * k + (lane >> 3)) * S::STG + 4 * (lane & 7)]);
+                const float4 hh = make_float4(tf32_hi(t.x), tf32_hi(t.y), tf32_hi(t.z), tf32_hi(t.w));
+                const long long off = (long long)(row0 + 4 * k + (lane >> 3)) * J.ld + 32 * c + 4 * (lane & 7);
+                *reinterpret_cast<float4 *>(J.Xh + off) = hh;
+                *reinterpret_cast<float4 *>(J.Xl + off) = make_float4(t.x - hh.x, t.y - hh.y, t.z - hh.z, t.w - hh.w);
+            }
+            __syncwarp();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, NCOL);
+    }
+    if (tid == 0 && *bad_s >= 0 && J.info) atomicCAS(J.info, 0, J.o + *bad_s + 1);
 }
 
 // ------------------------------------------------------------- scheduler
@@ -560,10 +594,10 @@ struct MatWork {
 
 void gen_ops(std::vector<Op> &ops, const MatWork &w, int o, int n, int *info) {
     const long long ld = w.dp;
-    if (n == LEAF) {
+    if (n == LEAF || n == LEAF_MAX) {  // one leaf launch (TMEM-resident block)
         Op op{};
         op.leaf = 1;
-        op.lj = LeafJob{w.Xh + o * ld + o, w.Xl + o * ld + o, ld, o, info};
+        op.lj = LeafJob{w.Xh + o * ld + o, w.Xl + o * ld + o, ld, o, info, n};
         ops.push_back(op);
         return;
     }
@@ -745,16 +779,42 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
     return KFAC_OK;
 }
 
-kfac_status leaf_launch(const std::vector<LeafJob> &jobs, cudaStream_t st) {
+template <int N>
+cudaError_t tleaf_smem_attr() {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(tleaf_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)TLeafSmem<N>::BYTES);
+    });
+    return err;
+}
+
+// One launch per leaf size present in the round (N threads, one CTA per block).
+kfac_status leaf_launch(const std::vector<LeafJob> &jobs, int *err, cudaStream_t st) {
     for (const LeafJob &j : jobs)  // the kernel moves rows in 16-byte pieces
-        if (j.ld % 4 != 0 || (uintptr_t)j.Xh % 16 != 0 || (uintptr_t)j.Xl % 16 != 0) return KFAC_ERR_WORKSPACE;
+        if (j.ld % 4 != 0 || (uintptr_t)j.Xh % 16 != 0 || (uintptr_t)j.Xl % 16 != 0 ||
+            (j.n != LEAF && j.n != LEAF_MAX))
+            return KFAC_ERR_WORKSPACE;
     std::unique_ptr<LeafParams> P(new LeafParams);
-    size_t pos = 0;
-    while (pos < jobs.size()) {
-        int n = 0;
-        while (pos < jobs.size() && n < MAT_MAX) P->j[n++] = jobs[pos++];
-        P->n = n;
-        KFAC_LAUNCH(KK_LEAF, st, leaf_kernel, n, LEAF_THREADS, 0, *P);
+    for (int size : {LEAF, LEAF_MAX}) {
+        size_t pos = 0;
+        while (pos < jobs.size()) {
+            int n = 0;
+            for (; pos < jobs.size() && n < MAT_MAX; ++pos)
+                if (jobs[pos].n == size) P->j[n++] = jobs[pos];
+            if (n == 0) break;
+            P->n = n;
+            P->error = err;
+            if (size == 128) {
+                if (tleaf_smem_attr<128>() != cudaSuccess) return KFAC_ERR_CUDA;
+                KFAC_LAUNCH(KK_LEAF, st, tleaf_kernel<128>, n, 128, TLeafSmem<128>::BYTES, *P);
+            } else {
+                if (tleaf_smem_attr<256>() != cudaSuccess) return KFAC_ERR_CUDA;
+                KFAC_LAUNCH(KK_LEAF, st, tleaf_kernel<256>, n, 256, TLeafSmem<256>::BYTES, *P);
+            }
+        }
+        if (LEAF_MAX == LEAF) break;
     }
     return KFAC_OK;
 }
@@ -832,7 +892,7 @@ kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st) {
             const Op &op = p.chains[ki.first][ki.second];
             if (op.leaf) leaves.push_back(op.lj); else gemms.push_back(op.g);
         }
-        if (!leaves.empty() && (s = leaf_launch(leaves, st)) != KFAC_OK) return s;
+        if (!leaves.empty() && (s = leaf_launch(leaves, p.err, st)) != KFAC_OK) return s;
         if (!gemms.empty()) {
             Arena tail(g.tc_ws, g.tc_bytes);
             if ((s = tc_run(gemms.data(), (int)gemms.size(), TC_KIND_TF32X3, p.dev_maps, tail, p.err, st,

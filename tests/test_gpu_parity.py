@@ -288,6 +288,28 @@ def test_damp_invert_not_pd_reports_info():
         assert info.cpu().tolist() == [1, 0]
 
 
+@pytest.mark.parametrize("d,bad", [(200, 77), (200, 199), (256, 255), (600, 450), (600, 130)])
+def test_damp_invert_not_pd_deep_pivot(d, bad):
+    """A positive diagonal with one negative entry (gamma = 0, no pi split):
+    the first failing pivot is that entry, inside a later 32-wide block step
+    of a 256-row leaf or in a later leaf of the recursion; info gives its
+    1-based index and every other pivot still eliminates normally."""
+    diag = torch.linspace(1.0, 2.0, d, device=DEV)
+    diag[bad] = -0.5
+    A = torch.diag(diag)
+    G = torch.eye(3, device=DEV)
+    Ai = torch.empty_like(A)
+    info = torch.zeros(2, dtype=torch.int32, device=DEV)
+    kfac.kfac_damp_invert([kfac.InvertPair(A, G, Ai, torch.empty_like(G))], 0.0, pi_split=False, info=info)
+    torch.cuda.synchronize()
+    assert info.cpu().tolist() == [bad + 1, 0]
+    # the other diagonal entries are still inverted (a diagonal matrix has no coupling)
+    ok = torch.ones(d, dtype=torch.bool)
+    ok[bad] = False
+    got = torch.diagonal(Ai).cpu()[ok].double()
+    np.testing.assert_allclose(got.numpy(), (1.0 / diag.cpu()[ok].double()).numpy(), rtol=1e-5)
+
+
 # -------------------------------------------------------------- precondition
 
 @pytest.mark.parametrize("dG,dA", [(32, 65), (128, 200), (256, 576), (130, 1001)])
