@@ -219,7 +219,7 @@ kfac_status plan_factor(const kfac_factor_desc *descs, int count, const std::vec
         TcJob j{};
         j.map_a = j.map_b = (int)p.maps.size();
         p.maps.emplace_back();
-        if (encode && !tc_make_map(&p.maps.back(), TC_KIND_BF16, src, lds, (int)g.M, g.dcore, 1))
+        if (encode && !tc_make_map(&p.maps.back(), TC_KIND_BF16, src, lds, (int)g.M, g.dcore))
             return KFAC_ERR_CUDA;
         j.a_mn = j.b_mn = 1;
         j.M = g.dcore; j.N = g.dcore; j.K = (int)g.M;
@@ -440,9 +440,9 @@ kfac_status plan_precond(const kfac_precond_desc *descs, int count, int dtype, A
                          bool encode) {
     p.err = ws.take<int>(64);
     if (dtype == KFAC_BF16) p.dev_maps = ws.take<CUtensorMap>(4 * (size_t)count);
-    auto map = [&](const void *ptr, long long ld, int rows, int cols, int mn) {
+    auto map = [&](const void *ptr, long long ld, int rows, int cols) {
         p.maps.emplace_back();
-        if (encode && !tc_make_map(&p.maps.back(), TC_KIND_BF16, ptr, ld, rows, cols, mn)) return -1;
+        if (encode && !tc_make_map(&p.maps.back(), TC_KIND_BF16, ptr, ld, rows, cols)) return -1;
         return (int)p.maps.size() - 1;
     };
     for (int i = 0; i < count; ++i) {
@@ -451,14 +451,14 @@ kfac_status plan_precond(const kfac_precond_desc *descs, int count, int dtype, A
             const long long ldt = (d.dA + 7) / 8 * 8;
             uint16_t *T = ws.take<uint16_t>((size_t)d.dG * ldt);
             TcJob a{};  // T = grad * A_inv   (A_inv symmetric: its rows are the columns of B)
-            a.map_a = map(d.grad, d.ld_grad, d.dG, d.dA, 0);
-            a.map_b = map(d.A_inv, d.ld_ainv, d.dA, d.dA, 0);
+            a.map_a = map(d.grad, d.ld_grad, d.dG, d.dA);
+            a.map_b = map(d.A_inv, d.ld_ainv, d.dA, d.dA);
             a.M = d.dG; a.N = d.dA; a.K = d.dA;
             a.epi = TC_EPI_STORE; a.alpha = 1.f; a.beta = 0.f;
             a.Cb = T; a.ldcb = ldt;
             TcJob b{};  // out = G_inv * T   (T read MN-major)
-            b.map_a = map(d.G_inv, d.ld_ginv, d.dG, d.dG, 0);
-            b.map_b = map(T, ldt, d.dG, d.dA, 1);
+            b.map_a = map(d.G_inv, d.ld_ginv, d.dG, d.dG);
+            b.map_b = map(T, ldt, d.dG, d.dA);  // read MN-major (b_mn)
             b.b_mn = 1;
             b.M = d.dG; b.N = d.dA; b.K = d.dG;
             b.epi = TC_EPI_STORE; b.alpha = 1.f; b.beta = 0.f;

@@ -55,10 +55,11 @@ struct TcJob {
 };
 
 // Tensor map of a row-major [rows][cols] matrix (ld elements) for the engine:
-// 128-byte swizzle, box 128 bytes wide and box_rows rows (default 128).  A tf32x3 operand is a run of four maps: hi and lo with
+// 128-byte swizzle, box 128 bytes wide and box_rows rows (default 128).  The
+// same map serves a K-major and an MN-major operand (the kernel picks the box
+// coordinates).  A tf32x3 operand is a run of four maps: hi and lo with
 // 128-row boxes, then hi and lo with 32-row boxes (B of narrow tiles).
-bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int mn_major,
-                 int box_rows = 0);
+bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int box_rows = 0);
 // Im2col tensor map of a bf16 NHWC tensor [n][h][w][c] for a square k x k
 // convolution (stride, pad): 64 channels x 128 output pixels per load,
 // 128-byte swizzle.  Requires c % 64 == 0 and a 16-byte aligned base.

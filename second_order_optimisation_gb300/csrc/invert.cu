@@ -739,7 +739,7 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
                 for (int v = 0; v < 4; ++v) {
                     p.maps.emplace_back();
                     if (encode && !tc_make_map(&p.maps.back(), TC_KIND_TF32X3, bufs[q + (v & 1)], w.dp, w.dp,
-                                               w.dp, 0, v < 2 ? 128 : 32))
+                                               w.dp, v < 2 ? 128 : 32))
                         return KFAC_ERR_CUDA;
                 }
             w.mx = base;

@@ -887,8 +887,7 @@ int units_of(const TcJob &j, int bn, int cl) {
 
 }  // namespace
 
-bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int mn_major,
-                 int box_rows) {
+bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int box_rows) {
     EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) return false;
     const int esz = kind == TC_KIND_BF16 ? 2 : 4;
