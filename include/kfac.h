@@ -35,6 +35,16 @@
  *     launch); the stream may then hold part of the work.
  *   - Matrices are row-major with an explicit leading dimension (elements).
  *     bf16 values are passed as uint16_t bit patterns.
+ *   - Device error word: the first int32 of the workspace of
+ *     kfac_factor_update, kfac_damp_invert and kfac_precondition.  Each call
+ *     sets it to 0 on its stream before its kernels; every wait of a kernel
+ *     on a shared-memory barrier has a time limit (about 2 s), and a wait
+ *     that runs out ORs a bit into the word (1, 2, 4: the tensor-core engine's
+ *     operand, stage and accumulator waits; 8: an inversion leaf's block-step
+ *     waits) and the kernel winds down without trapping.  A nonzero word after
+ *     the stream has been synchronised means that call's outputs are
+ *     undefined.  The call's return status cannot report it (the kernels run
+ *     after the call returns).
  */
 #ifndef KFAC_GB300_H
 #define KFAC_GB300_H

@@ -378,9 +378,9 @@ extern "C" size_t kfac_damp_invert_workspace_size(const kfac_invert_desc *descs,
     if (validate_invert(descs, count, 0.f) != KFAC_OK) return 0;
     std::vector<InvMatrix> m = inv_mats(descs, count);
     Arena a;
+    a.take<char>(inv_workspace_bytes(m.data(), (int)m.size()));  // starts with the error word
     a.take<float>(2 * (size_t)count);   // damping values
     a.take<int>(2 * (size_t)count);     // info
-    a.take<char>(inv_workspace_bytes(m.data(), (int)m.size()));
     return a.used;
 }
 
@@ -391,17 +391,23 @@ extern "C" kfac_status kfac_damp_invert(const kfac_invert_desc *descs, int count
     if (s != KFAC_OK) return s;
     if (count == 0) return KFAC_OK;
     if (!workspace || ((uintptr_t)workspace % 256) != 0) return KFAC_ERR_WORKSPACE;
-    if (workspace_bytes < kfac_damp_invert_workspace_size(descs, count)) return KFAC_ERR_WORKSPACE;
     std::vector<InvMatrix> m = inv_mats(descs, count);
+    // layout (the same takes as kfac_damp_invert_workspace_size): the
+    // inversion's own workspace first (its first int32 is the error word),
+    // then the damping values and info used when the caller passes none
+    const size_t inv_bytes = inv_workspace_bytes(m.data(), (int)m.size());
     Arena ws(workspace, workspace_bytes);
+    char *inv_ws = ws.take<char>(inv_bytes);
     float *dmp = ws.take<float>(2 * (size_t)count);
     int *inf = ws.take<int>(2 * (size_t)count);
+    if (!ws.fits()) return KFAC_ERR_WORKSPACE;
     if (damp) dmp = damp;
     if (info) inf = info;
     cudaStream_t st = (cudaStream_t)stream;
     KFAC_CUDA_TRY(cudaMemsetAsync(inf, 0, 2 * (size_t)count * sizeof(int), st));
     if ((s = damping_run(m.data(), count, gamma, pi_split, dmp, st)) != KFAC_OK) return s;
-    return inv_run(m.data(), (int)m.size(), dmp, inf, ws, st);
+    Arena inv_arena(inv_ws, inv_bytes);
+    return inv_run(m.data(), (int)m.size(), dmp, inf, inv_arena, st);
 }
 
 // ------------------------------------------------------------ precondition

@@ -267,7 +267,8 @@ def kfac_damp_invert_workspace_size(pairs: Sequence[InvertPair]) -> int:
 def kfac_damp_invert(pairs: Sequence[InvertPair], gamma: float, pi_split: bool = True,
                      info: Optional[torch.Tensor] = None, damp: Optional[torch.Tensor] = None,
                      workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Enqueue the damped inversions; returns the workspace used."""
+    """Enqueue the damped inversions; returns the workspace used (its first
+    int32 is the library's device error word: 0 = no internal timeout)."""
     lib = load()
     arr = _invert_descs(pairs)
     need = int(lib.kfac_damp_invert_workspace_size(arr, len(pairs)))

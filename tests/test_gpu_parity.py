@@ -257,6 +257,7 @@ def test_damp_invert_two_groups_eager_and_graph():
         kfac.kfac_damp_invert(pairs, gamma, info=info, damp=damp, workspace=ws, stream=s)
     torch.cuda.synchronize()
     assert info.cpu().tolist() == [0] * (2 * len(dims))
+    assert int(ws[:4].view(torch.int32).item()) == 0  # device error word: no wait ran out
     eager = [(f64(p.A_inv), f64(p.G_inv)) for p in pairs]
     for p in pairs:
         p.A_inv.zero_()
