@@ -307,8 +307,9 @@ struct LeafParams {
 // up to sign.  The next step's panel columns are updated (and signalled) ahead
 // of the rest of the product, whose MMAs overlap the next pivot block's
 // inverse (P^-1: a 32 x 32 Gauss-Jordan sweep by the warp holding rows K).
-// A pivot that is not positive and finite is recorded in info and eliminated
-// as 1 / a_kk = 0.
+// A pivot outside [FLT_MIN, inf) (not positive, subnormal or not finite) is
+// recorded in info and eliminated as 1 / a_kk = 0; the inverse is then
+// undefined, but the sweep runs to its end.
 template <int N>
 struct TLeafSmem {
     static constexpr int NH = N / 128;                 // 128-row halves
