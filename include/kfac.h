@@ -219,23 +219,28 @@ kfac_status kfac_precondition(const kfac_precond_desc *descs, int count, int dty
  * kfac_precondition_noalloc -- kfac_precondition without a caller workspace.
  *
  * The paper has no counterpart: this is a service for callers that cannot
- * allocate device memory -- code running while a CUDA graph is captured
- * (an allocation there breaks the capture), step loops where cudaMalloc's
- * implicit device synchronisation is not acceptable, and host frameworks that
- * own all device memory through their own allocator.  Same arguments, results
- * and errors as kfac_precondition, but the scratch comes from a fixed array
- * inside the library's own device memory of kfac_noalloc_scratch_bytes()
- * bytes (32 MiB) on every GPU that loads the library, held until the process
- * exits; nothing is allocated by the call.
+ * allocate device memory -- host frameworks that own all device memory
+ * through their own pool and do not let a library call cudaMalloc, step
+ * loops in which cudaMalloc's implicit device-wide synchronisation would
+ * stall the pipeline, and embedded callers whose device-memory budget is
+ * fixed at start-up.  Same arguments, results and errors as
+ * kfac_precondition (bitwise the same outputs), but the scratch comes from a
+ * fixed array in the library's own device memory, kfac_noalloc_scratch_bytes()
+ * bytes (32 MiB), held by every GPU that loads the library until the process
+ * exits.  The call allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine).
  *   - KFAC_ERR_WORKSPACE when kfac_precondition_workspace_size() of the
  *     arguments exceeds kfac_noalloc_scratch_bytes() (split the layers over
  *     several calls, or use kfac_precondition with a workspace).
- *   - The first call on a device looks up the array's device address (a
- *     runtime query, no allocation); make that first call before any stream
- *     capture begins.
+ *   - Set-up: the first call on a device (and the first call after that
+ *     device's context was re-created, e.g. by cudaDeviceReset) looks up the
+ *     array's device address with that device current (a runtime query, no
+ *     allocation).  Make that first call before any stream capture begins.
  *   - All calls on a device share the one array and its contents persist
- *     between calls: calls whose GPU work overlaps (e.g. on two streams
- *     without ordering between them) race on it.  Order them on one stream.
+ *     from call to call (each call clears the parts that must start at zero:
+ *     the error word, which is the array's first int32, and the split-K
+ *     counters).  Calls whose GPU work overlaps (e.g. on two streams without
+ *     ordering between them) race on the array: order them on one stream.
  * ==================================================================== */
 size_t kfac_noalloc_scratch_bytes(void);
 kfac_status kfac_precondition_noalloc(const kfac_precond_desc *descs, int count, int dtype,

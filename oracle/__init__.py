@@ -56,12 +56,13 @@ def _bind(path):
         lib.orc_lauum_upper.argtypes = [_dp, _L, _dp]
         lib.orc_damped_inverse.argtypes = [_dp, _L, ctypes.c_double, _dp]
         lib.orc_precondition.argtypes = [_dp, _L, _dp, _L, _dp, _dp]
+        lib.orc_precondition_rows.argtypes = [_dp, _L, _dp, _L, _dp, _lp, _L, _dp]
         lib.orc_bn_diag_fisher.argtypes = [_dp, _L, _L, ctypes.c_double, ctypes.c_double,
                                            _dp, _dp, _dp]
         for f in ("orc_im2col", "orc_gram", "orc_factor_ema", "orc_gram_entries",
                   "orc_weight_grad", "orc_pi_damping", "orc_cholesky_upper",
                   "orc_trtri_upper", "orc_lauum_upper", "orc_damped_inverse",
-                  "orc_precondition", "orc_bn_diag_fisher"):
+                  "orc_precondition", "orc_precondition_rows", "orc_bn_diag_fisher"):
             getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -213,6 +214,18 @@ def precondition(Ginv, grad, Ainv):
     dG, dA = grad.shape
     out = np.empty((dG, dA), dtype=np.float64)
     assert _load().orc_precondition(_p(Ginv), dG, _p(grad), dA, _p(Ainv), _p(out)) == 0
+    return out
+
+
+def precondition_rows(Ginv, grad, Ainv, rows):
+    """Rows `rows` of Ginv @ grad @ Ainv, evaluated as (Ginv[rows] @ grad) @ Ainv."""
+    Ginv, grad, Ainv = _d(Ginv), _d(grad), _d(Ainv)
+    dG, dA = grad.shape
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    assert rows.min() >= 0 and rows.max() < dG
+    out = np.empty((len(rows), dA), dtype=np.float64)
+    assert _load().orc_precondition_rows(_p(Ginv), dG, _p(grad), dA, _p(Ainv), rows.ctypes.data_as(_lp),
+                                         len(rows), _p(out)) == 0
     return out
 
 

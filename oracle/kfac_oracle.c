@@ -359,6 +359,35 @@ int orc_precondition(const double *Ginv, long dG, const double *grad, long dA,
     return 0;
 }
 
+/*
+ * Selected rows of the preconditioned gradient (Eq. 7 as above), for checks
+ * at sizes where the full product is too slow on the CPU:
+ *   out[t][j] = sum_o Ginv[rows[t]][o] * sum_k grad[o][k] * Ainv[k][j],
+ * evaluated as (Ginv[rows[t]] * grad) * Ainv, plain loops.
+ * Pinned: equals the corresponding rows of orc_precondition.
+ */
+int orc_precondition_rows(const double *Ginv, long dG, const double *grad, long dA,
+                          const double *Ainv, const long *rows, long nrows, double *out)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long t = 0; t < nrows; ++t) {
+        double *u = (double *)malloc(sizeof(double) * (size_t)dA);
+        const double *g = Ginv + rows[t] * dG;
+        for (long k = 0; k < dA; ++k) u[k] = 0.0;
+        for (long o = 0; o < dG; ++o) {
+            const double go = g[o];
+            for (long k = 0; k < dA; ++k) u[k] += go * grad[o * dA + k];
+        }
+        for (long j = 0; j < dA; ++j) out[t * dA + j] = 0.0;
+        for (long k = 0; k < dA; ++k) {
+            const double uk = u[k];
+            for (long j = 0; j < dA; ++j) out[t * dA + j] += uk * Ainv[k * dA + j];
+        }
+        free(u);
+    }
+    return 0;
+}
+
 /* -------------------------------------------------------------- BatchNorm */
 
 /*

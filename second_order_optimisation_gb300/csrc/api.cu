@@ -511,8 +511,8 @@ extern "C" kfac_status kfac_precondition(const kfac_precond_desc *descs, int cou
     p = PrecondPlan();
     if ((s = plan_precond(descs, count, dtype, ws, p, true)) != KFAC_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
+    KFAC_CUDA_TRY(cudaMemsetAsync(p.err, 0, sizeof(int), st));  // the error word, for every dtype
     if (dtype == KFAC_BF16) {
-        KFAC_CUDA_TRY(cudaMemsetAsync(p.err, 0, sizeof(int), st));
         if ((s = tc_upload_maps(p.maps.data(), (int)p.maps.size(), p.dev_maps, st)) != KFAC_OK) return s;
         Arena t_a(p.tc_ws, p.tc_bytes);
         if ((s = tc_run(p.g1.data(), (int)p.g1.size(), TC_KIND_BF16, p.dev_maps, t_a, p.err, st)) != KFAC_OK)

@@ -75,42 +75,6 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// As launch_kernel, in thread-block clusters of `cluster` CTAs along x.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_kernel_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                                  int cluster, Args &&...args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    int n = 0;
-    attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = (unsigned)cluster;
-    attr[n].val.clusterDim.y = 1;
-    attr[n].val.clusterDim.z = 1;
-    ++n;
-    if (pdl_enabled()) {
-        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[n].val.programmaticStreamSerializationAllowed = 1;
-        ++n;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
-
-#define KFAC_LAUNCH_CLUSTER(kind, st, cluster, kernel, grid, block, smem, ...)                          \
-    do {                                                                                                \
-        const int slot_ = ::kfac::timing_begin((kind), (st));                                           \
-        const cudaError_t e_ = ::kfac::launch_kernel_cluster((kernel), dim3(grid), dim3(block), (smem), \
-                                                             (st), (cluster), __VA_ARGS__);             \
-        ::kfac::timing_end(slot_, (st));                                                                \
-        ::kfac::count_launch();                                                                         \
-        if (e_ != cudaSuccess || cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;               \
-    } while (0)
-
 // KFAC_LAUNCH(kind, stream, kernel, grid, block, dynamic smem, args...)
 #define KFAC_LAUNCH(kind, st, kernel, grid, block, smem, ...)                                  \
     do {                                                                                       \
@@ -283,36 +247,6 @@ __device__ __forceinline__ void tc_mma_tf32(uint32_t d_tmem, uint64_t adesc, uin
 
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread
 // has completed.
-// ---- thread-block clusters (TMA multicast between the CTAs of a cluster)
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// All threads of all CTAs of the cluster (release / acquire).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Tile load written to the same shared-memory offset of every CTA in `mask`;
-// each destination's mbarrier at `bar`'s offset receives the bytes.
-__device__ __forceinline__ void tma_load_2d_mc(void *smem_dst, const CUtensorMap *map, int c0, int c1,
-                                               uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-        "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
-// Arrive on the mbarrier at `bar`'s offset of every CTA in `mask` once the
-// issuing thread's prior tcgen05.mma operations have completed.
-__device__ __forceinline__ void tc_commit_mc(uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
-
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

@@ -2,14 +2,15 @@
 // that cannot allocate device memory.
 //
 // kfac_precondition needs scratch (the intermediate grad * A_inv, tensor
-// maps, split-K partial tiles) that its caller normally allocates.  Some
-// callers cannot call cudaMalloc: code that runs while a CUDA graph is being
-// captured (an allocation there breaks or invalidates the capture), step loops
-// where cudaMalloc's implicit device synchronisation is not acceptable, and
-// host frameworks that own all device memory through their own allocator.
-// This entry point serves them from a fixed scratch array that lives in the
-// library's own device memory (see NOALLOC_SCRATCH_BYTES): every GPU that loads
-// the library holds it until the process exits.
+// maps, split-K partial tiles, the error word) that its caller normally
+// allocates.  Some callers cannot call cudaMalloc: host frameworks that own
+// all device memory through their own pool and do not let libraries allocate
+// behind their back, step loops in which cudaMalloc's implicit device-wide
+// synchronisation would stall the pipeline, and embedded callers whose device
+// memory budget is fixed when they start.  This entry point serves them from
+// a fixed scratch array in the library's own device memory (see
+// NOALLOC_SCRATCH_BYTES): every GPU that loads the library holds it until the
+// process exits.
 #include <mutex>
 
 #include "internal.h"
@@ -25,21 +26,52 @@ constexpr int MAX_DEVICES = 64;
 // cudaGetSymbolAddress on each device.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
-std::mutex g_mu;
-void *g_addr[MAX_DEVICES] = {nullptr};
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
 
-// Device address of the scratch on the current device, resolved once per
-// device with that device current.
+CtxGetCurrentFn ctx_get_current_fn() {
+    static std::once_flag once;
+    static CtxGetCurrentFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (CtxGetCurrentFn)p;
+    });
+    return fn;
+}
+
+struct DeviceScratch {
+    void *addr = nullptr;
+    CUcontext ctx = nullptr;  // the context the address belongs to
+};
+
+std::mutex g_mu;
+DeviceScratch g_scratch[MAX_DEVICES];
+
+// Device address of the scratch on the current device, looked up with that
+// device current on the first call there.  The address belongs to the
+// device's context: after cudaDeviceReset the runtime makes a new context
+// (and loads the library's module again), so the lookup is repeated when the
+// current context is not the one the cached address was found in.
 kfac_status scratch_address(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return KFAC_ERR_CUDA;
+    // make sure the device's primary context exists and is current before
+    // asking for it (a no-op when the runtime is already initialised)
+    if (cudaFree(nullptr) != cudaSuccess) return KFAC_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    CtxGetCurrentFn get = ctx_get_current_fn();
+    if (!get || get(&ctx) != CUDA_SUCCESS || !ctx) return KFAC_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
+    DeviceScratch &d = g_scratch[dev];
+    if (!d.addr || d.ctx != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KFAC_ERR_CUDA;
-        g_addr[dev] = p;
+        d.addr = p;
+        d.ctx = ctx;
     }
-    *out = g_addr[dev];
+    *out = d.addr;
     return KFAC_OK;
 }
 

@@ -41,10 +41,6 @@ constexpr int TILE_BYTES = 128 * 128;  // one tf32 operand tile: 128 rows x 128 
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_PROBS = 176;
-// bf16 launches run in clusters of two CTAs that share their A operand
-// tiles by TMA multicast, so each issues three operand boxes per stage
-// instead of four (the per-SM rate of TMA box loads bounds the engine's
-// operand stream); tf32x3 launches run as single CTAs (see make_plan).
 constexpr int MAPS_PER_COPY = 240;
 constexpr int STAGE_LD = 36;                              // epilogue staging row pitch (floats)
 constexpr size_t EPI_STAGE_BYTES = 4 * 32 * STAGE_LD * sizeof(float);
@@ -120,17 +116,10 @@ __global__ void map_copy_kernel(const __grid_constant__ MapCopyParams P) {
 
 struct Work {
     int p, tile, tm, tn, split, kt0, kt1;
-    bool valid;  // false: the idle half of a cluster pair (computes a copy, stores nothing)
 };
 
-// Work item w of the launch.  CL == 1: w is (problem, tile, K split).
-// CL == 2: w is (problem, tile pair, K split); the two CTAs of a cluster take
-// the two tiles of a pair -- neighbours in one row of output tiles, so they
-// read the same A rows over the same K range and share them by multicast.
-// A row with an odd number of tiles ends in a pair whose second tile does not
-// exist: that CTA repeats the first tile and stores nothing.
-template <int CL>
-__device__ __forceinline__ Work decode_work(const TcParams &P, int w, int rank) {
+// Work item w of the launch: (problem, output tile, K split).
+__device__ __forceinline__ Work decode_work(const TcParams &P, int w) {
     int lo = 0, hi = P.nprob - 1;
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
@@ -139,9 +128,8 @@ __device__ __forceinline__ Work decode_work(const TcParams &P, int w, int rank) 
     const TcProb &q = P.prob[lo];
     Work k;
     k.p = lo;
-    k.valid = true;
     const int local = w - q.work_begin;
-    const int unit = local / q.ksplit;  // tile (CL 1) or tile pair (CL 2)
+    const int unit = local / q.ksplit;  // output tile
     k.split = local - unit * q.ksplit;
     const int T = q.tiles_n;
     if (q.syrk || q.sym) {
@@ -150,26 +138,20 @@ __device__ __forceinline__ Work decode_work(const TcParams &P, int w, int rank) 
         int u = unit, tm = 0, base = 0;
         for (;;) {
             const int first = tm * BM / q.bn, cnt = T - first;
-            const int units = CL == 1 ? cnt : (cnt + 1) / 2;
-            if (u < units) {
-                int off = CL * u + (CL == 1 ? 0 : rank);
-                if (off >= cnt) { off = CL * u; k.valid = false; }
+            if (u < cnt) {
                 k.tm = tm;
-                k.tn = first + off;
-                k.tile = base + off;
+                k.tn = first + u;
+                k.tile = base + u;
                 break;
             }
-            u -= units;
+            u -= cnt;
             base += cnt;
             ++tm;
         }
     } else {
-        const int per_row = CL == 1 ? T : (T + 1) / 2;
-        k.tm = unit / per_row;
-        int off = CL * (unit - k.tm * per_row) + (CL == 1 ? 0 : rank);
-        if (off >= T) { off -= CL - 1; k.valid = false; }
-        k.tn = off;
-        k.tile = k.tm * T + off;
+        k.tm = unit / T;
+        k.tn = unit - k.tm * T;
+        k.tile = unit;
     }
     k.kt0 = (int)((long long)k.split * q.k_tiles / q.ksplit);
     k.kt1 = (int)((long long)(k.split + 1) * q.k_tiles / q.ksplit);
@@ -240,26 +222,6 @@ __device__ __forceinline__ void im2col_load(uint8_t *dst, const CUtensorMap *map
                            (uint16_t)cur.sx[2 * which + half], (uint16_t)cur.r[2 * which + half], bar);
 }
 
-__device__ __forceinline__ void tma_load_im2col_4d_mc(void *dst, const CUtensorMap *map, int c, int w, int h, int n,
-                                                      uint16_t off_w, uint16_t off_h, uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8}, %9;" ::"r"(smem_u32(dst)),
-        "l"((uint64_t)map), "r"(c), "r"(w), "r"(h), "r"(n), "r"(smem_u32(bar)), "h"(off_w), "h"(off_h), "h"(mask)
-        : "memory");
-}
-
-// Half `half` of the A operand (which 0) through the im2col map, multicast to `mask`.
-__device__ __forceinline__ void im2col_load_half_mc(uint8_t *dst, const CUtensorMap *map, const TcProb &q,
-                                                    const Im2colCursor &cur, int half, uint64_t *bar,
-                                                    uint16_t mask) {
-    const int w = cur.wo * q.im_stride - q.im_pad, h = cur.ho * q.im_stride - q.im_pad;
-    const int c0 = half ? cur.c0[1] : cur.c0[0];
-    const int sx = half ? cur.sx[1] : cur.sx[0];
-    const int r = half ? cur.r[1] : cur.r[0];
-    tma_load_im2col_4d_mc(dst + 16384 * half, map, c0, w, h, cur.img, (uint16_t)sx, (uint16_t)r, bar, mask);
-}
-
 __device__ __forceinline__ void im2col_advance(const TcProb &q, Im2colCursor &cur) {
     cur.wo += 128;
     while (cur.wo >= q.im_wo) {
@@ -288,16 +250,6 @@ __device__ __forceinline__ void load_tile_bf16(uint8_t *dst, const CUtensorMap *
         tma_load_2d(dst, map, col0 + k0, row0 + mn0, bar);
         tma_load_2d(dst + 16384, map, col0 + k0 + 64, row0 + mn0, bar);
     }
-}
-
-// Box `half` (0 | 1) of a bf16 operand tile (as load_tile_bf16), multicast to
-// the CTAs in `mask` when it is nonzero.
-__device__ __forceinline__ void load_half_bf16(uint8_t *dst, const CUtensorMap *map, int mn_major, int row0,
-                                               int col0, int mn0, int k0, int half, uint64_t *bar, uint16_t mask) {
-    const int c0 = mn_major ? col0 + mn0 + 64 * half : col0 + k0 + 64 * half;
-    const int c1 = mn_major ? row0 + k0 : row0 + mn0;
-    if (mask) tma_load_2d_mc(dst + 16384 * half, map, c0, c1, bar, mask);
-    else tma_load_2d(dst + 16384 * half, map, c0, c1, bar);
 }
 
 // Descriptors of the kk-th 32-byte K slice of a staged operand tile.
@@ -492,7 +444,7 @@ __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, con
     }
 }
 
-template <int KIND, int CL>
+template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams P) {
     using Tr = Traits<KIND>;
     constexpr int STAGE_BYTES = Tr::TILES * Tr::TILE;
@@ -509,15 +461,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     float *epi_stage = (float *)(smem + Tr::STAGES * STAGE_BYTES + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // CL == 2: clusters of two CTAs; work items are tile pairs (decode_work)
-    const int rank = CL == 1 ? 0 : (int)cluster_ctarank();
-    const int w_first = blockIdx.x / CL, w_step = gridDim.x / CL;
-    const uint16_t pair_mask = 0x3;
+    const int w_first = blockIdx.x, w_step = gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Tr::STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], CL);  // CL == 2: freed by the MMAs of both CTAs
+            mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf[b], 1);
@@ -529,10 +478,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     }
     if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
     tc_fence_before();
-    if (CL > 1)
-        cluster_sync();  // both CTAs' barriers exist before either multicasts into the other
-    else
-        __syncthreads();
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // the prologue above may overlap the preceding kernel; operands, maps and
@@ -546,7 +492,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             uint32_t phase = 0;
             int last_p = -1;
             for (int w = w_first; w < P.total_work && !*abort_flag; w += w_step) {
-                Work k = decode_work<CL>(P, w, rank);
+                Work k = decode_work(P, w);
                 const TcProb &q = P.prob[k.p];
                 const CUtensorMap *ma = P.maps + q.map_a;
                 const CUtensorMap *mb = P.maps + q.map_b;
@@ -574,31 +520,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     mbar_arrive_expect_tx(&full[stage], bytes);
                     uint8_t *sa = smem + stage * STAGE_BYTES;
                     const int k0 = kt * Tr::BK;
-                    // A: with CL == 2 each CTA loads one of its two boxes and
-                    // multicasts it to both (the pair shares the A rows)
                     if (KIND == TC_KIND_BF16 && q.im2col) {
-                        if (CL == 1) im2col_load(sa, ma, q, cur, 0, &full[stage]);
-                        else im2col_load_half_mc(sa, ma, q, cur, rank, &full[stage], pair_mask);
+                        im2col_load(sa, ma, q, cur, 0, &full[stage]);
                         if (!diag) im2col_load(sa + Tr::TILE, mb, q, cur, 1, &full[stage]);
                         im2col_advance(q, cur);
                     } else if (KIND == TC_KIND_BF16) {
-                        if (CL == 1)
-                            load_tile_bf16(sa, ma, q.a_mn, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
-                        else
-                            load_half_bf16(sa, ma, q.a_mn, q.a_row0, q.a_col0, k.tm * BM, k0, rank, &full[stage],
-                                           pair_mask);
+                        load_tile_bf16(sa, ma, q.a_mn, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
                         if (!diag)
                             load_tile_bf16(sa + Tr::TILE, mb, q.b_mn, q.b_row0, q.b_col0, k.tn * BN, k0,
                                            &full[stage]);
                     } else {
-                        if (CL == 1) {
-                            load_tile(sa, ma, 0, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
-                            load_tile(sa + TILE_BYTES, ma + 1, 0, q.a_row0, q.a_col0, k.tm * BM, k0,
-                                      &full[stage]);
-                        } else {  // rank 0: A hi, rank 1: A lo
-                            tma_load_2d_mc(sa + rank * TILE_BYTES, ma + rank, q.a_col0 + k0, q.a_row0 + k.tm * BM,
-                                           &full[stage], pair_mask);
-                        }
+                        load_tile(sa, ma, 0, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
+                        load_tile(sa + TILE_BYTES, ma + 1, 0, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
                         if (q.bn == BN) {
                             load_tile(sa + 2 * TILE_BYTES, mb, 0, q.b_row0, q.b_col0, k.tn * BN, k0, &full[stage]);
                             load_tile(sa + 3 * TILE_BYTES, mb + 1, 0, q.b_row0, q.b_col0, k.tn * BN, k0,
@@ -620,7 +553,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             uint32_t phase = 0;
             int it = 0;
             for (int w = w_first; w < P.total_work && !*abort_flag; w += w_step, ++it) {
-                Work k = decode_work<CL>(P, w, rank);
+                Work k = decode_work(P, w);
                 const TcProb &q = P.prob[k.p];
                 const bool diag = KIND == TC_KIND_BF16 && q.syrk && k.tm == k.tn;
                 const int b = it & 1;
@@ -661,10 +594,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                             tc_mma_tf32(d_tmem, operand_desc(al, 0, kk), dbh, idesc, 1u);
                         }
                     }
-                    if (CL > 1)
-                        tc_commit_mc(&empty[stage], pair_mask);  // the stage holds multicast data of both CTAs
-                    else
-                        tc_commit(&empty[stage]);
+                    tc_commit(&empty[stage]);
                     if (++stage == Tr::STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
@@ -679,7 +609,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         float *stage = epi_stage + (warp - 2) * 32 * STAGE_LD;
         int it = 0;
         for (int w = w_first; w < P.total_work && !*abort_flag; w += w_step, ++it) {
-            Work k = decode_work<CL>(P, w, rank);
+            Work k = decode_work(P, w);
             const TcProb &q = P.prob[k.p];
             const int b = it & 1;
             const uint32_t use = (uint32_t)(it >> 1);
@@ -688,18 +618,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             const bool mirror = q.sym && k.tn >= (k.tm + 1) * (BM / q.bn);
             float4 oh[8], ol[8];
             // the first chunk's old values load while the MMAs run
-            if (q.ksplit == 1 && k.valid) load_old(q, i0, k.tn * q.bn, lane, oh, ol);
+            if (q.ksplit == 1) load_old(q, i0, k.tn * q.bn, lane, oh, ol);
             if (!mbar_wait(&accf[b], use & 1)) {
                 atomicOr(P.error, ERR_TIMEOUT_ACC);
                 *abort_flag = 1;
                 break;
             }
             tc_fence_after();
-            if (!k.valid) {  // the idle half of a pair: nothing to store
-                tc_fence_before();
-                mbar_arrive(&acce[b]);
-                continue;
-            }
             const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + b * BN;
             if (q.ksplit == 1) {
 #pragma unroll 1
@@ -762,16 +687,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
-    // neither CTA of a pair leaves while the other may still multicast into
-    // its shared memory or arrive on its barriers
-    if (CL > 1) cluster_sync();
 }
 
 // ------------------------------------------------------------------ host
 
 struct Plan {
     int bn = BN;               // output tile width of every job in the call
-    int cl = 1;                // CTAs per cluster (1, or 2: A tiles shared by multicast)
     std::vector<int> order;    // job indices in launch order
     std::vector<int> ksplit;   // per job
     std::vector<int> tiles;    // per job
@@ -806,10 +727,6 @@ Plan make_plan(const TcJob *jobs, int n, int kind, int sms) {
         }
     }
     double total = 0.0;
-    // bf16 launches (factor statistics, preconditioning) run alone and pair
-    // up; the tf32x3 Schur launches overlap a concurrent stream, where a
-    // cluster's need for two free SMs at once costs more than multicast saves
-    p.cl = kind == TC_KIND_BF16 ? 2 : 1;
     for (int i = 0; i < n; ++i) {
         p.tiles[i] = tiles_of(jobs[i], p.bn);
         p.k_tiles[i] = (int)ceil_div(jobs[i].K, bk_of(kind));
@@ -866,23 +783,10 @@ cudaError_t set_smem_attr() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(tc_gemm_kernel<KIND, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        err = cudaFuncSetAttribute(tc_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)SMEM_BYTES);
-        if (err == cudaSuccess)
-            err = cudaFuncSetAttribute(tc_gemm_kernel<KIND, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SMEM_BYTES);
     });
     return err;
-}
-
-// Work units of a job: tiles (cl 1), or tile pairs of one tile row (cl 2).
-int units_of(const TcJob &j, int bn, int cl) {
-    const int tm = (int)ceil_div(j.M, BM), tn = (int)ceil_div(j.N, bn);
-    if (cl == 1) return tiles_of(j, bn);
-    if (!(j.syrk || j.sym)) return tm * ((tn + 1) / 2);
-    int n = 0;
-    for (int t = 0; t < tm; ++t) n += (std::max(0, tn - t * BM / bn) + 1) / 2;
-    return n;
 }
 
 }  // namespace
@@ -1002,7 +906,7 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
             q.im_ho = j.im_wo > 0 ? j.im_howo / j.im_wo : 0;
             q.partial = bufs.part[ji];
             q.counters = bufs.cnt[ji];
-            work += units_of(j, p.bn, p.cl) * p.ksplit[ji];
+            work += p.tiles[ji] * p.ksplit[ji];
             ++nprob;
             ++pos;
         }
@@ -1010,21 +914,11 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
         P->nprob = nprob;
         P->total_work = work;
         P->error = err;
-        const int grid = p.cl * std::max(1, std::min(work, sms / p.cl));
-        if (p.cl == 2) {
-            if (kind == TC_KIND_BF16)
-                KFAC_LAUNCH_CLUSTER(KK_TC_BF16, st, 2, (tc_gemm_kernel<TC_KIND_BF16, 2>), grid, NUM_THREADS,
-                                    SMEM_BYTES, *P);
-            else
-                KFAC_LAUNCH_CLUSTER(KK_TC_TF32X3, st, 2, (tc_gemm_kernel<TC_KIND_TF32X3, 2>), grid, NUM_THREADS,
-                                    SMEM_BYTES, *P);
-        } else {
-            if (kind == TC_KIND_BF16)
-                KFAC_LAUNCH(KK_TC_BF16, st, (tc_gemm_kernel<TC_KIND_BF16, 1>), grid, NUM_THREADS, SMEM_BYTES, *P);
-            else
-                KFAC_LAUNCH(KK_TC_TF32X3, st, (tc_gemm_kernel<TC_KIND_TF32X3, 1>), grid, NUM_THREADS, SMEM_BYTES,
-                            *P);
-        }
+        const int grid = std::max(1, std::min(work, sms));
+        if (kind == TC_KIND_BF16)
+            KFAC_LAUNCH(KK_TC_BF16, st, tc_gemm_kernel<TC_KIND_BF16>, grid, NUM_THREADS, SMEM_BYTES, *P);
+        else
+            KFAC_LAUNCH(KK_TC_TF32X3, st, tc_gemm_kernel<TC_KIND_TF32X3>, grid, NUM_THREADS, SMEM_BYTES, *P);
     }
     return KFAC_OK;
 }

@@ -349,6 +349,24 @@ def test_precondition_f32():
     assert rel(f64(out), oracle.precondition(Gi, grad, Ai)) <= 1e-4
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_precondition_clears_error_word(dtype):
+    """The first int32 of the workspace is the device error word: every call
+    sets it to 0 before its kernels, whatever the operand dtype."""
+    dG, dA = 40, 72
+    G = torch.eye(dG, device=DEV, dtype=dtype)
+    A = torch.eye(dA, device=DEV, dtype=dtype)
+    g = torch.ones(dG, dA, device=DEV, dtype=dtype)
+    out = torch.empty(dG, dA, device=DEV)
+    items = [kfac.PrecondItem(G, A, g, out)]
+    ws = torch.zeros(kfac.kfac_precondition_workspace_size(items), dtype=torch.uint8, device=DEV)
+    ws[:4].view(torch.int32).fill_(-1)
+    kfac.kfac_precondition(items, ws)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    assert bool((out == 1.0).all())
+
+
 # -------------------------------------------------------------- whole layer step
 
 def test_fc64x32_fp32_step():

@@ -41,6 +41,9 @@ MUTANTS = [
     ("precondition drops G^-1", "acc += Ginv[o * dG + k] * T[k * dA + j];",
      "acc += (k == o) * T[k * dA + j];",
      [lambda: pins.test_factored_preconditioner_is_explicit_kronecker_solve(3, 2)]),
+    ("precondition rows transposed A^-1", "out[t * dA + j] += uk * Ainv[k * dA + j];",
+     "out[t * dA + j] += uk * Ainv[j * dA + k] * (j == k ? 1.0 : 0.5);",
+     [pins.test_precondition_rows_are_rows_of_the_kronecker_solve]),
     ("bn unbiased variance", "double f = s2 / (double)ns;", "double f = s2 / (double)(ns - 1);",
      [pins.test_bn_diag_is_diagonal_of_explicit_fisher]),
     ("bn drops damping", "out[c] = gmean[c] / (F[c] + gamma);", "out[c] = gmean[c] / F[c];",

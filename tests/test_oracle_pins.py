@@ -206,6 +206,24 @@ def test_factored_preconditioner_is_explicit_kronecker_solve(dA, dG):
     np.testing.assert_allclose(out, ref, rtol=1e-9, atol=1e-12 * np.abs(ref).max())
 
 
+def test_precondition_rows_are_rows_of_the_kronecker_solve():
+    """Selected rows of Eq. 7 (the sampled check at sizes where the full
+    product is too slow): equal to rows of the explicit Kronecker solve, in
+    any order and with repeats."""
+    rng = np.random.default_rng(11)
+    dA, dG = 6, 5
+    A, G = _spd(dA, rng), _spd(dG, rng, scale=1e-2)
+    grad = rng.standard_normal((dG, dA))
+    Ainv, Ginv = oracle.damped_inverse(A, 0.1), oracle.damped_inverse(G, 0.01)
+    K = np.kron(G + 0.01 * np.eye(dG), A + 0.1 * np.eye(dA))
+    ref = np.linalg.solve(K, grad.reshape(-1)).reshape(dG, dA)
+    rows = [4, 0, 2, 2]
+    got = oracle.precondition_rows(Ginv, grad, Ainv, rows)
+    np.testing.assert_allclose(got, ref[rows], rtol=1e-9, atol=1e-12 * np.abs(ref).max())
+    full = oracle.precondition(Ginv, grad, Ainv)
+    np.testing.assert_allclose(got, full[rows], rtol=1e-12, atol=1e-15 * np.abs(full).max())
+
+
 def test_pi_split_is_invariant_to_moving_scale_between_factors():
     """A -> cA, G -> G/c leaves the pi-damped preconditioned gradient
     unchanged (so the choice of which factor carries 1/M is immaterial)."""
