@@ -25,7 +25,7 @@ enum TcEpilogue : int {
     TC_EPI_ACCUM = 0,  // fp32 C[i][j] = beta*C[i][j] + alpha*acc (C read only if beta != 0)
     TC_EPI_STORE = 1,  // C (fp32, optional) and/or Cb (bf16, optional) = alpha*acc
     TC_EPI_SPLIT = 2   // v = alpha*acc + beta*(C + C_lo); C = tf32(v), C_lo = v - C;
-                       // optional transposed copy into Ct / Ct_lo
+                       // optional transposed copy into Ct / Ct_lo (C may then be null)
 };
 
 struct TcJob {
@@ -34,8 +34,13 @@ struct TcJob {
     int a_row0, a_col0, b_row0, b_col0;
     int M, N, K;
     int syrk;
-    int sym;       // TF32X3 + SPLIT, M == N: the result is symmetric; only tiles on or
-                   // above the diagonal run and off-diagonal ones also write their transpose
+    int sym;       // M == N, symmetric result (TF32X3, SPLIT or STORE epilogue): only tiles
+                   // on or above the diagonal run and off-diagonal ones also write their
+                   // transpose
+    int lower;     // TF32X3: only tiles touching the lower triangle (i >= j) run, each
+                   // written in full (no mirror)
+    int ktri;      // TF32X3: the K range of output tile (tm, tn) starts at the tile's first
+                   // column (B upper triangular in its K index: B[j][t] = 0 for t < j)
     int no_split;
     int epi;
     float alpha, beta;

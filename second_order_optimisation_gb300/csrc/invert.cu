@@ -7,28 +7,22 @@
 // method it builds on):
 //     pi = sqrt((tr A/dA) / (tr G/dG)),  damp_A = pi sqrt(gamma),  damp_G = sqrt(gamma)/pi.
 //
-// Algorithm (the matrices advance in batched rounds, one launch per round, see
-// schedule_rounds; the longest chains and the rest run as two concurrent
-// groups, see InvGroup):
-//   1. traces -> damping values (one CTA per layer, fixed reduction order);
-//   2. X = sym(F) + damp I, padded with an identity block to a multiple of
-//      128 (the inverse of diag(X, I) is diag(X^-1, I)), stored as a (hi, lo)
-//      pair with hi exactly representable in tf32 and hi + lo = X;
-//   3. inversion by recursive 2x2 blocking on 128-row block boundaries down
-//      to leaves of 128 or 256 rows; the Schur complement X22 - X21 X11^-1 X12
-//      is the trailing update of a block Cholesky step:
-//        X11 <- X11^-1                               (recursion / leaf)
-//        T   <- X11 X12,   U <- T^T                  (tensor cores)
-//        X22 <- X22 - X21 T       (symmetric: upper tiles + mirror)
-//        X22 <- X22^-1                               (recursion / leaf)
-//        X12 <- -T X22,    X21 <- X12^T              (tensor cores)
-//        X11 <- X11 - X12 T^T     (symmetric: upper tiles + mirror)
-//      The GEMMs run on tcgen05 with three tf32 products per slice
-//      (hi*hi + hi*lo + lo*hi) and fp32 accumulation.  A leaf is inverted
-//      by one CTA with the block resident in TMEM: a Gauss-Jordan sweep in
-//      32-wide block steps, each one rank-32 tensor-core product (tleaf_kernel);
-//   4. out = hi + lo of the upper triangle mirrored to the lower one (exact
-//      symmetry), plus the optional bf16 copy.
+// Algorithm: Cholesky X = L L^T of X = sym(F) + damp I, the triangular
+// inverse W = L^-1, and X^-1 = W^T W (the order of a Cholesky-based
+// inversion: factor, triangular inverse, product of the inverse factors).  X
+// is padded with an identity block to a multiple of 128 (the inverse of
+// diag(X, I) is diag(X^-1, I)).  The Cholesky factor is formed left-looking
+// in 128-wide block columns (gen_chain), so every Schur-complement column
+// comes from Cholesky panels (no growth) and the inverse keeps fp32-level
+// accuracy on damped factors with condition numbers around 1e4; the 128 x 128
+// diagonal blocks are factored and inverted by one CTA each (diag_kernel).
+// The triangular inverse is recursive 2 x 2 blocking, the final product one
+// triangular-aware product that writes the caller's symmetric fp32 inverse
+// (and its bf16 copy) directly.  The products run on tcgen05 with three tf32
+// products per slice (hi*hi + hi*lo + lo*hi) and fp32 accumulation on (hi, lo)
+// pairs (hi exactly representable in tf32, hi + lo the fp32 value).  The
+// matrices advance in batched rounds, one launch per round (schedule_rounds);
+// the longest chains and the rest run as two concurrent groups (InvGroup).
 // A pivot that is not positive and finite records its 1-based index in
 // info[matrix]; nothing traps, and every wait on a barrier has a time limit.
 #include <algorithm>
@@ -43,14 +37,13 @@ namespace kfac {
 
 namespace {
 
-constexpr int LEAF = 128;
-constexpr int LEAF_MAX = 256;  // largest leaf block (one CTA, block resident in TMEM)
+constexpr int NB = 128;    // block width of the sweep
 constexpr int MAT_MAX = 224;
-// tensor maps of one matrix: X, T, U pairs, each as hi / lo with 128-row and
-// with 32-row boxes
+// tensor maps of one matrix: X, Wt, LT pairs, each as hi / lo with 128-row
+// and with 32-row boxes
 constexpr int MAPS_PER_MATRIX = 12;
 
-inline int padded(int d) { return (int)ceil_div(d, LEAF) * LEAF; }
+inline int padded(int d) { return (int)ceil_div(d, NB) * NB; }
 
 __device__ __forceinline__ float tf32_hi(float v) {
     return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
@@ -105,20 +98,16 @@ __global__ void __launch_bounds__(256) damping_kernel(const __grid_constant__ Da
     }
 }
 
-// ------------------------------------------------------ prepare / finish
+// ------------------------------------------------------------- prepare
 
 struct TileMat {
-    const float *F;   // prep: factor (upper read); finish: unused
+    const float *F;   // factor (upper triangle read)
     long long ldf;
     float *Xh, *Xl;   // working pair [dp][dp]
     int d, dp;
-    float *out;       // finish: full symmetric fp32 output
-    long long ldo;
-    uint16_t *out16;  // finish: optional bf16 copy
-    long long ld16;
     int damp_idx;
     int tiles;        // 64-wide tiles per side
-    int vec_f, vec_o, vec_b;  // F / out rows take 16-byte, out16 rows 8-byte accesses
+    int vec_f;        // F rows take 16-byte accesses
 };
 
 struct TileParams {
@@ -128,7 +117,7 @@ struct TileParams {
     const float *damp;
 };
 
-constexpr int TT = 64;  // prep / finish tile
+constexpr int TT = 64;  // prep tile
 
 // The upper tile pair (si <= sj) of this CTA: matrix index and tile coordinates.
 __device__ __forceinline__ const TileMat &tile_of(const TileParams &P, int &si, int &sj) {
@@ -145,17 +134,11 @@ __device__ __forceinline__ const TileMat &tile_of(const TileParams &P, int &si, 
     return q;
 }
 
-// Value (r, c) of output tile (ti, tj) from the staged upper tile t of the pair
-// (si, sj) = (min, max): the tile itself, its transpose, or (diagonal tile) its
-// upper triangle mirrored.
-__device__ __forceinline__ float tile_val(const float (*t)[TT + 1], int si, int sj, bool transposed, int r, int c) {
-    if (si != sj) return transposed ? t[c][r] : t[r][c];
-    return r <= c ? t[r][c] : t[c][r];
-}
-
-// X = split(sym(F) + damp I) on [d, d], identity on the padding.  One CTA per
-// upper 64 x 64 tile pair: the upper tile of F is read once (16-byte pieces
-// where the rows allow) and written to both its own and its mirrored position.
+// X = (lower part of sym(F) + damp I, zero strictly above the diagonal) as a
+// (hi, lo) pair on [d, d], identity on the padding.  One CTA per upper 64 x 64
+// tile pair: the upper tile of F is read once (16-byte pieces where the rows
+// allow) and written transposed to its lower position; the upper position
+// gets zeros (the diagonal tile: its lower triangle and zeros).
 __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ TileParams P) {
     pdl_wait();
     pdl_trigger();
@@ -195,12 +178,10 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ TileP
             for (int u = 0; u < 4; ++u) {
                 const int c = c4 + u, j = tj * TT + c;
                 float v;
-                if (i >= q.d || j >= q.d) {
-                    v = (i == j) ? 1.f : 0.f;
-                } else {
-                    v = tile_val(t, si, sj, side == 1, r, c);
-                    if (i == j) v += dv;
-                }
+                if (i >= q.d || j >= q.d) v = (i == j) ? 1.f : 0.f;
+                else if (side == 0 && si != sj) v = 0.f;     // strictly upper tile
+                else if (side == 0) v = r >= c ? t[c][r] + (i == j ? dv : 0.f) : 0.f;  // diagonal tile
+                else v = t[c][r];                             // lower position: F transposed
                 h[u] = tf32_hi(v);
                 l[u] = v - h[u];
             }
@@ -211,434 +192,412 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ TileP
     }
 }
 
-// out = hi + lo of the upper triangle, mirrored; optional bf16 copy.  One CTA
-// per upper 64 x 64 tile pair of [d, d].
-__global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ TileParams P) {
-    pdl_wait();
-    pdl_trigger();
-    __shared__ float t[TT][TT + 1];
-    int si, sj;
-    const TileMat &q = tile_of(P, si, sj);
-    const int tid = threadIdx.x, rr = tid >> 4, c4 = (tid & 15) * 4;
-    {
-        float4 h[4], l[4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {  // inside [dp, dp]: always in bounds
-            const long long o = (long long)(si * TT + rr + 16 * p) * q.dp + sj * TT + c4;
-            h[p] = *reinterpret_cast<const float4 *>(q.Xh + o);
-            l[p] = *reinterpret_cast<const float4 *>(q.Xl + o);
-        }
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const int r = rr + 16 * p;
-            t[r][c4] = h[p].x + l[p].x;
-            t[r][c4 + 1] = h[p].y + l[p].y;
-            t[r][c4 + 2] = h[p].z + l[p].z;
-            t[r][c4 + 3] = h[p].w + l[p].w;
-        }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int side = 0; side < 2; ++side) {
-        if (side == 1 && si == sj) break;
-        const int ti = side ? sj : si, tj = side ? si : sj;
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const int r = rr + 16 * p, i = ti * TT + r, j = tj * TT + c4;
-            if (i >= q.d) continue;
-            float v[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = tile_val(t, si, sj, side == 1, r, c4 + u);
-            float *dst = q.out + (long long)i * q.ldo + j;
-            if (q.vec_o && j + 3 < q.d) {
-                *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-            } else {
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (j + u < q.d) dst[u] = v[u];
-            }
-            if (q.out16) {
-                uint16_t *d16 = q.out16 + (long long)i * q.ld16 + j;
-                if (q.vec_b && j + 3 < q.d) {
-                    const uint32_t lo2 = f32_to_bf16_bits(v[0]) | ((uint32_t)f32_to_bf16_bits(v[1]) << 16);
-                    const uint32_t hi2 = f32_to_bf16_bits(v[2]) | ((uint32_t)f32_to_bf16_bits(v[3]) << 16);
-                    *reinterpret_cast<uint2 *>(d16) = make_uint2(lo2, hi2);
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        if (j + u < q.d) d16[u] = f32_to_bf16_bits(v[u]);
-                }
-            }
-        }
-    }
-}
+// ------------------------------------------------------------------ diag
 
-// ------------------------------------------------------------------ leaves
-
-struct LeafJob {
-    float *Xh, *Xl;  // block start (row o, column o) of the working pair
+struct DiagJob {
+    float *Xh, *Xl;    // block (k, k) of the working pair: its lower triangle is read, then
+                       // W_kk = L_kk^-1 written over the whole block (zeros above the diagonal)
+    float *Th, *Tl;    // the same block of the transposed pair: W_kk^T (zeros below)
     long long ld;
-    int o;           // global offset, for info
+    int o;             // global index of the block's first row (for info)
     int *info;
-    int n;           // block size: LEAF or 2 LEAF
 };
 
-struct LeafParams {
-    LeafJob j[MAT_MAX];
+struct DiagParams {
+    DiagJob j[MAT_MAX];
     int n;
-    int *error;      // timeout bits (TMEM-resident leaf)
 };
 
-// In-place inverse of one SPD N x N block (N = 128 or 256) by one CTA of N
-// threads, a blocked Gauss-Jordan sweep whose block steps run on the tensor
-// cores.  The block lives in TMEM for the whole sweep (row i at lane i % 128,
-// columns (i / 128) N .. +N-1); the CTA holds all of TMEM when N = 256.
-// Block step s pivots on K = {32s .. 32s+31}.  With C = A[:, K] (the pivot
-// column panel), P = A[K, K], W = P^-1 A[K, :] and E_K the rows of the
-// identity on K, the complete Gauss-Jordan update
-//   a_ij -= a_iK W_Kj,  a_Kj <- W_Kj,  a_iK <- -a_iK P^-1,  a_KK <- P^-1
-// is the single rank-32 product  A += (-C~) W~^T  where C~ = C - E_K (rows K
-// of the panel become P - I) and W~ = W with the columns K replaced by
-// I + P^-1; it runs as tf32 products of (hi, lo) splits (hi*hi + hi*lo +
-// lo*hi) with fp32 accumulation in TMEM.  The block stays sign-symmetric
-// (a_ij = -a_ji when exactly one of i, j has been pivoted), so A[K, j] is
-// +-C[j, :] and W never needs the pivot rows themselves: the product on the
-// columns K runs first and gives -C P^-1, and its rows are the columns of W
-// up to sign.  The next step's panel columns are updated (and signalled) ahead
-// of the rest of the product, whose MMAs overlap the next pivot block's
-// inverse (P^-1: a 32 x 32 Gauss-Jordan sweep by the warp holding rows K).
-// A pivot outside [FLT_MIN, inf) (not positive, subnormal or not finite) is
-// recorded in info and eliminated as 1 / a_kk = 0; the inverse is then
-// undefined, but the sweep runs to its end.
-template <int N>
-struct TLeafSmem {
-    static constexpr int NH = N / 128;                 // 128-row halves
-    static constexpr uint32_t A_TILE = 128 * 128;      // 128 rows x 32 tf32 (128-byte swizzled rows)
-    static constexpr uint32_t B_TILE = N * 128;        // N rows x 32 tf32
-    static constexpr uint32_t OFF_A = 0;               // [2 buffers][NH][hi, lo]
-    static constexpr uint32_t OFF_B = OFF_A + 2 * NH * 2 * A_TILE;  // [hi, lo]
-    static constexpr uint32_t OFF_K = OFF_B + 2 * B_TILE;           // pivot block B operand [hi, lo]
-    static constexpr uint32_t OFF_BAR = OFF_K + 2 * 4096;
-    static constexpr uint32_t BYTES = OFF_BAR + 64 + 1024;          // + alignment slack
-    static constexpr int STG = 36;                                  // row pitch of the I/O staging (floats)
-};
+// Cholesky factor and its inverse of one SPD 128 x 128 block S = L L^T, by
+// one CTA of 256 threads: W = L^-1, written over the block and, transposed,
+// into the same block of the transposed pair.
+//
+// The sweep works on one array M (lower triangle) that holds the Schur
+// complement still to be factored in its columns past the current pivots and
+// the rows of W in progress in the columns before.  A single pivot c, with
+// w = 1 / sqrt(M_cc) and p_i = w M_ic (= L_ic), does
+//   i > c, j < c:      M_ij -= p_i (w M_cj)    (rows of W in progress)
+//   i > c, j = c:      M_ic  = -p_i w
+//   i > c, c < j <= i: M_ij -= p_i p_j         (Schur complement)
+//   i = c, j < c:      M_cj *= w;   M_cc = w   (row c of W final)
+// and four pivots K = {c .. c+3} at a time are the same four steps fused:
+// with W_K = the 4 x 4 result of those rules on the pivot block alone,
+//   p_i = W_K M[i][K]   (i past K),   y_j = W_K M[K][j]   (j before K),
+//   i past K:  M_ij -= p_i . y_j (j < c),  M_iK = -p_i^T W_K,  M_ij -= p_i . p_j (K < j <= i)
+//   i in K:    M[K][j] = y_j (j < c),  M[K][K] = W_K.
+// Thread t keeps the elements of rows r0 + 16a and columns c0 + 16b
+// (r0 = t / 16, c0 = t % 16, a, b = 0..7) in registers; each step the pivot
+// column block and row block are published through shared memory, threads
+// 0..127 form the 4-vectors p_i / y_j once, and all threads apply the
+// rank-4 update (two barriers per step).  1 / sqrt is the correctly rounded
+// square root and division.  A pivot outside [FLT_MIN, inf) is recorded and
+// eliminated with w = 0 (the result is then undefined but finite).
+constexpr int DIAG_LD = NB + 4;  // staging row pitch (floats; rows stay 16-byte aligned)
+constexpr size_t DIAG_SMEM = (size_t)NB * DIAG_LD * sizeof(float)  // block staging
+                             + 2 * NB * sizeof(float4)              // pivot column blocks (double-buffered)
+                             + 2 * 4 * NB * sizeof(float)           // pivot row blocks
+                             + NB * sizeof(float4)                  // the 4-vectors p_i / y_j
+                             + 16 * sizeof(float) + 16;             // W_K, first bad pivot
 
-// Row r (32 tf32 of K) of a 128-byte-swizzled K-major operand tile, split
-// into hi / lo tiles.
-__device__ __forceinline__ void stage_row_split(uint8_t *hi, uint8_t *lo, int r, const float *x) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const float4 v = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
-        const float4 h = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
-        const uint32_t off = (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4);
-        *reinterpret_cast<float4 *>(hi + off) = h;
-        *reinterpret_cast<float4 *>(lo + off) = make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
-    }
+__device__ __forceinline__ float f4c(const float4 &v, int q) { return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w; }
+__device__ __forceinline__ void f4set(float4 &v, int q, float x) {
+    if (q == 0) v.x = x; else if (q == 1) v.y = x; else if (q == 2) v.z = x; else v.w = x;
 }
 
-// D[128 x ncols] += A[128 x 32] B[ncols x 32]^T with (hi, lo) operand tiles.
-__device__ __forceinline__ void tleaf_mma(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo,
-                                          int ncols) {
-    const uint32_t idesc = idesc_tf32_f32(128, ncols);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ah = smem_desc_sw128(a_hi + kk * 32, 16, 1024), al = smem_desc_sw128(a_lo + kk * 32, 16, 1024);
-        const uint64_t bh = smem_desc_sw128(b_hi + kk * 32, 16, 1024), bl = smem_desc_sw128(b_lo + kk * 32, 16, 1024);
-        tc_mma_tf32(d, ah, bh, idesc, 1u);
-        tc_mma_tf32(d, ah, bl, idesc, 1u);
-        tc_mma_tf32(d, al, bh, idesc, 1u);
-    }
-}
-
-// 1 / x for a pivot in [FLT_MIN, inf): the flush-to-zero approximate
-// reciprocal refined by one Newton-Raphson step, r <- r + r (1 - x r).
-__device__ __forceinline__ float recip_ftz_nr(float x) {
-    float r;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-    return fmaf(r, fmaf(-x, r, 1.0f), r);
-}
-
-// In-place inverse of the 32 x 32 pivot block held by one warp (lane r: row
-// r), Gauss-Jordan without pivoting (every leading block of an SPD matrix is
-// SPD).  The pivot row is broadcast with shuffles.  The row registers rotate
-// by one column per pivot (position j holds column (k + j) mod 32 before
-// pivot k), so that the pivot column is always p[0] and every index is
-// static; after 32 pivots the columns are back in place.  Rows i != k take
-// a_ij - f a_kj with f = a_ik / a_kk; the pivot row takes f = 1 - 1 / a_kk,
-// which turns the same FMA into a_kj / a_kk.  Returns the first pivot that
-// was not in [FLT_MIN, inf) (-1 if none); such a pivot is eliminated as
-// 1 / a_kk = 0.
-__device__ __forceinline__ int pivot_block_inverse(float (&p)[32], int lane) {
+// The single-pivot rules on a 4 x 4 lower block (element [r][q], r >= q):
+// returns W_K in place; bad = index (0..3) of the first pivot outside
+// [FLT_MIN, inf), or -1.
+__device__ __forceinline__ int pivot4(float (&S)[4][4]) {
     int bad = -1;
-#pragma unroll 2
-    for (int k = 0; k < 32; ++k) {
-        float pk[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) pk[j] = __shfl_sync(0xffffffffu, p[j], k);
-        const float d = pk[0];
-        const bool ok = d >= 1.17549435e-38f && d < INFINITY;
-        const float inv = ok ? recip_ftz_nr(d) : 0.f;
-        if (!ok && bad < 0) bad = k;
-        const bool own = lane == k;
-        const float f = own ? 1.f - inv : p[0] * inv;
+    for (int q = 0; q < 4; ++q) {
+        const float piv = S[q][q];
+        const bool ok = piv >= FLT_MIN && piv < INFINITY;
+        const float w = ok ? 1.0f / sqrtf(piv) : 0.f;
+        if (!ok && bad < 0) bad = q;
+        float p[4];
 #pragma unroll
-        for (int j = 0; j < 31; ++j) p[j] = fmaf(-f, pk[j + 1], p[j + 1]);
-        p[31] = own ? inv : -f;  // column k, now at the last position
+        for (int r = 0; r < 4; ++r) p[r] = r > q ? S[r][q] * w : 0.f;
+#pragma unroll
+        for (int r = q + 1; r < 4; ++r) {
+#pragma unroll
+            for (int j = 0; j < q; ++j) S[r][j] = fmaf(-p[r], w * S[q][j], S[r][j]);
+            S[r][q] = -p[r] * w;
+#pragma unroll
+            for (int j = q + 1; j <= r; ++j) S[r][j] = fmaf(-p[r], p[j], S[r][j]);
+        }
+#pragma unroll
+        for (int j = 0; j < q; ++j) S[q][j] *= w;
+        S[q][q] = w;
     }
     return bad;
 }
 
-template <int N>
-__global__ void __launch_bounds__(N, 1) tleaf_kernel(const __grid_constant__ LeafParams P) {
-    using S = TLeafSmem<N>;
-    constexpr int NH = S::NH, NS = N / 32;
-    constexpr uint32_t NCOL = N == 128 ? 128 : 512;
-    extern __shared__ uint8_t tl_raw[];
-    uint8_t *smem = (uint8_t *)(((uintptr_t)tl_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t *bar_k = (uint64_t *)(smem + S::OFF_BAR);
-    uint64_t *bar_next = bar_k + 1;
-    uint64_t *bar_done = bar_k + 2;
-    uint32_t *tmem_slot = (uint32_t *)(bar_k + 3);
-    int *bad_s = (int *)(tmem_slot + 1);
-    volatile int *abort_s = bad_s + 1;  // a wait ran out: every thread leaves the sweep
-
-    const LeafJob &J = P.j[blockIdx.x];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = warp >> 2, q = warp & 3;
-    const int row = 128 * h + 32 * q + lane;   // this thread's row of the block
-    const int row0 = row - lane;               // first row of this warp
-    const uint32_t lane_field = (uint32_t)(32 * q) << 16;
-
-    if (warp == 0) tmem_alloc(tmem_slot, NCOL);
-    if (tid == 0) {
-        mbar_init(bar_k, 1);
-        mbar_init(bar_next, 1);
-        mbar_init(bar_done, 1);
-        *bad_s = -1;
-        *abort_s = 0;
-        fence_barrier_init();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t t_row = tmem + lane_field + (uint32_t)(h * N);  // column 0 of this thread's row
+__global__ void __launch_bounds__(256, 1) diag_kernel(const __grid_constant__ DiagParams P) {
+    extern __shared__ float4 diag_smem4[];
+    float *st = reinterpret_cast<float *>(diag_smem4);
+    float4 *colb = reinterpret_cast<float4 *>(st + NB * DIAG_LD);  // [2][NB]: M[i][c .. c+3]
+    float *rowb = reinterpret_cast<float *>(colb + 2 * NB);        // [2][4][NB]: M[c + q][j]
+    float4 *pv = reinterpret_cast<float4 *>(rowb + 2 * 4 * NB);    // [NB]
+    float *wk = reinterpret_cast<float *>(pv + NB);                 // [4][4]
+    int *bad_s = reinterpret_cast<int *>(wk + 16);
+    const DiagJob &J = P.j[blockIdx.x];
+    const int tid = threadIdx.x, r0 = tid >> 4, c0 = tid & 15;
+    const bool dg = c0 <= r0;  // element (a, a) is on or below the diagonal
+    if (tid == 0) *bad_s = -1;
     pdl_wait();
     pdl_trigger();
-
-    // ---- load: X = hi + lo into TMEM (coalesced through a per-warp stage)
-    float *stg = (float *)(smem + S::OFF_A) + warp * 32 * S::STG;
-#pragma unroll 1
-    for (int c = 0; c < N / 32; ++c) {
-        float4 hv[8], lv[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const long long off = (long long)(row0 + 4 * k + (lane >> 3)) * J.ld + 32 * c + 4 * (lane & 7);
-            hv[k] = *reinterpret_cast<const float4 *>(J.Xh + off);
-            lv[k] = *reinterpret_cast<const float4 *>(J.Xl + off);
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            *reinterpret_cast<float4 *>(&stg[(4 * k + (lane >> 3)) * S::STG + 4 * (lane & 7)]) =
-                make_float4(hv[k].x + lv[k].x, hv[k].y + lv[k].y, hv[k].z + lv[k].z, hv[k].w + lv[k].w);
-        __syncwarp();
-        float v[32];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float4 t = *reinterpret_cast<const float4 *>(&stg[lane * S::STG + 4 * j]);
-            v[4 * j] = t.x; v[4 * j + 1] = t.y; v[4 * j + 2] = t.z; v[4 * j + 3] = t.w;
-        }
-        tmem_st_32x32b_x32(t_row + 32 * c, v);
-        __syncwarp();
+    // block -> shared memory (16-byte pieces, hi + lo) -> registers
+    for (int e = tid; e < NB * NB / 4; e += 256) {
+        const int i = e >> 5, j = (e & 31) * 4;
+        const long long off = (long long)i * J.ld + j;
+        const float4 h = *reinterpret_cast<const float4 *>(J.Xh + off);
+        const float4 l = *reinterpret_cast<const float4 *>(J.Xl + off);
+        *reinterpret_cast<float4 *>(st + i * DIAG_LD + j) = make_float4(h.x + l.x, h.y + l.y, h.z + l.z, h.w + l.w);
     }
-    tmem_st_wait();
-    tc_fence_before();
     __syncthreads();
-
-    uint8_t *const kb_hi = smem + S::OFF_K, *const kb_lo = kb_hi + 4096;
-    uint8_t *const bu_hi = smem + S::OFF_B, *const bu_lo = bu_hi + S::B_TILE;
-#pragma unroll 1
-    for (int s = 0; s < NS; ++s) {
-        const int ks = 32 * s;
-        const int pw = 4 * (ks >> 7) + ((ks & 127) >> 5);  // warp holding rows K
-        uint8_t *const au_hi = smem + S::OFF_A + (uint32_t)(((s & 1) * NH + h) * 2) * S::A_TILE;
-        uint8_t *const au_lo = au_hi + S::A_TILE;
-        // panel C = A[:, K] (updated by the previous step's first MMAs); the
-        // thread issuing the previous step's remaining MMAs joins later
-        if (s > 0 && !mbar_wait(bar_next, (uint32_t)((s - 1) & 1))) *abort_s = 1;
-        __syncwarp();  // warp 0 reconverges after its MMA issue (tcgen05.ld is warp-collective)
-        tc_fence_after();
-        float c[32];
-        tmem_ld_32x32b_x32(t_row + ks, c);
-        const bool in_k = row >= ks && row < ks + 32;
-        {
-            const int dj = in_k ? row - ks : -1;  // this row's column inside K
-            float a[32];  // -(C - E_K)
+    float m[8][8];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) a[j] = __int_as_float(__float_as_int(1.f) & -(int)(dj == j)) - c[j];
-            stage_row_split(au_hi, au_lo, 32 * q + lane, a);
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int i = r0 + 16 * a, j = c0 + 16 * b;
+            m[a][b] = j <= i ? st[i * DIAG_LD + j] : 0.f;
         }
-        if (warp == pw) {  // P^-1, then the pivot block's B rows I + P^-1
-            const int bad = pivot_block_inverse(c, lane);
-            if (lane == 0 && bad >= 0 && *bad_s < 0) *bad_s = ks + bad;
+    // pivot column block and row block of the first step
+    if (c0 < 4) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) c[j] += j == lane ? 1.f : 0.f;
-            stage_row_split(kb_hi, kb_lo, lane, c);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (*abort_s) break;
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int hh = 0; hh < NH; ++hh) {
-                const uint32_t a0 = smem_u32(smem + S::OFF_A + (uint32_t)(((s & 1) * NH + hh) * 2) * S::A_TILE);
-                tleaf_mma(tmem + (uint32_t)(hh * N + ks), a0, a0 + S::A_TILE, smem_u32(kb_hi), smem_u32(kb_lo), 32);
-            }
-            tc_commit(bar_k);
-        }
-        // columns K now hold -C P^-1 (rows outside K) and P^-1 (rows K);
-        // W[:, i] = +v (i pivoted before this step) or -v (i after K)
-        if (!mbar_wait(bar_k, (uint32_t)(s & 1))) *abort_s = 1;
-        __syncwarp();
-        tc_fence_after();
-        {
-            float v[32];
-            tmem_ld_32x32b_x32(t_row + ks, v);
-            if (!in_k) {
-                if (row > ks) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = -v[j];
-                }
-                stage_row_split(bu_hi, bu_lo, row, v);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (*abort_s) break;
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t bh = smem_u32(bu_hi), bl = smem_u32(bu_lo);
-            const bool more = s + 1 < NS;
-            if (more) {  // the next panel first
-#pragma unroll
-                for (int hh = 0; hh < NH; ++hh) {
-                    const uint32_t a0 = smem_u32(smem + S::OFF_A + (uint32_t)(((s & 1) * NH + hh) * 2) * S::A_TILE);
-                    tleaf_mma(tmem + (uint32_t)(hh * N + ks + 32), a0, a0 + S::A_TILE, bh + (ks + 32) * 128,
-                              bl + (ks + 32) * 128, 32);
-                }
-                tc_commit(bar_next);
-            }
-            const int r1 = more ? ks + 64 : N;  // remaining columns: [0, ks) and [r1, N)
-#pragma unroll
-            for (int hh = 0; hh < NH; ++hh) {
-                const uint32_t a0 = smem_u32(smem + S::OFF_A + (uint32_t)(((s & 1) * NH + hh) * 2) * S::A_TILE);
-                if (ks > 0) tleaf_mma(tmem + (uint32_t)(hh * N), a0, a0 + S::A_TILE, bh, bl, ks);
-                if (r1 < N)
-                    tleaf_mma(tmem + (uint32_t)(hh * N + r1), a0, a0 + S::A_TILE, bh + r1 * 128, bl + r1 * 128, N - r1);
-            }
-            if (!more) tc_commit(bar_done);
-        }
+        for (int a = 0; a < 8; ++a) reinterpret_cast<float *>(&colb[r0 + 16 * a])[c0] = m[a][0];
     }
-    bool ok = !*abort_s && mbar_wait(bar_done, 0u);
-    ok = __syncthreads_and(ok);
-    if (!ok && tid == 0 && P.error) atomicOr(P.error, ERR_TIMEOUT_LEAF);
-    tc_fence_after();
-
-    // ---- store: A^-1 as (hi, lo) (coalesced through the per-warp stage)
-    if (ok) {
-#pragma unroll 1
-        for (int c = 0; c < N / 32; ++c) {
-            float v[32];
-            tmem_ld_32x32b_x32(t_row + 32 * c, v);
+    if (r0 < 4) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<float4 *>(&stg[lane * S::STG + 4 * j]) =
-                    make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-            __syncwarp();
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float4 t = *reinterpret_cast<const float4 *>(&stg[(4 * k + (lane >> 3)) * S::STG + 4 * (lane & 7)]);
-                const float4 hh = make_float4(tf32_hi(t.x), tf32_hi(t.y), tf32_hi(t.z), tf32_hi(t.w));
-                const long long off = (long long)(row0 + 4 * k + (lane >> 3)) * J.ld + 32 * c + 4 * (lane & 7);
-                *reinterpret_cast<float4 *>(J.Xh + off) = hh;
-                *reinterpret_cast<float4 *>(J.Xl + off) = make_float4(t.x - hh.x, t.y - hh.y, t.z - hh.z, t.w - hh.w);
-            }
-            __syncwarp();
-        }
+        for (int b = 0; b < 8; ++b) rowb[r0 * NB + c0 + 16 * b] = m[0][b];
     }
-    tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
-        tc_fence_after();
-        tmem_dealloc(tmem, NCOL);
+#pragma unroll 1
+    for (int s = 0; s < NB / 4; ++s) {
+        const int c = 4 * s, cur = s & 1, nxt = cur ^ 1;
+        const float4 *cb = colb + cur * NB;
+        const float *rb = rowb + cur * 4 * NB;
+        if (tid < NB) {
+            float W[4][4];
+            // W_K from the pivot block (every phase-A thread; thread 0 publishes it)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v = cb[c + q];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) W[q][r] = r <= q ? f4c(v, r) : 0.f;
+            }
+            const int bad = pivot4(W);
+            if (tid == 0) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) wk[q * 4 + r] = W[q][r];
+                if (bad >= 0 && *bad_s < 0) *bad_s = c + bad;
+            }
+            // p_t = W_K M[t][K] (t past K), y_t = W_K M[K][t] (t before K)
+            const int t = tid;
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
+            if (t >= c + 4) {
+                const float4 v = cb[t];
+                x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+            } else if (t < c) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) x[r] = rb[r * NB + t];
+            }
+            float4 o;
+            o.x = W[0][0] * x[0];
+            o.y = fmaf(W[1][0], x[0], W[1][1] * x[1]);
+            o.z = fmaf(W[2][0], x[0], fmaf(W[2][1], x[1], W[2][2] * x[2]));
+            o.w = fmaf(W[3][0], x[0], fmaf(W[3][1], x[1], fmaf(W[3][2], x[2], W[3][3] * x[3])));
+            pv[t] = o;
+        }
+        __syncthreads();
+        // rows past K: M_ij -= p_i . z_j with z_j = y_j (j < c), p_j (j past K);
+        // the columns K take -p_i^T W_K
+        float4 z[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int j = c0 + 16 * b;
+            if (j >= c && j < c + 4) {
+                const int r = j - c;
+                z[b] = make_float4(wk[r], wk[4 + r], wk[8 + r], wk[12 + r]);
+            } else {
+                z[b] = pv[j];
+            }
+        }
+        const bool zk = (c0 & ~3) == (c & 15);  // this thread's columns K (at b = c / 16)
+        const int bk = c >> 4;
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+            if (r0 + 16 * a >= c + 4) {
+                const float4 pa = pv[r0 + 16 * a];
+#pragma unroll
+                for (int b = 0; b <= a; ++b) {
+                    if (b == a && !dg) continue;
+                    const float base = (zk && b == bk) ? 0.f : m[a][b];
+                    float v = fmaf(-pa.x, z[b].x, base);
+                    v = fmaf(-pa.y, z[b].y, v);
+                    v = fmaf(-pa.z, z[b].z, v);
+                    m[a][b] = fmaf(-pa.w, z[b].w, v);
+                }
+            }
+        }
+        // rows K: M[K][j] = y_j (j < c), M[K][K] = W_K
+        const int qr = r0 - (c & 15);
+        if (qr >= 0 && qr < 4) {
+            switch (bk) {
+#define KFAC_DIAG_ROWK(A)                                                             \
+    case A:                                                                           \
+        _Pragma("unroll") for (int b = 0; b <= A; ++b) {                              \
+            const int j = c0 + 16 * b;                                                \
+            if (j < c) m[A][b] = f4c(z[b], qr);                                       \
+            else if (j < c + 4 && j - c <= qr) m[A][b] = wk[qr * 4 + j - c];          \
+        }                                                                             \
+        break;
+                KFAC_DIAG_ROWK(0) KFAC_DIAG_ROWK(1) KFAC_DIAG_ROWK(2) KFAC_DIAG_ROWK(3)
+                KFAC_DIAG_ROWK(4) KFAC_DIAG_ROWK(5) KFAC_DIAG_ROWK(6) KFAC_DIAG_ROWK(7)
+#undef KFAC_DIAG_ROWK
+            }
+        }
+        // publish the next step's pivot column block and row block
+        const int n = c + 4;
+        if (n < NB) {
+            const int nl = n & 15, nh = n >> 4;
+            const int qc = c0 - nl, qn = r0 - nl;
+            if (qc >= 0 && qc < 4) {
+                float4 *dst = colb + nxt * NB;
+                switch (nh) {
+#define KFAC_DIAG_PUBC(B)                                                                                   \
+    case B:                                                                                                 \
+        _Pragma("unroll") for (int a = 0; a < 8; ++a) reinterpret_cast<float *>(&dst[r0 + 16 * a])[qc] = m[a][B]; \
+        break;
+                    KFAC_DIAG_PUBC(0) KFAC_DIAG_PUBC(1) KFAC_DIAG_PUBC(2) KFAC_DIAG_PUBC(3)
+                    KFAC_DIAG_PUBC(4) KFAC_DIAG_PUBC(5) KFAC_DIAG_PUBC(6) KFAC_DIAG_PUBC(7)
+#undef KFAC_DIAG_PUBC
+                }
+            }
+            if (qn >= 0 && qn < 4) {
+                float *dst = rowb + nxt * 4 * NB + qn * NB;
+                switch (nh) {
+#define KFAC_DIAG_PUBR(A)                                                             \
+    case A:                                                                           \
+        _Pragma("unroll") for (int b = 0; b < 8; ++b) dst[c0 + 16 * b] = m[A][b];     \
+        break;
+                    KFAC_DIAG_PUBR(0) KFAC_DIAG_PUBR(1) KFAC_DIAG_PUBR(2) KFAC_DIAG_PUBR(3)
+                    KFAC_DIAG_PUBR(4) KFAC_DIAG_PUBR(5) KFAC_DIAG_PUBR(6) KFAC_DIAG_PUBR(7)
+#undef KFAC_DIAG_PUBR
+                }
+            }
+        }
+        __syncthreads();
+    }
+    // W (lower, zeros above) into X and W^T (upper, zeros below) into the
+    // transposed pair, staged through shared memory so that every global
+    // store is a 16-byte piece of a row
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int i = r0 + 16 * a, j = c0 + 16 * b;
+            st[i * DIAG_LD + j] = j <= i ? m[a][b] : 0.f;
+        }
+    __syncthreads();
+    for (int e = tid; e < NB * NB / 4; e += 256) {
+        const int i = e >> 5, j = (e & 31) * 4;
+        float w4[4], t4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            w4[u] = st[i * DIAG_LD + j + u];
+            t4[u] = st[(j + u) * DIAG_LD + i];
+        }
+        float hw[4], ht[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            hw[u] = tf32_hi(w4[u]);
+            ht[u] = tf32_hi(t4[u]);
+        }
+        const long long off = (long long)i * J.ld + j;
+        *reinterpret_cast<float4 *>(J.Xh + off) = make_float4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<float4 *>(J.Xl + off) =
+            make_float4(w4[0] - hw[0], w4[1] - hw[1], w4[2] - hw[2], w4[3] - hw[3]);
+        *reinterpret_cast<float4 *>(J.Th + off) = make_float4(ht[0], ht[1], ht[2], ht[3]);
+        *reinterpret_cast<float4 *>(J.Tl + off) =
+            make_float4(t4[0] - ht[0], t4[1] - ht[1], t4[2] - ht[2], t4[3] - ht[3]);
     }
     if (tid == 0 && *bad_s >= 0 && J.info) atomicCAS(J.info, 0, J.o + *bad_s + 1);
 }
 
 // ------------------------------------------------------------- scheduler
 
+// One launch unit of a matrix's chain: a diag leaf, or engine problems that
+// go into the same launch.
 struct Op {
     int leaf;
-    LeafJob lj;
-    TcJob g;
+    DiagJob dj;
+    std::vector<TcJob> g;
 };
 
-// Working buffers of one matrix with d > LEAF.
+// Working buffers of one matrix (fp32 (hi, lo) pairs, [dp][dp] each):
+//   X   lower part: the factor, its block columns updated into Schur-complement
+//       columns, then W = L^-1 (diagonal blocks from the diag leaves, the
+//       rest from the triangular inverse); strictly upper part zero
+//   Wt  upper part: W^T (diagonal blocks in full, zeros below)
+//   LT  lower blocks: the Cholesky panels L_ik (i > k);  upper blocks:
+//       (L21 W11)^T of the triangular inverse
 struct MatWork {
     int d, dp;
-    float *Xh, *Xl, *Th, *Tl, *Uh, *Ul;
-    int mx, mt, mu;  // map indices (hi; lo at +1)
+    float *Xh, *Xl, *Wh, *Wl, *Lh, *Ll;
+    int mx, mw, ml;  // map indices (hi; lo at +1; 32-row boxes at +2, +3)
 };
 
-void gen_ops(std::vector<Op> &ops, const MatWork &w, int o, int n, int *info) {
+TcJob split_job(int ma, int ar, int ac, int mb, int br, int bc, int M, int N, int K, float alpha, float beta,
+                float *Ch, float *Cl, float *Cth, float *Ctl, long long ld) {
+    TcJob j{};
+    j.map_a = ma; j.a_row0 = ar; j.a_col0 = ac;
+    j.map_b = mb; j.b_row0 = br; j.b_col0 = bc;
+    j.M = M; j.N = N; j.K = K;
+    j.epi = TC_EPI_SPLIT;
+    j.alpha = alpha; j.beta = beta;
+    j.C = Ch; j.C_lo = Cl; j.ldc = ld;
+    j.Ct = Cth; j.Ct_lo = Ctl; j.ldct = ld;
+    return j;
+}
+
+// Nodes of the triangular-inverse recursion over [o, o + n) with their
+// heights (a 128-row block: height 0).
+int tri_nodes(int o, int n, std::vector<std::vector<std::pair<int, int>>> &by_height) {
+    if (n == NB) return 0;
+    const int nb = n / NB, h = NB * (nb / 2);
+    const int ht = 1 + std::max(tri_nodes(o, h, by_height), tri_nodes(o + h, n - h, by_height));
+    if ((int)by_height.size() <= ht) by_height.resize(ht + 1);
+    by_height[ht].push_back({o, n});
+    return ht;
+}
+
+// The chain of one matrix.
+//  1. left-looking blocked Cholesky, 128-wide block columns k:
+//       X[k:, k] -= L[k:, :k] L[k, :k]^T                 (engine; k > 0)
+//       W_kk = L_kk^-1 from X[k, k]                      (diag leaf)
+//       L[k+1:, k] = X[k+1:, k] W_kk^T                   (engine; the panel)
+//     every Schur-complement column comes from Cholesky panels (no growth);
+//  2. W = L^-1 by recursive 2 x 2 blocking, bottom up by height (the two
+//     halves of a node are independent):
+//       T = L21 W11,   W21 = -W22 T   (W21 over X's lower part, W21^T into Wt);
+//  3. X^-1 = W^T W = Wt Wt^T, written into the caller's output.
+// W11, W22 are lower triangular with zeros above in X and their transposes
+// upper triangular with zeros below in Wt, so the products run over whole
+// blocks; T reads W11^T from Wt only from each output tile's first column on
+// (ktri), where Wt holds its upper part and diagonal blocks.
+void gen_chain(std::vector<Op> &ops, const MatWork &w, const InvMatrix &mat, int *info) {
     const long long ld = w.dp;
-    if (n == LEAF || n == LEAF_MAX) {  // one leaf launch (TMEM-resident block)
-        Op op{};
-        op.leaf = 1;
-        op.lj = LeafJob{w.Xh + o * ld + o, w.Xl + o * ld + o, ld, o, info, n};
-        ops.push_back(op);
-        return;
+    const int nb = w.dp / NB;
+    for (int k = 0; k < nb; ++k) {
+        const int kb = k * NB;
+        if (k > 0) {
+            Op op{};
+            op.g.push_back(split_job(w.ml, kb, 0, w.ml, kb, 0, w.dp - kb, NB, kb, -1.f, 1.f, w.Xh + kb * ld + kb,
+                                     w.Xl + kb * ld + kb, nullptr, nullptr, ld));
+            ops.push_back(op);
+        }
+        {
+            Op op{};
+            op.leaf = 1;
+            op.dj = DiagJob{w.Xh + kb * ld + kb, w.Xl + kb * ld + kb, w.Wh + kb * ld + kb, w.Wl + kb * ld + kb,
+                            ld, kb, info};
+            ops.push_back(op);
+        }
+        if (k + 1 < nb) {
+            const long long c = (long long)(kb + NB) * ld + kb;
+            Op op{};
+            op.g.push_back(split_job(w.mx, kb + NB, kb, w.mx, kb, kb, w.dp - kb - NB, NB, NB, 1.f, 0.f, w.Lh + c,
+                                     w.Ll + c, nullptr, nullptr, ld));
+            ops.push_back(op);
+        }
     }
-    const int nb = n / LEAF, h = LEAF * (nb / 2), m = n - h;
-    gen_ops(ops, w, o, h, info);
-    auto gemm = [&](int ma, int ar, int ac, int mb, int br, int bc, int M, int N, int K, float alpha,
-                    float beta, float *Ch, float *Cl, float *Cth, float *Ctl, int sym) {
-        Op op{};
-        op.leaf = 0;
-        TcJob &j = op.g;
-        j.map_a = ma; j.a_row0 = ar; j.a_col0 = ac;
-        j.map_b = mb; j.b_row0 = br; j.b_col0 = bc;
-        j.M = M; j.N = N; j.K = K;
-        j.epi = TC_EPI_SPLIT;
-        j.alpha = alpha; j.beta = beta;
-        j.C = Ch; j.C_lo = Cl; j.ldc = ld;
-        j.Ct = Cth; j.Ct_lo = Ctl; j.ldct = ld;
-        j.sym = sym;
-        ops.push_back(op);
-    };
-    const long long x11 = o * ld + o, x12 = o * ld + o + h, x21 = (o + h) * ld + o, x22 = (o + h) * ld + o + h;
-    const long long tt = o * ld;  // T block: rows [o, o+h), columns [0, m)
-    // T = X11 X12 (B rows = X21 rows), U = T^T
-    gemm(w.mx, o, o, w.mx, o + h, o, h, m, h, 1.f, 0.f, w.Th + tt, w.Tl + tt, w.Uh, w.Ul, 0);
-    // X22 -= X21 T  (B rows = U rows)
-    gemm(w.mx, o + h, o, w.mu, 0, 0, m, m, h, -1.f, 1.f, w.Xh + x22, w.Xl + x22, nullptr, nullptr, 1);
-    gen_ops(ops, w, o + h, m, info);
-    // X12 = -T X22 (X22 symmetric: B rows = X22 rows), X21 = X12^T
-    gemm(w.mt, o, 0, w.mx, o + h, o + h, h, m, m, -1.f, 0.f, w.Xh + x12, w.Xl + x12, w.Xh + x21, w.Xl + x21, 0);
-    // X11 -= X12 T^T (B rows = T rows)
-    gemm(w.mx, o, o + h, w.mt, o, 0, h, h, m, -1.f, 1.f, w.Xh + x11, w.Xl + x11, nullptr, nullptr, 1);
+    std::vector<std::vector<std::pair<int, int>>> by_height;
+    tri_nodes(0, w.dp, by_height);
+    for (size_t ht = 1; ht < by_height.size(); ++ht) {
+        Op t{}, x{};
+        for (const auto &nd : by_height[ht]) {
+            const int o = nd.first, n = nd.second, h = NB * (n / NB / 2), m = n - h;
+            const long long x21 = (long long)(o + h) * ld + o, t12 = (long long)o * ld + o + h;
+            // T = L21 W11 (B rows: W11^T rows, in Wt), stored as T^T in LT's upper part
+            t.g.push_back(split_job(w.ml, o + h, o, w.mw, o, o, m, h, h, 1.f, 0.f, nullptr, nullptr, w.Lh + t12,
+                                    w.Ll + t12, ld));
+            t.g.back().ktri = 1;
+            // W21 = -W22 T (A: W22 rows, in X; B rows: T^T rows, in LT), W21^T into Wt
+            x.g.push_back(split_job(w.mx, o + h, o + h, w.ml, o, o + h, m, h, m, -1.f, 0.f, w.Xh + x21,
+                                    w.Xl + x21, w.Wh + t12, w.Wl + t12, ld));
+        }
+        ops.push_back(t);
+        ops.push_back(x);
+    }
+    Op fin{};
+    TcJob j{};
+    j.map_a = j.map_b = w.mw;
+    j.M = j.N = w.d;
+    j.K = w.dp;
+    j.sym = 1;
+    j.ktri = 1;
+    j.epi = TC_EPI_STORE;
+    j.alpha = 1.f;
+    j.C = mat.out;
+    j.ldc = mat.ldo;
+    j.Cb = mat.out_bf16;
+    j.ldcb = mat.ldo_bf16;
+    fin.g.push_back(j);
+    ops.push_back(fin);
 }
 
 // Round schedule of a group of chains: the group's longest chain sets the
-// sequence of rounds (one launch each, leaf or GEMM); every other chain of the
-// group is embedded as late as possible into rounds of the same op kind, in
-// order.  The long chain's late rounds are small, latency-bound launches with
-// most SMs idle, and the shorter chains' work fills them.  Falls back to
-// left-aligned lock-step (a leaf and a GEMM launch per round) if a chain does
-// not embed.  Rounds list (chain, op) pairs.
+// sequence of rounds (one launch each, leaf or engine); every other chain of
+// the group is embedded as late as possible into rounds of the same op kind,
+// in order.  The long chain's late rounds are small, latency-bound launches
+// with most SMs idle, and the shorter chains' work fills them.  Falls back to
+// left-aligned lock-step (a leaf and an engine launch per round) if a chain
+// does not embed.  Rounds list (chain, op) pairs.
 std::vector<std::vector<std::pair<int, int>>> schedule_rounds(const std::vector<std::vector<Op>> &chains,
                                                               const std::vector<int> &members,
                                                               std::vector<int> &round_kind) {
@@ -669,7 +628,6 @@ std::vector<std::vector<std::pair<int, int>>> schedule_rounds(const std::vector<
             for (int i = 0; i < (int)chains[k].size(); ++i) rounds[slot[k][i]].push_back({k, i});
         return rounds;
     }
-    // fallback: left-aligned lock-step, leaves then GEMMs in each step
     size_t longest = 0;
     for (int k : members) longest = std::max(longest, chains[k].size());
     rounds.clear();
@@ -687,18 +645,17 @@ std::vector<std::vector<std::pair<int, int>>> schedule_rounds(const std::vector<
     return rounds;
 }
 
-// Workspace layout shared by the size query and the run.
 // The chains run as two concurrent groups: the longest ones (the critical
 // path of the call) on a high-priority stream, all others on a low-priority
-// stream whose GEMM launches leave SMs free for the first group.  Each group
-// has its own rounds and engine scratch.
-constexpr int RESERVED_SMS = 32;  // SMs the second group's GEMM launches leave free
+// stream whose engine launches leave SMs free for the first group.  Each
+// group has its own rounds and engine scratch.
+constexpr int RESERVED_SMS = 32;  // SMs the second group's engine launches leave free
 
 struct InvGroup {
     std::vector<int> members;  // chain indices
     std::vector<std::vector<std::pair<int, int>>> rounds;
     std::vector<int> round_kind;
-    int max_ctas = 0;          // GEMM grid cap (0: all SMs)
+    int max_ctas = 0;          // engine grid cap (0: all SMs)
     char *tc_ws = nullptr;
     size_t tc_bytes = 0;
 };
@@ -713,11 +670,10 @@ struct InvPlan {
     size_t longest = 0;
 };
 
+// Workspace layout shared by the size query and the run.
 kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws, InvPlan &p, bool encode) {
     p.err = ws.take<int>(64);
-    int nbig = 0;
-    for (int k = 0; k < nmats; ++k) nbig += mats[k].d > LEAF;
-    p.dev_maps = ws.take<CUtensorMap>(MAPS_PER_MATRIX * (size_t)std::max(nbig, 1));
+    p.dev_maps = ws.take<CUtensorMap>(MAPS_PER_MATRIX * (size_t)std::max(nmats, 1));
     p.work.resize(nmats);
     p.chains.assign(nmats, {});
     for (int k = 0; k < nmats; ++k) {
@@ -727,32 +683,31 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
         const size_t sq = (size_t)w.dp * w.dp;
         w.Xh = ws.take<float>(sq);
         w.Xl = ws.take<float>(sq);
-        w.Th = w.Tl = w.Uh = w.Ul = nullptr;
-        w.mx = w.mt = w.mu = -1;
-        if (w.d > LEAF) {
-            w.Th = ws.take<float>(sq);
-            w.Tl = ws.take<float>(sq);
-            w.Uh = ws.take<float>(sq);
-            w.Ul = ws.take<float>(sq);
-            float *bufs[6] = {w.Xh, w.Xl, w.Th, w.Tl, w.Uh, w.Ul};
-            const int base = (int)p.maps.size();
-            for (int q = 0; q < 6; q += 2)  // per pair: hi, lo (128-row boxes), hi, lo (32-row boxes)
-                for (int v = 0; v < 4; ++v) {
-                    p.maps.emplace_back();
-                    if (encode && !tc_make_map(&p.maps.back(), TC_KIND_TF32X3, bufs[q + (v & 1)], w.dp, w.dp,
-                                               w.dp, v < 2 ? 128 : 32))
-                        return KFAC_ERR_CUDA;
-                }
-            w.mx = base;
-            w.mt = base + 4;
-            w.mu = base + 8;
+        w.Wh = ws.take<float>(sq);
+        w.Wl = ws.take<float>(sq);
+        w.Lh = w.Ll = nullptr;
+        if (w.dp > NB) {
+            w.Lh = ws.take<float>(sq);
+            w.Ll = ws.take<float>(sq);
         }
-        gen_ops(p.chains[k], w, 0, w.dp, info_dev ? info_dev + k : nullptr);
+        float *bufs[6] = {w.Xh, w.Xl, w.Wh, w.Wl, w.Lh, w.Ll};
+        const int base = (int)p.maps.size();
+        for (int q = 0; q < 6; q += 2)  // per pair: hi, lo (128-row boxes), hi, lo (32-row boxes)
+            for (int v = 0; v < 4; ++v) {
+                p.maps.emplace_back();
+                if (encode && bufs[q] &&
+                    !tc_make_map(&p.maps.back(), TC_KIND_TF32X3, bufs[q + (v & 1)], w.dp, w.dp, w.dp, v < 2 ? 128 : 32))
+                    return KFAC_ERR_CUDA;
+            }
+        w.mx = base;
+        w.mw = base + 4;
+        w.ml = base + 8;
+        gen_chain(p.chains[k], w, mats[k], info_dev ? info_dev + k : nullptr);
         p.longest = std::max(p.longest, p.chains[k].size());
     }
-    if (p.maps.size() != (size_t)MAPS_PER_MATRIX * nbig) return KFAC_ERR_WORKSPACE;  // device map area
+    if (p.maps.size() != (size_t)MAPS_PER_MATRIX * nmats) return KFAC_ERR_WORKSPACE;  // device map area
     // groups: chains at least 3/4 as long as the longest form the critical
-    // group; a second group exists only if it is worth a stream of its own
+    // group; the others run concurrently as a second group
     p.groups.assign(1, InvGroup{});
     InvGroup rest;
     for (int k = 0; k < nmats; ++k) {
@@ -763,15 +718,17 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
         rest.max_ctas = std::max(1, device_sm_count() - RESERVED_SMS);
         p.groups.push_back(rest);
     }
-    // engine scratch of each group: its largest GEMM round
+    // engine scratch of each group: its largest engine round
     std::vector<TcJob> round;
     for (InvGroup &g : p.groups) {
         g.rounds = schedule_rounds(p.chains, g.members, g.round_kind);
         size_t tcb = 0;
         for (size_t r = 0; r < g.rounds.size(); ++r) {
             round.clear();
-            for (const auto &ki : g.rounds[r])
-                if (!p.chains[ki.first][ki.second].leaf) round.push_back(p.chains[ki.first][ki.second].g);
+            for (const auto &ki : g.rounds[r]) {
+                const Op &op = p.chains[ki.first][ki.second];
+                if (!op.leaf) round.insert(round.end(), op.g.begin(), op.g.end());
+            }
             tcb = std::max(tcb, tc_workspace_bytes(round.data(), (int)round.size(), TC_KIND_TF32X3, g.max_ctas));
         }
         g.tc_bytes = tcb;
@@ -780,58 +737,42 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
     return KFAC_OK;
 }
 
-template <int N>
-cudaError_t tleaf_smem_attr() {
+cudaError_t diag_smem_attr() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(tleaf_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)TLeafSmem<N>::BYTES);
+        err = cudaFuncSetAttribute(diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DIAG_SMEM);
     });
     return err;
 }
 
-// One launch per leaf size present in the round (N threads, one CTA per block).
-kfac_status leaf_launch(const std::vector<LeafJob> &jobs, int *err, cudaStream_t st) {
-    for (const LeafJob &j : jobs)  // the kernel moves rows in 16-byte pieces
-        if (j.ld % 4 != 0 || (uintptr_t)j.Xh % 16 != 0 || (uintptr_t)j.Xl % 16 != 0 ||
-            (j.n != LEAF && j.n != LEAF_MAX))
+// One launch per round of leaves (one CTA per diagonal block).
+kfac_status diag_launch(const std::vector<DiagJob> &jobs, cudaStream_t st) {
+    for (const DiagJob &j : jobs)  // the kernel writes rows in 16-byte pieces
+        if (j.ld % 4 != 0 || (uintptr_t)j.Xh % 16 != 0 || (uintptr_t)j.Xl % 16 != 0 || (uintptr_t)j.Th % 16 != 0 ||
+            (uintptr_t)j.Tl % 16 != 0)
             return KFAC_ERR_WORKSPACE;
-    std::unique_ptr<LeafParams> P(new LeafParams);
-    for (int size : {LEAF, LEAF_MAX}) {
-        size_t pos = 0;
-        while (pos < jobs.size()) {
-            int n = 0;
-            for (; pos < jobs.size() && n < MAT_MAX; ++pos)
-                if (jobs[pos].n == size) P->j[n++] = jobs[pos];
-            if (n == 0) break;
-            P->n = n;
-            P->error = err;
-            if (size == 128) {
-                if (tleaf_smem_attr<128>() != cudaSuccess) return KFAC_ERR_CUDA;
-                KFAC_LAUNCH(KK_LEAF, st, tleaf_kernel<128>, n, 128, TLeafSmem<128>::BYTES, *P);
-            } else {
-                if (tleaf_smem_attr<256>() != cudaSuccess) return KFAC_ERR_CUDA;
-                KFAC_LAUNCH(KK_LEAF, st, tleaf_kernel<256>, n, 256, TLeafSmem<256>::BYTES, *P);
-            }
-        }
-        if (LEAF_MAX == LEAF) break;
+    if (diag_smem_attr() != cudaSuccess) return KFAC_ERR_CUDA;
+    std::unique_ptr<DiagParams> P(new DiagParams);
+    size_t pos = 0;
+    while (pos < jobs.size()) {
+        int n = 0;
+        for (; pos < jobs.size() && n < MAT_MAX; ++pos) P->j[n++] = jobs[pos];
+        P->n = n;
+        KFAC_LAUNCH(KK_LEAF, st, diag_kernel, n, 256, DIAG_SMEM, *P);
     }
     return KFAC_OK;
 }
 
-template <bool PREP>
-kfac_status tile_launch(std::vector<TileMat> &mats, const float *damp, cudaStream_t st) {
+kfac_status prep_launch(std::vector<TileMat> &mats, const float *damp, cudaStream_t st) {
     std::unique_ptr<TileParams> P(new TileParams);
     size_t pos = 0;
     while (pos < mats.size()) {
         int n = 0, tiles = 0;
         while (pos < mats.size() && n < MAT_MAX) {
             TileMat m = mats[pos++];
-            m.tiles = (int)ceil_div(PREP ? m.dp : m.d, TT);
+            m.tiles = (int)ceil_div(m.dp, TT);
             m.vec_f = m.F && m.ldf % 4 == 0 && (uintptr_t)m.F % 16 == 0;
-            m.vec_o = m.out && m.ldo % 4 == 0 && (uintptr_t)m.out % 16 == 0;
-            m.vec_b = m.out16 && m.ld16 % 4 == 0 && (uintptr_t)m.out16 % 8 == 0;
             P->m[n] = m;
             P->begin[n] = tiles;
             tiles += m.tiles * (m.tiles + 1) / 2;  // upper tile pairs
@@ -840,8 +781,7 @@ kfac_status tile_launch(std::vector<TileMat> &mats, const float *damp, cudaStrea
         P->begin[n] = tiles;
         P->n = n;
         P->damp = damp;
-        if (PREP) KFAC_LAUNCH(KK_PREP, st, prep_kernel, tiles, 256, 0, *P);
-        else KFAC_LAUNCH(KK_FINISH, st, finish_kernel, tiles, 256, 0, *P);
+        KFAC_LAUNCH(KK_PREP, st, prep_kernel, tiles, 256, 0, *P);
     }
     return KFAC_OK;
 }
@@ -883,7 +823,7 @@ namespace {
 
 // Enqueue one group's rounds on a stream.
 kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st) {
-    std::vector<LeafJob> leaves;
+    std::vector<DiagJob> leaves;
     std::vector<TcJob> gemms;
     kfac_status s = KFAC_OK;
     for (size_t r = 0; r < g.rounds.size(); ++r) {
@@ -891,9 +831,10 @@ kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st) {
         gemms.clear();
         for (const auto &ki : g.rounds[r]) {
             const Op &op = p.chains[ki.first][ki.second];
-            if (op.leaf) leaves.push_back(op.lj); else gemms.push_back(op.g);
+            if (op.leaf) leaves.push_back(op.dj);
+            else gemms.insert(gemms.end(), op.g.begin(), op.g.end());
         }
-        if (!leaves.empty() && (s = leaf_launch(leaves, p.err, st)) != KFAC_OK) return s;
+        if (!leaves.empty() && (s = diag_launch(leaves, st)) != KFAC_OK) return s;
         if (!gemms.empty()) {
             Arena tail(g.tc_ws, g.tc_bytes);
             if ((s = tc_run(gemms.data(), (int)gemms.size(), TC_KIND_TF32X3, p.dev_maps, tail, p.err, st,
@@ -941,48 +882,40 @@ kfac_status inv_run(const InvMatrix *mats, int nmats, const float *damp_dev, int
     if (s != KFAC_OK) return s;
     if (!ws.fits()) return KFAC_ERR_WORKSPACE;
     KFAC_CUDA_TRY(cudaMemsetAsync(p.err, 0, sizeof(int), st));
-    if (!p.maps.empty() && (s = tc_upload_maps(p.maps.data(), (int)p.maps.size(), p.dev_maps, st)) != KFAC_OK)
-        return s;
+    if ((s = tc_upload_maps(p.maps.data(), (int)p.maps.size(), p.dev_maps, st)) != KFAC_OK) return s;
 
-    // 1. X = split(sym(F) + damp I), identity padding
+    // 1. X = lower part of sym(F) + damp I (zero above), identity padding
     std::vector<TileMat> tm(nmats);
     for (int k = 0; k < nmats; ++k)
-        tm[k] = TileMat{mats[k].F, mats[k].ldf, p.work[k].Xh, p.work[k].Xl, mats[k].d, p.work[k].dp,
-                        mats[k].out, mats[k].ldo, mats[k].out_bf16, mats[k].ldo_bf16, k, 0, 0, 0, 0};
-    if ((s = tile_launch<true>(tm, damp_dev, st)) != KFAC_OK) return s;
+        tm[k] = TileMat{mats[k].F, mats[k].ldf, p.work[k].Xh, p.work[k].Xl, mats[k].d, p.work[k].dp, k, 0, 0};
+    if ((s = prep_launch(tm, damp_dev, st)) != KFAC_OK) return s;
 
-    // 2. rounds (see schedule_rounds): each round is one leaf or one GEMM
-    //    launch; with two groups, the critical one runs on a high-priority
-    //    stream and the other on a low-priority one, forked from and joined
-    //    back into the caller's stream
-    if (p.groups.size() == 1) {
-        if ((s = run_group(p, p.groups[0], st)) != KFAC_OK) return s;
-    } else {
-        int dev = 0;
-        KFAC_CUDA_TRY(cudaGetDevice(&dev));
-        GroupStreams &g = group_streams(dev);
-        std::lock_guard<std::mutex> lock(g.mu);
-        if ((s = ensure_streams(g)) != KFAC_OK) return s;
-        KFAC_CUDA_TRY(cudaEventRecord(g.fork, st));
-        KFAC_CUDA_TRY(cudaStreamWaitEvent(g.hi, g.fork, 0));
-        KFAC_CUDA_TRY(cudaStreamWaitEvent(g.lo, g.fork, 0));
-        const kfac_status s0 = run_group(p, p.groups[0], g.hi);
-        kfac_status s1;
-        {
-            const PdlScope no_pdl(false);
-            s1 = run_group(p, p.groups[1], g.lo);
-        }
-        // join in every case, so that a capture or later work stays ordered
-        KFAC_CUDA_TRY(cudaEventRecord(g.done_hi, g.hi));
-        KFAC_CUDA_TRY(cudaEventRecord(g.done_lo, g.lo));
-        KFAC_CUDA_TRY(cudaStreamWaitEvent(st, g.done_hi, 0));
-        KFAC_CUDA_TRY(cudaStreamWaitEvent(st, g.done_lo, 0));
-        if (s0 != KFAC_OK) return s0;
-        if (s1 != KFAC_OK) return s1;
+    // 2. rounds (see schedule_rounds), the last op of each chain writing the
+    //    caller's inverse; with two groups, the critical one runs on a
+    //    high-priority stream and the other on a low-priority one, forked
+    //    from and joined back into the caller's stream
+    if (p.groups.size() == 1) return run_group(p, p.groups[0], st);
+    int dev = 0;
+    KFAC_CUDA_TRY(cudaGetDevice(&dev));
+    GroupStreams &g = group_streams(dev);
+    std::lock_guard<std::mutex> lock(g.mu);
+    if ((s = ensure_streams(g)) != KFAC_OK) return s;
+    KFAC_CUDA_TRY(cudaEventRecord(g.fork, st));
+    KFAC_CUDA_TRY(cudaStreamWaitEvent(g.hi, g.fork, 0));
+    KFAC_CUDA_TRY(cudaStreamWaitEvent(g.lo, g.fork, 0));
+    const kfac_status s0 = run_group(p, p.groups[0], g.hi);
+    kfac_status s1;
+    {
+        const PdlScope no_pdl(false);
+        s1 = run_group(p, p.groups[1], g.lo);
     }
-
-    // 3. out = hi + lo, mirrored; bf16 copies
-    return tile_launch<false>(tm, damp_dev, st);
+    // join in every case, so that a capture or later work stays ordered
+    KFAC_CUDA_TRY(cudaEventRecord(g.done_hi, g.hi));
+    KFAC_CUDA_TRY(cudaEventRecord(g.done_lo, g.lo));
+    KFAC_CUDA_TRY(cudaStreamWaitEvent(st, g.done_hi, 0));
+    KFAC_CUDA_TRY(cudaStreamWaitEvent(st, g.done_lo, 0));
+    if (s0 != KFAC_OK) return s0;
+    return s1;
 }
 
 }  // namespace kfac

@@ -39,7 +39,7 @@ namespace {
 constexpr int BM = 128, BN = 128;
 constexpr int TILE_BYTES = 128 * 128;  // one tf32 operand tile: 128 rows x 128 bytes
 constexpr int NUM_THREADS = 192;
-constexpr int TMEM_COLS = 2 * BN;
+constexpr int TMEM_ACC = 2 * BN;  // two accumulators (columns 0 and BN), alternating
 constexpr int MAX_PROBS = 176;
 constexpr int MAPS_PER_COPY = 240;
 constexpr int STAGE_LD = 36;                              // epilogue staging row pitch (floats)
@@ -50,11 +50,20 @@ template <int KIND> struct Traits;
 template <> struct Traits<TC_KIND_BF16> {
     // 128 K per stage: every operand box is 64 x 128 elements (16 KB); a
     // streaming SM sustains about twice the bytes with 16 KB TMA boxes as
-    // with 8 KB ones (the per-SM rate of box loads is the limit)
+    // with 8 KB ones (the per-SM rate of box loads is the limit).  One
+    // accumulation per work item.
     static constexpr int BK = 128, STAGES = 3, TILES = 2, ESZ = 2, TILE = 128 * 128 * 2;
+    static constexpr int CHUNK = 1 << 30, TMEM_COLS = TMEM_ACC;
 };
 template <> struct Traits<TC_KIND_TF32X3> {
+    // A work item accumulates its K range in chunks of CHUNK K tiles (128 K),
+    // alternating between the two TMEM accumulators; the epilogue warps add
+    // each chunk into a running sum held in TMEM (columns 2 BN ..) with fp32
+    // round-to-nearest additions.  Long sums accumulated within one tensor-core
+    // accumulator lose accuracy faster than that (the Cholesky updates of the
+    // inversion run over K up to the factor's width).
     static constexpr int BK = 32, STAGES = 3, TILES = 4, ESZ = 4, TILE = TILE_BYTES;
+    static constexpr int CHUNK = 4, TMEM_COLS = 512;
 };
 
 struct TcProb {
@@ -66,7 +75,7 @@ struct TcProb {
     int bn;                  // output tile width: 128, or 64 / 32 to spread small problems over SMs
     int tiles_n, ksplit, work_begin;
     uint8_t a_mn, b_mn;      // MN-major operand (bf16 only)
-    uint8_t syrk, sym, epi;
+    uint8_t syrk, sym, lower, ktri, epi;
     uint8_t vec;             // C (and C_lo) rows take 16-byte accesses (ldc % 4 == 0, aligned)
     uint8_t vecb;            // Cb rows take 8-byte accesses
     uint8_t im2col, im_k, im_stride, im_pad;  // operands through an im2col map (see TcJob)
@@ -148,15 +157,37 @@ __device__ __forceinline__ Work decode_work(const TcParams &P, int w) {
             base += cnt;
             ++tm;
         }
+    } else if (q.lower) {
+        // tiles touching the lower triangle: row block tm runs column blocks
+        // 0 .. (tm + 1) * 128 / bn - 1
+        int u = unit, tm = 0, base = 0;
+        for (;;) {
+            const int cnt = min(T, (tm + 1) * BM / q.bn);
+            if (u < cnt) {
+                k.tm = tm;
+                k.tn = u;
+                k.tile = base + u;
+                break;
+            }
+            u -= cnt;
+            base += cnt;
+            ++tm;
+        }
     } else {
         k.tm = unit / T;
         k.tn = unit - k.tm * T;
         k.tile = unit;
     }
-    k.kt0 = (int)((long long)k.split * q.k_tiles / q.ksplit);
-    k.kt1 = (int)((long long)(k.split + 1) * q.k_tiles / q.ksplit);
+    // ktri (tf32x3 only, K tiles of 32): K starts at the tile's first column
+    // (an upper tile of the product of an upper-triangular matrix with its
+    // transpose)
+    const int kb = q.ktri ? k.tn * q.bn / Traits<TC_KIND_TF32X3>::BK : 0;
+    k.kt0 = kb + (int)((long long)k.split * (q.k_tiles - kb) / q.ksplit);
+    k.kt1 = kb + (int)((long long)(k.split + 1) * (q.k_tiles - kb) / q.ksplit);
     return k;
 }
+
+__device__ __forceinline__ int ceil_div_dev(int a, int b) { return (a + b - 1) / b; }
 
 __device__ __forceinline__ void acquire_map(const CUtensorMap *m) {
     asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"((uint64_t)m) : "memory");
@@ -325,7 +356,7 @@ __device__ __forceinline__ void load_old(const TcProb &q, int i0, int j0, int la
 // is written straight from v (consecutive lanes are consecutive addresses of
 // Ct); the mirror of a symmetric off-diagonal tile goes back through the stage.
 __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, const float *v, float *stage,
-                                            int lane, bool mirror, float4 (&oh)[8], float4 (&ol)[8]) {
+                                            int lane, bool mirror, bool diagblk, float4 (&oh)[8], float4 (&ol)[8]) {
     const float a = q.alpha, b = q.beta;
     if (q.epi == TC_EPI_SPLIT && q.Ct) {  // host guarantees beta == 0 here
         const int i = i0 + lane;
@@ -370,6 +401,10 @@ __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, con
             }
         }
     } else if (q.epi == TC_EPI_STORE) {
+        // a tile in a diagonal 128-block of a symmetric output (diagblk)
+        // stores its upper part only and mirrors that, so the result is
+        // exactly symmetric
+        const bool up = diagblk;
         const bool fullb = q.vecb && j + 3 < q.N;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -378,22 +413,39 @@ __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, con
             const float4 o = make_float4(a * acc[k].x, a * acc[k].y, a * acc[k].z, a * acc[k].w);
             if (q.C) {
                 float *dst = q.C + (long long)i * q.ldc + j;
-                if (full) {
+                if (full && (!up || j >= i)) {
                     st4(dst, o);
                 } else {
                     for (int t = 0; t < 4; ++t)
-                        if (j + t < q.N) dst[t] = comp(o, t);
+                        if (j + t < q.N && (!up || j + t >= i)) dst[t] = comp(o, t);
                 }
             }
             if (q.Cb) {
                 uint16_t *dst = q.Cb + (long long)i * q.ldcb + j;
-                if (fullb) {
+                if (fullb && (!up || j >= i)) {
                     const uint32_t lo2 = f32_to_bf16_bits(o.x) | ((uint32_t)f32_to_bf16_bits(o.y) << 16);
                     const uint32_t hi2 = f32_to_bf16_bits(o.z) | ((uint32_t)f32_to_bf16_bits(o.w) << 16);
                     *reinterpret_cast<uint2 *>(dst) = make_uint2(lo2, hi2);
                 } else {
                     for (int t = 0; t < 4; ++t)
-                        if (j + t < q.N) dst[t] = f32_to_bf16_bits(comp(o, t));
+                        if (j + t < q.N && (!up || j + t >= i)) dst[t] = f32_to_bf16_bits(comp(o, t));
+                }
+            }
+        }
+        if (mirror || up) {
+            // symmetric output: the transposed position C[j][i0 .. i0+31],
+            // straight from the TMEM layout (lane = row i0 + lane), so every
+            // store instruction covers one contiguous row segment
+            const int i = i0 + lane;
+            if (i < q.M) {
+#pragma unroll 8
+                for (int c = 0; c < 32; ++c) {
+                    const int jj = j0 + c;
+                    if (jj >= q.N) break;
+                    if (up && jj <= i) continue;
+                    const float o = a * v[c];
+                    if (q.C) q.C[(long long)jj * q.ldc + i] = o;
+                    if (q.Cb) q.Cb[(long long)jj * q.ldcb + i] = f32_to_bf16_bits(o);
                 }
             }
         }
@@ -408,7 +460,7 @@ __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, con
             const float4 h = tf32_hi4(o), l = sub4(o, h);
             oh[k] = h;  // the final pair, kept for the mirror below
             ol[k] = l;
-            if (i >= q.M) continue;
+            if (i >= q.M || !q.C) continue;  // (no C: only the transposed copy Ct)
             const long long off = (long long)i * q.ldc + j;
             if (full) {
                 st4(q.C + off, h);
@@ -476,7 +528,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         *last_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+    if (warp == 1) tmem_alloc(tmem_slot, Tr::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -551,54 +603,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            int it = 0;
-            for (int w = w_first; w < P.total_work && !*abort_flag; w += w_step, ++it) {
+            int cc = 0;  // accumulation chunks so far (accumulator cc & 1)
+            bool ok = true;
+            for (int w = w_first; w < P.total_work && ok && !*abort_flag; w += w_step) {
                 Work k = decode_work(P, w);
                 const TcProb &q = P.prob[k.p];
                 const bool diag = KIND == TC_KIND_BF16 && q.syrk && k.tm == k.tn;
-                const int b = it & 1;
-                const uint32_t use = (uint32_t)(it >> 1);
-                if (!mbar_wait(&acce[b], (use & 1) ^ 1)) {
-                    atomicOr(P.error, ERR_TIMEOUT_ACC);
-                    *abort_flag = 1;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + b * BN;
                 const uint32_t idesc = KIND == TC_KIND_BF16 ? idesc_bf16_f32(BM, BN, q.a_mn, q.b_mn)
                                                             : idesc_tf32_f32(BM, q.bn);
-                bool ok = true;
-                for (int kt = k.kt0; kt < k.kt1; ++kt) {
-                    if (!mbar_wait(&full[stage], phase)) {
-                        atomicOr(P.error, ERR_TIMEOUT_FULL);
+                const int nchunk = max(1, (int)ceil_div_dev(k.kt1 - k.kt0, Tr::CHUNK));
+                for (int ch = 0; ch < nchunk && ok; ++ch, ++cc) {
+                    const int b = cc & 1;
+                    const uint32_t use = (uint32_t)(cc >> 1);
+                    if (!mbar_wait(&acce[b], (use & 1) ^ 1)) {
+                        atomicOr(P.error, ERR_TIMEOUT_ACC);
                         *abort_flag = 1;
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t s0 = smem_u32(smem + stage * STAGE_BYTES);
-                    if (KIND == TC_KIND_BF16) {
-                        const uint32_t b_base = diag ? s0 : s0 + Tr::TILE;
-#pragma unroll
-                        for (int kk = 0; kk < KSLICES; ++kk)
-                            tc_mma_f16(d_tmem, operand_desc_bf16(s0, q.a_mn, kk), operand_desc_bf16(b_base, q.b_mn, kk),
-                                       idesc, (kt > k.kt0 || kk > 0) ? 1u : 0u);
-                    } else {
-                        const uint32_t ah = s0, al = s0 + TILE_BYTES, bh = s0 + 2 * TILE_BYTES,
-                                       bl = s0 + 3 * TILE_BYTES;
-#pragma unroll
-                        for (int kk = 0; kk < KSLICES; ++kk) {
-                            const uint64_t dah = operand_desc(ah, 0, kk), dbh = operand_desc(bh, 0, kk);
-                            tc_mma_tf32(d_tmem, dah, dbh, idesc, (kt > k.kt0 || kk > 0) ? 1u : 0u);
-                            tc_mma_tf32(d_tmem, dah, operand_desc(bl, 0, kk), idesc, 1u);
-                            tc_mma_tf32(d_tmem, operand_desc(al, 0, kk), dbh, idesc, 1u);
+                    const uint32_t d_tmem = tmem_base + b * BN;
+                    const int k_lo = k.kt0 + ch * Tr::CHUNK;
+                    const int k_hi = ch + 1 == nchunk ? k.kt1 : k_lo + Tr::CHUNK;
+                    for (int kt = k_lo; kt < k_hi; ++kt) {
+                        if (!mbar_wait(&full[stage], phase)) {
+                            atomicOr(P.error, ERR_TIMEOUT_FULL);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
                         }
+                        tc_fence_after();
+                        const uint32_t s0 = smem_u32(smem + stage * STAGE_BYTES);
+                        if (KIND == TC_KIND_BF16) {
+                            const uint32_t b_base = diag ? s0 : s0 + Tr::TILE;
+    #pragma unroll
+                            for (int kk = 0; kk < KSLICES; ++kk)
+                                tc_mma_f16(d_tmem, operand_desc_bf16(s0, q.a_mn, kk), operand_desc_bf16(b_base, q.b_mn, kk),
+                                           idesc, (kt > k_lo || kk > 0) ? 1u : 0u);
+                        } else {
+                            const uint32_t ah = s0, al = s0 + TILE_BYTES, bh = s0 + 2 * TILE_BYTES,
+                                           bl = s0 + 3 * TILE_BYTES;
+    #pragma unroll
+                            for (int kk = 0; kk < KSLICES; ++kk) {
+                                const uint64_t dah = operand_desc(ah, 0, kk), dbh = operand_desc(bh, 0, kk);
+                                tc_mma_tf32(d_tmem, dah, dbh, idesc, (kt > k_lo || kk > 0) ? 1u : 0u);
+                                tc_mma_tf32(d_tmem, dah, operand_desc(bl, 0, kk), idesc, 1u);
+                                tc_mma_tf32(d_tmem, operand_desc(al, 0, kk), dbh, idesc, 1u);
+                            }
+                        }
+                        tc_commit(&empty[stage]);
+                        if (++stage == Tr::STAGES) { stage = 0; phase ^= 1; }
                     }
-                    tc_commit(&empty[stage]);
-                    if (++stage == Tr::STAGES) { stage = 0; phase ^= 1; }
+                    if (!ok) break;
+                    tc_commit(&accf[b]);
                 }
-                if (!ok) break;
-                tc_commit(&accf[b]);
             }
         }
     } else {
@@ -607,17 +665,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         const int row = quarter * 32 + lane;
         const int etid = threadIdx.x - 64;  // 0..127
         float *stage = epi_stage + (warp - 2) * 32 * STAGE_LD;
-        int it = 0;
-        for (int w = w_first; w < P.total_work && !*abort_flag; w += w_step, ++it) {
+        const uint32_t t_quarter = tmem_base + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t t_sum = t_quarter + 2 * BN;  // running sum of a chunked item (tf32x3)
+        int cc = 0;
+        for (int w = w_first; w < P.total_work && !*abort_flag; w += w_step) {
             Work k = decode_work(P, w);
             const TcProb &q = P.prob[k.p];
-            const int b = it & 1;
-            const uint32_t use = (uint32_t)(it >> 1);
             const int i0 = k.tm * BM + quarter * 32;
             const int nch = q.bn / 32;
             const bool mirror = q.sym && k.tn >= (k.tm + 1) * (BM / q.bn);
+            const bool diagblk = q.sym && !mirror;
+            const int nchunk = max(1, (int)ceil_div_dev(k.kt1 - k.kt0, Tr::CHUNK));
+            // all chunks but the last: add into the running sum
+            bool ok = true;
+            for (int ch = 0; ch + 1 < nchunk; ++ch, ++cc) {
+                const int b = cc & 1;
+                if (!mbar_wait(&accf[b], (uint32_t)(cc >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < nch; ++c) {
+                    float v[32];
+                    tmem_ld_32x32b_x32(t_quarter + b * BN + c * 32, v);
+                    if (ch > 0) {
+                        float s2[32];
+                        tmem_ld_32x32b_x32(t_sum + c * 32, s2);
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) v[t] += s2[t];
+                    }
+                    tmem_st_32x32b_x32(t_sum + c * 32, v);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&acce[b]);
+            }
+            if (!ok) {
+                atomicOr(P.error, ERR_TIMEOUT_ACC);
+                *abort_flag = 1;
+                break;
+            }
+            const int b = cc & 1;
+            const uint32_t use = (uint32_t)(cc >> 1);
+            ++cc;
             float4 oh[8], ol[8];
-            // the first chunk's old values load while the MMAs run
+            // the first column chunk's old values load while the MMAs run
             if (q.ksplit == 1) load_old(q, i0, k.tn * q.bn, lane, oh, ol);
             if (!mbar_wait(&accf[b], use & 1)) {
                 atomicOr(P.error, ERR_TIMEOUT_ACC);
@@ -625,14 +718,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 break;
             }
             tc_fence_after();
-            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + b * BN;
+            const uint32_t t_row = t_quarter + b * BN;
+            // a split with an empty K range (ktri tiles near the end) issued
+            // no MMA: its accumulator holds nothing of this tile and counts as 0
+            const bool empty = k.kt0 >= k.kt1;
+            const bool summed = nchunk > 1;
             if (q.ksplit == 1) {
 #pragma unroll 1
                 for (int c = 0; c < nch; ++c) {
                     if (c > 0) load_old(q, i0, k.tn * q.bn + c * 32, lane, oh, ol);
                     float v[32];
                     tmem_ld_32x32b_x32(t_row + c * 32, v);
-                    chunk_store(q, i0, k.tn * q.bn + c * 32, v, stage, lane, mirror, oh, ol);
+                    if (summed) {
+                        float s2[32];
+                        tmem_ld_32x32b_x32(t_sum + c * 32, s2);
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) v[t] += s2[t];
+                    }
+                    if (empty) {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) v[t] = 0.f;
+                    }
+                    chunk_store(q, i0, k.tn * q.bn + c * 32, v, stage, lane, mirror, diagblk, oh, ol);
                 }
                 tc_fence_before();
                 mbar_arrive(&acce[b]);
@@ -642,6 +749,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 for (int c = 0; c < nch; ++c) {
                     float v[32];
                     tmem_ld_32x32b_x32(t_row + c * 32, v);
+                    if (summed) {
+                        float s2[32];
+                        tmem_ld_32x32b_x32(t_sum + c * 32, s2);
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) v[t] += s2[t];
+                    }
+                    if (empty) {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) v[t] = 0.f;
+                    }
 #pragma unroll
                     for (int f = 0; f < 8; ++f)
                         part[(c * 8 + f) * BM + row] = make_float4(v[4 * f], v[4 * f + 1], v[4 * f + 2], v[4 * f + 3]);
@@ -674,7 +791,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                                 v[4 * f] += t.x; v[4 * f + 1] += t.y; v[4 * f + 2] += t.z; v[4 * f + 3] += t.w;
                             }
                         }
-                        chunk_store(q, i0, k.tn * q.bn + c * 32, v, stage, lane, mirror, oh, ol);
+                        chunk_store(q, i0, k.tn * q.bn + c * 32, v, stage, lane, mirror, diagblk, oh, ol);
                     }
                     if (etid == 0) q.counters[k.tile] = 0;
                 }
@@ -685,7 +802,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tmem_dealloc(tmem_base, Tr::TMEM_COLS);
     }
 }
 
@@ -703,6 +820,11 @@ int bk_of(int kind) { return kind == TC_KIND_BF16 ? Traits<TC_KIND_BF16>::BK : T
 
 int tiles_of(const TcJob &j, int bn) {
     const int tm = (int)ceil_div(j.M, BM), tn = (int)ceil_div(j.N, bn);
+    if (j.lower) {  // row block t runs column blocks 0 .. (t+1)*128/bn - 1
+        int n = 0;
+        for (int t = 0; t < tm; ++t) n += std::min(tn, (t + 1) * BM / bn);
+        return n;
+    }
     if (!(j.syrk || j.sym)) return tm * tn;
     const int r = BM / bn;  // upper tiles: row block t runs column blocks t*r .. tn-1
     int n = 0;
@@ -741,7 +863,7 @@ Plan make_plan(const TcJob *jobs, int n, int kind, int sms) {
     for (int i = 0; i < n; ++i) {
         int ks = (int)std::ceil(p.k_tiles[i] / target);
         ks = std::max(1, std::min(ks, std::min(p.k_tiles[i], 256)));
-        if (jobs[i].no_split) ks = 1;
+        if (jobs[i].no_split || jobs[i].ktri) ks = 1;  // (a ktri split would leave late tiles empty)
         p.ksplit[i] = ks;
     }
     p.order.resize(n);
@@ -857,7 +979,11 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
     for (int i = 0; i < njobs; ++i) {
         const TcJob &j = jobs[i];
         if (j.Ct && j.beta != 0.f) return KFAC_ERR_INVALID;                       // transposed copy needs beta == 0
-        if (j.sym && (kind != TC_KIND_TF32X3 || j.M != j.N || j.epi != TC_EPI_SPLIT)) return KFAC_ERR_INVALID;
+        if (j.sym && (kind != TC_KIND_TF32X3 || j.M != j.N || (j.epi != TC_EPI_SPLIT && j.epi != TC_EPI_STORE)))
+            return KFAC_ERR_INVALID;
+        if (j.lower && (kind != TC_KIND_TF32X3 || j.sym || j.syrk || j.epi != TC_EPI_SPLIT)) return KFAC_ERR_INVALID;
+        if (j.ktri && kind != TC_KIND_TF32X3) return KFAC_ERR_INVALID;
+        if (!j.C && !j.Ct && !j.Cb) return KFAC_ERR_INVALID;
     }
     const int sms = cta_cap(max_ctas);
     Plan p = make_plan(jobs, njobs, kind, sms);
@@ -890,6 +1016,8 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
             q.tiles_n = (int)ceil_div(j.N, p.bn);
             q.syrk = j.syrk;
             q.sym = j.sym;
+            q.lower = j.lower;
+            q.ktri = j.ktri;
             q.ksplit = p.ksplit[ji];
             q.work_begin = work;
             q.epi = j.epi;
