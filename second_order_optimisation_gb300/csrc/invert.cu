@@ -209,248 +209,190 @@ struct DiagParams {
 };
 
 // Cholesky factor and its inverse of one SPD 128 x 128 block S = L L^T, by
-// one CTA of 256 threads: W = L^-1, written over the block and, transposed,
+// one CTA of 512 threads: W = L^-1, written over the block and, transposed,
 // into the same block of the transposed pair.
 //
-// The sweep works on one array M (lower triangle) that holds the Schur
-// complement still to be factored in its columns past the current pivots and
-// the rows of W in progress in the columns before.  A single pivot c, with
-// w = 1 / sqrt(M_cc) and p_i = w M_ic (= L_ic), does
+// The sweep works on one array M (the lower triangle, in shared memory) that
+// holds the Schur complement still to be factored in its columns past the
+// current pivots and the rows of W in progress in the columns before.  A
+// single pivot c, with w = 1 / sqrt(M_cc) and p_i = w M_ic (= L_ic), does
 //   i > c, j < c:      M_ij -= p_i (w M_cj)    (rows of W in progress)
 //   i > c, j = c:      M_ic  = -p_i w
 //   i > c, c < j <= i: M_ij -= p_i p_j         (Schur complement)
 //   i = c, j < c:      M_cj *= w;   M_cc = w   (row c of W final)
-// and four pivots K = {c .. c+3} at a time are the same four steps fused:
-// with W_K = the 4 x 4 result of those rules on the pivot block alone,
-//   p_i = W_K M[i][K]   (i past K),   y_j = W_K M[K][j]   (j before K),
-//   i past K:  M_ij -= p_i . y_j (j < c),  M_iK = -p_i^T W_K,  M_ij -= p_i . p_j (K < j <= i)
-//   i in K:    M[K][j] = y_j (j < c),  M[K][K] = W_K.
-// Thread t keeps the elements of rows r0 + 16a and columns c0 + 16b
-// (r0 = t / 16, c0 = t % 16, a, b = 0..7) in registers; each step the pivot
-// column block and row block are published through shared memory, threads
-// 0..127 form the 4-vectors p_i / y_j once, and all threads apply the
-// rank-4 update (two barriers per step).  1 / sqrt is the correctly rounded
-// square root and division.  A pivot outside [FLT_MIN, inf) is recorded and
+// The kernel runs these rules 8 pivots K = {c .. c+7} at a time:
+//   1. each of threads 0..127 applies them to the 8 x 8 pivot block alone
+//      (straight-line code on registers), giving W_K, and forms row j = tid
+//      of Z [128 x 8]:
+//        Z_j = W_K M[K][j]      (j before K: the final rows K of W, as columns)
+//        Z_j = W_K^T e_(j-c)    (j in K)
+//        Z_j = W_K M[j][K]      (j past K: the panel L_jK);
+//   2. rows K:         M[K][j] = Z_j (j before K),  M[K][K] = W_K;
+//      rows i past K:  M_ij = (j in K ? 0 : M_ij) - Z_i . Z_j  (j <= i),
+//      one row and 8 columns per item, consecutive threads on consecutive rows
+//      (the Z_i reads are contiguous, the Z_j reads broadcasts).
+// 1 / sqrt is the hardware approximation refined by one Newton-Raphson step,
+// y <- y (3 - x y^2) / 2.  A pivot outside [FLT_MIN, inf) is recorded and
 // eliminated with w = 0 (the result is then undefined but finite).
-constexpr int DIAG_LD = NB + 4;  // staging row pitch (floats; rows stay 16-byte aligned)
-constexpr size_t DIAG_SMEM = (size_t)NB * DIAG_LD * sizeof(float)  // block staging
-                             + 2 * NB * sizeof(float4)              // pivot column blocks (double-buffered)
-                             + 2 * 4 * NB * sizeof(float)           // pivot row blocks
-                             + NB * sizeof(float4)                  // the 4-vectors p_i / y_j
-                             + 16 * sizeof(float) + 16;             // W_K, first bad pivot
+constexpr int DLD = NB + 4;  // M row pitch (floats; rows stay 16-byte aligned)
+constexpr int DIAG_THREADS = 512;
+constexpr size_t DIAG_SMEM = ((size_t)NB * DLD + (size_t)NB * 8 + 64 + 4) * sizeof(float);
 
-__device__ __forceinline__ float f4c(const float4 &v, int q) { return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w; }
-__device__ __forceinline__ void f4set(float4 &v, int q, float x) {
-    if (q == 0) v.x = x; else if (q == 1) v.y = x; else if (q == 2) v.z = x; else v.w = x;
+__device__ __forceinline__ float rsqrt_nr(float x) {
+    const float y = rsqrtf(x);
+    return y * fmaf(-0.5f * x * y, y, 1.5f);
 }
 
-// The single-pivot rules on a 4 x 4 lower block (element [r][q], r >= q):
-// returns W_K in place; bad = index (0..3) of the first pivot outside
-// [FLT_MIN, inf), or -1.
-__device__ __forceinline__ int pivot4(float (&S)[4][4]) {
+// The single-pivot rules on an 8 x 8 lower block alone, in registers (every
+// loop has constant bounds so that the block stays in registers): W_K in
+// place; returns the first pivot (0..7) outside [FLT_MIN, inf), or -1.
+__device__ __forceinline__ int pivot8(float (&w)[8][8]) {
     int bad = -1;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float piv = S[q][q];
+    for (int q = 0; q < 8; ++q) {
+        const float piv = w[q][q];
         const bool ok = piv >= FLT_MIN && piv < INFINITY;
-        const float w = ok ? 1.0f / sqrtf(piv) : 0.f;
-        if (!ok && bad < 0) bad = q;
-        float p[4];
+        const float wq = ok ? rsqrt_nr(piv) : 0.f;
+        bad = (!ok && bad < 0) ? q : bad;
+        float p[8], rowq[8];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) p[r] = r > q ? S[r][q] * w : 0.f;
+        for (int r = 0; r < 8; ++r) p[r] = r > q ? w[r][q] * wq : 0.f;
 #pragma unroll
-        for (int r = q + 1; r < 4; ++r) {
+        for (int j = 0; j < 8; ++j) rowq[j] = wq * w[q][j];
 #pragma unroll
-            for (int j = 0; j < q; ++j) S[r][j] = fmaf(-p[r], w * S[q][j], S[r][j]);
-            S[r][q] = -p[r] * w;
+        for (int r = 0; r < 8; ++r)
 #pragma unroll
-            for (int j = q + 1; j <= r; ++j) S[r][j] = fmaf(-p[r], p[j], S[r][j]);
-        }
+            for (int j = 0; j < 8; ++j) {
+                if (r <= q || j > r) continue;
+                if (j < q) w[r][j] = fmaf(-p[r], rowq[j], w[r][j]);
+                else if (j == q) w[r][j] = -p[r] * wq;
+                else w[r][j] = fmaf(-p[r], p[j], w[r][j]);
+            }
 #pragma unroll
-        for (int j = 0; j < q; ++j) S[q][j] *= w;
-        S[q][q] = w;
+        for (int j = 0; j < 8; ++j)
+            if (j < q) w[q][j] *= wq;
+        w[q][q] = wq;
     }
     return bad;
 }
 
-__global__ void __launch_bounds__(256, 1) diag_kernel(const __grid_constant__ DiagParams P) {
+__global__ void __launch_bounds__(DIAG_THREADS, 1) diag_kernel(const __grid_constant__ DiagParams P) {
     extern __shared__ float4 diag_smem4[];
-    float *st = reinterpret_cast<float *>(diag_smem4);
-    float4 *colb = reinterpret_cast<float4 *>(st + NB * DIAG_LD);  // [2][NB]: M[i][c .. c+3]
-    float *rowb = reinterpret_cast<float *>(colb + 2 * NB);        // [2][4][NB]: M[c + q][j]
-    float4 *pv = reinterpret_cast<float4 *>(rowb + 2 * 4 * NB);    // [NB]
-    float *wk = reinterpret_cast<float *>(pv + NB);                 // [4][4]
-    int *bad_s = reinterpret_cast<int *>(wk + 16);
+    float *M = reinterpret_cast<float *>(diag_smem4);
+    float *Z = M + NB * DLD;       // [NB][8]
+    float *wk = Z + NB * 8;          // [8][8]
+    int *bad_s = reinterpret_cast<int *>(wk + 64);
     const DiagJob &J = P.j[blockIdx.x];
-    const int tid = threadIdx.x, r0 = tid >> 4, c0 = tid & 15;
-    const bool dg = c0 <= r0;  // element (a, a) is on or below the diagonal
+    const int tid = threadIdx.x, lane = tid & 31;
     if (tid == 0) *bad_s = -1;
     pdl_wait();
     pdl_trigger();
-    // block -> shared memory (16-byte pieces, hi + lo) -> registers
-    for (int e = tid; e < NB * NB / 4; e += 256) {
+    for (int e = tid; e < NB * NB / 4; e += DIAG_THREADS) {
         const int i = e >> 5, j = (e & 31) * 4;
         const long long off = (long long)i * J.ld + j;
         const float4 h = *reinterpret_cast<const float4 *>(J.Xh + off);
         const float4 l = *reinterpret_cast<const float4 *>(J.Xl + off);
-        *reinterpret_cast<float4 *>(st + i * DIAG_LD + j) = make_float4(h.x + l.x, h.y + l.y, h.z + l.z, h.w + l.w);
-    }
-    __syncthreads();
-    float m[8][8];
-#pragma unroll
-    for (int a = 0; a < 8; ++a)
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const int i = r0 + 16 * a, j = c0 + 16 * b;
-            m[a][b] = j <= i ? st[i * DIAG_LD + j] : 0.f;
-        }
-    // pivot column block and row block of the first step
-    if (c0 < 4) {
-#pragma unroll
-        for (int a = 0; a < 8; ++a) reinterpret_cast<float *>(&colb[r0 + 16 * a])[c0] = m[a][0];
-    }
-    if (r0 < 4) {
-#pragma unroll
-        for (int b = 0; b < 8; ++b) rowb[r0 * NB + c0 + 16 * b] = m[0][b];
+        *reinterpret_cast<float4 *>(M + i * DLD + j) = make_float4(h.x + l.x, h.y + l.y, h.z + l.z, h.w + l.w);
     }
     __syncthreads();
 #pragma unroll 1
-    for (int s = 0; s < NB / 4; ++s) {
-        const int c = 4 * s, cur = s & 1, nxt = cur ^ 1;
-        const float4 *cb = colb + cur * NB;
-        const float *rb = rowb + cur * 4 * NB;
+    for (int s = 0; s < NB / 8; ++s) {
+        const int c = 8 * s, E = c + 8;
+        // 1. + 2. Z rows, one per thread t < 128; each such thread first turns
+        //    the 8 x 8 pivot block into W_K itself (the single-pivot rules on
+        //    the block alone, in registers): j < c: W_K M[K][j];  j in K:
+        //    W_K^T e;  j past K: W_K M[j][K]
         if (tid < NB) {
-            float W[4][4];
-            // W_K from the pivot block (every phase-A thread; thread 0 publishes it)
+            float w[8][8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 v = cb[c + q];
+            for (int r = 0; r < 8; ++r)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) W[q][r] = r <= q ? f4c(v, r) : 0.f;
-            }
-            const int bad = pivot4(W);
+                for (int q = 0; q < 8; ++q) w[r][q] = q <= r ? M[(c + r) * DLD + c + q] : 0.f;
+            const int bad = pivot8(w);
             if (tid == 0) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
+                for (int r = 0; r < 8; ++r)
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) wk[q * 4 + r] = W[q][r];
+                    for (int q = 0; q < 8; ++q) wk[r * 8 + q] = w[r][q];
                 if (bad >= 0 && *bad_s < 0) *bad_s = c + bad;
             }
-            // p_t = W_K M[t][K] (t past K), y_t = W_K M[K][t] (t before K)
-            const int t = tid;
-            float x[4] = {0.f, 0.f, 0.f, 0.f};
-            if (t >= c + 4) {
-                const float4 v = cb[t];
-                x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-            } else if (t < c) {
+            // Z_j = W_K x with x = M[K][j] (j before K), e_(j-c) (j in K), M[j][K] (j past K)
+            const int j = tid;
+            float x[8];
+            if (j < c) {
 #pragma unroll
-                for (int r = 0; r < 4; ++r) x[r] = rb[r * NB + t];
+                for (int r = 0; r < 8; ++r) x[r] = M[(c + r) * DLD + j];
+            } else if (j < E) {
+#pragma unroll
+                for (int r = 0; r < 8; ++r) x[r] = j - c == r ? 1.f : 0.f;
+            } else {
+                const float4 a = *reinterpret_cast<const float4 *>(M + j * DLD + c);
+                const float4 b = *reinterpret_cast<const float4 *>(M + j * DLD + c + 4);
+                x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
             }
-            float4 o;
-            o.x = W[0][0] * x[0];
-            o.y = fmaf(W[1][0], x[0], W[1][1] * x[1]);
-            o.z = fmaf(W[2][0], x[0], fmaf(W[2][1], x[1], W[2][2] * x[2]));
-            o.w = fmaf(W[3][0], x[0], fmaf(W[3][1], x[1], fmaf(W[3][2], x[2], W[3][3] * x[3])));
-            pv[t] = o;
+            float z[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float acc = 0.f;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) acc = r <= q ? fmaf(w[q][r], x[r], acc) : acc;
+                z[q] = acc;
+            }
+            *reinterpret_cast<float4 *>(Z + j * 8) = make_float4(z[0], z[1], z[2], z[3]);
+            *reinterpret_cast<float4 *>(Z + j * 8 + 4) = make_float4(z[4], z[5], z[6], z[7]);
         }
         __syncthreads();
-        // rows past K: M_ij -= p_i . z_j with z_j = y_j (j < c), p_j (j past K);
-        // the columns K take -p_i^T W_K
-        float4 z[8];
+        // 3. rows K: M[K][j] = Z_j (j < c), W_K on the pivot block
+        for (int e = tid; e < 8 * E; e += DIAG_THREADS) {
+            const int q = e / E, j = e - q * E;
+            if (j < c) M[(c + q) * DLD + j] = Z[j * 8 + q];
+            else if (j - c <= q) M[(c + q) * DLD + j] = wk[q * 8 + (j - c)];
+        }
+        //    rows past K, one row i and 8 columns 8J .. 8J+7 (8J <= i) per
+        //    item, consecutive threads on consecutive rows:
+        //    M_ij = (j in K ? 0 : M_ij) - Z_i . Z_j  for j <= i
+        for (int J = tid >> 7; J < 16; J += DIAG_THREADS / NB) {
+            const int i = tid & (NB - 1);
+            if (i < E || 8 * J > i) continue;
+            float acc[8];
+            {
+                const float4 a = *reinterpret_cast<const float4 *>(M + i * DLD + 8 * J);
+                const float4 b = *reinterpret_cast<const float4 *>(M + i * DLD + 8 * J + 4);
+                acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w; acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+            }
+            if (8 * J == c) {  // the columns K take -Z_i . W_K
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const int j = c0 + 16 * b;
-            if (j >= c && j < c + 4) {
-                const int r = j - c;
-                z[b] = make_float4(wk[r], wk[4 + r], wk[8 + r], wk[12 + r]);
+                for (int v = 0; v < 8; ++v) acc[v] = 0.f;
+            }
+            const float4 za = *reinterpret_cast<const float4 *>(Z + i * 8);
+            const float4 zb = *reinterpret_cast<const float4 *>(Z + i * 8 + 4);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const float4 a = *reinterpret_cast<const float4 *>(Z + (8 * J + v) * 8);
+                const float4 b = *reinterpret_cast<const float4 *>(Z + (8 * J + v) * 8 + 4);
+                float x = acc[v];
+                x = fmaf(-za.x, a.x, x); x = fmaf(-za.y, a.y, x); x = fmaf(-za.z, a.z, x); x = fmaf(-za.w, a.w, x);
+                x = fmaf(-zb.x, b.x, x); x = fmaf(-zb.y, b.y, x); x = fmaf(-zb.z, b.z, x); acc[v] = fmaf(-zb.w, b.w, x);
+            }
+            if (8 * J + 7 <= i) {
+                *reinterpret_cast<float4 *>(M + i * DLD + 8 * J) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                *reinterpret_cast<float4 *>(M + i * DLD + 8 * J + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
             } else {
-                z[b] = pv[j];
-            }
-        }
-        const bool zk = (c0 & ~3) == (c & 15);  // this thread's columns K (at b = c / 16)
-        const int bk = c >> 4;
 #pragma unroll
-        for (int a = 0; a < 8; ++a) {
-            if (r0 + 16 * a >= c + 4) {
-                const float4 pa = pv[r0 + 16 * a];
-#pragma unroll
-                for (int b = 0; b <= a; ++b) {
-                    if (b == a && !dg) continue;
-                    const float base = (zk && b == bk) ? 0.f : m[a][b];
-                    float v = fmaf(-pa.x, z[b].x, base);
-                    v = fmaf(-pa.y, z[b].y, v);
-                    v = fmaf(-pa.z, z[b].z, v);
-                    m[a][b] = fmaf(-pa.w, z[b].w, v);
-                }
-            }
-        }
-        // rows K: M[K][j] = y_j (j < c), M[K][K] = W_K
-        const int qr = r0 - (c & 15);
-        if (qr >= 0 && qr < 4) {
-            switch (bk) {
-#define KFAC_DIAG_ROWK(A)                                                             \
-    case A:                                                                           \
-        _Pragma("unroll") for (int b = 0; b <= A; ++b) {                              \
-            const int j = c0 + 16 * b;                                                \
-            if (j < c) m[A][b] = f4c(z[b], qr);                                       \
-            else if (j < c + 4 && j - c <= qr) m[A][b] = wk[qr * 4 + j - c];          \
-        }                                                                             \
-        break;
-                KFAC_DIAG_ROWK(0) KFAC_DIAG_ROWK(1) KFAC_DIAG_ROWK(2) KFAC_DIAG_ROWK(3)
-                KFAC_DIAG_ROWK(4) KFAC_DIAG_ROWK(5) KFAC_DIAG_ROWK(6) KFAC_DIAG_ROWK(7)
-#undef KFAC_DIAG_ROWK
-            }
-        }
-        // publish the next step's pivot column block and row block
-        const int n = c + 4;
-        if (n < NB) {
-            const int nl = n & 15, nh = n >> 4;
-            const int qc = c0 - nl, qn = r0 - nl;
-            if (qc >= 0 && qc < 4) {
-                float4 *dst = colb + nxt * NB;
-                switch (nh) {
-#define KFAC_DIAG_PUBC(B)                                                                                   \
-    case B:                                                                                                 \
-        _Pragma("unroll") for (int a = 0; a < 8; ++a) reinterpret_cast<float *>(&dst[r0 + 16 * a])[qc] = m[a][B]; \
-        break;
-                    KFAC_DIAG_PUBC(0) KFAC_DIAG_PUBC(1) KFAC_DIAG_PUBC(2) KFAC_DIAG_PUBC(3)
-                    KFAC_DIAG_PUBC(4) KFAC_DIAG_PUBC(5) KFAC_DIAG_PUBC(6) KFAC_DIAG_PUBC(7)
-#undef KFAC_DIAG_PUBC
-                }
-            }
-            if (qn >= 0 && qn < 4) {
-                float *dst = rowb + nxt * 4 * NB + qn * NB;
-                switch (nh) {
-#define KFAC_DIAG_PUBR(A)                                                             \
-    case A:                                                                           \
-        _Pragma("unroll") for (int b = 0; b < 8; ++b) dst[c0 + 16 * b] = m[A][b];     \
-        break;
-                    KFAC_DIAG_PUBR(0) KFAC_DIAG_PUBR(1) KFAC_DIAG_PUBR(2) KFAC_DIAG_PUBR(3)
-                    KFAC_DIAG_PUBR(4) KFAC_DIAG_PUBR(5) KFAC_DIAG_PUBR(6) KFAC_DIAG_PUBR(7)
-#undef KFAC_DIAG_PUBR
-                }
+                for (int v = 0; v < 8; ++v)
+                    if (8 * J + v <= i) M[i * DLD + 8 * J + v] = acc[v];
             }
         }
         __syncthreads();
     }
-    // W (lower, zeros above) into X and W^T (upper, zeros below) into the
-    // transposed pair, staged through shared memory so that every global
-    // store is a 16-byte piece of a row
-#pragma unroll
-    for (int a = 0; a < 8; ++a)
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const int i = r0 + 16 * a, j = c0 + 16 * b;
-            st[i * DIAG_LD + j] = j <= i ? m[a][b] : 0.f;
-        }
-    __syncthreads();
-    for (int e = tid; e < NB * NB / 4; e += 256) {
+    // W (lower, zeros above) into X and W^T (upper, zeros below) into the transposed pair
+    for (int e = tid; e < NB * NB / 4; e += DIAG_THREADS) {
         const int i = e >> 5, j = (e & 31) * 4;
         float w4[4], t4[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            w4[u] = st[i * DIAG_LD + j + u];
-            t4[u] = st[(j + u) * DIAG_LD + i];
+            w4[u] = j + u <= i ? M[i * DLD + j + u] : 0.f;
+            t4[u] = i <= j + u ? M[(j + u) * DLD + i] : 0.f;
         }
         float hw[4], ht[4];
 #pragma unroll
@@ -467,6 +409,7 @@ __global__ void __launch_bounds__(256, 1) diag_kernel(const __grid_constant__ Di
             make_float4(t4[0] - ht[0], t4[1] - ht[1], t4[2] - ht[2], t4[3] - ht[3]);
     }
     if (tid == 0 && *bad_s >= 0 && J.info) atomicCAS(J.info, 0, J.o + *bad_s + 1);
+    __syncthreads();
 }
 
 // ------------------------------------------------------------- scheduler
@@ -759,7 +702,7 @@ kfac_status diag_launch(const std::vector<DiagJob> &jobs, cudaStream_t st) {
         int n = 0;
         for (; pos < jobs.size() && n < MAT_MAX; ++pos) P->j[n++] = jobs[pos];
         P->n = n;
-        KFAC_LAUNCH(KK_LEAF, st, diag_kernel, n, 256, DIAG_SMEM, *P);
+        KFAC_LAUNCH(KK_LEAF, st, diag_kernel, n, DIAG_THREADS, DIAG_SMEM, *P);
     }
     return KFAC_OK;
 }

@@ -8,7 +8,7 @@ its Cholesky factor X = L L^T: W = L^-1, then X^-1 = W^T W.  This file
 restates, operation by operation and with the same buffer offsets:
 
   * the diag kernel's sweep, which turns the lower triangle of a 128 x 128
-    SPD block into W = L^-1 in place, four pivots per step (the single-pivot
+    SPD block into W = L^-1 in place, 8 pivots per step (the single-pivot
     rules M_ij -= p_i y_j, M_ic = -p_i w, M_cj *= w, M_cc = w, with
     w = 1/sqrt(M_cc) and p_i = w M_ic, fused over the pivot block);
   * the chain of one matrix: left-looking Cholesky block columns (update,
@@ -28,13 +28,15 @@ import pytest
 NB = 128
 
 
-def pivot4(S):
-    """The single-pivot rules applied to a 4 x 4 lower block alone: W_K."""
+def pivot_block(S):
+    """The single-pivot rules applied to a square lower block alone (what each
+    of the diag kernel's first 128 threads does with its 8 x 8 pivot block): W_K."""
     S = np.tril(np.array(S, dtype=np.float64))
-    for q in range(4):
+    n = S.shape[0]
+    for q in range(n):
         w = 1.0 / np.sqrt(S[q, q])
-        p = np.where(np.arange(4) > q, S[:, q] * w, 0.0)
-        for r in range(q + 1, 4):
+        p = np.where(np.arange(n) > q, S[:, q] * w, 0.0)
+        for r in range(q + 1, n):
             S[r, :q] -= p[r] * w * S[q, :q]
             S[r, q] = -p[r] * w
             S[r, q + 1:r + 1] -= p[r] * p[q + 1:r + 1]
@@ -43,28 +45,28 @@ def pivot4(S):
     return S
 
 
-def diag_sweep(S):
-    """The diag kernel's sweep on the lower triangle of S, four pivots
-    K = {c .. c+3} per step: W_K from the pivot block, p_i = W_K M[i][K]
-    (i past K), y_j = W_K M[K][j] (j before K); rows past K take
-    M_ij -= p_i . y_j (j < c), M_iK = -p_i^T W_K, M_ij -= p_i . p_j
-    (K < j <= i); rows K take y_j (j < c) and W_K."""
+def diag_sweep(S, panel=8):
+    """The diag kernel's sweep on the lower triangle of S, `panel` pivots
+    K = {c .. c+panel-1} per step: W_K from the pivot block alone, then
+    Z_j = W_K M[K][j] (j before K), W_K^T e_(j-c) (j in K), W_K M[j][K]
+    (j past K); rows past K take M_ij = (j in K ? 0 : M_ij) - Z_i . Z_j
+    (j <= i), rows K take Z_j (j before K) and W_K."""
     n = S.shape[0]
     M = np.tril(S).astype(np.float64)
-    for c in range(0, n, 4):
-        K = slice(c, c + 4)
-        Wk = pivot4(M[K, K])
-        P = M[c + 4:, K] @ Wk.T            # p_i as rows
-        Y = (Wk @ M[K, :c]).T              # y_j as rows
-        Z = np.vstack([Y, Wk.T, P])        # z_j for every column j <= last row
+    for c in range(0, n, panel):
+        E = c + panel
+        Wk = pivot_block(M[c:E, c:E])
+        Zb = (Wk @ M[c:E, :c]).T          # j before K
+        Zk = Wk.T                          # j in K: row j-c of W_K^T
+        Zp = M[E:, c:E] @ Wk.T             # j past K
+        Z = np.vstack([Zb, Zk, Zp])
         new = M.copy()
-        R = slice(c + 4, n)
-        low = np.tril(np.ones((n, n), dtype=bool))[R]
-        upd = M[R] - P @ Z.T
-        upd[:, K] = -(P @ Wk)
-        new[R] = np.where(low, upd, M[R])
-        new[K, :c] = Y.T
-        new[K, K] = Wk
+        low = np.tril(np.ones((n, n), dtype=bool))[E:]
+        base = M[E:].copy()
+        base[:, c:E] = 0.0
+        new[E:] = np.where(low, base - Z[E:] @ Z.T, M[E:])
+        new[c:E, :c] = Zb.T
+        new[c:E, c:E] = Wk
         M = new
     return M
 
@@ -153,19 +155,21 @@ def invert_like_the_library(F, damp, bn):
     return out[:d, :d]
 
 
-def test_pivot_block_rules_are_the_inverse_cholesky_factor():
+@pytest.mark.parametrize("n", [4, 8, 32])
+def test_pivot_block_rules_are_the_inverse_cholesky_factor(n):
     rng = np.random.default_rng(4)
-    Z = rng.standard_normal((4, 4))
-    S = Z @ Z.T + 0.1 * np.eye(4)
-    np.testing.assert_allclose(pivot4(S), np.linalg.inv(np.linalg.cholesky(S)), rtol=0, atol=1e-12)
+    Z = rng.standard_normal((n, n))
+    S = Z @ Z.T / n + 0.1 * np.eye(n)
+    np.testing.assert_allclose(pivot_block(S), np.linalg.inv(np.linalg.cholesky(S)), rtol=0, atol=1e-10)
 
 
 def test_diag_sweep_is_the_inverse_cholesky_factor():
     rng = np.random.default_rng(3)
     Z = rng.standard_normal((NB, NB))
     S = Z @ Z.T / NB + 0.01 * np.eye(NB)
-    W = diag_sweep(S)
-    np.testing.assert_allclose(np.tril(W), np.linalg.inv(np.linalg.cholesky(S)), rtol=0, atol=1e-11)
+    for panel in (4, 8, 32):
+        W = diag_sweep(S, panel)
+        np.testing.assert_allclose(np.tril(W), np.linalg.inv(np.linalg.cholesky(S)), rtol=0, atol=1e-11)
     assert np.all(np.triu(W, 1) == 0.0)
 
 
