@@ -57,12 +57,15 @@ def _bind(path):
         lib.orc_damped_inverse.argtypes = [_dp, _L, ctypes.c_double, _dp]
         lib.orc_precondition.argtypes = [_dp, _L, _dp, _L, _dp, _dp]
         lib.orc_precondition_rows.argtypes = [_dp, _L, _dp, _L, _dp, _lp, _L, _dp]
+        lib.orc_weight_update.argtypes = [_dp, _dp, _L, _L, ctypes.c_double]
+        lib.orc_is_refresh_step.argtypes = [_L, _L, _L]
         lib.orc_bn_diag_fisher.argtypes = [_dp, _L, _L, ctypes.c_double, ctypes.c_double,
                                            _dp, _dp, _dp]
         for f in ("orc_im2col", "orc_gram", "orc_factor_ema", "orc_gram_entries",
                   "orc_weight_grad", "orc_pi_damping", "orc_cholesky_upper",
                   "orc_trtri_upper", "orc_lauum_upper", "orc_damped_inverse",
-                  "orc_precondition", "orc_precondition_rows", "orc_bn_diag_fisher"):
+                  "orc_precondition", "orc_precondition_rows", "orc_bn_diag_fisher",
+                  "orc_weight_update", "orc_is_refresh_step"):
             getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -227,6 +230,40 @@ def precondition_rows(Ginv, grad, Ainv, rows):
     assert _load().orc_precondition_rows(_p(Ginv), dG, _p(grad), dA, _p(Ainv), rows.ctypes.data_as(_lp),
                                          len(rows), _p(out)) == 0
     return out
+
+
+def weight_update(w, P, eta):
+    """w - eta * P (Eq. 8), returned as a new array."""
+    w = _d(w).copy()
+    P = _d(P)
+    assert w.shape == P.shape
+    assert _load().orc_weight_update(_p(w), _p(P), w.shape[0], w.shape[1], float(eta)) == 0
+    return w
+
+
+def is_refresh_step(t, warmup, every):
+    """True when step t of the stale-factor schedule refreshes the factors and inverses."""
+    return bool(_load().orc_is_refresh_step(int(t), int(warmup), int(every)))
+
+
+def kfac_schedule(A0, G0, steps, xi, gamma, warmup, every):
+    """The stale-factor schedule over a sequence of steps of one layer.
+    steps: list of (P, Gam, grad) per step.  Returns the preconditioned
+    gradient of every step: refresh steps update both factors (running
+    average from A0, G0), damp and invert them; other steps reuse the last
+    inverses."""
+    A, G = _d(A0).copy(), _d(G0).copy()
+    Ainv = Ginv = None
+    outs = []
+    for t, (P, Gam, grad) in enumerate(steps):
+        if is_refresh_step(t, warmup, every) or Ainv is None:
+            A = factor_ema(A, P, xi)
+            G = factor_ema(G, Gam, xi)
+            da, dg = pi_damping(A, G, gamma)
+            Ainv = damped_inverse(A, da)
+            Ginv = damped_inverse(G, dg)
+        outs.append(precondition(Ginv, grad, Ainv))
+    return outs
 
 
 def bn_diag_fisher(x, gamma, xi=0.0, F=None):

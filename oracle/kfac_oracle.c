@@ -388,6 +388,35 @@ int orc_precondition_rows(const double *Ginv, long dG, const double *grad, long 
     return 0;
 }
 
+/*
+ * Weight update with the preconditioned gradient (Osawa et al. section 3.2,
+ * Eq. 8: w <- w - eta * G, G the natural gradient of Eq. 7):
+ *   w[o][j] <- w[o][j] - eta * P[o][j].
+ * Pinned: eta = 0 leaves w unchanged; w = 0, eta = 1 gives -P; linearity in eta.
+ */
+int orc_weight_update(double *w, const double *P, long dG, long dA, double eta)
+{
+    for (long o = 0; o < dG; ++o)
+        for (long j = 0; j < dA; ++j) w[o * dA + j] -= eta * P[o * dA + j];
+    return 0;
+}
+
+/*
+ * Steps of the stale-factor schedule (Osawa et al. section 1: after a few
+ * hundred iterations the Fisher matrix need not be refreshed every step):
+ * step t (0-based) refreshes the factors and their inverses when
+ * t < warmup, or when (t - warmup) is a multiple of every; other steps
+ * precondition with the inverses of the last refresh.
+ * Pinned: every = 1 refreshes every step; warmup >= steps refreshes every
+ * step; the count of refreshes over T steps has a closed form.
+ */
+int orc_is_refresh_step(long t, long warmup, long every)
+{
+    if (every < 1) return 1;
+    if (t < warmup) return 1;
+    return (t - warmup) % every == 0;
+}
+
 /* -------------------------------------------------------------- BatchNorm */
 
 /*

@@ -41,6 +41,8 @@ struct TcJob {
                    // written in full (no mirror)
     int ktri;      // TF32X3: the K range of output tile (tm, tn) starts at the tile's first
                    // column (B upper triangular in its K index: B[j][t] = 0 for t < j)
+    int ktril;     // TF32X3: the K range of output tile (tm, tn) ends after the tile's last
+                   // row (A lower triangular in its K index: A[i][t] = 0 for t > i)
     int no_split;
     int epi;
     float alpha, beta;

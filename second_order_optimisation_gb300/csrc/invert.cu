@@ -38,6 +38,11 @@ namespace kfac {
 namespace {
 
 constexpr int NB = 128;    // block width of the sweep
+// Lookahead: split each Cholesky update into the last panel's share (kept on
+// the chain) and the rest (on a side stream, overlapping the diag leaf and the
+// panel).  Measured on the ResNet-50 step it gained nothing (the side
+// launches' persistent CTAs hold SMs the chain needs next), so it is off.
+constexpr bool LOOKAHEAD = false;
 constexpr int MAT_MAX = 224;
 // tensor maps of one matrix: X, Wt, LT pairs, each as hi / lo with 128-row
 // and with 32-row boxes
@@ -420,6 +425,9 @@ struct Op {
     int leaf;
     DiagJob dj;
     std::vector<TcJob> g;
+    std::vector<TcJob> side;  // engine problems that may start once this op is done (lookahead,
+                              // launched on the group's side stream)
+    int needs_side = -1;      // chain index of the op whose side problems must be done first
 };
 
 // Working buffers of one matrix (fp32 (hi, lo) pairs, [dp][dp] each):
@@ -464,7 +472,11 @@ int tri_nodes(int o, int n, std::vector<std::vector<std::pair<int, int>>> &by_he
 //       X[k:, k] -= L[k:, :k] L[k, :k]^T                 (engine; k > 0)
 //       W_kk = L_kk^-1 from X[k, k]                      (diag leaf)
 //       L[k+1:, k] = X[k+1:, k] W_kk^T                   (engine; the panel)
-//     every Schur-complement column comes from Cholesky panels (no growth);
+//     every Schur-complement column comes from Cholesky panels (no growth).
+//     The update of column k by panels 0 .. k-2 needs nothing later than
+//     panel k-2: it runs as a side problem once that panel is done (on the
+//     group's side stream, while the diag leaf and panel of k-1 run), and
+//     only the update by panel k-1 (K = 128) stays on the chain;
 //  2. W = L^-1 by recursive 2 x 2 blocking, bottom up by height (the two
 //     halves of a node are independent):
 //       T = L21 W11,   W21 = -W22 T   (W21 over X's lower part, W21^T into Wt);
@@ -476,12 +488,21 @@ int tri_nodes(int o, int n, std::vector<std::vector<std::pair<int, int>>> &by_he
 void gen_chain(std::vector<Op> &ops, const MatWork &w, const InvMatrix &mat, int *info) {
     const long long ld = w.dp;
     const int nb = w.dp / NB;
+    std::vector<int> panel_op(nb, -1);
     for (int k = 0; k < nb; ++k) {
         const int kb = k * NB;
-        if (k > 0) {
+        if (k > 0 && !LOOKAHEAD) {
             Op op{};
             op.g.push_back(split_job(w.ml, kb, 0, w.ml, kb, 0, w.dp - kb, NB, kb, -1.f, 1.f, w.Xh + kb * ld + kb,
                                      w.Xl + kb * ld + kb, nullptr, nullptr, ld));
+            ops.push_back(op);
+        } else if (k > 0) {
+            // the update by the last panel (k - 1) stays on the chain; the
+            // earlier panels' share ran as the lookahead of panel k - 2
+            Op op{};
+            op.g.push_back(split_job(w.ml, kb, kb - NB, w.ml, kb, kb - NB, w.dp - kb, NB, NB, -1.f, 1.f,
+                                     w.Xh + kb * ld + kb, w.Xl + kb * ld + kb, nullptr, nullptr, ld));
+            if (k >= 2) op.needs_side = panel_op[k - 2];
             ops.push_back(op);
         }
         {
@@ -496,6 +517,13 @@ void gen_chain(std::vector<Op> &ops, const MatWork &w, const InvMatrix &mat, int
             Op op{};
             op.g.push_back(split_job(w.mx, kb + NB, kb, w.mx, kb, kb, w.dp - kb - NB, NB, NB, 1.f, 0.f, w.Lh + c,
                                      w.Ll + c, nullptr, nullptr, ld));
+            if (k + 2 < nb && LOOKAHEAD) {
+                // lookahead: X[k2:, k2] -= L[k2:, :k+1] L[k2, :k+1]^T for block column k2 = k + 2
+                const int k2b = (k + 2) * NB;
+                op.side.push_back(split_job(w.ml, k2b, 0, w.ml, k2b, 0, w.dp - k2b, NB, kb + NB, -1.f, 1.f,
+                                            w.Xh + k2b * ld + k2b, w.Xl + k2b * ld + k2b, nullptr, nullptr, ld));
+            }
+            panel_op[k] = (int)ops.size();
             ops.push_back(op);
         }
     }
@@ -513,6 +541,7 @@ void gen_chain(std::vector<Op> &ops, const MatWork &w, const InvMatrix &mat, int
             // W21 = -W22 T (A: W22 rows, in X; B rows: T^T rows, in LT), W21^T into Wt
             x.g.push_back(split_job(w.mx, o + h, o + h, w.ml, o, o + h, m, h, m, -1.f, 0.f, w.Xh + x21,
                                     w.Xl + x21, w.Wh + t12, w.Wl + t12, ld));
+            x.g.back().ktril = 1;  // W22 is lower triangular
         }
         ops.push_back(t);
         ops.push_back(x);
@@ -592,15 +621,23 @@ std::vector<std::vector<std::pair<int, int>>> schedule_rounds(const std::vector<
 // path of the call) on a high-priority stream, all others on a low-priority
 // stream whose engine launches leave SMs free for the first group.  Each
 // group has its own rounds and engine scratch.
-constexpr int RESERVED_SMS = 32;  // SMs the second group's engine launches leave free
+constexpr int RESERVED_SMS = 32;   // SMs the second group's engine launches leave free
+constexpr int SIDE_FREE_SMS = 48;  // SMs a group's side launches leave to its own chain
+constexpr int SIDE_GROUPS = 1;     // groups whose lookahead updates run on a side stream (the others
+                                   // run them in their own stream, right after the enabling round)
 
 struct InvGroup {
     std::vector<int> members;  // chain indices
     std::vector<std::vector<std::pair<int, int>>> rounds;
     std::vector<int> round_kind;
+    std::vector<std::vector<TcJob>> side;   // per round: side problems launched once it is done
+    std::vector<std::vector<int>> waits;    // per round: rounds whose side launch must finish first
     int max_ctas = 0;          // engine grid cap (0: all SMs)
+    int side_ctas = 0;         // grid cap of the side launches
     char *tc_ws = nullptr;
     size_t tc_bytes = 0;
+    char *side_ws = nullptr;   // the side launches' own engine scratch (they overlap the rounds)
+    size_t side_bytes = 0;
 };
 
 struct InvPlan {
@@ -661,21 +698,44 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
         rest.max_ctas = std::max(1, device_sm_count() - RESERVED_SMS);
         p.groups.push_back(rest);
     }
-    // engine scratch of each group: its largest engine round
+    // rounds, side launches and engine scratch of each group
+    const int sms = device_sm_count();
     std::vector<TcJob> round;
     for (InvGroup &g : p.groups) {
         g.rounds = schedule_rounds(p.chains, g.members, g.round_kind);
-        size_t tcb = 0;
-        for (size_t r = 0; r < g.rounds.size(); ++r) {
+        g.side_ctas = std::max(1, (g.max_ctas > 0 ? g.max_ctas : sms) - SIDE_FREE_SMS);
+        const size_t R = g.rounds.size();
+        g.side.assign(R, {});
+        g.waits.assign(R, {});
+        std::vector<std::vector<int>> round_of(p.chains.size());
+        for (int k : g.members) round_of[k].assign(p.chains[k].size(), -1);
+        for (size_t r = 0; r < R; ++r)
+            for (const auto &ki : g.rounds[r]) round_of[ki.first][ki.second] = (int)r;
+        size_t tcb = 0, sideb = 0;
+        for (size_t r = 0; r < R; ++r) {
             round.clear();
             for (const auto &ki : g.rounds[r]) {
                 const Op &op = p.chains[ki.first][ki.second];
                 if (!op.leaf) round.insert(round.end(), op.g.begin(), op.g.end());
+                g.side[r].insert(g.side[r].end(), op.side.begin(), op.side.end());
+                if (op.needs_side >= 0) {
+                    const int src = round_of[ki.first][op.needs_side];
+                    if (std::find(g.waits[r].begin(), g.waits[r].end(), src) == g.waits[r].end())
+                        g.waits[r].push_back(src);
+                }
             }
             tcb = std::max(tcb, tc_workspace_bytes(round.data(), (int)round.size(), TC_KIND_TF32X3, g.max_ctas));
+            if (!g.side[r].empty()) {  // launched on the side stream (side_ctas) or inline (max_ctas)
+                sideb = std::max(sideb, tc_workspace_bytes(g.side[r].data(), (int)g.side[r].size(), TC_KIND_TF32X3,
+                                                           g.side_ctas));
+                sideb = std::max(sideb, tc_workspace_bytes(g.side[r].data(), (int)g.side[r].size(), TC_KIND_TF32X3,
+                                                           g.max_ctas));
+            }
         }
         g.tc_bytes = tcb;
         g.tc_ws = ws.take<char>(tcb);
+        g.side_bytes = sideb;
+        g.side_ws = ws.take<char>(sideb);
     }
     return KFAC_OK;
 }
@@ -764,12 +824,18 @@ kfac_status damping_run(const InvMatrix *mats, int nlayers, float gamma, int pi_
 
 namespace {
 
-// Enqueue one group's rounds on a stream.
-kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st) {
+// Enqueue one group's rounds on a stream, and its side launches (the
+// lookahead updates) on a second stream: a side launch starts once the round
+// that enables it is done (an event), and a round that needs a side launch
+// waits for its event.  ev_main / ev_side hold one event per round.
+kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st, cudaStream_t side, bool use_side,
+                      cudaEvent_t *ev_main, cudaEvent_t *ev_side) {
     std::vector<DiagJob> leaves;
     std::vector<TcJob> gemms;
     kfac_status s = KFAC_OK;
     for (size_t r = 0; r < g.rounds.size(); ++r) {
+        if (use_side)
+            for (int src : g.waits[r]) KFAC_CUDA_TRY(cudaStreamWaitEvent(st, ev_side[src], 0));
         leaves.clear();
         gemms.clear();
         for (const auto &ki : g.rounds[r]) {
@@ -784,18 +850,36 @@ kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st) {
                             g.max_ctas)) != KFAC_OK)
                 return s;
         }
+        if (!g.side[r].empty() && !use_side) {
+            Arena tail(g.side_ws, g.side_bytes);
+            if ((s = tc_run(g.side[r].data(), (int)g.side[r].size(), TC_KIND_TF32X3, p.dev_maps, tail, p.err, st,
+                            g.max_ctas)) != KFAC_OK)
+                return s;
+        } else if (!g.side[r].empty()) {
+            KFAC_CUDA_TRY(cudaEventRecord(ev_main[r], st));
+            KFAC_CUDA_TRY(cudaStreamWaitEvent(side, ev_main[r], 0));
+            Arena tail(g.side_ws, g.side_bytes);
+            if ((s = tc_run(g.side[r].data(), (int)g.side[r].size(), TC_KIND_TF32X3, p.dev_maps, tail, p.err, side,
+                            g.side_ctas)) != KFAC_OK)
+                return s;
+            KFAC_CUDA_TRY(cudaEventRecord(ev_side[r], side));
+        }
     }
     return KFAC_OK;
 }
 
-// Library-owned streams and events of one device for the two groups (created
-// on first use; the mutex also keeps concurrent callers from interleaving
-// their fork / join records on the shared events).
+// Library-owned streams and events of one device: a main and a side stream
+// for each of the two groups (created on first use; the mutex also keeps
+// concurrent callers from interleaving their fork / join records on the
+// shared events).
+constexpr int EVENT_POOL = 1024;
+
 struct GroupStreams {
     std::mutex mu;
     bool ready = false;
-    cudaStream_t hi = nullptr, lo = nullptr;
-    cudaEvent_t fork = nullptr, done_hi = nullptr, done_lo = nullptr;
+    cudaStream_t main[2] = {nullptr, nullptr}, side[2] = {nullptr, nullptr};
+    cudaEvent_t fork = nullptr, done[4] = {nullptr, nullptr, nullptr, nullptr};
+    std::vector<cudaEvent_t> pool;  // per-round events of the two groups
 };
 
 GroupStreams &group_streams(int dev) {
@@ -807,11 +891,15 @@ kfac_status ensure_streams(GroupStreams &g) {
     if (g.ready) return KFAC_OK;
     int least = 0, greatest = 0;
     KFAC_CUDA_TRY(cudaDeviceGetStreamPriorityRange(&least, &greatest));
-    KFAC_CUDA_TRY(cudaStreamCreateWithPriority(&g.hi, cudaStreamNonBlocking, greatest));
-    KFAC_CUDA_TRY(cudaStreamCreateWithPriority(&g.lo, cudaStreamNonBlocking, least));
+    for (int k = 0; k < 2; ++k) {
+        const int prio = k == 0 ? greatest : least;
+        KFAC_CUDA_TRY(cudaStreamCreateWithPriority(&g.main[k], cudaStreamNonBlocking, prio));
+        KFAC_CUDA_TRY(cudaStreamCreateWithPriority(&g.side[k], cudaStreamNonBlocking, prio));
+    }
     KFAC_CUDA_TRY(cudaEventCreateWithFlags(&g.fork, cudaEventDisableTiming));
-    KFAC_CUDA_TRY(cudaEventCreateWithFlags(&g.done_hi, cudaEventDisableTiming));
-    KFAC_CUDA_TRY(cudaEventCreateWithFlags(&g.done_lo, cudaEventDisableTiming));
+    for (int k = 0; k < 4; ++k) KFAC_CUDA_TRY(cudaEventCreateWithFlags(&g.done[k], cudaEventDisableTiming));
+    g.pool.resize(EVENT_POOL);
+    for (cudaEvent_t &e : g.pool) KFAC_CUDA_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
     g.ready = true;
     return KFAC_OK;
 }
@@ -834,31 +922,42 @@ kfac_status inv_run(const InvMatrix *mats, int nmats, const float *damp_dev, int
     if ((s = prep_launch(tm, damp_dev, st)) != KFAC_OK) return s;
 
     // 2. rounds (see schedule_rounds), the last op of each chain writing the
-    //    caller's inverse; with two groups, the critical one runs on a
-    //    high-priority stream and the other on a low-priority one, forked
-    //    from and joined back into the caller's stream
-    if (p.groups.size() == 1) return run_group(p, p.groups[0], st);
+    //    caller's inverse: each group on a main stream with a side stream for
+    //    its lookahead updates, the critical group at high priority and the
+    //    other at low priority, all forked from and joined back into the
+    //    caller's stream
     int dev = 0;
     KFAC_CUDA_TRY(cudaGetDevice(&dev));
     GroupStreams &g = group_streams(dev);
     std::lock_guard<std::mutex> lock(g.mu);
     if ((s = ensure_streams(g)) != KFAC_OK) return s;
+    size_t events = 0;
+    for (const InvGroup &gr : p.groups) events += 2 * gr.rounds.size();
+    if (events > g.pool.size()) return KFAC_ERR_UNSUPPORTED;
+    const int ngroups = (int)p.groups.size();
     KFAC_CUDA_TRY(cudaEventRecord(g.fork, st));
-    KFAC_CUDA_TRY(cudaStreamWaitEvent(g.hi, g.fork, 0));
-    KFAC_CUDA_TRY(cudaStreamWaitEvent(g.lo, g.fork, 0));
-    const kfac_status s0 = run_group(p, p.groups[0], g.hi);
-    kfac_status s1;
-    {
-        const PdlScope no_pdl(false);
-        s1 = run_group(p, p.groups[1], g.lo);
+    for (int k = 0; k < ngroups; ++k) {
+        KFAC_CUDA_TRY(cudaStreamWaitEvent(g.main[k], g.fork, 0));
+        KFAC_CUDA_TRY(cudaStreamWaitEvent(g.side[k], g.fork, 0));
+    }
+    kfac_status res[2] = {KFAC_OK, KFAC_OK};
+    size_t ev = 0;
+    for (int k = 0; k < ngroups; ++k) {
+        const InvGroup &gr = p.groups[k];
+        cudaEvent_t *em = g.pool.data() + ev, *es = em + gr.rounds.size();
+        ev += 2 * gr.rounds.size();
+        const PdlScope pdl(k == 0);  // early-launched CTAs of the low-priority group would hold SMs
+        res[k] = run_group(p, gr, g.main[k], g.side[k], k < SIDE_GROUPS, em, es);
     }
     // join in every case, so that a capture or later work stays ordered
-    KFAC_CUDA_TRY(cudaEventRecord(g.done_hi, g.hi));
-    KFAC_CUDA_TRY(cudaEventRecord(g.done_lo, g.lo));
-    KFAC_CUDA_TRY(cudaStreamWaitEvent(st, g.done_hi, 0));
-    KFAC_CUDA_TRY(cudaStreamWaitEvent(st, g.done_lo, 0));
-    if (s0 != KFAC_OK) return s0;
-    return s1;
+    for (int k = 0; k < ngroups; ++k) {
+        KFAC_CUDA_TRY(cudaEventRecord(g.done[2 * k], g.main[k]));
+        KFAC_CUDA_TRY(cudaEventRecord(g.done[2 * k + 1], g.side[k]));
+        KFAC_CUDA_TRY(cudaStreamWaitEvent(st, g.done[2 * k], 0));
+        KFAC_CUDA_TRY(cudaStreamWaitEvent(st, g.done[2 * k + 1], 0));
+    }
+    if (res[0] != KFAC_OK) return res[0];
+    return res[1];
 }
 
 }  // namespace kfac

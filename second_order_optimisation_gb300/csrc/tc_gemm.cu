@@ -40,7 +40,15 @@ constexpr int BM = 128, BN = 128;
 constexpr int TILE_BYTES = 128 * 128;  // one tf32 operand tile: 128 rows x 128 bytes
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_ACC = 2 * BN;  // two accumulators (columns 0 and BN), alternating
-constexpr int MAX_PROBS = 176;
+constexpr int MAX_PROBS = 160;
+constexpr int GROUP = 8;              // row blocks per band of the grouped tile order
+constexpr int TF32X3_MAX_SPLIT = 6;   // K splits of a tf32x3 tile (the last CTA sums the partials)
+// Planning choices for tf32x3 launches, as measured on the ResNet-50 step:
+// splitting long K ranges before narrowing tiles, and fewer K tiles per split,
+// both made the inversion slower; the grouped tile order made no difference.
+constexpr bool TF32X3_PREFER_SPLIT = false;  // split long K ranges before narrowing tiles
+constexpr double TF32X3_MIN_KT = 64.0;       // K tiles a tf32x3 split keeps at least
+constexpr bool TF32X3_GROUPED = false;       // grouped tile order for tf32x3 launches
 constexpr int MAPS_PER_COPY = 240;
 constexpr int STAGE_LD = 36;                              // epilogue staging row pitch (floats)
 constexpr size_t EPI_STAGE_BYTES = 4 * 32 * STAGE_LD * sizeof(float);
@@ -75,7 +83,8 @@ struct TcProb {
     int bn;                  // output tile width: 128, or 64 / 32 to spread small problems over SMs
     int tiles_n, ksplit, work_begin;
     uint8_t a_mn, b_mn;      // MN-major operand (bf16 only)
-    uint8_t syrk, sym, lower, ktri, epi;
+    uint8_t syrk, sym, lower, ktri, ktril, grouped, epi;
+    int tiles_m;             // 128-row blocks of the output
     uint8_t vec;             // C (and C_lo) rows take 16-byte accesses (ldc % 4 == 0, aligned)
     uint8_t vecb;            // Cb rows take 8-byte accesses
     uint8_t im2col, im_k, im_stride, im_pad;  // operands through an im2col map (see TcJob)
@@ -141,7 +150,37 @@ __device__ __forceinline__ Work decode_work(const TcParams &P, int w) {
     const int unit = local / q.ksplit;  // output tile
     k.split = local - unit * q.ksplit;
     const int T = q.tiles_n;
-    if (q.syrk || q.sym) {
+    if ((q.syrk || q.sym) && q.grouped) {
+        // upper tiles in bands of GROUP row blocks; inside a band column by
+        // column, rows innermost, so that the CTAs running at the same time
+        // share their A row panels and B column panels in L2.  first(tm) =
+        // tm * r with r = 128 / bn; row block tm holds T - first(tm) tiles.
+        const int r = BM / q.bn;
+        int u = unit, b0 = 0;
+        for (;;) {
+            const int gb = min(GROUP, q.tiles_m - b0);
+            const int size = gb * T - r * (gb * b0 + gb * (gb - 1) / 2);
+            if (u < size) break;
+            u -= size;
+            b0 += gb;
+        }
+        const int gb = min(GROUP, q.tiles_m - b0);
+        const int stair = r * gb * (gb + 1) / 2;  // columns r*b0 .. r*(b0+gb)-1 hold 1 .. gb rows
+        if (u < stair) {
+            int tn = r * b0;
+            for (;;) {
+                const int cnt = tn / r - b0 + 1;
+                if (u < cnt) { k.tm = b0 + u; k.tn = tn; break; }
+                u -= cnt;
+                ++tn;
+            }
+        } else {
+            u -= stair;
+            k.tn = r * (b0 + gb) + u / gb;
+            k.tm = b0 + u % gb;
+        }
+        k.tile = k.tm * T - r * (k.tm * (k.tm - 1) / 2) + (k.tn - k.tm * r);
+    } else if (q.syrk || q.sym) {
         // upper tiles only: row block tm (128 rows) runs column blocks from the
         // one holding its diagonal, first(tm) = tm * 128 / bn
         int u = unit, tm = 0, base = 0;
@@ -173,6 +212,14 @@ __device__ __forceinline__ Work decode_work(const TcParams &P, int w) {
             base += cnt;
             ++tm;
         }
+    } else if (q.grouped) {
+        // bands of GROUP row blocks, column by column, rows innermost
+        const int band = unit / (GROUP * T);
+        const int b0 = band * GROUP, gb = min(GROUP, q.tiles_m - b0);
+        const int rem = unit - band * GROUP * T;
+        k.tn = rem / gb;
+        k.tm = b0 + rem % gb;
+        k.tile = k.tm * T + k.tn;
     } else {
         k.tm = unit / T;
         k.tn = unit - k.tm * T;
@@ -181,9 +228,12 @@ __device__ __forceinline__ Work decode_work(const TcParams &P, int w) {
     // ktri (tf32x3 only, K tiles of 32): K starts at the tile's first column
     // (an upper tile of the product of an upper-triangular matrix with its
     // transpose)
+    // ktril (tf32x3): K ends after the tile's last row (A lower triangular
+    // in its K index: A[i][t] = 0 for t > i)
     const int kb = q.ktri ? k.tn * q.bn / Traits<TC_KIND_TF32X3>::BK : 0;
-    k.kt0 = kb + (int)((long long)k.split * (q.k_tiles - kb) / q.ksplit);
-    k.kt1 = kb + (int)((long long)(k.split + 1) * (q.k_tiles - kb) / q.ksplit);
+    const int ke = q.ktril ? min(q.k_tiles, (k.tm + 1) * BM / Traits<TC_KIND_TF32X3>::BK) : q.k_tiles;
+    k.kt0 = kb + (int)((long long)k.split * (ke - kb) / q.ksplit);
+    k.kt1 = kb + (int)((long long)(k.split + 1) * (ke - kb) / q.ksplit);
     return k;
 }
 
@@ -840,12 +890,20 @@ Plan make_plan(const TcJob *jobs, int n, int kind, int sms) {
     // A launch with few 128-wide tiles leaves most SMs idle and funnels each
     // tile's loads and stores through one SM: narrow the tiles (tf32x3 only)
     // until the launch covers at least half of the SMs.
+    // Long K ranges are split instead (each split keeps at least 8 K tiles),
+    // which keeps 128-wide tiles and so reads each A row panel once per tile.
     if (kind == TC_KIND_TF32X3) {
-        for (;;) {
-            long long t = 0;
-            for (int i = 0; i < n; ++i) t += tiles_of(jobs[i], p.bn);
-            if (p.bn == 32 || 2 * t >= sms) break;
-            p.bn /= 2;
+        long long splittable = 0;
+        for (int i = 0; i < n; ++i)
+            splittable += (long long)tiles_of(jobs[i], BN) *
+                          std::max(1, std::min(TF32X3_MAX_SPLIT, (int)(ceil_div(jobs[i].K, 32) / 8)));
+        if (!TF32X3_PREFER_SPLIT || splittable < sms) {
+            for (;;) {
+                long long t = 0;
+                for (int i = 0; i < n; ++i) t += tiles_of(jobs[i], p.bn);
+                if (p.bn == 32 || 2 * t >= sms) break;
+                p.bn /= 2;
+            }
         }
     }
     double total = 0.0;
@@ -857,11 +915,13 @@ Plan make_plan(const TcJob *jobs, int n, int kind, int sms) {
     // Split K only where one problem's tiles would otherwise be the critical
     // path: the longest work item should not exceed about twice the average
     // share of one SM.  A split costs a partial-tile round trip through L2, so
-    // items keep at least 8 (bf16) / 64 (tf32x3) K tiles.
-    const double min_kt = kind == TC_KIND_BF16 ? 8.0 : 64.0;
+    // items keep at least 8 K tiles; a tf32x3 tile takes at most
+    // TF32X3_MAX_SPLIT splits (its last CTA reads all partials).
+    const double min_kt = kind == TC_KIND_BF16 ? 8.0 : TF32X3_MIN_KT;
     const double target = std::max(min_kt, total / (sms * 2.0));
     for (int i = 0; i < n; ++i) {
         int ks = (int)std::ceil(p.k_tiles[i] / target);
+        if (kind == TC_KIND_TF32X3) ks = std::min(ks, TF32X3_MAX_SPLIT);
         ks = std::max(1, std::min(ks, std::min(p.k_tiles[i], 256)));
         if (jobs[i].no_split || jobs[i].ktri) ks = 1;  // (a ktri split would leave late tiles empty)
         p.ksplit[i] = ks;
@@ -982,7 +1042,7 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
         if (j.sym && (kind != TC_KIND_TF32X3 || j.M != j.N || (j.epi != TC_EPI_SPLIT && j.epi != TC_EPI_STORE)))
             return KFAC_ERR_INVALID;
         if (j.lower && (kind != TC_KIND_TF32X3 || j.sym || j.syrk || j.epi != TC_EPI_SPLIT)) return KFAC_ERR_INVALID;
-        if (j.ktri && kind != TC_KIND_TF32X3) return KFAC_ERR_INVALID;
+        if ((j.ktri || j.ktril) && kind != TC_KIND_TF32X3) return KFAC_ERR_INVALID;
         if (!j.C && !j.Ct && !j.Cb) return KFAC_ERR_INVALID;
     }
     const int sms = cta_cap(max_ctas);
@@ -1018,6 +1078,9 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
             q.sym = j.sym;
             q.lower = j.lower;
             q.ktri = j.ktri;
+            q.ktril = j.ktril;
+            q.grouped = TF32X3_GROUPED && kind == TC_KIND_TF32X3 && !j.lower;
+            q.tiles_m = (int)ceil_div(j.M, BM);
             q.ksplit = p.ksplit[ji];
             q.work_begin = work;
             q.epi = j.epi;

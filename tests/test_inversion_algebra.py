@@ -71,9 +71,9 @@ def diag_sweep(S, panel=8):
     return M
 
 
-def _job(A, ar, ac, B, br, bc, M, N, K, alpha, beta, C=None, Ct=None, ktri=False):
+def _job(A, ar, ac, B, br, bc, M, N, K, alpha, beta, C=None, Ct=None, ktri=False, ktril=False):
     return dict(A=A, ar=ar, ac=ac, B=B, br=br, bc=bc, M=M, N=N, K=K, alpha=alpha, beta=beta, C=C, Ct=Ct,
-                ktri=ktri)
+                ktri=ktri, ktril=ktril)
 
 
 def _tri_nodes(o, n, by_height):
@@ -88,16 +88,25 @@ def _tri_nodes(o, n, by_height):
 
 
 def chain(dp):
-    """Ops of one dp x dp matrix, in the library's order (leaf or engine)."""
+    """Ops of one dp x dp matrix, in the library's order (leaf or engine).
+    An engine op may carry side problems (the lookahead update of column
+    block k + 2 by panels 0 .. k), which the library launches on a second
+    stream once the op is done and which finish before the chain's update of
+    that column by its last panel."""
     ops, nb = [], dp // NB
     for k in range(nb):
         kb = k * NB
-        if k > 0:   # X[k:, k] -= L[k:, :k] L[k, :k]^T
-            ops.append(("gemm", [_job("L", kb, 0, "L", kb, 0, dp - kb, NB, kb, -1.0, 1.0, C=("X", kb, kb))]))
+        if k > 0:   # X[k:, k] -= L[k:, k-1] L[k, k-1]^T   (the last panel's share)
+            ops.append(("gemm", [_job("L", kb, kb - NB, "L", kb, kb - NB, dp - kb, NB, NB, -1.0, 1.0,
+                                      C=("X", kb, kb))], []))
         ops.append(("leaf", kb))
         if k + 1 < nb:   # L[k+1:, k] = X[k+1:, k] W_kk^T
+            side = []
+            if k + 2 < nb:   # X[k2:, k2] -= L[k2:, :k+1] L[k2, :k+1]^T
+                k2b = (k + 2) * NB
+                side = [_job("L", k2b, 0, "L", k2b, 0, dp - k2b, NB, kb + NB, -1.0, 1.0, C=("X", k2b, k2b))]
             ops.append(("gemm", [_job("X", kb + NB, kb, "X", kb, kb, dp - kb - NB, NB, NB, 1.0, 0.0,
-                                      C=("L", kb + NB, kb))]))
+                                      C=("L", kb + NB, kb))], side))
     by_height = []
     _tri_nodes(0, dp, by_height)
     for ht in range(1, len(by_height)):
@@ -107,9 +116,9 @@ def chain(dp):
             m = n - h
             t.append(_job("L", o + h, o, "W", o, o, m, h, h, 1.0, 0.0, Ct=("L", o, o + h), ktri=True))
             x.append(_job("X", o + h, o + h, "L", o, o + h, m, h, m, -1.0, 0.0, C=("X", o + h, o),
-                          Ct=("W", o, o + h)))
-        ops.append(("gemm", t))
-        ops.append(("gemm", x))
+                          Ct=("W", o, o + h), ktril=True))
+        ops.append(("gemm", t, []))
+        ops.append(("gemm", x, []))
     return ops
 
 
@@ -120,22 +129,17 @@ def invert_like_the_library(F, damp, bn):
     X0[:d, :d] = F + damp * np.eye(d)
     buf = {k: np.full((dp, dp), np.nan) for k in ("X", "W", "L")}
     buf["X"][:] = np.tril(X0)                     # prep: lower part, zeros above
-    for op in chain(dp):
-        if op[0] == "leaf":
-            o = op[1]
-            W = diag_sweep(buf["X"][o:o + NB, o:o + NB])
-            buf["X"][o:o + NB, o:o + NB] = np.tril(W)
-            buf["W"][o:o + NB, o:o + NB] = np.triu(W.T)
-            continue
+    def launch(jobs):
         results = []
-        for j in op[1]:   # every problem of one launch reads before any writes
+        for j in jobs:   # every problem of one launch reads before any writes
             A = buf[j["A"]][j["ar"]:j["ar"] + j["M"], j["ac"]:j["ac"] + j["K"]]
             B = buf[j["B"]][j["br"]:j["br"] + j["N"], j["bc"]:j["bc"] + j["K"]]
             acc = np.full((j["M"], j["N"]), np.nan)
             for tm in range(0, j["M"], NB):
                 for tn in range(0, j["N"], bn):
-                    k0 = tn if j["ktri"] else 0
-                    acc[tm:tm + NB, tn:tn + bn] = A[tm:tm + NB, k0:] @ B[tn:tn + bn, k0:].T
+                    k0 = tn if j["ktri"] else 0                       # B[j][t] = 0 for t < j
+                    k1 = min(j["K"], tm + NB) if j["ktril"] else j["K"]  # A[i][t] = 0 for t > i
+                    acc[tm:tm + NB, tn:tn + bn] = A[tm:tm + NB, k0:k1] @ B[tn:tn + bn, k0:k1].T
             results.append((j, acc))
         for j, acc in results:
             if j["C"]:
@@ -145,6 +149,17 @@ def invert_like_the_library(F, damp, bn):
             if j["Ct"]:
                 b, r, c = j["Ct"]
                 buf[b][r:r + j["N"], c:c + j["M"]] = (j["alpha"] * acc).T
+
+    for op in chain(dp):
+        if op[0] == "leaf":
+            o = op[1]
+            W = diag_sweep(buf["X"][o:o + NB, o:o + NB])
+            buf["X"][o:o + NB, o:o + NB] = np.tril(W)
+            buf["W"][o:o + NB, o:o + NB] = np.triu(W.T)
+            continue
+        launch(op[1])
+        if op[2]:
+            launch(op[2])
     Wt = buf["W"]
     out = np.full((dp, dp), np.nan)
     for tm in range(0, dp, NB):

@@ -44,6 +44,11 @@ MUTANTS = [
     ("precondition rows transposed A^-1", "out[t * dA + j] += uk * Ainv[k * dA + j];",
      "out[t * dA + j] += uk * Ainv[j * dA + k] * (j == k ? 1.0 : 0.5);",
      [pins.test_precondition_rows_are_rows_of_the_kronecker_solve]),
+    ("weight update sign", "w[o * dA + j] -= eta * P[o * dA + j];", "w[o * dA + j] += eta * P[o * dA + j];",
+     [pins.test_weight_update_closed_forms]),
+    ("refresh schedule off by one", "return (t - warmup) % every == 0;", "return (t - warmup + 1) % every == 0;",
+     [lambda: pins.test_refresh_schedule_closed_forms(3, 4, 20),
+      pins.test_stale_schedule_equals_stepwise_composition]),
     ("bn unbiased variance", "double f = s2 / (double)ns;", "double f = s2 / (double)(ns - 1);",
      [pins.test_bn_diag_is_diagonal_of_explicit_fisher]),
     ("bn drops damping", "out[c] = gmean[c] / (F[c] + gamma);", "out[c] = gmean[c] / F[c];",

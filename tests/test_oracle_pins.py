@@ -275,3 +275,47 @@ def test_fc_step_matches_stored_oracle_values():
         assert abs(got[k]["fro"] - ref[k]["fro"]) <= 1e-12 * ref[k]["fro"]
         for (i, j, v), (_, _, w) in zip(got[k]["entries"], ref[k]["entries"]):
             assert abs(v - w) <= 1e-12 * max(abs(w), 1e-30) + 1e-300
+
+
+# ------------------------------------------------------- Eq. 8 / stale schedule
+
+def test_weight_update_closed_forms():
+    rng = np.random.default_rng(21)
+    w = rng.standard_normal((4, 6))
+    P = rng.standard_normal((4, 6))
+    np.testing.assert_array_equal(oracle.weight_update(w, P, 0.0), w)
+    np.testing.assert_array_equal(oracle.weight_update(np.zeros_like(P), P, 1.0), -P)
+    a = oracle.weight_update(w, P, 0.3)
+    b = oracle.weight_update(w, P, 0.7)
+    np.testing.assert_allclose(a + b - w, oracle.weight_update(w, P, 1.0), rtol=1e-14, atol=1e-15)
+
+
+@pytest.mark.parametrize("warmup,every,steps", [(0, 1, 7), (3, 4, 20), (10, 5, 8), (2, 10, 30)])
+def test_refresh_schedule_closed_forms(warmup, every, steps):
+    flags = [oracle.is_refresh_step(t, warmup, every) for t in range(steps)]
+    assert all(flags[:warmup])
+    if every == 1 or warmup >= steps:
+        assert all(flags)
+    after = max(0, steps - warmup)
+    assert sum(flags) == min(warmup, steps) + (after + every - 1) // every
+
+
+def test_stale_schedule_equals_stepwise_composition():
+    """The schedule is the per-step composition of EMA, damping, inversion and
+    preconditioning on refresh steps and preconditioning with the kept
+    inverses otherwise."""
+    rng = np.random.default_rng(22)
+    steps = []
+    for t in range(5):
+        P = np.maximum(rng.standard_normal((12, 5)), 0)
+        Gam = rng.standard_normal((12, 3)) * 1e-2
+        steps.append((P, Gam, rng.standard_normal((3, 5)) * 1e-3))
+    outs = oracle.kfac_schedule(np.eye(5), np.eye(3), steps, 0.95, 1e-3, warmup=1, every=3)
+    A, G = np.eye(5), np.eye(3)
+    for t, (P, Gam, grad) in enumerate(steps):
+        if t in (0, 1, 4):   # warmup 1, every 3: steps 0, 1, 4 refresh
+            A = oracle.factor_ema(A, P, 0.95)
+            G = oracle.factor_ema(G, Gam, 0.95)
+            da, dg = oracle.pi_damping(A, G, 1e-3)
+            Ai, Gi = oracle.damped_inverse(A, da), oracle.damped_inverse(G, dg)
+        np.testing.assert_allclose(outs[t], oracle.precondition(Gi, grad, Ai), rtol=1e-12)
