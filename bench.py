@@ -4,33 +4,54 @@ preconditioning) for the ResNet-50 layer set at 32 samples per GPU, on
 synthetic inputs with ResNet-50's shapes.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
-                  [--workload resnet50|conv3x3_256|fc4096|fc64x32]
+                  [--workload resnet50|conv3x3_256|fc4096]
 
-Prints ONE JSON line (rank 0).  The default arm times the CUDA library
-(device-resident inputs; whole step captured once in a CUDA graph and
-replayed); `e2e` times the same step through the C ABI with host buffers
-(pinned H2D of the step's inputs and D2H of the preconditioned gradients
-inside the timed region).  `--impl reference` times the CPU oracle (the
-method's plain fp64 statement) on a bounded sample of the same workload and
-scales it to one step by algorithmic FLOPs.  Under torchrun every rank runs
-an independent replica (the step has no data-path exchange on one GPU per
-replica); the time reported is the max over ranks.
+Prints ONE JSON line (rank 0).
+
+Default arm (the CUDA library): inputs resident in HBM; the whole step is
+captured once in a CUDA graph and replayed K times between CUDA events
+(`value`); each phase is also captured and timed on its own (`phases`).
+`e2e` times the same step with the inputs copied from pinned host memory and
+the preconditioned gradients copied back inside the timed region.
+`schedule` gives the amortised ms per step of the stale-factor schedule
+(refresh every k steps) for k in {1, 5, 10, 20}, measured by replaying the
+refresh and the precondition-only graphs in that pattern.  For the ResNet-50
+workload the line also carries sub-records for FC 4096 and the 3x3 conv
+(`subrecords`) and the BatchNorm diagonal Fisher (`bn_fisher`).
+
+`--impl reference` runs the CPU oracle (the method's plain fp64 statement)
+on the host cores: one whole step, every layer's oracle step timed once
+(layers of identical shape are timed once and counted with their
+multiplicity), so `value` is the measured time of one full oracle step.
+
+Under torchrun every rank runs an independent replica (the step has no
+data-path exchange); the time reported is the max over ranks.
 """
 from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
 import sys
 import tempfile
 import time
+from collections import Counter
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "ResNet-50 K-FAC step ms (factors+inverse+precond); TFLOP/s vs GB300 peak"
+NB = 128            # block width of the inversion
+SCHEDULE_KS = (1, 5, 10, 20)
+
+# DRAM traffic per launch of a kernel kind from one ncu capture of the same
+# kernel build (dram__bytes_read.sum + dram__bytes_write.sum), with the
+# profile summary it comes from; None where no capture of the current build
+# exists.
+NCU_TRAFFIC = {}
 
 
 # ------------------------------------------------------------------ workloads
@@ -47,6 +68,10 @@ def workload(name):
 
 
 def flops(layers, batch):
+    """Algorithmic FLOPs of one step: SYRK M d (d + 1) per factor, the
+    Cholesky-based inversion d^3 per factor (factor d^3/3, triangular inverse
+    d^3/3, product of the inverse factors d^3/3), and the two preconditioning
+    products 2 dG^2 dA + 2 dG dA^2 per layer."""
     syrk = inv = pc = 0
     for L in layers:
         M = L.rows(batch)
@@ -56,87 +81,68 @@ def flops(layers, batch):
     return dict(syrk=syrk, inv=inv, precond=pc, total=syrk + inv + pc)
 
 
-def schur_gemm_flops(d, leaf=128, leaf_max=256):
-    """Useful fp32 flops of the tensor-core Schur-complement GEMMs that invert
-    one d x d factor (padded to a multiple of 128, split on 128-row block
-    boundaries down to leaves of 128 or 256 rows; the two symmetric updates
-    count half)."""
-    def rec(n):
-        if n <= leaf or n == leaf_max:
-            return 0
-        nb = n // leaf
-        h = leaf * (nb // 2)
-        m = n - h
-        return rec(h) + rec(m) + 2 * h * m * h + m * m * h + 2 * h * m * m + h * h * m
-    dp = -(-d // leaf) * leaf
-    return rec(dp)
+def diag_flops(d):
+    """FLOPs of the 128 x 128 diagonal blocks of one d x d factor, each
+    factored and inverted on CUDA cores (Cholesky + triangular inverse,
+    2/3 * 128^3 each block)."""
+    return math.ceil(d / NB) * 2 * NB ** 3 // 3
 
 
-def leaf_sizes(d, leaf=128, leaf_max=256):
-    """Block sizes of the leaves that invert one d x d factor."""
-    out = []
-    def rec(n):
-        if n <= leaf or n == leaf_max:
-            out.append(n)
-            return
-        nb = n // leaf
-        h = leaf * (nb // 2)
-        rec(h)
-        rec(n - h)
-    rec(-(-d // leaf) * leaf)
-    return out
+def inversion_split(layers):
+    """(tensor-core engine FLOPs, diag-kernel FLOPs) of the inversion."""
+    dims = [L.d_a for L in layers] + [L.d_g for L in layers]
+    dg = sum(diag_flops(d) for d in dims)
+    return sum(d ** 3 for d in dims) - dg, dg
 
 
-def leaf_flops(n):
-    """Gauss-Jordan inverse of an n x n block: n^3 multiply-adds (2 n^3 flops)."""
-    return 2 * n ** 3
-
-
-def kernel_rooflines(kern, layers, batch, fl, pk, steps):
-    """Per-kernel achieved rate vs its roofline from the per-phase event
-    totals.  Algorithmic work per step:
-      tc_gemm_bf16 (factors)  SYRK M*d(d+1) per factor            (tensor, bf16 peak)
-      tc_gemm_bf16 (precond)  2 dG^2 dA + 2 dG dA^2 per layer      (tensor, bf16 peak)
-      tc_gemm_tf32x3          Schur GEMM flops (schur_gemm_flops)  (tensor, tf32 peak / 3 products)
-      inv_leaf                2 n^3 per n-block leaf (n = 128, 256)  (tensor, tf32 peak / 3 products)
-      im2col                  bytes of the materialised patch matrices written + inputs read (HBM)
-      inv_prep                upper triangle of F read (4 B) + the (hi, lo) pair written, dp^2 x 8 B
-      inv_finish              upper triangle of the pair read (8 B) + fp32 and bf16 inverses written
-                              (d^2 x 6 B)                          (HBM)"""
+def kernel_work(layers, batch, fl, pk, sm_mhz):
+    """Algorithmic work of one step per (phase, kernel kind):
+      tc_gemm_bf16 (factors)   SYRK M d(d+1) per factor                   tensor, bf16 peak
+      tc_gemm_bf16 (precond)   2 dG^2 dA + 2 dG dA^2 per layer            tensor, bf16 peak
+      tc_gemm_tf32x3 (inverse) d^3 - diag blocks' share per factor        tensor, 3 tf32 products
+      inv_diag (inverse)       2/3 * 128^3 per 128 x 128 diagonal block   fp32 CUDA cores (alu)
+      inv_prep (inverse)       upper triangle of F read (4 B) + the (hi, lo) working pair
+                               written (dp^2 x 8 B)                       HBM
+      im2col (factors)         materialised patch bytes written + input read   HBM"""
     tf32x3_peak = pk["bf16"] * (1.1 / 2.25) / 3.0
-    schur = sum(schur_gemm_flops(L.d_a) + schur_gemm_flops(L.d_g) for L in layers)
-    leaves = sum(leaf_flops(n) for L in layers for d in (L.d_a, L.d_g) for n in leaf_sizes(d))
+    # fp32 FMA rate: 152 SMs x 128 lanes x 2 FLOP per cycle at the SM clock
+    alu_peak = 152 * 128 * 2 * (sm_mhz or 2070.0) * 1e6 / 1e12
+    eng, dgf = inversion_split(layers)
     im2col_bytes = 0
     for L in layers:
-        # patches are materialised only where the SYRK cannot read the input
-        # through an im2col tensor map (channels not in whole 64-wide taps)
         if (L.k > 1 or L.stride > 1) and L.cin % 64 != 0:
             im2col_bytes += L.rows(batch) * L.k * L.k * L.cin * 2 + batch * L.hin * L.hin * L.cin * 2
-    pad = lambda d: (d + 127) // 128 * 128
+    pad = lambda d: (d + NB - 1) // NB * NB
     dims = [L.d_a for L in layers] + [L.d_g for L in layers]
     prep_bytes = sum(d * (d + 1) // 2 * 4 + pad(d) ** 2 * 8 for d in dims)
-    finish_bytes = sum(d * (d + 1) // 2 * 8 + d * d * 6 for d in dims)
-    work = {("factors", "tc_gemm_bf16"): (fl["syrk"], "tensor", pk["bf16"], "TFLOP/s"),
-            ("inverse", "inv_prep"): (prep_bytes, "hbm", pk["hbm"], "GB/s"),
-            ("inverse", "inv_finish"): (finish_bytes, "hbm", pk["hbm"], "GB/s"),
-            ("precond", "tc_gemm_bf16"): (fl["precond"], "tensor", pk["bf16"], "TFLOP/s"),
-            ("inverse", "tc_gemm_tf32x3"): (schur, "tensor", tf32x3_peak, "TFLOP/s"),
-            ("inverse", "inv_leaf"): (leaves, "tensor", tf32x3_peak, "TFLOP/s"),
-            ("factors", "im2col"): (im2col_bytes, "hbm", pk["hbm"], "GB/s")}
+    return {("factors", "tc_gemm_bf16"): (fl["syrk"], "tensor", pk["bf16"], "TFLOP/s", "bf16 burst (measured)"),
+            ("precond", "tc_gemm_bf16"): (fl["precond"], "tensor", pk["bf16"], "TFLOP/s", "bf16 burst (measured)"),
+            ("inverse", "tc_gemm_tf32x3"): (eng, "tensor", tf32x3_peak, "TFLOP/s",
+                                            "measured bf16 burst x 1.1/2.25 (tf32/bf16 nominal) / 3 products"),
+            ("inverse", "inv_diag"): (dgf, "alu", alu_peak, "TFLOP/s",
+                                      "152 SMs x 128 fp32 lanes x 2 FLOP x SM clock"),
+            ("inverse", "inv_prep"): (prep_bytes, "hbm", pk["hbm"], "GB/s", "HBM copy (measured)"),
+            ("factors", "im2col"): (im2col_bytes, "hbm", pk["hbm"], "GB/s", "HBM copy (measured)")}
+
+
+def kernel_rooflines(kern, work, steps):
+    """Per-kernel achieved rate from the library's per-launch event timings
+    (eager run, each launch bracketed by events on its own stream)."""
     out = {}
     for ph, ks in kern.items():
         for name, (t, n) in ks.items():
-            key = f"{name}@{ph}"
             ms_step = t / steps
-            rec = {"ms_per_step": ms_step, "launches_per_step": n / steps,
-                   "avg_launch_us": 1e3 * t / max(n, 1)}
+            rec = {"ms_per_step": ms_step, "launches_per_step": n / steps, "avg_launch_us": 1e3 * t / max(n, 1)}
             if (ph, name) in work:
-                w, bound, peak, unit = work[(ph, name)]
+                w, bound, peak, unit, psrc = work[(ph, name)]
                 scale = 1e12 if unit == "TFLOP/s" else 1e9
-                ach = w / (ms_step * 1e-3) / scale
+                ach = w / (ms_step * 1e-3) / scale if ms_step > 0 else 0.0
+                tr = NCU_TRAFFIC.get(f"{name}@{ph}")
                 rec.update({"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
-                            "traffic": None})
-            out[key] = rec
+                            "peak_source": psrc, "work_per_step": w,
+                            "traffic": tr[0] if tr else None,
+                            "traffic_source": tr[1] if tr else "no ncu capture of this build"})
+            out[f"{name}@{ph}"] = rec
     return out
 
 
@@ -195,8 +201,9 @@ class Clocks:
 # ------------------------------------------------------------------ oracle
 
 def oracle_layer_step(L, batch, tag="bench"):
-    """The oracle's full step for one layer (factors from I, EMA, pi damping,
-    Cholesky inverses, preconditioning); returns seconds and FLOPs."""
+    """The oracle's whole step for one layer (patches, both factors from I
+    with xi = 0.95, pi-split damping, Cholesky-based inverses,
+    preconditioning); returns seconds."""
     import numpy as np
 
     import oracle
@@ -210,35 +217,47 @@ def oracle_layer_step(L, batch, tag="bench"):
     t0 = time.perf_counter()
     P = oracle.im2col(xo, L.k, L.k, (L.stride,) * 2, (L.pad,) * 2, append_one=L.bias)
     oracle.kfac_layer_step(np.eye(L.d_a), np.eye(L.d_g), P, go, gr, xi=0.95, gamma=1e-3)
-    dt = time.perf_counter() - t0
-    return dt, flops([L], batch)["total"]
+    return time.perf_counter() - t0
 
 
-SAMPLE_LAYERS = ("s2b2_3x3", "s3b2_1x1a", "s3b3_3x3")
+def shape_key(L):
+    return (L.k, L.cin, L.cout, L.stride, L.pad, L.hin, L.hout, L.bias)
 
 
-def cpu_baseline(layers, batch, budget_s=20.0):
-    """Oracle on a bounded sample: whole layer steps of a few ResNet-50 layers
-    until ~budget_s of CPU work, scaled to one full step by algorithmic FLOPs."""
+def oracle_full_step(layers, batch, tag="bench"):
+    """One whole oracle step: each distinct layer shape's step timed once and
+    counted with its multiplicity (the oracle's time depends only on the
+    shapes).  Returns (seconds, distinct shapes, layers)."""
+    counts = Counter(shape_key(L) for L in layers)
+    first = {}
+    for L in layers:
+        first.setdefault(shape_key(L), L)
+    total = 0.0
+    for key, L in first.items():
+        total += counts[key] * oracle_layer_step(L, batch, tag)
+    return total, len(first), len(layers)
+
+
+def cpu_baseline(layers, batch):
+    """The oracle as it stands on the host cores: the whole step on all
+    cores (measured, distinct shapes once), and the single-thread time of one
+    mid-size layer beside its all-core time, which scales the whole step to
+    one thread (an estimate, labelled as such)."""
     import oracle
+    oracle.build()
     cores = oracle.set_threads(0)
-    names = [L.name for L in layers]
-    sample = [L for L in layers if L.name in SAMPLE_LAYERS] or layers[:1]
-    t = f = 0.0
-    used = []
-    t_start = time.perf_counter()
-    for L in sample:
-        dt, fl = oracle_layer_step(L, batch)
-        t += dt
-        f += fl
-        used.append(L.name)
-        if time.perf_counter() - t_start > budget_s:
-            break
-    total = flops(layers, batch)["total"]
-    ms = t / f * total * 1e3
-    return {"value": ms, "unit": "ms", "cores": cores, "kind": "oracle",
-            "sample": f"oracle layer steps of {'+'.join(used)} ({f / 1e9:.1f} GFLOP, {t:.1f} s) scaled by "
-                      f"algorithmic FLOPs to the {len(names)}-layer step ({total / 1e9:.0f} GFLOP)"}
+    t_all, nshapes, nlayers = oracle_full_step(layers, batch, "cpu")
+    probe = [L for L in layers if L.name == "s3b2_1x1a"] or layers[:1]
+    a = oracle_layer_step(probe[0], batch, "cpu1")
+    oracle.set_threads(1)
+    s = oracle_layer_step(probe[0], batch, "cpu1")
+    oracle.set_threads(0)
+    return {"value": t_all * 1e3, "unit": "ms", "cores": cores, "kind": "oracle",
+            "sample": f"the whole {nlayers}-layer step: every distinct layer shape's oracle step timed once "
+                      f"({nshapes} shapes) and counted with its multiplicity; all {cores} host threads",
+            "single_thread_ms_estimate": t_all * 1e3 * s / a,
+            "single_thread_sample": f"{probe[0].name}: {s * 1e3:.0f} ms on 1 thread vs {a * 1e3:.0f} ms on "
+                                    f"{cores}; the whole step scaled by that ratio"}
 
 
 # ------------------------------------------------------------------ dist
@@ -273,171 +292,176 @@ def barrier(world):
         dist.barrier()
 
 
-# ------------------------------------------------------------------ arms
+# ------------------------------------------------------------------ reference arm
 
 def run_reference(args, world, rank):
+    """One whole oracle step (see oracle_full_step) on rank 0; the other
+    ranks exit without work."""
     if rank != 0:
         return 0
     layers, batch = workload(args.workload)
     import oracle
     oracle.build()
     cores = oracle.set_threads(0)
-    sample = [L for L in layers if L.name in SAMPLE_LAYERS] or layers[:1]
-    total = flops(layers, batch)["total"]
-    ests = []
-    for i in range(args.warmup + args.steps):
-        L = sample[i % len(sample)]
-        dt, fl = oracle_layer_step(L, batch, tag=f"ref{i}")
-        if i >= args.warmup:
-            ests.append(dt / fl * total * 1e3)
-    ms = statistics.mean(ests)
+    small = min(layers, key=lambda L: L.d_a ** 3 + L.rows(batch) * L.d_a ** 2)
+    for i in range(args.warmup):
+        oracle_layer_step(small, batch, tag=f"refw{i}")
+    t, nshapes, nlayers = oracle_full_step(layers, batch, "ref")
+    ms = t * 1e3
     line = {"impl": "reference", "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+            "steps": 1, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{args.workload}_kfac_step", "layers": len(layers), "batch_per_gpu": batch},
+            "config": {"workload": f"{args.workload}_kfac_step", "layers": nlayers, "batch_per_gpu": batch},
             "cpu_baseline": {"value": ms, "unit": "ms", "cores": cores, "kind": "oracle",
-                             "sample": "each step: one oracle layer step cycling over "
-                                       f"{'+'.join(L.name for L in sample)}, scaled by algorithmic FLOPs "
-                                       f"to the full step ({total / 1e9:.0f} GFLOP)"},
+                             "sample": f"one whole step ({nlayers} layers; each of the {nshapes} distinct "
+                                       f"layer shapes' oracle step timed once and counted with its "
+                                       f"multiplicity); --steps {args.steps} requested, one full step timed"},
             "e2e": {"value": ms, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
 
-def run_ours(args, world, rank, local):
-    import numpy as np
+# ------------------------------------------------------------------ our arm
+
+class Inputs:
+    """All inputs of a step packed in ONE pinned host buffer and ONE device
+    buffer (256-byte aligned slots), so the end-to-end copy is a single H2D."""
+
+    def __init__(self, layers, batch, dev, tag="bench"):
+        import torch
+
+        from second_order_optimisation_gb300 import workloads as W
+        host_t, self.slots, off = [], [], 0
+        for L in layers:
+            x, g, grad = W.layer_inputs(L, batch, tag)
+            if L.hin == 1:
+                x = x.reshape(x.shape[0], -1)
+            ld = (L.d_a + 7) // 8 * 8
+            gp = torch.zeros(L.d_g, ld, dtype=torch.bfloat16)
+            gp[:, :L.d_a] = grad
+            for t in (x, g, gp):
+                t = t.contiguous()
+                host_t.append(t)
+                self.slots.append((off, t.shape))
+                off += (t.numel() * 2 + 255) // 256 * 256
+        self.nbytes = off
+        self.layers = layers
+        self.hbuf = torch.empty(off, dtype=torch.uint8).pin_memory()
+        for t, (o, shp) in zip(host_t, self.slots):
+            self.hbuf[o:o + t.numel() * 2].view(torch.bfloat16).view(shp).copy_(t)
+        self.dbuf = torch.empty(off, dtype=torch.uint8, device=dev)
+        self.dbuf.copy_(self.hbuf, non_blocking=True)
+        self.views = self.device_views(self.dbuf)
+
+    def device_views(self, db):
+        import torch
+        vv = [db[o:o + int(math.prod(shp)) * 2].view(torch.bfloat16).view(shp) for (o, shp) in self.slots]
+        return vv[0::3], vv[1::3], [t[:, :L.d_a] for t, L in zip(vv[2::3], self.layers)]
+
+
+def graph_of(fn, stream):
     import torch
-
-    import __graft_entry__
-    from second_order_optimisation_gb300 import kfac
-    from second_order_optimisation_gb300 import workloads as W
-    from second_order_optimisation_gb300.step import KfacStep
-
-    __graft_entry__.build()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    layers, batch = workload(args.workload)
-    fl = flops(layers, batch)
-    pk = peaks()
-
-    # seeded synthetic inputs, pinned on the host and resident on the device
-    # all inputs of a step packed in ONE pinned host buffer and ONE device
-    # buffer (256-byte aligned slots), so the end-to-end copy is a single H2D
-    host_t, slots, off = [], [], 0
-    for L in layers:
-        x, g, grad = W.layer_inputs(L, batch, "bench")
-        if L.hin == 1:
-            x = x.reshape(x.shape[0], -1)
-        ld = (L.d_a + 7) // 8 * 8
-        gp = torch.zeros(L.d_g, ld, dtype=torch.bfloat16)
-        gp[:, :L.d_a] = grad
-        for t in (x, g, gp):
-            t = t.contiguous()
-            host_t.append(t)
-            slots.append((off, t.shape))
-            off += (t.numel() * 2 + 255) // 256 * 256
-    in_bytes = off
-    hbuf = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
-    dbuf = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
-    hv, dv = [], []
-    for t, (o, shp) in zip(host_t, slots):
-        n = t.numel() * 2
-        h = hbuf[o:o + n].view(torch.bfloat16).view(shp)
-        h.copy_(t)
-        hv.append(h)
-        dv.append(dbuf[o:o + n].view(torch.bfloat16).view(shp))
-    del host_t
-    dbuf.copy_(hbuf, non_blocking=True)
-    dx, dg, dgr = dv[0::3], dv[1::3], dv[2::3]
-    dgr_v = [t[:, :L.d_a] for t, L in zip(dgr, layers)]
-    step = KfacStep(layers, batch, device=dev)
-    torch.cuda.synchronize()
-
-    # eager warm-up (also sizes and caches the workspaces)
-    for _ in range(max(args.warmup, 1)):
-        step.run(dx, dg, dgr_v)
-    torch.cuda.synchronize()
-    if args.profile:
-        torch.cuda.nvtx.range_push("kfac_step")
-        for _ in range(args.steps):
-            step.run(dx, dg, dgr_v)
-        torch.cuda.nvtx.range_pop()
-        torch.cuda.synchronize()
-        print(json.dumps({"profile": args.workload, "steps": args.steps,
-                          "info_ok": int(step.info.abs().sum().item()) == 0}), flush=True)
-        return 0
-    n0 = kfac.launch_count()
-    step.run(dx, dg, dgr_v)
-    torch.cuda.synchronize()
-    launches_per_step = kfac.launch_count() - n0
-    assert int(step.info.abs().sum().item()) == 0, "an inversion reported a non-positive pivot"
-
-    # per-phase device times (eager), on the launching stream, and every
-    # library kernel timed with CUDA events by the library's timing hooks
-    stream = torch.cuda.current_stream()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    kern = {"factors": {}, "inverse": {}, "precond": {}}
-
-    def add(ph):
-        for name, (t, n) in kfac.timing_read().items():
-            a = kern[ph].setdefault(name, [0.0, 0])
-            a[0] += t
-            a[1] += n
-
-    kfac.timing_enable(True)
-    kfac.timing_read()
-    for k in range(args.steps):
-        ev[k][0].record(stream)
-        step.factor_update(dx, dg)
-        ev[k][1].record(stream)
-        add("factors")
-        step.damp_invert()
-        ev[k][2].record(stream)
-        add("inverse")
-        step.precondition(dgr_v)
-        ev[k][3].record(stream)
-        add("precond")
-    kfac.timing_enable(False)
-    torch.cuda.synchronize()
-    ph = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ev)
-          for i, n in enumerate(("factors", "inverse", "precond"))}
-    eager_ms = statistics.mean(e[0].elapsed_time(e[3]) for e in ev)
-
-    # CUDA graph of one whole step, replayed K times (the timed region)
-    graph = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream()
     side.wait_stream(stream)
     with torch.cuda.stream(side):
-        step.run(dx, dg, dgr_v)
+        fn()
     stream.wait_stream(side)
     torch.cuda.synchronize()
-    with torch.cuda.graph(graph):
-        step.run(dx, dg, dgr_v)
-    for _ in range(args.warmup):
-        graph.replay()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
     torch.cuda.synchronize()
-    clocks = Clocks(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
-    clocks.start()
-    time.sleep(0.3)
-    barrier(world)
+    return g
+
+
+def time_replays(graphs, reps, warmup, stream):
+    """ms per repetition of replaying `graphs` in order (CUDA events on the
+    launching stream, synchronised on both sides)."""
+    import torch
+    for _ in range(warmup):
+        for g in graphs:
+            g.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_wall = time.perf_counter()
     e0.record(stream)
-    for _ in range(args.steps):
-        graph.replay()
+    for _ in range(reps):
+        for g in graphs:
+            g.replay()
     e1.record(stream)
     torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall
-    barrier(world)
-    clk = clocks.stop()
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    return e0.elapsed_time(e1) / reps
 
-    # end to end through the C ABI with host buffers: every step copies its
-    # inputs (one pinned H2D of the packed buffer) and reads back every
-    # preconditioned gradient (one D2H); the H2D and the D2H run on two more
-    # streams, double buffered, so step k's copies overlap the compute of its
-    # neighbours and each other (the host link carries both directions at once)
+
+def measure(name, steps, warmup, dev, pk, kernels=True):
+    """Graph-timed step and phases of one workload, plus the library's
+    per-launch event timings (eager).  Returns a dict and the live objects."""
+    import torch
+
+    from second_order_optimisation_gb300 import kfac
+    from second_order_optimisation_gb300.step import KfacStep
+    layers, batch = workload(name)
+    inp = Inputs(layers, batch, dev)
+    dx, dg, dgr = inp.views
+    step = KfacStep(layers, batch, device=dev)
+    torch.cuda.synchronize()
+    for _ in range(max(warmup, 1)):
+        step.run(dx, dg, dgr)
+    torch.cuda.synchronize()
+    n0 = kfac.launch_count()
+    step.run(dx, dg, dgr)
+    torch.cuda.synchronize()
+    launches = kfac.launch_count() - n0
+    assert int(step.info.abs().sum().item()) == 0, "an inversion reported a failing pivot"
+    stream = torch.cuda.current_stream()
+    kern = {"factors": {}, "inverse": {}, "precond": {}}
+    if kernels:
+        def add(ph):
+            for kname, (t, n) in kfac.timing_read().items():
+                a = kern[ph].setdefault(kname, [0.0, 0])
+                a[0] += t
+                a[1] += n
+        kfac.timing_enable(True)
+        kfac.timing_read()
+        for _ in range(steps):
+            step.factor_update(dx, dg)
+            add("factors")
+            step.damp_invert()
+            add("inverse")
+            step.precondition(dgr)
+            add("precond")
+        kfac.timing_enable(False)
+        torch.cuda.synchronize()
+    g_step = graph_of(lambda: step.run(dx, dg, dgr), stream)
+    g_fac = graph_of(lambda: step.factor_update(dx, dg), stream)
+    g_inv = graph_of(lambda: step.damp_invert(), stream)
+    g_pc = graph_of(lambda: step.precondition(dgr), stream)
+    phases = {"factors": time_replays([g_fac], steps, warmup, stream),
+              "inverse": time_replays([g_inv], steps, warmup, stream),
+              "precond": time_replays([g_pc], steps, warmup, stream)}
+    return dict(layers=layers, batch=batch, inp=inp, step=step, stream=stream, launches=launches, kern=kern,
+                graphs=dict(step=g_step, precond=g_pc), phases=phases)
+
+
+def schedule_amortised(m, steps, warmup):
+    """Amortised ms per step of the stale-factor schedule: a refresh step
+    (the whole step graph) followed by k - 1 precondition-only steps,
+    replayed in that pattern."""
+    out = {}
+    for k in SCHEDULE_KS:
+        cycles = max(1, -(-steps // k))
+        pattern = [m["graphs"]["step"]] + [m["graphs"]["precond"]] * (k - 1)
+        out[f"k{k}"] = time_replays(pattern, cycles, max(1, warmup // k), m["stream"]) / k
+    return out
+
+
+def e2e_time(m, steps, world, dev):
+    """Same step with the inputs copied from pinned host memory (one H2D of
+    the packed buffer) and all preconditioned gradients copied back (one D2H)
+    inside the timed region: torch copies on two copy streams around the
+    library calls (the C ABI itself takes device pointers), double-buffered
+    so step k's copies overlap the compute of its neighbours."""
+    import torch
+    step, inp, stream, layers = m["step"], m["inp"], m["stream"], m["layers"]
     out_sizes = [s.out.numel() for s in step.state]
     out_dev = [torch.empty(sum(out_sizes), device=dev) for _ in range(2)]
     out_host = torch.empty(sum(out_sizes)).pin_memory()
@@ -448,14 +472,10 @@ def run_ours(args, world, rank, local):
             vs.append(od[o:o + n].view(s_.out.shape))
             o += n
         out_views.append(vs)
-    dbufs = [dbuf, torch.empty_like(dbuf)]
-    in_views = []
-    for db in dbufs:
-        vv = [db[o:o + int(np.prod(shp)) * 2].view(torch.bfloat16).view(shp) for (o, shp) in slots]
-        in_views.append((vv[0::3], vv[1::3], [t[:, :L.d_a] for t, L in zip(vv[2::3], layers)]))
-    out_bytes = out_dev[0].numel() * 4
-    copy = torch.cuda.Stream()
-    copy_out = torch.cuda.Stream()
+    keep = [s_.out for s_ in step.state]
+    dbufs = [inp.dbuf, torch.empty_like(inp.dbuf)]
+    in_views = [inp.device_views(db) for db in dbufs]
+    copy, copy_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
@@ -464,15 +484,15 @@ def run_ours(args, world, rank, local):
     f0.record(stream)
     copy.wait_stream(stream)
     with torch.cuda.stream(copy):
-        dbufs[0].copy_(hbuf, non_blocking=True)
+        dbufs[0].copy_(inp.hbuf, non_blocking=True)
         ev_in[0].record(copy)
-    for k in range(args.steps):
+    for k in range(steps):
         b = k % 2
-        if k + 1 < args.steps:
+        if k + 1 < steps:
             with torch.cuda.stream(copy):
                 if k >= 1:
                     copy.wait_event(ev_done[1 - b])     # step k-1 no longer reads that buffer
-                dbufs[1 - b].copy_(hbuf, non_blocking=True)
+                dbufs[1 - b].copy_(inp.hbuf, non_blocking=True)
                 ev_in[1 - b].record(copy)
         stream.wait_event(ev_in[b])
         if k >= 2:
@@ -490,34 +510,99 @@ def run_ours(args, world, rank, local):
     stream.wait_stream(copy_out)
     f1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / args.steps, world, dev)
+    for s_, o in zip(step.state, keep):
+        s_.out = o
+    return f0.elapsed_time(f1) / steps, inp.nbytes, out_dev[0].numel() * 4
 
-    # BatchNorm diagonal Fisher of the 53 BN layers, per-sample scale and
-    # shift gradients [1024, C] fp32 (the large-mini-batch accumulation case)
-    bn_line = bn_bench(args, dev, stream, pk) if args.workload == "resnet50" else None
 
-    # per-kernel rooflines from the live event timings; the dominant kernel
-    # (largest share of the step's device time) goes in "roofline"
-    kernels = kernel_rooflines(kern, layers, batch, fl, pk, args.steps)
-    dom_name = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
-    roof = dict(kernels[dom_name])
-    roof["kernel"] = dom_name
-    phase_share = {k: v / sum(ph.values()) for k, v in ph.items()}
-    phases = {n: {"ms": ph[n], "share": phase_share[n]} for n in ph}
+def subrecord(name, steps, warmup, dev, pk, sm_mhz):
+    """Graph-timed step and phases of another workload, with the SYRK and
+    preconditioner rooflines (as sub-records of the main line)."""
+    m = measure(name, steps, warmup, dev, pk)
+    ms = time_replays([m["graphs"]["step"]], steps, warmup, m["stream"])
+    fl = flops(m["layers"], m["batch"])
+    ks = kernel_rooflines(m["kern"], kernel_work(m["layers"], m["batch"], fl, pk, sm_mhz), steps)
+    keep = ("tc_gemm_bf16@factors", "tc_gemm_bf16@precond", "tc_gemm_tf32x3@inverse", "inv_diag@inverse")
+    return {"workload": f"{name}_kfac_step", "ms": ms, "tflops": fl["total"] / (ms * 1e-3) / 1e12,
+            "phases_ms": m["phases"], "gpu_launches_per_step": m["launches"],
+            "kernels": {k: ks[k] for k in keep if k in ks}}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    m = measure(args.workload, args.steps, args.warmup, dev, pk)
+    layers, batch, stream = m["layers"], m["batch"], m["stream"]
+    fl = flops(layers, batch)
+    if args.profile:
+        torch.cuda.nvtx.range_push("kfac_step")
+        for _ in range(args.steps):
+            m["step"].run(*m["inp"].views)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": args.workload, "steps": args.steps,
+                          "info_ok": int(m["step"].info.abs().sum().item()) == 0}), flush=True)
+        return 0
+
+    # the timed region: K replays of the whole-step graph, clocks sampled meanwhile
+    g = m["graphs"]["step"]
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    clocks = Clocks(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall = time.perf_counter()
+    e0.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    clk = clocks.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+
+    e2e_ms, h2d, d2h = e2e_time(m, args.steps, world, dev)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    sched = schedule_amortised(m, max(args.steps, max(SCHEDULE_KS)), args.warmup)
+
+    kernels = kernel_rooflines(m["kern"], kernel_work(layers, batch, fl, pk, clk.get("sm_mhz")), args.steps)
+    dom = max((k for k in kernels if "frac" in kernels[k]), key=lambda k: kernels[k]["ms_per_step"])
+    roof = dict(kernels[dom])
+    roof["kernel"] = dom
+    phases = {n: {"ms": v, "share": v / sum(m["phases"].values())} for n, v in m["phases"].items()}
+
+    subs = None
+    bn_line = None
+    if args.workload == "resnet50" and not args.no_subrecords:
+        subs = {n: subrecord(n, min(args.steps, 10), min(args.warmup, 3), dev, pk, clk.get("sm_mhz"))
+                for n in ("fc4096", "conv3x3_256")}
+        bn_line = bn_bench(args, dev, stream, pk)
 
     line = {"metric": METRIC, "value": ms, "unit": "ms", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; ResNet-50 shapes, no ImageNet)",
             "config": {"workload": f"{args.workload}_kfac_step", "layers": len(layers), "batch_per_gpu": batch,
-                       "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB per step), no flush",
-                       "graph": True, "xi": 0.95, "gamma": 1e-3},
+                       "l2": f"inputs larger than L2 ({m['inp'].nbytes / 1e6:.0f} MB per step), no flush",
+                       "graph": True, "xi": 0.95, "gamma": 1e-3, "inversion": "fp32 (3 tf32 products)"},
             "tflops": fl["total"] / (ms * 1e-3) / 1e12, "gflop_per_step": fl["total"] / 1e9,
-            "eager_ms": eager_ms, "phases": phases, "roofline": roof, "kernels": kernels,
-            "clocks": clk, "gpu_launches": launches_per_step * args.steps, "bn_fisher": bn_line,
-            "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": in_bytes,
-                    "d2h_bytes_per_step": out_bytes,
-                    "how": "C ABI calls with host buffers; per step one pinned H2D of the packed inputs and "
-                           "one D2H of all preconditioned gradients, double-buffered on two copy streams (H2D, D2H)"},
+            "phases": phases, "schedule_amortised_ms": sched, "roofline": roof, "kernels": kernels,
+            "clocks": clk, "gpu_launches": m["launches"] * args.steps, "gpu_launches_per_step": m["launches"],
+            "bn_fisher": bn_line, "subrecords": subs,
+            "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "how": "the library's calls on device buffers, with torch copies of pinned host buffers "
+                           "inside the timed region: per step one H2D of the packed inputs and one D2H of "
+                           "all preconditioned gradients, double-buffered on two copy streams"},
             "wall_s_timed": t_wall}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(layers, batch)
@@ -545,16 +630,7 @@ def bn_bench(args, dev, stream, pk, nsamples=1024):
     graph = torch.cuda.CUDAGraph()                   # one launch per replay, no host overhead inside
     with torch.cuda.graph(graph):
         kfac.kfac_bn_diag_fisher(items, 1e-3)
-    for _ in range(args.warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        graph.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = time_replays([graph], args.steps, args.warmup, stream)
     gbs = (read + written) / (ms * 1e-3) / 1e9
     return {"layers": len(chans), "tensors": len(items), "n_samples": nsamples, "ms": ms,
             "bytes": read + written, "achieved_gbs": gbs, "peak_gbs": pk["hbm"], "frac": gbs / pk["hbm"],
@@ -567,8 +643,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="resnet50")
+    ap.add_argument("--workload", default="resnet50", choices=("resnet50", "conv3x3_256", "fc4096"))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-subrecords", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="eager warm-up, then --steps eager steps inside the NVTX range 'kfac_step' "
                          "(for ncu --nvtx-include kfac_step/); prints no bench line")

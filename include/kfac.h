@@ -37,14 +37,26 @@
  *     bf16 values are passed as uint16_t bit patterns.
  *   - Device error word: the first int32 of the workspace of
  *     kfac_factor_update, kfac_damp_invert and kfac_precondition.  Each call
- *     sets it to 0 on its stream before its kernels; every wait of a kernel
- *     on a shared-memory barrier has a time limit (about 2 s), and a wait
- *     that runs out ORs a bit into the word (1, 2, 4: the tensor-core engine's
- *     operand, stage and accumulator waits; 8: an inversion leaf's block-step
- *     waits) and the kernel winds down without trapping.  A nonzero word after
- *     the stream has been synchronised means that call's outputs are
- *     undefined.  The call's return status cannot report it (the kernels run
- *     after the call returns).
+ *     sets it to 0 on its stream before its kernels; its kernels OR bits into
+ *     it, which the caller reads after synchronising the stream (the call's
+ *     return status cannot report them: the kernels run after it returns):
+ *       KFAC_ERRW_NONFINITE (16): a value the call wrote to an output (a
+ *         factor, an inverse or one of the inversion's intermediate blocks,
+ *         a preconditioned gradient, an updated weight) is NaN or infinite --
+ *         e.g. the input held NaN/Inf or the statistic overflowed fp32 --
+ *         or an entry of the upper triangle of a factor that
+ *         kfac_damp_invert reads is.  The values are written as computed
+ *         (NaN stays NaN); nothing is clamped.  Layers of the same call whose
+ *         inputs are finite are not affected, but the bit does not say which
+ *         layer it was (kfac_damp_invert's info does, per factor).
+ *       1, 2, 4 (KFAC_ERRW_TIMEOUT_*): a wait of the tensor-core engine on a
+ *         shared-memory barrier (operand stage, free stage, accumulator) ran
+ *         past its limit (about 2 s; never expected in a healthy run).  The
+ *         CTA then stops issuing work, waits (bounded) for the copies and
+ *         products it already issued, releases its tensor memory and exits
+ *         without trapping; 8 is set when that drain wait ran out too.  The
+ *         call's outputs are then undefined.
+ *     A word of 0 means no kernel of the call saw either condition.
  */
 #ifndef KFAC_GB300_H
 #define KFAC_GB300_H
@@ -65,7 +77,27 @@ typedef enum {
     KFAC_ERR_WORKSPACE = 5     /* workspace missing, misaligned or too small      */
 } kfac_status;
 
-typedef enum { KFAC_BF16 = 0, KFAC_F32 = 1 } kfac_dtype;
+typedef enum { KFAC_BF16 = 0, KFAC_F32 = 1, KFAC_F16 = 2 } kfac_dtype;
+
+/* Storage of a symmetric fp32 factor (only its upper triangle is stored or
+ * read):
+ *   KFAC_LAYOUT_FULL          row-major [d][ld], entry (i, j) at F[i*ld + j];
+ *   KFAC_LAYOUT_PACKED_UPPER  the upper triangle row after row, d(d+1)/2
+ *                             floats: entry (i, j), i <= j, at
+ *                             F[i*d - i*(i+1)/2 + j]  (row i holds j = i..d-1);
+ *                             the ld argument is ignored.
+ * The packed form halves a factor's footprint (Osawa et al. section 1: the
+ * symmetry of the Kronecker factors is exploited to reduce overhead). */
+typedef enum { KFAC_LAYOUT_FULL = 0, KFAC_LAYOUT_PACKED_UPPER = 1 } kfac_layout;
+
+/* Bits of the device error word (see above). */
+enum {
+    KFAC_ERRW_TIMEOUT_OPERAND = 1,
+    KFAC_ERRW_TIMEOUT_STAGE = 2,
+    KFAC_ERRW_TIMEOUT_ACCUM = 4,
+    KFAC_ERRW_TIMEOUT_DRAIN = 8,
+    KFAC_ERRW_NONFINITE = 16
+};
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *kfac_status_string(int status);
@@ -113,11 +145,16 @@ const char *kfac_timing_kind_name(int k);
  * h = w = kh = kw = stride = 1, pad = 0, n = M rows.
  *
  * Fields:
- *   dtype   KFAC_BF16 (tensor-core path) or KFAC_F32 (fp32 CUDA-core path)
+ *   dtype   KFAC_BF16 or KFAC_F16 (tensor cores, fp32 accumulation; the
+ *           paper computes in half precision) or KFAC_F32 (fp32 CUDA cores)
  *   x       device, dense NHWC [n][h][w][c] of dtype (channel stride 1)
- *   F, ldf  device fp32 [d][ldf], ldf >= d; upper triangle updated
+ *   F, ldf  device fp32 factor in `layout`: KFAC_LAYOUT_FULL [d][ldf] with
+ *           ldf >= d, or KFAC_LAYOUT_PACKED_UPPER (d(d+1)/2 floats, ldf
+ *           ignored); its upper triangle is updated
+ *   layout  kfac_layout of F (a trailing field: zero-initialised = FULL)
  * Errors: INVALID for null x/F, n,h,w,c,kh,kw,stride < 1, pad < 0, Ho/Wo < 1,
- *   ldf < d; UNSUPPORTED for d > 65536 or more than 2^31 rows.
+ *   ldf < d (full layout), an unknown dtype or layout; UNSUPPORTED for
+ *   d > 65536 or more than 2^31 rows.
  * Workspace: kfac_factor_update_workspace_size(descs, count) bytes.
  * ==================================================================== */
 typedef struct {
@@ -129,6 +166,7 @@ typedef struct {
     float *F;
     int64_t ldf;
     float alpha, beta;
+    int32_t layout;
 } kfac_factor_desc;
 
 size_t kfac_factor_update_workspace_size(const kfac_factor_desc *descs, int count);
@@ -144,24 +182,27 @@ kfac_status kfac_factor_update(const kfac_factor_desc *descs, int count,
  *     pi = sqrt((tr A / dA) / (tr G / dG)),
  *     damp_A = pi * sqrt(gamma),  damp_G = sqrt(gamma) / pi      (pi_split != 0)
  *     damp_A = damp_G = sqrt(gamma)                              (pi_split == 0)
- * and writes the FULL symmetric fp32 inverses
+ * and writes the FULL symmetric fp32 inverses (both triangles, exactly
+ * symmetric)
  *     A_inv = (A + damp_A I)^-1,  G_inv = (G + damp_G I)^-1
- * computed in fp32 by block elimination: Schur complements on tensor cores
- * (three tf32 products per slice) down to 128 x 128 or 256 x 256 blocks,
- * each inverted by a Gauss-Jordan sweep whose 32-wide block steps are
- * tensor-core products on the block held in tensor memory.  Only the upper
- * triangles of A and G are read.
+ * computed in fp32 through a Cholesky factorisation X = L L^T (left-looking,
+ * 128-wide block columns; each 128 x 128 diagonal block factored and
+ * inverted by one CTA), the triangular inverse W = L^-1 (recursive 2 x 2
+ * blocking) and X^-1 = W^T W.  The block products run on tensor cores as
+ * three tf32 products per slice on (hi, lo) splits of the fp32 operands with
+ * fp32 accumulation.  Only the upper triangles of A and G are read.
  *
- * Streams: the call is ordered on `stream` as a whole.  When its matrices
- * form chains of very different length, the middle part forks onto two
- * library-owned streams of the current device (the longest chains at high
- * priority, the rest at low priority; created on the first such call,
- * with three events) and joins back into `stream` before the final kernel,
- * so stream capture records a graph with two parallel branches.  Make the
- * first call of a process outside stream capture.  Optional bf16 copies of the inverses are
- * written when the *_bf16 pointers are non-NULL (their ld must be a multiple
- * of 8 elements and their base 16-byte aligned, for the tensor-core
- * preconditioner).
+ * Streams: the call is ordered on `stream` as a whole.  Its middle part forks
+ * onto library-owned streams of the current device (the longest chains at
+ * high priority, the rest at low priority; created with their events on the
+ * first call on a device) and joins back into `stream`, so stream capture
+ * records a graph with parallel branches.  Make the first call on a device
+ * outside stream capture.  Optional 16-bit copies of the inverses (bf16, or
+ * fp16 when copy_dtype is KFAC_F16) are written when the *_bf16 pointers are
+ * non-NULL (their ld must be a multiple of 8 elements and their base 16-byte
+ * aligned, for the tensor-core preconditioner).  A and G may be stored in
+ * either kfac_layout (layout_A, layout_G; the lda/ldg of a packed factor are
+ * ignored); the inverses are always full row-major.
  *
  * Device outputs besides the inverses:
  *   info   int32 [2*count] (may be NULL): info[2l] for A of layer l,
@@ -170,8 +211,9 @@ kfac_status kfac_factor_update(const kfac_factor_desc *descs, int count,
  *          corresponding inverse is then undefined.  The call itself still
  *          returns KFAC_OK: read info after synchronising the stream.
  *   damp   float [2*count] (may be NULL): the damp_A, damp_G applied.
- * Errors: INVALID for null A/G/A_inv/G_inv, dA/dG < 1, ld < d, gamma < 0;
- *   UNSUPPORTED for d > 16384 or a bf16 ld not a multiple of 8.
+ * Errors: INVALID for null A/G/A_inv/G_inv, dA/dG < 1, ld < d (full layouts
+ *   and the outputs), gamma < 0, an unknown layout or copy_dtype;
+ *   UNSUPPORTED for d > 16384 or a 16-bit copy's ld not a multiple of 8.
  * Workspace: kfac_damp_invert_workspace_size(descs, count) bytes.
  * ==================================================================== */
 typedef struct {
@@ -179,8 +221,10 @@ typedef struct {
     const float *G; int32_t dG; int64_t ldg;
     float *A_inv; int64_t ld_ainv;
     float *G_inv; int64_t ld_ginv;
-    uint16_t *A_inv_bf16; int64_t ld_ainv_bf16;   /* optional */
-    uint16_t *G_inv_bf16; int64_t ld_ginv_bf16;   /* optional */
+    uint16_t *A_inv_bf16; int64_t ld_ainv_bf16;   /* optional 16-bit copy */
+    uint16_t *G_inv_bf16; int64_t ld_ginv_bf16;   /* optional 16-bit copy */
+    int32_t layout_A, layout_G;                   /* kfac_layout of A and G */
+    int32_t copy_dtype;                           /* KFAC_BF16 (0) or KFAC_F16 */
 } kfac_invert_desc;
 
 size_t kfac_damp_invert_workspace_size(const kfac_invert_desc *descs, int count);
@@ -198,9 +242,17 @@ kfac_status kfac_damp_invert(const kfac_invert_desc *descs, int count, float gam
  * dtype KFAC_BF16: G_inv, A_inv, grad are bf16 (tensor cores, fp32
  *   accumulation; the intermediate grad*A_inv is rounded to bf16); each ld
  *   must be a multiple of 8 and each base 16-byte aligned.
+ * dtype KFAC_F16: the same with fp16 operands (the intermediate is rounded
+ *   to fp16).
  * dtype KFAC_F32: all operands fp32 (CUDA cores).
- * Errors: INVALID for null pointers, d < 1, ld < width; UNSUPPORTED for a
- *   bf16 ld/alignment violation or d > 65536.
+ * Fused step on the weights (Osawa et al. section 3.2, Eq. 8): when w is not
+ *   NULL, the epilogue of the second product also applies
+ *       w <- w - eta * out               (w fp32 [dG][ld_w], in place)
+ *   with the fp32 value of out before it is stored; out may then be NULL
+ *   (the preconditioned gradient is not kept).  w must not overlap any other
+ *   operand.  Zero-initialised trailing fields (w = NULL) leave w alone.
+ * Errors: INVALID for null G_inv/A_inv/grad, both out and w NULL, d < 1,
+ *   ld < width; UNSUPPORTED for a bf16 ld/alignment violation or d > 65536.
  * Workspace: kfac_precondition_workspace_size(descs, count, dtype) bytes.
  * ==================================================================== */
 typedef struct {
@@ -208,7 +260,9 @@ typedef struct {
     const void *G_inv; int64_t ld_ginv;
     const void *A_inv; int64_t ld_ainv;
     const void *grad;  int64_t ld_grad;
-    float *out;        int64_t ld_out;
+    float *out;        int64_t ld_out;    /* may be NULL when w is set */
+    float *w;          int64_t ld_w;      /* optional: the layer's weights */
+    float eta;                            /* learning rate of the step on w */
 } kfac_precond_desc;
 
 size_t kfac_precondition_workspace_size(const kfac_precond_desc *descs, int count, int dtype);

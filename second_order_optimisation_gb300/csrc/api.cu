@@ -13,6 +13,11 @@
 
 #include "internal.h"
 
+static_assert(kfac::ERR_TIMEOUT_FULL == KFAC_ERRW_TIMEOUT_OPERAND && kfac::ERR_TIMEOUT_EMPTY == KFAC_ERRW_TIMEOUT_STAGE &&
+                  kfac::ERR_TIMEOUT_ACC == KFAC_ERRW_TIMEOUT_ACCUM && kfac::ERR_TIMEOUT_DRAIN == KFAC_ERRW_TIMEOUT_DRAIN &&
+                  kfac::ERR_NONFINITE == KFAC_ERRW_NONFINITE,
+              "device error word bits match the public header");
+
 namespace kfac {
 
 static std::atomic<long long> g_launches{0};
@@ -119,7 +124,7 @@ bool geom_of(const kfac_factor_desc &d, FactorGeom &g) {
     g.M = (long long)d.n * g.ho * g.wo;
     g.dcore = d.kh * d.kw * d.c;
     g.d = g.dcore + (d.append_one ? 1 : 0);
-    g.direct = d.dtype == KFAC_BF16 && d.kh == 1 && d.kw == 1 && d.stride_h == 1 &&
+    g.direct = d.dtype != KFAC_F32 && d.kh == 1 && d.kw == 1 && d.stride_h == 1 &&
                d.stride_w == 1 && d.pad_h == 0 && d.pad_w == 0 && d.c % 8 == 0 &&
                ((uintptr_t)d.x % 16) == 0;
     return true;
@@ -131,13 +136,14 @@ kfac_status validate_factor(const kfac_factor_desc *descs, int count, std::vecto
     for (int i = 0; i < count; ++i) {
         const kfac_factor_desc &d = descs[i];
         if (!d.x || !d.F) return KFAC_ERR_INVALID;
-        if (d.dtype != KFAC_BF16 && d.dtype != KFAC_F32) return KFAC_ERR_INVALID;
+        if (d.dtype != KFAC_BF16 && d.dtype != KFAC_F32 && d.dtype != KFAC_F16) return KFAC_ERR_INVALID;
+        if (d.layout != KFAC_LAYOUT_FULL && d.layout != KFAC_LAYOUT_PACKED_UPPER) return KFAC_ERR_INVALID;
         if (d.n < 1 || d.h < 1 || d.w < 1 || d.c < 1 || d.kh < 1 || d.kw < 1 || d.stride_h < 1 ||
             d.stride_w < 1 || d.pad_h < 0 || d.pad_w < 0)
             return KFAC_ERR_INVALID;
         if (!std::isfinite(d.alpha) || !std::isfinite(d.beta)) return KFAC_ERR_INVALID;
         if (!geom_of(d, geo[i])) return KFAC_ERR_INVALID;
-        if (d.ldf < geo[i].d) return KFAC_ERR_INVALID;
+        if (d.layout == KFAC_LAYOUT_FULL && d.ldf < geo[i].d) return KFAC_ERR_INVALID;
         if (geo[i].d > 65536 || geo[i].M >= (1LL << 31)) return KFAC_ERR_UNSUPPORTED;
         // a materialised patch matrix is indexed with 32-bit element counts
         if (!geo[i].direct && geo[i].M * (long long)(geo[i].d + 8) >= (1LL << 31)) return KFAC_ERR_UNSUPPORTED;
@@ -147,10 +153,11 @@ kfac_status validate_factor(const kfac_factor_desc *descs, int count, std::vecto
 
 // Everything the factor update enqueues, laid out in one arena.
 struct FactorPlan {
-    std::vector<Im2colJob> im16, im32;
+    std::vector<Im2colJob> im16, imh, im32;  // bf16, fp16, fp32 patch matrices
     std::vector<TcJob> tc;
     std::vector<SgJob> sg;
     std::vector<ColsumJob> cs;
+    float *cs_partial = nullptr;
     int *err = nullptr;
     char *tc_ws = nullptr;
     size_t tc_bytes = 0;
@@ -164,12 +171,14 @@ struct FactorPlan {
 kfac_status plan_factor(const kfac_factor_desc *descs, int count, const std::vector<FactorGeom> &geo,
                         Arena &ws, FactorPlan &p, bool encode) {
     p.err = ws.take<int>(64);
-    int nbf16 = 0;
-    for (int i = 0; i < count; ++i) nbf16 += descs[i].dtype == KFAC_BF16;
-    p.dev_maps = ws.take<CUtensorMap>(std::max(nbf16, 1));
+    int n16 = 0;
+    for (int i = 0; i < count; ++i) n16 += descs[i].dtype != KFAC_F32;
+    p.dev_maps = ws.take<CUtensorMap>(std::max(n16, 1));
     for (int i = 0; i < count; ++i) {
         const kfac_factor_desc &d = descs[i];
         const FactorGeom &g = geo[i];
+        const bool packed = d.layout == KFAC_LAYOUT_PACKED_UPPER;
+        const bool f16 = d.dtype == KFAC_F16;
         if (d.dtype == KFAC_F32) {
             // fp32 path: explicit patches (with the ones column) + CUDA-core SYRK
             const long long ldp = g.d;
@@ -177,7 +186,7 @@ kfac_status plan_factor(const kfac_factor_desc *descs, int count, const std::vec
             p.im32.push_back(Im2colJob{d.x, d.n, d.h, d.w, d.c, d.kh, d.kw, d.stride_h, d.stride_w,
                                        d.pad_h, d.pad_w, g.ho, g.wo, d.append_one, P, ldp});
             p.sg.push_back(SgJob{P, ldp, 1, P, ldp, 0, d.F, d.ldf, nullptr, 0, g.d, g.d, (int)g.M,
-                                 d.alpha, d.beta, 1});
+                                 d.alpha, d.beta, 1, nullptr, 0, 0.f, packed ? g.d : 0});
             continue;
         }
         // a convolution whose channels fill 64-wide taps is read straight
@@ -190,7 +199,8 @@ kfac_status plan_factor(const kfac_factor_desc *descs, int count, const std::vec
             TcJob j{};
             j.map_a = j.map_b = (int)p.maps.size();
             p.maps.emplace_back();
-            if (encode && !tc_make_im2col_map(&p.maps.back(), d.x, d.n, d.h, d.w, d.c, d.kh, d.stride_h, d.pad_h))
+            if (encode &&
+                !tc_make_im2col_map(&p.maps.back(), d.x, d.n, d.h, d.w, d.c, d.kh, d.stride_h, d.pad_h, f16))
                 return KFAC_ERR_CUDA;
             j.a_mn = j.b_mn = 1;
             j.M = g.dcore; j.N = g.dcore; j.K = (int)g.M;
@@ -201,6 +211,8 @@ kfac_status plan_factor(const kfac_factor_desc *descs, int count, const std::vec
             j.im2col = 1;
             j.im_c = d.c; j.im_k = d.kh; j.im_stride = d.stride_h; j.im_pad = d.pad_h;
             j.im_wo = g.wo; j.im_howo = g.ho * g.wo;
+            j.f16 = f16;
+            j.packed = packed; j.packed_d = g.d;
             p.tc.push_back(j);
             continue;
         }
@@ -212,14 +224,14 @@ kfac_status plan_factor(const kfac_factor_desc *descs, int count, const std::vec
         } else {
             lds = (g.dcore + 7) / 8 * 8;
             uint16_t *P = ws.take<uint16_t>((size_t)g.M * lds);
-            p.im16.push_back(Im2colJob{d.x, d.n, d.h, d.w, d.c, d.kh, d.kw, d.stride_h, d.stride_w,
-                                       d.pad_h, d.pad_w, g.ho, g.wo, 0, P, lds});
+            (f16 ? p.imh : p.im16).push_back(Im2colJob{d.x, d.n, d.h, d.w, d.c, d.kh, d.kw, d.stride_h,
+                                                        d.stride_w, d.pad_h, d.pad_w, g.ho, g.wo, 0, P, lds});
             src = P;
         }
         TcJob j{};
         j.map_a = j.map_b = (int)p.maps.size();
         p.maps.emplace_back();
-        if (encode && !tc_make_map(&p.maps.back(), TC_KIND_BF16, src, lds, (int)g.M, g.dcore))
+        if (encode && !tc_make_map(&p.maps.back(), TC_KIND_BF16, src, lds, (int)g.M, g.dcore, 0, f16))
             return KFAC_ERR_CUDA;
         j.a_mn = j.b_mn = 1;
         j.M = g.dcore; j.N = g.dcore; j.K = (int)g.M;
@@ -227,14 +239,17 @@ kfac_status plan_factor(const kfac_factor_desc *descs, int count, const std::vec
         j.epi = TC_EPI_ACCUM;
         j.alpha = d.alpha; j.beta = d.beta;
         j.C = d.F; j.ldc = d.ldf;
+        j.f16 = f16;
+        j.packed = packed; j.packed_d = g.d;
         p.tc.push_back(j);
         if (d.append_one) {
             // bias row/column: needs the source rows [M][c]; an FC layer has
             // h = w = kh = kw = 1 so the source is x itself
             if (!(d.kh == 1 && d.kw == 1 && d.h == 1 && d.w == 1)) return KFAC_ERR_UNSUPPORTED;
-            p.cs.push_back(ColsumJob{(const uint16_t *)d.x, g.M, d.c, d.F, d.ldf, d.alpha, d.beta});
+            p.cs.push_back(ColsumJob{(const uint16_t *)d.x, g.M, d.c, d.F, d.ldf, d.alpha, d.beta, f16, packed});
         }
     }
+    p.cs_partial = ws.take<float>(std::max<size_t>(colsum_partial_floats(p.cs.data(), (int)p.cs.size()), 1));
     p.tc_bytes = tc_workspace_bytes(p.tc.data(), (int)p.tc.size(), TC_KIND_BF16);
     p.tc_ws = ws.take<char>(p.tc_bytes);
     return KFAC_OK;
@@ -269,9 +284,9 @@ extern "C" int kfac_timing_enable(int on) {
 }
 
 extern "C" const char *kfac_timing_kind_name(int k) {
-    static const char *names[KK_COUNT] = {"tc_gemm_bf16", "tc_gemm_tf32x3", "inv_leaf", "inv_prep",
-                                          "inv_finish", "damping", "im2col", "colsum", "sgemm_f32",
-                                          "bn_fisher", "map_copy"};
+    static const char *names[KK_COUNT] = {"tc_gemm_bf16", "tc_gemm_tf32x3", "inv_diag", "inv_prep",
+                                          "damping", "im2col", "colsum", "sgemm_f32", "bn_fisher",
+                                          "map_copy"};
     return (k >= 0 && k < KK_COUNT) ? names[k] : "";
 }
 
@@ -327,6 +342,8 @@ extern "C" kfac_status kfac_factor_update(const kfac_factor_desc *descs, int cou
     KFAC_CUDA_TRY(cudaMemsetAsync(p.err, 0, sizeof(int), st));
     if (!p.im16.empty() && (s = im2col_run(p.im16.data(), (int)p.im16.size(), KFAC_BF16, st)) != KFAC_OK)
         return s;
+    if (!p.imh.empty() && (s = im2col_run(p.imh.data(), (int)p.imh.size(), KFAC_F16, st)) != KFAC_OK)
+        return s;
     if (!p.im32.empty() && (s = im2col_run(p.im32.data(), (int)p.im32.size(), KFAC_F32, st)) != KFAC_OK)
         return s;
     if (!p.tc.empty()) {
@@ -334,8 +351,8 @@ extern "C" kfac_status kfac_factor_update(const kfac_factor_desc *descs, int cou
         if ((s = tc_run(p.tc.data(), (int)p.tc.size(), TC_KIND_BF16, p.dev_maps, tail, p.err, st)) != KFAC_OK)
             return s;
     }
-    if (!p.sg.empty() && (s = sg_run(p.sg.data(), (int)p.sg.size(), st)) != KFAC_OK) return s;
-    if (!p.cs.empty() && (s = colsum_run(p.cs.data(), (int)p.cs.size(), st)) != KFAC_OK) return s;
+    if (!p.sg.empty() && (s = sg_run(p.sg.data(), (int)p.sg.size(), p.err, st)) != KFAC_OK) return s;
+    if (!p.cs.empty() && (s = colsum_run(p.cs.data(), (int)p.cs.size(), p.cs_partial, st)) != KFAC_OK) return s;
     return KFAC_OK;
 }
 
@@ -349,7 +366,11 @@ kfac_status validate_invert(const kfac_invert_desc *descs, int count, float gamm
     for (int i = 0; i < count; ++i) {
         const kfac_invert_desc &d = descs[i];
         if (!d.A || !d.G || !d.A_inv || !d.G_inv) return KFAC_ERR_INVALID;
-        if (d.dA < 1 || d.dG < 1 || d.lda < d.dA || d.ldg < d.dG || d.ld_ainv < d.dA ||
+        const bool pa = d.layout_A == KFAC_LAYOUT_PACKED_UPPER, pg = d.layout_G == KFAC_LAYOUT_PACKED_UPPER;
+        if ((!pa && d.layout_A != KFAC_LAYOUT_FULL) || (!pg && d.layout_G != KFAC_LAYOUT_FULL) ||
+            (d.copy_dtype != KFAC_BF16 && d.copy_dtype != KFAC_F16))
+            return KFAC_ERR_INVALID;
+        if (d.dA < 1 || d.dG < 1 || (!pa && d.lda < d.dA) || (!pg && d.ldg < d.dG) || d.ld_ainv < d.dA ||
             d.ld_ginv < d.dG)
             return KFAC_ERR_INVALID;
         if ((d.A_inv_bf16 && d.ld_ainv_bf16 < d.dA) || (d.G_inv_bf16 && d.ld_ginv_bf16 < d.dG))
@@ -366,8 +387,11 @@ std::vector<InvMatrix> inv_mats(const kfac_invert_desc *descs, int count) {
     std::vector<InvMatrix> m(2 * count);
     for (int i = 0; i < count; ++i) {
         const kfac_invert_desc &d = descs[i];
-        m[2 * i] = InvMatrix{d.A, d.lda, d.dA, d.A_inv, d.ld_ainv, d.A_inv_bf16, d.ld_ainv_bf16};
-        m[2 * i + 1] = InvMatrix{d.G, d.ldg, d.dG, d.G_inv, d.ld_ginv, d.G_inv_bf16, d.ld_ginv_bf16};
+        const int h = d.copy_dtype == KFAC_F16;
+        m[2 * i] = InvMatrix{d.A, d.lda, d.dA, d.A_inv, d.ld_ainv, d.A_inv_bf16, d.ld_ainv_bf16,
+                             d.layout_A == KFAC_LAYOUT_PACKED_UPPER, h};
+        m[2 * i + 1] = InvMatrix{d.G, d.ldg, d.dG, d.G_inv, d.ld_ginv, d.G_inv_bf16, d.ld_ginv_bf16,
+                                 d.layout_G == KFAC_LAYOUT_PACKED_UPPER, h};
     }
     return m;
 }
@@ -416,15 +440,15 @@ namespace {
 
 kfac_status validate_precond(const kfac_precond_desc *descs, int count, int dtype) {
     if (count < 0 || (count > 0 && !descs)) return KFAC_ERR_INVALID;
-    if (dtype != KFAC_BF16 && dtype != KFAC_F32) return KFAC_ERR_INVALID;
+    if (dtype != KFAC_BF16 && dtype != KFAC_F32 && dtype != KFAC_F16) return KFAC_ERR_INVALID;
     for (int i = 0; i < count; ++i) {
         const kfac_precond_desc &d = descs[i];
-        if (!d.G_inv || !d.A_inv || !d.grad || !d.out) return KFAC_ERR_INVALID;
+        if (!d.G_inv || !d.A_inv || !d.grad || (!d.out && !d.w)) return KFAC_ERR_INVALID;
         if (d.dG < 1 || d.dA < 1 || d.ld_ginv < d.dG || d.ld_ainv < d.dA || d.ld_grad < d.dA ||
-            d.ld_out < d.dA)
+            (d.out && d.ld_out < d.dA) || (d.w && d.ld_w < d.dA))
             return KFAC_ERR_INVALID;
         if (d.dG > 65536 || d.dA > 65536) return KFAC_ERR_UNSUPPORTED;
-        if (dtype == KFAC_BF16 &&
+        if (dtype != KFAC_F32 &&
             (d.ld_ginv % 8 || d.ld_ainv % 8 || d.ld_grad % 8 || (uintptr_t)d.G_inv % 16 ||
              (uintptr_t)d.A_inv % 16 || (uintptr_t)d.grad % 16))
             return KFAC_ERR_UNSUPPORTED;
@@ -445,15 +469,16 @@ struct PrecondPlan {
 kfac_status plan_precond(const kfac_precond_desc *descs, int count, int dtype, Arena &ws, PrecondPlan &p,
                          bool encode) {
     p.err = ws.take<int>(64);
-    if (dtype == KFAC_BF16) p.dev_maps = ws.take<CUtensorMap>(4 * (size_t)count);
+    const bool f16 = dtype == KFAC_F16;
+    if (dtype != KFAC_F32) p.dev_maps = ws.take<CUtensorMap>(4 * (size_t)count);
     auto map = [&](const void *ptr, long long ld, int rows, int cols) {
         p.maps.emplace_back();
-        if (encode && !tc_make_map(&p.maps.back(), TC_KIND_BF16, ptr, ld, rows, cols)) return -1;
+        if (encode && !tc_make_map(&p.maps.back(), TC_KIND_BF16, ptr, ld, rows, cols, 0, f16)) return -1;
         return (int)p.maps.size() - 1;
     };
     for (int i = 0; i < count; ++i) {
         const kfac_precond_desc &d = descs[i];
-        if (dtype == KFAC_BF16) {
+        if (dtype != KFAC_F32) {
             const long long ldt = (d.dA + 7) / 8 * 8;
             uint16_t *T = ws.take<uint16_t>((size_t)d.dG * ldt);
             TcJob a{};  // T = grad * A_inv   (A_inv symmetric: its rows are the columns of B)
@@ -462,13 +487,16 @@ kfac_status plan_precond(const kfac_precond_desc *descs, int count, int dtype, A
             a.M = d.dG; a.N = d.dA; a.K = d.dA;
             a.epi = TC_EPI_STORE; a.alpha = 1.f; a.beta = 0.f;
             a.Cb = T; a.ldcb = ldt;
+            a.f16 = f16; a.cb_f16 = f16;
             TcJob b{};  // out = G_inv * T   (T read MN-major)
             b.map_a = map(d.G_inv, d.ld_ginv, d.dG, d.dG);
             b.map_b = map(T, ldt, d.dG, d.dA);  // read MN-major (b_mn)
             b.b_mn = 1;
             b.M = d.dG; b.N = d.dA; b.K = d.dG;
             b.epi = TC_EPI_STORE; b.alpha = 1.f; b.beta = 0.f;
+            b.f16 = f16;
             b.C = d.out; b.ldc = d.ld_out;
+            b.W = d.w; b.ldw = d.ld_w; b.eta = d.eta;  // Eq. 8, fused into the epilogue
             if (a.map_a < 0 || a.map_b < 0 || b.map_a < 0 || b.map_b < 0) return KFAC_ERR_CUDA;
             p.g1.push_back(a);
             p.g2.push_back(b);
@@ -477,7 +505,7 @@ kfac_status plan_precond(const kfac_precond_desc *descs, int count, int dtype, A
             p.s1.push_back(SgJob{(const float *)d.grad, d.ld_grad, 0, (const float *)d.A_inv, d.ld_ainv, 0,
                                  T, d.dA, nullptr, 0, d.dG, d.dA, d.dA, 1.f, 0.f, 0});
             p.s2.push_back(SgJob{(const float *)d.G_inv, d.ld_ginv, 0, T, d.dA, 0, d.out, d.ld_out,
-                                 nullptr, 0, d.dG, d.dA, d.dG, 1.f, 0.f, 0});
+                                 nullptr, 0, d.dG, d.dA, d.dG, 1.f, 0.f, 0, d.w, d.ld_w, d.eta});
         }
     }
     size_t t1 = tc_workspace_bytes(p.g1.data(), (int)p.g1.size(), TC_KIND_BF16);
@@ -512,7 +540,7 @@ extern "C" kfac_status kfac_precondition(const kfac_precond_desc *descs, int cou
     if ((s = plan_precond(descs, count, dtype, ws, p, true)) != KFAC_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
     KFAC_CUDA_TRY(cudaMemsetAsync(p.err, 0, sizeof(int), st));  // the error word, for every dtype
-    if (dtype == KFAC_BF16) {
+    if (dtype != KFAC_F32) {
         if ((s = tc_upload_maps(p.maps.data(), (int)p.maps.size(), p.dev_maps, st)) != KFAC_OK) return s;
         Arena t_a(p.tc_ws, p.tc_bytes);
         if ((s = tc_run(p.g1.data(), (int)p.g1.size(), TC_KIND_BF16, p.dev_maps, t_a, p.err, st)) != KFAC_OK)
@@ -520,6 +548,6 @@ extern "C" kfac_status kfac_precondition(const kfac_precond_desc *descs, int cou
         Arena t_b(p.tc_ws, p.tc_bytes);
         return tc_run(p.g2.data(), (int)p.g2.size(), TC_KIND_BF16, p.dev_maps, t_b, p.err, st);
     }
-    if ((s = sg_run(p.s1.data(), (int)p.s1.size(), st)) != KFAC_OK) return s;
-    return sg_run(p.s2.data(), (int)p.s2.size(), st);
+    if ((s = sg_run(p.s1.data(), (int)p.s1.size(), p.err, st)) != KFAC_OK) return s;
+    return sg_run(p.s2.data(), (int)p.s2.size(), p.err, st);
 }

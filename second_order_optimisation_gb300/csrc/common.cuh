@@ -10,6 +10,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <utility>
 #include <stdint.h>
@@ -32,7 +33,7 @@ void count_launch();
 
 // Kernel kinds for the optional per-kernel timing (kfac_timing_*).
 enum KernelKind : int {
-    KK_TC_BF16 = 0, KK_TC_TF32X3, KK_LEAF, KK_PREP, KK_FINISH, KK_DAMPING, KK_IM2COL, KK_COLSUM,
+    KK_TC_BF16 = 0, KK_TC_TF32X3, KK_DIAG, KK_PREP, KK_DAMPING, KK_IM2COL, KK_COLSUM,
     KK_SGEMM, KK_BN, KK_MAPCOPY, KK_COUNT
 };
 // Returns a slot (>= 0) after recording a start event on `st` when timing is
@@ -120,7 +121,22 @@ typedef CUresult (*EncodeIm2colFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_
 EncodeIm2colFn encode_im2col_fn();
 
 // Device error word shared by the kernels of one call lives in the workspace.
-enum : int { ERR_TIMEOUT_FULL = 1, ERR_TIMEOUT_EMPTY = 2, ERR_TIMEOUT_ACC = 4, ERR_TIMEOUT_LEAF = 8 };
+// Bits 1, 2, 4: a wait of the tensor-core engine on an operand stage, a free
+// stage or an accumulator ran out; 8: after such a timeout, the wait for the
+// CTA's own copies and products in flight ran out too; 16: an output value
+// was NaN or infinite.
+enum : int {
+    ERR_TIMEOUT_FULL = 1,
+    ERR_TIMEOUT_EMPTY = 2,
+    ERR_TIMEOUT_ACC = 4,
+    ERR_TIMEOUT_DRAIN = 8,
+    ERR_NONFINITE = 16
+};
+
+__device__ __forceinline__ bool finite4(float4 v) {
+    return fabsf(v.x) <= 3.402823466e38f && fabsf(v.y) <= 3.402823466e38f && fabsf(v.z) <= 3.402823466e38f &&
+           fabsf(v.w) <= 3.402823466e38f;
+}
 
 // ---------------------------------------------------------------- device
 
@@ -315,10 +331,10 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t start, uint32_t lbo
 
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 inputs and fp32
 // accumulation.  a_mn / b_mn select MN-major ("transposed") operands.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn, int f16 = 0) {
     return (1u << 4)                      // D format: f32
-           | (1u << 7)                    // A format: bf16
-           | (1u << 10)                   // B format: bf16
+           | ((f16 ? 0u : 1u) << 7)       // A format: f16 (0) or bf16 (1)
+           | ((f16 ? 0u : 1u) << 10)      // B format: the same as A
            | ((uint32_t)a_mn << 15)       // A major (0 = K, 1 = MN)
            | ((uint32_t)b_mn << 16)       // B major
            | ((uint32_t)(N >> 3) << 17)   // N / 8
@@ -341,6 +357,16 @@ __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
     __nv_bfloat16 h = __float2bfloat16_rn(f);
     return *reinterpret_cast<uint16_t *>(&h);
+}
+
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float f) {
+    __half h = __float2half_rn(f);
+    return *reinterpret_cast<uint16_t *>(&h);
+}
+
+// A 16-bit copy of an fp32 value: fp16 bits when f16, else bf16 bits.
+__device__ __forceinline__ uint16_t f32_to_16_bits(float f, bool f16) {
+    return f16 ? f32_to_f16_bits(f) : f32_to_bf16_bits(f);
 }
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {

@@ -54,6 +54,16 @@ struct TcJob {
     long long ldct;
     uint16_t *Cb;
     long long ldcb;
+    int f16;       // BF16 kind: both operands fp16 instead of bf16
+    int cb_f16;    // Cb receives fp16 bits instead of bf16
+    int packed;    // ACCUM: C is a packed upper triangle of a packed_d x packed_d
+                   // matrix (entry (i, j) at C[i*packed_d - i*(i+1)/2 + j]; ldc unused)
+    int packed_d;
+    // STORE epilogue, not symmetric: W[i][j] -= eta * result[i][j] in place
+    // (fp32, row stride ldw); C may then be null
+    float *W;
+    long long ldw;
+    float eta;
     // BF16 SYRK of a convolution read straight from its NHWC input through an
     // im2col tensor map (map_a): K runs over output pixels, the MN index over
     // d = (r * k + s) * c + channel.  c is a multiple of 64.
@@ -66,11 +76,13 @@ struct TcJob {
 // same map serves a K-major and an MN-major operand (the kernel picks the box
 // coordinates).  A tf32x3 operand is a run of four maps: hi and lo with
 // 128-row boxes, then hi and lo with 32-row boxes (B of narrow tiles).
-bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int box_rows = 0);
+bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int box_rows = 0,
+                 bool f16 = false);
 // Im2col tensor map of a bf16 NHWC tensor [n][h][w][c] for a square k x k
 // convolution (stride, pad): 64 channels x 128 output pixels per load,
 // 128-byte swizzle.  Requires c % 64 == 0 and a 16-byte aligned base.
-bool tc_make_im2col_map(CUtensorMap *m, const void *x, int n, int h, int w, int c, int k, int stride, int pad);
+bool tc_make_im2col_map(CUtensorMap *m, const void *x, int n, int h, int w, int c, int k, int stride, int pad,
+                        bool f16 = false);
 // Copies host-built maps into device memory (128-byte aligned) on the stream.
 kfac_status tc_upload_maps(const CUtensorMap *maps, int n, CUtensorMap *dev, cudaStream_t st);
 // Workspace needed by tc_run for these jobs (split-K partials, counters).
@@ -102,8 +114,14 @@ struct SgJob {
     int M, N, K;
     float alpha, beta;
     int upper;
+    float *W;        // W[i][j] -= eta * result[i][j] in place (row stride ldw); C may then be null
+    long long ldw;
+    float eta;
+    int packed_d;    // upper: C is a packed upper triangle of this order (0: row-major, ldc)
 };
-kfac_status sg_run(const SgJob *jobs, int njobs, cudaStream_t st);
+// err: the call's device error word (ERR_NONFINITE is ORed in when a stored
+// value is NaN or infinite), or null
+kfac_status sg_run(const SgJob *jobs, int njobs, int *err, cudaStream_t st);
 
 // ----------------------------------------------------- patches / reductions
 // bf16 or fp32 im2col into P[M][ldp] (columns d..ldp-1 untouched).
@@ -115,6 +133,7 @@ struct Im2colJob {
     void *P;
     long long ldp;
 };
+// dtype KFAC_BF16 / KFAC_F16 (16-bit elements) or KFAC_F32
 kfac_status im2col_run(const Im2colJob *jobs, int njobs, int dtype, cudaStream_t st);
 
 // Bias row/column of an FC factor with append_one: for a bf16 source x[M][c]
@@ -127,8 +146,14 @@ struct ColsumJob {
     float *F;
     long long ldf;
     float alpha, beta;
+    int f16;       // x holds fp16 (else bf16)
+    int packed;    // F is a packed upper triangle of order c + 1 (ldf unused)
 };
-kfac_status colsum_run(const ColsumJob *jobs, int njobs, cudaStream_t st);
+// Column sums of each job in row slabs with partials in `partial` (device,
+// colsum_partial_floats(jobs) floats), then a fixed-order finish: results
+// are bitwise reproducible.
+size_t colsum_partial_floats(const ColsumJob *jobs, int njobs);
+kfac_status colsum_run(const ColsumJob *jobs, int njobs, float *partial, cudaStream_t st);
 
 // ----------------------------------------------------- inversion
 struct InvMatrix {
@@ -139,6 +164,8 @@ struct InvMatrix {
     long long ldo;
     uint16_t *out_bf16;
     long long ldo_bf16;
+    int packed;       // F is a packed upper triangle (ldf unused)
+    int copy_f16;     // out_bf16 receives fp16 bits
 };
 size_t inv_workspace_bytes(const InvMatrix *mats, int nmats);
 // damp[k] (device) is added to the diagonal of matrix k; info[k] receives 0

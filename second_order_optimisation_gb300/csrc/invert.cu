@@ -59,7 +59,7 @@ __device__ __forceinline__ float tf32_hi(float v) {
 struct DampParams {
     const float *A[MAT_MAX / 2];
     const float *G[MAT_MAX / 2];
-    long long lda[MAT_MAX / 2], ldg[MAT_MAX / 2];
+    long long lda[MAT_MAX / 2], ldg[MAT_MAX / 2];  // -1: packed upper triangle
     int dA[MAT_MAX / 2], dG[MAT_MAX / 2];
     int n;
     float gamma;
@@ -74,8 +74,12 @@ __global__ void __launch_bounds__(256) damping_kernel(const __grid_constant__ Da
     __shared__ float ra[256], rg[256];
     const int l = blockIdx.x;
     float ta = 0.f, tg = 0.f;
-    for (int i = threadIdx.x; i < P.dA[l]; i += 256) ta += P.A[l][(long long)i * P.lda[l] + i];
-    for (int i = threadIdx.x; i < P.dG[l]; i += 256) tg += P.G[l][(long long)i * P.ldg[l] + i];
+    // entry (i, i): row-major i*ld + i, or packed i*d - i*(i+1)/2 + i
+    auto diag = [](int i, long long ld, int d) {
+        return ld < 0 ? (long long)i * d - (long long)i * (i + 1) / 2 + i : (long long)i * ld + i;
+    };
+    for (int i = threadIdx.x; i < P.dA[l]; i += 256) ta += P.A[l][diag(i, P.lda[l], P.dA[l])];
+    for (int i = threadIdx.x; i < P.dG[l]; i += 256) tg += P.G[l][diag(i, P.ldg[l], P.dG[l])];
     ra[threadIdx.x] = ta;
     rg[threadIdx.x] = tg;
     __syncthreads();
@@ -107,7 +111,7 @@ __global__ void __launch_bounds__(256) damping_kernel(const __grid_constant__ Da
 
 struct TileMat {
     const float *F;   // factor (upper triangle read)
-    long long ldf;
+    long long ldf;    // -1: packed upper triangle (entry (i, j) at i*d - i*(i+1)/2 + j)
     float *Xh, *Xl;   // working pair [dp][dp]
     int d, dp;
     int damp_idx;
@@ -120,6 +124,7 @@ struct TileParams {
     int begin[MAT_MAX + 1];
     int n;
     const float *damp;
+    int *error;       // the call's error word: ERR_NONFINITE for a NaN / inf factor entry
 };
 
 constexpr int TT = 64;  // prep tile
@@ -151,24 +156,34 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ TileP
     int si, sj;
     const TileMat &q = tile_of(P, si, sj);
     const int tid = threadIdx.x, rr = tid >> 4, c4 = (tid & 15) * 4;
+    bool bad = false;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
         const int r = rr + 16 * p, i = si * TT + r, j = sj * TT + c4;
         float v[4] = {0.f, 0.f, 0.f, 0.f};
         if (i < q.d) {
-            const float *src = q.F + (long long)i * q.ldf + j;
-            if (q.vec_f && j + 3 < q.d) {
+            const bool packed = q.ldf < 0;
+            const float *src =
+                q.F + (packed ? (long long)i * q.d - (long long)i * (i + 1) / 2 : (long long)i * q.ldf) + j;
+            if (!packed && q.vec_f && j + 3 < q.d) {
                 const float4 x = *reinterpret_cast<const float4 *>(src);
                 v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
             } else {
+                // (a packed row holds only j >= i: the lower half of a
+                // diagonal tile is not read)
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    if (j + u < q.d) v[u] = src[u];
+                    if (j + u < q.d && (!packed || j + u >= i)) v[u] = src[u];
             }
         }
+        // a NaN or infinite entry of the upper triangle (the part read) is
+        // reported; the lower half of a diagonal tile is not part of F
+#pragma unroll
+        for (int u = 0; u < 4; ++u) bad |= (si != sj || j + u >= i) && !(fabsf(v[u]) <= FLT_MAX);
 #pragma unroll
         for (int u = 0; u < 4; ++u) t[r][c4 + u] = v[u];
     }
+    if (__any_sync(0xffffffffu, bad) && (tid & 31) == 0) atomicOr(P.error, ERR_NONFINITE);
     __syncthreads();
     const float dv = P.damp[q.damp_idx];
 #pragma unroll
@@ -558,6 +573,7 @@ void gen_chain(std::vector<Op> &ops, const MatWork &w, const InvMatrix &mat, int
     j.C = mat.out;
     j.ldc = mat.ldo;
     j.Cb = mat.out_bf16;
+    j.cb_f16 = mat.copy_f16;
     j.ldcb = mat.ldo_bf16;
     fin.g.push_back(j);
     ops.push_back(fin);
@@ -762,12 +778,12 @@ kfac_status diag_launch(const std::vector<DiagJob> &jobs, cudaStream_t st) {
         int n = 0;
         for (; pos < jobs.size() && n < MAT_MAX; ++pos) P->j[n++] = jobs[pos];
         P->n = n;
-        KFAC_LAUNCH(KK_LEAF, st, diag_kernel, n, DIAG_THREADS, DIAG_SMEM, *P);
+        KFAC_LAUNCH(KK_DIAG, st, diag_kernel, n, DIAG_THREADS, DIAG_SMEM, *P);
     }
     return KFAC_OK;
 }
 
-kfac_status prep_launch(std::vector<TileMat> &mats, const float *damp, cudaStream_t st) {
+kfac_status prep_launch(std::vector<TileMat> &mats, const float *damp, int *err, cudaStream_t st) {
     std::unique_ptr<TileParams> P(new TileParams);
     size_t pos = 0;
     while (pos < mats.size()) {
@@ -775,7 +791,7 @@ kfac_status prep_launch(std::vector<TileMat> &mats, const float *damp, cudaStrea
         while (pos < mats.size() && n < MAT_MAX) {
             TileMat m = mats[pos++];
             m.tiles = (int)ceil_div(m.dp, TT);
-            m.vec_f = m.F && m.ldf % 4 == 0 && (uintptr_t)m.F % 16 == 0;
+            m.vec_f = m.F && m.ldf > 0 && m.ldf % 4 == 0 && (uintptr_t)m.F % 16 == 0;
             P->m[n] = m;
             P->begin[n] = tiles;
             tiles += m.tiles * (m.tiles + 1) / 2;  // upper tile pairs
@@ -784,6 +800,7 @@ kfac_status prep_launch(std::vector<TileMat> &mats, const float *damp, cudaStrea
         P->begin[n] = tiles;
         P->n = n;
         P->damp = damp;
+        P->error = err;
         KFAC_LAUNCH(KK_PREP, st, prep_kernel, tiles, 256, 0, *P);
     }
     return KFAC_OK;
@@ -807,8 +824,8 @@ kfac_status damping_run(const InvMatrix *mats, int nlayers, float gamma, int pi_
         const int base = pos;
         while (pos < nlayers && n < MAT_MAX / 2) {
             const InvMatrix &A = mats[2 * pos], &G = mats[2 * pos + 1];
-            P->A[n] = A.F; P->lda[n] = A.ldf; P->dA[n] = A.d;
-            P->G[n] = G.F; P->ldg[n] = G.ldf; P->dG[n] = G.d;
+            P->A[n] = A.F; P->lda[n] = A.packed ? -1 : A.ldf; P->dA[n] = A.d;
+            P->G[n] = G.F; P->ldg[n] = G.packed ? -1 : G.ldf; P->dG[n] = G.d;
             ++n;
             ++pos;
         }
@@ -918,8 +935,9 @@ kfac_status inv_run(const InvMatrix *mats, int nmats, const float *damp_dev, int
     // 1. X = lower part of sym(F) + damp I (zero above), identity padding
     std::vector<TileMat> tm(nmats);
     for (int k = 0; k < nmats; ++k)
-        tm[k] = TileMat{mats[k].F, mats[k].ldf, p.work[k].Xh, p.work[k].Xl, mats[k].d, p.work[k].dp, k, 0, 0};
-    if ((s = prep_launch(tm, damp_dev, st)) != KFAC_OK) return s;
+        tm[k] = TileMat{mats[k].F, mats[k].packed ? -1 : mats[k].ldf, p.work[k].Xh, p.work[k].Xl, mats[k].d,
+                        p.work[k].dp, k, 0, 0};
+    if ((s = prep_launch(tm, damp_dev, p.err, st)) != KFAC_OK) return s;
 
     // 2. rounds (see schedule_rounds), the last op of each chain writing the
     //    caller's inverse: each group on a main stream with a side stream for

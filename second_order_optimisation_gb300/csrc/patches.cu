@@ -89,78 +89,114 @@ __global__ void __launch_bounds__(256) im2col_kernel(const __grid_constant__ ImP
     }
 }
 
-// Column sums of a bf16 [M][c] matrix, one CTA per 64 columns, fixed
-// reduction order; then the bias row/column update of F.
+// Column sums of a 16-bit [M][c] matrix: CTA (chunk, slab) sums 64 columns
+// over CS_ROWS rows into partial[slab][column]; the finish kernel adds the
+// slabs in order and updates the bias row/column of F.  Both reductions have
+// a fixed order, so the results are bitwise reproducible.
 constexpr int CS_MAX = 64;
+constexpr int CS_ROWS = 256;
 struct CsParams {
     ColsumJob j[CS_MAX];
-    int begin[CS_MAX + 1];  // prefix of 64-column chunks
-    long long ldx[CS_MAX];
+    int begin[CS_MAX + 1];  // prefix of CTAs: chunks x slabs per job
+    long long pbase[CS_MAX];  // offset of the job's partials
     int n;
+    float *partial;
 };
+
+__device__ __forceinline__ float h16_to_f32(uint16_t b, bool f16) {
+    return f16 ? __half2float(__ushort_as_half(b)) : bf16_bits_to_f32(b);
+}
+
+__device__ __forceinline__ int job_of(const CsParams &P, int b) {
+    int lo = 0, hi = P.n - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (P.begin[mid] <= b) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int slabs_of(const ColsumJob &q) { return (int)((q.M + CS_ROWS - 1) / CS_ROWS); }
 
 __global__ void __launch_bounds__(256) colsum_kernel(const __grid_constant__ CsParams P) {
     pdl_wait();
     pdl_trigger();
     __shared__ float red[32][65];
-    int lo = 0, hi = P.n - 1;
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (P.begin[mid] <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
-    }
-    const ColsumJob &q = P.j[lo];
-    const long long ldx = P.ldx[lo];
-    const int c0 = (blockIdx.x - P.begin[lo]) * 64;
+    const int jb = job_of(P, blockIdx.x);
+    const ColsumJob &q = P.j[jb];
+    const int slabs = slabs_of(q);
+    const int t = blockIdx.x - P.begin[jb];
+    const int chunk = t / slabs, slab = t - chunk * slabs;
+    const int c0 = chunk * 64;
     const int cg = threadIdx.x & 7;   // 8 groups of 8 columns
     const int rg = threadIdx.x >> 3;  // 32 row groups
     float s[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) s[k] = 0.f;
     const int col = c0 + cg * 8;
-    const bool vec = (q.c % 8 == 0) && ((ldx % 8) == 0) && ((uintptr_t)q.x % 16 == 0);
-    for (long long m = rg; m < q.M; m += 32) {
-        const uint16_t *row = q.x + m * ldx;
+    const bool f16 = q.f16 != 0;
+    const bool vec = (q.c % 8 == 0) && ((uintptr_t)q.x % 16 == 0);
+    const long long m1 = min(q.M, (long long)(slab + 1) * CS_ROWS);
+    for (long long m = (long long)slab * CS_ROWS + rg; m < m1; m += 32) {
+        const uint16_t *row = q.x + m * q.c;
         if (vec && col + 8 <= q.c) {
             uint4 v = *(const uint4 *)(row + col);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                s[2 * k] += __uint_as_float(w[k] << 16);
-                s[2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
+                s[2 * k] += h16_to_f32((uint16_t)(w[k] & 0xFFFFu), f16);
+                s[2 * k + 1] += h16_to_f32((uint16_t)(w[k] >> 16), f16);
             }
         } else {
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-                if (col + k < q.c) s[k] += bf16_bits_to_f32(row[col + k]);
+                if (col + k < q.c) s[k] += h16_to_f32(row[col + k], f16);
         }
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) red[rg][cg * 8 + k] = s[k];
     __syncthreads();
-    if (threadIdx.x < 64) {
-        float t = 0.f;
-        for (int r = 0; r < 32; ++r) t += red[r][threadIdx.x];
-        const int i = c0 + threadIdx.x;
-        if (i < q.c) {
-            float *f = q.F + (long long)i * q.ldf + q.c;
-            float o = q.alpha * t;
-            if (q.beta != 0.f) o = fmaf(q.beta, *f, o);
-            *f = o;
-        }
-        if (blockIdx.x == P.begin[lo] && threadIdx.x == 0) {
-            float *f = q.F + (long long)q.c * q.ldf + q.c;
-            float o = q.alpha * (float)q.M;
-            if (q.beta != 0.f) o = fmaf(q.beta, *f, o);
-            *f = o;
-        }
+    if (threadIdx.x < 64 && c0 + threadIdx.x < q.c) {
+        float a = 0.f;
+        for (int r = 0; r < 32; ++r) a += red[r][threadIdx.x];
+        P.partial[P.pbase[jb] + (long long)slab * q.c + c0 + threadIdx.x] = a;
     }
+}
+
+// F entry (i, c) of the bias column (i <= c), in either layout.
+__device__ __forceinline__ float *bias_entry(const ColsumJob &q, int i) {
+    const int d = q.c + 1;
+    return q.F + (q.packed ? (long long)i * d - (long long)i * (i + 1) / 2 : (long long)i * q.ldf) + q.c;
+}
+
+__global__ void __launch_bounds__(256) colsum_finish_kernel(const __grid_constant__ CsParams P) {
+    pdl_wait();
+    pdl_trigger();
+    // one thread per column 0 .. c of the job (column c: the ones column); begin counts CTAs of 256
+    const int jb = job_of(P, blockIdx.x);
+    const ColsumJob &q = P.j[jb];
+    const int i = (blockIdx.x - P.begin[jb]) * 256 + threadIdx.x;
+    if (i > q.c) return;
+    float *f = bias_entry(q, i);
+    float o;
+    if (i < q.c) {
+        const int slabs = slabs_of(q);
+        const float *pp = P.partial + P.pbase[jb] + i;
+        float a = 0.f;
+        for (int sl = 0; sl < slabs; ++sl) a += pp[(long long)sl * q.c];
+        o = q.alpha * a;
+    } else {
+        o = q.alpha * (float)q.M;  // the ones column with itself: the row count
+    }
+    if (q.beta != 0.f) o = fmaf(q.beta, *f, o);
+    *f = o;
 }
 
 }  // namespace
 
 kfac_status im2col_run(const Im2colJob *jobs, int njobs, int dtype, cudaStream_t st) {
     std::unique_ptr<ImParams> P(new ImParams);
-    const size_t esz = dtype == KFAC_BF16 ? 2 : 4;
+    const size_t esz = dtype == KFAC_F32 ? 4 : 2;
     const int vw = (int)(16 / esz);
     int pos = 0;
     while (pos < njobs) {
@@ -187,28 +223,45 @@ kfac_status im2col_run(const Im2colJob *jobs, int njobs, int dtype, cudaStream_t
         if (ctas == 0) continue;
         if (dtype == KFAC_BF16)
             KFAC_LAUNCH(KK_IM2COL, st, im2col_kernel<__nv_bfloat16>, (int)ctas, 256, 0, *P);
+        else if (dtype == KFAC_F16)
+            KFAC_LAUNCH(KK_IM2COL, st, im2col_kernel<__half>, (int)ctas, 256, 0, *P);
         else
             KFAC_LAUNCH(KK_IM2COL, st, im2col_kernel<float>, (int)ctas, 256, 0, *P);
     }
     return KFAC_OK;
 }
 
-kfac_status colsum_run(const ColsumJob *jobs, int njobs, cudaStream_t st) {
-    std::unique_ptr<CsParams> P(new CsParams);
+size_t colsum_partial_floats(const ColsumJob *jobs, int njobs) {
+    size_t n = 0;
+    for (int k = 0; k < njobs; ++k) n += (size_t)ceil_div(jobs[k].M, CS_ROWS) * jobs[k].c;
+    return n;
+}
+
+kfac_status colsum_run(const ColsumJob *jobs, int njobs, float *partial, cudaStream_t st) {
+    std::unique_ptr<CsParams> P(new CsParams), F(new CsParams);
     int pos = 0;
+    long long pb = 0;
     while (pos < njobs) {
-        int n = 0, chunks = 0;
+        int n = 0, ctas = 0, fin = 0;
         while (pos < njobs && n < CS_MAX) {
             const ColsumJob &j = jobs[pos++];
-            P->j[n] = j;
-            P->ldx[n] = j.c;  // dense rows
-            P->begin[n] = chunks;
-            chunks += (int)ceil_div(j.c, 64);
+            if (j.M < 1 || j.M >= (1LL << 31) || j.c < 1) return KFAC_ERR_UNSUPPORTED;
+            P->j[n] = F->j[n] = j;
+            P->pbase[n] = F->pbase[n] = pb;
+            P->begin[n] = ctas;
+            F->begin[n] = fin;
+            const long long slabs = ceil_div(j.M, CS_ROWS);
+            ctas += (int)(ceil_div(j.c, 64) * slabs);
+            fin += (int)ceil_div(j.c + 1, 256);
+            pb += slabs * j.c;
             ++n;
         }
-        P->begin[n] = chunks;
-        P->n = n;
-        KFAC_LAUNCH(KK_COLSUM, st, colsum_kernel, chunks, 256, 0, *P);
+        P->begin[n] = ctas;
+        F->begin[n] = fin;
+        P->n = F->n = n;
+        P->partial = F->partial = partial;
+        KFAC_LAUNCH(KK_COLSUM, st, colsum_kernel, ctas, 256, 0, *P);
+        KFAC_LAUNCH(KK_COLSUM, st, colsum_finish_kernel, fin, 256, 0, *F);
     }
     return KFAC_OK;
 }

@@ -4,7 +4,8 @@
 // section 3.2): the factor statistic P^T P of fp32 sources (Eq. 5) and the
 // preconditioned gradient G^-1 grad A^-1 of fp32 operands (Eq. 7).
 //
-// C[M x N] = alpha * op(A) op(B) + beta * C, one 128x128 tile per CTA, 256
+// C[M x N] = alpha * op(A) op(B) + beta * C (and optionally W -= eta * C, the
+// step on the weights of Eq. 8), one 128x128 tile per CTA, 256
 // threads with 8x8 register tiles, K in steps of 16 staged through shared
 // memory with register prefetch of the next step.  One launch covers a list
 // of independent problems (heterogeneous sizes).
@@ -25,14 +26,18 @@ struct SgProb {
     const float *B;
     float *C;
     float *Ct;
-    long long lda, ldb, ldc, ldct;
+    float *W;
+    long long lda, ldb, ldc, ldct, ldw;
+    float eta;
     int ta, tb, M, N, K, upper, tiles_n, tile_begin;
+    int packed_d;  // upper: C is a packed upper triangle of this order (0: row-major)
     float alpha, beta;
 };
 
 struct SgParams {
     SgProb p[SG_MAX];
     int n;
+    int *error;  // device error word (ERR_NONFINITE), or null
 };
 
 __global__ void __launch_bounds__(STHREADS) sgemm_kernel(const __grid_constant__ SgParams P) {
@@ -121,6 +126,7 @@ __global__ void __launch_bounds__(STHREADS) sgemm_kernel(const __grid_constant__
         }
     }
 
+    bool bad = false;  // a value this thread stored was NaN or infinite
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         int gi = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
@@ -130,18 +136,30 @@ __global__ void __launch_bounds__(STHREADS) sgemm_kernel(const __grid_constant__
             int gj = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
             if (gj >= q.N || (q.upper && gj < gi)) continue;
             float o = q.alpha * acc[i][j];
-            float *c = q.C + (long long)gi * q.ldc + gj;
-            if (q.beta != 0.f) o = fmaf(q.beta, *c, o);
-            *c = o;
+            if (q.C) {
+                float *c = q.C + (q.packed_d ? (long long)gi * q.packed_d - (long long)gi * (gi + 1) / 2
+                                             : (long long)gi * q.ldc) + gj;
+                if (q.beta != 0.f) o = fmaf(q.beta, *c, o);
+                *c = o;
+            }
             if (q.Ct) q.Ct[(long long)gj * q.ldct + gi] = o;
+            bad |= !(fabsf(o) <= 3.402823466e38f);
+            if (q.W) {
+                float *w = q.W + (long long)gi * q.ldw + gj;
+                const float nw = fmaf(-q.eta, o, *w);
+                bad |= !(fabsf(nw) <= 3.402823466e38f);
+                *w = nw;
+            }
         }
     }
+    if (__any_sync(0xffffffffu, bad) && (tid & 31) == 0 && P.error) atomicOr(P.error, ERR_NONFINITE);
 }
 
 }  // namespace
 
-kfac_status sg_run(const SgJob *jobs, int njobs, cudaStream_t st) {
+kfac_status sg_run(const SgJob *jobs, int njobs, int *err, cudaStream_t st) {
     std::unique_ptr<SgParams> P(new SgParams);
+    P->error = err;
     int pos = 0;
     while (pos < njobs) {
         int n = 0, tiles = 0;
@@ -153,6 +171,8 @@ kfac_status sg_run(const SgJob *jobs, int njobs, cudaStream_t st) {
             q.lda = j.lda; q.ldb = j.ldb; q.ldc = j.ldc; q.ldct = j.ldct;
             q.ta = j.ta; q.tb = j.tb; q.M = j.M; q.N = j.N; q.K = j.K;
             q.upper = j.upper;
+            q.W = j.W; q.ldw = j.ldw; q.eta = j.eta;
+            q.packed_d = j.upper ? j.packed_d : 0;
             q.alpha = j.alpha; q.beta = j.beta;
             int tm = (int)ceil_div(j.M, SB), tn = (int)ceil_div(j.N, SB);
             q.tiles_n = tn;

@@ -40,7 +40,7 @@ constexpr int BM = 128, BN = 128;
 constexpr int TILE_BYTES = 128 * 128;  // one tf32 operand tile: 128 rows x 128 bytes
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_ACC = 2 * BN;  // two accumulators (columns 0 and BN), alternating
-constexpr int MAX_PROBS = 160;
+constexpr int MAX_PROBS = 152;
 constexpr int GROUP = 8;              // row blocks per band of the grouped tile order
 constexpr int TF32X3_MAX_SPLIT = 6;   // K splits of a tf32x3 tile (the last CTA sums the partials)
 // Planning choices for tf32x3 launches, as measured on the ResNet-50 step:
@@ -84,12 +84,17 @@ struct TcProb {
     int tiles_n, ksplit, work_begin;
     uint8_t a_mn, b_mn;      // MN-major operand (bf16 only)
     uint8_t syrk, sym, lower, ktri, ktril, grouped, epi;
-    int tiles_m;             // 128-row blocks of the output
     uint8_t vec;             // C (and C_lo) rows take 16-byte accesses (ldc % 4 == 0, aligned)
     uint8_t vecb;            // Cb rows take 8-byte accesses
+    uint8_t vecw;            // W rows take 16-byte accesses
     uint8_t im2col, im_k, im_stride, im_pad;  // operands through an im2col map (see TcJob)
+    uint8_t f16, cb_f16;     // fp16 operands / fp16 copy Cb (else bf16)
+    uint8_t packed;          // ACCUM: C packed upper triangle of order packed_d
+    int packed_d;
+    int tiles_m;             // 128-row blocks of the output
     int im_c, im_wo, im_ho, im_howo;
     float alpha, beta;
+    float eta;               // STORE: W -= eta * result, in place (fp32, ldw)
     float *C;
     float *C_lo;
     long long ldc;
@@ -98,6 +103,8 @@ struct TcProb {
     long long ldct;
     uint16_t *Cb;
     long long ldcb;
+    float *W;
+    long long ldw;
     float *partial;  // [tiles][ksplit][BM*BN] when ksplit > 1
     int *counters;   // [tiles]
 };
@@ -369,6 +376,12 @@ __device__ __forceinline__ float4 sub4(float4 a, float4 b) {
 }
 __device__ __forceinline__ float comp(float4 v, int t) { return t == 0 ? v.x : t == 1 ? v.y : t == 2 ? v.z : v.w; }
 
+// Offset of C's entry (i, 0): row-major with ldc, or the packed upper
+// triangle (row i's entries j >= i start at i*d - i*(i+1)/2 + i).
+__device__ __forceinline__ long long c_row(const TcProb &q, int i) {
+    return q.packed ? (long long)i * q.packed_d - (long long)i * (i + 1) / 2 : (long long)i * q.ldc;
+}
+
 // Old values of the chunk at (i0, j0) (zeros where beta == 0 or out of range).
 __device__ __forceinline__ void load_old(const TcProb &q, int i0, int j0, int lane, float4 (&oh)[8],
                                          float4 (&ol)[8]) {
@@ -381,14 +394,14 @@ __device__ __forceinline__ void load_old(const TcProb &q, int i0, int j0, int la
         const int i = i0 + 4 * k + (lane >> 3);
         float4 h = make_float4(0.f, 0.f, 0.f, 0.f), l = h;
         if (need && i < q.M) {
-            const long long off = (long long)i * q.ldc + j;
-            if (full) {
+            const long long off = c_row(q, i) + j;
+            if (full && (!q.packed || (off & 3) == 0)) {
                 h = ld4(q.C + off);
                 if (lo) l = ld4(q.C_lo + off);
             } else {
                 float hv[4] = {0.f, 0.f, 0.f, 0.f}, lv[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int t = 0; t < 4; ++t)
-                    if (j + t < q.N) {
+                    if (j + t < q.N && (!q.packed || j + t >= i)) {
                         hv[t] = q.C[off + t];
                         if (lo) lv[t] = q.C_lo[off + t];
                     }
@@ -405,9 +418,11 @@ __device__ __forceinline__ void load_old(const TcProb &q, int i0, int j0, int la
 // row), oh / ol the old values from load_old.  The transposed copy Ct (if any)
 // is written straight from v (consecutive lanes are consecutive addresses of
 // Ct); the mirror of a symmetric off-diagonal tile goes back through the stage.
-__device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, const float *v, float *stage,
+// Returns true when a value this lane wrote is NaN or infinite.
+__device__ __forceinline__ bool chunk_store(const TcProb &q, int i0, int j0, const float *v, float *stage,
                                             int lane, bool mirror, bool diagblk, float4 (&oh)[8], float4 (&ol)[8]) {
     const float a = q.alpha, b = q.beta;
+    bool bad = false;
     if (q.epi == TC_EPI_SPLIT && q.Ct) {  // host guarantees beta == 0 here
         const int i = i0 + lane;
         if (i < q.M) {
@@ -442,8 +457,9 @@ __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, con
             if (i >= q.M) continue;
             const float4 o = make_float4(fmaf(b, oh[k].x, a * acc[k].x), fmaf(b, oh[k].y, a * acc[k].y),
                                          fmaf(b, oh[k].z, a * acc[k].z), fmaf(b, oh[k].w, a * acc[k].w));
-            float *dst = q.C + (long long)i * q.ldc + j;
-            if (full && (!upper || j >= i)) {
+            bad |= j < q.N && !finite4(o);  // (past the last column the values are zero padding)
+            float *dst = q.C + c_row(q, i) + j;
+            if (full && (!upper || j >= i) && (!q.packed || ((uintptr_t)dst & 15) == 0)) {
                 st4(dst, o);
             } else {
                 for (int t = 0; t < 4; ++t)
@@ -461,6 +477,7 @@ __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, con
             const int i = i0 + 4 * k + (lane >> 3);
             if (i >= q.M) continue;
             const float4 o = make_float4(a * acc[k].x, a * acc[k].y, a * acc[k].z, a * acc[k].w);
+            bad |= j < q.N && !finite4(o);
             if (q.C) {
                 float *dst = q.C + (long long)i * q.ldc + j;
                 if (full && (!up || j >= i)) {
@@ -470,15 +487,34 @@ __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, con
                         if (j + t < q.N && (!up || j + t >= i)) dst[t] = comp(o, t);
                 }
             }
+            if (q.W) {  // the step on the weights (never a symmetric output)
+                float *dw = q.W + (long long)i * q.ldw + j;
+                const float ne = -q.eta;
+                if (q.vecw && j + 3 < q.N) {
+                    float4 w4 = ld4(dw);
+                    w4.x = fmaf(ne, o.x, w4.x); w4.y = fmaf(ne, o.y, w4.y);
+                    w4.z = fmaf(ne, o.z, w4.z); w4.w = fmaf(ne, o.w, w4.w);
+                    bad |= !finite4(w4);
+                    st4(dw, w4);
+                } else {
+                    for (int t = 0; t < 4; ++t)
+                        if (j + t < q.N) {
+                            const float nw = fmaf(ne, comp(o, t), dw[t]);
+                            bad |= !(fabsf(nw) <= 3.402823466e38f);
+                            dw[t] = nw;
+                        }
+                }
+            }
             if (q.Cb) {
                 uint16_t *dst = q.Cb + (long long)i * q.ldcb + j;
                 if (fullb && (!up || j >= i)) {
-                    const uint32_t lo2 = f32_to_bf16_bits(o.x) | ((uint32_t)f32_to_bf16_bits(o.y) << 16);
-                    const uint32_t hi2 = f32_to_bf16_bits(o.z) | ((uint32_t)f32_to_bf16_bits(o.w) << 16);
+                    const bool h16 = q.cb_f16;
+                    const uint32_t lo2 = f32_to_16_bits(o.x, h16) | ((uint32_t)f32_to_16_bits(o.y, h16) << 16);
+                    const uint32_t hi2 = f32_to_16_bits(o.z, h16) | ((uint32_t)f32_to_16_bits(o.w, h16) << 16);
                     *reinterpret_cast<uint2 *>(dst) = make_uint2(lo2, hi2);
                 } else {
                     for (int t = 0; t < 4; ++t)
-                        if (j + t < q.N && (!up || j + t >= i)) dst[t] = f32_to_bf16_bits(comp(o, t));
+                        if (j + t < q.N && (!up || j + t >= i)) dst[t] = f32_to_16_bits(comp(o, t), q.cb_f16);
                 }
             }
         }
@@ -495,7 +531,7 @@ __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, con
                     if (up && jj <= i) continue;
                     const float o = a * v[c];
                     if (q.C) q.C[(long long)jj * q.ldc + i] = o;
-                    if (q.Cb) q.Cb[(long long)jj * q.ldcb + i] = f32_to_bf16_bits(o);
+                    if (q.Cb) q.Cb[(long long)jj * q.ldcb + i] = f32_to_16_bits(o, q.cb_f16);
                 }
             }
         }
@@ -507,6 +543,7 @@ __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, con
                                          fmaf(b, oh[k].y + ol[k].y, a * acc[k].y),
                                          fmaf(b, oh[k].z + ol[k].z, a * acc[k].z),
                                          fmaf(b, oh[k].w + ol[k].w, a * acc[k].w));
+            bad |= i < q.M && j < q.N && !finite4(o);
             const float4 h = tf32_hi4(o), l = sub4(o, h);
             oh[k] = h;  // the final pair, kept for the mirror below
             ol[k] = l;
@@ -544,6 +581,7 @@ __device__ __forceinline__ void chunk_store(const TcProb &q, int i0, int j0, con
             }
         }
     }
+    return bad;
 }
 
 template <int KIND>
@@ -557,7 +595,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     uint64_t *empty = full + Tr::STAGES;
     uint64_t *accf = empty + Tr::STAGES;
     uint64_t *acce = accf + 2;
-    uint32_t *tmem_slot = (uint32_t *)(acce + 2);
+    uint64_t *drain = acce + 2;  // completion of this CTA's products after an abort
+    uint32_t *tmem_slot = (uint32_t *)(drain + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
     volatile int *last_flag = abort_flag + 1;
     float *epi_stage = (float *)(smem + Tr::STAGES * STAGE_BYTES + 256);
@@ -574,6 +613,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             mbar_init(&accf[b], 1);
             mbar_init(&acce[b], 128);
         }
+        mbar_init(drain, 1);
         *abort_flag = 0;
         *last_flag = 0;
         fence_barrier_init();
@@ -593,6 +633,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             int stage = 0;
             uint32_t phase = 0;
             int last_p = -1;
+            int issued = 0;  // stages armed so far
             for (int w = w_first; w < P.total_work && !*abort_flag; w += w_step) {
                 Work k = decode_work(P, w);
                 const TcProb &q = P.prob[k.p];
@@ -613,7 +654,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 const uint32_t bytes = KIND == TC_KIND_TF32X3 ? (uint32_t)(2 * (BM + q.bn) * 128)
                                        : diag                 ? (uint32_t)Tr::TILE
                                                               : (uint32_t)STAGE_BYTES;
-                for (int kt = k.kt0; kt < k.kt1; ++kt) {
+                for (int kt = k.kt0; kt < k.kt1 && !*abort_flag; ++kt) {
                     if (!mbar_wait(&empty[stage], phase ^ 1)) {
                         atomicOr(P.error, ERR_TIMEOUT_EMPTY);
                         *abort_flag = 1;
@@ -646,6 +687,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                         }
                     }
                     if (++stage == Tr::STAGES) { stage = 0; phase ^= 1; }
+                    ++issued;
+                }
+            }
+            if (*abort_flag) {
+                // the run was cut short: before the CTA exits, wait (bounded)
+                // for the copies this thread issued into the last STAGES
+                // stages (older stages were consumed, so their copies landed)
+                for (int n = 0; n < min(issued, Tr::STAGES); ++n) {
+                    if (stage == 0) { stage = Tr::STAGES - 1; phase ^= 1; } else { --stage; }
+                    if (!mbar_wait(&full[stage], phase)) atomicOr(P.error, ERR_TIMEOUT_DRAIN);
                 }
             }
         }
@@ -659,7 +710,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 Work k = decode_work(P, w);
                 const TcProb &q = P.prob[k.p];
                 const bool diag = KIND == TC_KIND_BF16 && q.syrk && k.tm == k.tn;
-                const uint32_t idesc = KIND == TC_KIND_BF16 ? idesc_bf16_f32(BM, BN, q.a_mn, q.b_mn)
+                const uint32_t idesc = KIND == TC_KIND_BF16 ? idesc_bf16_f32(BM, BN, q.a_mn, q.b_mn, q.f16)
                                                             : idesc_tf32_f32(BM, q.bn);
                 const int nchunk = max(1, (int)ceil_div_dev(k.kt1 - k.kt0, Tr::CHUNK));
                 for (int ch = 0; ch < nchunk && ok; ++ch, ++cc) {
@@ -708,6 +759,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     tc_commit(&accf[b]);
                 }
             }
+            if (*abort_flag) {
+                // the run was cut short: wait (bounded) for every product
+                // this thread issued before the accumulators are released
+                tc_commit(drain);
+                if (!mbar_wait(drain, 0)) atomicOr(P.error, ERR_TIMEOUT_DRAIN);
+            }
         }
     } else {
         // epilogue warps 2..5 -> TMEM lane quarters 2,3,0,1
@@ -718,6 +775,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         const uint32_t t_quarter = tmem_base + ((uint32_t)(quarter * 32) << 16);
         const uint32_t t_sum = t_quarter + 2 * BN;  // running sum of a chunked item (tf32x3)
         int cc = 0;
+        bool nonfin = false;  // a value this lane stored was NaN or infinite
         for (int w = w_first; w < P.total_work && !*abort_flag; w += w_step) {
             Work k = decode_work(P, w);
             const TcProb &q = P.prob[k.p];
@@ -789,7 +847,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 #pragma unroll
                         for (int t = 0; t < 32; ++t) v[t] = 0.f;
                     }
-                    chunk_store(q, i0, k.tn * q.bn + c * 32, v, stage, lane, mirror, diagblk, oh, ol);
+                    nonfin |= chunk_store(q, i0, k.tn * q.bn + c * 32, v, stage, lane, mirror, diagblk, oh, ol);
                 }
                 tc_fence_before();
                 mbar_arrive(&acce[b]);
@@ -841,12 +899,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                                 v[4 * f] += t.x; v[4 * f + 1] += t.y; v[4 * f + 2] += t.z; v[4 * f + 3] += t.w;
                             }
                         }
-                        chunk_store(q, i0, k.tn * q.bn + c * 32, v, stage, lane, mirror, diagblk, oh, ol);
+                        nonfin |= chunk_store(q, i0, k.tn * q.bn + c * 32, v, stage, lane, mirror, diagblk, oh, ol);
                     }
                     if (etid == 0) q.counters[k.tile] = 0;
                 }
             }
         }
+        if (__any_sync(0xffffffffu, nonfin) && lane == 0) atomicOr(P.error, ERR_NONFINITE);
     }
 
     __syncthreads();
@@ -973,7 +1032,8 @@ cudaError_t set_smem_attr() {
 
 }  // namespace
 
-bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int box_rows) {
+bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int box_rows,
+                 bool f16) {
     EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) return false;
     const int esz = kind == TC_KIND_BF16 ? 2 : 4;
@@ -982,14 +1042,17 @@ bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int ro
     const cuuint32_t inner = 128u / esz;  // 128-byte rows
     cuuint32_t box[2] = {inner, box_rows > 0 ? (cuuint32_t)box_rows : 128u};
     cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = enc(m, kind == TC_KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                     2, (void *)ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    const CUtensorMapDataType dt = kind == TC_KIND_BF16
+                                       ? (f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)
+                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    CUresult r = enc(m, dt, 2, (void *)ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-bool tc_make_im2col_map(CUtensorMap *m, const void *x, int n, int h, int w, int c, int k, int stride, int pad) {
+bool tc_make_im2col_map(CUtensorMap *m, const void *x, int n, int h, int w, int c, int k, int stride, int pad,
+                        bool f16) {
     EncodeIm2colFn enc = encode_im2col_fn();
     if (!enc) return false;
     cuuint64_t dims[4] = {(cuuint64_t)c, (cuuint64_t)w, (cuuint64_t)h, (cuuint64_t)n};
@@ -999,7 +1062,8 @@ bool tc_make_im2col_map(CUtensorMap *m, const void *x, int n, int h, int w, int 
     int lower[2] = {-pad, -pad};
     int upper[2] = {pad - (k - 1), pad - (k - 1)};
     cuuint32_t estr[4] = {1u, (cuuint32_t)stride, (cuuint32_t)stride, 1u};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void *)x, dims, strides, lower, upper, 64u, 128u, estr,
+    CUresult r = enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void *)x, dims,
+                     strides, lower, upper, 64u, 128u, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -1043,7 +1107,10 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
             return KFAC_ERR_INVALID;
         if (j.lower && (kind != TC_KIND_TF32X3 || j.sym || j.syrk || j.epi != TC_EPI_SPLIT)) return KFAC_ERR_INVALID;
         if ((j.ktri || j.ktril) && kind != TC_KIND_TF32X3) return KFAC_ERR_INVALID;
-        if (!j.C && !j.Ct && !j.Cb) return KFAC_ERR_INVALID;
+        if (j.W && (j.epi != TC_EPI_STORE || j.sym)) return KFAC_ERR_INVALID;
+        if (j.f16 && kind != TC_KIND_BF16) return KFAC_ERR_INVALID;
+        if (j.packed && (j.epi != TC_EPI_ACCUM || !j.syrk || j.packed_d < j.N)) return KFAC_ERR_INVALID;
+        if (!j.C && !j.Ct && !j.Cb && !j.W) return KFAC_ERR_INVALID;
     }
     const int sms = cta_cap(max_ctas);
     Plan p = make_plan(jobs, njobs, kind, sms);
@@ -1091,6 +1158,12 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
             q.Cb = j.Cb; q.ldcb = j.ldcb;
             q.vec = (j.ldc % 4 == 0) && ((uintptr_t)j.C % 16 == 0) && ((uintptr_t)j.C_lo % 16 == 0);
             q.vecb = (j.ldcb % 4 == 0) && ((uintptr_t)j.Cb % 8 == 0);
+            q.W = j.W; q.ldw = j.ldw; q.eta = j.eta;
+            q.f16 = j.f16 ? 1 : 0;
+            q.cb_f16 = j.cb_f16 ? 1 : 0;
+            q.packed = j.packed ? 1 : 0;
+            q.packed_d = j.packed_d;
+            q.vecw = (j.ldw % 4 == 0) && ((uintptr_t)j.W % 16 == 0);
             q.im2col = j.im2col ? 1 : 0;
             q.im_k = (uint8_t)j.im_k; q.im_stride = (uint8_t)j.im_stride; q.im_pad = (uint8_t)j.im_pad;
             q.im_c = j.im_c; q.im_wo = j.im_wo; q.im_howo = j.im_howo;

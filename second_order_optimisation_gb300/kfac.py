@@ -24,7 +24,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkfac_gb300.so")
 
 KFAC_OK, KFAC_ERR_INVALID, KFAC_ERR_UNSUPPORTED, KFAC_ERR_NOT_PD, KFAC_ERR_CUDA, KFAC_ERR_WORKSPACE = range(6)
-KFAC_BF16, KFAC_F32 = 0, 1
+KFAC_BF16, KFAC_F32, KFAC_F16 = 0, 1, 2
+KFAC_LAYOUT_FULL, KFAC_LAYOUT_PACKED_UPPER = 0, 1
+# bits of the device error word (the first int32 of a call's workspace)
+ERRW_TIMEOUT_OPERAND, ERRW_TIMEOUT_STAGE, ERRW_TIMEOUT_ACCUM, ERRW_TIMEOUT_DRAIN, ERRW_NONFINITE = 1, 2, 4, 8, 16
 
 EXPORTS = ("kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_timing_enable",
            "kfac_timing_read", "kfac_timing_kind_name", "kfac_factor_update_workspace_size",
@@ -47,7 +50,8 @@ class FactorDesc(ctypes.Structure):
                 ("pad_h", ctypes.c_int32), ("pad_w", ctypes.c_int32),
                 ("append_one", ctypes.c_int32),
                 ("F", ctypes.c_void_p), ("ldf", ctypes.c_int64),
-                ("alpha", ctypes.c_float), ("beta", ctypes.c_float)]
+                ("alpha", ctypes.c_float), ("beta", ctypes.c_float),
+                ("layout", ctypes.c_int32)]
 
 
 class InvertDesc(ctypes.Structure):
@@ -56,7 +60,9 @@ class InvertDesc(ctypes.Structure):
                 ("A_inv", ctypes.c_void_p), ("ld_ainv", ctypes.c_int64),
                 ("G_inv", ctypes.c_void_p), ("ld_ginv", ctypes.c_int64),
                 ("A_inv_bf16", ctypes.c_void_p), ("ld_ainv_bf16", ctypes.c_int64),
-                ("G_inv_bf16", ctypes.c_void_p), ("ld_ginv_bf16", ctypes.c_int64)]
+                ("G_inv_bf16", ctypes.c_void_p), ("ld_ginv_bf16", ctypes.c_int64),
+                ("layout_A", ctypes.c_int32), ("layout_G", ctypes.c_int32),
+                ("copy_dtype", ctypes.c_int32)]
 
 
 class PrecondDesc(ctypes.Structure):
@@ -64,7 +70,9 @@ class PrecondDesc(ctypes.Structure):
                 ("G_inv", ctypes.c_void_p), ("ld_ginv", ctypes.c_int64),
                 ("A_inv", ctypes.c_void_p), ("ld_ainv", ctypes.c_int64),
                 ("grad", ctypes.c_void_p), ("ld_grad", ctypes.c_int64),
-                ("out", ctypes.c_void_p), ("ld_out", ctypes.c_int64)]
+                ("out", ctypes.c_void_p), ("ld_out", ctypes.c_int64),
+                ("w", ctypes.c_void_p), ("ld_w", ctypes.c_int64),
+                ("eta", ctypes.c_float)]
 
 
 class BnDesc(ctypes.Structure):
@@ -179,7 +187,9 @@ def _ld(t: torch.Tensor) -> int:
 @dataclass
 class FactorSource:
     """One factor update: F[:d, :d] (upper) <- beta F + alpha P^T P, P the patch
-    matrix of x.  x: NHWC [n, h, w, c] (conv) or [rows, c] (FC / output grads)."""
+    matrix of x.  x: NHWC [n, h, w, c] (conv) or [rows, c] (FC / output grads),
+    bf16, fp16 or fp32.  With packed, F is the packed upper triangle (a 1-D
+    tensor of d(d+1)/2 floats, see pack_upper)."""
     x: torch.Tensor
     F: torch.Tensor
     kh: int = 1
@@ -189,6 +199,38 @@ class FactorSource:
     append_one: bool = False
     alpha: float = 1.0
     beta: float = 0.0
+    packed: bool = False
+
+
+_DTYPES = {torch.bfloat16: KFAC_BF16, torch.float16: KFAC_F16, torch.float32: KFAC_F32}
+
+
+def packed_size(d: int) -> int:
+    """Floats of a packed upper triangle of order d."""
+    return d * (d + 1) // 2
+
+
+def pack_upper(F: torch.Tensor) -> torch.Tensor:
+    """The packed upper triangle (KFAC_LAYOUT_PACKED_UPPER) of a square
+    matrix: row i's entries j >= i, row after row (a layout conversion)."""
+    d = F.shape[0]
+    iu = torch.triu_indices(d, d, device=F.device)
+    return F[iu[0], iu[1]].contiguous()
+
+
+def unpack_upper(Fp: torch.Tensor, d: int) -> torch.Tensor:
+    """Square matrix holding a packed upper triangle (zeros below)."""
+    out = torch.zeros(d, d, dtype=Fp.dtype, device=Fp.device)
+    iu = torch.triu_indices(d, d, device=Fp.device)
+    out[iu[0], iu[1]] = Fp
+    return out
+
+
+def _fld(F: torch.Tensor, packed: bool) -> int:
+    if packed:
+        assert F.dim() == 1 and F.is_contiguous() and F.dtype == torch.float32
+        return 0
+    return _ld(F)
 
 
 def _factor_descs(sources: Sequence[FactorSource]):
@@ -200,16 +242,13 @@ def _factor_descs(sources: Sequence[FactorSource]):
             n, h, w, c = x.shape[0], 1, 1, x.shape[1]
         else:
             n, h, w, c = x.shape
-        if x.dtype == torch.bfloat16:
-            dt = KFAC_BF16
-        elif x.dtype == torch.float32:
-            dt = KFAC_F32
-        else:
+        if x.dtype not in _DTYPES:
             raise TypeError(f"unsupported source dtype {x.dtype}")
         assert s.F.dtype == torch.float32
-        arr[i] = FactorDesc(dt, x.data_ptr(), n, h, w, c, s.kh, s.kw, s.stride[0], s.stride[1],
-                            s.pad[0], s.pad[1], int(bool(s.append_one)), s.F.data_ptr(), _ld(s.F),
-                            float(s.alpha), float(s.beta))
+        arr[i] = FactorDesc(_DTYPES[x.dtype], x.data_ptr(), n, h, w, c, s.kh, s.kw, s.stride[0], s.stride[1],
+                            s.pad[0], s.pad[1], int(bool(s.append_one)), s.F.data_ptr(), _fld(s.F, s.packed),
+                            float(s.alpha), float(s.beta),
+                            KFAC_LAYOUT_PACKED_UPPER if s.packed else KFAC_LAYOUT_FULL)
     return arr
 
 
@@ -221,7 +260,8 @@ def kfac_factor_update_workspace_size(sources: Sequence[FactorSource]) -> int:
 def kfac_factor_update(sources: Sequence[FactorSource], workspace: Optional[torch.Tensor] = None,
                        stream=None) -> torch.Tensor:
     """Enqueue the factor updates; returns the workspace used (its first int32
-    is the library's device error word: 0 = no internal timeout)."""
+    is the library's device error word: 0 = no timeout and no NaN or infinite
+    output; ERRW_* bits otherwise)."""
     lib = load()
     arr = _factor_descs(sources)
     need = int(lib.kfac_factor_update_workspace_size(arr, len(sources)))
@@ -237,7 +277,9 @@ def kfac_factor_update(sources: Sequence[FactorSource], workspace: Optional[torc
 
 @dataclass
 class InvertPair:
-    """Both factors of one layer and where their damped inverses go."""
+    """Both factors of one layer and where their damped inverses go.  The
+    optional 16-bit copies are bf16 or fp16 (both the same dtype); a packed
+    factor is a 1-D tensor of d(d+1)/2 floats (then dA / dG are required)."""
     A: torch.Tensor
     G: torch.Tensor
     A_inv: torch.Tensor
@@ -246,17 +288,25 @@ class InvertPair:
     G_inv_bf16: Optional[torch.Tensor] = None
     dA: Optional[int] = None
     dG: Optional[int] = None
+    packed_A: bool = False
+    packed_G: bool = False
 
 
 def _invert_descs(pairs: Sequence[InvertPair]):
     arr = (InvertDesc * max(len(pairs), 1))()
     for i, p in enumerate(pairs):
-        dA = p.dA or p.A.shape[0]
-        dG = p.dG or p.G.shape[0]
-        arr[i] = InvertDesc(p.A.data_ptr(), dA, _ld(p.A), p.G.data_ptr(), dG, _ld(p.G),
+        dA = p.dA or p.A_inv.shape[0]
+        dG = p.dG or p.G_inv.shape[0]
+        copies = {t.dtype for t in (p.A_inv_bf16, p.G_inv_bf16) if t is not None}
+        if not copies <= {torch.bfloat16, torch.float16} or len(copies) > 1:
+            raise TypeError(f"16-bit inverse copies must be both bf16 or both fp16, got {copies}")
+        cdt = KFAC_F16 if copies == {torch.float16} else KFAC_BF16
+        arr[i] = InvertDesc(p.A.data_ptr(), dA, _fld(p.A, p.packed_A), p.G.data_ptr(), dG, _fld(p.G, p.packed_G),
                             p.A_inv.data_ptr(), _ld(p.A_inv), p.G_inv.data_ptr(), _ld(p.G_inv),
                             _ptr(p.A_inv_bf16), _ld(p.A_inv_bf16) if p.A_inv_bf16 is not None else 0,
-                            _ptr(p.G_inv_bf16), _ld(p.G_inv_bf16) if p.G_inv_bf16 is not None else 0)
+                            _ptr(p.G_inv_bf16), _ld(p.G_inv_bf16) if p.G_inv_bf16 is not None else 0,
+                            KFAC_LAYOUT_PACKED_UPPER if p.packed_A else KFAC_LAYOUT_FULL,
+                            KFAC_LAYOUT_PACKED_UPPER if p.packed_G else KFAC_LAYOUT_FULL, cdt)
     return arr
 
 
@@ -268,7 +318,8 @@ def kfac_damp_invert(pairs: Sequence[InvertPair], gamma: float, pi_split: bool =
                      info: Optional[torch.Tensor] = None, damp: Optional[torch.Tensor] = None,
                      workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Enqueue the damped inversions; returns the workspace used (its first
-    int32 is the library's device error word: 0 = no internal timeout)."""
+    int32 is the library's device error word: 0 = no timeout and no NaN or
+    infinite output; ERRW_* bits otherwise)."""
     lib = load()
     arr = _invert_descs(pairs)
     need = int(lib.kfac_damp_invert_workspace_size(arr, len(pairs)))
@@ -287,13 +338,16 @@ def kfac_damp_invert(pairs: Sequence[InvertPair], gamma: float, pi_split: bool =
 
 @dataclass
 class PrecondItem:
-    """out = G_inv @ grad @ A_inv for one layer (grad [dG, dA])."""
+    """out = G_inv @ grad @ A_inv for one layer (grad [dG, dA]); with w, also
+    w -= eta * out in place (out may then be None)."""
     G_inv: torch.Tensor
     A_inv: torch.Tensor
     grad: torch.Tensor
-    out: torch.Tensor
+    out: Optional[torch.Tensor]
     dG: Optional[int] = None
     dA: Optional[int] = None
+    w: Optional[torch.Tensor] = None
+    eta: float = 0.0
 
 
 def _precond_descs(items: Sequence[PrecondItem]):
@@ -301,18 +355,22 @@ def _precond_descs(items: Sequence[PrecondItem]):
     for i, it in enumerate(items):
         dG = it.dG or it.grad.shape[0]
         dA = it.dA or it.grad.shape[1]
+        if it.w is not None and it.w.dtype != torch.float32:
+            raise TypeError("w must be fp32")
         arr[i] = PrecondDesc(dG, dA, it.G_inv.data_ptr(), _ld(it.G_inv), it.A_inv.data_ptr(), _ld(it.A_inv),
-                             it.grad.data_ptr(), _ld(it.grad), it.out.data_ptr(), _ld(it.out))
+                             it.grad.data_ptr(), _ld(it.grad),
+                             it.out.data_ptr() if it.out is not None else None,
+                             _ld(it.out) if it.out is not None else 0,
+                             it.w.data_ptr() if it.w is not None else None,
+                             _ld(it.w) if it.w is not None else 0, float(it.eta))
     return arr
 
 
 def _precond_dtype(items: Sequence[PrecondItem]) -> int:
     dts = {it.grad.dtype for it in items} | {it.A_inv.dtype for it in items} | {it.G_inv.dtype for it in items}
-    if dts == {torch.bfloat16}:
-        return KFAC_BF16
-    if dts == {torch.float32}:
-        return KFAC_F32
-    raise TypeError(f"operands must be all bf16 or all fp32, got {dts}")
+    if len(dts) == 1 and next(iter(dts)) in _DTYPES:
+        return _DTYPES[next(iter(dts))]
+    raise TypeError(f"operands must be all bf16, all fp16 or all fp32, got {dts}")
 
 
 def kfac_precondition_workspace_size(items: Sequence[PrecondItem]) -> int:

@@ -14,6 +14,16 @@ Inputs are the per-layer bf16 tensors x (NHWC), g ([M, C_out]) and grad
 ([C_out, d_A]); with `rows_total` the statistic of several chunks of a larger
 mini-batch can be accumulated before the inversion (gradient accumulation,
 section 2).
+
+`step()` runs the same phases under the stale-factor schedule of the paper's
+contributions list (section 1: after a few hundred iterations the Fisher is
+updated less often).  The pages give no period, so it is a parameter: steps
+t < warmup refresh the factors and their inverses every time; after that only
+every `update_every`-th step does ((t - warmup) % update_every == 0), and the
+other steps precondition with the inverses of the last refresh.  A stale step
+skips the factor statistic as well as the inversion (the factors are
+"updated" less often, not only inverted less often).  With `weights` the
+preconditioner also applies w <- w - eta * P in its epilogue (Eq. 8).
 """
 from __future__ import annotations
 
@@ -44,12 +54,22 @@ class LayerState:
 
 class KfacStep:
     def __init__(self, layers: Sequence[Layer], batch: int, xi: float = 0.95, gamma: float = 1e-3,
-                 device="cuda"):
+                 device="cuda", update_every: int = 1, warmup: int = 0,
+                 weights: Optional[Sequence[torch.Tensor]] = None, eta: float = 0.0):
         self.layers = list(layers)
         self.batch = batch
         self.xi = xi
         self.gamma = gamma
         self.device = torch.device(device)
+        if update_every < 1 or warmup < 0:
+            raise ValueError("update_every must be >= 1 and warmup >= 0")
+        self.update_every = int(update_every)
+        self.warmup = int(warmup)
+        self.t = 0                  # steps taken by step()
+        if weights is not None and len(weights) != len(self.layers):
+            raise ValueError("one weight tensor per layer")
+        self.weights = list(weights) if weights is not None else None
+        self.eta = float(eta)
         self.state: List[LayerState] = []
         for L in self.layers:
             dA, dG = L.d_a, L.d_g
@@ -91,8 +111,10 @@ class KfacStep:
                                 s.G_inv16[:, :s.G.shape[0]]) for s in self.state]
 
     def precond_items(self, grads):
-        return [kfac.PrecondItem(s.G_inv16[:, :s.G.shape[0]], s.A_inv16[:, :s.A.shape[0]], gr, s.out)
-                for s, gr in zip(self.state, grads)]
+        ws = self.weights if self.weights is not None else [None] * len(self.state)
+        return [kfac.PrecondItem(s.G_inv16[:, :s.G.shape[0]], s.A_inv16[:, :s.A.shape[0]], gr, s.out,
+                                 w=w, eta=self.eta)
+                for s, gr, w in zip(self.state, grads, ws)]
 
     def _workspace(self, key, nbytes):
         w = self._ws.get(key)
@@ -122,3 +144,20 @@ class KfacStep:
         self.factor_update(xs, gs, stream=stream)
         self.damp_invert(stream)
         self.precondition(grads, stream)
+
+    # ---------------------------------------------------------------- schedule
+    def refresh_due(self, t: Optional[int] = None) -> bool:
+        """Whether step t (default: the next one) refreshes factors and inverses."""
+        t = self.t if t is None else t
+        return t < self.warmup or (t - self.warmup) % self.update_every == 0
+
+    def step(self, xs, gs, grads, stream=None) -> bool:
+        """Step t of the stale-factor schedule; returns whether it refreshed.
+        xs / gs are only read on refresh steps (None is accepted otherwise)."""
+        refresh = self.refresh_due()
+        if refresh:
+            self.factor_update(xs, gs, stream=stream)
+            self.damp_invert(stream)
+        self.precondition(grads, stream)
+        self.t += 1
+        return refresh

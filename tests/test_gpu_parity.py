@@ -367,6 +367,66 @@ def test_precondition_clears_error_word(dtype):
     assert bool((out == 1.0).all())
 
 
+# -------------------------------------------------------------- fused step on the weights (Eq. 8)
+
+def _precond_operands(dG, dA, dtype, tag):
+    """Symmetric inverses and a 1e-3-scale gradient; bf16 operands sit in
+    row-padded buffers (ld a multiple of 8) so the views have ragged widths."""
+    Gi = workloads.normal_f32((dG, dG), 1.0, "wu", tag, "G")
+    Ai = workloads.normal_f32((dA, dA), 1.0, "wu", tag, "A")
+    Gi, Ai = (Gi + Gi.T) / 2, (Ai + Ai.T) / 2
+    grad = workloads.normal_f32((dG, dA), 1e-3, "wu", tag, "g")
+    if dtype == torch.float32:
+        return ([torch.from_numpy(x).to(DEV) for x in (Gi, Ai, grad)], (Gi, Ai, grad))
+    host = [bf16(x) for x in (Gi, Ai, grad)]
+    dev = []
+    for x in host:
+        r, c = x.shape
+        buf = torch.zeros(r, (c + 7) // 8 * 8, dtype=torch.bfloat16, device=DEV)
+        buf[:, :c] = x.to(DEV)
+        dev.append(buf[:, :c])
+    return dev, tuple(x.float().numpy() for x in host)
+
+
+@pytest.mark.parametrize("dtype,dG,dA", [(torch.bfloat16, 130, 1001), (torch.bfloat16, 256, 576),
+                                         (torch.float32, 70, 133), (torch.float32, 129, 260)],
+                         ids=["bf16-130x1001", "bf16-256x576", "fp32-70x133", "fp32-129x260"])
+@pytest.mark.parametrize("keep_out", [True, False], ids=["out", "no-out"])
+def test_precondition_fused_weight_update(dtype, dG, dA, keep_out):
+    """w <- w - eta * (G^-1 grad A^-1) in the second product's epilogue, against
+    the oracle's preconditioned gradient and update; with out kept, out is
+    bitwise the unfused result and w is one fused multiply-add of it."""
+    (Gd, Ad, gd), (Gh, Ah, gh) = _precond_operands(dG, dA, dtype, f"{dtype}{dG}x{dA}")
+    eta = 0.125
+    w0 = workloads.normal_f32((dG, dA), 5e-2, "wu", dG, dA, "w")
+    ldw = dA + 3  # padded rows (16-byte row access only where dA + 3 is a multiple of 4)
+    wbuf = torch.zeros(dG, ldw, device=DEV)
+    wbuf[:, :dA] = torch.from_numpy(w0).to(DEV)
+    w = wbuf[:, :dA]
+    out = torch.empty(dG, dA, device=DEV) if keep_out else None
+    kfac.kfac_precondition([kfac.PrecondItem(Gd, Ad, gd, out, w=w, eta=eta)])
+    plain = torch.empty(dG, dA, device=DEV)
+    kfac.kfac_precondition([kfac.PrecondItem(Gd, Ad, gd, plain)])
+    torch.cuda.synchronize()
+    P_ref = oracle.precondition(Gh, gh, Ah)
+    w_ref = oracle.weight_update(w0.astype(np.float64), P_ref, eta)
+    tol = 2e-2 if dtype == torch.bfloat16 else 1e-4
+    assert rel(f64(w) - w0, w_ref - w0) <= tol
+    assert rel(f64(w), w_ref) <= tol
+    assert bool((wbuf[:, dA:] == 0).all())  # the row padding is untouched
+    if keep_out:
+        assert torch.equal(out, plain)
+    np.testing.assert_allclose(f64(w), w0.astype(np.float64) - np.float64(np.float32(eta)) * f64(plain),
+                               rtol=3e-7, atol=1e-9)
+
+
+def test_precondition_weight_update_only_rejects_no_destination():
+    G = torch.eye(8, device=DEV)
+    g = torch.ones(8, 8, device=DEV)
+    with pytest.raises(kfac.KfacError):
+        kfac.kfac_precondition([kfac.PrecondItem(G, G, g, None)])
+
+
 # -------------------------------------------------------------- whole layer step
 
 def test_fc64x32_fp32_step():
