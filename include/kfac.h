@@ -30,7 +30,10 @@
  *     calls on different streams with disjoint buffers and workspaces are
  *     allowed.
  *   - KFAC_ERR_INVALID / KFAC_ERR_UNSUPPORTED / KFAC_ERR_WORKSPACE are
- *     returned BEFORE anything is enqueued (outputs untouched).
+ *     returned BEFORE anything is enqueued (outputs untouched).  Every
+ *     operand must be memory of the current device (or managed memory):
+ *     host memory or another GPU's memory gives KFAC_ERR_INVALID (checked
+ *     last, right before the call enqueues its work).
  *     KFAC_ERR_CUDA reports a launch failure (cudaGetLastError after a
  *     launch); the stream may then hold part of the work.
  *   - Matrices are row-major with an explicit leading dimension (elements).

@@ -59,13 +59,15 @@ def _bind(path):
         lib.orc_precondition_rows.argtypes = [_dp, _L, _dp, _L, _dp, _lp, _L, _dp]
         lib.orc_weight_update.argtypes = [_dp, _dp, _L, _L, ctypes.c_double]
         lib.orc_is_refresh_step.argtypes = [_L, _L, _L]
+        lib.orc_pack_upper.argtypes = [_dp, _L, _dp]
+        lib.orc_unpack_upper.argtypes = [_dp, _L, _dp]
         lib.orc_bn_diag_fisher.argtypes = [_dp, _L, _L, ctypes.c_double, ctypes.c_double,
                                            _dp, _dp, _dp]
         for f in ("orc_im2col", "orc_gram", "orc_factor_ema", "orc_gram_entries",
                   "orc_weight_grad", "orc_pi_damping", "orc_cholesky_upper",
                   "orc_trtri_upper", "orc_lauum_upper", "orc_damped_inverse",
                   "orc_precondition", "orc_precondition_rows", "orc_bn_diag_fisher",
-                  "orc_weight_update", "orc_is_refresh_step"):
+                  "orc_weight_update", "orc_is_refresh_step", "orc_pack_upper", "orc_unpack_upper"):
             getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -244,6 +246,24 @@ def weight_update(w, P, eta):
 def is_refresh_step(t, warmup, every):
     """True when step t of the stale-factor schedule refreshes the factors and inverses."""
     return bool(_load().orc_is_refresh_step(int(t), int(warmup), int(every)))
+
+
+def pack_upper(F):
+    """Packed upper triangle of F [d, d]: row i's entries j >= i, row after row."""
+    F = _d(F)
+    d = F.shape[0]
+    out = np.empty(d * (d + 1) // 2)
+    assert _load().orc_pack_upper(_p(F), d, _p(out)) == 0
+    return out
+
+
+def unpack_upper(Fp, d):
+    """Symmetric [d, d] matrix from its packed upper triangle."""
+    Fp = _d(Fp)
+    assert Fp.size == d * (d + 1) // 2
+    F = np.empty((d, d))
+    assert _load().orc_unpack_upper(_p(Fp), d, _p(F)) == 0
+    return F
 
 
 def kfac_schedule(A0, G0, steps, xi, gamma, warmup, every):

@@ -402,6 +402,34 @@ int orc_weight_update(double *w, const double *P, long dG, long dA, double eta)
 }
 
 /*
+ * Packed storage of a symmetric factor (section 1, contributions: the
+ * symmetry of the Kronecker factors is exploited to reduce overhead).
+ * Reading: the upper triangle is kept row after row, row i holding the
+ * entries j = i .. d-1, so that entry (i, j), i <= j, sits at position
+ * i*d - i*(i+1)/2 + j of the d(d+1)/2 stored values.  pack reads the upper
+ * triangle of F [d][d]; unpack writes both triangles.
+ */
+int orc_pack_upper(const double *F, long d, double *out)
+{
+    long t = 0;
+    for (long i = 0; i < d; ++i)
+        for (long j = i; j < d; ++j) out[t++] = F[i * d + j];
+    return 0;
+}
+
+int orc_unpack_upper(const double *Fp, long d, double *F)
+{
+    long t = 0;
+    for (long i = 0; i < d; ++i)
+        for (long j = i; j < d; ++j) {
+            F[i * d + j] = Fp[t];
+            F[j * d + i] = Fp[t];
+            ++t;
+        }
+    return 0;
+}
+
+/*
  * Steps of the stale-factor schedule (Osawa et al. section 1: after a few
  * hundred iterations the Fisher matrix need not be refreshed every step):
  * step t (0-based) refreshes the factors and their inverses when

@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <vector>
 
@@ -106,6 +107,27 @@ EncodeIm2colFn encode_im2col_fn() {
             fn = (EncodeIm2colFn)p;
     });
     return fn;
+}
+
+// Every operand must be memory of the current device (or managed memory):
+// host memory or another GPU's memory is rejected before anything runs.
+bool on_this_device(const void *p) {
+    if (!p) return true;  // (null pointers are checked where they are not allowed)
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+        return false;
+    }
+    if (a.type == cudaMemoryTypeManaged) return true;
+    int dev = -1;
+    if (a.type != cudaMemoryTypeDevice || cudaGetDevice(&dev) != cudaSuccess) return false;
+    return a.device == dev;
+}
+
+bool all_on_this_device(std::initializer_list<const void *> ps) {
+    for (const void *p : ps)
+        if (!on_this_device(p)) return false;
+    return true;
 }
 
 namespace {
@@ -333,6 +355,8 @@ extern "C" kfac_status kfac_factor_update(const kfac_factor_desc *descs, int cou
     FactorPlan p;
     if ((s = plan_factor(descs, count, geo, ws, p, false)) != KFAC_OK) return s;
     if (!ws.fits()) return KFAC_ERR_WORKSPACE;
+    for (int i = 0; i < count; ++i)
+        if (!all_on_this_device({descs[i].x, descs[i].F})) return KFAC_ERR_INVALID;
     ws = Arena(workspace, workspace_bytes);
     p = FactorPlan();
     if ((s = plan_factor(descs, count, geo, ws, p, true)) != KFAC_OK) return s;
@@ -427,6 +451,11 @@ extern "C" kfac_status kfac_damp_invert(const kfac_invert_desc *descs, int count
     if (!ws.fits()) return KFAC_ERR_WORKSPACE;
     if (damp) dmp = damp;
     if (info) inf = info;
+    for (int i = 0; i < count; ++i) {
+        const kfac_invert_desc &d = descs[i];
+        if (!all_on_this_device({d.A, d.G, d.A_inv, d.G_inv, d.A_inv_bf16, d.G_inv_bf16, info, damp}))
+            return KFAC_ERR_INVALID;
+    }
     cudaStream_t st = (cudaStream_t)stream;
     KFAC_CUDA_TRY(cudaMemsetAsync(inf, 0, 2 * (size_t)count * sizeof(int), st));
     if ((s = damping_run(m.data(), count, gamma, pi_split, dmp, st)) != KFAC_OK) return s;
@@ -535,6 +564,10 @@ extern "C" kfac_status kfac_precondition(const kfac_precond_desc *descs, int cou
     PrecondPlan p;
     if ((s = plan_precond(descs, count, dtype, ws, p, false)) != KFAC_OK) return s;
     if (!ws.fits()) return KFAC_ERR_WORKSPACE;
+    for (int i = 0; i < count; ++i) {
+        const kfac_precond_desc &d = descs[i];
+        if (!all_on_this_device({d.G_inv, d.A_inv, d.grad, d.out, d.w})) return KFAC_ERR_INVALID;
+    }
     ws = Arena(workspace, workspace_bytes);
     p = PrecondPlan();
     if ((s = plan_precond(descs, count, dtype, ws, p, true)) != KFAC_OK) return s;

@@ -121,6 +121,10 @@ extern "C" kfac_status kfac_bn_diag_fisher(const kfac_bn_desc *descs, int count,
         if (!d.x || !d.F || !d.precond || d.C < 1) return KFAC_ERR_INVALID;
     }
     if (count == 0) return KFAC_OK;
+    for (int i = 0; i < count; ++i) {
+        const kfac_bn_desc &d = descs[i];
+        if (!all_on_this_device({d.x, d.F, d.precond, d.grad_mean})) return KFAC_ERR_INVALID;
+    }
     cudaStream_t st = (cudaStream_t)stream;
     std::unique_ptr<BnParams> P(new BnParams);
     int pos = 0;

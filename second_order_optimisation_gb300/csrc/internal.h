@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <initializer_list>
+
 #include "common.cuh"
 
 namespace kfac {
@@ -18,8 +20,10 @@ namespace kfac {
 //                   b_mn = 1: B stored [K][N] (N contiguous); 0: B stored [N][K].
 //                   syrk = 1: B is A (Gram matrix of a [K][M] source), only
 //                   tiles touching the upper triangle run and only i <= j is written.
-//   TC_KIND_TF32X3: K-major only (A [M][K], B [N][K]); maps come in (hi, lo)
-//                   pairs at consecutive indices; 3 MMAs per K slice.
+//   TC_KIND_TF32X3: K-major only (A [M][K], B [N][K]); an operand names a run
+//                   of four maps: hi with 128-row boxes, the (hi, lo) pair map
+//                   with 128-row boxes (tc_make_pair_map), hi and lo with 32-row
+//                   boxes; 3 MMAs per K slice.
 enum TcKind : int { TC_KIND_BF16 = 0, TC_KIND_TF32X3 = 1 };
 enum TcEpilogue : int {
     TC_EPI_ACCUM = 0,  // fp32 C[i][j] = beta*C[i][j] + alpha*acc (C read only if beta != 0)
@@ -78,6 +82,12 @@ struct TcJob {
 // 128-row boxes, then hi and lo with 32-row boxes (B of narrow tiles).
 bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int rows, int cols, int box_rows = 0,
                  bool f16 = false);
+// Tensor map of an fp32 (hi, lo) pair of row-major [rows][cols] matrices
+// (ld elements each; lo at a fixed byte offset after hi) as one 3-D tensor
+// [2][rows][cols]: a box is 128-byte rows x box_rows for both planes, hi
+// landing first and lo right after it (one copy instead of two).
+bool tc_make_pair_map(CUtensorMap *m, const float *hi, const float *lo, long long ld, int rows, int cols,
+                      int box_rows);
 // Im2col tensor map of a bf16 NHWC tensor [n][h][w][c] for a square k x k
 // convolution (stride, pad): 64 channels x 128 output pixels per load,
 // 128-byte swizzle.  Requires c % 64 == 0 and a 16-byte aligned base.
@@ -154,6 +164,11 @@ struct ColsumJob {
 // are bitwise reproducible.
 size_t colsum_partial_floats(const ColsumJob *jobs, int njobs);
 kfac_status colsum_run(const ColsumJob *jobs, int njobs, float *partial, cudaStream_t st);
+
+// True when p is device memory of the current device or managed memory (or
+// null); the entry points reject every other operand before enqueueing.
+bool on_this_device(const void *p);
+bool all_on_this_device(std::initializer_list<const void *> ps);
 
 // ----------------------------------------------------- inversion
 struct InvMatrix {

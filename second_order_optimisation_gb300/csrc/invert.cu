@@ -38,14 +38,16 @@ namespace kfac {
 namespace {
 
 constexpr int NB = 128;    // block width of the sweep
-// Lookahead: split each Cholesky update into the last panel's share (kept on
-// the chain) and the rest (on a side stream, overlapping the diag leaf and the
-// panel).  Measured on the ResNet-50 step it gained nothing (the side
-// launches' persistent CTAs hold SMs the chain needs next), so it is off.
-constexpr bool LOOKAHEAD = false;
+#ifndef KFAC_INV_FUSED_PANEL
+#define KFAC_INV_FUSED_PANEL 1
+#endif
+// The Cholesky panel below each diagonal block: formed by the diag kernel's
+// other CTAs (1), or by a separate engine launch (0).  A tuning constant that
+// may be set at build time.
+constexpr bool FUSED_PANEL = KFAC_INV_FUSED_PANEL;
 constexpr int MAT_MAX = 224;
-// tensor maps of one matrix: X, Wt, LT pairs, each as hi / lo with 128-row
-// and with 32-row boxes
+// tensor maps of one matrix: X, Wt, LT pairs, each as hi and the (hi, lo)
+// pair with 128-row boxes, and hi / lo with 32-row boxes
 constexpr int MAPS_PER_MATRIX = 12;
 
 inline int padded(int d) { return (int)ceil_div(d, NB) * NB; }
@@ -113,6 +115,7 @@ struct TileMat {
     const float *F;   // factor (upper triangle read)
     long long ldf;    // -1: packed upper triangle (entry (i, j) at i*d - i*(i+1)/2 + j)
     float *Xh, *Xl;   // working pair [dp][dp]
+    float *Dh, *Dl;   // diagonal 128 x 128 blocks, stacked [dp][128]
     int d, dp;
     int damp_idx;
     int tiles;        // 64-wide tiles per side
@@ -208,6 +211,11 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ TileP
             const long long o = (long long)i * q.dp + tj * TT + c4;
             *reinterpret_cast<float4 *>(q.Xh + o) = make_float4(h[0], h[1], h[2], h[3]);
             *reinterpret_cast<float4 *>(q.Xl + o) = make_float4(l[0], l[1], l[2], l[3]);
+            if ((ti * TT) / NB == (tj * TT) / NB) {  // inside a diagonal 128-block: also into D
+                const long long od = (long long)i * NB + (tj * TT) % NB + c4;
+                *reinterpret_cast<float4 *>(q.Dh + od) = make_float4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<float4 *>(q.Dl + od) = make_float4(l[0], l[1], l[2], l[3]);
+            }
         }
     }
 }
@@ -215,195 +223,299 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ TileP
 // ------------------------------------------------------------------ diag
 
 struct DiagJob {
-    float *Xh, *Xl;    // block (k, k) of the working pair: its lower triangle is read, then
-                       // W_kk = L_kk^-1 written over the whole block (zeros above the diagonal)
-    float *Th, *Tl;    // the same block of the transposed pair: W_kk^T (zeros below)
+    const float *Sh, *Sl;  // the Schur-complement block S_kk (lower triangle read), row pitch NB;
+                           // no CTA of the launch writes it
+    float *Xh, *Xl;    // (owner) block (k, k) of the working pair: W_kk = L_kk^-1 written over
+                       // the whole block (zeros above the diagonal)
+    float *Th, *Tl;    // (owner) the same block of the transposed pair: W_kk^T (zeros below)
+    const float *Ph, *Pl;  // (panel) block (i, k) of the working pair, i > k
+    float *Lh, *Ll;        // (panel) where its Cholesky panel L_ik = X_ik W_kk^T goes
     long long ld;
     int o;             // global index of the block's first row (for info)
+    int panel;         // 0: the owner of the diagonal block, 1: one panel block
     int *info;
 };
 
+constexpr int DIAG_MAX = 300;  // CTAs per diag launch (parameter block < 32 KB)
 struct DiagParams {
-    DiagJob j[MAT_MAX];
+    DiagJob j[DIAG_MAX];
     int n;
 };
 
 // Cholesky factor and its inverse of one SPD 128 x 128 block S = L L^T, by
-// one CTA of 512 threads: W = L^-1, written over the block and, transposed,
-// into the same block of the transposed pair.
-//
-// The sweep works on one array M (the lower triangle, in shared memory) that
-// holds the Schur complement still to be factored in its columns past the
-// current pivots and the rows of W in progress in the columns before.  A
-// single pivot c, with w = 1 / sqrt(M_cc) and p_i = w M_ic (= L_ic), does
-//   i > c, j < c:      M_ij -= p_i (w M_cj)    (rows of W in progress)
-//   i > c, j = c:      M_ic  = -p_i w
-//   i > c, c < j <= i: M_ij -= p_i p_j         (Schur complement)
-//   i = c, j < c:      M_cj *= w;   M_cc = w   (row c of W final)
-// The kernel runs these rules 8 pivots K = {c .. c+7} at a time:
-//   1. each of threads 0..127 applies them to the 8 x 8 pivot block alone
-//      (straight-line code on registers), giving W_K, and forms row j = tid
-//      of Z [128 x 8]:
-//        Z_j = W_K M[K][j]      (j before K: the final rows K of W, as columns)
-//        Z_j = W_K^T e_(j-c)    (j in K)
-//        Z_j = W_K M[j][K]      (j past K: the panel L_jK);
-//   2. rows K:         M[K][j] = Z_j (j before K),  M[K][K] = W_K;
-//      rows i past K:  M_ij = (j in K ? 0 : M_ij) - Z_i . Z_j  (j <= i),
-//      one row and 8 columns per item, consecutive threads on consecutive rows
-//      (the Z_i reads are contiguous, the Z_j reads broadcasts).
+// one CTA of 256 threads: W = L^-1.  The owner CTA of a diagonal block writes
+// W over the block and, transposed, into the same block of the transposed
+// pair; each other CTA of the block column recomputes W (no CTA waits for
+// another) and turns one block X_ik below it into the Cholesky panel
+// L_ik = X_ik W^T (fp32 on CUDA cores, 8 x 8 outputs per thread).  Both steps
+// of W run in shared memory, blocked by DB = 16:
+//   1. right-looking Cholesky, for each 16-wide block column c:
+//        L_cc = chol(S_cc)            one warp, lane r holding row r of the
+//                                     16 x 16 block in registers; column
+//                                     values by shuffle
+//        L_ic = S_ic L_cc^-T          i past c: a thread per row (forward
+//                                     substitution with L_cc)
+//        S_ij -= L_ic L_jc^T          i >= j past c: 4 x 4 register tiles
+//   2. W = L^-1 by block rows: the diagonal blocks W_ii = L_ii^-1 at once (a
+//      thread per column), then for i = 1 .. 7
+//        T_ij = sum_{t=j}^{i-1} L_it W_tj,   W_ij = -W_ii T_ij   (j < i).
 // 1 / sqrt is the hardware approximation refined by one Newton-Raphson step,
 // y <- y (3 - x y^2) / 2.  A pivot outside [FLT_MIN, inf) is recorded and
-// eliminated with w = 0 (the result is then undefined but finite).
-constexpr int DLD = NB + 4;  // M row pitch (floats; rows stay 16-byte aligned)
-constexpr int DIAG_THREADS = 512;
-constexpr size_t DIAG_SMEM = ((size_t)NB * DLD + (size_t)NB * 8 + 64 + 4) * sizeof(float);
+// eliminated with w = 0 (the result is then undefined; finite unless the
+// block held NaN or inf).
+constexpr int DLD = NB + 4;  // row pitch (floats; rows stay 16-byte aligned)
+constexpr int DB = 16;       // blocking of both steps
+constexpr int DIAG_THREADS = 256;
+constexpr size_t DIAG_SMEM = (2 * (size_t)NB * DLD + NB + 4) * sizeof(float);
 
 __device__ __forceinline__ float rsqrt_nr(float x) {
     const float y = rsqrtf(x);
     return y * fmaf(-0.5f * x * y, y, 1.5f);
 }
 
-// The single-pivot rules on an 8 x 8 lower block alone, in registers (every
-// loop has constant bounds so that the block stays in registers): W_K in
-// place; returns the first pivot (0..7) outside [FLT_MIN, inf), or -1.
-__device__ __forceinline__ int pivot8(float (&w)[8][8]) {
-    int bad = -1;
+__device__ __forceinline__ void ld16(const float *src, float (&x)[DB]) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const float piv = w[q][q];
-        const bool ok = piv >= FLT_MIN && piv < INFINITY;
-        const float wq = ok ? rsqrt_nr(piv) : 0.f;
-        bad = (!ok && bad < 0) ? q : bad;
-        float p[8], rowq[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) p[r] = r > q ? w[r][q] * wq : 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) rowq[j] = wq * w[q][j];
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (r <= q || j > r) continue;
-                if (j < q) w[r][j] = fmaf(-p[r], rowq[j], w[r][j]);
-                else if (j == q) w[r][j] = -p[r] * wq;
-                else w[r][j] = fmaf(-p[r], p[j], w[r][j]);
-            }
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (j < q) w[q][j] *= wq;
-        w[q][q] = wq;
+    for (int q = 0; q < DB; q += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(src + q);
+        x[q] = v.x; x[q + 1] = v.y; x[q + 2] = v.z; x[q + 3] = v.w;
     }
-    return bad;
+}
+
+__device__ __forceinline__ void st16(float *dst, const float (&x)[DB]) {
+#pragma unroll
+    for (int q = 0; q < DB; q += 4) *reinterpret_cast<float4 *>(dst + q) = make_float4(x[q], x[q + 1], x[q + 2], x[q + 3]);
 }
 
 __global__ void __launch_bounds__(DIAG_THREADS, 1) diag_kernel(const __grid_constant__ DiagParams P) {
     extern __shared__ float4 diag_smem4[];
-    float *M = reinterpret_cast<float *>(diag_smem4);
-    float *Z = M + NB * DLD;       // [NB][8]
-    float *wk = Z + NB * 8;          // [8][8]
-    int *bad_s = reinterpret_cast<int *>(wk + 64);
+    float *M = reinterpret_cast<float *>(diag_smem4);  // S, then L (lower triangle)
+    float *Wm = M + NB * DLD;                           // W (lower triangle)
+    float *invd = Wm + NB * DLD;                        // 1 / L_ii
+    int *bad_s = reinterpret_cast<int *>(invd + NB);    // first failing pivot (NB: none)
     const DiagJob &J = P.j[blockIdx.x];
-    const int tid = threadIdx.x, lane = tid & 31;
-    if (tid == 0) *bad_s = -1;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) *bad_s = NB;
     pdl_wait();
     pdl_trigger();
     for (int e = tid; e < NB * NB / 4; e += DIAG_THREADS) {
         const int i = e >> 5, j = (e & 31) * 4;
-        const long long off = (long long)i * J.ld + j;
-        const float4 h = *reinterpret_cast<const float4 *>(J.Xh + off);
-        const float4 l = *reinterpret_cast<const float4 *>(J.Xl + off);
+        const float4 h = *reinterpret_cast<const float4 *>(J.Sh + i * NB + j);
+        const float4 l = *reinterpret_cast<const float4 *>(J.Sl + i * NB + j);
         *reinterpret_cast<float4 *>(M + i * DLD + j) = make_float4(h.x + l.x, h.y + l.y, h.z + l.z, h.w + l.w);
     }
     __syncthreads();
+
+    // 1. Cholesky
 #pragma unroll 1
-    for (int s = 0; s < NB / 8; ++s) {
-        const int c = 8 * s, E = c + 8;
-        // 1. + 2. Z rows, one per thread t < 128; each such thread first turns
-        //    the 8 x 8 pivot block into W_K itself (the single-pivot rules on
-        //    the block alone, in registers): j < c: W_K M[K][j];  j in K:
-        //    W_K^T e;  j past K: W_K M[j][K]
-        if (tid < NB) {
-            float w[8][8];
+    for (int c = 0; c < NB; c += DB) {
+        if (warp == 0) {
+            const int r = lane & (DB - 1);  // lanes 16..31 repeat rows 0..15 (only 0..15 store)
+            float a[DB];
+            ld16(M + (c + r) * DLD + c, a);
+            float wr = 0.f;
+            int bad = -1;
 #pragma unroll
-            for (int r = 0; r < 8; ++r)
+            for (int q = 0; q < DB; ++q) {
+                const float piv = __shfl_sync(0xffffffffu, a[q], q);
+                const bool ok = piv >= FLT_MIN && piv < INFINITY;
+                const float w = ok ? rsqrt_nr(piv) : 0.f;
+                bad = (!ok && bad < 0) ? q : bad;
+                if (r == q) {
+                    a[q] = ok ? piv * w : 0.f;  // L_qq
+                    wr = w;
+                } else if (r > q) {
+                    a[q] *= w;                  // L_rq
+                }
 #pragma unroll
-                for (int q = 0; q < 8; ++q) w[r][q] = q <= r ? M[(c + r) * DLD + c + q] : 0.f;
-            const int bad = pivot8(w);
-            if (tid == 0) {
-#pragma unroll
-                for (int r = 0; r < 8; ++r)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) wk[r * 8 + q] = w[r][q];
-                if (bad >= 0 && *bad_s < 0) *bad_s = c + bad;
+                for (int j = 1; j < DB; ++j) {
+                    if (j > q) {
+                        const float lj = __shfl_sync(0xffffffffu, a[q], j);
+                        if (r >= j) a[j] = fmaf(-a[q], lj, a[j]);
+                    }
+                }
             }
-            // Z_j = W_K x with x = M[K][j] (j before K), e_(j-c) (j in K), M[j][K] (j past K)
-            const int j = tid;
-            float x[8];
-            if (j < c) {
-#pragma unroll
-                for (int r = 0; r < 8; ++r) x[r] = M[(c + r) * DLD + j];
-            } else if (j < E) {
-#pragma unroll
-                for (int r = 0; r < 8; ++r) x[r] = j - c == r ? 1.f : 0.f;
-            } else {
-                const float4 a = *reinterpret_cast<const float4 *>(M + j * DLD + c);
-                const float4 b = *reinterpret_cast<const float4 *>(M + j * DLD + c + 4);
-                x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+            if (lane < DB) {
+                st16(M + (c + r) * DLD + c, a);
+                invd[c + r] = wr;
             }
-            float z[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                float acc = 0.f;
-#pragma unroll
-                for (int r = 0; r < 8; ++r) acc = r <= q ? fmaf(w[q][r], x[r], acc) : acc;
-                z[q] = acc;
-            }
-            *reinterpret_cast<float4 *>(Z + j * 8) = make_float4(z[0], z[1], z[2], z[3]);
-            *reinterpret_cast<float4 *>(Z + j * 8 + 4) = make_float4(z[4], z[5], z[6], z[7]);
+            if (lane == 0 && bad >= 0) atomicMin(bad_s, c + bad);
         }
         __syncthreads();
-        // 3. rows K: M[K][j] = Z_j (j < c), W_K on the pivot block
-        for (int e = tid; e < 8 * E; e += DIAG_THREADS) {
-            const int q = e / E, j = e - q * E;
-            if (j < c) M[(c + q) * DLD + j] = Z[j * 8 + q];
-            else if (j - c <= q) M[(c + q) * DLD + j] = wk[q * 8 + (j - c)];
+        const int nrest = NB - c - DB;
+        if (tid < nrest) {  // the panel: row i solves L_cc y = S_ic^T
+            const int i = c + DB + tid;
+            float x[DB];
+            ld16(M + i * DLD + c, x);
+#pragma unroll
+            for (int q = 0; q < DB; ++q) {
+                x[q] *= invd[c + q];
+#pragma unroll
+                for (int j = q + 1; j < DB; ++j) x[j] = fmaf(-x[q], M[(c + j) * DLD + c + q], x[j]);
+            }
+            st16(M + i * DLD + c, x);
         }
-        //    rows past K, one row i and 8 columns 8J .. 8J+7 (8J <= i) per
-        //    item, consecutive threads on consecutive rows:
-        //    M_ij = (j in K ? 0 : M_ij) - Z_i . Z_j  for j <= i
-        for (int J = tid >> 7; J < 16; J += DIAG_THREADS / NB) {
-            const int i = tid & (NB - 1);
-            if (i < E || 8 * J > i) continue;
+        __syncthreads();
+        // the trailing update, 4 x 4 tiles (I, Jt) of the lower triangle past c
+        const int nT = nrest / 4;
+        const int ntiles = nT * (nT + 1) / 2;
+        for (int t = tid; t < ntiles; t += DIAG_THREADS) {
+            int I = (int)((sqrtf(8.f * (float)t + 1.f) - 1.f) * 0.5f);
+            while (I * (I + 1) / 2 > t) --I;
+            while ((I + 1) * (I + 2) / 2 <= t) ++I;
+            const int Jt = t - I * (I + 1) / 2;
+            const int i0 = c + DB + 4 * I, j0 = c + DB + 4 * Jt;
+            float acc[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 v = *reinterpret_cast<const float4 *>(M + (i0 + u) * DLD + j0);
+                acc[u][0] = v.x; acc[u][1] = v.y; acc[u][2] = v.z; acc[u][3] = v.w;
+            }
+#pragma unroll
+            for (int q = 0; q < DB; q += 4) {
+                float4 li[4], lj[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    li[u] = *reinterpret_cast<const float4 *>(M + (i0 + u) * DLD + c + q);
+                    lj[u] = *reinterpret_cast<const float4 *>(M + (j0 + u) * DLD + c + q);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        float x = acc[u][v];
+                        x = fmaf(-li[u].x, lj[v].x, x);
+                        x = fmaf(-li[u].y, lj[v].y, x);
+                        x = fmaf(-li[u].z, lj[v].z, x);
+                        acc[u][v] = fmaf(-li[u].w, lj[v].w, x);
+                    }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (I != Jt) {
+                    *reinterpret_cast<float4 *>(M + (i0 + u) * DLD + j0) =
+                        make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+                } else {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        if (v <= u) M[(i0 + u) * DLD + j0 + v] = acc[u][v];
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // 2. W = L^-1: diagonal blocks, a thread per column q of block b
+    if (tid < NB) {
+        const int b = (tid / DB) * DB, q = tid % DB;
+        float x[DB];
+#pragma unroll
+        for (int r = 0; r < DB; ++r) {
+            float v = r == q ? 1.f : 0.f;
+#pragma unroll
+            for (int t = 0; t < r; ++t) v = fmaf(-M[(b + r) * DLD + b + t], x[t], v);
+            x[r] = v * invd[b + r];
+        }
+#pragma unroll
+        for (int r = 0; r < DB; ++r) Wm[(b + r) * DLD + b + q] = x[r];
+    }
+    __syncthreads();
+    //    block rows i = 1 .. 7
+#pragma unroll 1
+    for (int i = DB; i < NB; i += DB) {
+        // T_ij = sum_{t=j}^{i-1} L_it W_tj: thread (j, r, half) -> 8 entries of row r of T_ij
+        const int nb = i / DB;
+        if (tid < nb * 32) {
+            const int j = (tid >> 5) * DB, r = (tid & 31) >> 1, h = (tid & 1) * 8;
             float acc[8];
-            {
-                const float4 a = *reinterpret_cast<const float4 *>(M + i * DLD + 8 * J);
-                const float4 b = *reinterpret_cast<const float4 *>(M + i * DLD + 8 * J + 4);
-                acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w; acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
-            }
-            if (8 * J == c) {  // the columns K take -Z_i . W_K
 #pragma unroll
-                for (int v = 0; v < 8; ++v) acc[v] = 0.f;
+            for (int v = 0; v < 8; ++v) acc[v] = 0.f;
+            const float *lrow = M + (i + r) * DLD;
+#pragma unroll 4
+            for (int k = j; k < i; ++k) {
+                const float l = lrow[k];
+                const float4 w0 = *reinterpret_cast<const float4 *>(Wm + k * DLD + j + h);
+                const float4 w1 = *reinterpret_cast<const float4 *>(Wm + k * DLD + j + h + 4);
+                acc[0] = fmaf(l, w0.x, acc[0]); acc[1] = fmaf(l, w0.y, acc[1]);
+                acc[2] = fmaf(l, w0.z, acc[2]); acc[3] = fmaf(l, w0.w, acc[3]);
+                acc[4] = fmaf(l, w1.x, acc[4]); acc[5] = fmaf(l, w1.y, acc[5]);
+                acc[6] = fmaf(l, w1.z, acc[6]); acc[7] = fmaf(l, w1.w, acc[7]);
             }
-            const float4 za = *reinterpret_cast<const float4 *>(Z + i * 8);
-            const float4 zb = *reinterpret_cast<const float4 *>(Z + i * 8 + 4);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                const float4 a = *reinterpret_cast<const float4 *>(Z + (8 * J + v) * 8);
-                const float4 b = *reinterpret_cast<const float4 *>(Z + (8 * J + v) * 8 + 4);
-                float x = acc[v];
-                x = fmaf(-za.x, a.x, x); x = fmaf(-za.y, a.y, x); x = fmaf(-za.z, a.z, x); x = fmaf(-za.w, a.w, x);
-                x = fmaf(-zb.x, b.x, x); x = fmaf(-zb.y, b.y, x); x = fmaf(-zb.z, b.z, x); acc[v] = fmaf(-zb.w, b.w, x);
-            }
-            if (8 * J + 7 <= i) {
-                *reinterpret_cast<float4 *>(M + i * DLD + 8 * J) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                *reinterpret_cast<float4 *>(M + i * DLD + 8 * J + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-            } else {
-#pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    if (8 * J + v <= i) M[i * DLD + 8 * J + v] = acc[v];
-            }
+            *reinterpret_cast<float4 *>(Wm + (i + r) * DLD + j + h) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            *reinterpret_cast<float4 *>(Wm + (i + r) * DLD + j + h + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
         }
         __syncthreads();
+        // W_ij = -W_ii T_ij, in place: thread (j, q) owns column q of block (i, j)
+        if (tid < nb * DB) {
+            const int j = (tid / DB) * DB, q = tid % DB;
+            float tcol[DB], y[DB];
+#pragma unroll
+            for (int v = 0; v < DB; ++v) tcol[v] = Wm[(i + v) * DLD + j + q];
+#pragma unroll
+            for (int r = 0; r < DB; ++r) {
+                float a = 0.f;
+#pragma unroll
+                for (int v = 0; v <= r; ++v) a = fmaf(Wm[(i + r) * DLD + i + v], tcol[v], a);
+                y[r] = -a;
+            }
+#pragma unroll
+            for (int r = 0; r < DB; ++r) Wm[(i + r) * DLD + j + q] = y[r];
+        }
+        __syncthreads();
+    }
+
+    if (J.panel) {
+        // L_ik = X_ik W^T: X_ik (hi + lo) into M, then thread (ti, tj) forms
+        // rows ti + 16 a (a < 8) and columns 8 tj .. 8 tj + 7; W is lower
+        // triangular, so K stops at the block's last column (W's upper
+        // entries inside a 16-block are the zeros written above)
+        for (int e = tid; e < NB * NB / 4; e += DIAG_THREADS) {
+            const int i = e >> 5, j = (e & 31) * 4;
+            const long long off = (long long)i * J.ld + j;
+            const float4 h = *reinterpret_cast<const float4 *>(J.Ph + off);
+            const float4 l = *reinterpret_cast<const float4 *>(J.Pl + off);
+            *reinterpret_cast<float4 *>(M + i * DLD + j) = make_float4(h.x + l.x, h.y + l.y, h.z + l.z, h.w + l.w);
+        }
+        __syncthreads();
+        const int ti = tid & 15, tj = tid >> 4;
+        float acc[8][8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a)
+#pragma unroll
+            for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+        const int kend = 8 * tj + 8;
+#pragma unroll 1
+        for (int t = 0; t < kend; t += 4) {
+            float4 w4[8];
+#pragma unroll
+            for (int b = 0; b < 8; ++b) w4[b] = *reinterpret_cast<const float4 *>(Wm + (8 * tj + b) * DLD + t);
+#pragma unroll
+            for (int a = 0; a < 8; ++a) {
+                const float4 x4 = *reinterpret_cast<const float4 *>(M + (ti + 16 * a) * DLD + t);
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    float v = acc[a][b];
+                    v = fmaf(x4.x, w4[b].x, v);
+                    v = fmaf(x4.y, w4[b].y, v);
+                    v = fmaf(x4.z, w4[b].z, v);
+                    acc[a][b] = fmaf(x4.w, w4[b].w, v);
+                }
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+            const long long off = (long long)(ti + 16 * a) * J.ld + 8 * tj;
+            float h[8], l[8];
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                h[b] = tf32_hi(acc[a][b]);
+                l[b] = acc[a][b] - h[b];
+            }
+            *reinterpret_cast<float4 *>(J.Lh + off) = make_float4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<float4 *>(J.Lh + off + 4) = make_float4(h[4], h[5], h[6], h[7]);
+            *reinterpret_cast<float4 *>(J.Ll + off) = make_float4(l[0], l[1], l[2], l[3]);
+            *reinterpret_cast<float4 *>(J.Ll + off + 4) = make_float4(l[4], l[5], l[6], l[7]);
+        }
+        return;
     }
     // W (lower, zeros above) into X and W^T (upper, zeros below) into the transposed pair
     for (int e = tid; e < NB * NB / 4; e += DIAG_THREADS) {
@@ -411,8 +523,8 @@ __global__ void __launch_bounds__(DIAG_THREADS, 1) diag_kernel(const __grid_cons
         float w4[4], t4[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            w4[u] = j + u <= i ? M[i * DLD + j + u] : 0.f;
-            t4[u] = i <= j + u ? M[(j + u) * DLD + i] : 0.f;
+            w4[u] = j + u <= i ? Wm[i * DLD + j + u] : 0.f;
+            t4[u] = i <= j + u ? Wm[(j + u) * DLD + i] : 0.f;
         }
         float hw[4], ht[4];
 #pragma unroll
@@ -428,7 +540,7 @@ __global__ void __launch_bounds__(DIAG_THREADS, 1) diag_kernel(const __grid_cons
         *reinterpret_cast<float4 *>(J.Tl + off) =
             make_float4(t4[0] - ht[0], t4[1] - ht[1], t4[2] - ht[2], t4[3] - ht[3]);
     }
-    if (tid == 0 && *bad_s >= 0 && J.info) atomicCAS(J.info, 0, J.o + *bad_s + 1);
+    if (tid == 0 && *bad_s < NB && J.info) atomicCAS(J.info, 0, J.o + *bad_s + 1);
     __syncthreads();
 }
 
@@ -438,7 +550,7 @@ __global__ void __launch_bounds__(DIAG_THREADS, 1) diag_kernel(const __grid_cons
 // go into the same launch.
 struct Op {
     int leaf;
-    DiagJob dj;
+    std::vector<DiagJob> dj;  // leaf: the owner of the diagonal block, then its panel blocks
     std::vector<TcJob> g;
     std::vector<TcJob> side;  // engine problems that may start once this op is done (lookahead,
                               // launched on the group's side stream)
@@ -455,6 +567,7 @@ struct Op {
 struct MatWork {
     int d, dp;
     float *Xh, *Xl, *Wh, *Wl, *Lh, *Ll;
+    float *Dh, *Dl;  // diagonal 128 x 128 blocks of the Schur complement, stacked [dp][128]
     int mx, mw, ml;  // map indices (hi; lo at +1; 32-row boxes at +2, +3)
 };
 
@@ -484,14 +597,11 @@ int tri_nodes(int o, int n, std::vector<std::vector<std::pair<int, int>>> &by_he
 
 // The chain of one matrix.
 //  1. left-looking blocked Cholesky, 128-wide block columns k:
-//       X[k:, k] -= L[k:, :k] L[k, :k]^T                 (engine; k > 0)
-//       W_kk = L_kk^-1 from X[k, k]                      (diag leaf)
-//       L[k+1:, k] = X[k+1:, k] W_kk^T                   (engine; the panel)
-//     every Schur-complement column comes from Cholesky panels (no growth).
-//     The update of column k by panels 0 .. k-2 needs nothing later than
-//     panel k-2: it runs as a side problem once that panel is done (on the
-//     group's side stream, while the diag leaf and panel of k-1 run), and
-//     only the update by panel k-1 (K = 128) stays on the chain;
+//       D_k = X[k, k] - L[k, :k] L[k, :k]^T,
+//       X[k+1:, k] -= L[k+1:, :k] L[k, :k]^T              (engine; k > 0)
+//       W_kk = L_kk^-1 from D_k, and the panel
+//       L[k+1:, k] = X[k+1:, k] W_kk^T                   (diag kernel, a CTA per block)
+//     every Schur-complement column comes from Cholesky panels (no growth);
 //  2. W = L^-1 by recursive 2 x 2 blocking, bottom up by height (the two
 //     halves of a node are independent):
 //       T = L21 W11,   W21 = -W22 T   (W21 over X's lower part, W21^T into Wt);
@@ -503,43 +613,39 @@ int tri_nodes(int o, int n, std::vector<std::vector<std::pair<int, int>>> &by_he
 void gen_chain(std::vector<Op> &ops, const MatWork &w, const InvMatrix &mat, int *info) {
     const long long ld = w.dp;
     const int nb = w.dp / NB;
-    std::vector<int> panel_op(nb, -1);
     for (int k = 0; k < nb; ++k) {
         const int kb = k * NB;
-        if (k > 0 && !LOOKAHEAD) {
+        const float *Dh = w.Dh + (long long)kb * NB, *Dl = w.Dl + (long long)kb * NB;
+        if (k > 0) {
+            // the diagonal block into D, the blocks below it in X
             Op op{};
-            op.g.push_back(split_job(w.ml, kb, 0, w.ml, kb, 0, w.dp - kb, NB, kb, -1.f, 1.f, w.Xh + kb * ld + kb,
-                                     w.Xl + kb * ld + kb, nullptr, nullptr, ld));
-            ops.push_back(op);
-        } else if (k > 0) {
-            // the update by the last panel (k - 1) stays on the chain; the
-            // earlier panels' share ran as the lookahead of panel k - 2
-            Op op{};
-            op.g.push_back(split_job(w.ml, kb, kb - NB, w.ml, kb, kb - NB, w.dp - kb, NB, NB, -1.f, 1.f,
-                                     w.Xh + kb * ld + kb, w.Xl + kb * ld + kb, nullptr, nullptr, ld));
-            if (k >= 2) op.needs_side = panel_op[k - 2];
+            op.g.push_back(split_job(w.ml, kb, 0, w.ml, kb, 0, NB, NB, kb, -1.f, 1.f, w.Dh + (long long)kb * NB,
+                                     w.Dl + (long long)kb * NB, nullptr, nullptr, NB));
+            if (k + 1 < nb)
+                op.g.push_back(split_job(w.ml, kb + NB, 0, w.ml, kb, 0, w.dp - kb - NB, NB, kb, -1.f, 1.f,
+                                         w.Xh + (kb + NB) * ld + kb, w.Xl + (kb + NB) * ld + kb, nullptr, nullptr,
+                                         ld));
             ops.push_back(op);
         }
-        {
-            Op op{};
-            op.leaf = 1;
-            op.dj = DiagJob{w.Xh + kb * ld + kb, w.Xl + kb * ld + kb, w.Wh + kb * ld + kb, w.Wl + kb * ld + kb,
-                            ld, kb, info};
-            ops.push_back(op);
+        // W_kk and the panel L[k+1:, k] = X[k+1:, k] W_kk^T, one CTA per block;
+        // every CTA reads S_kk from D, which no CTA of the launch writes (the
+        // owner writes W_kk over X's block)
+        Op op{};
+        op.leaf = 1;
+        op.dj.push_back(DiagJob{Dh, Dl, w.Xh + kb * ld + kb, w.Xl + kb * ld + kb, w.Wh + kb * ld + kb,
+                                w.Wl + kb * ld + kb, nullptr, nullptr, nullptr, nullptr, ld, kb, 0, info});
+        for (int i = k + 1; FUSED_PANEL && i < nb; ++i) {
+            const long long c = (long long)i * NB * ld + kb;
+            op.dj.push_back(DiagJob{Dh, Dl, nullptr, nullptr, nullptr, nullptr, w.Xh + c, w.Xl + c, w.Lh + c, w.Ll + c,
+                                    ld, kb, 1, nullptr});
         }
-        if (k + 1 < nb) {
+        ops.push_back(op);
+        if (!FUSED_PANEL && k + 1 < nb) {  // L[k+1:, k] = X[k+1:, k] W_kk^T on the engine
             const long long c = (long long)(kb + NB) * ld + kb;
-            Op op{};
-            op.g.push_back(split_job(w.mx, kb + NB, kb, w.mx, kb, kb, w.dp - kb - NB, NB, NB, 1.f, 0.f, w.Lh + c,
+            Op pn{};
+            pn.g.push_back(split_job(w.mx, kb + NB, kb, w.mx, kb, kb, w.dp - kb - NB, NB, NB, 1.f, 0.f, w.Lh + c,
                                      w.Ll + c, nullptr, nullptr, ld));
-            if (k + 2 < nb && LOOKAHEAD) {
-                // lookahead: X[k2:, k2] -= L[k2:, :k+1] L[k2, :k+1]^T for block column k2 = k + 2
-                const int k2b = (k + 2) * NB;
-                op.side.push_back(split_job(w.ml, k2b, 0, w.ml, k2b, 0, w.dp - k2b, NB, kb + NB, -1.f, 1.f,
-                                            w.Xh + k2b * ld + k2b, w.Xl + k2b * ld + k2b, nullptr, nullptr, ld));
-            }
-            panel_op[k] = (int)ops.size();
-            ops.push_back(op);
+            ops.push_back(pn);
         }
     }
     std::vector<std::vector<std::pair<int, int>>> by_height;
@@ -637,7 +743,11 @@ std::vector<std::vector<std::pair<int, int>>> schedule_rounds(const std::vector<
 // path of the call) on a high-priority stream, all others on a low-priority
 // stream whose engine launches leave SMs free for the first group.  Each
 // group has its own rounds and engine scratch.
-constexpr int RESERVED_SMS = 32;   // SMs the second group's engine launches leave free
+#ifndef KFAC_INV_RESERVED_SMS
+#define KFAC_INV_RESERVED_SMS 32
+#endif
+constexpr int RESERVED_SMS = KFAC_INV_RESERVED_SMS;  // SMs the second group's engine launches leave free
+                                                     // (a tuning constant that may be set at build time)
 constexpr int SIDE_FREE_SMS = 48;  // SMs a group's side launches leave to its own chain
 constexpr int SIDE_GROUPS = 1;     // groups whose lookahead updates run on a side stream (the others
                                    // run them in their own stream, right after the enabling round)
@@ -682,18 +792,22 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
         w.Wh = ws.take<float>(sq);
         w.Wl = ws.take<float>(sq);
         w.Lh = w.Ll = nullptr;
+        w.Dh = ws.take<float>((size_t)w.dp * NB);
+        w.Dl = ws.take<float>((size_t)w.dp * NB);
         if (w.dp > NB) {
             w.Lh = ws.take<float>(sq);
             w.Ll = ws.take<float>(sq);
         }
         float *bufs[6] = {w.Xh, w.Xl, w.Wh, w.Wl, w.Lh, w.Ll};
         const int base = (int)p.maps.size();
-        for (int q = 0; q < 6; q += 2)  // per pair: hi, lo (128-row boxes), hi, lo (32-row boxes)
+        for (int q = 0; q < 6; q += 2)  // per pair: hi, the (hi, lo) pair (128-row boxes), hi, lo (32-row boxes)
             for (int v = 0; v < 4; ++v) {
                 p.maps.emplace_back();
-                if (encode && bufs[q] &&
-                    !tc_make_map(&p.maps.back(), TC_KIND_TF32X3, bufs[q + (v & 1)], w.dp, w.dp, w.dp, v < 2 ? 128 : 32))
-                    return KFAC_ERR_CUDA;
+                if (!encode || !bufs[q]) continue;
+                const bool ok = v == 1 ? tc_make_pair_map(&p.maps.back(), bufs[q], bufs[q + 1], w.dp, w.dp, w.dp, 128)
+                                       : tc_make_map(&p.maps.back(), TC_KIND_TF32X3, bufs[q + (v & 1)], w.dp, w.dp,
+                                                     w.dp, v < 2 ? 128 : 32);
+                if (!ok) return KFAC_ERR_CUDA;
             }
         w.mx = base;
         w.mw = base + 4;
@@ -767,16 +881,19 @@ cudaError_t diag_smem_attr() {
 
 // One launch per round of leaves (one CTA per diagonal block).
 kfac_status diag_launch(const std::vector<DiagJob> &jobs, cudaStream_t st) {
-    for (const DiagJob &j : jobs)  // the kernel writes rows in 16-byte pieces
-        if (j.ld % 4 != 0 || (uintptr_t)j.Xh % 16 != 0 || (uintptr_t)j.Xl % 16 != 0 || (uintptr_t)j.Th % 16 != 0 ||
-            (uintptr_t)j.Tl % 16 != 0)
+    for (const DiagJob &j : jobs)  // the kernel reads and writes rows in 16-byte pieces
+        if (j.ld % 4 != 0 || !j.Sh || !j.Sl || (uintptr_t)j.Sh % 16 != 0 || (uintptr_t)j.Sl % 16 != 0 ||
+            (uintptr_t)j.Xh % 16 != 0 || (uintptr_t)j.Xl % 16 != 0 || (uintptr_t)j.Th % 16 != 0 ||
+            (uintptr_t)j.Tl % 16 != 0 || (uintptr_t)j.Ph % 16 != 0 || (uintptr_t)j.Pl % 16 != 0 ||
+            (uintptr_t)j.Lh % 16 != 0 || (uintptr_t)j.Ll % 16 != 0 || (j.panel && !(j.Ph && j.Pl && j.Lh && j.Ll)) ||
+            (!j.panel && !(j.Xh && j.Xl && j.Th && j.Tl)))
             return KFAC_ERR_WORKSPACE;
     if (diag_smem_attr() != cudaSuccess) return KFAC_ERR_CUDA;
     std::unique_ptr<DiagParams> P(new DiagParams);
     size_t pos = 0;
     while (pos < jobs.size()) {
         int n = 0;
-        for (; pos < jobs.size() && n < MAT_MAX; ++pos) P->j[n++] = jobs[pos];
+        for (; pos < jobs.size() && n < DIAG_MAX; ++pos) P->j[n++] = jobs[pos];
         P->n = n;
         KFAC_LAUNCH(KK_DIAG, st, diag_kernel, n, DIAG_THREADS, DIAG_SMEM, *P);
     }
@@ -857,7 +974,7 @@ kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st, cuda
         gemms.clear();
         for (const auto &ki : g.rounds[r]) {
             const Op &op = p.chains[ki.first][ki.second];
-            if (op.leaf) leaves.push_back(op.dj);
+            if (op.leaf) leaves.insert(leaves.end(), op.dj.begin(), op.dj.end());
             else gemms.insert(gemms.end(), op.g.begin(), op.g.end());
         }
         if (!leaves.empty() && (s = diag_launch(leaves, st)) != KFAC_OK) return s;
@@ -935,8 +1052,8 @@ kfac_status inv_run(const InvMatrix *mats, int nmats, const float *damp_dev, int
     // 1. X = lower part of sym(F) + damp I (zero above), identity padding
     std::vector<TileMat> tm(nmats);
     for (int k = 0; k < nmats; ++k)
-        tm[k] = TileMat{mats[k].F, mats[k].packed ? -1 : mats[k].ldf, p.work[k].Xh, p.work[k].Xl, mats[k].d,
-                        p.work[k].dp, k, 0, 0};
+        tm[k] = TileMat{mats[k].F, mats[k].packed ? -1 : mats[k].ldf, p.work[k].Xh, p.work[k].Xl, p.work[k].Dh,
+                        p.work[k].Dl, mats[k].d, p.work[k].dp, k, 0, 0};
     if ((s = prep_launch(tm, damp_dev, p.err, st)) != KFAC_OK) return s;
 
     // 2. rounds (see schedule_rounds), the last op of each chain writing the

@@ -42,12 +42,22 @@ constexpr int NUM_THREADS = 192;
 constexpr int TMEM_ACC = 2 * BN;  // two accumulators (columns 0 and BN), alternating
 constexpr int MAX_PROBS = 152;
 constexpr int GROUP = 8;              // row blocks per band of the grouped tile order
-constexpr int TF32X3_MAX_SPLIT = 6;   // K splits of a tf32x3 tile (the last CTA sums the partials)
+#ifndef KFAC_TF32X3_MAX_SPLIT
+#define KFAC_TF32X3_MAX_SPLIT 6
+#endif
+#ifndef KFAC_TF32X3_MIN_KT
+#define KFAC_TF32X3_MIN_KT 64.0
+#endif
+// (both tuning constants may be set at build time)
+constexpr int TF32X3_MAX_SPLIT = KFAC_TF32X3_MAX_SPLIT;   // K splits of a tf32x3 tile (the last CTA sums the partials)
 // Planning choices for tf32x3 launches, as measured on the ResNet-50 step:
 // splitting long K ranges before narrowing tiles, and fewer K tiles per split,
 // both made the inversion slower; the grouped tile order made no difference.
-constexpr bool TF32X3_PREFER_SPLIT = false;  // split long K ranges before narrowing tiles
-constexpr double TF32X3_MIN_KT = 64.0;       // K tiles a tf32x3 split keeps at least
+#ifndef KFAC_TF32X3_PREFER_SPLIT
+#define KFAC_TF32X3_PREFER_SPLIT false
+#endif
+constexpr bool TF32X3_PREFER_SPLIT = KFAC_TF32X3_PREFER_SPLIT;  // split long K ranges before narrowing tiles
+constexpr double TF32X3_MIN_KT = KFAC_TF32X3_MIN_KT;       // K tiles a tf32x3 split keeps at least
 constexpr bool TF32X3_GROUPED = false;       // grouped tile order for tf32x3 launches
 constexpr int MAPS_PER_COPY = 240;
 constexpr int STAGE_LD = 36;                              // epilogue staging row pitch (floats)
@@ -75,8 +85,8 @@ template <> struct Traits<TC_KIND_TF32X3> {
 };
 
 struct TcProb {
-    int map_a, map_b;        // map indices; tf32x3: hi at map, lo at map + 1 (B of a narrow
-                             // tile: the 32-row-box pair at map + 2, map + 3)
+    int map_a, map_b;        // map indices; tf32x3: the (hi, lo) pair map at map + 1 (B of a
+                             // narrow tile: hi and lo with 32-row boxes at map + 2, map + 3)
     int a_row0, a_col0;      // operand sub-block origin inside its map (rows, columns)
     int b_row0, b_col0;
     int M, N, k_tiles;
@@ -673,12 +683,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                             load_tile_bf16(sa + Tr::TILE, mb, q.b_mn, q.b_row0, q.b_col0, k.tn * BN, k0,
                                            &full[stage]);
                     } else {
-                        load_tile(sa, ma, 0, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
-                        load_tile(sa + TILE_BYTES, ma + 1, 0, q.a_row0, q.a_col0, k.tm * BM, k0, &full[stage]);
+                        // (hi, lo) pairs in one copy each: hi at the tile, lo right after it
+                        tma_load_3d(sa, ma + 1, q.a_col0 + k0, q.a_row0 + k.tm * BM, 0, &full[stage]);
                         if (q.bn == BN) {
-                            load_tile(sa + 2 * TILE_BYTES, mb, 0, q.b_row0, q.b_col0, k.tn * BN, k0, &full[stage]);
-                            load_tile(sa + 3 * TILE_BYTES, mb + 1, 0, q.b_row0, q.b_col0, k.tn * BN, k0,
-                                      &full[stage]);
+                            tma_load_3d(sa + 2 * TILE_BYTES, mb + 1, q.b_col0 + k0, q.b_row0 + k.tn * BN, 0,
+                                        &full[stage]);
                         } else {  // narrow tile: B from the 32-row-box maps
                             load_rows_tf32(sa + 2 * TILE_BYTES, mb, q.b_row0, q.b_col0, k.tn * q.bn, q.bn, k0,
                                            &full[stage]);
@@ -1047,6 +1056,22 @@ bool tc_make_map(CUtensorMap *m, int kind, const void *ptr, long long ld, int ro
                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     CUresult r = enc(m, dt, 2, (void *)ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool tc_make_pair_map(CUtensorMap *m, const float *hi, const float *lo, long long ld, int rows, int cols,
+                      int box_rows) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc || lo <= hi) return false;
+    const long long plane = (long long)((const char *)lo - (const char *)hi);
+    if (plane % 16 != 0) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, 2};
+    cuuint64_t strides[2] = {(cuuint64_t)ld * 4, (cuuint64_t)plane};
+    cuuint32_t box[3] = {32u, (cuuint32_t)box_rows, 2u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, (void *)hi, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

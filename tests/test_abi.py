@@ -146,3 +146,22 @@ def test_product_path_has_no_fallback():
     assert "oracle" not in src.replace("no CPU or PyTorch fallback", "")
     for fn in os.listdir(os.path.join(ROOT, "second_order_optimisation_gb300", "csrc")):
         assert "oracle" not in open(os.path.join(ROOT, "second_order_optimisation_gb300", "csrc", fn)).read()
+
+
+def test_host_memory_operands_are_rejected(lib):
+    """Operands must be memory of the current device: host arrays give
+    KFAC_ERR_INVALID once every other check has passed (on a machine without
+    a GPU no pointer is device memory)."""
+    import numpy as np
+    x = np.zeros(4 * 6 * 6 * 64, dtype=np.uint16)
+    F = np.zeros(576 * 576, dtype=np.float32)
+    arr = (kfac.FactorDesc * 1)(_fdesc(x=x.ctypes.data, F=F.ctypes.data))
+    need = lib.kfac_factor_update_workspace_size(arr, 1)
+    assert need > 0
+    assert lib.kfac_factor_update(arr, 1, 0x100000, need, None) == kfac.KFAC_ERR_INVALID
+    g = np.zeros(16 * 24, dtype=np.float32)
+    parr = (kfac.PrecondDesc * 1)(_pdesc(G_inv=g.ctypes.data, A_inv=g.ctypes.data, grad=g.ctypes.data,
+                                         out=g.ctypes.data))
+    assert lib.kfac_precondition(parr, 1, kfac.KFAC_F32, 0x100000, 1 << 20, None) == kfac.KFAC_ERR_INVALID
+    b = kfac.BnDesc(g.ctypes.data, 16, g.ctypes.data, None, g.ctypes.data)
+    assert lib.kfac_bn_diag_fisher((kfac.BnDesc * 1)(b), 1, 8, 1e-3, 0.0, None) == kfac.KFAC_ERR_INVALID

@@ -7,12 +7,11 @@ factor X = F + damp I is inverted on its own.  The library inverts X through
 its Cholesky factor X = L L^T: W = L^-1, then X^-1 = W^T W.  This file
 restates, operation by operation and with the same buffer offsets:
 
-  * the diag kernel's sweep, which turns the lower triangle of a 128 x 128
-    SPD block into W = L^-1 in place, 8 pivots per step (the single-pivot
-    rules M_ij -= p_i y_j, M_ic = -p_i w, M_cj *= w, M_cc = w, with
-    w = 1/sqrt(M_cc) and p_i = w M_ic, fused over the pivot block);
+  * the diag kernel, which turns the lower triangle of a 128 x 128 SPD
+    block into L (blocked right-looking Cholesky by 16) and W = L^-1
+    (blocked by rows of 16);
   * the chain of one matrix: left-looking Cholesky block columns (update,
-    diag leaf, panel), the triangular inverse by recursive 2 x 2 blocking
+    then the diag kernel, whose other CTAs form the panel below the block), the triangular inverse by recursive 2 x 2 blocking
     bottom up by height (T = L21 W11, W21 = -W22 T), and the final product
     Wt Wt^T over upper tiles with K from each tile's first column (ktri),
     mirrored.
@@ -28,47 +27,46 @@ import pytest
 NB = 128
 
 
-def pivot_block(S):
-    """The single-pivot rules applied to a square lower block alone (what each
-    of the diag kernel's first 128 threads does with its 8 x 8 pivot block): W_K."""
-    S = np.tril(np.array(S, dtype=np.float64))
-    n = S.shape[0]
-    for q in range(n):
-        w = 1.0 / np.sqrt(S[q, q])
-        p = np.where(np.arange(n) > q, S[:, q] * w, 0.0)
-        for r in range(q + 1, n):
-            S[r, :q] -= p[r] * w * S[q, :q]
-            S[r, q] = -p[r] * w
-            S[r, q + 1:r + 1] -= p[r] * p[q + 1:r + 1]
-        S[q, :q] *= w
-        S[q, q] = w
-    return S
+DB = 16
 
 
-def diag_sweep(S, panel=8):
-    """The diag kernel's sweep on the lower triangle of S, `panel` pivots
-    K = {c .. c+panel-1} per step: W_K from the pivot block alone, then
-    Z_j = W_K M[K][j] (j before K), W_K^T e_(j-c) (j in K), W_K M[j][K]
-    (j past K); rows past K take M_ij = (j in K ? 0 : M_ij) - Z_i . Z_j
-    (j <= i), rows K take Z_j (j before K) and W_K."""
+def diag_block(S):
+    """The diag kernel on the lower triangle of a 128 x 128 SPD block, blocked
+    by 16: right-looking Cholesky (L_cc = chol(S_cc) column by column as the
+    warp does it; L_ic = S_ic L_cc^-T; S_ij -= L_ic L_jc^T for i >= j past c,
+    lower triangle only), then W = L^-1 by block rows (W_ii = L_ii^-1;
+    W_ij = -W_ii sum_{t=j}^{i-1} L_it W_tj).  Returns (L, W)."""
     n = S.shape[0]
-    M = np.tril(S).astype(np.float64)
-    for c in range(0, n, panel):
-        E = c + panel
-        Wk = pivot_block(M[c:E, c:E])
-        Zb = (Wk @ M[c:E, :c]).T          # j before K
-        Zk = Wk.T                          # j in K: row j-c of W_K^T
-        Zp = M[E:, c:E] @ Wk.T             # j past K
-        Z = np.vstack([Zb, Zk, Zp])
-        new = M.copy()
-        low = np.tril(np.ones((n, n), dtype=bool))[E:]
-        base = M[E:].copy()
-        base[:, c:E] = 0.0
-        new[E:] = np.where(low, base - Z[E:] @ Z.T, M[E:])
-        new[c:E, :c] = Zb.T
-        new[c:E, c:E] = Wk
-        M = new
-    return M
+    M = np.tril(np.array(S, dtype=np.float64))
+    for c in range(0, n, DB):
+        e = c + DB
+        B = M[c:e, c:e].copy()
+        for q in range(DB):
+            B[q, q] = np.sqrt(B[q, q])
+            B[q + 1:, q] /= B[q, q]
+            for j in range(q + 1, DB):
+                B[j:, j] -= B[j:, q] * B[j, q]
+        M[c:e, c:e] = np.tril(B)
+        if e < n:
+            Lcc = M[c:e, c:e]
+            for q in range(DB):          # forward substitution, a row per thread
+                M[e:, c + q] /= Lcc[q, q]
+                M[e:, c + q + 1:e] -= np.outer(M[e:, c + q], Lcc[q + 1:, q])
+            M[e:, e:] -= np.tril(M[e:, c:e] @ M[e:, c:e].T)
+    L = np.tril(M)
+    W = np.zeros_like(L)
+    for b in range(0, n, DB):
+        Lb = L[b:b + DB, b:b + DB]
+        for q in range(DB):              # a thread per column of W_bb
+            x = np.zeros(DB)
+            for r in range(DB):
+                x[r] = ((1.0 if r == q else 0.0) - Lb[r, :r] @ x[:r]) / Lb[r, r]
+            W[b:b + DB, b + q] = x
+    for i in range(DB, n, DB):
+        for j in range(0, i, DB):
+            T = L[i:i + DB, j:i] @ W[j:i, j:j + DB]
+            W[i:i + DB, j:j + DB] = -W[i:i + DB, i:i + DB] @ T
+    return L, W
 
 
 def _job(A, ar, ac, B, br, bc, M, N, K, alpha, beta, C=None, Ct=None, ktri=False, ktril=False):
@@ -88,25 +86,19 @@ def _tri_nodes(o, n, by_height):
 
 
 def chain(dp):
-    """Ops of one dp x dp matrix, in the library's order (leaf or engine).
-    An engine op may carry side problems (the lookahead update of column
-    block k + 2 by panels 0 .. k), which the library launches on a second
-    stream once the op is done and which finish before the chain's update of
-    that column by its last panel."""
+    """Ops of one dp x dp matrix, in the library's order: ("leaf", k) for a
+    diag kernel launch, ("gemm", problems, side problems) for an engine launch
+    (the library has no side problems at present; the field stays empty)."""
     ops, nb = [], dp // NB
     for k in range(nb):
         kb = k * NB
-        if k > 0:   # X[k:, k] -= L[k:, k-1] L[k, k-1]^T   (the last panel's share)
-            ops.append(("gemm", [_job("L", kb, kb - NB, "L", kb, kb - NB, dp - kb, NB, NB, -1.0, 1.0,
-                                      C=("X", kb, kb))], []))
-        ops.append(("leaf", kb))
-        if k + 1 < nb:   # L[k+1:, k] = X[k+1:, k] W_kk^T
-            side = []
-            if k + 2 < nb:   # X[k2:, k2] -= L[k2:, :k+1] L[k2, :k+1]^T
-                k2b = (k + 2) * NB
-                side = [_job("L", k2b, 0, "L", k2b, 0, dp - k2b, NB, kb + NB, -1.0, 1.0, C=("X", k2b, k2b))]
-            ops.append(("gemm", [_job("X", kb + NB, kb, "X", kb, kb, dp - kb - NB, NB, NB, 1.0, 0.0,
-                                      C=("L", kb + NB, kb))], side))
+        if k > 0:   # D_k -= L[k, :k] L[k, :k]^T;  X[k+1:, k] -= L[k+1:, :k] L[k, :k]^T
+            jobs = [_job("L", kb, 0, "L", kb, 0, NB, NB, kb, -1.0, 1.0, C=("D", kb, 0))]
+            if k + 1 < nb:
+                jobs.append(_job("L", kb + NB, 0, "L", kb, 0, dp - kb - NB, NB, kb, -1.0, 1.0,
+                                 C=("X", kb + NB, kb)))
+            ops.append(("gemm", jobs, []))
+        ops.append(("leaf", kb))   # W_kk from D_k, and the panel L[k+1:, k] = X[k+1:, k] W_kk^T
     by_height = []
     _tri_nodes(0, dp, by_height)
     for ht in range(1, len(by_height)):
@@ -128,7 +120,10 @@ def invert_like_the_library(F, damp, bn):
     X0 = np.eye(dp)
     X0[:d, :d] = F + damp * np.eye(d)
     buf = {k: np.full((dp, dp), np.nan) for k in ("X", "W", "L")}
+    buf["D"] = np.full((dp, NB), np.nan)
     buf["X"][:] = np.tril(X0)                     # prep: lower part, zeros above
+    for b in range(0, dp, NB):                     # ... and its diagonal blocks into D
+        buf["D"][b:b + NB] = np.tril(X0)[b:b + NB, b:b + NB]
     def launch(jobs):
         results = []
         for j in jobs:   # every problem of one launch reads before any writes
@@ -153,9 +148,14 @@ def invert_like_the_library(F, damp, bn):
     for op in chain(dp):
         if op[0] == "leaf":
             o = op[1]
-            W = diag_sweep(buf["X"][o:o + NB, o:o + NB])
+            # the owner first (the CTAs of one launch run in any order): the
+            # panel CTAs must not see its output, so every CTA reads D_k
+            W = diag_block(buf["D"][o:o + NB])[1]
             buf["X"][o:o + NB, o:o + NB] = np.tril(W)
             buf["W"][o:o + NB, o:o + NB] = np.triu(W.T)
+            for i in range(o + NB, dp, NB):
+                Wp = diag_block(buf["D"][o:o + NB])[1]
+                buf["L"][i:i + NB, o:o + NB] = buf["X"][i:i + NB, o:o + NB] @ Wp.T
             continue
         launch(op[1])
         if op[2]:
@@ -170,22 +170,21 @@ def invert_like_the_library(F, damp, bn):
     return out[:d, :d]
 
 
-@pytest.mark.parametrize("n", [4, 8, 32])
-def test_pivot_block_rules_are_the_inverse_cholesky_factor(n):
-    rng = np.random.default_rng(4)
-    Z = rng.standard_normal((n, n))
-    S = Z @ Z.T / n + 0.1 * np.eye(n)
-    np.testing.assert_allclose(pivot_block(S), np.linalg.inv(np.linalg.cholesky(S)), rtol=0, atol=1e-10)
-
-
-def test_diag_sweep_is_the_inverse_cholesky_factor():
+def test_diag_block_is_the_cholesky_factor_and_its_inverse():
     rng = np.random.default_rng(3)
-    Z = rng.standard_normal((NB, NB))
-    S = Z @ Z.T / NB + 0.01 * np.eye(NB)
-    for panel in (4, 8, 32):
-        W = diag_sweep(S, panel)
-        np.testing.assert_allclose(np.tril(W), np.linalg.inv(np.linalg.cholesky(S)), rtol=0, atol=1e-11)
-    assert np.all(np.triu(W, 1) == 0.0)
+    for scale in (0.01, 1e-4):
+        Z = rng.standard_normal((NB, NB))
+        S = Z @ Z.T / NB + scale * np.eye(NB)
+        L, W = diag_block(S)
+        Lr = np.linalg.cholesky(S)
+        np.testing.assert_allclose(L, Lr, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(W, np.linalg.inv(Lr), rtol=1e-9, atol=1e-9)
+        assert np.all(np.triu(W, 1) == 0.0) and np.all(np.triu(L, 1) == 0.0)
+    # only the lower triangle is read
+    Su = S.copy()
+    Su[np.triu_indices(NB, 1)] = np.nan
+    L2, W2 = diag_block(Su)
+    assert np.array_equal(L2, L) and np.array_equal(W2, W)
 
 
 @pytest.mark.parametrize("bn", [128, 64, 32])
@@ -203,7 +202,8 @@ def test_chain_inverts_and_reads_only_written_regions(d, bn):
 
 
 def test_chain_launch_counts():
-    """Ops per matrix: 3 per 128-wide block column (minus the first update and
-    the last panel) and 2 per level of the triangular inverse."""
-    for dp, expect in ((128, 1), (256, 4 + 2), (1152, 9 * 3 - 2 + 2 * 4), (4608, 36 * 3 - 2 + 2 * 6)):
+    """Ops per matrix: 2 per 128-wide block column (an update, then the diag
+    kernel with the panel; no update for the first) and 2 per level of the
+    triangular inverse."""
+    for dp, expect in ((128, 1), (256, 3 + 2), (1152, 9 * 2 - 1 + 2 * 4), (4608, 36 * 2 - 1 + 2 * 6)):
         assert len(chain(dp)) == expect, dp

@@ -49,6 +49,9 @@ MUTANTS = [
     ("refresh schedule off by one", "return (t - warmup) % every == 0;", "return (t - warmup + 1) % every == 0;",
      [lambda: pins.test_refresh_schedule_closed_forms(3, 4, 20),
       pins.test_stale_schedule_equals_stepwise_composition]),
+    ("packed row skips the diagonal", "for (long j = i; j < d; ++j) out[t++] = F[i * d + j];",
+     "for (long j = i; j < d; ++j) out[t++] = F[i * d + (j + 1) % d];",
+     [pins.test_packed_upper_closed_form_and_round_trip]),
     ("bn unbiased variance", "double f = s2 / (double)ns;", "double f = s2 / (double)(ns - 1);",
      [pins.test_bn_diag_is_diagonal_of_explicit_fisher]),
     ("bn drops damping", "out[c] = gmean[c] / (F[c] + gamma);", "out[c] = gmean[c] / F[c];",

@@ -319,3 +319,30 @@ def test_stale_schedule_equals_stepwise_composition():
             da, dg = oracle.pi_damping(A, G, 1e-3)
             Ai, Gi = oracle.damped_inverse(A, da), oracle.damped_inverse(G, dg)
         np.testing.assert_allclose(outs[t], oracle.precondition(Gi, grad, Ai), rtol=1e-12)
+
+
+# ------------------------------------------------------------- packed factor storage
+
+def test_packed_upper_closed_form_and_round_trip():
+    """Packed upper triangle (section 1: exploit the symmetry of the factors):
+    for d = 3 the stored order is (0,0) (0,1) (0,2) (1,1) (1,2) (2,2); the
+    position of (i, j) is i*d - i*(i+1)/2 + j, checked against an enumeration
+    of the upper triangle; unpacking restores the symmetric matrix exactly."""
+    F = np.array([[0.0, 1.0, 2.0], [1.0, 3.0, 4.0], [2.0, 4.0, 5.0]])
+    np.testing.assert_array_equal(oracle.pack_upper(F), [0, 1, 2, 3, 4, 5])
+    for d in (1, 2, 7, 64, 129):
+        X = np.random.default_rng(d).standard_normal((d, d))
+        S = X + X.T
+        p = oracle.pack_upper(S)
+        assert p.size == d * (d + 1) // 2
+        pos = 0
+        for i in range(d):
+            for j in range(i, d):
+                assert i * d - i * (i + 1) // 2 + j == pos
+                assert p[pos] == S[i, j]
+                pos += 1
+        np.testing.assert_array_equal(oracle.unpack_upper(p, d), S)
+        # only the upper triangle is read
+        L = S.copy()
+        L[np.tril_indices(d, -1)] = np.nan
+        np.testing.assert_array_equal(oracle.pack_upper(L), p)
