@@ -4,7 +4,7 @@ preconditioning) for the ResNet-50 layer set at 32 samples per GPU, on
 synthetic inputs with ResNet-50's shapes.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
-                  [--workload resnet50|conv3x3_256|fc4096]
+                  [--workload resnet50|conv3x3_256|fc4096|conv3x3_512]
 
 Prints ONE JSON line (rank 0).
 
@@ -64,6 +64,8 @@ def workload(name):
         return [W.conv_3x3_256()], 32
     if name == "fc4096":
         return [W.fc_4096()], 8192
+    if name == "conv3x3_512":   # ResNet-50's last 3x3 conv (A 4608 x 4608, G 512 x 512), 7 x 7, batch 32
+        return [L for L in W.resnet50_layers() if L.name == "s4b3_3x3"], 32
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -548,7 +550,10 @@ def run_ours(args, world, rank, local):
     if args.profile:
         torch.cuda.nvtx.range_push("kfac_step")
         for _ in range(args.steps):
-            m["step"].run(*m["inp"].views)
+            if args.phase == "inverse":
+                m["step"].damp_invert()
+            else:
+                m["step"].run(*m["inp"].views)
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         print(json.dumps({"profile": args.workload, "steps": args.steps,
@@ -649,7 +654,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="resnet50", choices=("resnet50", "conv3x3_256", "fc4096"))
+    ap.add_argument("--workload", default="resnet50", choices=("resnet50", "conv3x3_256", "fc4096", "conv3x3_512"))
+    ap.add_argument("--phase", default="step", choices=("step", "inverse"),
+                    help="with --profile: the NVTX range holds whole steps, or only the damped inversion")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-subrecords", action="store_true")
     ap.add_argument("--profile", action="store_true",

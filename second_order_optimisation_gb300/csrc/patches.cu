@@ -10,6 +10,8 @@
 // of A is the column sum of the input and the row count, computed here
 // without forming P.
 #include <algorithm>
+#include <cstring>
+#include <vector>
 #include <memory>
 
 #include "internal.h"
@@ -86,6 +88,78 @@ __global__ void __launch_bounds__(256) im2col_kernel(const __grid_constant__ ImP
             }
         }
         if (q.append_one && lane == 0) prow[dcore] = (T)1.0f;
+    }
+}
+
+// Patch rows of one output row strip (image img, output row ho, every wo) by
+// one CTA, for convolutions whose kh input rows of the strip fit in shared
+// memory (few channels, e.g. a network's first 7 x 7 layer on RGB input):
+// the kh x Wn x c input window (zeros outside the image) is read once,
+// coalesced, into shared memory; then consecutive threads write consecutive
+// 16-byte pieces of the strip's patch rows, which are contiguous in P, so
+// the whole strip goes out as one coalesced block.  A shared table maps each
+// column of a patch row to its offset in the window (for output column wo,
+// add wo * stride * c).
+constexpr int IMS_MAX = 64;
+constexpr int IMS_SMEM = 48 * 1024;   // input window + table (bytes)
+struct ImsParams {
+    Im2colJob j[IMS_MAX];
+    int begin[IMS_MAX + 1];   // prefix of CTAs (n * ho strips per job)
+    int n;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) im2col_strip_kernel(const __grid_constant__ ImsParams P) {
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ float4 ims_smem4[];
+    int lo = 0, hi = P.n - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (P.begin[mid] <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
+    }
+    const Im2colJob &q = P.j[lo];
+    constexpr int VW = 16 / sizeof(T);
+    const int strip = blockIdx.x - P.begin[lo];
+    const int img = strip / q.ho, ho = strip - img * q.ho;
+    const int dcore = q.kh * q.kw * q.c;
+    const int Wn = (q.wo - 1) * q.sw + q.kw;      // input columns of the window
+    int *table = reinterpret_cast<int *>(ims_smem4);           // dcore entries: (r * Wn + s) * c + ch
+    T *win = reinterpret_cast<T *>(table + ((dcore + 3) & ~3));  // [kh][Wn][c]
+    for (int e = threadIdx.x; e < dcore; e += blockDim.x) {
+        const int rs = e / q.c, ch = e - rs * q.c, r = rs / q.kw, sx = rs - r * q.kw;
+        table[e] = (r * Wn + sx) * q.c + ch;
+    }
+    const int hb = ho * q.sh - q.ph, wb = -q.pw;
+    const T *xi = (const T *)q.x + (long long)img * q.h * q.w * q.c;
+    const int rowlen = Wn * q.c;
+    for (int e = threadIdx.x; e < q.kh * rowlen; e += blockDim.x) {
+        const int r = e / rowlen, rest = e - r * rowlen;
+        const int wc = rest / q.c, ch = rest - wc * q.c;
+        const int hh = hb + r, ww = wb + wc;
+        win[e] = (hh >= 0 && hh < q.h && ww >= 0 && ww < q.w) ? xi[((long long)hh * q.w + ww) * q.c + ch] : (T)0.0f;
+    }
+    __syncthreads();
+    const int nun = q.ldp / VW;                   // 16-byte pieces of a patch row (padding included)
+    T *pstrip = (T *)q.P + (long long)strip * q.wo * q.ldp;
+    for (int idx = threadIdx.x; idx < q.wo * nun; idx += blockDim.x) {
+        const int wo = idx / nun, u = idx - wo * nun;
+        const int wofs = wo * q.sw * q.c;
+        T vals[VW];
+#pragma unroll
+        for (int t = 0; t < VW; ++t) {
+            const int e = u * VW + t;
+            T v = (T)0.0f;
+            if (e < dcore) {
+                v = win[table[e] + wofs];
+            } else if (e == dcore && q.append_one) {
+                v = (T)1.0f;
+            }
+            vals[t] = v;
+        }
+        uint4 pk;
+        memcpy(&pk, vals, 16);
+        *reinterpret_cast<uint4 *>(pstrip + (long long)wo * q.ldp + u * VW) = pk;
     }
 }
 
@@ -194,7 +268,64 @@ __global__ void __launch_bounds__(256) colsum_finish_kernel(const __grid_constan
 
 }  // namespace
 
-kfac_status im2col_run(const Im2colJob *jobs, int njobs, int dtype, cudaStream_t st) {
+// Strip kernel eligibility: 16-byte aligned rows whose padding absorbs the
+// last 16-byte piece, and an input window that fits the shared budget.
+size_t strip_smem(const Im2colJob &j, size_t esz) {
+    const long long dcore = (long long)j.kh * j.kw * j.c;
+    const long long win = (long long)j.kh * ((long long)(j.wo - 1) * j.sw + j.kw) * j.c * (long long)esz;
+    return (size_t)(((dcore + 3) & ~3LL) * 4 + win);
+}
+
+bool strip_ok(const Im2colJob &j, size_t esz) {
+    const int vw = (int)(16 / esz);
+    const long long dcore = (long long)j.kh * j.kw * j.c;
+    return j.ldp % vw == 0 && (uintptr_t)j.P % 16 == 0 && dcore + (j.append_one ? 1 : 0) <= j.ldp &&
+           strip_smem(j, esz) <= (size_t)IMS_SMEM && (long long)j.n * j.ho < (1LL << 30);
+}
+
+template <typename T>
+kfac_status strip_run(const std::vector<Im2colJob> &jobs, cudaStream_t st) {
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(im2col_strip_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, IMS_SMEM) !=
+            cudaSuccess)
+            return KFAC_ERR_CUDA;
+        attr = true;
+    }
+    std::unique_ptr<ImsParams> P(new ImsParams);
+    size_t pos = 0;
+    while (pos < jobs.size()) {
+        int n = 0;
+        long long ctas = 0;
+        while (pos < jobs.size() && n < IMS_MAX && ctas + (long long)jobs[pos].n * jobs[pos].ho < (1LL << 30)) {
+            P->j[n] = jobs[pos];
+            P->begin[n] = (int)ctas;
+            ctas += (long long)jobs[pos].n * jobs[pos].ho;
+            ++n;
+            ++pos;
+        }
+        if (n == 0) return KFAC_ERR_UNSUPPORTED;
+        P->begin[n] = (int)ctas;
+        P->n = n;
+        size_t smem = 0;  // the launch's largest window + table: more CTAs per SM than the budget
+        for (int k = 0; k < n; ++k) smem = std::max(smem, strip_smem(P->j[k], sizeof(T)));
+        KFAC_LAUNCH(KK_IM2COL, st, im2col_strip_kernel<T>, (int)ctas, 256, (int)smem, *P);
+    }
+    return KFAC_OK;
+}
+
+kfac_status im2col_run(const Im2colJob *all, int nall, int dtype, cudaStream_t st) {
+    const size_t esz0 = dtype == KFAC_F32 ? 4 : 2;
+    std::vector<Im2colJob> strips, rows;
+    for (int k = 0; k < nall; ++k) (strip_ok(all[k], esz0) ? strips : rows).push_back(all[k]);
+    if (!strips.empty()) {
+        kfac_status s = dtype == KFAC_BF16  ? strip_run<__nv_bfloat16>(strips, st)
+                        : dtype == KFAC_F16 ? strip_run<__half>(strips, st)
+                                            : strip_run<float>(strips, st);
+        if (s != KFAC_OK) return s;
+    }
+    const Im2colJob *jobs = rows.data();
+    const int njobs = (int)rows.size();
     std::unique_ptr<ImParams> P(new ImParams);
     const size_t esz = dtype == KFAC_F32 ? 4 : 2;
     const int vw = (int)(16 / esz);

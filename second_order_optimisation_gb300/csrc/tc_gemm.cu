@@ -42,6 +42,9 @@ constexpr int NUM_THREADS = 192;
 constexpr int TMEM_ACC = 2 * BN;  // two accumulators (columns 0 and BN), alternating
 constexpr int MAX_PROBS = 152;
 constexpr int GROUP = 8;              // row blocks per band of the grouped tile order
+#ifndef KFAC_TF32X3_CHUNK
+#define KFAC_TF32X3_CHUNK 8
+#endif
 #ifndef KFAC_TF32X3_MAX_SPLIT
 #define KFAC_TF32X3_MAX_SPLIT 6
 #endif
@@ -74,14 +77,14 @@ template <> struct Traits<TC_KIND_BF16> {
     static constexpr int CHUNK = 1 << 30, TMEM_COLS = TMEM_ACC;
 };
 template <> struct Traits<TC_KIND_TF32X3> {
-    // A work item accumulates its K range in chunks of CHUNK K tiles (128 K),
+    // A work item accumulates its K range in chunks of CHUNK K tiles (256 K),
     // alternating between the two TMEM accumulators; the epilogue warps add
     // each chunk into a running sum held in TMEM (columns 2 BN ..) with fp32
     // round-to-nearest additions.  Long sums accumulated within one tensor-core
     // accumulator lose accuracy faster than that (the Cholesky updates of the
     // inversion run over K up to the factor's width).
     static constexpr int BK = 32, STAGES = 3, TILES = 4, ESZ = 4, TILE = TILE_BYTES;
-    static constexpr int CHUNK = 4, TMEM_COLS = 512;
+    static constexpr int CHUNK = KFAC_TF32X3_CHUNK, TMEM_COLS = 512;
 };
 
 struct TcProb {
@@ -197,6 +200,24 @@ __device__ __forceinline__ Work decode_work(const TcParams &P, int w) {
             k.tm = b0 + u % gb;
         }
         k.tile = k.tm * T - r * (k.tm * (k.tm - 1) / 2) + (k.tn - k.tm * r);
+    } else if (q.sym && q.ktri) {
+        // upper tiles column by column (column block tn holds row blocks
+        // 0 .. the one holding its last column): K starts at the tile's first
+        // column, so this order is longest first and the static round-robin
+        // over CTAs balances
+        int u = unit, tn = 0, base = 0;
+        for (;;) {
+            const int cnt = min(q.tiles_m, ((tn + 1) * q.bn - 1) / BM + 1);
+            if (u < cnt) {
+                k.tm = u;
+                k.tn = tn;
+                k.tile = base + u;
+                break;
+            }
+            u -= cnt;
+            base += cnt;
+            ++tn;
+        }
     } else if (q.syrk || q.sym) {
         // upper tiles only: row block tm (128 rows) runs column blocks from the
         // one holding its diagonal, first(tm) = tm * 128 / bn
@@ -236,6 +257,17 @@ __device__ __forceinline__ Work decode_work(const TcParams &P, int w) {
         const int rem = unit - band * GROUP * T;
         k.tn = rem / gb;
         k.tm = b0 + rem % gb;
+        k.tile = k.tm * T + k.tn;
+    } else if (q.ktri) {
+        // column by column: K starts at the tile's first column, longest first
+        k.tn = unit / q.tiles_m;
+        k.tm = unit - k.tn * q.tiles_m;
+        k.tile = k.tm * T + k.tn;
+    } else if (q.ktril) {
+        // row blocks from the last: K ends after the tile's last row, longest first
+        const int r = unit / T;
+        k.tm = q.tiles_m - 1 - r;
+        k.tn = unit - r * T;
         k.tile = k.tm * T + k.tn;
     } else {
         k.tm = unit / T;
@@ -534,11 +566,10 @@ __device__ __forceinline__ bool chunk_store(const TcProb &q, int i0, int j0, con
             // store instruction covers one contiguous row segment
             const int i = i0 + lane;
             if (i < q.M) {
-#pragma unroll 8
-                for (int c = 0; c < 32; ++c) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {  // (fully unrolled: v stays in registers)
                     const int jj = j0 + c;
-                    if (jj >= q.N) break;
-                    if (up && jj <= i) continue;
+                    if (jj >= q.N || (up && jj <= i)) continue;
                     const float o = a * v[c];
                     if (q.C) q.C[(long long)jj * q.ldc + i] = o;
                     if (q.Cb) q.Cb[(long long)jj * q.ldcb + i] = f32_to_16_bits(o, q.cb_f16);
@@ -805,12 +836,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 #pragma unroll 1
                 for (int c = 0; c < nch; ++c) {
                     float v[32];
-                    tmem_ld_32x32b_x32(t_quarter + b * BN + c * 32, v);
                     if (ch > 0) {
                         float s2[32];
-                        tmem_ld_32x32b_x32(t_sum + c * 32, s2);
+                        tmem_ld_pair_32x32b_x32(t_quarter + b * BN + c * 32, v, t_sum + c * 32, s2);
 #pragma unroll
                         for (int t = 0; t < 32; ++t) v[t] += s2[t];
+                    } else {
+                        tmem_ld_32x32b_x32(t_quarter + b * BN + c * 32, v);
                     }
                     tmem_st_32x32b_x32(t_sum + c * 32, v);
                 }
@@ -845,12 +877,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 for (int c = 0; c < nch; ++c) {
                     if (c > 0) load_old(q, i0, k.tn * q.bn + c * 32, lane, oh, ol);
                     float v[32];
-                    tmem_ld_32x32b_x32(t_row + c * 32, v);
                     if (summed) {
                         float s2[32];
-                        tmem_ld_32x32b_x32(t_sum + c * 32, s2);
+                        tmem_ld_pair_32x32b_x32(t_row + c * 32, v, t_sum + c * 32, s2);
 #pragma unroll
                         for (int t = 0; t < 32; ++t) v[t] += s2[t];
+                    } else {
+                        tmem_ld_32x32b_x32(t_row + c * 32, v);
                     }
                     if (empty) {
 #pragma unroll
@@ -865,12 +898,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 #pragma unroll 1
                 for (int c = 0; c < nch; ++c) {
                     float v[32];
-                    tmem_ld_32x32b_x32(t_row + c * 32, v);
                     if (summed) {
                         float s2[32];
-                        tmem_ld_32x32b_x32(t_sum + c * 32, s2);
+                        tmem_ld_pair_32x32b_x32(t_row + c * 32, v, t_sum + c * 32, s2);
 #pragma unroll
                         for (int t = 0; t < 32; ++t) v[t] += s2[t];
+                    } else {
+                        tmem_ld_32x32b_x32(t_row + c * 32, v);
                     }
                     if (empty) {
 #pragma unroll
