@@ -48,6 +48,8 @@ struct TcJob {
     int ktril;     // TF32X3: the K range of output tile (tm, tn) ends after the tile's last
                    // row (A lower triangular in its K index: A[i][t] = 0 for t > i)
     int no_split;
+    int fine_split; // a latency-critical job: split its K range into pieces of about 12 K tiles
+                    // (up to 16 pieces) whatever the rest of the launch
     int epi;
     float alpha, beta;
     float *C;

@@ -48,6 +48,13 @@ constexpr int NB = 128;    // block width of the sweep
 // (each redoing the 128 x 128 factorisation) wait for SMs held by the second
 // group's engine launches: 9.1 ms against 8.5 ms for the engine panel.
 constexpr bool FUSED_PANEL = KFAC_INV_FUSED_PANEL;
+#ifndef KFAC_INV_LOOKAHEAD
+#define KFAC_INV_LOOKAHEAD 1
+#endif
+// Lookahead (see gen_chain): the rest of each Cholesky block column on the
+// side stream, off the chain of diagonal blocks.  A tuning constant that may
+// be set at build time.
+constexpr bool LOOKAHEAD = KFAC_INV_LOOKAHEAD && !KFAC_INV_FUSED_PANEL;
 constexpr int MAT_MAX = 224;
 // tensor maps of one matrix: X, Wt, LT pairs, each as hi and the (hi, lo)
 // pair with 128-row boxes, and hi / lo with 32-row boxes
@@ -602,9 +609,12 @@ int tri_nodes(int o, int n, std::vector<std::vector<std::pair<int, int>>> &by_he
 //  1. left-looking blocked Cholesky, 128-wide block columns k:
 //       D_k = X[k, k] - L[k, :k] L[k, :k]^T,
 //       X[k+1:, k] -= L[k+1:, :k] L[k, :k]^T              (engine; k > 0)
-//       W_kk = L_kk^-1 from D_k, and the panel
-//       L[k+1:, k] = X[k+1:, k] W_kk^T                   (diag kernel, a CTA per block)
-//     every Schur-complement column comes from Cholesky panels (no growth);
+//       W_kk = L_kk^-1 from D_k                           (diag kernel)
+//       L[k+1:, k] = X[k+1:, k] W_kk^T                    (engine, the panel)
+//     every Schur-complement column comes from Cholesky panels (no growth).
+//     With the lookahead only the diagonal update, the diag kernel and the
+//     panel's first block stay on the chain; the rest of each column runs on
+//     the side stream (details in gen_chain);
 //  2. W = L^-1 by recursive 2 x 2 blocking, bottom up by height (the two
 //     halves of a node are independent):
 //       T = L21 W11,   W21 = -W22 T   (W21 over X's lower part, W21^T into Wt);
@@ -616,23 +626,12 @@ int tri_nodes(int o, int n, std::vector<std::vector<std::pair<int, int>>> &by_he
 void gen_chain(std::vector<Op> &ops, const MatWork &w, const InvMatrix &mat, int *info) {
     const long long ld = w.dp;
     const int nb = w.dp / NB;
-    for (int k = 0; k < nb; ++k) {
+    auto diag_op = [&](int k) {
+        // W_kk from D_k (every CTA reads S_kk from D, which no CTA of the launch
+        // writes; the owner writes W_kk over X's block), and with the fused
+        // panel one more CTA per block below forming L[i, k] = X[i, k] W_kk^T
         const int kb = k * NB;
         const float *Dh = w.Dh + (long long)kb * NB, *Dl = w.Dl + (long long)kb * NB;
-        if (k > 0) {
-            // the diagonal block into D, the blocks below it in X
-            Op op{};
-            op.g.push_back(split_job(w.ml, kb, 0, w.ml, kb, 0, NB, NB, kb, -1.f, 1.f, w.Dh + (long long)kb * NB,
-                                     w.Dl + (long long)kb * NB, nullptr, nullptr, NB));
-            if (k + 1 < nb)
-                op.g.push_back(split_job(w.ml, kb + NB, 0, w.ml, kb, 0, w.dp - kb - NB, NB, kb, -1.f, 1.f,
-                                         w.Xh + (kb + NB) * ld + kb, w.Xl + (kb + NB) * ld + kb, nullptr, nullptr,
-                                         ld));
-            ops.push_back(op);
-        }
-        // W_kk and the panel L[k+1:, k] = X[k+1:, k] W_kk^T, one CTA per block;
-        // every CTA reads S_kk from D, which no CTA of the launch writes (the
-        // owner writes W_kk over X's block)
         Op op{};
         op.leaf = 1;
         op.dj.push_back(DiagJob{Dh, Dl, w.Xh + kb * ld + kb, w.Xl + kb * ld + kb, w.Wh + kb * ld + kb,
@@ -642,15 +641,77 @@ void gen_chain(std::vector<Op> &ops, const MatWork &w, const InvMatrix &mat, int
             op.dj.push_back(DiagJob{Dh, Dl, nullptr, nullptr, nullptr, nullptr, w.Xh + c, w.Xl + c, w.Lh + c, w.Ll + c,
                                     ld, kb, 1, nullptr});
         }
-        ops.push_back(op);
-        if (!FUSED_PANEL && k + 1 < nb) {  // L[k+1:, k] = X[k+1:, k] W_kk^T on the engine
-            const long long c = (long long)(kb + NB) * ld + kb;
-            Op pn{};
-            pn.g.push_back(split_job(w.mx, kb + NB, kb, w.mx, kb, kb, w.dp - kb - NB, NB, NB, 1.f, 0.f, w.Lh + c,
-                                     w.Ll + c, nullptr, nullptr, ld));
-            ops.push_back(pn);
+        return op;
+    };
+    // L[r0:r1, k] = X[r0:r1, k] W_kk^T
+    auto panel = [&](int k, int r0, int r1) {
+        const int kb = k * NB;
+        const long long c = (long long)r0 * ld + kb;
+        return split_job(w.mx, r0, kb, w.mx, kb, kb, r1 - r0, NB, NB, 1.f, 0.f, w.Lh + c, w.Ll + c, nullptr, nullptr,
+                         ld);
+    };
+    // C[r0:r1, k] -= L[r0:r1, :k] L[k, :k]^T  (C = D_k for the diagonal block)
+    auto update = [&](int k, int r0, int r1, bool diag) {
+        const int kb = k * NB;
+        float *ch = diag ? w.Dh + (long long)kb * NB : w.Xh + (long long)r0 * ld + kb;
+        float *cl = diag ? w.Dl + (long long)kb * NB : w.Xl + (long long)r0 * ld + kb;
+        return split_job(w.ml, r0, 0, w.ml, kb, 0, r1 - r0, NB, kb, -1.f, 1.f, ch, cl, nullptr, nullptr,
+                         diag ? NB : ld);
+    };
+    int last_side = -1;  // chain index of the last op with side problems
+    if (!LOOKAHEAD) {
+        for (int k = 0; k < nb; ++k) {
+            const int kb = k * NB;
+            if (k > 0) {  // the diagonal block into D, the blocks below it in X
+                Op op{};
+                op.g.push_back(update(k, kb, kb + NB, true));
+                if (k + 1 < nb) op.g.push_back(update(k, kb + NB, w.dp, false));
+                ops.push_back(op);
+            }
+            ops.push_back(diag_op(k));
+            if (!FUSED_PANEL && k + 1 < nb) {
+                Op pn{};
+                pn.g.push_back(panel(k, kb + NB, w.dp));
+                ops.push_back(pn);
+            }
+        }
+    } else {
+        // Lookahead: the chain carries only what the next diagonal block
+        // needs -- the first panel block L[k+1, k], then D_{k+1} -= L[k+1, :k+1]
+        // L[k+1, :k+1]^T (split finely over K) -- and the rest of each block
+        // column runs as side problems on the group's side stream, in order:
+        // after the diag op of k, the panel L[k+2:, k]; after the first panel
+        // block of k, the update X[k+2:, k+1] -= L[k+2:, :k+1] L[k+1, :k+1]^T.
+        // The first panel block of k waits for the side update of column k
+        // (launched after the first panel block of k - 1), the diagonal update
+        // of k + 1 for the side panel of k - 1 (the last one that holds a block
+        // of row k + 1), and the triangular inverse for the last side launch.
+        std::vector<int> i_diag(nb, -1), i_first(nb, -1);
+        for (int k = 0; k < nb; ++k) {
+            const int kb = k * NB;
+            Op d = diag_op(k);
+            if (!FUSED_PANEL && k + 2 < nb) d.side.push_back(panel(k, kb + 2 * NB, w.dp));
+            i_diag[k] = (int)ops.size();
+            if (!d.side.empty()) last_side = i_diag[k];
+            ops.push_back(d);
+            if (k + 1 == nb) break;
+            if (!FUSED_PANEL) {
+                Op pf{};
+                pf.g.push_back(panel(k, kb + NB, kb + 2 * NB));
+                if (k >= 1) pf.needs_side = i_first[k - 1];
+                if (k + 2 < nb) pf.side.push_back(update(k + 1, kb + 2 * NB, w.dp, false));
+                i_first[k] = (int)ops.size();
+                if (!pf.side.empty()) last_side = i_first[k];
+                ops.push_back(pf);
+            }
+            Op ud{};
+            ud.g.push_back(update(k + 1, kb + NB, kb + 2 * NB, true));
+            ud.g.back().fine_split = 1;
+            if (k >= 1) ud.needs_side = i_diag[k - 1];
+            ops.push_back(ud);
         }
     }
+    const size_t first_tri = ops.size();
     std::vector<std::vector<std::pair<int, int>>> by_height;
     tri_nodes(0, w.dp, by_height);
     for (size_t ht = 1; ht < by_height.size(); ++ht) {
@@ -667,10 +728,12 @@ void gen_chain(std::vector<Op> &ops, const MatWork &w, const InvMatrix &mat, int
                                     w.Xl + x21, w.Wh + t12, w.Wl + t12, ld));
             x.g.back().ktril = 1;  // W22 is lower triangular
         }
+        if (ops.size() == first_tri) t.needs_side = last_side;
         ops.push_back(t);
         ops.push_back(x);
     }
     Op fin{};
+    if (ops.size() == first_tri) fin.needs_side = last_side;
     TcJob j{};
     j.map_a = j.map_b = w.mw;
     j.M = j.N = w.d;
@@ -751,8 +814,14 @@ std::vector<std::vector<std::pair<int, int>>> schedule_rounds(const std::vector<
 #endif
 constexpr int RESERVED_SMS = KFAC_INV_RESERVED_SMS;  // SMs the second group's engine launches leave free
                                                      // (a tuning constant that may be set at build time)
-constexpr int SIDE_FREE_SMS = 48;  // SMs a group's side launches leave to its own chain
-constexpr int SIDE_GROUPS = 1;     // groups whose lookahead updates run on a side stream (the others
+#ifndef KFAC_INV_SIDE_FREE_SMS
+#define KFAC_INV_SIDE_FREE_SMS 48
+#endif
+constexpr int SIDE_FREE_SMS = KFAC_INV_SIDE_FREE_SMS;  // SMs a group's side launches leave to its own chain
+#ifndef KFAC_INV_SIDE_GROUPS
+#define KFAC_INV_SIDE_GROUPS 1
+#endif
+constexpr int SIDE_GROUPS = KFAC_INV_SIDE_GROUPS;  // groups whose lookahead updates run on a side stream (the others
                                    // run them in their own stream, right after the enabling round)
 
 struct InvGroup {

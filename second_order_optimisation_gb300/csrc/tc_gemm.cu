@@ -1025,6 +1025,7 @@ Plan make_plan(const TcJob *jobs, int n, int kind, int sms) {
         int ks = (int)std::ceil(p.k_tiles[i] / target);
         if (kind == TC_KIND_TF32X3) ks = std::min(ks, TF32X3_MAX_SPLIT);
         ks = std::max(1, std::min(ks, std::min(p.k_tiles[i], 256)));
+        if (jobs[i].fine_split) ks = std::max(1, std::min(16, (int)ceil_div(p.k_tiles[i], 12)));
         if (jobs[i].no_split || jobs[i].ktri) ks = 1;  // (a ktri split would leave late tiles empty)
         p.ksplit[i] = ks;
     }

@@ -86,19 +86,32 @@ def _tri_nodes(o, n, by_height):
 
 
 def chain(dp):
-    """Ops of one dp x dp matrix, in the library's order: ("leaf", k) for a
-    diag kernel launch, ("gemm", problems, side problems) for an engine launch
-    (the library has no side problems at present; the field stays empty)."""
+    """Ops of one dp x dp matrix, in the library's order: ("leaf", k, side
+    problems) for a diag kernel launch, ("gemm", problems, side problems) for
+    an engine launch."""
     ops, nb = [], dp // NB
+    # the lookahead form: the chain holds the diag launch of k, the first panel
+    # block L[k+1, k] and the diagonal update of k + 1; the rest of each block
+    # column is side work launched after them (the library runs it on a side
+    # stream, ordered by events; here it runs right after its op)
     for k in range(nb):
         kb = k * NB
-        if k > 0:   # D_k -= L[k, :k] L[k, :k]^T;  X[k+1:, k] -= L[k+1:, :k] L[k, :k]^T
-            jobs = [_job("L", kb, 0, "L", kb, 0, NB, NB, kb, -1.0, 1.0, C=("D", kb, 0))]
-            if k + 1 < nb:
-                jobs.append(_job("L", kb + NB, 0, "L", kb, 0, dp - kb - NB, NB, kb, -1.0, 1.0,
-                                 C=("X", kb + NB, kb)))
-            ops.append(("gemm", jobs, []))
-        ops.append(("leaf", kb))   # W_kk from D_k, and the panel L[k+1:, k] = X[k+1:, k] W_kk^T
+        side = []
+        if k + 2 < nb:   # L[k+2:, k] = X[k+2:, k] W_kk^T
+            side = [_job("X", kb + 2 * NB, kb, "X", kb, kb, dp - kb - 2 * NB, NB, NB, 1.0, 0.0,
+                         C=("L", kb + 2 * NB, kb))]
+        ops.append(("leaf", kb, side))
+        if k + 1 == nb:
+            break
+        side = []
+        if k + 2 < nb:   # X[k+2:, k+1] -= L[k+2:, :k+1] L[k+1, :k+1]^T
+            side = [_job("L", kb + 2 * NB, 0, "L", kb + NB, 0, dp - kb - 2 * NB, NB, kb + NB, -1.0, 1.0,
+                         C=("X", kb + 2 * NB, kb + NB))]
+        ops.append(("gemm", [_job("X", kb + NB, kb, "X", kb, kb, NB, NB, NB, 1.0, 0.0, C=("L", kb + NB, kb))],
+                    side))
+        # D_{k+1} -= L[k+1, :k+1] L[k+1, :k+1]^T
+        ops.append(("gemm", [_job("L", kb + NB, 0, "L", kb + NB, 0, NB, NB, kb + NB, -1.0, 1.0,
+                                  C=("D", kb + NB, 0))], []))
     by_height = []
     _tri_nodes(0, dp, by_height)
     for ht in range(1, len(by_height)):
@@ -148,14 +161,11 @@ def invert_like_the_library(F, damp, bn):
     for op in chain(dp):
         if op[0] == "leaf":
             o = op[1]
-            # the owner first (the CTAs of one launch run in any order): the
-            # panel CTAs must not see its output, so every CTA reads D_k
             W = diag_block(buf["D"][o:o + NB])[1]
             buf["X"][o:o + NB, o:o + NB] = np.tril(W)
             buf["W"][o:o + NB, o:o + NB] = np.triu(W.T)
-            for i in range(o + NB, dp, NB):
-                Wp = diag_block(buf["D"][o:o + NB])[1]
-                buf["L"][i:i + NB, o:o + NB] = buf["X"][i:i + NB, o:o + NB] @ Wp.T
+            if op[2]:
+                launch(op[2])
             continue
         launch(op[1])
         if op[2]:
@@ -202,8 +212,8 @@ def test_chain_inverts_and_reads_only_written_regions(d, bn):
 
 
 def test_chain_launch_counts():
-    """Ops per matrix: 2 per 128-wide block column (an update, then the diag
-    kernel with the panel; no update for the first) and 2 per level of the
-    triangular inverse."""
-    for dp, expect in ((128, 1), (256, 3 + 2), (1152, 9 * 2 - 1 + 2 * 4), (4608, 36 * 2 - 1 + 2 * 6)):
+    """Ops on the chain of one matrix: the diag launch of every 128-wide block
+    column, the first panel block and the next diagonal update between them,
+    and 2 per level of the triangular inverse."""
+    for dp, expect in ((128, 1), (256, 2 + 2 * 1 + 2), (1152, 9 + 2 * 8 + 2 * 4), (4608, 36 + 2 * 35 + 2 * 6)):
         assert len(chain(dp)) == expect, dp
