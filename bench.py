@@ -16,8 +16,9 @@ the preconditioned gradients copied back inside the timed region.
 `schedule` gives the amortised ms per step of the stale-factor schedule
 (refresh every k steps) for k in {1, 5, 10, 20}, measured by replaying the
 refresh and the precondition-only graphs in that pattern.  For the ResNet-50
-workload the line also carries sub-records for FC 4096 and the 3x3 conv
-(`subrecords`) and the BatchNorm diagonal Fisher (`bn_fisher`).
+workload the line also carries sub-records (`subrecords`: FC 4096, the 3x3
+conv, the single FC layer in fp32, the 1024-sample accumulation in 32 chunks)
+and the BatchNorm diagonal Fisher (`bn_fisher`).
 
 `--impl reference` runs the CPU oracle (the method's plain fp64 statement)
 on the host cores: one whole step, every layer's oracle step timed once
@@ -535,6 +536,62 @@ def subrecord(name, steps, warmup, dev, pk, sm_mhz):
             "kernels": {k: ks[k] for k in keep if k in ks}}
 
 
+def fc_small_fp32_record(steps, warmup, dev):
+    """The single FC layer in fp32 (a [32, 64] + bias column, g [32, 32];
+    factors from I, xi = 0.95, pi-split gamma = 1e-3): the whole step through
+    the C ABI, graph-timed, in microseconds (a latency-bound case)."""
+    import numpy as np
+    import torch
+
+    from second_order_optimisation_gb300 import kfac
+    from second_order_optimisation_gb300 import workloads as W
+    a, g = W.fc_small_fp32()
+    grad = np.concatenate([a, np.ones((32, 1), np.float32)], 1).T @ g / 32.0   # [65, 32] -> G x A below
+    ad, gd = torch.from_numpy(a).to(dev), torch.from_numpy(g).to(dev)
+    gr = torch.from_numpy(np.ascontiguousarray(grad.T)).to(dev)
+    A, G = torch.eye(65, device=dev), torch.eye(32, device=dev)
+    Ai, Gi = torch.empty_like(A), torch.empty_like(G)
+    out = torch.empty(32, 65, device=dev)
+    srcs = [kfac.FactorSource(ad, A, append_one=True, alpha=0.05 / 32, beta=0.95),
+            kfac.FactorSource(gd, G, alpha=0.05 / 32, beta=0.95)]
+    pairs = [kfac.InvertPair(A, G, Ai, Gi)]
+    items = [kfac.PrecondItem(Gi, Ai, gr, out)]
+    wf = torch.empty(kfac.kfac_factor_update_workspace_size(srcs), dtype=torch.uint8, device=dev)
+    wi = torch.empty(kfac.kfac_damp_invert_workspace_size(pairs), dtype=torch.uint8, device=dev)
+    wp = torch.empty(kfac.kfac_precondition_workspace_size(items), dtype=torch.uint8, device=dev)
+
+    def one():
+        kfac.kfac_factor_update(srcs, wf)
+        kfac.kfac_damp_invert(pairs, 1e-3, workspace=wi)
+        kfac.kfac_precondition(items, wp)
+    stream = torch.cuda.current_stream()
+    g_ = graph_of(one, stream)
+    ms = time_replays([g_], max(steps, 20), warmup, stream)
+    return {"workload": "fc64x32_fp32_kfac_step", "us": ms * 1e3, "dtype": "f32"}
+
+
+def accumulation_record(steps, warmup, dev, pk, chunks=32):
+    """The ResNet-50 set with factors accumulated over a 1024-sample
+    mini-batch in 32 chunks of 32 (beta = xi on the first chunk, 1 after;
+    the same seeded chunk re-read each time, 1.38 GB, larger than L2), then
+    damped, inverted and applied: graph-timed."""
+    import torch
+    m = measure("resnet50", 1, 1, dev, pk, kernels=False)
+    step, (dx, dg, dgr), stream = m["step"], m["inp"].views, m["stream"]
+    rows = [L.rows(m["batch"]) * chunks for L in m["layers"]]
+
+    def acc():
+        for c in range(chunks):
+            step.factor_update(dx, dg, rows_total=rows, first=(c == 0))
+        step.damp_invert()
+        step.precondition(dgr)
+    g_ = graph_of(acc, stream)
+    ms = time_replays([g_], max(1, min(steps, 5)), 1, stream)
+    syrk = flops(m["layers"], m["batch"])["syrk"] * chunks
+    return {"workload": "resnet50_accum1024_kfac_step", "ms": ms, "chunks": chunks,
+            "syrk_tflops": syrk / (ms * 1e-3) / 1e12}
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -597,6 +654,8 @@ def run_ours(args, world, rank, local):
     if args.workload == "resnet50" and not args.no_subrecords:
         subs = {n: subrecord(n, min(args.steps, 10), min(args.warmup, 3), dev, pk, clk.get("sm_mhz"))
                 for n in ("fc4096", "conv3x3_256")}
+        subs["fc64x32_fp32"] = fc_small_fp32_record(args.steps, args.warmup, dev)
+        subs["accum1024"] = accumulation_record(args.steps, args.warmup, dev, pk)
         bn_line = bn_bench(args, dev, stream, pk)
 
     line = {"metric": METRIC, "value": ms, "unit": "ms", "n_gpus": args.gpus, "steps": args.steps,

@@ -819,7 +819,7 @@ constexpr int RESERVED_SMS = KFAC_INV_RESERVED_SMS;  // SMs the second group's e
 #endif
 constexpr int SIDE_FREE_SMS = KFAC_INV_SIDE_FREE_SMS;  // SMs a group's side launches leave to its own chain
 #ifndef KFAC_INV_SIDE_GROUPS
-#define KFAC_INV_SIDE_GROUPS 1
+#define KFAC_INV_SIDE_GROUPS 2
 #endif
 constexpr int SIDE_GROUPS = KFAC_INV_SIDE_GROUPS;  // groups whose lookahead updates run on a side stream (the others
                                    // run them in their own stream, right after the enabling round)
