@@ -52,7 +52,14 @@ SCHEDULE_KS = (1, 5, 10, 20)
 # kernel build (dram__bytes_read.sum + dram__bytes_write.sum), with the
 # profile summary it comes from; None where no capture of the current build
 # exists.
-NCU_TRAFFIC = {}
+_TRAFFIC_SRC = "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch (serialised, cold caches), " \
+               "profiles/resnet50_kfac_step_launches.md"
+NCU_TRAFFIC = {
+    "tc_gemm_tf32x3@inverse": (48.78e6, _TRAFFIC_SRC),
+    "inv_diag@inverse": (1.66e6, _TRAFFIC_SRC),
+    "inv_prep@inverse": (1578.7e6, _TRAFFIC_SRC),
+    "im2col@factors": (69.6e6, _TRAFFIC_SRC),
+}
 
 
 # ------------------------------------------------------------------ workloads

@@ -42,6 +42,12 @@ constexpr int NUM_THREADS = 192;
 constexpr int TMEM_ACC = 2 * BN;  // two accumulators (columns 0 and BN), alternating
 constexpr int MAX_PROBS = 152;
 constexpr int GROUP = 8;              // row blocks per band of the grouped tile order
+#ifndef KFAC_BF16_ITEMS_PER_SM
+#define KFAC_BF16_ITEMS_PER_SM 4.0  // bf16 K splits aim at this many work items per SM (tuning constant)
+#endif
+#ifndef KFAC_ZIGZAG
+#define KFAC_ZIGZAG 1  // reverse the CTA order of work items every other round (tuning constant)
+#endif
 #ifndef KFAC_TF32X3_CHUNK
 #define KFAC_TF32X3_CHUNK 8
 #endif
@@ -644,6 +650,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int w_first = blockIdx.x, w_step = gridDim.x;
+    // work item of round r: items are sorted longest first, and the CTA order
+    // reverses every other round (a CTA that took a long item takes a short
+    // one next), which evens out the CTAs' totals
+    auto widx = [&](int r) { return r * w_step + ((KFAC_ZIGZAG && (r & 1)) ? w_step - 1 - w_first : w_first); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Tr::STAGES; ++s) {
@@ -675,7 +685,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             uint32_t phase = 0;
             int last_p = -1;
             int issued = 0;  // stages armed so far
-            for (int w = w_first; w < P.total_work && !*abort_flag; w += w_step) {
+            for (int r = 0, w = widx(0); w < P.total_work && !*abort_flag; w = widx(++r)) {
                 Work k = decode_work(P, w);
                 const TcProb &q = P.prob[k.p];
                 const CUtensorMap *ma = P.maps + q.map_a;
@@ -746,7 +756,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             uint32_t phase = 0;
             int cc = 0;  // accumulation chunks so far (accumulator cc & 1)
             bool ok = true;
-            for (int w = w_first; w < P.total_work && ok && !*abort_flag; w += w_step) {
+            for (int r = 0, w = widx(0); w < P.total_work && ok && !*abort_flag; w = widx(++r)) {
                 Work k = decode_work(P, w);
                 const TcProb &q = P.prob[k.p];
                 const bool diag = KIND == TC_KIND_BF16 && q.syrk && k.tm == k.tn;
@@ -816,7 +826,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         const uint32_t t_sum = t_quarter + 2 * BN;  // running sum of a chunked item (tf32x3)
         int cc = 0;
         bool nonfin = false;  // a value this lane stored was NaN or infinite
-        for (int w = w_first; w < P.total_work && !*abort_flag; w += w_step) {
+        for (int r = 0, w = widx(0); w < P.total_work && !*abort_flag; w = widx(++r)) {
             Work k = decode_work(P, w);
             const TcProb &q = P.prob[k.p];
             const int i0 = k.tm * BM + quarter * 32;
@@ -1020,7 +1030,7 @@ Plan make_plan(const TcJob *jobs, int n, int kind, int sms) {
     // items keep at least 8 K tiles; a tf32x3 tile takes at most
     // TF32X3_MAX_SPLIT splits (its last CTA reads all partials).
     const double min_kt = kind == TC_KIND_BF16 ? 8.0 : TF32X3_MIN_KT;
-    const double target = std::max(min_kt, total / (sms * 2.0));
+    const double target = std::max(min_kt, total / (sms * (kind == TC_KIND_BF16 ? KFAC_BF16_ITEMS_PER_SM : 2.0)));
     for (int i = 0; i < n; ++i) {
         int ks = (int)std::ceil(p.k_tiles[i] / target);
         if (kind == TC_KIND_TF32X3) ks = std::min(ks, TF32X3_MAX_SPLIT);
