@@ -333,6 +333,27 @@ extern "C" int kfac_timing_read(double *ms, long long *launches, int n) {
     return status;
 }
 
+extern "C" int kfac_timing_read_launches(double *start_ms, double *dur_ms, int *kind, int n) {
+    std::lock_guard<std::mutex> lock(g_tmu);
+    int count = 0;
+    bool failed = false;
+    for (TimingRec &r : g_recs) {
+        float t = 0.f, t0 = 0.f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess ||
+            cudaEventElapsedTime(&t0, g_recs.front().start, r.start) != cudaSuccess)
+            failed = true;
+        if (count < n) {
+            if (start_ms) start_ms[count] = t0;
+            if (dur_ms) dur_ms[count] = t;
+            if (kind) kind[count] = r.kind;
+        }
+        ++count;
+        g_free.push_back(r);
+    }
+    g_recs.clear();
+    return failed ? -1 : count;
+}
+
 // ------------------------------------------------------------ factor update
 
 extern "C" size_t kfac_factor_update_workspace_size(const kfac_factor_desc *descs, int count) {

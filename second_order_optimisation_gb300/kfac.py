@@ -33,7 +33,7 @@ EXPORTS = ("kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_timi
            "kfac_timing_read", "kfac_timing_kind_name", "kfac_factor_update_workspace_size",
            "kfac_factor_update", "kfac_damp_invert_workspace_size", "kfac_damp_invert",
            "kfac_precondition_workspace_size", "kfac_precondition", "kfac_bn_diag_fisher",
-           "kfac_noalloc_scratch_bytes", "kfac_precondition_noalloc")
+           "kfac_noalloc_scratch_bytes", "kfac_precondition_noalloc", "kfac_timing_read_launches")
 
 
 class KfacError(RuntimeError):
@@ -104,6 +104,8 @@ def load() -> ctypes.CDLL:
         lib.kfac_timing_enable.restype = i32
         lib.kfac_timing_read.argtypes = [vp, vp, i32]
         lib.kfac_timing_read.restype = i32
+        lib.kfac_timing_read_launches.argtypes = [vp, vp, vp, i32]
+        lib.kfac_timing_read_launches.restype = i32
         lib.kfac_timing_kind_name.argtypes = [i32]
         lib.kfac_timing_kind_name.restype = ctypes.c_char_p
         lib.kfac_factor_update_workspace_size.argtypes = [vp, i32]
@@ -148,6 +150,19 @@ def timing_read() -> dict:
         if name and cnt[k]:
             out[name] = (ms[k], int(cnt[k]))
     return out
+
+
+def timing_read_launches(n: int = 65536) -> list:
+    """[(start ms, duration ms, kernel kind name)] of every recorded launch in
+    enqueue order, since the last read (synchronises)."""
+    lib = load()
+    st = (ctypes.c_double * n)()
+    du = (ctypes.c_double * n)()
+    kd = (ctypes.c_int * n)()
+    cnt = lib.kfac_timing_read_launches(st, du, kd, n)
+    if cnt < 0:
+        raise KfacError(KFAC_ERR_CUDA, "kfac_timing_read_launches")
+    return [(st[i], du[i], lib.kfac_timing_kind_name(kd[i]).decode()) for i in range(min(cnt, n))]
 
 
 def status_string(status: int) -> str:

@@ -455,3 +455,21 @@ def test_fc64x32_fp32_step():
         R = (F + dmp * np.eye(F.shape[0])) @ inv - np.eye(F.shape[0])
         assert np.abs(R).max() <= 1e-3
     assert rel(f64(out), ref["precond"]) <= 1e-4
+
+
+def test_timing_records_every_launch():
+    """The diagnostic per-launch record: one entry per library launch, in
+    enqueue order, with its kernel kind; reading clears it."""
+    x = bf16(workloads.relu_normal_f32((2, 9, 9, 64), "timing")).to(DEV)
+    F = torch.zeros(576, 576, device=DEV)
+    kfac.timing_enable(True)
+    kfac.timing_read_launches()
+    n0 = kfac.launch_count()
+    kfac.kfac_factor_update([kfac.FactorSource(x, F, 3, 3, (1, 1), (1, 1), alpha=1.0 / 162)])
+    n1 = kfac.launch_count()
+    rec = kfac.timing_read_launches()
+    kfac.timing_enable(False)
+    assert len(rec) == n1 - n0 > 0
+    assert all(d >= 0.0 for _, d, _ in rec) and rec[0][0] == 0.0
+    assert "tc_gemm_bf16" in {k for _, _, k in rec}
+    assert kfac.timing_read_launches() == []
