@@ -27,6 +27,7 @@
 // info[matrix]; nothing traps, and every wait on a barrier has a time limit.
 #include <algorithm>
 #include <cfloat>
+#include <functional>
 #include <memory>
 #include <mutex>
 #include <vector>
@@ -55,6 +56,32 @@ constexpr bool FUSED_PANEL = KFAC_INV_FUSED_PANEL;
 // side stream, off the chain of diagonal blocks.  A tuning constant that may
 // be set at build time.
 constexpr bool LOOKAHEAD = KFAC_INV_LOOKAHEAD && !KFAC_INV_FUSED_PANEL;
+#ifndef KFAC_INV_SIDE_DIAG_BULK
+#define KFAC_INV_SIDE_DIAG_BULK 1
+#endif
+// With the lookahead: the diagonal update of block k + 1 keeps only its last
+// term L[k+1, k] L[k+1, k]^T on the chain, the earlier terms run with the
+// side update of column k (1); or the whole sum on the chain, split finely
+// over K (0).  A tuning constant that may be set at build time.
+constexpr bool SIDE_DIAG_BULK = KFAC_INV_SIDE_DIAG_BULK;
+#ifndef KFAC_INV_EARLY_TRI
+#define KFAC_INV_EARLY_TRI 0
+#endif
+#ifndef KFAC_INV_EARLY_TRI_MIN_NB
+#define KFAC_INV_EARLY_TRI_MIN_NB 8
+#endif
+// Early triangular inverse (see gen_chain): for a matrix of at least
+// EARLY_TRI_MIN_NB block columns and at least 3/4 as many as the call's
+// widest, each node of W = L^-1 runs on a third stream as soon as the
+// Cholesky columns it reads are done, instead of after the whole
+// factorisation.  Tuning constants that may be set at build time.  Measured:
+// three 4608-wide factors alone 5.50 -> 5.25 ms, but the ResNet-50 factor set
+// 7.06 -> 7.35 ms (graph; 8.4 ms unless the process allows more than the
+// default 8 hardware queues): there the second group's work already fills
+// the critical group's tail, and the inverse's products moved into the
+// factorisation slow its chain.  Off by default.
+constexpr bool EARLY_TRI = KFAC_INV_EARLY_TRI && LOOKAHEAD;
+constexpr int EARLY_TRI_MIN_NB = KFAC_INV_EARLY_TRI_MIN_NB;
 constexpr int MAT_MAX = 224;
 // tensor maps of one matrix: X, Wt, LT pairs, each as hi and the (hi, lo)
 // pair with 128-row boxes, and hi / lo with 32-row boxes
@@ -565,6 +592,14 @@ struct Op {
     std::vector<TcJob> side;  // engine problems that may start once this op is done (lookahead,
                               // launched on the group's side stream)
     int needs_side = -1;      // chain index of the op whose side problems must be done first
+    bool needs_tri = false;   // waits for the chain's early triangular inverse
+};
+
+// One launch of a chain's early triangular inverse (a node's T or W21
+// product), on the group's third stream once chain op `after` is done.
+struct TriOp {
+    int after;
+    TcJob job;
 };
 
 // Working buffers of one matrix (fp32 (hi, lo) pairs, [dp][dp] each):
@@ -623,7 +658,8 @@ int tri_nodes(int o, int n, std::vector<std::vector<std::pair<int, int>>> &by_he
 // upper triangular with zeros below in Wt, so the products run over whole
 // blocks; T reads W11^T from Wt only from each output tile's first column on
 // (ktri), where Wt holds its upper part and diagonal blocks.
-void gen_chain(std::vector<Op> &ops, const MatWork &w, const InvMatrix &mat, int *info) {
+void gen_chain(std::vector<Op> &ops, std::vector<TriOp> &tri, bool early_tri, const MatWork &w, const InvMatrix &mat,
+               int *info) {
     const long long ld = w.dp;
     const int nb = w.dp / NB;
     auto diag_op = [&](int k) {
@@ -658,7 +694,14 @@ void gen_chain(std::vector<Op> &ops, const MatWork &w, const InvMatrix &mat, int
         return split_job(w.ml, r0, 0, w.ml, kb, 0, r1 - r0, NB, kb, -1.f, 1.f, ch, cl, nullptr, nullptr,
                          diag ? NB : ld);
     };
+    // D_c -= L[c, j0:j1] L[c, j0:j1]^T (block columns j0 .. j1 - 1)
+    auto dupd = [&](int c, int j0, int j1) {
+        const int cb = c * NB;
+        return split_job(w.ml, cb, j0 * NB, w.ml, cb, j0 * NB, NB, NB, (j1 - j0) * NB, -1.f, 1.f,
+                         w.Dh + (long long)cb * NB, w.Dl + (long long)cb * NB, nullptr, nullptr, NB);
+    };
     int last_side = -1;  // chain index of the last op with side problems
+    std::vector<int> i_diag(nb, -1), i_first(nb, -1);
     if (!LOOKAHEAD) {
         for (int k = 0; k < nb; ++k) {
             const int kb = k * NB;
@@ -677,16 +720,20 @@ void gen_chain(std::vector<Op> &ops, const MatWork &w, const InvMatrix &mat, int
         }
     } else {
         // Lookahead: the chain carries only what the next diagonal block
-        // needs -- the first panel block L[k+1, k], then D_{k+1} -= L[k+1, :k+1]
-        // L[k+1, :k+1]^T (split finely over K) -- and the rest of each block
-        // column runs as side problems on the group's side stream, in order:
-        // after the diag op of k, the panel L[k+2:, k]; after the first panel
-        // block of k, the update X[k+2:, k+1] -= L[k+2:, :k+1] L[k+1, :k+1]^T.
-        // The first panel block of k waits for the side update of column k
-        // (launched after the first panel block of k - 1), the diagonal update
-        // of k + 1 for the side panel of k - 1 (the last one that holds a block
-        // of row k + 1), and the triangular inverse for the last side launch.
-        std::vector<int> i_diag(nb, -1), i_first(nb, -1);
+        // needs -- the first panel block L[k+1, k], then the last term of the
+        // diagonal update, D_{k+1} -= L[k+1, k] L[k+1, k]^T -- and the rest of
+        // each block column runs as side problems on the group's side stream,
+        // in order: after the diag op of k, the panel L[k+2:, k]; after the
+        // first panel block of k, the update X[k+2:, k+1] -= L[k+2:, :k+1]
+        // L[k+1, :k+1]^T and the earlier terms of the next diagonal block,
+        // D_{k+2} -= L[k+2, :k+1] L[k+2, :k+1]^T.  The first panel block of k
+        // waits for the side launch after the first panel block of k - 1 (the
+        // update of column k and the earlier terms of D_{k+1}, which the
+        // diagonal update after it then completes), and the triangular
+        // inverse for the last side launch.  (Without SIDE_DIAG_BULK the
+        // chain's diagonal update runs over all of L[k+1, :k+1], split finely
+        // over K, after the side panel of k - 1, the last one holding a block
+        // of row k + 1.)
         for (int k = 0; k < nb; ++k) {
             const int kb = k * NB;
             Op d = diag_op(k);
@@ -699,40 +746,89 @@ void gen_chain(std::vector<Op> &ops, const MatWork &w, const InvMatrix &mat, int
                 Op pf{};
                 pf.g.push_back(panel(k, kb + NB, kb + 2 * NB));
                 if (k >= 1) pf.needs_side = i_first[k - 1];
-                if (k + 2 < nb) pf.side.push_back(update(k + 1, kb + 2 * NB, w.dp, false));
+                if (k + 2 < nb) {
+                    pf.side.push_back(update(k + 1, kb + 2 * NB, w.dp, false));
+                    // D_{k+2} -= L[k+2, :k+1] L[k+2, :k+1]^T (its last term stays on the chain)
+                    if (SIDE_DIAG_BULK) pf.side.push_back(dupd(k + 2, 0, k + 1));
+                }
                 i_first[k] = (int)ops.size();
                 if (!pf.side.empty()) last_side = i_first[k];
                 ops.push_back(pf);
             }
             Op ud{};
-            ud.g.push_back(update(k + 1, kb + NB, kb + 2 * NB, true));
-            ud.g.back().fine_split = 1;
-            if (k >= 1) ud.needs_side = i_diag[k - 1];
+            if (SIDE_DIAG_BULK) {
+                // D_{k+1} -= L[k+1, k] L[k+1, k]^T: the terms before it were
+                // subtracted by the side launch the first panel block waited for
+                ud.g.push_back(dupd(k + 1, k, k + 1));
+            } else {
+                ud.g.push_back(update(k + 1, kb + NB, kb + 2 * NB, true));
+                ud.g.back().fine_split = 1;
+                if (k >= 1) ud.needs_side = i_diag[k - 1];
+            }
             ops.push_back(ud);
         }
     }
+    // the two products of the triangular-inverse node over [o, o + n)
+    auto node_t = [&](int o, int n) {
+        const int h = NB * (n / NB / 2), m = n - h;
+        const long long t12 = (long long)o * ld + o + h;
+        // T = L21 W11 (B rows: W11^T rows, in Wt), stored as T^T in LT's upper part
+        TcJob j = split_job(w.ml, o + h, o, w.mw, o, o, m, h, h, 1.f, 0.f, nullptr, nullptr, w.Lh + t12,
+                            w.Ll + t12, ld);
+        j.ktri = 1;
+        return j;
+    };
+    auto node_x = [&](int o, int n) {
+        const int h = NB * (n / NB / 2), m = n - h;
+        const long long x21 = (long long)(o + h) * ld + o, t12 = (long long)o * ld + o + h;
+        // W21 = -W22 T (A: W22 rows, in X; B rows: T^T rows, in LT), W21^T into Wt
+        TcJob j = split_job(w.mx, o + h, o + h, w.ml, o, o + h, m, h, m, -1.f, 0.f, w.Xh + x21, w.Xl + x21,
+                            w.Wh + t12, w.Wl + t12, ld);
+        j.ktril = 1;  // W22 is lower triangular
+        return j;
+    };
     const size_t first_tri = ops.size();
-    std::vector<std::vector<std::pair<int, int>>> by_height;
-    tri_nodes(0, w.dp, by_height);
-    for (size_t ht = 1; ht < by_height.size(); ++ht) {
-        Op t{}, x{};
-        for (const auto &nd : by_height[ht]) {
-            const int o = nd.first, n = nd.second, h = NB * (n / NB / 2), m = n - h;
-            const long long x21 = (long long)(o + h) * ld + o, t12 = (long long)o * ld + o + h;
-            // T = L21 W11 (B rows: W11^T rows, in Wt), stored as T^T in LT's upper part
-            t.g.push_back(split_job(w.ml, o + h, o, w.mw, o, o, m, h, h, 1.f, 0.f, nullptr, nullptr, w.Lh + t12,
-                                    w.Ll + t12, ld));
-            t.g.back().ktri = 1;
-            // W21 = -W22 T (A: W22 rows, in X; B rows: T^T rows, in LT), W21^T into Wt
-            x.g.push_back(split_job(w.mx, o + h, o + h, w.ml, o, o + h, m, h, m, -1.f, 0.f, w.Xh + x21,
-                                    w.Xl + x21, w.Wh + t12, w.Wl + t12, ld));
-            x.g.back().ktril = 1;  // W22 is lower triangular
-        }
-        if (ops.size() == first_tri) t.needs_side = last_side;
-        ops.push_back(t);
-        ops.push_back(x);
-    }
     Op fin{};
+    if (early_tri) {
+        // Early triangular inverse: the nodes in post-order with each T
+        // before the right subtree, every product a launch of its own on the
+        // third stream.  T of node [o, o + n) (split at h) reads L21 -- the
+        // panels of block columns below (o + h) / 128 -- and W11 (the left
+        // subtree, earlier on the stream); the first panel block of column
+        // c + 1 is done only after the side panel of column c (the side
+        // stream runs that panel before the update the first block waits
+        // for), so T waits for the first panel block of column (o + h) / 128
+        // (of the column before it when that is the last one).  W21 needs
+        // W22, whose last diagonal block comes from the diag op of column
+        // (o + n) / 128 - 1.  Both write only what the factorisation no
+        // longer reads: T^T above L's diagonal, W21 over X's block row
+        // (the Schur columns there were consumed by their panels) and W21^T
+        // above Wt's diagonal.
+        std::function<void(int, int)> visit = [&](int o, int n) {
+            if (n == NB) return;
+            const int h = NB * (n / NB / 2);
+            visit(o, h);
+            const int c = (o + h) / NB;  // first column of the right half
+            tri.push_back(TriOp{i_first[std::min(c, nb - 2)], node_t(o, n)});
+            visit(o + h, n - h);
+            tri.push_back(TriOp{i_diag[(o + n) / NB - 1], node_x(o, n)});
+        };
+        visit(0, w.dp);
+        fin.needs_tri = true;
+    } else {
+        std::vector<std::vector<std::pair<int, int>>> by_height;
+        tri_nodes(0, w.dp, by_height);
+        for (size_t ht = 1; ht < by_height.size(); ++ht) {
+            Op t{}, x{};
+            for (const auto &nd : by_height[ht]) {
+                t.g.push_back(node_t(nd.first, nd.second));
+                x.g.push_back(node_x(nd.first, nd.second));
+            }
+            if (ops.size() == first_tri) t.needs_side = last_side;
+            ops.push_back(t);
+            ops.push_back(x);
+        }
+    }
     if (ops.size() == first_tri) fin.needs_side = last_side;
     TcJob j{};
     j.map_a = j.map_b = w.mw;
@@ -821,8 +917,24 @@ constexpr int SIDE_FREE_SMS = KFAC_INV_SIDE_FREE_SMS;  // SMs a group's side lau
 #ifndef KFAC_INV_SIDE_GROUPS
 #define KFAC_INV_SIDE_GROUPS 2
 #endif
+#ifndef KFAC_INV_TRI_FREE_SMS
+#define KFAC_INV_TRI_FREE_SMS 48
+#endif
+constexpr int TRI_FREE_SMS = KFAC_INV_TRI_FREE_SMS;  // SMs a group's early-inverse launches leave to the rest
+#ifndef KFAC_INV_TRI_HIGH_PRIO
+#define KFAC_INV_TRI_HIGH_PRIO 0
+#endif
+constexpr bool TRI_HIGH_PRIO = KFAC_INV_TRI_HIGH_PRIO;  // early-inverse streams at their group's priority (else low)
 constexpr int SIDE_GROUPS = KFAC_INV_SIDE_GROUPS;  // groups whose lookahead updates run on a side stream (the others
                                    // run them in their own stream, right after the enabling round)
+
+// One launch of a group's early triangular inverse: the same step of every
+// chain of one width, after the rounds that hold the ops it waits for.
+struct TriStep {
+    std::vector<TcJob> g;
+    std::vector<int> wait_rounds;  // main-stream rounds to wait for
+    int key = 0;                   // enqueued after this round (non-decreasing)
+};
 
 struct InvGroup {
     std::vector<int> members;  // chain indices
@@ -830,6 +942,12 @@ struct InvGroup {
     std::vector<int> round_kind;
     std::vector<std::vector<TcJob>> side;   // per round: side problems launched once it is done
     std::vector<std::vector<int>> waits;    // per round: rounds whose side launch must finish first
+    std::vector<TriStep> tri;               // early triangular inverse, in stream order
+    std::vector<std::vector<int>> tri_waits;  // per round: tri steps that must finish first
+    std::vector<char> record_main;          // per round: a tri step waits for it
+    int tri_ctas = 0;
+    char *tri_ws = nullptr;
+    size_t tri_bytes = 0;
     int max_ctas = 0;          // engine grid cap (0: all SMs)
     int side_ctas = 0;         // grid cap of the side launches
     char *tc_ws = nullptr;
@@ -844,6 +962,7 @@ struct InvPlan {
     std::vector<CUtensorMap> maps;
     std::vector<MatWork> work;
     std::vector<std::vector<Op>> chains;
+    std::vector<std::vector<TriOp>> tri;  // per chain: its early triangular inverse (or empty)
     std::vector<InvGroup> groups;  // groups[0]: the critical chains
     size_t longest = 0;
 };
@@ -854,6 +973,12 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
     p.dev_maps = ws.take<CUtensorMap>(MAPS_PER_MATRIX * (size_t)std::max(nmats, 1));
     p.work.resize(nmats);
     p.chains.assign(nmats, {});
+    p.tri.assign(nmats, {});
+    // the early triangular inverse serves the longest chains (the critical
+    // group's); the others keep theirs at the end of the chain, which costs
+    // the critical group less in contention
+    int nb_max = 0;
+    for (int k = 0; k < nmats; ++k) nb_max = std::max(nb_max, padded(mats[k].d) / NB);
     for (int k = 0; k < nmats; ++k) {
         MatWork &w = p.work[k];
         w.d = mats[k].d;
@@ -884,7 +1009,9 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
         w.mx = base;
         w.mw = base + 4;
         w.ml = base + 8;
-        gen_chain(p.chains[k], w, mats[k], info_dev ? info_dev + k : nullptr);
+        const int nbk = w.dp / NB;
+        const bool early = EARLY_TRI && nbk >= EARLY_TRI_MIN_NB && 4 * nbk >= 3 * nb_max;
+        gen_chain(p.chains[k], p.tri[k], early, w, mats[k], info_dev ? info_dev + k : nullptr);
         p.longest = std::max(p.longest, p.chains[k].size());
     }
     if (p.maps.size() != (size_t)MAPS_PER_MATRIX * nmats) return KFAC_ERR_WORKSPACE;  // device map area
@@ -938,6 +1065,69 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
         g.tc_ws = ws.take<char>(tcb);
         g.side_bytes = sideb;
         g.side_ws = ws.take<char>(sideb);
+
+        // early triangular inverse: chains of one padded width have the same
+        // steps, batched into one launch each; the widths' sequences are
+        // merged by the round each step can be enqueued after
+        g.tri.clear();
+        g.tri_waits.assign(R, {});
+        g.record_main.assign(R, 0);
+        g.tri_ctas = std::max(1, (g.max_ctas > 0 ? g.max_ctas : sms) - TRI_FREE_SMS);
+        std::vector<int> cls_dp;
+        std::vector<std::vector<int>> cls;
+        for (int k : g.members) {
+            if (p.tri[k].empty()) continue;
+            size_t c = 0;
+            while (c < cls_dp.size() && cls_dp[c] != p.work[k].dp) ++c;
+            if (c == cls_dp.size()) { cls_dp.push_back(p.work[k].dp); cls.emplace_back(); }
+            cls[c].push_back(k);
+        }
+        std::vector<std::pair<int, int>> last_of;  // (class, index in g.tri of its last step)
+        std::vector<std::vector<TriStep>> seqs(cls.size());
+        for (size_t c = 0; c < cls.size(); ++c) {
+            const size_t nsteps = p.tri[cls[c][0]].size();
+            int run = 0;
+            for (size_t s = 0; s < nsteps; ++s) {
+                TriStep st;
+                for (int k : cls[c]) {
+                    const TriOp &t = p.tri[k][s];
+                    st.g.push_back(t.job);
+                    const int r = round_of[k][t.after];
+                    if (std::find(st.wait_rounds.begin(), st.wait_rounds.end(), r) == st.wait_rounds.end())
+                        st.wait_rounds.push_back(r);
+                    run = std::max(run, r);
+                }
+                st.key = run;
+                seqs[c].push_back(st);
+            }
+        }
+        std::vector<size_t> pos(cls.size(), 0);
+        std::vector<int> last_step(cls.size(), -1);
+        for (;;) {  // merge by key, each width's order kept
+            int best = -1;
+            for (size_t c = 0; c < cls.size(); ++c)
+                if (pos[c] < seqs[c].size() && (best < 0 || seqs[c][pos[c]].key < seqs[best][pos[best]].key))
+                    best = (int)c;
+            if (best < 0) break;
+            last_step[best] = (int)g.tri.size();
+            g.tri.push_back(seqs[best][pos[best]++]);
+        }
+        size_t trib = 0;
+        for (const TriStep &st : g.tri) {
+            for (int r : st.wait_rounds) g.record_main[r] = 1;
+            trib = std::max(trib, tc_workspace_bytes(st.g.data(), (int)st.g.size(), TC_KIND_TF32X3, g.tri_ctas));
+        }
+        // a chain's last op (the final product) waits for its width's last step
+        for (size_t c = 0; c < cls.size(); ++c)
+            for (int k : cls[c]) {
+                const int r = round_of[k][(int)p.chains[k].size() - 1];
+                if (!p.chains[k].back().needs_tri || last_step[c] < 0) return KFAC_ERR_UNSUPPORTED;
+                if (g.tri[last_step[c]].key >= r) return KFAC_ERR_UNSUPPORTED;  // (cannot happen)
+                if (std::find(g.tri_waits[r].begin(), g.tri_waits[r].end(), last_step[c]) == g.tri_waits[r].end())
+                    g.tri_waits[r].push_back(last_step[c]);
+            }
+        g.tri_bytes = trib;
+        g.tri_ws = ws.take<char>(trib);
     }
     return KFAC_OK;
 }
@@ -1034,14 +1224,16 @@ namespace {
 // lookahead updates) on a second stream: a side launch starts once the round
 // that enables it is done (an event), and a round that needs a side launch
 // waits for its event.  ev_main / ev_side hold one event per round.
-kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st, cudaStream_t side, bool use_side,
-                      cudaEvent_t *ev_main, cudaEvent_t *ev_side) {
+kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st, cudaStream_t side, cudaStream_t tri,
+                      bool use_side, cudaEvent_t *ev_main, cudaEvent_t *ev_side, cudaEvent_t *ev_tri) {
     std::vector<DiagJob> leaves;
     std::vector<TcJob> gemms;
     kfac_status s = KFAC_OK;
+    size_t next_tri = 0;
     for (size_t r = 0; r < g.rounds.size(); ++r) {
         if (use_side)
             for (int src : g.waits[r]) KFAC_CUDA_TRY(cudaStreamWaitEvent(st, ev_side[src], 0));
+        for (int t : g.tri_waits[r]) KFAC_CUDA_TRY(cudaStreamWaitEvent(st, ev_tri[t], 0));
         leaves.clear();
         gemms.clear();
         for (const auto &ki : g.rounds[r]) {
@@ -1070,6 +1262,17 @@ kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st, cuda
                 return s;
             KFAC_CUDA_TRY(cudaEventRecord(ev_side[r], side));
         }
+        if (g.record_main[r] && !(use_side && !g.side[r].empty())) KFAC_CUDA_TRY(cudaEventRecord(ev_main[r], st));
+        // early triangular inverse: every step whose rounds are now enqueued
+        for (; next_tri < g.tri.size() && g.tri[next_tri].key <= (int)r; ++next_tri) {
+            const TriStep &ts = g.tri[next_tri];
+            for (int wr : ts.wait_rounds) KFAC_CUDA_TRY(cudaStreamWaitEvent(tri, ev_main[wr], 0));
+            Arena tail(g.tri_ws, g.tri_bytes);
+            if ((s = tc_run(ts.g.data(), (int)ts.g.size(), TC_KIND_TF32X3, p.dev_maps, tail, p.err, tri,
+                            g.tri_ctas)) != KFAC_OK)
+                return s;
+            KFAC_CUDA_TRY(cudaEventRecord(ev_tri[next_tri], tri));
+        }
     }
     return KFAC_OK;
 }
@@ -1083,8 +1286,8 @@ constexpr int EVENT_POOL = 1024;
 struct GroupStreams {
     std::mutex mu;
     bool ready = false;
-    cudaStream_t main[2] = {nullptr, nullptr}, side[2] = {nullptr, nullptr};
-    cudaEvent_t fork = nullptr, done[4] = {nullptr, nullptr, nullptr, nullptr};
+    cudaStream_t main[2] = {nullptr, nullptr}, side[2] = {nullptr, nullptr}, tri[2] = {nullptr, nullptr};
+    cudaEvent_t fork = nullptr, done[6] = {};
     std::vector<cudaEvent_t> pool;  // per-round events of the two groups
 };
 
@@ -1101,9 +1304,10 @@ kfac_status ensure_streams(GroupStreams &g) {
         const int prio = k == 0 ? greatest : least;
         KFAC_CUDA_TRY(cudaStreamCreateWithPriority(&g.main[k], cudaStreamNonBlocking, prio));
         KFAC_CUDA_TRY(cudaStreamCreateWithPriority(&g.side[k], cudaStreamNonBlocking, prio));
+        KFAC_CUDA_TRY(cudaStreamCreateWithPriority(&g.tri[k], cudaStreamNonBlocking, TRI_HIGH_PRIO ? prio : least));
     }
     KFAC_CUDA_TRY(cudaEventCreateWithFlags(&g.fork, cudaEventDisableTiming));
-    for (int k = 0; k < 4; ++k) KFAC_CUDA_TRY(cudaEventCreateWithFlags(&g.done[k], cudaEventDisableTiming));
+    for (int k = 0; k < 6; ++k) KFAC_CUDA_TRY(cudaEventCreateWithFlags(&g.done[k], cudaEventDisableTiming));
     g.pool.resize(EVENT_POOL);
     for (cudaEvent_t &e : g.pool) KFAC_CUDA_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
     g.ready = true;
@@ -1139,29 +1343,31 @@ kfac_status inv_run(const InvMatrix *mats, int nmats, const float *damp_dev, int
     std::lock_guard<std::mutex> lock(g.mu);
     if ((s = ensure_streams(g)) != KFAC_OK) return s;
     size_t events = 0;
-    for (const InvGroup &gr : p.groups) events += 2 * gr.rounds.size();
+    for (const InvGroup &gr : p.groups) events += 2 * gr.rounds.size() + gr.tri.size();
     if (events > g.pool.size()) return KFAC_ERR_UNSUPPORTED;
     const int ngroups = (int)p.groups.size();
     KFAC_CUDA_TRY(cudaEventRecord(g.fork, st));
     for (int k = 0; k < ngroups; ++k) {
         KFAC_CUDA_TRY(cudaStreamWaitEvent(g.main[k], g.fork, 0));
         KFAC_CUDA_TRY(cudaStreamWaitEvent(g.side[k], g.fork, 0));
+        KFAC_CUDA_TRY(cudaStreamWaitEvent(g.tri[k], g.fork, 0));
     }
     kfac_status res[2] = {KFAC_OK, KFAC_OK};
     size_t ev = 0;
     for (int k = 0; k < ngroups; ++k) {
         const InvGroup &gr = p.groups[k];
-        cudaEvent_t *em = g.pool.data() + ev, *es = em + gr.rounds.size();
-        ev += 2 * gr.rounds.size();
+        cudaEvent_t *em = g.pool.data() + ev, *es = em + gr.rounds.size(), *et = es + gr.rounds.size();
+        ev += 2 * gr.rounds.size() + gr.tri.size();
         const PdlScope pdl(k == 0);  // early-launched CTAs of the low-priority group would hold SMs
-        res[k] = run_group(p, gr, g.main[k], g.side[k], k < SIDE_GROUPS, em, es);
+        res[k] = run_group(p, gr, g.main[k], g.side[k], g.tri[k], k < SIDE_GROUPS, em, es, et);
     }
     // join in every case, so that a capture or later work stays ordered
     for (int k = 0; k < ngroups; ++k) {
-        KFAC_CUDA_TRY(cudaEventRecord(g.done[2 * k], g.main[k]));
-        KFAC_CUDA_TRY(cudaEventRecord(g.done[2 * k + 1], g.side[k]));
-        KFAC_CUDA_TRY(cudaStreamWaitEvent(st, g.done[2 * k], 0));
-        KFAC_CUDA_TRY(cudaStreamWaitEvent(st, g.done[2 * k + 1], 0));
+        const cudaStream_t sts[3] = {g.main[k], g.side[k], g.tri[k]};
+        for (int q = 0; q < 3; ++q) {
+            KFAC_CUDA_TRY(cudaEventRecord(g.done[3 * k + q], sts[q]));
+            KFAC_CUDA_TRY(cudaStreamWaitEvent(st, g.done[3 * k + q], 0));
+        }
     }
     if (res[0] != KFAC_OK) return res[0];
     return res[1];

@@ -59,15 +59,23 @@ constexpr int GROUP = 8;              // row blocks per band of the grouped tile
 #endif
 // (both tuning constants may be set at build time)
 constexpr int TF32X3_MAX_SPLIT = KFAC_TF32X3_MAX_SPLIT;   // K splits of a tf32x3 tile (the last CTA sums the partials)
-// Planning choices for tf32x3 launches, as measured on the ResNet-50 step:
-// splitting long K ranges before narrowing tiles, and fewer K tiles per split,
-// both made the inversion slower; the grouped tile order made no difference.
+// Planning choices for tf32x3 launches, as measured on the ResNet-50 factor
+// set: splitting long K ranges before narrowing tiles is faster (7.34 ->
+// 7.08 ms; each split keeps 128-wide tiles, which read an A row panel once
+// per tile), fewer K tiles per split is slower, the grouped tile order makes
+// no difference.
 #ifndef KFAC_TF32X3_PREFER_SPLIT
-#define KFAC_TF32X3_PREFER_SPLIT false
+#define KFAC_TF32X3_PREFER_SPLIT true
 #endif
 constexpr bool TF32X3_PREFER_SPLIT = KFAC_TF32X3_PREFER_SPLIT;  // split long K ranges before narrowing tiles
 constexpr double TF32X3_MIN_KT = KFAC_TF32X3_MIN_KT;       // K tiles a tf32x3 split keeps at least
 constexpr bool TF32X3_GROUPED = false;       // grouped tile order for tf32x3 launches
+#ifndef KFAC_TF32X3_EARLY_RELEASE
+#define KFAC_TF32X3_EARLY_RELEASE 1
+#endif
+// tf32x3 epilogue: move an item's sum into the running-sum columns and
+// release its accumulator before the global stores (else after them)
+constexpr bool TF32X3_EARLY_RELEASE = KFAC_TF32X3_EARLY_RELEASE;
 constexpr int MAPS_PER_COPY = 240;
 constexpr int STAGE_LD = 36;                              // epilogue staging row pitch (floats)
 constexpr size_t EPI_STAGE_BYTES = 4 * 32 * STAGE_LD * sizeof(float);
@@ -877,11 +885,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 break;
             }
             tc_fence_after();
-            const uint32_t t_row = t_quarter + b * BN;
+            uint32_t t_row = t_quarter + b * BN;
             // a split with an empty K range (ktri tiles near the end) issued
             // no MMA: its accumulator holds nothing of this tile and counts as 0
             const bool empty = k.kt0 >= k.kt1;
-            const bool summed = nchunk > 1;
+            bool summed = nchunk > 1;
+            if (KIND == TC_KIND_TF32X3 && TF32X3_EARLY_RELEASE) {
+                // release the accumulator before the stores: the item's sum
+                // goes into the running-sum columns and is stored from there,
+                // so the next item's second chunk need not wait for the stores
+#pragma unroll 1
+                for (int c = 0; c < nch; ++c) {
+                    float v[32];
+                    if (summed) {
+                        float s2[32];
+                        tmem_ld_pair_32x32b_x32(t_row + c * 32, v, t_sum + c * 32, s2);
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) v[t] += s2[t];
+                    } else {
+                        tmem_ld_32x32b_x32(t_row + c * 32, v);
+                    }
+                    tmem_st_32x32b_x32(t_sum + c * 32, v);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&acce[b]);
+                t_row = t_sum;
+                summed = false;
+            }
             if (q.ksplit == 1) {
 #pragma unroll 1
                 for (int c = 0; c < nch; ++c) {
@@ -901,8 +932,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     }
                     nonfin |= chunk_store(q, i0, k.tn * q.bn + c * 32, v, stage, lane, mirror, diagblk, oh, ol);
                 }
-                tc_fence_before();
-                mbar_arrive(&acce[b]);
+                if (!(KIND == TC_KIND_TF32X3 && TF32X3_EARLY_RELEASE)) {
+                    tc_fence_before();
+                    mbar_arrive(&acce[b]);
+                }
             } else {
                 float4 *part = (float4 *)(q.partial + ((long long)k.tile * q.ksplit + k.split) * (BM * BN));
 #pragma unroll 1
@@ -924,8 +957,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                     for (int f = 0; f < 8; ++f)
                         part[(c * 8 + f) * BM + row] = make_float4(v[4 * f], v[4 * f + 1], v[4 * f + 2], v[4 * f + 3]);
                 }
-                tc_fence_before();
-                mbar_arrive(&acce[b]);
+                if (!(KIND == TC_KIND_TF32X3 && TF32X3_EARLY_RELEASE)) {
+                    tc_fence_before();
+                    mbar_arrive(&acce[b]);
+                }
                 __threadfence();
                 named_barrier_sync(1, 128);
                 if (etid == 0) {

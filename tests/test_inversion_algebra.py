@@ -10,11 +10,17 @@ restates, operation by operation and with the same buffer offsets:
   * the diag kernel, which turns the lower triangle of a 128 x 128 SPD
     block into L (blocked right-looking Cholesky by 16) and W = L^-1
     (blocked by rows of 16);
-  * the chain of one matrix: left-looking Cholesky block columns (update,
-    then the diag kernel, whose other CTAs form the panel below the block), the triangular inverse by recursive 2 x 2 blocking
-    bottom up by height (T = L21 W11, W21 = -W22 T), and the final product
-    Wt Wt^T over upper tiles with K from each tile's first column (ktri),
-    mirrored.
+  * the chain of one matrix: left-looking Cholesky block columns with
+    lookahead (the diag kernel, the first panel block and the last term of
+    the next diagonal update on the chain, the rest of each column and the
+    earlier terms of the diagonal update after it as side work), the
+    triangular inverse by recursive 2 x 2 blocking (T = L21 W11,
+    W21 = -W22 T), bottom up by height, and the final product Wt Wt^T over
+    upper tiles with K from each tile's first column (ktri), mirrored;
+  * the same chain as launches on three streams (chain, side work, and the
+    early triangular inverse whose nodes start once the Cholesky columns
+    they read are done), executed in random and adversarial orders that
+    keep only the dependencies the library declares.
 
 Every buffer region the library never writes is NaN here, so a product that
 reads one shows up as a NaN in the result; output tiles are 128 rows by 128,
@@ -85,6 +91,11 @@ def _tri_nodes(o, n, by_height):
     return ht
 
 
+def _dupd(c, j0, j1):
+    """D_c -= L[c, j0:j1] L[c, j0:j1]^T (block columns j0 .. j1 - 1)."""
+    return _job("L", c * NB, j0 * NB, "L", c * NB, j0 * NB, NB, NB, (j1 - j0) * NB, -1.0, 1.0, C=("D", c * NB, 0))
+
+
 def chain(dp):
     """Ops of one dp x dp matrix, in the library's order: ("leaf", k, side
     problems) for a diag kernel launch, ("gemm", problems, side problems) for
@@ -104,14 +115,13 @@ def chain(dp):
         if k + 1 == nb:
             break
         side = []
-        if k + 2 < nb:   # X[k+2:, k+1] -= L[k+2:, :k+1] L[k+1, :k+1]^T
+        if k + 2 < nb:   # X[k+2:, k+1] -= L[k+2:, :k+1] L[k+1, :k+1]^T, D_{k+2} -= L[k+2, :k+1] L[k+2, :k+1]^T
             side = [_job("L", kb + 2 * NB, 0, "L", kb + NB, 0, dp - kb - 2 * NB, NB, kb + NB, -1.0, 1.0,
-                         C=("X", kb + 2 * NB, kb + NB))]
+                         C=("X", kb + 2 * NB, kb + NB)), _dupd(k + 2, 0, k + 1)]
         ops.append(("gemm", [_job("X", kb + NB, kb, "X", kb, kb, NB, NB, NB, 1.0, 0.0, C=("L", kb + NB, kb))],
                     side))
-        # D_{k+1} -= L[k+1, :k+1] L[k+1, :k+1]^T
-        ops.append(("gemm", [_job("L", kb + NB, 0, "L", kb + NB, 0, NB, NB, kb + NB, -1.0, 1.0,
-                                  C=("D", kb + NB, 0))], []))
+        # D_{k+1} -= L[k+1, k] L[k+1, k]^T (the earlier terms ran with the side work above)
+        ops.append(("gemm", [_dupd(k + 1, k, k + 1)], []))
     by_height = []
     _tri_nodes(0, dp, by_height)
     for ht in range(1, len(by_height)):
@@ -217,3 +227,194 @@ def test_chain_launch_counts():
     and 2 per level of the triangular inverse."""
     for dp, expect in ((128, 1), (256, 2 + 2 * 1 + 2), (1152, 9 + 2 * 8 + 2 * 4), (4608, 36 + 2 * 35 + 2 * 6)):
         assert len(chain(dp)) == expect, dp
+
+
+# ---------------------------------------------------------------------------
+# The same chain as launches on three streams, ordered only by what the
+# library declares: each stream in order, a side launch after the op that
+# enables it, an op after the side launch it names, every early-inverse step
+# after the chain op it names, the final product after the last step.  Run in
+# random and adversarial orders that respect exactly those edges, a missing
+# edge shows up as a NaN read or a wrong inverse.
+
+EARLY_TRI_MIN_NB = 8
+
+
+def _t_job(o, n):
+    h = NB * (n // NB // 2)
+    return _job("L", o + h, o, "W", o, o, n - h, h, h, 1.0, 0.0, Ct=("L", o, o + h), ktri=True)
+
+
+def _x_job(o, n):
+    h = NB * (n // NB // 2)
+    m = n - h
+    return _job("X", o + h, o + h, "L", o, o + h, m, h, m, -1.0, 0.0, C=("X", o + h, o),
+                Ct=("W", o, o + h), ktril=True)
+
+
+def launch_graph(dp, early=True):
+    """[(stream, kind, payload, deps)] in enqueue order; deps index earlier
+    entries.  kind: "leaf" (payload: block offset) or "gemm" (payload: jobs)."""
+    nb = dp // NB
+    nodes, last = [], {}
+
+    def add(stream, kind, payload, deps=()):
+        d = set(deps)
+        if stream in last:
+            d.add(last[stream])
+        nodes.append((stream, kind, payload, sorted(d)))
+        last[stream] = len(nodes) - 1
+        return len(nodes) - 1
+
+    side_of, i_diag, i_first = {}, [None] * nb, [None] * nb
+
+    def main(kind, payload, side=None, needs=None):
+        i = add("main", kind, payload, [side_of[needs]] if needs is not None else [])
+        if side:
+            side_of[i] = add("side", "gemm", side, [i])
+        return i
+
+    last_side = None
+    for k in range(nb):
+        kb = k * NB
+        side = None
+        if k + 2 < nb:
+            side = [_job("X", kb + 2 * NB, kb, "X", kb, kb, dp - kb - 2 * NB, NB, NB, 1.0, 0.0,
+                         C=("L", kb + 2 * NB, kb))]
+        i_diag[k] = main("leaf", kb, side)
+        if side:
+            last_side = i_diag[k]
+        if k + 1 == nb:
+            break
+        side = None
+        if k + 2 < nb:
+            side = [_job("L", kb + 2 * NB, 0, "L", kb + NB, 0, dp - kb - 2 * NB, NB, kb + NB, -1.0, 1.0,
+                         C=("X", kb + 2 * NB, kb + NB)), _dupd(k + 2, 0, k + 1)]
+        i_first[k] = main("gemm", [_job("X", kb + NB, kb, "X", kb, kb, NB, NB, NB, 1.0, 0.0,
+                                        C=("L", kb + NB, kb))], side, i_first[k - 1] if k >= 1 else None)
+        if side:
+            last_side = i_first[k]
+        main("gemm", [_dupd(k + 1, k, k + 1)])
+    fin_deps = []
+    if early and nb >= EARLY_TRI_MIN_NB:
+        def visit(o, n):
+            if n == NB:
+                return
+            h = NB * (n // NB // 2)
+            visit(o, h)
+            add("tri", "gemm", [_t_job(o, n)], [i_first[min((o + h) // NB, nb - 2)]])
+            visit(o + h, n - h)
+            add("tri", "gemm", [_x_job(o, n)], [i_diag[(o + n) // NB - 1]])
+        visit(0, dp)
+        fin_deps = [last["tri"]]
+    else:
+        by_height = []
+        _tri_nodes(0, dp, by_height)
+        for ht in range(1, len(by_height)):
+            main("gemm", [_t_job(o, n) for o, n in by_height[ht]], None, last_side if ht == 1 else None)
+            main("gemm", [_x_job(o, n) for o, n in by_height[ht]])
+        if len(by_height) <= 1 and last_side is not None:
+            fin_deps = [side_of[last_side]]
+    add("main", "fin", None, fin_deps)
+    return nodes
+
+
+def _emulated_inverse(F, damp, order):
+    d = F.shape[0]
+    dp = -(-d // NB) * NB
+    X0 = np.eye(dp)
+    X0[:d, :d] = F + damp * np.eye(d)
+    buf = {k: np.full((dp, dp), np.nan) for k in ("X", "W", "L")}
+    buf["D"] = np.full((dp, NB), np.nan)
+    buf["X"][:] = np.tril(X0)
+    for b in range(0, dp, NB):
+        buf["D"][b:b + NB] = np.tril(X0)[b:b + NB, b:b + NB]
+    out = None
+    for kind, payload in order:
+        if kind == "leaf":
+            o = payload
+            W = diag_block(buf["D"][o:o + NB])[1]
+            buf["X"][o:o + NB, o:o + NB] = np.tril(W)
+            buf["W"][o:o + NB, o:o + NB] = np.triu(W.T)
+        elif kind == "gemm":
+            results = []
+            for j in payload:
+                A = buf[j["A"]][j["ar"]:j["ar"] + j["M"], j["ac"]:j["ac"] + j["K"]]
+                B = buf[j["B"]][j["br"]:j["br"] + j["N"], j["bc"]:j["bc"] + j["K"]]
+                acc = np.full((j["M"], j["N"]), np.nan)
+                for tm in range(0, j["M"], NB):
+                    for tn in range(0, j["N"], NB):
+                        k0 = tn if j["ktri"] else 0
+                        k1 = min(j["K"], tm + NB) if j["ktril"] else j["K"]
+                        acc[tm:tm + NB, tn:tn + NB] = A[tm:tm + NB, k0:k1] @ B[tn:tn + NB, k0:k1].T
+                results.append((j, acc))
+            for j, acc in results:
+                if j["C"]:
+                    b, r, c = j["C"]
+                    old = buf[b][r:r + j["M"], c:c + j["N"]]
+                    buf[b][r:r + j["M"], c:c + j["N"]] = j["alpha"] * acc + (j["beta"] * old if j["beta"] else 0.0)
+                if j["Ct"]:
+                    b, r, c = j["Ct"]
+                    buf[b][r:r + j["N"], c:c + j["M"]] = (j["alpha"] * acc).T
+        else:
+            Wt = buf["W"]
+            out = np.full((dp, dp), np.nan)
+            for tm in range(0, dp, NB):
+                for tn in range(tm, dp, NB):
+                    tile = Wt[tm:tm + NB, tn:] @ Wt[tn:tn + NB, tn:].T
+                    out[tm:tm + NB, tn:tn + NB] = tile
+                    out[tn:tn + NB, tm:tm + NB] = tile.T
+    return out[:d, :d]
+
+
+def _orders(nodes, policy, seed):
+    """A topological order of the launch graph: random, or the early-inverse
+    and side streams as early (or the main stream as late) as the edges allow."""
+    rng = np.random.default_rng(seed)
+    done, order, left = set(), [], list(range(len(nodes)))
+    rank = {"tri": 0, "side": 1, "main": 2}
+    while left:
+        ready = [i for i in left if all(d in done for d in nodes[i][3])]
+        if policy == "random":
+            i = ready[rng.integers(len(ready))]
+        elif policy == "helpers_first":
+            i = min(ready, key=lambda i: (rank[nodes[i][0]], i))
+        else:  # main first
+            i = min(ready, key=lambda i: (-rank[nodes[i][0]], i))
+        left.remove(i)
+        done.add(i)
+        order.append((nodes[i][1], nodes[i][2]))
+    return order
+
+
+@pytest.mark.parametrize("early", [False, True])
+@pytest.mark.parametrize("d", [1000, 1100, 1536])
+@pytest.mark.parametrize("policy", ["random", "helpers_first", "main_first"])
+def test_three_stream_schedule_respects_its_dependencies(d, policy, early):
+    """The library's default keeps the triangular inverse on the chain
+    (early=False: two streams); the early inverse is a build-time option."""
+    rng = np.random.default_rng(d)
+    Z = rng.standard_normal((d, d // 2))
+    F = Z @ Z.T / (d // 2)
+    damp = 0.05
+    nodes = launch_graph(-(-d // NB) * NB, early=early)
+    assert any(n[0] == "tri" for n in nodes) == early
+    for seed in range(2 if policy == "random" else 1):
+        inv = _emulated_inverse(F, damp, _orders(nodes, policy, seed))
+        assert np.isfinite(inv).all()
+        R = (F + damp * np.eye(d)) @ inv - np.eye(d)
+        assert np.abs(R).max() < 1e-8
+
+
+def test_early_inverse_graph_shape():
+    """Main-stream launches of a 4608-wide matrix with the early inverse: 36
+    diag launches, 35 first panel blocks, 35 last terms of the diagonal
+    updates and the final product; the inverse's 35 nodes are 70 launches on
+    the third stream."""
+    nodes = launch_graph(4608, early=True)
+    count = {}
+    for n in nodes:
+        count[n[0]] = count.get(n[0], 0) + 1
+    assert count == {"main": 36 + 35 + 35 + 1, "side": 34 + 34, "tri": 70}
+    # a matrix under the threshold keeps the inverse on its chain
+    assert not any(n[0] == "tri" for n in launch_graph(896, early=True))
