@@ -323,6 +323,34 @@ __device__ __forceinline__ void st16(float *dst, const float (&x)[DB]) {
     for (int q = 0; q < DB; q += 4) *reinterpret_cast<float4 *>(dst + q) = make_float4(x[q], x[q + 1], x[q + 2], x[q + 3]);
 }
 
+// ROWS x 128 floats of an fp32 (hi, lo) pair in global memory (row pitch ld),
+// summed into shared memory (row pitch sld): each thread issues up to eight
+// 16-byte loads of each plane before it stores, so a block costs a few L2
+// round trips rather than one per row group.
+template <int THREADS, int ROWS>
+__device__ __forceinline__ void stage_pair(float *dst, int sld, const float *hi, const float *lo, long long ld,
+                                           int tid) {
+    constexpr int N = ROWS * (NB / 4), PER = N / THREADS, BATCH = PER < 8 ? PER : 8;
+    static_assert(N % THREADS == 0 && PER % BATCH == 0, "whole batches");
+#pragma unroll
+    for (int b = 0; b < PER; b += BATCH) {
+        float4 h[BATCH], l[BATCH];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const int e = (b + u) * THREADS + tid;
+            const long long off = (long long)(e >> 5) * ld + (e & 31) * 4;
+            h[u] = __ldcg(reinterpret_cast<const float4 *>(hi + off));
+            l[u] = __ldcg(reinterpret_cast<const float4 *>(lo + off));
+        }
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const int e = (b + u) * THREADS + tid;
+            *reinterpret_cast<float4 *>(dst + (e >> 5) * sld + (e & 31) * 4) =
+                make_float4(h[u].x + l[u].x, h[u].y + l[u].y, h[u].z + l[u].z, h[u].w + l[u].w);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(DIAG_THREADS, 1) diag_kernel(const __grid_constant__ DiagParams P) {
     extern __shared__ float4 diag_smem4[];
     float *M = reinterpret_cast<float *>(diag_smem4);  // S, then L (lower triangle)
@@ -334,12 +362,7 @@ __global__ void __launch_bounds__(DIAG_THREADS, 1) diag_kernel(const __grid_cons
     if (tid == 0) *bad_s = NB;
     pdl_wait();
     pdl_trigger();
-    for (int e = tid; e < NB * NB / 4; e += DIAG_THREADS) {
-        const int i = e >> 5, j = (e & 31) * 4;
-        const float4 h = *reinterpret_cast<const float4 *>(J.Sh + i * NB + j);
-        const float4 l = *reinterpret_cast<const float4 *>(J.Sl + i * NB + j);
-        *reinterpret_cast<float4 *>(M + i * DLD + j) = make_float4(h.x + l.x, h.y + l.y, h.z + l.z, h.w + l.w);
-    }
+    stage_pair<DIAG_THREADS, NB>(M, DLD, J.Sh, J.Sl, NB, tid);
     __syncthreads();
 
     // 1. Cholesky
@@ -505,13 +528,7 @@ __global__ void __launch_bounds__(DIAG_THREADS, 1) diag_kernel(const __grid_cons
         // rows ti + 16 a (a < 8) and columns 8 tj .. 8 tj + 7; W is lower
         // triangular, so K stops at the block's last column (W's upper
         // entries inside a 16-block are the zeros written above)
-        for (int e = tid; e < NB * NB / 4; e += DIAG_THREADS) {
-            const int i = e >> 5, j = (e & 31) * 4;
-            const long long off = (long long)i * J.ld + j;
-            const float4 h = *reinterpret_cast<const float4 *>(J.Ph + off);
-            const float4 l = *reinterpret_cast<const float4 *>(J.Pl + off);
-            *reinterpret_cast<float4 *>(M + i * DLD + j) = make_float4(h.x + l.x, h.y + l.y, h.z + l.z, h.w + l.w);
-        }
+        stage_pair<DIAG_THREADS, NB>(M, DLD, J.Ph, J.Pl, J.ld, tid);
         __syncthreads();
         const int ti = tid & 15, tj = tid >> 4;
         float acc[8][8];
@@ -586,7 +603,7 @@ __global__ void __launch_bounds__(DIAG_THREADS, 1) diag_kernel(const __grid_cons
 // One launch unit of a matrix's chain: a diag leaf, or engine problems that
 // go into the same launch.
 struct Op {
-    int leaf;
+    int leaf;                 // launch kind: 0 engine, 1 diag kernel
     std::vector<DiagJob> dj;  // leaf: the owner of the diagonal block, then its panel blocks
     std::vector<TcJob> g;
     std::vector<TcJob> side;  // engine problems that may start once this op is done (lookahead,
@@ -889,7 +906,7 @@ std::vector<std::vector<std::pair<int, int>>> schedule_rounds(const std::vector<
     rounds.clear();
     round_kind.clear();
     for (size_t r = 0; r < longest; ++r)
-        for (int kind = 1; kind >= 0; --kind) {
+        for (int kind : {1, 0}) {
             std::vector<std::pair<int, int>> v;
             for (int k : members)
                 if (r < chains[k].size() && chains[k][r].leaf == kind) v.push_back({k, (int)r});
@@ -1045,7 +1062,7 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
             round.clear();
             for (const auto &ki : g.rounds[r]) {
                 const Op &op = p.chains[ki.first][ki.second];
-                if (!op.leaf) round.insert(round.end(), op.g.begin(), op.g.end());
+                if (op.leaf == 0) round.insert(round.end(), op.g.begin(), op.g.end());
                 g.side[r].insert(g.side[r].end(), op.side.begin(), op.side.end());
                 if (op.needs_side >= 0) {
                     const int src = round_of[ki.first][op.needs_side];
@@ -1238,7 +1255,7 @@ kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st, cuda
         gemms.clear();
         for (const auto &ki : g.rounds[r]) {
             const Op &op = p.chains[ki.first][ki.second];
-            if (op.leaf) leaves.insert(leaves.end(), op.dj.begin(), op.dj.end());
+            if (op.leaf == 1) leaves.insert(leaves.end(), op.dj.begin(), op.dj.end());
             else gemms.insert(gemms.end(), op.g.begin(), op.g.end());
         }
         if (!leaves.empty() && (s = diag_launch(leaves, st)) != KFAC_OK) return s;

@@ -223,8 +223,8 @@ def test_chain_inverts_and_reads_only_written_regions(d, bn):
 
 def test_chain_launch_counts():
     """Ops on the chain of one matrix: the diag launch of every 128-wide block
-    column, the first panel block and the next diagonal update between them,
-    and 2 per level of the triangular inverse."""
+    column, the first panel block and the last term of the next diagonal
+    update between them, and 2 per level of the triangular inverse."""
     for dp, expect in ((128, 1), (256, 2 + 2 * 1 + 2), (1152, 9 + 2 * 8 + 2 * 4), (4608, 36 + 2 * 35 + 2 * 6)):
         assert len(chain(dp)) == expect, dp
 
