@@ -124,10 +124,11 @@ int kfac_timing_enable(int on);
 int kfac_timing_read(double *ms, long long *launches, int n);
 const char *kfac_timing_kind_name(int k);
 /* The same record launch by launch, in enqueue order: for the first n launches
- * the start (ms after the first recorded launch's start), the duration (ms) and
- * the kernel kind; clears the record and returns the number of launches it
- * held (-1 if an event query failed). */
-int kfac_timing_read_launches(double *start_ms, double *dur_ms, int *kind, int n);
+ * the start (ms after the first recorded launch's start), the duration (ms),
+ * the kernel kind and the launch stream's handle (a value that tells streams
+ * apart, nothing more); any output may be NULL.  Clears the record and
+ * returns the number of launches it held (-1 if an event query failed). */
+int kfac_timing_read_launches(double *start_ms, double *dur_ms, int *kind, unsigned long long *stream, int n);
 
 /* ======================================================================
  * kfac_factor_update -- Kronecker factor statistic + running average.

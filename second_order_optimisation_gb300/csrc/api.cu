@@ -31,6 +31,7 @@ constexpr int TIMING_MAX = 65536;
 struct TimingRec {
     int kind;
     cudaEvent_t start, stop;
+    unsigned long long stream;  // the launch stream's handle (identifies the stream, nothing more)
 };
 std::mutex g_tmu;
 bool g_timing = false;
@@ -42,7 +43,7 @@ int timing_begin(int kind, cudaStream_t st) {
     if (!g_timing) return -1;
     std::lock_guard<std::mutex> lock(g_tmu);
     if (!g_timing || (int)g_recs.size() >= TIMING_MAX) return -1;
-    TimingRec r{kind, nullptr, nullptr};
+    TimingRec r{kind, nullptr, nullptr, (unsigned long long)(uintptr_t)st};
     if (!g_free.empty()) {
         r.start = g_free.back().start;
         r.stop = g_free.back().stop;
@@ -333,7 +334,8 @@ extern "C" int kfac_timing_read(double *ms, long long *launches, int n) {
     return status;
 }
 
-extern "C" int kfac_timing_read_launches(double *start_ms, double *dur_ms, int *kind, int n) {
+extern "C" int kfac_timing_read_launches(double *start_ms, double *dur_ms, int *kind, unsigned long long *stream,
+                                         int n) {
     std::lock_guard<std::mutex> lock(g_tmu);
     int count = 0;
     bool failed = false;
@@ -346,6 +348,7 @@ extern "C" int kfac_timing_read_launches(double *start_ms, double *dur_ms, int *
             if (start_ms) start_ms[count] = t0;
             if (dur_ms) dur_ms[count] = t;
             if (kind) kind[count] = r.kind;
+            if (stream) stream[count] = r.stream;
         }
         ++count;
         g_free.push_back(r);

@@ -104,7 +104,7 @@ def load() -> ctypes.CDLL:
         lib.kfac_timing_enable.restype = i32
         lib.kfac_timing_read.argtypes = [vp, vp, i32]
         lib.kfac_timing_read.restype = i32
-        lib.kfac_timing_read_launches.argtypes = [vp, vp, vp, i32]
+        lib.kfac_timing_read_launches.argtypes = [vp, vp, vp, vp, i32]
         lib.kfac_timing_read_launches.restype = i32
         lib.kfac_timing_kind_name.argtypes = [i32]
         lib.kfac_timing_kind_name.restype = ctypes.c_char_p
@@ -153,16 +153,20 @@ def timing_read() -> dict:
 
 
 def timing_read_launches(n: int = 65536) -> list:
-    """[(start ms, duration ms, kernel kind name)] of every recorded launch in
-    enqueue order, since the last read (synchronises)."""
+    """[(start ms, duration ms, kernel kind name, stream id)] of every recorded
+    launch in enqueue order, since the last read (synchronises); stream ids
+    number the launch streams 0, 1, ... in order of first appearance."""
     lib = load()
     st = (ctypes.c_double * n)()
     du = (ctypes.c_double * n)()
     kd = (ctypes.c_int * n)()
-    cnt = lib.kfac_timing_read_launches(st, du, kd, n)
+    sm = (ctypes.c_ulonglong * n)()
+    cnt = lib.kfac_timing_read_launches(st, du, kd, sm, n)
     if cnt < 0:
         raise KfacError(KFAC_ERR_CUDA, "kfac_timing_read_launches")
-    return [(st[i], du[i], lib.kfac_timing_kind_name(kd[i]).decode()) for i in range(min(cnt, n))]
+    ids = {}
+    return [(st[i], du[i], lib.kfac_timing_kind_name(kd[i]).decode(), ids.setdefault(sm[i], len(ids)))
+            for i in range(min(cnt, n))]
 
 
 def status_string(status: int) -> str:

@@ -470,6 +470,7 @@ def test_timing_records_every_launch():
     rec = kfac.timing_read_launches()
     kfac.timing_enable(False)
     assert len(rec) == n1 - n0 > 0
-    assert all(d >= 0.0 for _, d, _ in rec) and rec[0][0] == 0.0
-    assert "tc_gemm_bf16" in {k for _, _, k in rec}
+    assert all(d >= 0.0 for _, d, _, _ in rec) and rec[0][0] == 0.0
+    assert "tc_gemm_bf16" in {k for _, _, k, _ in rec}
+    assert {sid for _, _, _, sid in rec} == {0}  # all on the caller's stream
     assert kfac.timing_read_launches() == []
