@@ -114,6 +114,7 @@ struct TcProb {
     uint8_t vec;             // C (and C_lo) rows take 16-byte accesses (ldc % 4 == 0, aligned)
     uint8_t vecb;            // Cb rows take 8-byte accesses
     uint8_t vecw;            // W rows take 16-byte accesses
+    uint8_t vect;            // Ct (and Ct_lo) rows take 16-byte accesses
     uint8_t im2col, im_k, im_stride, im_pad;  // operands through an im2col map (see TcJob)
     uint8_t f16, cb_f16;     // fp16 operands / fp16 copy Cb (else bf16)
     uint8_t packed;          // ACCUM: C packed upper triangle of order packed_d
@@ -479,7 +480,27 @@ __device__ __forceinline__ bool chunk_store(const TcProb &q, int i0, int j0, con
                                             int lane, bool mirror, bool diagblk, float4 (&oh)[8], float4 (&ol)[8]) {
     const float a = q.alpha, b = q.beta;
     bool bad = false;
-    if (q.epi == TC_EPI_SPLIT && q.Ct) {  // host guarantees beta == 0 here
+    // transposed stores of a whole chunk: the chunk goes through the stage
+    // column by column (stage row c = output row j0 + c), so that lane l then
+    // holds 4 consecutive outputs of row j0 + 4k + l/8 and every store is
+    // 16 bytes (8 B for 16-bit outputs) in rows of 128 consecutive bytes
+    const bool whole = i0 + 32 <= q.M && j0 + 32 <= q.N;
+    const int tr = lane >> 3, tc = 4 * (lane & 7);
+    if (q.epi == TC_EPI_SPLIT && q.Ct && whole && q.vect) {  // host guarantees beta == 0 here
+#pragma unroll
+        for (int c = 0; c < 32; ++c) stage[c * STAGE_LD + lane] = a * v[c];
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int r = 4 * k + tr;
+            const float4 o = *reinterpret_cast<const float4 *>(&stage[r * STAGE_LD + tc]);
+            const float4 h = tf32_hi4(o);
+            const long long off = (long long)(j0 + r) * q.ldct + i0 + tc;
+            st4(q.Ct + off, h);
+            st4(q.Ct_lo + off, sub4(o, h));
+        }
+        __syncwarp();
+    } else if (q.epi == TC_EPI_SPLIT && q.Ct) {
         const int i = i0 + lane;
         if (i < q.M) {
 #pragma unroll
@@ -574,7 +595,28 @@ __device__ __forceinline__ bool chunk_store(const TcProb &q, int i0, int j0, con
                 }
             }
         }
-        if (mirror || up) {
+        // a chunk of a diagonal block entirely above its diagonal mirrors
+        // whole, one entirely below mirrors nothing, one on it goes entry by
+        // entry (only j > i)
+        const bool above = mirror || (up && j0 >= i0 + 32);
+        if (above && whole && (!q.C || q.vec) && (!q.Cb || q.vecb)) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) stage[c * STAGE_LD + lane] = a * v[c];
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int r = 4 * k + tr;
+                const float4 o = *reinterpret_cast<const float4 *>(&stage[r * STAGE_LD + tc]);
+                if (q.C) st4(q.C + (long long)(j0 + r) * q.ldc + i0 + tc, o);
+                if (q.Cb) {
+                    const bool h16 = q.cb_f16;
+                    const uint32_t lo2 = f32_to_16_bits(o.x, h16) | ((uint32_t)f32_to_16_bits(o.y, h16) << 16);
+                    const uint32_t hi2 = f32_to_16_bits(o.z, h16) | ((uint32_t)f32_to_16_bits(o.w, h16) << 16);
+                    *reinterpret_cast<uint2 *>(q.Cb + (long long)(j0 + r) * q.ldcb + i0 + tc) = make_uint2(lo2, hi2);
+                }
+            }
+            __syncwarp();
+        } else if ((mirror || up) && !(up && j0 + 32 <= i0)) {
             // symmetric output: the transposed position C[j][i0 .. i0+31],
             // straight from the TMEM layout (lane = row i0 + lane), so every
             // store instruction covers one contiguous row segment
@@ -1269,6 +1311,7 @@ kfac_status tc_run(const TcJob *jobs, int njobs, int kind, const CUtensorMap *de
             q.packed = j.packed ? 1 : 0;
             q.packed_d = j.packed_d;
             q.vecw = (j.ldw % 4 == 0) && ((uintptr_t)j.W % 16 == 0);
+            q.vect = (j.ldct % 4 == 0) && ((uintptr_t)j.Ct % 16 == 0) && ((uintptr_t)j.Ct_lo % 16 == 0);
             q.im2col = j.im2col ? 1 : 0;
             q.im_k = (uint8_t)j.im_k; q.im_stride = (uint8_t)j.im_stride; q.im_pad = (uint8_t)j.im_pad;
             q.im_c = j.im_c; q.im_wo = j.im_wo; q.im_howo = j.im_howo;
