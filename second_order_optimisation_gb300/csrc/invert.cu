@@ -365,13 +365,30 @@ __global__ void __launch_bounds__(DIAG_THREADS, 1) diag_kernel(const __grid_cons
     stage_pair<DIAG_THREADS, NB>(M, DLD, J.Sh, J.Sl, NB, tid);
     __syncthreads();
 
-    // 1. Cholesky
+    // 1. Cholesky, for each 16-wide block column c, with the trailing update
+    //    of the previous block column split: warp 0 applies it to block c's
+    //    diagonal block and factors that block while warps 1..7 apply it to
+    //    everything else past c; then the panel below block c
 #pragma unroll 1
     for (int c = 0; c < NB; c += DB) {
         if (warp == 0) {
             const int r = lane & (DB - 1);  // lanes 16..31 repeat rows 0..15 (only 0..15 store)
             float a[DB];
             ld16(M + (c + r) * DLD + c, a);
+            if (c > 0) {
+                // S_rj -= L[c+r][c-16 ..] . L[c+j][c-16 ..]  (the previous panel)
+                float lr[DB];
+                ld16(M + (c + r) * DLD + c - DB, lr);
+#pragma unroll
+                for (int j = 0; j < DB; ++j) {
+                    float lj[DB];
+                    ld16(M + (c + j) * DLD + c - DB, lj);
+                    float x = a[j];
+#pragma unroll
+                    for (int t = 0; t < DB; ++t) x = fmaf(-lr[t], lj[t], x);
+                    a[j] = x;
+                }
+            }
             float wr = 0.f;
             int bad = -1;
 #pragma unroll
@@ -399,6 +416,55 @@ __global__ void __launch_bounds__(DIAG_THREADS, 1) diag_kernel(const __grid_cons
                 invd[c + r] = wr;
             }
             if (lane == 0 && bad >= 0) atomicMin(bad_s, c + bad);
+        } else if (c > 0) {
+            // the previous panel's update of the lower triangle past c, 4 x 4
+            // tiles (I, Jt), without the 10 tiles of block c's diagonal block
+            const int p = c - DB;
+            const int nT = (NB - c) / 4;
+            const int ntiles = nT * (nT + 1) / 2;
+            for (int t = tid - 32 + 10; t < ntiles; t += DIAG_THREADS - 32) {
+                int I = (int)((sqrtf(8.f * (float)t + 1.f) - 1.f) * 0.5f);
+                while (I * (I + 1) / 2 > t) --I;
+                while ((I + 1) * (I + 2) / 2 <= t) ++I;
+                const int Jt = t - I * (I + 1) / 2;
+                const int i0 = c + 4 * I, j0 = c + 4 * Jt;
+                float acc[4][4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 v = *reinterpret_cast<const float4 *>(M + (i0 + u) * DLD + j0);
+                    acc[u][0] = v.x; acc[u][1] = v.y; acc[u][2] = v.z; acc[u][3] = v.w;
+                }
+#pragma unroll
+                for (int q = 0; q < DB; q += 4) {
+                    float4 li[4], lj[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        li[u] = *reinterpret_cast<const float4 *>(M + (i0 + u) * DLD + p + q);
+                        lj[u] = *reinterpret_cast<const float4 *>(M + (j0 + u) * DLD + p + q);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            float x = acc[u][v];
+                            x = fmaf(-li[u].x, lj[v].x, x);
+                            x = fmaf(-li[u].y, lj[v].y, x);
+                            x = fmaf(-li[u].z, lj[v].z, x);
+                            acc[u][v] = fmaf(-li[u].w, lj[v].w, x);
+                        }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (I != Jt) {
+                        *reinterpret_cast<float4 *>(M + (i0 + u) * DLD + j0) =
+                            make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            if (v <= u) M[(i0 + u) * DLD + j0 + v] = acc[u][v];
+                    }
+                }
+            }
         }
         __syncthreads();
         const int nrest = NB - c - DB;
@@ -413,53 +479,6 @@ __global__ void __launch_bounds__(DIAG_THREADS, 1) diag_kernel(const __grid_cons
                 for (int j = q + 1; j < DB; ++j) x[j] = fmaf(-x[q], M[(c + j) * DLD + c + q], x[j]);
             }
             st16(M + i * DLD + c, x);
-        }
-        __syncthreads();
-        // the trailing update, 4 x 4 tiles (I, Jt) of the lower triangle past c
-        const int nT = nrest / 4;
-        const int ntiles = nT * (nT + 1) / 2;
-        for (int t = tid; t < ntiles; t += DIAG_THREADS) {
-            int I = (int)((sqrtf(8.f * (float)t + 1.f) - 1.f) * 0.5f);
-            while (I * (I + 1) / 2 > t) --I;
-            while ((I + 1) * (I + 2) / 2 <= t) ++I;
-            const int Jt = t - I * (I + 1) / 2;
-            const int i0 = c + DB + 4 * I, j0 = c + DB + 4 * Jt;
-            float acc[4][4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float4 v = *reinterpret_cast<const float4 *>(M + (i0 + u) * DLD + j0);
-                acc[u][0] = v.x; acc[u][1] = v.y; acc[u][2] = v.z; acc[u][3] = v.w;
-            }
-#pragma unroll
-            for (int q = 0; q < DB; q += 4) {
-                float4 li[4], lj[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    li[u] = *reinterpret_cast<const float4 *>(M + (i0 + u) * DLD + c + q);
-                    lj[u] = *reinterpret_cast<const float4 *>(M + (j0 + u) * DLD + c + q);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        float x = acc[u][v];
-                        x = fmaf(-li[u].x, lj[v].x, x);
-                        x = fmaf(-li[u].y, lj[v].y, x);
-                        x = fmaf(-li[u].z, lj[v].z, x);
-                        acc[u][v] = fmaf(-li[u].w, lj[v].w, x);
-                    }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (I != Jt) {
-                    *reinterpret_cast<float4 *>(M + (i0 + u) * DLD + j0) =
-                        make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
-                } else {
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        if (v <= u) M[(i0 + u) * DLD + j0 + v] = acc[u][v];
-                }
-            }
         }
         __syncthreads();
     }
