@@ -137,9 +137,12 @@ def kernel_work(layers, batch, fl, pk, sm_mhz):
             ("factors", "im2col"): (im2col_bytes, "hbm", pk["hbm"], "GB/s", "HBM copy (measured)")}
 
 
-def kernel_rooflines(kern, work, steps):
+def kernel_rooflines(kern, work, steps, traffic=None):
     """Per-kernel achieved rate from the library's per-launch event timings
-    (eager run, each launch bracketed by events on its own stream)."""
+    (eager run, each launch bracketed by events on its own stream); DRAM
+    traffic per launch from `traffic` (the ResNet-50 step's ncu capture by
+    default; other workloads have none)."""
+    traffic = NCU_TRAFFIC if traffic is None else traffic
     out = {}
     for ph, ks in kern.items():
         for name, (t, n) in ks.items():
@@ -149,11 +152,11 @@ def kernel_rooflines(kern, work, steps):
                 w, bound, peak, unit, psrc = work[(ph, name)]
                 scale = 1e12 if unit == "TFLOP/s" else 1e9
                 ach = w / (ms_step * 1e-3) / scale if ms_step > 0 else 0.0
-                tr = NCU_TRAFFIC.get(f"{name}@{ph}")
+                tr = traffic.get(f"{name}@{ph}")
                 rec.update({"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
                             "peak_source": psrc, "work_per_step": w,
                             "traffic": tr[0] if tr else None,
-                            "traffic_source": tr[1] if tr else "no ncu capture of this build"})
+                            "traffic_source": tr[1] if tr else "no ncu capture of this build and workload"})
             out[f"{name}@{ph}"] = rec
     return out
 
@@ -538,7 +541,7 @@ def subrecord(name, steps, warmup, dev, pk, sm_mhz):
     m = measure(name, steps, warmup, dev, pk)
     ms = time_replays([m["graphs"]["step"]], steps, warmup, m["stream"])
     fl = flops(m["layers"], m["batch"])
-    ks = kernel_rooflines(m["kern"], kernel_work(m["layers"], m["batch"], fl, pk, sm_mhz), steps)
+    ks = kernel_rooflines(m["kern"], kernel_work(m["layers"], m["batch"], fl, pk, sm_mhz), steps, traffic={})
     keep = ("tc_gemm_bf16@factors", "tc_gemm_bf16@precond", "tc_gemm_tf32x3@inverse", "inv_diag@inverse")
     return {"workload": f"{name}_kfac_step", "ms": ms, "tflops": fl["total"] / (ms * 1e-3) / 1e12,
             "phases_ms": m["phases"], "gpu_launches_per_step": m["launches"],
