@@ -236,6 +236,7 @@ kfac_status plan_factor(const kfac_factor_desc *descs, int count, const std::vec
             j.im_wo = g.wo; j.im_howo = g.ho * g.wo;
             j.f16 = f16;
             j.packed = packed; j.packed_d = g.d;
+            j.dyn = 1;  // problems of very different sizes: hand the work items out dynamically
             p.tc.push_back(j);
             continue;
         }
@@ -264,6 +265,7 @@ kfac_status plan_factor(const kfac_factor_desc *descs, int count, const std::vec
         j.C = d.F; j.ldc = d.ldf;
         j.f16 = f16;
         j.packed = packed; j.packed_d = g.d;
+        j.dyn = 1;  // problems of very different sizes: hand the work items out dynamically
         p.tc.push_back(j);
         if (d.append_one) {
             // bias row/column: needs the source rows [M][c]; an FC layer has

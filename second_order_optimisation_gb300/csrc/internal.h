@@ -50,6 +50,7 @@ struct TcJob {
     int no_split;
     int fine_split; // a latency-critical job: split its K range into pieces of about 12 K tiles
                     // (up to 16 pieces) whatever the rest of the launch
+    int dyn;        // the launch hands out its work items dynamically (any job asks for it)
     int epi;
     float alpha, beta;
     float *C;
