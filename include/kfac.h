@@ -119,7 +119,8 @@ long long kfac_launch_count(void);
  * milliseconds (ms[k]) and the number of launches (launches[k]), and clears
  * the record; it returns KFAC_OK or KFAC_ERR_CUDA.  kfac_timing_enable
  * returns the previous setting.  Kind names: kfac_timing_kind_name(k) ("" past
- * the last kind).  Do not enable it while a stream is being captured. */
+ * the last kind).  Launches enqueued during stream capture are recorded as
+ * external event nodes of the graph: read the record after the graph has run. */
 int kfac_timing_enable(int on);
 int kfac_timing_read(double *ms, long long *launches, int n);
 const char *kfac_timing_kind_name(int k);

@@ -39,6 +39,18 @@ std::vector<TimingRec> g_recs;      // in use
 std::vector<TimingRec> g_free;      // recycled event pairs
 }  // namespace
 
+namespace {
+// An event record on `st`; during stream capture an external event node of
+// the graph, which records the event each time the graph runs.
+void timing_record(cudaEvent_t e, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+    else
+        cudaEventRecord(e, st);
+}
+}  // namespace
+
 int timing_begin(int kind, cudaStream_t st) {
     if (!g_timing) return -1;
     std::lock_guard<std::mutex> lock(g_tmu);
@@ -51,7 +63,7 @@ int timing_begin(int kind, cudaStream_t st) {
     } else if (cudaEventCreate(&r.start) != cudaSuccess || cudaEventCreate(&r.stop) != cudaSuccess) {
         return -1;
     }
-    cudaEventRecord(r.start, st);
+    timing_record(r.start, st);
     g_recs.push_back(r);
     return (int)g_recs.size() - 1;
 }
@@ -59,7 +71,7 @@ int timing_begin(int kind, cudaStream_t st) {
 void timing_end(int slot, cudaStream_t st) {
     if (slot < 0) return;
     std::lock_guard<std::mutex> lock(g_tmu);
-    if (slot < (int)g_recs.size()) cudaEventRecord(g_recs[slot].stop, st);
+    if (slot < (int)g_recs.size()) timing_record(g_recs[slot].stop, st);
 }
 
 namespace {
