@@ -51,6 +51,9 @@ constexpr int GROUP = 8;              // row blocks per band of the grouped tile
 #ifndef KFAC_TF32X3_CHUNK
 #define KFAC_TF32X3_CHUNK 8
 #endif
+#ifndef KFAC_TF32X3_NACC
+#define KFAC_TF32X3_NACC 3  // tf32x3 chunk accumulators in TMEM (2 or 3; the running sum follows them)
+#endif
 #ifndef KFAC_TF32X3_MAX_SPLIT
 #define KFAC_TF32X3_MAX_SPLIT 6
 #endif
@@ -99,17 +102,19 @@ template <> struct Traits<TC_KIND_BF16> {
     // with 8 KB ones (the per-SM rate of box loads is the limit).  One
     // accumulation per work item.
     static constexpr int BK = 128, STAGES = 3, TILES = 2, ESZ = 2, TILE = 128 * 128 * 2;
-    static constexpr int CHUNK = 1 << 30, TMEM_COLS = TMEM_ACC;
+    static constexpr int CHUNK = 1 << 30, TMEM_COLS = TMEM_ACC, NACC = 2;
 };
 template <> struct Traits<TC_KIND_TF32X3> {
     // A work item accumulates its K range in chunks of CHUNK K tiles (256 K),
-    // alternating between the two TMEM accumulators; the epilogue warps add
-    // each chunk into a running sum held in TMEM (columns 2 BN ..) with fp32
-    // round-to-nearest additions.  Long sums accumulated within one tensor-core
+    // rotating over NACC TMEM accumulators (three: the MMA warp can run two
+    // chunks ahead of the epilogue while it stores an item); the epilogue
+    // warps add each chunk into a running sum held in TMEM (columns NACC BN ..)
+    // with fp32 round-to-nearest additions.  Long sums accumulated within one tensor-core
     // accumulator lose accuracy faster than that (the Cholesky updates of the
     // inversion run over K up to the factor's width).
     static constexpr int BK = 32, STAGES = 3, TILES = 4, ESZ = 4, TILE = TILE_BYTES;
-    static constexpr int CHUNK = KFAC_TF32X3_CHUNK, TMEM_COLS = 512;
+    static constexpr int CHUNK = KFAC_TF32X3_CHUNK, TMEM_COLS = 512, NACC = KFAC_TF32X3_NACC;
+    static_assert((NACC + 1) * BN <= TMEM_COLS, "accumulators and the running sum fit in TMEM");
 };
 
 struct TcProb {
@@ -703,8 +708,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     uint64_t *full = (uint64_t *)(smem + Tr::STAGES * STAGE_BYTES);
     uint64_t *empty = full + Tr::STAGES;
     uint64_t *accf = empty + Tr::STAGES;
-    uint64_t *acce = accf + 2;
-    uint64_t *drain = acce + 2;  // completion of this CTA's products after an abort
+    uint64_t *acce = accf + Tr::NACC;
+    uint64_t *drain = acce + Tr::NACC;  // completion of this CTA's products after an abort
     uint64_t *item_full = drain + 1;        // [RING] an item index is in the ring slot
     uint64_t *item_empty = item_full + RING;  // [RING] the MMA thread and the epilogue have read it
     volatile int *ring = (volatile int *)(item_empty + RING);
@@ -759,7 +764,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < Tr::NACC; ++b) {
             mbar_init(&accf[b], 1);
             mbar_init(&acce[b], 128);
         }
@@ -859,7 +864,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            int cc = 0;  // accumulation chunks so far (accumulator cc & 1)
+            int cc = 0;  // accumulation chunks so far (accumulator cc % NACC)
             bool ok = true;
             for (int r = 0;; ++r) {
                 const int w = take(r);
@@ -871,8 +876,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                                                             : idesc_tf32_f32(BM, q.bn);
                 const int nchunk = max(1, (int)ceil_div_dev(k.kt1 - k.kt0, Tr::CHUNK));
                 for (int ch = 0; ch < nchunk && ok; ++ch, ++cc) {
-                    const int b = cc & 1;
-                    const uint32_t use = (uint32_t)(cc >> 1);
+                    const int b = cc % Tr::NACC;
+                    const uint32_t use = (uint32_t)(cc / Tr::NACC);
                     if (!mbar_wait(&acce[b], (use & 1) ^ 1)) {
                         atomicOr(P.error, ERR_TIMEOUT_ACC);
                         *abort_flag = 1;
@@ -930,7 +935,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         const int etid = threadIdx.x - 64;  // 0..127
         float *stage = epi_stage + (warp - 2) * 32 * STAGE_LD;
         const uint32_t t_quarter = tmem_base + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t t_sum = t_quarter + 2 * BN;  // running sum of a chunked item (tf32x3)
+        const uint32_t t_sum = t_quarter + Tr::NACC * BN;  // running sum of a chunked item (tf32x3)
         int cc = 0;
         bool nonfin = false;  // a value this lane stored was NaN or infinite
         for (int r = 0;; ++r) {
@@ -946,8 +951,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             // all chunks but the last: add into the running sum
             bool ok = true;
             for (int ch = 0; ch + 1 < nchunk; ++ch, ++cc) {
-                const int b = cc & 1;
-                if (!mbar_wait(&accf[b], (uint32_t)(cc >> 1) & 1)) {
+                const int b = cc % Tr::NACC;
+                if (!mbar_wait(&accf[b], (uint32_t)(cc / Tr::NACC) & 1)) {
                     ok = false;
                     break;
                 }
@@ -974,8 +979,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 *abort_flag = 1;
                 break;
             }
-            const int b = cc & 1;
-            const uint32_t use = (uint32_t)(cc >> 1);
+            const int b = cc % Tr::NACC;
+            const uint32_t use = (uint32_t)(cc / Tr::NACC);
             ++cc;
             float4 oh[8], ol[8];
             // the first column chunk's old values load while the MMAs run
