@@ -57,7 +57,6 @@ _TRAFFIC_SRC = "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch (ser
 NCU_TRAFFIC = {
     "tc_gemm_tf32x3@inverse": (47.30e6, _TRAFFIC_SRC),
     "inv_diag@inverse": (1.66e6, _TRAFFIC_SRC),
-    "inv_prep@inverse": (1578.8e6, _TRAFFIC_SRC),
     "im2col@factors": (69.5e6, _TRAFFIC_SRC),
     "tc_gemm_bf16@factors": (2010.7e6, _TRAFFIC_SRC),
     "tc_gemm_bf16@precond": ((330.2e6 + 152.5e6) / 2, _TRAFFIC_SRC),
@@ -114,7 +113,8 @@ def kernel_work(layers, batch, fl, pk, sm_mhz):
       tc_gemm_tf32x3 (inverse) d^3 - diag blocks' share per factor        tensor, 3 tf32 products
       inv_diag (inverse)       2/3 * 128^3 per 128 x 128 diagonal block   fp32 CUDA cores (alu)
       inv_prep (inverse)       upper triangle of F read (4 B) + the (hi, lo) working pair
-                               written (dp^2 x 8 B)                       HBM
+                               written below the diagonal 128-blocks and  HBM
+                               the diagonal blocks (8 B)
       im2col (factors)         materialised patch bytes written + input read   HBM"""
     tf32x3_peak = pk["bf16"] * (1.1 / 2.25) / 3.0
     # fp32 FMA rate: 152 SMs x 128 lanes x 2 FLOP per cycle at the SM clock
@@ -126,7 +126,8 @@ def kernel_work(layers, batch, fl, pk, sm_mhz):
             im2col_bytes += L.rows(batch) * L.k * L.k * L.cin * 2 + batch * L.hin * L.hin * L.cin * 2
     pad = lambda d: (d + NB - 1) // NB * NB
     dims = [L.d_a for L in layers] + [L.d_g for L in layers]
-    prep_bytes = sum(d * (d + 1) // 2 * 4 + pad(d) ** 2 * 8 for d in dims)
+    prep_bytes = sum(d * (d + 1) // 2 * 4 + (pad(d) // NB) * (pad(d) // NB - 1) // 2 * NB * NB * 8
+                     + pad(d) * NB * 8 for d in dims)
     return {("factors", "tc_gemm_bf16"): (fl["syrk"], "tensor", pk["bf16"], "TFLOP/s", "bf16 burst (measured)"),
             ("precond", "tc_gemm_bf16"): (fl["precond"], "tensor", pk["bf16"], "TFLOP/s", "bf16 burst (measured)"),
             ("inverse", "tc_gemm_tf32x3"): (eng, "tensor", tf32x3_peak, "TFLOP/s",

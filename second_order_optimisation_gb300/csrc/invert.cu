@@ -184,11 +184,13 @@ __device__ __forceinline__ const TileMat &tile_of(const TileParams &P, int &si, 
     return q;
 }
 
-// X = (lower part of sym(F) + damp I, zero strictly above the diagonal) as a
-// (hi, lo) pair on [d, d], identity on the padding.  One CTA per upper 64 x 64
-// tile pair: the upper tile of F is read once (16-byte pieces where the rows
-// allow) and written transposed to its lower position; the upper position
-// gets zeros (the diagonal tile: its lower triangle and zeros).
+// X = lower part of sym(F) + damp I as a (hi, lo) pair on [d, d], identity on
+// the padding: the blocks below the diagonal 128-blocks go into X, the
+// diagonal 128-blocks into D (lower part, zeros above; the diag kernel reads
+// them from there and writes W_kk over X's block).  X's diagonal blocks and
+// everything above them are not written: no product reads them.  One
+// CTA per upper 64 x 64 tile pair: the upper tile of F is read once (16-byte
+// pieces where the rows allow) and written transposed to its lower position.
 __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ TileParams P) {
     pdl_wait();
     pdl_trigger();
@@ -230,6 +232,10 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ TileP
     for (int side = 0; side < 2; ++side) {
         if (side == 1 && si == sj) break;
         const int ti = side ? sj : si, tj = side ? si : sj;
+        const bool in_diag = (ti * TT) / NB == (tj * TT) / NB;  // inside a diagonal 128-block: D only
+        // above the diagonal 128-blocks nothing reads X; inside one, D gets
+        // the whole block (the diagonal updates read it back in full)
+        if (side == 0 && si != sj && !in_diag) continue;
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             const int r = rr + 16 * p, i = ti * TT + r;
@@ -245,13 +251,14 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ TileP
                 h[u] = tf32_hi(v);
                 l[u] = v - h[u];
             }
-            const long long o = (long long)i * q.dp + tj * TT + c4;
-            *reinterpret_cast<float4 *>(q.Xh + o) = make_float4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<float4 *>(q.Xl + o) = make_float4(l[0], l[1], l[2], l[3]);
-            if ((ti * TT) / NB == (tj * TT) / NB) {  // inside a diagonal 128-block: also into D
+            if (in_diag) {
                 const long long od = (long long)i * NB + (tj * TT) % NB + c4;
                 *reinterpret_cast<float4 *>(q.Dh + od) = make_float4(h[0], h[1], h[2], h[3]);
                 *reinterpret_cast<float4 *>(q.Dl + od) = make_float4(l[0], l[1], l[2], l[3]);
+            } else {
+                const long long o = (long long)i * q.dp + tj * TT + c4;
+                *reinterpret_cast<float4 *>(q.Xh + o) = make_float4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<float4 *>(q.Xl + o) = make_float4(l[0], l[1], l[2], l[3]);
             }
         }
     }
@@ -639,9 +646,10 @@ struct TriOp {
 };
 
 // Working buffers of one matrix (fp32 (hi, lo) pairs, [dp][dp] each):
-//   X   lower part: the factor, its block columns updated into Schur-complement
-//       columns, then W = L^-1 (diagonal blocks from the diag leaves, the
-//       rest from the triangular inverse); strictly upper part zero
+//   X   blocks below the diagonal 128-blocks: the factor, its block columns
+//       updated into Schur-complement columns, then W = L^-1 (diagonal blocks
+//       from the diag leaves, zeros above their diagonal; the rest from the
+//       triangular inverse); blocks above the diagonal are never written or read
 //   Wt  upper part: W^T (diagonal blocks in full, zeros below)
 //   LT  lower blocks: the Cholesky panels L_ik (i > k);  upper blocks:
 //       (L21 W11)^T of the triangular inverse

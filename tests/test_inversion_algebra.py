@@ -137,6 +137,16 @@ def chain(dp):
     return ops
 
 
+def _prep(buf, X0, dp):
+    """The prep kernel: the blocks strictly below the diagonal 128-blocks into X
+    (X's diagonal blocks and everything above them stay unwritten: NaN here),
+    the diagonal blocks into D (lower part, zeros above)."""
+    for bi in range(0, dp, NB):
+        for bj in range(0, bi, NB):
+            buf["X"][bi:bi + NB, bj:bj + NB] = X0[bi:bi + NB, bj:bj + NB]
+        buf["D"][bi:bi + NB] = np.tril(X0[bi:bi + NB, bi:bi + NB])
+
+
 def invert_like_the_library(F, damp, bn):
     d = F.shape[0]
     dp = -(-d // NB) * NB
@@ -144,9 +154,7 @@ def invert_like_the_library(F, damp, bn):
     X0[:d, :d] = F + damp * np.eye(d)
     buf = {k: np.full((dp, dp), np.nan) for k in ("X", "W", "L")}
     buf["D"] = np.full((dp, NB), np.nan)
-    buf["X"][:] = np.tril(X0)                     # prep: lower part, zeros above
-    for b in range(0, dp, NB):                     # ... and its diagonal blocks into D
-        buf["D"][b:b + NB] = np.tril(X0)[b:b + NB, b:b + NB]
+    _prep(buf, X0, dp)
     def launch(jobs):
         results = []
         for j in jobs:   # every problem of one launch reads before any writes
@@ -326,9 +334,7 @@ def _emulated_inverse(F, damp, order):
     X0[:d, :d] = F + damp * np.eye(d)
     buf = {k: np.full((dp, dp), np.nan) for k in ("X", "W", "L")}
     buf["D"] = np.full((dp, NB), np.nan)
-    buf["X"][:] = np.tril(X0)
-    for b in range(0, dp, NB):
-        buf["D"][b:b + NB] = np.tril(X0)[b:b + NB, b:b + NB]
+    _prep(buf, X0, dp)
     out = None
     for kind, payload in order:
         if kind == "leaf":
