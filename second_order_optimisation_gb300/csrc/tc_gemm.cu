@@ -39,7 +39,7 @@ namespace {
 constexpr int BM = 128, BN = 128;
 constexpr int TILE_BYTES = 128 * 128;  // one tf32 operand tile: 128 rows x 128 bytes
 constexpr int NUM_THREADS = 192;
-constexpr int TMEM_ACC = 2 * BN;  // two accumulators (columns 0 and BN), alternating
+constexpr int TMEM_ACC = 2 * BN;  // bf16: two accumulators (columns 0 and BN), alternating
 constexpr int MAX_PROBS = 152;
 constexpr int GROUP = 8;              // row blocks per band of the grouped tile order
 #ifndef KFAC_BF16_ITEMS_PER_SM
