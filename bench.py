@@ -353,7 +353,7 @@ class Inputs:
             x, g, grad = W.layer_inputs(L, batch, tag)
             if L.hin == 1:
                 x = x.reshape(x.shape[0], -1)
-            ld = (L.d_a + 7) // 8 * 8
+            ld = (L.d_a + 63) // 64 * 64   # rows on 128-byte boundaries
             gp = torch.zeros(L.d_g, ld, dtype=torch.bfloat16)
             gp[:, :L.d_a] = grad
             for t in (x, g, gp):

@@ -546,7 +546,7 @@ kfac_status plan_precond(const kfac_precond_desc *descs, int count, int dtype, A
     for (int i = 0; i < count; ++i) {
         const kfac_precond_desc &d = descs[i];
         if (dtype != KFAC_F32) {
-            const long long ldt = (d.dA + 7) / 8 * 8;
+            const long long ldt = (d.dA + 63) / 64 * 64;  // T's rows on 128-byte boundaries
             uint16_t *T = ws.take<uint16_t>((size_t)d.dG * ldt);
             TcJob a{};  // T = grad * A_inv   (A_inv symmetric: its rows are the columns of B)
             a.map_a = map(d.grad, d.ld_grad, d.dG, d.dA);

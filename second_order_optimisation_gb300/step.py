@@ -36,8 +36,20 @@ from . import kfac
 from .workloads import Layer
 
 
-def _ld8(d: int) -> int:
-    return (d + 7) // 8 * 8
+def _pitch(d: int) -> int:
+    """Row pitch (elements) of the step's matrices: rows start on 128-byte
+    boundaries (16-bit) / 256-byte boundaries (fp32), which the tensor-memory
+    copies read in whole 128-byte segments (FC 4096's preconditioner: 0.36 ->
+    0.31 ms against rows padded to 8 elements only)."""
+    return (d + 63) // 64 * 64
+
+
+def _matrix(rows: int, cols: int, device, dtype=torch.float32, eye: bool = False) -> torch.Tensor:
+    """A [rows, cols] view of a buffer with row pitch _pitch(cols)."""
+    v = torch.zeros(rows, _pitch(cols), dtype=dtype, device=device)[:, :cols]
+    if eye:
+        v.copy_(torch.eye(rows, cols, dtype=dtype, device=device))
+    return v
 
 
 @dataclass
@@ -47,7 +59,7 @@ class LayerState:
     G: torch.Tensor
     A_inv: torch.Tensor
     G_inv: torch.Tensor
-    A_inv16: torch.Tensor      # [dA, ld8(dA)] bf16 (view of the first dA columns used)
+    A_inv16: torch.Tensor      # [dA, dA] bf16 view (row pitch _pitch(dA))
     G_inv16: torch.Tensor
     out: torch.Tensor          # preconditioned gradient [dG, dA] fp32
 
@@ -75,11 +87,10 @@ class KfacStep:
             dA, dG = L.d_a, L.d_g
             self.state.append(LayerState(
                 L,
-                torch.eye(dA, device=self.device), torch.eye(dG, device=self.device),
-                torch.empty(dA, dA, device=self.device), torch.empty(dG, dG, device=self.device),
-                torch.empty(dA, _ld8(dA), dtype=torch.bfloat16, device=self.device),
-                torch.empty(dG, _ld8(dG), dtype=torch.bfloat16, device=self.device),
-                torch.empty(dG, dA, device=self.device)))
+                _matrix(dA, dA, self.device, eye=True), _matrix(dG, dG, self.device, eye=True),
+                _matrix(dA, dA, self.device), _matrix(dG, dG, self.device),
+                _matrix(dA, dA, self.device, torch.bfloat16), _matrix(dG, dG, self.device, torch.bfloat16),
+                _matrix(dG, dA, self.device)))
         self.info = torch.zeros(2 * len(self.layers), dtype=torch.int32, device=self.device)
         self.damp = torch.zeros(2 * len(self.layers), device=self.device)
         self._ws = {}
@@ -107,12 +118,11 @@ class KfacStep:
         return srcs
 
     def invert_pairs(self):
-        return [kfac.InvertPair(s.A, s.G, s.A_inv, s.G_inv, s.A_inv16[:, :s.A.shape[0]],
-                                s.G_inv16[:, :s.G.shape[0]]) for s in self.state]
+        return [kfac.InvertPair(s.A, s.G, s.A_inv, s.G_inv, s.A_inv16, s.G_inv16) for s in self.state]
 
     def precond_items(self, grads):
         ws = self.weights if self.weights is not None else [None] * len(self.state)
-        return [kfac.PrecondItem(s.G_inv16[:, :s.G.shape[0]], s.A_inv16[:, :s.A.shape[0]], gr, s.out,
+        return [kfac.PrecondItem(s.G_inv16, s.A_inv16, gr, s.out,
                                  w=w, eta=self.eta)
                 for s, gr, w in zip(self.state, grads, ws)]
 
