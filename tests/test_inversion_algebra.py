@@ -327,6 +327,80 @@ def launch_graph(dp, early=True):
     return nodes
 
 
+def launch_graph_bulk(dp):
+    """The chain with a third stream for the bulk of each column's update (the
+    library's default): per block column k, after the diag launch, the side
+    stream takes the panel L[k+2:, k] and the bulk stream, once that panel is
+    done, the terms j <= k of column k + 2 (X[k+3:, k+2] and D_{k+2}); after
+    the first panel block of k the side stream takes the last term of column
+    k + 1 (K = 128) once column k + 1's bulk is done; the diagonal update on
+    the chain waits for that bulk too.  Streams main / side / bulk."""
+    nb = dp // NB
+    nodes, last = [], {}
+
+    def add(stream, kind, payload, deps=()):
+        d = set(deps)
+        if stream in last:
+            d.add(last[stream])
+        nodes.append((stream, kind, payload, sorted(d)))
+        last[stream] = len(nodes) - 1
+        return len(nodes) - 1
+
+    side_of, bulk_of, i_diag, i_first = {}, {}, [None] * nb, [None] * nb
+
+    def main(kind, payload, side=None, bulk=None, needs_side=None, needs_bulk=None, side_needs_bulk=None):
+        deps = ([side_of[needs_side]] if needs_side is not None else []) + \
+               ([bulk_of[needs_bulk]] if needs_bulk is not None else [])
+        i = add("main", kind, payload, deps)
+        if side:
+            side_of[i] = add("side", "gemm", side, [i] + ([bulk_of[side_needs_bulk]]
+                                                          if side_needs_bulk is not None else []))
+        if bulk:
+            bulk_of[i] = add("bulk", "gemm", bulk, [side_of[i]])
+        return i
+
+    last_side = last_bulk = None
+    for k in range(nb):
+        kb = k * NB
+        side = bulk = None
+        if k + 2 < nb:
+            side = [_job("X", kb + 2 * NB, kb, "X", kb, kb, dp - kb - 2 * NB, NB, NB, 1.0, 0.0,
+                         C=("L", kb + 2 * NB, kb))]
+            bulk = [_dupd(k + 2, 0, k + 1)]
+            if k + 3 < nb:   # X[k+3:, k+2] -= L[k+3:, :k+1] L[k+2, :k+1]^T
+                bulk.insert(0, _job("L", kb + 3 * NB, 0, "L", kb + 2 * NB, 0, dp - kb - 3 * NB, NB, kb + NB,
+                                    -1.0, 1.0, C=("X", kb + 3 * NB, kb + 2 * NB)))
+        i_diag[k] = main("leaf", kb, side, bulk)
+        if side:
+            last_side = last_bulk = i_diag[k]
+        if k + 1 == nb:
+            break
+        side = None
+        bulk_k1 = i_diag[k - 1] if k >= 1 and k + 1 < nb else None   # column k + 1's bulk
+        if k + 2 < nb:       # X[k+2:, k+1] -= L[k+2:, k] L[k+1, k]^T
+            side = [_job("L", kb + 2 * NB, kb, "L", kb + NB, kb, dp - kb - 2 * NB, NB, NB, -1.0, 1.0,
+                         C=("X", kb + 2 * NB, kb + NB))]
+        i_first[k] = main("gemm", [_job("X", kb + NB, kb, "X", kb, kb, NB, NB, NB, 1.0, 0.0,
+                                        C=("L", kb + NB, kb))], side,
+                          needs_side=i_first[k - 1] if k >= 1 else None,
+                          side_needs_bulk=bulk_k1 if side else None)
+        if side:
+            last_side = i_first[k]
+        main("gemm", [_dupd(k + 1, k, k + 1)], needs_bulk=bulk_k1)
+    by_height = []
+    _tri_nodes(0, dp, by_height)
+    for ht in range(1, len(by_height)):
+        first = ht == 1
+        main("gemm", [_t_job(o, n) for o, n in by_height[ht]], None, None,
+             needs_side=last_side if first else None, needs_bulk=last_bulk if first else None)
+        main("gemm", [_x_job(o, n) for o, n in by_height[ht]])
+    fin_deps = []
+    if len(by_height) <= 1 and last_side is not None:
+        fin_deps = [side_of[last_side], bulk_of[last_bulk]]
+    add("main", "fin", None, fin_deps)
+    return nodes
+
+
 def _emulated_inverse(F, damp, order):
     d = F.shape[0]
     dp = -(-d // NB) * NB
@@ -378,7 +452,7 @@ def _orders(nodes, policy, seed):
     and side streams as early (or the main stream as late) as the edges allow."""
     rng = np.random.default_rng(seed)
     done, order, left = set(), [], list(range(len(nodes)))
-    rank = {"tri": 0, "side": 1, "main": 2}
+    rank = {"tri": 0, "bulk": 0, "side": 1, "main": 2}
     while left:
         ready = [i for i in left if all(d in done for d in nodes[i][3])]
         if policy == "random":
@@ -424,3 +498,76 @@ def test_early_inverse_graph_shape():
     assert count == {"main": 36 + 35 + 35 + 1, "side": 34 + 34, "tri": 70}
     # a matrix under the threshold keeps the inverse on its chain
     assert not any(n[0] == "tri" for n in launch_graph(896, early=True))
+
+
+@pytest.mark.parametrize("d", [1, 200, 384, 1000, 1100, 1536])
+@pytest.mark.parametrize("policy", ["random", "helpers_first", "main_first"])
+def test_bulk_stream_schedule_respects_its_dependencies(d, policy):
+    """The three-stream Cholesky (bulk of each column's update one column early
+    on a stream of its own) in random and adversarial orders."""
+    rng = np.random.default_rng(d + 7)
+    Z = rng.standard_normal((d, max(d // 2, 1)))
+    F = Z @ Z.T / max(d // 2, 1)
+    damp = 0.05
+    nodes = launch_graph_bulk(-(-d // NB) * NB)
+    for seed in range(2 if policy == "random" else 1):
+        inv = _emulated_inverse(F, damp, _orders(nodes, policy, seed))
+        assert np.isfinite(inv).all()
+        R = (F + damp * np.eye(d)) @ inv - np.eye(d)
+        assert np.abs(R).max() < 1e-8
+
+
+def _regions(kind, payload, dp):
+    """(reads, writes) of one launch as (buffer, r0, r1, c0, c1) rectangles."""
+    if kind == "leaf":
+        o = payload
+        return [("D", o, o + NB, 0, NB)], [("X", o, o + NB, o, o + NB), ("W", o, o + NB, o, o + NB)]
+    if kind == "fin":
+        return [("W", 0, dp, 0, dp)], []
+    rd, wr = [], []
+    for j in payload:
+        rd.append((j["A"], j["ar"], j["ar"] + j["M"], j["ac"], j["ac"] + j["K"]))
+        rd.append((j["B"], j["br"], j["br"] + j["N"], j["bc"], j["bc"] + j["K"]))
+        if j["C"]:
+            b, r, c = j["C"]
+            wr.append((b, r, r + j["M"], c, c + j["N"]))
+            if j["beta"]:
+                rd.append((b, r, r + j["M"], c, c + j["N"]))
+        if j["Ct"]:
+            b, r, c = j["Ct"]
+            wr.append((b, r, r + j["N"], c, c + j["M"]))
+    return rd, wr
+
+
+def _overlap(a, b):
+    return a[0] == b[0] and a[1] < b[2] and b[1] < a[2] and a[3] < b[4] and b[3] < a[4]
+
+
+def _races(nodes, dp):
+    """Pairs of launches that touch a common region (one of them writing it)
+    with no dependency path between them in either direction."""
+    n = len(nodes)
+    reach = [set() for _ in range(n)]      # reach[i]: nodes that must finish before i starts
+    for i, nd in enumerate(nodes):
+        for d in nd[3]:
+            reach[i] |= reach[d] | {d}
+    regs = [_regions(nd[1], nd[2], dp) for nd in nodes]
+    out = []
+    for i in range(n):
+        for k in range(i):
+            if k in reach[i] or i in reach[k]:
+                continue
+            ri, wi = regs[i]
+            rk, wk = regs[k]
+            if any(_overlap(a, b) for a in wi for b in rk + wk) or any(_overlap(a, b) for a in wk for b in ri):
+                out.append((k, i))
+    return out
+
+
+@pytest.mark.parametrize("dp", [128, 384, 1024, 1536])
+def test_launch_graphs_have_no_unordered_conflicting_launches(dp):
+    """Every two launches that touch a common region, one writing it, are
+    ordered by the declared dependencies (a check of the whole graph, which
+    also covers the updates that commute and so pass any execution order)."""
+    assert _races(launch_graph_bulk(dp), dp) == []
+    assert _races(launch_graph(dp, early=False), dp) == []
