@@ -64,6 +64,23 @@ constexpr bool LOOKAHEAD = KFAC_INV_LOOKAHEAD && !KFAC_INV_FUSED_PANEL;
 // side update of column k (1); or the whole sum on the chain, split finely
 // over K (0).  A tuning constant that may be set at build time.
 constexpr bool SIDE_DIAG_BULK = KFAC_INV_SIDE_DIAG_BULK;
+#ifndef KFAC_INV_SIDE_BULK
+#define KFAC_INV_SIDE_BULK 1
+#endif
+// With the lookahead and SIDE_DIAG_BULK: the side update of block column
+// k + 1 keeps only its last term L[k+2:, k] L[k+1, k]^T, and the earlier
+// terms (of the column and of its diagonal block) run on a third stream as
+// soon as the panel of column k - 1 is done (1); or the whole update runs on
+// the side stream after the first panel block of k (0).  A tuning constant
+// that may be set at build time.
+constexpr bool SIDE_BULK = KFAC_INV_SIDE_BULK && SIDE_DIAG_BULK && LOOKAHEAD;
+#ifndef KFAC_INV_BULK_REST
+#define KFAC_INV_BULK_REST 0
+#endif
+// The bulk stream for the second (low-priority) group's chains too (1), or
+// for the critical group's only (0).  A tuning constant that may be set at
+// build time.
+constexpr bool BULK_REST = KFAC_INV_BULK_REST;
 #ifndef KFAC_INV_EARLY_TRI
 #define KFAC_INV_EARLY_TRI 0
 #endif
@@ -634,7 +651,11 @@ struct Op {
     std::vector<TcJob> g;
     std::vector<TcJob> side;  // engine problems that may start once this op is done (lookahead,
                               // launched on the group's side stream)
+    std::vector<TcJob> bulk;  // engine problems that may start once this op's side problems are done
+                              // (launched on the group's bulk stream)
     int needs_side = -1;      // chain index of the op whose side problems must be done first
+    int needs_bulk = -1;      // chain index of the op whose bulk problems must be done first
+    int side_needs_bulk = -1; // the same, for this op's side problems
     bool needs_tri = false;   // waits for the chain's early triangular inverse
 };
 
@@ -702,8 +723,8 @@ int tri_nodes(int o, int n, std::vector<std::vector<std::pair<int, int>>> &by_he
 // upper triangular with zeros below in Wt, so the products run over whole
 // blocks; T reads W11^T from Wt only from each output tile's first column on
 // (ktri), where Wt holds its upper part and diagonal blocks.
-void gen_chain(std::vector<Op> &ops, std::vector<TriOp> &tri, bool early_tri, const MatWork &w, const InvMatrix &mat,
-               int *info) {
+void gen_chain(std::vector<Op> &ops, std::vector<TriOp> &tri, bool early_tri, bool side_bulk, const MatWork &w,
+               const InvMatrix &mat, int *info) {
     const long long ld = w.dp;
     const int nb = w.dp / NB;
     auto diag_op = [&](int k) {
@@ -744,7 +765,14 @@ void gen_chain(std::vector<Op> &ops, std::vector<TriOp> &tri, bool early_tri, co
         return split_job(w.ml, cb, j0 * NB, w.ml, cb, j0 * NB, NB, NB, (j1 - j0) * NB, -1.f, 1.f,
                          w.Dh + (long long)cb * NB, w.Dl + (long long)cb * NB, nullptr, nullptr, NB);
     };
-    int last_side = -1;  // chain index of the last op with side problems
+    // X[r0:r1, c] -= L[r0:r1, j0:j1] L[c, j0:j1]^T (block columns j0 .. j1 - 1)
+    auto xupd = [&](int c, int r0, int r1, int j0, int j1) {
+        const int cb = c * NB;
+        const long long o = (long long)r0 * ld + cb;
+        return split_job(w.ml, r0, j0 * NB, w.ml, cb, j0 * NB, r1 - r0, NB, (j1 - j0) * NB, -1.f, 1.f, w.Xh + o,
+                         w.Xl + o, nullptr, nullptr, ld);
+    };
+    int last_side = -1, last_bulk = -1;  // chain indices of the last ops with side / bulk problems
     std::vector<int> i_diag(nb, -1), i_first(nb, -1);
     if (!LOOKAHEAD) {
         for (int k = 0; k < nb; ++k) {
@@ -777,20 +805,35 @@ void gen_chain(std::vector<Op> &ops, std::vector<TriOp> &tri, bool early_tri, co
         // inverse for the last side launch.  (Without SIDE_DIAG_BULK the
         // chain's diagonal update runs over all of L[k+1, :k+1], split finely
         // over K, after the side panel of k - 1, the last one holding a block
-        // of row k + 1.)
+        // of row k + 1.)  With SIDE_BULK the side update after the first
+        // panel block of k keeps only the last term, X[k+2:, k+1] -=
+        // L[k+2:, k] L[k+1, k]^T; the terms j < k of column k + 1 and of
+        // D_{k+1} were subtracted on the bulk stream after the side panel of
+        // k - 1, and both that last term and the diagonal update on the chain
+        // wait for them.
         for (int k = 0; k < nb; ++k) {
             const int kb = k * NB;
             Op d = diag_op(k);
-            if (!FUSED_PANEL && k + 2 < nb) d.side.push_back(panel(k, kb + 2 * NB, w.dp));
+            if (!FUSED_PANEL && k + 2 < nb) {
+                d.side.push_back(panel(k, kb + 2 * NB, w.dp));
+                if (side_bulk) {  // the terms j <= k of column k + 2 and of D_{k+2}
+                    if (k + 3 < nb) d.bulk.push_back(xupd(k + 2, kb + 3 * NB, w.dp, 0, k + 1));
+                    d.bulk.push_back(dupd(k + 2, 0, k + 1));
+                }
+            }
             i_diag[k] = (int)ops.size();
             if (!d.side.empty()) last_side = i_diag[k];
+            if (!d.bulk.empty()) last_bulk = i_diag[k];
             ops.push_back(d);
             if (k + 1 == nb) break;
             if (!FUSED_PANEL) {
                 Op pf{};
                 pf.g.push_back(panel(k, kb + NB, kb + 2 * NB));
                 if (k >= 1) pf.needs_side = i_first[k - 1];
-                if (k + 2 < nb) {
+                if (k + 2 < nb && side_bulk) {
+                    pf.side.push_back(xupd(k + 1, kb + 2 * NB, w.dp, k, k + 1));
+                    if (k >= 1) pf.side_needs_bulk = i_diag[k - 1];
+                } else if (k + 2 < nb) {
                     pf.side.push_back(update(k + 1, kb + 2 * NB, w.dp, false));
                     // D_{k+2} -= L[k+2, :k+1] L[k+2, :k+1]^T (its last term stays on the chain)
                     if (SIDE_DIAG_BULK) pf.side.push_back(dupd(k + 2, 0, k + 1));
@@ -804,6 +847,7 @@ void gen_chain(std::vector<Op> &ops, std::vector<TriOp> &tri, bool early_tri, co
                 // D_{k+1} -= L[k+1, k] L[k+1, k]^T: the terms before it were
                 // subtracted by the side launch the first panel block waited for
                 ud.g.push_back(dupd(k + 1, k, k + 1));
+                if (side_bulk && k >= 1) ud.needs_bulk = i_diag[k - 1];
             } else {
                 ud.g.push_back(update(k + 1, kb + NB, kb + 2 * NB, true));
                 ud.g.back().fine_split = 1;
@@ -868,12 +912,18 @@ void gen_chain(std::vector<Op> &ops, std::vector<TriOp> &tri, bool early_tri, co
                 t.g.push_back(node_t(nd.first, nd.second));
                 x.g.push_back(node_x(nd.first, nd.second));
             }
-            if (ops.size() == first_tri) t.needs_side = last_side;
+            if (ops.size() == first_tri) {
+                t.needs_side = last_side;
+                t.needs_bulk = last_bulk;
+            }
             ops.push_back(t);
             ops.push_back(x);
         }
     }
-    if (ops.size() == first_tri) fin.needs_side = last_side;
+    if (ops.size() == first_tri) {
+        fin.needs_side = last_side;
+        fin.needs_bulk = last_bulk;
+    }
     TcJob j{};
     j.map_a = j.map_b = w.mw;
     j.M = j.N = w.d;
@@ -969,6 +1019,14 @@ constexpr int TRI_FREE_SMS = KFAC_INV_TRI_FREE_SMS;  // SMs a group's early-inve
 #define KFAC_INV_TRI_HIGH_PRIO 0
 #endif
 constexpr bool TRI_HIGH_PRIO = KFAC_INV_TRI_HIGH_PRIO;  // early-inverse streams at their group's priority (else low)
+#ifndef KFAC_INV_BULK_FREE_SMS
+#define KFAC_INV_BULK_FREE_SMS 48
+#endif
+constexpr int BULK_FREE_SMS = KFAC_INV_BULK_FREE_SMS;  // SMs a group's bulk launches leave to the rest
+#ifndef KFAC_INV_BULK_HIGH_PRIO
+#define KFAC_INV_BULK_HIGH_PRIO 1
+#endif
+constexpr bool BULK_HIGH_PRIO = KFAC_INV_BULK_HIGH_PRIO;  // bulk streams at their group's priority (else low)
 constexpr int SIDE_GROUPS = KFAC_INV_SIDE_GROUPS;  // groups whose lookahead updates run on a side stream (the others
                                    // run them in their own stream, right after the enabling round)
 
@@ -986,6 +1044,12 @@ struct InvGroup {
     std::vector<int> round_kind;
     std::vector<std::vector<TcJob>> side;   // per round: side problems launched once it is done
     std::vector<std::vector<int>> waits;    // per round: rounds whose side launch must finish first
+    std::vector<std::vector<TcJob>> bulk;   // per round: bulk problems launched once its side launch is done
+    std::vector<std::vector<int>> bulk_waits;       // per round: rounds whose bulk launch must finish first
+    std::vector<std::vector<int>> side_bulk_waits;  // the same, for the round's side launch
+    int bulk_ctas = 0;
+    char *bulk_ws = nullptr;
+    size_t bulk_bytes = 0;
     std::vector<TriStep> tri;               // early triangular inverse, in stream order
     std::vector<std::vector<int>> tri_waits;  // per round: tri steps that must finish first
     std::vector<char> record_main;          // per round: a tri step waits for it
@@ -1055,7 +1119,7 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
         w.ml = base + 8;
         const int nbk = w.dp / NB;
         const bool early = EARLY_TRI && nbk >= EARLY_TRI_MIN_NB && 4 * nbk >= 3 * nb_max;
-        gen_chain(p.chains[k], p.tri[k], early, w, mats[k], info_dev ? info_dev + k : nullptr);
+        gen_chain(p.chains[k], p.tri[k], early, SIDE_BULK, w, mats[k], info_dev ? info_dev + k : nullptr);
         p.longest = std::max(p.longest, p.chains[k].size());
     }
     if (p.maps.size() != (size_t)MAPS_PER_MATRIX * nmats) return KFAC_ERR_WORKSPACE;  // device map area
@@ -1070,6 +1134,16 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
     if (!rest.members.empty()) {
         rest.max_ctas = std::max(1, device_sm_count() - RESERVED_SMS);
         p.groups.push_back(rest);
+        // the second group's chains without the bulk stream (the chain's
+        // ops, and so the grouping, are the same either way)
+        for (int k : rest.members)
+            if (SIDE_BULK && !BULK_REST) {
+                const MatWork &w = p.work[k];
+                const bool early = !p.tri[k].empty();
+                p.chains[k].clear();
+                p.tri[k].clear();
+                gen_chain(p.chains[k], p.tri[k], early, false, w, mats[k], info_dev ? info_dev + k : nullptr);
+            }
     }
     // rounds, side launches and engine scratch of each group
     const int sms = device_sm_count();
@@ -1080,22 +1154,37 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
         const size_t R = g.rounds.size();
         g.side.assign(R, {});
         g.waits.assign(R, {});
+        g.bulk.assign(R, {});
+        g.bulk_waits.assign(R, {});
+        g.side_bulk_waits.assign(R, {});
+        g.bulk_ctas = std::max(1, (g.max_ctas > 0 ? g.max_ctas : sms) - BULK_FREE_SMS);
         std::vector<std::vector<int>> round_of(p.chains.size());
         for (int k : g.members) round_of[k].assign(p.chains[k].size(), -1);
         for (size_t r = 0; r < R; ++r)
             for (const auto &ki : g.rounds[r]) round_of[ki.first][ki.second] = (int)r;
-        size_t tcb = 0, sideb = 0;
+        size_t tcb = 0, sideb = 0, bulkb = 0;
+        auto add_wait = [&](std::vector<int> &v, int k, int op) {
+            if (op < 0) return;
+            const int src = round_of[k][op];
+            if (std::find(v.begin(), v.end(), src) == v.end()) v.push_back(src);
+        };
         for (size_t r = 0; r < R; ++r) {
             round.clear();
             for (const auto &ki : g.rounds[r]) {
                 const Op &op = p.chains[ki.first][ki.second];
                 if (op.leaf == 0) round.insert(round.end(), op.g.begin(), op.g.end());
                 g.side[r].insert(g.side[r].end(), op.side.begin(), op.side.end());
-                if (op.needs_side >= 0) {
-                    const int src = round_of[ki.first][op.needs_side];
-                    if (std::find(g.waits[r].begin(), g.waits[r].end(), src) == g.waits[r].end())
-                        g.waits[r].push_back(src);
-                }
+                g.bulk[r].insert(g.bulk[r].end(), op.bulk.begin(), op.bulk.end());
+                add_wait(g.waits[r], ki.first, op.needs_side);
+                add_wait(g.bulk_waits[r], ki.first, op.needs_bulk);
+                add_wait(g.side_bulk_waits[r], ki.first, op.side_needs_bulk);
+            }
+            if (!g.bulk[r].empty() && g.side[r].empty()) return KFAC_ERR_UNSUPPORTED;  // (cannot happen)
+            if (!g.bulk[r].empty()) {  // on the bulk stream (bulk_ctas) or inline (max_ctas)
+                bulkb = std::max(bulkb, tc_workspace_bytes(g.bulk[r].data(), (int)g.bulk[r].size(), TC_KIND_TF32X3,
+                                                           g.bulk_ctas));
+                bulkb = std::max(bulkb, tc_workspace_bytes(g.bulk[r].data(), (int)g.bulk[r].size(), TC_KIND_TF32X3,
+                                                           g.max_ctas));
             }
             tcb = std::max(tcb, tc_workspace_bytes(round.data(), (int)round.size(), TC_KIND_TF32X3, g.max_ctas));
             if (!g.side[r].empty()) {  // launched on the side stream (side_ctas) or inline (max_ctas)
@@ -1107,8 +1196,17 @@ kfac_status plan_inv(const InvMatrix *mats, int nmats, int *info_dev, Arena &ws,
         }
         g.tc_bytes = tcb;
         g.tc_ws = ws.take<char>(tcb);
+        for (size_t r = 0; r < R; ++r) {  // every awaited launch exists (else the wait would be a no-op)
+            for (int src : g.waits[r])
+                if (g.side[src].empty()) return KFAC_ERR_UNSUPPORTED;
+            for (const auto *v : {&g.bulk_waits[r], &g.side_bulk_waits[r]})
+                for (int src : *v)
+                    if (g.bulk[src].empty() || src >= (int)r) return KFAC_ERR_UNSUPPORTED;
+        }
         g.side_bytes = sideb;
         g.side_ws = ws.take<char>(sideb);
+        g.bulk_bytes = bulkb;
+        g.bulk_ws = ws.take<char>(bulkb);
 
         // early triangular inverse: chains of one padded width have the same
         // steps, batched into one launch each; the widths' sequences are
@@ -1264,19 +1362,24 @@ kfac_status damping_run(const InvMatrix *mats, int nlayers, float gamma, int pi_
 
 namespace {
 
-// Enqueue one group's rounds on a stream, and its side launches (the
-// lookahead updates) on a second stream: a side launch starts once the round
-// that enables it is done (an event), and a round that needs a side launch
-// waits for its event.  ev_main / ev_side hold one event per round.
-kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st, cudaStream_t side, cudaStream_t tri,
-                      bool use_side, cudaEvent_t *ev_main, cudaEvent_t *ev_side, cudaEvent_t *ev_tri) {
+// Enqueue one group's rounds on a stream, its side launches (the lookahead
+// updates) on a second stream and its bulk launches on a third: a side
+// launch starts once the round that enables it is done (an event), a bulk
+// launch once the side launch of its round is done, and a round or side
+// launch that needs a side or bulk launch waits for its event.  ev_main /
+// ev_side / ev_bulk hold one event per round.
+kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st, cudaStream_t side, cudaStream_t bulk,
+                      cudaStream_t tri, bool use_side, cudaEvent_t *ev_main, cudaEvent_t *ev_side,
+                      cudaEvent_t *ev_bulk, cudaEvent_t *ev_tri) {
     std::vector<DiagJob> leaves;
     std::vector<TcJob> gemms;
     kfac_status s = KFAC_OK;
     size_t next_tri = 0;
     for (size_t r = 0; r < g.rounds.size(); ++r) {
-        if (use_side)
+        if (use_side) {
             for (int src : g.waits[r]) KFAC_CUDA_TRY(cudaStreamWaitEvent(st, ev_side[src], 0));
+            for (int src : g.bulk_waits[r]) KFAC_CUDA_TRY(cudaStreamWaitEvent(st, ev_bulk[src], 0));
+        }
         for (int t : g.tri_waits[r]) KFAC_CUDA_TRY(cudaStreamWaitEvent(st, ev_tri[t], 0));
         leaves.clear();
         gemms.clear();
@@ -1292,19 +1395,32 @@ kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st, cuda
                             g.max_ctas)) != KFAC_OK)
                 return s;
         }
-        if (!g.side[r].empty() && !use_side) {
+        if (!g.side[r].empty() && !use_side) {  // side and bulk problems inline, in that order
             Arena tail(g.side_ws, g.side_bytes);
             if ((s = tc_run(g.side[r].data(), (int)g.side[r].size(), TC_KIND_TF32X3, p.dev_maps, tail, p.err, st,
                             g.max_ctas)) != KFAC_OK)
                 return s;
+            Arena btail(g.bulk_ws, g.bulk_bytes);
+            if (!g.bulk[r].empty() && (s = tc_run(g.bulk[r].data(), (int)g.bulk[r].size(), TC_KIND_TF32X3,
+                                                  p.dev_maps, btail, p.err, st, g.max_ctas)) != KFAC_OK)
+                return s;
         } else if (!g.side[r].empty()) {
             KFAC_CUDA_TRY(cudaEventRecord(ev_main[r], st));
             KFAC_CUDA_TRY(cudaStreamWaitEvent(side, ev_main[r], 0));
+            for (int src : g.side_bulk_waits[r]) KFAC_CUDA_TRY(cudaStreamWaitEvent(side, ev_bulk[src], 0));
             Arena tail(g.side_ws, g.side_bytes);
             if ((s = tc_run(g.side[r].data(), (int)g.side[r].size(), TC_KIND_TF32X3, p.dev_maps, tail, p.err, side,
                             g.side_ctas)) != KFAC_OK)
                 return s;
             KFAC_CUDA_TRY(cudaEventRecord(ev_side[r], side));
+            if (!g.bulk[r].empty()) {
+                KFAC_CUDA_TRY(cudaStreamWaitEvent(bulk, ev_side[r], 0));
+                Arena btail(g.bulk_ws, g.bulk_bytes);
+                if ((s = tc_run(g.bulk[r].data(), (int)g.bulk[r].size(), TC_KIND_TF32X3, p.dev_maps, btail, p.err,
+                                bulk, g.bulk_ctas)) != KFAC_OK)
+                    return s;
+                KFAC_CUDA_TRY(cudaEventRecord(ev_bulk[r], bulk));
+            }
         }
         if (g.record_main[r] && !(use_side && !g.side[r].empty())) KFAC_CUDA_TRY(cudaEventRecord(ev_main[r], st));
         // early triangular inverse: every step whose rounds are now enqueued
@@ -1321,8 +1437,8 @@ kfac_status run_group(const InvPlan &p, const InvGroup &g, cudaStream_t st, cuda
     return KFAC_OK;
 }
 
-// Library-owned streams and events of one device: a main and a side stream
-// for each of the two groups (created on first use; the mutex also keeps
+// Library-owned streams and events of one device: a main, a side, a bulk and
+// an early-inverse stream for each of the two groups (created on first use; the mutex also keeps
 // concurrent callers from interleaving their fork / join records on the
 // shared events).
 constexpr int EVENT_POOL = 1024;
@@ -1330,8 +1446,9 @@ constexpr int EVENT_POOL = 1024;
 struct GroupStreams {
     std::mutex mu;
     bool ready = false;
-    cudaStream_t main[2] = {nullptr, nullptr}, side[2] = {nullptr, nullptr}, tri[2] = {nullptr, nullptr};
-    cudaEvent_t fork = nullptr, done[6] = {};
+    cudaStream_t main[2] = {nullptr, nullptr}, side[2] = {nullptr, nullptr}, bulk[2] = {nullptr, nullptr},
+                 tri[2] = {nullptr, nullptr};
+    cudaEvent_t fork = nullptr, done[8] = {};
     std::vector<cudaEvent_t> pool;  // per-round events of the two groups
 };
 
@@ -1348,10 +1465,11 @@ kfac_status ensure_streams(GroupStreams &g) {
         const int prio = k == 0 ? greatest : least;
         KFAC_CUDA_TRY(cudaStreamCreateWithPriority(&g.main[k], cudaStreamNonBlocking, prio));
         KFAC_CUDA_TRY(cudaStreamCreateWithPriority(&g.side[k], cudaStreamNonBlocking, prio));
+        KFAC_CUDA_TRY(cudaStreamCreateWithPriority(&g.bulk[k], cudaStreamNonBlocking, BULK_HIGH_PRIO ? prio : least));
         KFAC_CUDA_TRY(cudaStreamCreateWithPriority(&g.tri[k], cudaStreamNonBlocking, TRI_HIGH_PRIO ? prio : least));
     }
     KFAC_CUDA_TRY(cudaEventCreateWithFlags(&g.fork, cudaEventDisableTiming));
-    for (int k = 0; k < 6; ++k) KFAC_CUDA_TRY(cudaEventCreateWithFlags(&g.done[k], cudaEventDisableTiming));
+    for (int k = 0; k < 8; ++k) KFAC_CUDA_TRY(cudaEventCreateWithFlags(&g.done[k], cudaEventDisableTiming));
     g.pool.resize(EVENT_POOL);
     for (cudaEvent_t &e : g.pool) KFAC_CUDA_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
     g.ready = true;
@@ -1387,30 +1505,32 @@ kfac_status inv_run(const InvMatrix *mats, int nmats, const float *damp_dev, int
     std::lock_guard<std::mutex> lock(g.mu);
     if ((s = ensure_streams(g)) != KFAC_OK) return s;
     size_t events = 0;
-    for (const InvGroup &gr : p.groups) events += 2 * gr.rounds.size() + gr.tri.size();
+    for (const InvGroup &gr : p.groups) events += 3 * gr.rounds.size() + gr.tri.size();
     if (events > g.pool.size()) return KFAC_ERR_UNSUPPORTED;
     const int ngroups = (int)p.groups.size();
     KFAC_CUDA_TRY(cudaEventRecord(g.fork, st));
     for (int k = 0; k < ngroups; ++k) {
         KFAC_CUDA_TRY(cudaStreamWaitEvent(g.main[k], g.fork, 0));
         KFAC_CUDA_TRY(cudaStreamWaitEvent(g.side[k], g.fork, 0));
+        KFAC_CUDA_TRY(cudaStreamWaitEvent(g.bulk[k], g.fork, 0));
         KFAC_CUDA_TRY(cudaStreamWaitEvent(g.tri[k], g.fork, 0));
     }
     kfac_status res[2] = {KFAC_OK, KFAC_OK};
     size_t ev = 0;
     for (int k = 0; k < ngroups; ++k) {
         const InvGroup &gr = p.groups[k];
-        cudaEvent_t *em = g.pool.data() + ev, *es = em + gr.rounds.size(), *et = es + gr.rounds.size();
-        ev += 2 * gr.rounds.size() + gr.tri.size();
+        cudaEvent_t *em = g.pool.data() + ev, *es = em + gr.rounds.size(), *eb = es + gr.rounds.size(),
+                    *et = eb + gr.rounds.size();
+        ev += 3 * gr.rounds.size() + gr.tri.size();
         const PdlScope pdl(k == 0);  // early-launched CTAs of the low-priority group would hold SMs
-        res[k] = run_group(p, gr, g.main[k], g.side[k], g.tri[k], k < SIDE_GROUPS, em, es, et);
+        res[k] = run_group(p, gr, g.main[k], g.side[k], g.bulk[k], g.tri[k], k < SIDE_GROUPS, em, es, eb, et);
     }
     // join in every case, so that a capture or later work stays ordered
     for (int k = 0; k < ngroups; ++k) {
-        const cudaStream_t sts[3] = {g.main[k], g.side[k], g.tri[k]};
-        for (int q = 0; q < 3; ++q) {
-            KFAC_CUDA_TRY(cudaEventRecord(g.done[3 * k + q], sts[q]));
-            KFAC_CUDA_TRY(cudaStreamWaitEvent(st, g.done[3 * k + q], 0));
+        const cudaStream_t sts[4] = {g.main[k], g.side[k], g.bulk[k], g.tri[k]};
+        for (int q = 0; q < 4; ++q) {
+            KFAC_CUDA_TRY(cudaEventRecord(g.done[4 * k + q], sts[q]));
+            KFAC_CUDA_TRY(cudaStreamWaitEvent(st, g.done[4 * k + q], 0));
         }
     }
     if (res[0] != KFAC_OK) return res[0];
