@@ -317,9 +317,12 @@ struct DiagParams {
 //        L_ic = S_ic L_cc^-T          i past c: a thread per row (forward
 //                                     substitution with L_cc)
 //        S_ij -= L_ic L_jc^T          i >= j past c: 4 x 4 register tiles
-//   2. W = L^-1 by block rows: the diagonal blocks W_ii = L_ii^-1 at once (a
-//      thread per column), then for i = 1 .. 7
-//        T_ij = sum_{t=j}^{i-1} L_it W_tj,   W_ij = -W_ii T_ij   (j < i).
+//   2. W = L^-1 by block rows i, each in the iteration of step 1 that
+//      factors block i:
+//        T_ij = sum_{t=j}^{i-1} L_it W_tj  (j < i)   warps 1..7, after their
+//                                                    share of the update
+//        W_ii = L_ii^-1,  W_ij = -W_ii T_ij          threads 128..255, while
+//                                                    threads below solve the panel
 // 1 / sqrt is the hardware approximation refined by one Newton-Raphson step,
 // y <- y (3 - x y^2) / 2.  A pivot outside [FLT_MIN, inf) is recorded and
 // eliminated with w = 0 (the result is then undefined; finite unless the
@@ -490,9 +493,72 @@ __global__ void __launch_bounds__(DIAG_THREADS, 1) diag_kernel(const __grid_cons
                 }
             }
         }
+        if (warp > 0) {
+            // W's block row c / 16, first half: T_cj = sum_{t=j}^{c-1} L_ct W_tj
+            // for the block columns j < c (rows c .. c + 15 of the panels and
+            // block rows of W before c are final); item (j, r, half) -> 8
+            // entries of row r of T_cj, written over W's block (c, j)
+#pragma unroll 1
+            for (int it = tid - 32; it < c * 2; it += DIAG_THREADS - 32) {
+                const int j = (it >> 5) * DB, r = (it & 31) >> 1, h = (it & 1) * 8;
+                float acc[8];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) acc[v] = 0.f;
+                const float *lrow = M + (c + r) * DLD;
+#pragma unroll 4
+                for (int k = j; k < c; ++k) {
+                    const float l = lrow[k];
+                    const float4 w0 = *reinterpret_cast<const float4 *>(Wm + k * DLD + j + h);
+                    const float4 w1 = *reinterpret_cast<const float4 *>(Wm + k * DLD + j + h + 4);
+                    acc[0] = fmaf(l, w0.x, acc[0]); acc[1] = fmaf(l, w0.y, acc[1]);
+                    acc[2] = fmaf(l, w0.z, acc[2]); acc[3] = fmaf(l, w0.w, acc[3]);
+                    acc[4] = fmaf(l, w1.x, acc[4]); acc[5] = fmaf(l, w1.y, acc[5]);
+                    acc[6] = fmaf(l, w1.z, acc[6]); acc[7] = fmaf(l, w1.w, acc[7]);
+                }
+                *reinterpret_cast<float4 *>(Wm + (c + r) * DLD + j + h) =
+                    make_float4(acc[0], acc[1], acc[2], acc[3]);
+                *reinterpret_cast<float4 *>(Wm + (c + r) * DLD + j + h + 4) =
+                    make_float4(acc[4], acc[5], acc[6], acc[7]);
+            }
+        }
         __syncthreads();
         const int nrest = NB - c - DB;
-        if (tid < nrest) {  // the panel: row i solves L_cc y = S_ic^T
+        if (tid >= NB) {
+            // W's block row c / 16, second half, by threads 128..255 while the
+            // panel below runs: W_cc = L_cc^-1 (a thread per column q, zeros
+            // above the diagonal), then W_cj = -W_cc T_cj (thread (j, q) owns
+            // column q of block (c, j))
+            const int u = tid - NB;
+            if (u < DB) {
+                const int q = u;
+                float x[DB];
+#pragma unroll
+                for (int r = 0; r < DB; ++r) {
+                    float v = r == q ? 1.f : 0.f;
+#pragma unroll
+                    for (int t = 0; t < r; ++t) v = fmaf(-M[(c + r) * DLD + c + t], x[t], v);
+                    x[r] = v * invd[c + r];
+                }
+#pragma unroll
+                for (int r = 0; r < DB; ++r) Wm[(c + r) * DLD + c + q] = x[r];
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(DIAG_THREADS - NB) : "memory");
+            if (u < c) {
+                const int j = (u / DB) * DB, q = u % DB;
+                float tcol[DB], y[DB];
+#pragma unroll
+                for (int v = 0; v < DB; ++v) tcol[v] = Wm[(c + v) * DLD + j + q];
+#pragma unroll
+                for (int r = 0; r < DB; ++r) {
+                    float a = 0.f;
+#pragma unroll
+                    for (int v = 0; v <= r; ++v) a = fmaf(Wm[(c + r) * DLD + c + v], tcol[v], a);
+                    y[r] = -a;
+                }
+#pragma unroll
+                for (int r = 0; r < DB; ++r) Wm[(c + r) * DLD + j + q] = y[r];
+            }
+        } else if (tid < nrest) {  // the panel: row i solves L_cc y = S_ic^T
             const int i = c + DB + tid;
             float x[DB];
             ld16(M + i * DLD + c, x);
@@ -503,65 +569,6 @@ __global__ void __launch_bounds__(DIAG_THREADS, 1) diag_kernel(const __grid_cons
                 for (int j = q + 1; j < DB; ++j) x[j] = fmaf(-x[q], M[(c + j) * DLD + c + q], x[j]);
             }
             st16(M + i * DLD + c, x);
-        }
-        __syncthreads();
-    }
-
-    // 2. W = L^-1: diagonal blocks, a thread per column q of block b
-    if (tid < NB) {
-        const int b = (tid / DB) * DB, q = tid % DB;
-        float x[DB];
-#pragma unroll
-        for (int r = 0; r < DB; ++r) {
-            float v = r == q ? 1.f : 0.f;
-#pragma unroll
-            for (int t = 0; t < r; ++t) v = fmaf(-M[(b + r) * DLD + b + t], x[t], v);
-            x[r] = v * invd[b + r];
-        }
-#pragma unroll
-        for (int r = 0; r < DB; ++r) Wm[(b + r) * DLD + b + q] = x[r];
-    }
-    __syncthreads();
-    //    block rows i = 1 .. 7
-#pragma unroll 1
-    for (int i = DB; i < NB; i += DB) {
-        // T_ij = sum_{t=j}^{i-1} L_it W_tj: thread (j, r, half) -> 8 entries of row r of T_ij
-        const int nb = i / DB;
-        if (tid < nb * 32) {
-            const int j = (tid >> 5) * DB, r = (tid & 31) >> 1, h = (tid & 1) * 8;
-            float acc[8];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) acc[v] = 0.f;
-            const float *lrow = M + (i + r) * DLD;
-#pragma unroll 4
-            for (int k = j; k < i; ++k) {
-                const float l = lrow[k];
-                const float4 w0 = *reinterpret_cast<const float4 *>(Wm + k * DLD + j + h);
-                const float4 w1 = *reinterpret_cast<const float4 *>(Wm + k * DLD + j + h + 4);
-                acc[0] = fmaf(l, w0.x, acc[0]); acc[1] = fmaf(l, w0.y, acc[1]);
-                acc[2] = fmaf(l, w0.z, acc[2]); acc[3] = fmaf(l, w0.w, acc[3]);
-                acc[4] = fmaf(l, w1.x, acc[4]); acc[5] = fmaf(l, w1.y, acc[5]);
-                acc[6] = fmaf(l, w1.z, acc[6]); acc[7] = fmaf(l, w1.w, acc[7]);
-            }
-            *reinterpret_cast<float4 *>(Wm + (i + r) * DLD + j + h) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            *reinterpret_cast<float4 *>(Wm + (i + r) * DLD + j + h + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        }
-        __syncthreads();
-        // W_ij = -W_ii T_ij, in place: thread (j, q) owns column q of block (i, j)
-        if (tid < nb * DB) {
-            const int j = (tid / DB) * DB, q = tid % DB;
-            float tcol[DB], y[DB];
-#pragma unroll
-            for (int v = 0; v < DB; ++v) tcol[v] = Wm[(i + v) * DLD + j + q];
-#pragma unroll
-            for (int r = 0; r < DB; ++r) {
-                float a = 0.f;
-#pragma unroll
-                for (int v = 0; v <= r; ++v) a = fmaf(Wm[(i + r) * DLD + i + v], tcol[v], a);
-                y[r] = -a;
-            }
-#pragma unroll
-            for (int r = 0; r < DB; ++r) Wm[(i + r) * DLD + j + q] = y[r];
         }
         __syncthreads();
     }
