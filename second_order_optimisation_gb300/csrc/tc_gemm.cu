@@ -450,6 +450,17 @@ __device__ __forceinline__ float4 sub4(float4 a, float4 b) {
 }
 __device__ __forceinline__ float comp(float4 v, int t) { return t == 0 ? v.x : t == 1 ? v.y : t == 2 ? v.z : v.w; }
 
+// The ragged-edge fallbacks of the epilogue's stores, out of line: the
+// epilogue's unrolled row-group loops stay small enough for the instruction
+// cache (inlined, each row group carried a scalar copy of its stores, and the
+// loop's code, not its stores, set the time of a 32 x 32 chunk: ~3 us).
+__device__ __noinline__ void store_pair_edge(float *C, float *C_lo, long long off, int n, float4 h, float4 l) {
+    for (int t = 0; t < 4 && t < n; ++t) {
+        C[off + t] = comp(h, t);
+        C_lo[off + t] = comp(l, t);
+    }
+}
+
 // Offset of C's entry (i, 0): row-major with ldc, or the packed upper
 // triangle (row i's entries j >= i start at i*d - i*(i+1)/2 + i).
 __device__ __forceinline__ long long c_row(const TcProb &q, int i) {
@@ -667,11 +678,7 @@ __device__ __forceinline__ bool chunk_store(const TcProb &q, int i0, int j0, con
                 st4(q.C + off, h);
                 st4(q.C_lo + off, l);
             } else {
-                for (int t = 0; t < 4; ++t)
-                    if (j + t < q.N) {
-                        q.C[off + t] = comp(h, t);
-                        q.C_lo[off + t] = comp(l, t);
-                    }
+                store_pair_edge(q.C, q.C_lo, off, q.N - j, h, l);
             }
         }
         if (mirror) {
