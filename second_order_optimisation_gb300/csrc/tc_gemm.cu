@@ -460,6 +460,29 @@ __device__ __noinline__ void store_pair_edge(float *C, float *C_lo, long long of
         C_lo[off + t] = comp(l, t);
     }
 }
+// components t0 <= t < n (of 4) of o into dst[t]
+__device__ __noinline__ void store4_edge(float *dst, int t0, int n, float4 o) {
+    for (int t = max(t0, 0); t < 4 && t < n; ++t) dst[t] = comp(o, t);
+}
+__device__ __noinline__ void store4b_edge(uint16_t *dst, int t0, int n, float4 o, bool h16) {
+    for (int t = max(t0, 0); t < 4 && t < n; ++t) dst[t] = f32_to_16_bits(comp(o, t), h16);
+}
+// dw[t] -= eta o[t] for t < n; true when a result is NaN or infinite
+__device__ __noinline__ bool step4_edge(float *dw, int n, float ne, float4 o) {
+    bool bad = false;
+    for (int t = 0; t < 4 && t < n; ++t) {
+        const float nw = fmaf(ne, comp(o, t), dw[t]);
+        bad |= !(fabsf(nw) <= 3.402823466e38f);
+        dw[t] = nw;
+    }
+    return bad;
+}
+// src[t] for t0 <= t < n (of 4), zeros elsewhere
+__device__ __noinline__ float4 load4_edge(const float *src, int t0, int n) {
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int t = max(t0, 0); t < 4 && t < n; ++t) v[t] = src[t];
+    return make_float4(v[0], v[1], v[2], v[3]);
+}
 
 // Offset of C's entry (i, 0): row-major with ldc, or the packed upper
 // triangle (row i's entries j >= i start at i*d - i*(i+1)/2 + i).
@@ -484,14 +507,9 @@ __device__ __forceinline__ void load_old(const TcProb &q, int i0, int j0, int la
                 h = ld4(q.C + off);
                 if (lo) l = ld4(q.C_lo + off);
             } else {
-                float hv[4] = {0.f, 0.f, 0.f, 0.f}, lv[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int t = 0; t < 4; ++t)
-                    if (j + t < q.N && (!q.packed || j + t >= i)) {
-                        hv[t] = q.C[off + t];
-                        if (lo) lv[t] = q.C_lo[off + t];
-                    }
-                h = make_float4(hv[0], hv[1], hv[2], hv[3]);
-                l = make_float4(lv[0], lv[1], lv[2], lv[3]);
+                const int t0 = q.packed ? i - j : 0;
+                h = load4_edge(q.C + off, t0, q.N - j);
+                if (lo) l = load4_edge(q.C_lo + off, t0, q.N - j);
             }
         }
         oh[k] = h;
@@ -567,8 +585,7 @@ __device__ __forceinline__ bool chunk_store(const TcProb &q, int i0, int j0, con
             if (full && (!upper || j >= i) && (!q.packed || ((uintptr_t)dst & 15) == 0)) {
                 st4(dst, o);
             } else {
-                for (int t = 0; t < 4; ++t)
-                    if (j + t < q.N && (!upper || j + t >= i)) dst[t] = comp(o, t);
+                store4_edge(dst, upper ? i - j : 0, q.N - j, o);
             }
         }
     } else if (q.epi == TC_EPI_STORE) {
@@ -588,8 +605,7 @@ __device__ __forceinline__ bool chunk_store(const TcProb &q, int i0, int j0, con
                 if (full && (!up || j >= i)) {
                     st4(dst, o);
                 } else {
-                    for (int t = 0; t < 4; ++t)
-                        if (j + t < q.N && (!up || j + t >= i)) dst[t] = comp(o, t);
+                    store4_edge(dst, up ? i - j : 0, q.N - j, o);
                 }
             }
             if (q.W) {  // the step on the weights (never a symmetric output)
@@ -602,12 +618,7 @@ __device__ __forceinline__ bool chunk_store(const TcProb &q, int i0, int j0, con
                     bad |= !finite4(w4);
                     st4(dw, w4);
                 } else {
-                    for (int t = 0; t < 4; ++t)
-                        if (j + t < q.N) {
-                            const float nw = fmaf(ne, comp(o, t), dw[t]);
-                            bad |= !(fabsf(nw) <= 3.402823466e38f);
-                            dw[t] = nw;
-                        }
+                    bad |= step4_edge(dw, q.N - j, ne, o);
                 }
             }
             if (q.Cb) {
@@ -618,8 +629,7 @@ __device__ __forceinline__ bool chunk_store(const TcProb &q, int i0, int j0, con
                     const uint32_t hi2 = f32_to_16_bits(o.z, h16) | ((uint32_t)f32_to_16_bits(o.w, h16) << 16);
                     *reinterpret_cast<uint2 *>(dst) = make_uint2(lo2, hi2);
                 } else {
-                    for (int t = 0; t < 4; ++t)
-                        if (j + t < q.N && (!up || j + t >= i)) dst[t] = f32_to_16_bits(comp(o, t), q.cb_f16);
+                    store4b_edge(dst, up ? i - j : 0, q.N - j, o, q.cb_f16);
                 }
             }
         }
