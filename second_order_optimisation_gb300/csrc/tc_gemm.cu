@@ -572,7 +572,18 @@ __device__ __forceinline__ bool chunk_store(const TcProb &q, int i0, int j0, con
     __syncwarp();
     const int j = j0 + 4 * (lane & 7);
     const bool full = q.vec && j + 3 < q.N;
-    if (q.epi == TC_EPI_ACCUM) {
+    if (q.epi == TC_EPI_ACCUM && whole && q.vec && !q.packed && (!q.syrk || j0 >= i0 + 32)) {
+        // an interior chunk (entirely above the diagonal of a SYRK): no edge code in the loop
+        float *dst = q.C + (long long)(i0 + (lane >> 3)) * q.ldc + j;
+        const long long step = 4 * q.ldc;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float4 o = make_float4(fmaf(b, oh[k].x, a * acc[k].x), fmaf(b, oh[k].y, a * acc[k].y),
+                                         fmaf(b, oh[k].z, a * acc[k].z), fmaf(b, oh[k].w, a * acc[k].w));
+            bad |= !finite4(o);
+            st4(dst + k * step, o);
+        }
+    } else if (q.epi == TC_EPI_ACCUM) {
         const bool upper = q.syrk;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -594,6 +605,24 @@ __device__ __forceinline__ bool chunk_store(const TcProb &q, int i0, int j0, con
         // exactly symmetric
         const bool up = diagblk;
         const bool fullb = q.vecb && j + 3 < q.N;
+        if (whole && !up && !q.W && q.C && q.vec && (!q.Cb || q.vecb)) {
+            // an interior chunk off the diagonal blocks: no edge code in the loop
+            float *dst = q.C + (long long)(i0 + (lane >> 3)) * q.ldc + j;
+            uint16_t *dstb = q.Cb ? q.Cb + (long long)(i0 + (lane >> 3)) * q.ldcb + j : nullptr;
+            const long long step = 4 * q.ldc, stepb = 4 * q.ldcb;
+            const bool h16 = q.cb_f16;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float4 o = make_float4(a * acc[k].x, a * acc[k].y, a * acc[k].z, a * acc[k].w);
+                bad |= !finite4(o);
+                st4(dst + k * step, o);
+                if (dstb) {
+                    const uint32_t lo2 = f32_to_16_bits(o.x, h16) | ((uint32_t)f32_to_16_bits(o.y, h16) << 16);
+                    const uint32_t hi2 = f32_to_16_bits(o.z, h16) | ((uint32_t)f32_to_16_bits(o.w, h16) << 16);
+                    *reinterpret_cast<uint2 *>(dstb + k * stepb) = make_uint2(lo2, hi2);
+                }
+            }
+        } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int i = i0 + 4 * k + (lane >> 3);
@@ -633,6 +662,7 @@ __device__ __forceinline__ bool chunk_store(const TcProb &q, int i0, int j0, con
                 }
             }
         }
+        }
         // a chunk of a diagonal block entirely above its diagonal mirrors
         // whole, one entirely below mirrors nothing, one on it goes entry by
         // entry (only j > i)
@@ -669,6 +699,23 @@ __device__ __forceinline__ bool chunk_store(const TcProb &q, int i0, int j0, con
                     if (q.Cb) q.Cb[(long long)jj * q.ldcb + i] = f32_to_16_bits(o, q.cb_f16);
                 }
             }
+        }
+    } else if (whole && q.vec && q.C && !mirror) {  // TC_EPI_SPLIT, an interior chunk: no edge code
+        const float *C0 = q.C;
+        float *Ch = q.C + (long long)(i0 + (lane >> 3)) * q.ldc + j, *Cl = q.C_lo + (Ch - C0);
+        const long long step = 4 * q.ldc;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float4 o = make_float4(fmaf(b, oh[k].x + ol[k].x, a * acc[k].x),
+                                         fmaf(b, oh[k].y + ol[k].y, a * acc[k].y),
+                                         fmaf(b, oh[k].z + ol[k].z, a * acc[k].z),
+                                         fmaf(b, oh[k].w + ol[k].w, a * acc[k].w));
+            bad |= !finite4(o);
+            const float4 h = tf32_hi4(o), l = sub4(o, h);
+            oh[k] = h;
+            ol[k] = l;
+            st4(Ch + k * step, h);
+            st4(Cl + k * step, l);
         }
     } else {  // TC_EPI_SPLIT
 #pragma unroll
