@@ -497,6 +497,16 @@ __device__ __forceinline__ void load_old(const TcProb &q, int i0, int j0, int la
     const bool need = q.beta != 0.f && q.epi != TC_EPI_STORE;
     const bool lo = q.epi == TC_EPI_SPLIT;
     const bool full = q.vec && j + 3 < q.N;
+    if (need && q.vec && !q.packed && i0 + 32 <= q.M && j0 + 32 <= q.N) {
+        // an interior chunk: a loop with no edge code
+        const long long off = (long long)(i0 + (lane >> 3)) * q.ldc + j, step = 4 * q.ldc;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            oh[k] = ld4(q.C + off + k * step);
+            ol[k] = lo ? ld4(q.C_lo + off + k * step) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        return;
+    }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const int i = i0 + 4 * k + (lane >> 3);
