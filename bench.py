@@ -55,12 +55,12 @@ SCHEDULE_KS = (1, 5, 10, 20)
 _TRAFFIC_SRC = "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch (serialised, cold caches), " \
                "profiles/resnet50_kfac_step_launches.md"
 NCU_TRAFFIC = {
-    "tc_gemm_tf32x3@inverse": (43.99e6, _TRAFFIC_SRC),
+    "tc_gemm_tf32x3@inverse": (43.67e6, _TRAFFIC_SRC),
     "inv_diag@inverse": (1.66e6, _TRAFFIC_SRC),
     "inv_prep@inverse": (918.9e6, _TRAFFIC_SRC),
-    "im2col@factors": (69.5e6, _TRAFFIC_SRC),
-    "tc_gemm_bf16@factors": (2005.0e6, _TRAFFIC_SRC),
-    "tc_gemm_bf16@precond": ((329.5e6 + 154.2e6) / 2, _TRAFFIC_SRC),
+    "im2col@factors": (69.8e6, _TRAFFIC_SRC),
+    "tc_gemm_bf16@factors": (2004.1e6, _TRAFFIC_SRC),
+    "tc_gemm_bf16@precond": ((330.2e6 + 153.8e6) / 2, _TRAFFIC_SRC),
 }
 
 
